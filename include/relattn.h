@@ -1,0 +1,223 @@
+/*
+ * relattn.h -- C ABI of the paged relative-bias attention library (GB300,
+ * sm_103a).
+ *
+ * The operation.  Inkling-family attention is grouped-query attention with no
+ * RoPE.  The pre-softmax logit of query i (position P_i, head h) for key j is
+ *
+ *     q_i . k_j / sqrt(d_qk) + rel[i, h, P_i - j]
+ *
+ * ("Inkling-Small on Gaudi 2", section "Why it needed a port": rel[i, h, i-j]
+ * is a per-query, per-distance term; "vLLM TML Inkling Support", section "TML
+ * Inkling Model Architecture": a learned relative-position term added to the
+ * pre-softmax logits instead of RoPE).  rel = r @ rel_logits_proj is computed
+ * by the model per query and head over distances 0..rel_extent-1 ("Inkling-
+ * Small on Gaudi 2", section "Attention with a relative bias"); this library
+ * takes it as an input.  A distance at or beyond rel_extent adds 0.
+ *
+ * Window.  A sliding-window layer (window W > 0) lets the query at position P
+ * see keys P-W+1 .. P: W keys counting its own ("Inkling-Small on Gaudi 2",
+ * section "Decode window": the mask cuts a 512-key window at exactly 512).
+ * W <= 0 is a global layer (every key 0..P).  Only blocks that hold a visible
+ * key are read: ceil(W/128)+1 blocks at most on a local layer.
+ *
+ * Paged KV cache.  Keys and values live in a pool of 128-token blocks
+ * ("Inkling-Small on Gaudi 2", section "At a glance": a pool of 2,560 blocks
+ * holds 327,680 tokens).  Position pos of sequence b is slot pos % 128 of
+ * physical block block_table[b * max_blocks_per_seq + pos / 128].  Layout
+ * (row-major, bf16):  k: [num_blocks][128][num_kv_heads][d_qk],
+ *                     v: [num_blocks][128][num_kv_heads][d_v].
+ * GQA: query head h reads KV head h / (num_q_heads / num_kv_heads).
+ * Softmax scale: 1/sqrt(d_qk), also when d_v != d_qk ("Inkling on Two DGX
+ * Sparks", section "Wall 1": head_dim 128, v_head_dim 64).
+ *
+ * Conventions shared by every entry point.
+ *  - All tensor pointers are DEVICE pointers owned by the caller and must be
+ *    16-byte aligned.  The library never allocates, frees or synchronises
+ *    (except relattn_read_status, which reads a word back).  Work is enqueued
+ *    on `stream` (a cudaStream_t; NULL = legacy default stream) and is safe to
+ *    capture in a CUDA graph: no call reads device memory from the host.
+ *  - Return value: RELATTN_OK or one of the RELATTN_ERR_* codes below.
+ *    Argument errors are found on the host before anything is enqueued.
+ *  - Errors that only the device can see (a block id outside the pool, a
+ *    length beyond the block table) never fault: the kernel skips the
+ *    affected tile or sequence, ORs a RELATTN_DEV_* bit into the workspace's
+ *    status word and carries on.  A skipped sequence's output rows are zero.
+ *  - The workspace (size from relattn_workspace_size) must be zero-filled
+ *    once before first use (relattn_workspace_init).  Calls leave it ready for
+ *    the next call.  Calls that share one workspace must be ordered on one
+ *    stream: concurrent calls on the same workspace race.
+ */
+#ifndef RELATTN_H_
+#define RELATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Return codes. */
+#define RELATTN_OK               0
+#define RELATTN_ERR_INVALID_ARG  1 /* null/misaligned pointer, bad size */
+#define RELATTN_ERR_UNSUPPORTED  2 /* valid but not built: see relattn_decode */
+#define RELATTN_ERR_WORKSPACE    3 /* workspace too small */
+#define RELATTN_ERR_CUDA         4 /* a CUDA runtime/driver call failed */
+
+/* Device status bits, ORed into the workspace status word. */
+#define RELATTN_DEV_BAD_BLOCK_ID 0x1u /* a needed table entry was outside
+                                         [0, num_blocks): its tile was skipped */
+#define RELATTN_DEV_BAD_LENGTH   0x2u /* a length outside the block table's
+                                         capacity: the sequence was skipped */
+#define RELATTN_DEV_WAIT_TIMEOUT 0x4u /* an internal pipeline wait ran past its
+                                         limit (about 2 s): the CTA gave up */
+
+/* The paged KV cache (device memory, caller-owned). */
+typedef struct relattn_kv_cache {
+  void*   k;            /* bf16 [num_blocks][block_size][num_kv_heads][d_qk] */
+  void*   v;            /* bf16 [num_blocks][block_size][num_kv_heads][d_v]  */
+  int32_t num_blocks;   /* physical blocks in the pool                       */
+  int32_t block_size;   /* tokens per block: must be 128                     */
+  int32_t num_kv_heads; /* Hkv                                               */
+  int32_t d_qk;         /* key/query head size: must be 128                  */
+  int32_t d_v;          /* value head size: 64 or 128                        */
+} relattn_kv_cache;
+
+/* Host-side sizes of one call.  No field is read from device memory. */
+typedef struct relattn_dims {
+  int32_t batch;              /* B: sequences in the call                   */
+  int32_t num_q_heads;        /* Hq: a multiple of Hkv, Hq/Hkv <= 16        */
+  int32_t max_blocks_per_seq; /* entries per block_table row                */
+  int32_t num_tokens;         /* prefill: T = cu_seqlens[B]; decode: unused */
+  int32_t max_q_len;          /* prefill: upper bound of every chunk length
+                                 cu_seqlens[b+1]-cu_seqlens[b]; decode: unused */
+  int32_t num_ctas;           /* 0: library choice (one persistent CTA per
+                                 SM); > 0 forces the grid size (testing)    */
+} relattn_dims;
+
+/*
+ * Bytes of workspace a decode or prefill call with these sizes needs.  The
+ * workspace holds the status word, the split-combine counters and the
+ * partial softmax states of split-KV decode.  Returns 0 on invalid sizes.
+ */
+size_t relattn_workspace_size(const relattn_dims* dims,
+                              const relattn_kv_cache* cache);
+
+/* Zero-fill a workspace on `stream` (once, before its first use). */
+int relattn_workspace_init(void* workspace, size_t workspace_bytes,
+                           void* stream);
+
+/*
+ * Paged decode: one query per sequence, attending to its own cached keys.
+ *
+ *   q          bf16 [B][Hq][d_qk]
+ *   rel        fp32 [B][Hq][rel_extent]: the relative logits of each query
+ *   kv_cache   the pool; must already hold each sequence's current token
+ *   block_table int32 [B][max_blocks_per_seq]; only the entries of blocks
+ *              holding a visible key are read
+ *   seq_lens   int32 [B]: tokens in each sequence including the current one;
+ *              the query sits at position seq_lens[b]-1.  Must lie in
+ *              [1, max_blocks_per_seq*128], else RELATTN_DEV_BAD_LENGTH.
+ *   window     W > 0: sliding window of W keys; W <= 0: global layer
+ *   rel_extent distances covered by rel; must be a positive multiple of 4
+ *   out        bf16 [B][Hq][d_v]
+ *
+ * Split-KV ("vLLM TML Inkling Support", section "Low-Latency Collectives and
+ * Kernels": num_splits picked from batch and KV length): one persistent
+ * kernel cuts the total window-aware key work of all sequences into equal
+ * contiguous ranges, one per CTA, so the number of splits of each sequence
+ * follows from batch, heads and lengths on the device.  A sequence cut by a
+ * range boundary leaves partial softmax states in the workspace; the CTA that
+ * finishes a sequence last merges them.  All query heads of one KV head are
+ * packed into one tile, so each key/value is read once
+ * ("Inkling 2 Small on vLLM", section "vLLM integration and optimisation":
+ * six heads packed into one tile, KV read once).
+ */
+int relattn_decode(const void* q, const float* rel,
+                   const relattn_kv_cache* kv_cache,
+                   const int32_t* block_table, const int32_t* seq_lens,
+                   int32_t window, int32_t rel_extent,
+                   const relattn_dims* dims, void* out,
+                   void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Chunked prefill with a cached prefix.
+ *
+ *   q          bf16 [T][Hq][d_qk]: the new tokens of all sequences, packed
+ *   k, v       bf16 [T][Hkv][d_qk], [T][Hkv][d_v]: their keys and values
+ *   rel        fp32 [T][Hq][rel_extent]
+ *   cu_seqlens int32 [B+1]: new tokens of sequence b are rows
+ *              cu_seqlens[b] .. cu_seqlens[b+1]-1 (cu_seqlens[0] = 0)
+ *   cache      the pool (in-out): new token t of sequence b is first written
+ *              to position ctx_lens[b]+t, then attends to positions
+ *              0 .. ctx_lens[b]+t (windowed) -- the cached prefix and the
+ *              chunk ("Inkling-Small on Gaudi 2", section "Attention with a
+ *              relative bias": later chunks and prefix-cache hits prepend the
+ *              cached context)
+ *   block_table int32 [B][max_blocks_per_seq], covering ctx_lens[b] +
+ *              chunk length positions
+ *   ctx_lens   int32 [B]: cached prefix lengths
+ *   window, rel_extent: as for relattn_decode
+ *   out        bf16 [T][Hq][d_v]
+ *
+ * dims->num_tokens must equal cu_seqlens[B] and dims->max_q_len must bound
+ * every chunk length (both host-side; nothing is read back).
+ */
+int relattn_prefill(const void* q, const void* k, const void* v,
+                    const float* rel, const int32_t* cu_seqlens,
+                    const relattn_kv_cache* cache,
+                    const int32_t* block_table, const int32_t* ctx_lens,
+                    int32_t window, int32_t rel_extent,
+                    const relattn_dims* dims, void* out,
+                    void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Read the device status word of a workspace into *status (synchronises
+ * `stream`).  The word accumulates RELATTN_DEV_* bits until cleared with
+ * relattn_workspace_init.
+ */
+int relattn_read_status(const void* workspace, uint32_t* status, void* stream);
+
+/* Human-readable name of a return code. */
+const char* relattn_status_string(int code);
+
+/*
+ * Test hook: replay the decode kernel's window-aware block walk and work
+ * split without computing attention.  Each visited 64-key tile appends one
+ * record of 6 int32 to `records` (device, capacity max_records records):
+ *   { cta, sequence, kv_head, key_tile (first key / 64),
+ *     logical_block, physical_block }
+ * and *count (device int32, zero it first) counts the records.  The same
+ * device code as relattn_decode picks the tiles.
+ */
+int relattn_debug_walk_decode(const int32_t* block_table,
+                              const int32_t* seq_lens, int32_t window,
+                              const relattn_kv_cache* cache,
+                              const relattn_dims* dims, int32_t* records,
+                              int32_t max_records, int32_t* count,
+                              void* workspace, size_t workspace_bytes,
+                              void* stream);
+
+/*
+ * Test hook: replay the prefill kernel's block walk.  Each (query tile, key
+ * tile) visit appends { sequence, first_row_of_query_tile, key_tile,
+ * logical_block, physical_block, 0 } (6 int32) to `records`.
+ */
+int relattn_debug_walk_prefill(const int32_t* cu_seqlens,
+                               const int32_t* ctx_lens,
+                               const int32_t* block_table, int32_t window,
+                               const relattn_kv_cache* cache,
+                               const relattn_dims* dims, int32_t* records,
+                               int32_t max_records, int32_t* count,
+                               void* workspace, size_t workspace_bytes,
+                               void* stream);
+
+/* ABI version of this header (major * 100 + minor). */
+int relattn_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RELATTN_H_ */

@@ -1,0 +1,354 @@
+// Host side of the relattn C ABI: argument validation, workspace layout,
+// TMA descriptors and kernel launches.  Nothing here reads device memory
+// (except relattn_read_status), so every call can be captured in a graph.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/relattn.h"
+#include "relattn_internal.h"
+
+namespace relattn {
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int kMaxStages = 6;
+constexpr size_t kStatusBytes = 256;
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool aligned16(const void* p) {
+  return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
+}
+
+struct DeviceInfo {
+  int sms = 0;
+  int smem_optin = 0;
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+bool device_info(DeviceInfo* out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_dev[dev].sms == 0) {
+    int sms = 0, smem = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return false;
+    if (cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+        cudaSuccess)
+      return false;
+    g_dev[dev].sms = sms;
+    g_dev[dev].smem_optin = smem;
+  }
+  *out = g_dev[dev];
+  return true;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  return g_encode;
+}
+
+// Tiled map over a row-major tensor; dims/box innermost first.
+bool make_map(CUtensorMap* m, CUtensorMapDataType dt, int rank, void* base,
+              const cuuint64_t* dims, const cuuint64_t* strides_bytes,
+              const cuuint32_t* box, CUtensorMapSwizzle swz) {
+  auto enc = encoder();
+  if (!enc) return false;
+  cuuint32_t es[5] = {1, 1, 1, 1, 1};
+  return enc(m, dt, rank, base, dims, strides_bytes, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool cache_maps(const relattn_kv_cache* c, CUtensorMap* tk, CUtensorMap* tv) {
+  const cuuint64_t rows = static_cast<cuuint64_t>(c->num_blocks) * c->block_size;
+  const cuuint64_t kd[3] = {static_cast<cuuint64_t>(c->d_qk),
+                            static_cast<cuuint64_t>(c->num_kv_heads), rows};
+  const cuuint64_t ks[2] = {static_cast<cuuint64_t>(c->d_qk) * 2,
+                            static_cast<cuuint64_t>(c->num_kv_heads) * c->d_qk * 2};
+  const cuuint64_t vd[3] = {static_cast<cuuint64_t>(c->d_v),
+                            static_cast<cuuint64_t>(c->num_kv_heads), rows};
+  const cuuint64_t vs[2] = {static_cast<cuuint64_t>(c->d_v) * 2,
+                            static_cast<cuuint64_t>(c->num_kv_heads) * c->d_v * 2};
+  const cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(kTileKeys)};
+  return make_map(tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, c->k, kd, ks, box,
+                  CU_TENSOR_MAP_SWIZZLE_128B) &&
+         make_map(tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, c->v, vd, vs, box,
+                  CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+int check_cache(const relattn_kv_cache* c) {
+  if (!c || !c->k || !c->v) return RELATTN_ERR_INVALID_ARG;
+  if (!aligned16(c->k) || !aligned16(c->v)) return RELATTN_ERR_INVALID_ARG;
+  if (c->num_blocks < 1 || c->num_kv_heads < 1) return RELATTN_ERR_INVALID_ARG;
+  if (static_cast<long long>(c->num_blocks) * 128 > 0x7fffffffLL) return RELATTN_ERR_UNSUPPORTED;
+  if (c->block_size != 128 || c->d_qk != 128) return RELATTN_ERR_UNSUPPORTED;
+  if (c->d_v != 64 && c->d_v != 128) return RELATTN_ERR_UNSUPPORTED;
+  return RELATTN_OK;
+}
+
+int check_dims(const relattn_dims* d, const relattn_kv_cache* c) {
+  if (!d) return RELATTN_ERR_INVALID_ARG;
+  if (d->batch < 1 || d->num_q_heads < 1 || d->max_blocks_per_seq < 1 || d->num_ctas < 0)
+    return RELATTN_ERR_INVALID_ARG;
+  if (d->num_q_heads % c->num_kv_heads != 0) return RELATTN_ERR_INVALID_ARG;
+  if (d->num_q_heads / c->num_kv_heads > 16) return RELATTN_ERR_UNSUPPORTED;
+  if (static_cast<long long>(d->max_blocks_per_seq) * 128 > 0x7fffffffLL)
+    return RELATTN_ERR_UNSUPPORTED;
+  return RELATTN_OK;
+}
+
+struct WsLayout {
+  size_t counters, lse, part, total;
+};
+
+WsLayout ws_layout(const relattn_dims* d, const relattn_kv_cache* c, int grid) {
+  const int g = d->num_q_heads / c->num_kv_heads;
+  WsLayout w;
+  w.counters = kStatusBytes;
+  w.lse = w.counters + round_up(static_cast<size_t>(d->batch) * c->num_kv_heads * 4, 256);
+  w.part = w.lse + round_up(static_cast<size_t>(2) * grid * g * 4, 256);
+  w.total = w.part + static_cast<size_t>(2) * grid * g * c->d_v * 4;
+  return w;
+}
+
+int decode_grid(const relattn_dims* d, const DeviceInfo& di) {
+  return d->num_ctas > 0 ? d->num_ctas : di.sms;
+}
+
+int to_status(cudaError_t e) { return e == cudaSuccess ? RELATTN_OK : RELATTN_ERR_CUDA; }
+
+}  // namespace
+}  // namespace relattn
+
+using namespace relattn;
+
+extern "C" {
+
+int relattn_abi_version(void) { return 100; }
+
+const char* relattn_status_string(int code) {
+  switch (code) {
+    case RELATTN_OK: return "ok";
+    case RELATTN_ERR_INVALID_ARG: return "invalid argument";
+    case RELATTN_ERR_UNSUPPORTED: return "unsupported configuration";
+    case RELATTN_ERR_WORKSPACE: return "workspace too small";
+    case RELATTN_ERR_CUDA: return "CUDA error";
+    default: return "unknown status";
+  }
+}
+
+size_t relattn_workspace_size(const relattn_dims* dims, const relattn_kv_cache* cache) {
+  if (check_cache(cache) != RELATTN_OK || check_dims(dims, cache) != RELATTN_OK) return 0;
+  DeviceInfo di;
+  if (!device_info(&di)) return 0;
+  return ws_layout(dims, cache, decode_grid(dims, di)).total;
+}
+
+int relattn_workspace_init(void* workspace, size_t bytes, void* stream) {
+  if (!workspace || bytes < kStatusBytes) return RELATTN_ERR_INVALID_ARG;
+  return to_status(cudaMemsetAsync(workspace, 0, bytes, static_cast<cudaStream_t>(stream)));
+}
+
+int relattn_read_status(const void* workspace, uint32_t* status, void* stream) {
+  if (!workspace || !status) return RELATTN_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(status, workspace, 4, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  return to_status(e);
+}
+
+static int prepare_decode(const void* q, const float* rel, const relattn_kv_cache* cache,
+                          const int32_t* block_table, const int32_t* seq_lens,
+                          int32_t window, int32_t rel_extent, const relattn_dims* dims,
+                          void* out, void* workspace, size_t ws_bytes, bool walk,
+                          DecodeLaunch* L, DeviceInfo* di) {
+  int rc = check_cache(cache);
+  if (rc != RELATTN_OK) return rc;
+  rc = check_dims(dims, cache);
+  if (rc != RELATTN_OK) return rc;
+  if (!block_table || !seq_lens || !workspace) return RELATTN_ERR_INVALID_ARG;
+  if (!walk) {
+    if (!q || !rel || !out) return RELATTN_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(rel) || !aligned16(out)) return RELATTN_ERR_INVALID_ARG;
+    if (rel_extent < 4 || rel_extent % 4 != 0) return RELATTN_ERR_UNSUPPORTED;
+  }
+  if (!aligned16(workspace)) return RELATTN_ERR_INVALID_ARG;
+  if (!device_info(di)) return RELATTN_ERR_CUDA;
+  const int grid = decode_grid(dims, *di);
+  const WsLayout w = ws_layout(dims, cache, grid);
+  if (ws_bytes < w.total) return RELATTN_ERR_WORKSPACE;
+  const int g = dims->num_q_heads / cache->num_kv_heads;
+  std::memset(L, 0, sizeof(*L));
+  DecodeParams& p = L->p;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.block_table = block_table;
+  p.seq_lens = seq_lens;
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.status = reinterpret_cast<uint32_t*>(ws);
+  p.counters = reinterpret_cast<int32_t*>(ws + w.counters);
+  p.part_lse = reinterpret_cast<float*>(ws + w.lse);
+  p.part_o = reinterpret_cast<float*>(ws + w.part);
+  p.B = dims->batch;
+  p.Hq = dims->num_q_heads;
+  p.Hkv = cache->num_kv_heads;
+  p.g = g;
+  p.dv = cache->d_v;
+  p.max_blocks = dims->max_blocks_per_seq;
+  p.num_blocks = cache->num_blocks;
+  p.window = window;
+  p.rel_extent = rel_extent;
+  p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(128.0));
+  L->grid = grid;
+  if (walk) {
+    p.nstages = 0;
+    p.stage_bytes = 0;
+    return RELATTN_OK;
+  }
+  p.rel_off = 16384 + kTileKeys * cache->d_v * 2;
+  p.stage_bytes = p.rel_off + static_cast<int>(round_up(static_cast<size_t>(g) * kRelBoxW * 4, 1024));
+  p.nstages = kMaxStages;
+  while (p.nstages >= 2 &&
+         decode_smem_bytes(p.nstages, p.stage_bytes, p.B, p.dv) > di->smem_optin)
+    --p.nstages;
+  if (p.nstages < 2) return RELATTN_ERR_UNSUPPORTED;  // batch too large for shared memory
+  if (!cache_maps(cache, &L->tm_k, &L->tm_v)) return RELATTN_ERR_CUDA;
+  const cuuint64_t rd[2] = {static_cast<cuuint64_t>(rel_extent),
+                            static_cast<cuuint64_t>(dims->batch) * dims->num_q_heads};
+  const cuuint64_t rs[1] = {static_cast<cuuint64_t>(rel_extent) * 4};
+  const cuuint32_t rb[2] = {static_cast<cuuint32_t>(kRelBoxW), static_cast<cuuint32_t>(g)};
+  if (!make_map(&L->tm_rel, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(rel), rd,
+                rs, rb, CU_TENSOR_MAP_SWIZZLE_NONE))
+    return RELATTN_ERR_CUDA;
+  return RELATTN_OK;
+}
+
+int relattn_decode(const void* q, const float* rel, const relattn_kv_cache* kv_cache,
+                   const int32_t* block_table, const int32_t* seq_lens, int32_t window,
+                   int32_t rel_extent, const relattn_dims* dims, void* out, void* workspace,
+                   size_t workspace_bytes, void* stream) {
+  DecodeLaunch L;
+  DeviceInfo di;
+  const int rc = prepare_decode(q, rel, kv_cache, block_table, seq_lens, window, rel_extent,
+                                dims, out, workspace, workspace_bytes, false, &L, &di);
+  if (rc != RELATTN_OK) return rc;
+  return to_status(launch_decode(L, static_cast<cudaStream_t>(stream)));
+}
+
+int relattn_debug_walk_decode(const int32_t* block_table, const int32_t* seq_lens,
+                              int32_t window, const relattn_kv_cache* cache,
+                              const relattn_dims* dims, int32_t* records, int32_t max_records,
+                              int32_t* count, void* workspace, size_t workspace_bytes,
+                              void* stream) {
+  if (!records || !count || max_records < 0) return RELATTN_ERR_INVALID_ARG;
+  DecodeLaunch L;
+  DeviceInfo di;
+  const int rc = prepare_decode(nullptr, nullptr, cache, block_table, seq_lens, window, 4, dims,
+                                nullptr, workspace, workspace_bytes, true, &L, &di);
+  if (rc != RELATTN_OK) return rc;
+  L.p.dbg_records = records;
+  L.p.dbg_count = count;
+  L.p.dbg_max = max_records;
+  return to_status(launch_decode_walk(L.p, L.grid, static_cast<cudaStream_t>(stream)));
+}
+
+static int prepare_prefill(const void* q, const void* k, const void* v, const float* rel,
+                           const int32_t* cu_seqlens, const relattn_kv_cache* cache,
+                           const int32_t* block_table, const int32_t* ctx_lens,
+                           int32_t window, int32_t rel_extent, const relattn_dims* dims,
+                           void* out, void* workspace, size_t ws_bytes, bool walk,
+                           PrefillLaunch* L) {
+  int rc = check_cache(cache);
+  if (rc != RELATTN_OK) return rc;
+  rc = check_dims(dims, cache);
+  if (rc != RELATTN_OK) return rc;
+  if (!cu_seqlens || !block_table || !ctx_lens || !workspace) return RELATTN_ERR_INVALID_ARG;
+  if (dims->max_q_len < 0 || dims->num_tokens < 0) return RELATTN_ERR_INVALID_ARG;
+  if (!walk) {
+    if (!q || !k || !v || !rel || !out) return RELATTN_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(rel) || !aligned16(out))
+      return RELATTN_ERR_INVALID_ARG;
+    if (rel_extent < 4 || rel_extent % 4 != 0) return RELATTN_ERR_UNSUPPORTED;
+  }
+  if (!aligned16(workspace) || ws_bytes < kStatusBytes) return RELATTN_ERR_WORKSPACE;
+  std::memset(L, 0, sizeof(*L));
+  PrefillParams& p = L->p;
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.k = static_cast<const __nv_bfloat16*>(k);
+  p.v = static_cast<const __nv_bfloat16*>(v);
+  p.rel = rel;
+  p.cu_seqlens = cu_seqlens;
+  p.ctx_lens = ctx_lens;
+  p.block_table = block_table;
+  p.k_cache = static_cast<__nv_bfloat16*>(cache->k);
+  p.v_cache = static_cast<__nv_bfloat16*>(cache->v);
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.status = static_cast<uint32_t*>(workspace);
+  p.B = dims->batch;
+  p.T = dims->num_tokens;
+  p.Hq = dims->num_q_heads;
+  p.Hkv = cache->num_kv_heads;
+  p.g = dims->num_q_heads / cache->num_kv_heads;
+  p.dv = cache->d_v;
+  p.max_blocks = dims->max_blocks_per_seq;
+  p.num_blocks = cache->num_blocks;
+  p.window = window;
+  p.rel_extent = rel_extent;
+  p.max_q_len = dims->max_q_len;
+  p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(128.0));
+  if (walk) return RELATTN_OK;
+  if (!cache_maps(cache, &L->tm_k, &L->tm_v)) return RELATTN_ERR_CUDA;
+  return RELATTN_OK;
+}
+
+int relattn_prefill(const void* q, const void* k, const void* v, const float* rel,
+                    const int32_t* cu_seqlens, const relattn_kv_cache* cache,
+                    const int32_t* block_table, const int32_t* ctx_lens, int32_t window,
+                    int32_t rel_extent, const relattn_dims* dims, void* out, void* workspace,
+                    size_t workspace_bytes, void* stream) {
+  PrefillLaunch L;
+  const int rc = prepare_prefill(q, k, v, rel, cu_seqlens, cache, block_table, ctx_lens, window,
+                                 rel_extent, dims, out, workspace, workspace_bytes, false, &L);
+  if (rc != RELATTN_OK) return rc;
+  if (dims->max_q_len == 0 || dims->num_tokens == 0) return RELATTN_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_cache_write(L.p, s);
+  if (e == cudaSuccess) e = launch_prefill(L, s);
+  return to_status(e);
+}
+
+int relattn_debug_walk_prefill(const int32_t* cu_seqlens, const int32_t* ctx_lens,
+                               const int32_t* block_table, int32_t window,
+                               const relattn_kv_cache* cache, const relattn_dims* dims,
+                               int32_t* records, int32_t max_records, int32_t* count,
+                               void* workspace, size_t workspace_bytes, void* stream) {
+  if (!records || !count || max_records < 0) return RELATTN_ERR_INVALID_ARG;
+  PrefillLaunch L;
+  const int rc = prepare_prefill(nullptr, nullptr, nullptr, nullptr, cu_seqlens, cache,
+                                 block_table, ctx_lens, window, 4, dims, nullptr, workspace,
+                                 workspace_bytes, true, &L);
+  if (rc != RELATTN_OK) return rc;
+  if (dims->max_q_len == 0) return RELATTN_OK;
+  L.p.dbg_records = records;
+  L.p.dbg_count = count;
+  L.p.dbg_max = max_records;
+  return to_status(launch_prefill_walk(L.p, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,71 @@
+// Host <-> kernel interface of the relattn library (not part of the C ABI).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace relattn {
+
+constexpr int kBlockSize = 128;  // tokens per KV block
+constexpr int kTileKeys = 64;    // keys per pipeline stage
+constexpr int kDqk = 128;
+constexpr int kRelBoxW = 68;     // distances per rel box: 64 keys + alignment
+
+struct DecodeParams {
+  const __nv_bfloat16* q;      // [B][Hq][128]
+  const int32_t* block_table;  // [B][max_blocks]
+  const int32_t* seq_lens;     // [B]
+  __nv_bfloat16* out;          // [B][Hq][dv]
+  uint32_t* status;            // workspace status word
+  int32_t* counters;           // [B][Hkv] split-combine arrival counters
+  float* part_lse;             // [2*grid][g] base-2 log-sum-exp of a piece
+  float* part_o;               // [2*grid][g][dv] normalised output of a piece
+  int32_t* dbg_records;        // walk replay only
+  int32_t* dbg_count;
+  int dbg_max;
+  int B, Hq, Hkv, g, dv, max_blocks, num_blocks, window, rel_extent;
+  int nstages, stage_bytes, rel_off;
+  float scale_log2;  // log2(e) / sqrt(d_qk)
+};
+
+struct DecodeLaunch {
+  CUtensorMap tm_k, tm_v, tm_rel;
+  DecodeParams p;
+  int grid;
+};
+
+struct PrefillParams {
+  const __nv_bfloat16* q;      // [T][Hq][128]
+  const __nv_bfloat16* k;      // [T][Hkv][128]
+  const __nv_bfloat16* v;      // [T][Hkv][dv]
+  const float* rel;            // [T][Hq][E]
+  const int32_t* cu_seqlens;   // [B+1]
+  const int32_t* ctx_lens;     // [B]
+  const int32_t* block_table;  // [B][max_blocks]
+  __nv_bfloat16* k_cache;      // [NB][128][Hkv][128]
+  __nv_bfloat16* v_cache;      // [NB][128][Hkv][dv]
+  __nv_bfloat16* out;          // [T][Hq][dv]
+  uint32_t* status;
+  int32_t* dbg_records;
+  int32_t* dbg_count;
+  int dbg_max;
+  int B, T, Hq, Hkv, g, dv, max_blocks, num_blocks, window, rel_extent, max_q_len;
+  float scale_log2;
+};
+
+struct PrefillLaunch {
+  CUtensorMap tm_k, tm_v;
+  PrefillParams p;
+};
+
+int decode_smem_bytes(int nstages, int stage_bytes, int B, int dv);
+cudaError_t launch_decode(const DecodeLaunch& L, cudaStream_t stream);
+cudaError_t launch_decode_walk(const DecodeParams& p, int grid, cudaStream_t stream);
+
+cudaError_t launch_cache_write(const PrefillParams& p, cudaStream_t stream);
+cudaError_t launch_prefill(const PrefillLaunch& L, cudaStream_t stream);
+cudaError_t launch_prefill_walk(const PrefillParams& p, cudaStream_t stream);
+
+}  // namespace relattn

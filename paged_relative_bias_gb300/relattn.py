@@ -1,0 +1,284 @@
+"""Python binding of the relattn C ABI (``include/relattn.h``).
+
+Argument marshalling only: every step of the attention runs in the CUDA
+library ``lib/librelattn.so``.  Tensors are torch device tensors; their data
+pointers and the current CUDA stream are handed to the C entry points.  There
+is no fallback: if the library is missing, every call raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from ctypes import POINTER, c_char_p, c_int, c_int32, c_size_t, c_uint32, c_void_p
+
+import torch
+
+from . import build as _build
+
+OK = 0
+ERR_INVALID_ARG = 1
+ERR_UNSUPPORTED = 2
+ERR_WORKSPACE = 3
+ERR_CUDA = 4
+
+DEV_BAD_BLOCK_ID = 0x1
+DEV_BAD_LENGTH = 0x2
+DEV_WAIT_TIMEOUT = 0x4
+
+EXPORTS = (
+    "relattn_workspace_size",
+    "relattn_workspace_init",
+    "relattn_decode",
+    "relattn_prefill",
+    "relattn_read_status",
+    "relattn_status_string",
+    "relattn_debug_walk_decode",
+    "relattn_debug_walk_prefill",
+    "relattn_abi_version",
+)
+
+
+class KVCacheDesc(ctypes.Structure):
+    _fields_ = [("k", c_void_p), ("v", c_void_p), ("num_blocks", c_int32),
+                ("block_size", c_int32), ("num_kv_heads", c_int32),
+                ("d_qk", c_int32), ("d_v", c_int32)]
+
+
+class Dims(ctypes.Structure):
+    _fields_ = [("batch", c_int32), ("num_q_heads", c_int32),
+                ("max_blocks_per_seq", c_int32), ("num_tokens", c_int32),
+                ("max_q_len", c_int32), ("num_ctas", c_int32)]
+
+
+class RelattnError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: {status_string(code)} (code {code})")
+        self.code = code
+
+
+_LIB = None
+
+
+def library_path() -> str:
+    return _build.lib_path()
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded C library; raises if it has not been built."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    path = library_path()
+    if not os.path.exists(path):
+        raise RuntimeError(
+            f"relattn CUDA library not found at {path}; build it with "
+            "`python -m paged_relative_bias_gb300.build` (there is no CPU fallback)")
+    L = ctypes.CDLL(path)
+    P, S = POINTER(KVCacheDesc), POINTER(Dims)
+    L.relattn_workspace_size.argtypes = [S, P]
+    L.relattn_workspace_size.restype = c_size_t
+    L.relattn_workspace_init.argtypes = [c_void_p, c_size_t, c_void_p]
+    L.relattn_workspace_init.restype = c_int
+    L.relattn_decode.argtypes = [c_void_p, c_void_p, P, c_void_p, c_void_p, c_int32,
+                                 c_int32, S, c_void_p, c_void_p, c_size_t, c_void_p]
+    L.relattn_decode.restype = c_int
+    L.relattn_prefill.argtypes = [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, P,
+                                  c_void_p, c_void_p, c_int32, c_int32, S, c_void_p,
+                                  c_void_p, c_size_t, c_void_p]
+    L.relattn_prefill.restype = c_int
+    L.relattn_read_status.argtypes = [c_void_p, POINTER(c_uint32), c_void_p]
+    L.relattn_read_status.restype = c_int
+    L.relattn_status_string.argtypes = [c_int]
+    L.relattn_status_string.restype = c_char_p
+    L.relattn_debug_walk_decode.argtypes = [c_void_p, c_void_p, c_int32, P, S, c_void_p,
+                                            c_int32, c_void_p, c_void_p, c_size_t, c_void_p]
+    L.relattn_debug_walk_decode.restype = c_int
+    L.relattn_debug_walk_prefill.argtypes = [c_void_p, c_void_p, c_void_p, c_int32, P, S,
+                                             c_void_p, c_int32, c_void_p, c_void_p,
+                                             c_size_t, c_void_p]
+    L.relattn_debug_walk_prefill.restype = c_int
+    L.relattn_abi_version.argtypes = []
+    L.relattn_abi_version.restype = c_int
+    _LIB = L
+    return L
+
+
+def status_string(code: int) -> str:
+    return lib().relattn_status_string(code).decode()
+
+
+def _check(rc: int, what: str) -> None:
+    if rc != OK:
+        raise RelattnError(rc, what)
+
+
+def _ptr(t: torch.Tensor | None) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(device: torch.device) -> int:
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def _need(t: torch.Tensor, name: str, dtype, dims: int, device) -> None:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != dims:
+        raise ValueError(f"{name} must have {dims} dimensions, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+
+
+def cache_desc(k_cache: torch.Tensor, v_cache: torch.Tensor) -> KVCacheDesc:
+    return KVCacheDesc(k_cache.data_ptr(), v_cache.data_ptr(), k_cache.shape[0],
+                       k_cache.shape[1], k_cache.shape[2], k_cache.shape[3],
+                       v_cache.shape[3])
+
+
+def workspace_size(dims: Dims, cache: KVCacheDesc) -> int:
+    n = lib().relattn_workspace_size(ctypes.byref(dims), ctypes.byref(cache))
+    if n == 0:
+        raise RelattnError(ERR_INVALID_ARG, "relattn_workspace_size")
+    return int(n)
+
+
+def new_workspace(nbytes: int, device) -> torch.Tensor:
+    """A zero-filled workspace buffer (allocated by torch, initialised by the library)."""
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    _check(lib().relattn_workspace_init(ws.data_ptr(), nbytes, _stream(ws.device)),
+           "relattn_workspace_init")
+    return ws
+
+
+def read_status(workspace: torch.Tensor) -> int:
+    st = c_uint32(0)
+    _check(lib().relattn_read_status(workspace.data_ptr(), ctypes.byref(st),
+                                     _stream(workspace.device)), "relattn_read_status")
+    return int(st.value)
+
+
+def clear_status(workspace: torch.Tensor) -> None:
+    _check(lib().relattn_workspace_init(workspace.data_ptr(), workspace.numel(),
+                                        _stream(workspace.device)), "relattn_workspace_init")
+
+
+def decode_dims(q, block_table, num_ctas=0) -> Dims:
+    return Dims(q.shape[0], q.shape[1], block_table.shape[1], 0, 0, num_ctas)
+
+
+def relattn_decode(q, rel, k_cache, v_cache, block_table, seq_lens, window: int,
+                   rel_extent: int, out=None, workspace=None, num_ctas: int = 0):
+    """Paged relative-bias decode; see ``relattn_decode`` in include/relattn.h."""
+    dev = q.device
+    B, Hq, dqk = q.shape
+    _need(q, "q", torch.bfloat16, 3, dev)
+    _need(rel, "rel", torch.float32, 3, dev)
+    _need(k_cache, "k_cache", torch.bfloat16, 4, dev)
+    _need(v_cache, "v_cache", torch.bfloat16, 4, dev)
+    _need(block_table, "block_table", torch.int32, 2, dev)
+    _need(seq_lens, "seq_lens", torch.int32, 1, dev)
+    if tuple(rel.shape) != (B, Hq, rel_extent):
+        raise ValueError("rel must be [B, Hq, rel_extent]")
+    if seq_lens.shape[0] != B or block_table.shape[0] != B:
+        raise ValueError("seq_lens / block_table batch mismatch")
+    cache = cache_desc(k_cache, v_cache)
+    dims = decode_dims(q, block_table, num_ctas)
+    if out is None:
+        out = torch.empty((B, Hq, v_cache.shape[3]), dtype=torch.bfloat16, device=dev)
+    else:
+        _need(out, "out", torch.bfloat16, 3, dev)
+    if workspace is None:
+        workspace = new_workspace(workspace_size(dims, cache), dev)
+    _check(lib().relattn_decode(
+        q.data_ptr(), rel.data_ptr(), ctypes.byref(cache), block_table.data_ptr(),
+        seq_lens.data_ptr(), int(window), int(rel_extent), ctypes.byref(dims),
+        out.data_ptr(), workspace.data_ptr(), workspace.numel(), _stream(dev)),
+        "relattn_decode")
+    return out
+
+
+def prefill_dims(q, block_table, ctx_lens, max_q_len: int, num_ctas=0) -> Dims:
+    return Dims(ctx_lens.shape[0], q.shape[1], block_table.shape[1], q.shape[0],
+                int(max_q_len), num_ctas)
+
+
+def relattn_prefill(q, k, v, rel, cu_seqlens, k_cache, v_cache, block_table, ctx_lens,
+                    window: int, rel_extent: int, max_q_len: int, out=None,
+                    workspace=None):
+    """Chunked prefill with a cached prefix; writes k, v into the cache."""
+    dev = q.device
+    T, Hq, dqk = q.shape
+    _need(q, "q", torch.bfloat16, 3, dev)
+    _need(k, "k", torch.bfloat16, 3, dev)
+    _need(v, "v", torch.bfloat16, 3, dev)
+    _need(rel, "rel", torch.float32, 3, dev)
+    _need(k_cache, "k_cache", torch.bfloat16, 4, dev)
+    _need(v_cache, "v_cache", torch.bfloat16, 4, dev)
+    _need(block_table, "block_table", torch.int32, 2, dev)
+    _need(cu_seqlens, "cu_seqlens", torch.int32, 1, dev)
+    _need(ctx_lens, "ctx_lens", torch.int32, 1, dev)
+    if tuple(rel.shape) != (T, Hq, rel_extent):
+        raise ValueError("rel must be [T, Hq, rel_extent]")
+    if k.shape[0] != T or v.shape[0] != T:
+        raise ValueError("k / v must have one row per new token")
+    B = ctx_lens.shape[0]
+    if cu_seqlens.shape[0] != B + 1 or block_table.shape[0] != B:
+        raise ValueError("cu_seqlens / block_table batch mismatch")
+    cache = cache_desc(k_cache, v_cache)
+    dims = prefill_dims(q, block_table, ctx_lens, max_q_len)
+    if out is None:
+        out = torch.empty((T, Hq, v_cache.shape[3]), dtype=torch.bfloat16, device=dev)
+    else:
+        _need(out, "out", torch.bfloat16, 3, dev)
+    if workspace is None:
+        workspace = new_workspace(workspace_size(dims, cache), dev)
+    _check(lib().relattn_prefill(
+        q.data_ptr(), k.data_ptr(), v.data_ptr(), rel.data_ptr(), cu_seqlens.data_ptr(),
+        ctypes.byref(cache), block_table.data_ptr(), ctx_lens.data_ptr(), int(window),
+        int(rel_extent), ctypes.byref(dims), out.data_ptr(), workspace.data_ptr(),
+        workspace.numel(), _stream(dev)), "relattn_prefill")
+    return out
+
+
+def debug_walk_decode(block_table, seq_lens, window: int, k_cache, v_cache, num_q_heads: int,
+                      num_ctas: int = 0, max_records: int = 1 << 20):
+    """Replay of the decode kernel's block walk: int32 [n, 6] records."""
+    dev = block_table.device
+    cache = cache_desc(k_cache, v_cache)
+    dims = Dims(block_table.shape[0], num_q_heads, block_table.shape[1], 0, 0, num_ctas)
+    ws = new_workspace(workspace_size(dims, cache), dev)
+    rec = torch.zeros((max_records, 6), dtype=torch.int32, device=dev)
+    cnt = torch.zeros(1, dtype=torch.int32, device=dev)
+    _check(lib().relattn_debug_walk_decode(
+        block_table.data_ptr(), seq_lens.data_ptr(), int(window), ctypes.byref(cache),
+        ctypes.byref(dims), rec.data_ptr(), max_records, cnt.data_ptr(), ws.data_ptr(),
+        ws.numel(), _stream(dev)), "relattn_debug_walk_decode")
+    n = int(cnt.item())
+    if n > max_records:
+        raise RuntimeError("walk produced more records than the buffer holds")
+    return rec[:n].cpu(), read_status(ws)
+
+
+def debug_walk_prefill(cu_seqlens, ctx_lens, block_table, window: int, k_cache, v_cache,
+                       num_q_heads: int, max_q_len: int, max_records: int = 1 << 20):
+    """Replay of the prefill kernel's block walk: int32 [n, 6] records."""
+    dev = block_table.device
+    cache = cache_desc(k_cache, v_cache)
+    dims = Dims(ctx_lens.shape[0], num_q_heads, block_table.shape[1], 0, int(max_q_len), 0)
+    ws = new_workspace(workspace_size(dims, cache), dev)
+    rec = torch.zeros((max_records, 6), dtype=torch.int32, device=dev)
+    cnt = torch.zeros(1, dtype=torch.int32, device=dev)
+    _check(lib().relattn_debug_walk_prefill(
+        cu_seqlens.data_ptr(), ctx_lens.data_ptr(), block_table.data_ptr(), int(window),
+        ctypes.byref(cache), ctypes.byref(dims), rec.data_ptr(), max_records,
+        cnt.data_ptr(), ws.data_ptr(), ws.numel(), _stream(dev)),
+        "relattn_debug_walk_prefill")
+    n = int(cnt.item())
+    if n > max_records:
+        raise RuntimeError("walk produced more records than the buffer holds")
+    return rec[:n].cpu(), read_status(ws)

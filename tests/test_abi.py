@@ -1,0 +1,99 @@
+"""The C-ABI library loads and exports what include/relattn.h declares.
+
+Runs without a GPU: only host-side entry points are called (no kernel).
+"""
+
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from paged_relative_bias_gb300 import build as B
+from paged_relative_bias_gb300 import relattn as R
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "relattn.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(relattn_\w+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return R.lib()
+
+
+def test_header_lists_the_entry_points():
+    names = declared_functions()
+    assert "relattn_decode" in names and "relattn_prefill" in names
+    assert set(names) == set(R.EXPORTS)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", B.lib_path()],
+                         capture_output=True, text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (relattn_\w+)", out))
+    for name in declared_functions():
+        assert name in exported, name
+        assert getattr(lib, name) is not None
+
+
+def test_no_torch_types_in_the_abi():
+    text = open(HEADER).read()
+    for bad in ("torch", "at::", "Tensor", "c10"):
+        assert bad not in text
+
+
+def test_status_strings_and_version(lib):
+    assert R.status_string(0) == "ok"
+    assert "invalid" in R.status_string(1)
+    assert "unsupported" in R.status_string(2)
+    assert "workspace" in R.status_string(3)
+    assert "CUDA" in R.status_string(4)
+    assert lib.relattn_abi_version() == 100
+
+
+def test_invalid_arguments_rejected_on_host(lib):
+    """Null or inconsistent arguments fail before any CUDA work."""
+    dims = R.Dims(1, 4, 2, 0, 0, 0)
+    good = R.KVCacheDesc(16, 16, 2, 128, 1, 128, 128)
+    rc = lib.relattn_decode(None, None, ctypes.byref(good), None, None, 0, 64,
+                            ctypes.byref(dims), None, None, 0, None)
+    assert rc == R.ERR_INVALID_ARG
+    bad_bs = R.KVCacheDesc(16, 16, 2, 64, 1, 128, 128)
+    rc = lib.relattn_decode(16, 16, ctypes.byref(bad_bs), 16, 16, 0, 64,
+                            ctypes.byref(dims), 16, 16, 1 << 20, None)
+    assert rc == R.ERR_UNSUPPORTED
+    bad_dv = R.KVCacheDesc(16, 16, 2, 128, 1, 128, 96)
+    rc = lib.relattn_decode(16, 16, ctypes.byref(bad_dv), 16, 16, 0, 64,
+                            ctypes.byref(dims), 16, 16, 1 << 20, None)
+    assert rc == R.ERR_UNSUPPORTED
+    misaligned = R.KVCacheDesc(17, 16, 2, 128, 1, 128, 128)
+    rc = lib.relattn_decode(16, 16, ctypes.byref(misaligned), 16, 16, 0, 64,
+                            ctypes.byref(dims), 16, 16, 1 << 20, None)
+    assert rc == R.ERR_INVALID_ARG
+    gqa = R.Dims(1, 5, 2, 0, 0, 0)  # 5 query heads over 2 KV heads
+    two = R.KVCacheDesc(16, 16, 2, 128, 2, 128, 128)
+    rc = lib.relattn_decode(16, 16, ctypes.byref(two), 16, 16, 0, 64,
+                            ctypes.byref(gqa), 16, 16, 1 << 20, None)
+    assert rc == R.ERR_INVALID_ARG
+    wide = R.Dims(1, 34, 2, 0, 0, 0)  # 17 query heads per KV head
+    rc = lib.relattn_decode(16, 16, ctypes.byref(two), 16, 16, 0, 64,
+                            ctypes.byref(wide), 16, 16, 1 << 20, None)
+    assert rc == R.ERR_UNSUPPORTED
+    rc = lib.relattn_prefill(None, None, None, None, None, ctypes.byref(good), None, None,
+                             0, 64, ctypes.byref(dims), None, None, 0, None)
+    assert rc == R.ERR_INVALID_ARG
+
+
+def test_product_path_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(R, "_LIB", None)
+    monkeypatch.setattr(R, "library_path", lambda: str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="no CPU fallback"):
+        R.lib()
