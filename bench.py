@@ -1,0 +1,534 @@
+#!/usr/bin/env python3
+"""Benchmark of paged relative-bias attention on GB300.
+
+One step = one relattn_decode call on the Inkling-Small local-layer decode
+workload (16 sequences, 32/8 heads, d = 128, window = rel_extent = 512,
+lengths uniform in [4096, 32768], 128-token blocks from a 4096-block pool):
+the window-aware walk, the split-KV kernel and the split-combine, all in one
+kernel launch.  L2 is flushed (a write of 2x the L2 size) between steps and
+each step is timed alone with CUDA events on the launching stream.
+
+The JSON line reports decode HBM GB/s of algorithmic bytes (window keys at
+token granularity, q, the used part of rel, out, block-table entries), the
+decode kernel's roofline against the measured HBM copy peak, an end-to-end
+figure through the C ABI with host buffers, the float64 oracle timed on the
+host cores, and -- under "secondary" -- the other decode workloads and the
+chunked prefill's TFLOP/s.
+
+--impl reference times the oracle itself (on host cores) on the same
+workload and metric.  --gpus N runs N independent replicas (one per rank);
+the path does not shard.
+"""
+
+import os
+
+# The oracle legs run with one BLAS thread; the count is reported.
+for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+import argparse  # noqa: E402
+import json  # noqa: E402
+import math  # noqa: E402
+import statistics  # noqa: E402
+import subprocess  # noqa: E402
+import sys  # noqa: E402
+import time  # noqa: E402
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from paged_relative_bias_gb300 import inputs as I  # noqa: E402
+
+METRIC = ("relattn decode HBM GB/s (% of peak) + ms/step; "
+          "prefill TFLOP/s (% BF16 peak)")
+BLOCK = 128
+
+
+# ---------------------------------------------------------------------------
+# algorithmic work
+# ---------------------------------------------------------------------------
+
+def decode_work(wl, seq_lens):
+    """Algorithmic bytes of one decode call and of each (sequence, KV head)."""
+    g = wl.num_q_heads // wl.num_kv_heads
+    total = 0
+    per_group = []
+    for L in seq_lens:
+        n = min(wl.window, L) if wl.window > 0 else L
+        P = L - 1
+        lo = P - n + 1
+        blocks = P // BLOCK - lo // BLOCK + 1
+        kv = n * (wl.d_qk + wl.d_v) * 2
+        head = wl.d_qk * 2 + min(wl.rel_extent, n) * 4 + wl.d_v * 2
+        grp = kv + g * head
+        per_group.append(grp)
+        total += wl.num_kv_heads * grp + blocks * 4 + 4
+    return total, per_group
+
+
+def prefill_work(wl):
+    """(flops, bytes) of one chunked-prefill call, visible pairs only."""
+    flops = 0
+    rel = 0
+    kv_prefix = 0
+    for n, ctx in zip(wl.new_tokens, wl.ctx_lens):
+        for t in range(n):
+            P = ctx + t
+            vis = min(wl.window, P + 1) if wl.window > 0 else P + 1
+            flops += vis
+            rel += min(wl.rel_extent, vis)
+        lo = max(0, ctx - wl.window + 1) if wl.window > 0 else 0
+        kv_prefix += max(0, ctx - lo)
+    T = sum(wl.new_tokens)
+    Hq, Hkv = wl.num_q_heads, wl.num_kv_heads
+    kvrow = Hkv * (wl.d_qk + wl.d_v) * 2
+    flops *= Hq * 2 * (wl.d_qk + wl.d_v)
+    nbytes = (rel * Hq * 4 + T * Hq * (wl.d_qk + wl.d_v) * 2 + 2 * T * kvrow
+              + kv_prefix * kvrow)
+    return flops, nbytes
+
+
+def describe(wl):
+    if isinstance(wl, I.DecodeWorkload):
+        lens = {"fixed": lambda s: f"L={s[1]}", "uniform": lambda s: f"L~U[{s[1]},{s[2]}]",
+                "loguniform": lambda s: f"L~logU[{s[1]},{s[2]}]"}[wl.lengths[0]](wl.lengths)
+        win = f"W={wl.window}" if wl.window > 0 else "global"
+        return (f"{wl.name}: decode B={wl.batch}, {wl.num_q_heads}/{wl.num_kv_heads} heads, "
+                f"d_qk={wl.d_qk} d_v={wl.d_v}, {win}, rel_extent={wl.rel_extent}, {lens}, "
+                f"bf16 paged KV in 128-token blocks, random block tables")
+    win = f"W={wl.window}" if wl.window > 0 else "global"
+    return (f"{wl.name}: chunked prefill {len(wl.new_tokens)}x{wl.new_tokens[0]} new tokens "
+            f"after {wl.ctx_lens[0]} cached, {wl.num_q_heads}/{wl.num_kv_heads} heads, "
+            f"d={wl.d_qk}, {win}, rel_extent={wl.rel_extent}")
+
+
+# ---------------------------------------------------------------------------
+# environment
+# ---------------------------------------------------------------------------
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return dict(hbm=float(d["hbm_gbs"]), bf16=float(d["bf16_tflops"]),
+                    bf16_sustained=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                    source="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sustained=1700.0, source="fallback")
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples every 100 ms while running."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        ident = str(device_index)
+        try:
+            u = str(torch.cuda.get_device_properties(device_index).uuid)
+            ident = u if u.startswith("GPU-") else "GPU-" + u
+        except Exception:
+            pass
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", ident], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        self.windows = []
+
+    def mark(self, t0, t1):
+        self.windows.append((t0, t1))
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        rows = []
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                ts = time.mktime(time.strptime(f[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                rows.append(dict(ts=ts, sm=float(f[1]), smax=float(f[2]),
+                                 hw=f[5], hwt=f[6], swt=f[7], swp=f[8]))
+            except ValueError:
+                continue
+        inside = [r for r in rows if any(a - 1 <= r["ts"] <= b + 1 for a, b in self.windows)]
+        use = inside if len(inside) >= 3 else rows
+        reasons = set()
+        for r in use:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("swp", "sw_power_cap")):
+                if r[key].lower().startswith("active"):
+                    reasons.add(name)
+        if not use:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(r["sm"] for r in use),
+                "sm_max_mhz": max(r["smax"] for r in use),
+                "reasons": sorted(reasons), "samples": len(use)}
+
+
+class Dist:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as dist
+            torch.cuda.set_device(self.local)
+            dist.init_process_group("nccl", device_id=torch.device("cuda", self.local))
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, x: float) -> float:
+        if not self.pg:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=f"cuda:{self.local}")
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------
+# timing
+# ---------------------------------------------------------------------------
+
+def timed_steps(fn, steps, warmup, flush, dist, sampler):
+    """Per-step device times (ms) of fn, L2 flushed before every step."""
+    for _ in range(warmup):
+        flush()
+        fn()
+    torch.cuda.synchronize()
+    dist.barrier()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    t0 = time.time()
+    for a, b in ev:
+        flush()
+        a.record()
+        fn()
+        b.record()
+    torch.cuda.synchronize()
+    dist.barrier()
+    torch.cuda.synchronize()
+    sampler.mark(t0, time.time())
+    return [a.elapsed_time(b) for a, b in ev]
+
+
+def roofline(bound, achieved, peak, unit, traffic):
+    return {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
+            "frac": round(achieved / peak, 4), "traffic": traffic}
+
+
+def committed_traffic(kernel_tag):
+    """dram bytes per launch from a committed ncu summary, if still current.
+
+    profiles/<tag>.traffic holds `<bytes> <sha256 of the kernel source>`; the
+    number is used only while the source is unchanged since the capture.
+    """
+    import hashlib
+    path = os.path.join(ROOT, "profiles", kernel_tag + ".traffic")
+    if not os.path.exists(path):
+        return None
+    try:
+        nbytes, digest = open(path).read().split()[:2]
+    except ValueError:
+        return None
+    src = os.path.join(ROOT, "paged_relative_bias_gb300", "csrc",
+                       {"decode": "relattn_decode.cu", "prefill": "relattn_prefill.cu"}[
+                           kernel_tag.split("_")[0]])
+    h = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    return int(float(nbytes)) if h == digest else None
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def run_decode(R, wl, device, steps, warmup, flush, dist, sampler):
+    case = I.make_decode(wl, device)
+    lens = case["seq_lens"].cpu().tolist()
+    alg, _ = decode_work(wl, lens)
+    dims = R.decode_dims(case["q"], case["block_table"])
+    ws = R.new_workspace(R.workspace_size(dims, R.cache_desc(case["k_cache"],
+                                                             case["v_cache"])), device)
+    out = torch.empty((wl.batch, wl.num_q_heads, wl.d_v), dtype=torch.bfloat16, device=device)
+
+    def step():
+        R.relattn_decode(case["q"], case["rel"], case["k_cache"], case["v_cache"],
+                         case["block_table"], case["seq_lens"], wl.window, wl.rel_extent,
+                         out=out, workspace=ws)
+
+    times = timed_steps(step, steps, warmup, flush, dist, sampler)
+    if R.read_status(ws) != 0:
+        raise RuntimeError("decode reported a device status")
+    return case, alg, times, ws, out
+
+
+def run_decode_e2e(R, case, wl, alg, ws, device, steps, warmup, flush, dist, sampler):
+    """Same call with host inputs: pinned H2D copies and the D2H of out inside."""
+    host = {k: case[k].cpu().pin_memory() for k in ("q", "rel", "seq_lens", "block_table")}
+    dev = {k: torch.empty_like(case[k]) for k in host}
+    out_h = torch.empty((wl.batch, wl.num_q_heads, wl.d_v), dtype=torch.bfloat16).pin_memory()
+    out_d = torch.empty_like(out_h, device=device)
+
+    def step():
+        for k in host:
+            dev[k].copy_(host[k], non_blocking=True)
+        R.relattn_decode(dev["q"], dev["rel"], case["k_cache"], case["v_cache"],
+                         dev["block_table"], dev["seq_lens"], wl.window, wl.rel_extent,
+                         out=out_d, workspace=ws)
+        out_h.copy_(out_d, non_blocking=True)
+
+    times = timed_steps(step, steps, warmup, flush, dist, sampler)
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_h.numel() * out_h.element_size()
+    return times, h2d, d2h
+
+
+def run_prefill(R, wl, device, steps, warmup, flush, dist, sampler):
+    case = I.make_prefill(wl, device)
+    dims = R.prefill_dims(case["q"], case["block_table"], case["ctx_lens"], case["max_q_len"])
+    ws = R.new_workspace(R.workspace_size(dims, R.cache_desc(case["k_cache"],
+                                                             case["v_cache"])), device)
+    out = torch.empty((case["num_tokens"], wl.num_q_heads, wl.d_v), dtype=torch.bfloat16,
+                      device=device)
+
+    def step():
+        R.relattn_prefill(case["q"], case["k"], case["v"], case["rel"], case["cu_seqlens"],
+                          case["k_cache"], case["v_cache"], case["block_table"],
+                          case["ctx_lens"], wl.window, wl.rel_extent, case["max_q_len"],
+                          out=out, workspace=ws)
+
+    times = timed_steps(step, steps, warmup, flush, dist, sampler)
+    if R.read_status(ws) != 0:
+        raise RuntimeError("prefill reported a device status")
+    del case
+    return times
+
+
+def oracle_decode_sample(case, wl, budget_s):
+    """Time the float64 oracle on (sequence, KV head) groups for ~budget_s."""
+    from oracle import relattn_oracle as O
+    from paged_relative_bias_gb300.inputs import bf16_bits
+    lens = case["seq_lens"].cpu().tolist()
+    _, per_group = decode_work(wl, lens)
+    g = wl.num_q_heads // wl.num_kv_heads
+    q = bf16_bits(case["q"])
+    rel = case["rel"].cpu().numpy()
+    table = case["block_table"].cpu().numpy()
+    done, nbytes, elapsed = 0, 0, 0.0
+    groups = [(b, kvh) for b in range(wl.batch) for kvh in range(wl.num_kv_heads)]
+    for b, kvh in groups:
+        if elapsed >= budget_s:
+            break
+        L = lens[b]
+        blocks = O.decode_blocks(L, wl.window, table[b])
+        ids = torch.tensor([p for _, p in blocks], device=case["k_cache"].device)
+        kc = bf16_bits(case["k_cache"].index_select(0, ids))
+        vc = bf16_bits(case["v_cache"].index_select(0, ids))
+        sub = np.full((1, table.shape[1]), -1, dtype=np.int64)
+        for i, (lblk, _) in enumerate(blocks):
+            sub[0, lblk] = i
+        heads = list(range(kvh * g, (kvh + 1) * g))
+        t0 = time.perf_counter()
+        O.decode(q[b:b + 1], rel[b:b + 1], kc, vc, sub, np.array([L]), wl.window,
+                 wl.rel_extent, heads=heads)
+        elapsed += time.perf_counter() - t0
+        done += 1
+        nbytes += per_group[b]
+    return nbytes / elapsed / 1e9, done, len(groups), elapsed
+
+
+def cores_used():
+    return int(os.environ.get("OMP_NUM_THREADS", "1"))
+
+
+def ours(args):
+    from paged_relative_bias_gb300 import build as B
+    from paged_relative_bias_gb300 import relattn as R
+    B.build()
+    R.lib()
+    dist = Dist()
+    device = torch.device("cuda", dist.local)
+    torch.cuda.set_device(device)
+    peaks = load_peaks()
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    flush_buf = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=device)
+
+    def flush():
+        flush_buf.zero_()
+
+    sampler = ClockSampler(device.index)
+    wl = I.WORKLOADS[args.workload]
+    case, alg, times, ws, _ = run_decode(R, wl, device, args.steps, args.warmup, flush, dist,
+                                         sampler)
+    t_ms = sum(times) / len(times)
+    t_max = dist.max(sum(times))
+    value = alg * dist.world * args.steps / (t_max / 1e3) / 1e9
+    kernel_gbs = alg / (t_ms / 1e3) / 1e9
+    e2e_times, h2d, d2h = run_decode_e2e(R, case, wl, alg, ws, device, args.steps,
+                                         args.warmup, flush, dist, sampler)
+    e2e_max = dist.max(sum(e2e_times))
+    e2e_value = alg * dist.world * args.steps / (e2e_max / 1e3) / 1e9
+
+    secondary = []
+    if not args.no_secondary:
+        for name in ("global_decode_b1", "global_decode_b8", "diffhead_decode"):
+            w2 = I.WORKLOADS[name]
+            c2, a2, t2, _, _ = run_decode(R, w2, device, args.secondary_steps, 3, flush, dist,
+                                          sampler)
+            m2 = sum(t2) / len(t2)
+            gbs = a2 / (m2 / 1e3) / 1e9
+            secondary.append({
+                "workload": describe(w2), "metric": "decode HBM GB/s", "value": round(gbs, 2),
+                "unit": "GB/s", "ms_per_step": round(m2, 5), "alg_bytes": a2,
+                "roofline": roofline("hbm", gbs, peaks["hbm"], "GB/s", None),
+                "frac_of_nominal_8000": round(gbs / 8000.0, 4)})
+            del c2
+            torch.cuda.empty_cache()
+        wp = I.WORKLOADS["chunked_prefill"]
+        flops, pbytes = prefill_work(wp)
+        tp = run_prefill(R, wp, device, max(3, args.secondary_steps // 4), 2, flush, dist,
+                         sampler)
+        mp = sum(tp) / len(tp)
+        tflops = flops / (mp / 1e3) / 1e12
+        gbs = pbytes / (mp / 1e3) / 1e9
+        secondary.append({
+            "workload": describe(wp), "metric": "prefill TFLOP/s", "value": round(tflops, 2),
+            "unit": "TFLOP/s", "ms_per_step": round(mp, 4), "alg_flops": flops,
+            "alg_bytes": pbytes,
+            "roofline": roofline("hbm", gbs, peaks["hbm"], "GB/s", None),
+            "tensor_frac_of_bf16_peak": round(tflops / peaks["bf16"], 4),
+            "note": "step = cache write + attention kernels; rel (fp32) is most of the bytes"})
+        torch.cuda.empty_cache()
+    clocks = sampler.stop()
+
+    cpu = None
+    if dist.world == 1 and not args.no_cpu_baseline:
+        gbs, done, total, el = oracle_decode_sample(case, wl, args.cpu_budget)
+        cpu = {"value": round(gbs, 6), "unit": "GB/s", "cores": cores_used(), "kind": "oracle",
+               "sample": f"{done} of {total} (sequence, KV head) groups of the same workload, "
+                         f"float64 numpy, {el:.3f} s of CPU time"}
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": dist.world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t_ms, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) q/k/v bf16, rel fp32)",
+        "config": {"workload": describe(wl), "l2": "flushed before every step (2x L2 write)",
+                   "parallelism": f"replicas x{dist.world} (the path does not shard)"},
+        "roofline": roofline("hbm", kernel_gbs, peaks["hbm"], "GB/s",
+                             committed_traffic("decode_" + args.workload)),
+        "peak_source": peaks["source"],
+        "frac_of_nominal_8000": round(kernel_gbs / 8000.0, 4),
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(sum(e2e_times) / len(e2e_times), 5)},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+        "secondary": secondary,
+    }
+    if dist.rank == 0:
+        print(json.dumps(line), flush=True)
+    dist.close()
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the oracle on host cores
+# ---------------------------------------------------------------------------
+
+def reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from oracle import relattn_oracle as O
+    from paged_relative_bias_gb300.inputs import bf16_bits
+    wl = I.WORKLOADS[args.workload]
+    device = "cuda" if torch.cuda.is_available() else "cpu"
+    case = I.make_decode(wl, device)
+    lens = case["seq_lens"].cpu().tolist()
+    _, per_group = decode_work(wl, lens)
+    g = wl.num_q_heads // wl.num_kv_heads
+    q = bf16_bits(case["q"])
+    rel = case["rel"].cpu().numpy()
+    table = case["block_table"].cpu().numpy()
+    groups = [(b, kvh) for b in range(wl.batch) for kvh in range(wl.num_kv_heads)]
+    prepared = []
+    for b in range(wl.batch):
+        blocks = O.decode_blocks(lens[b], wl.window, table[b])
+        ids = torch.tensor([p for _, p in blocks], device=case["k_cache"].device)
+        sub = np.full((1, table.shape[1]), -1, dtype=np.int64)
+        for i, (lblk, _) in enumerate(blocks):
+            sub[0, lblk] = i
+        prepared.append((bf16_bits(case["k_cache"].index_select(0, ids)),
+                         bf16_bits(case["v_cache"].index_select(0, ids)), sub))
+
+    def step(i):
+        b, kvh = groups[i % len(groups)]
+        kc, vc, sub = prepared[b]
+        O.decode(q[b:b + 1], rel[b:b + 1], kc, vc, sub, np.array([lens[b]]), wl.window,
+                 wl.rel_extent, heads=list(range(kvh * g, (kvh + 1) * g)))
+        return per_group[b]
+
+    for i in range(args.warmup):
+        step(i)
+    nbytes = 0
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        nbytes += step(args.warmup + i)
+    el = time.perf_counter() - t0
+    value = nbytes / el / 1e9
+    sample = (f"each step: one (sequence, KV head) group of the workload "
+              f"({g} query heads over its window), float64 numpy oracle")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "GB/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(el / args.steps * 1e3, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": describe(wl), "l2": "n/a (host)", "parallelism": "host"},
+        "cpu_baseline": {"value": round(value, 6), "unit": "GB/s", "cores": cores_used(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0}}), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="local_decode",
+                    choices=["local_decode", "global_decode_b1", "global_decode_b8",
+                             "diffhead_decode"])
+    ap.add_argument("--secondary-steps", type=int, default=50)
+    ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        reference(args)
+    else:
+        ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -218,15 +218,13 @@ static int prepare_decode(const void* q, const float* rel, const relattn_kv_cach
   L->grid = grid;
   if (walk) {
     p.nstages = 0;
-    p.stage_bytes = 0;
     return RELATTN_OK;
   }
-  p.rel_off = 16384 + kTileKeys * cache->d_v * 2;
-  p.stage_bytes = p.rel_off + static_cast<int>(round_up(static_cast<size_t>(g) * kRelBoxW * 4, 1024));
+  // An even number of stages: the decode kernel's two consumer groups each
+  // own every other stage.
   p.nstages = kMaxStages;
-  while (p.nstages >= 2 &&
-         decode_smem_bytes(p.nstages, p.stage_bytes, p.B, p.dv) > di->smem_optin)
-    --p.nstages;
+  while (p.nstages >= 2 && decode_smem_bytes(p.nstages, p.B, p.g, p.dv) > di->smem_optin)
+    p.nstages -= 2;
   if (p.nstages < 2) return RELATTN_ERR_UNSUPPORTED;  // batch too large for shared memory
   if (!cache_maps(cache, &L->tm_k, &L->tm_v)) return RELATTN_ERR_CUDA;
   const cuuint64_t rd[2] = {static_cast<cuuint64_t>(rel_extent),
@@ -235,6 +233,13 @@ static int prepare_decode(const void* q, const float* rel, const relattn_kv_cach
   const cuuint32_t rb[2] = {static_cast<cuuint32_t>(kRelBoxW), static_cast<cuuint32_t>(g)};
   if (!make_map(&L->tm_rel, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(rel), rd,
                 rs, rb, CU_TENSOR_MAP_SWIZZLE_NONE))
+    return RELATTN_ERR_CUDA;
+  // query rows of one KV group: [B*Hq][128] bf16, two 64-column halves
+  const cuuint64_t qd[2] = {128, static_cast<cuuint64_t>(dims->batch) * dims->num_q_heads};
+  const cuuint64_t qs[1] = {256};
+  const cuuint32_t qbx[2] = {64, static_cast<cuuint32_t>(g)};
+  if (!make_map(&L->tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(q), qd, qs,
+                qbx, CU_TENSOR_MAP_SWIZZLE_128B))
     return RELATTN_ERR_CUDA;
   return RELATTN_OK;
 }

@@ -4,21 +4,25 @@
 //  * the window-aware walk: each sequence contributes the 64-key tiles that
 //    hold a visible key (at most ceil(W/128)+1 blocks on a local layer --
 //    "Inkling-Small on Gaudi 2", section "Decode window");
-//  * the work split: the tiles of all (sequence, KV head) pairs are laid end
-//    to end and cut into gridDim.x equal contiguous ranges, one per CTA, so
-//    the number of splits per sequence follows from batch, heads and lengths
-//    ("vLLM TML Inkling Support", section "Low-Latency Collectives and
-//    Kernels": num_splits chosen from batch size and KV length);
-//  * the split kernel: one producer warp streams K, V and the rel slice of
-//    each tile with TMA into a ring of shared-memory stages; four consumer
-//    warps each take 16 keys of every tile, with all g query heads of the KV
-//    head packed as the 16 rows of an mma.sync tile ("Inkling 2 Small on
-//    vLLM", section "vLLM integration and optimisation": heads of one KV group
-//    packed into one tile, KV read once), add the bias from the stage's rel
-//    slice and run an online softmax;
-//  * the split-combine: a sequence cut by a range boundary leaves a partial
-//    (normalised output, log-sum-exp) per piece in the workspace; the CTA
-//    that finishes the sequence last (counted with an atomic) merges them.
+//  * the work split ("vLLM TML Inkling Support", section "Low-Latency
+//    Collectives and Kernels": num_splits chosen from batch size and KV
+//    length): the tiles of all (sequence, KV head) segments are laid end to
+//    end and cut into gridDim.x equal contiguous ranges, one per CTA.  When
+//    no segment is much longer than a CTA's share, the cuts snap to segment
+//    boundaries so that no segment is split (no partials, no combine);
+//    otherwise segments are cut exactly where the ranges end;
+//  * the split kernel: a producer warp streams each piece's query rows, and
+//    K, V and the rel slice of every tile, with TMA into shared memory; two
+//    groups of four consumer warps take alternate tiles, each warp 16 keys
+//    of a tile, with all g query heads of the KV head packed as the 16 rows
+//    of an mma.sync tile ("Inkling 2 Small on vLLM", section "vLLM
+//    integration and optimisation": the heads of one KV group packed into
+//    one tile, KV read once); the bias comes from the stage's rel slice and
+//    feeds an online softmax;
+//  * the split-combine: a segment cut by a range boundary leaves one partial
+//    (normalised output, base-2 log-sum-exp) per piece in the workspace; the
+//    CTA that finishes the segment last (counted with an acq_rel atomic)
+//    merges them in a fixed order.
 #include "relattn_common.cuh"
 #include "relattn_internal.h"
 
@@ -26,8 +30,11 @@ namespace relattn {
 
 namespace {
 
-constexpr int kDecodeThreads = 160;  // warp 0: producer, warps 1-4: consumers
-constexpr int kConsumers = 4;
+constexpr int kConsumerWarps = 8;  // two groups of four
+constexpr int kDecodeThreads = 32 * (1 + kConsumerWarps);
+constexpr int kConsumerThreads = 32 * kConsumerWarps;
+constexpr int kWholeSlackTiles = 4;  // tolerated imbalance to avoid a split
+constexpr int kQBufBytes = 4096;     // 16 rows x 256 B as two swizzled halves
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kNegInf = -__builtin_huge_valf();
 
@@ -37,24 +44,47 @@ __device__ __forceinline__ float lg2(float x) {
   return y;
 }
 
-// Shared-memory carve-up; identical on host and device.
+__device__ __forceinline__ int atom_add_acq_rel(int* p, int v) {
+  int old;
+  asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], %2;"
+               : "=r"(old)
+               : "l"(p), "r"(v)
+               : "memory");
+  return old;
+}
+
+// Shared-memory carve-up (byte offsets from a 1024-aligned base); identical
+// on host and device.  K/V stages are 1024-aligned for the 128-byte swizzle;
+// the rel slices of the stages live in a ring of their own.
 struct DecodeSmem {
-  int stages, bars, valid, seqlen, nt, pref, m, l, M, L, obuf, flag, total;
-  __host__ __device__ DecodeSmem(int nstages, int stage_bytes, int B, int dv) {
-    stages = 0;
-    bars = nstages * stage_bytes;
-    valid = bars + nstages * 16;
+  int qbuf, stages, stage_bytes, rel, rel_bytes, slices, bars, valid, seqlen, nt, pref, m, l,
+      M, L, misc, total;
+  __host__ __device__ DecodeSmem(int nstages, int B, int g, int dv) {
+    stage_bytes = 16384 + kTileKeys * dv * 2;
+    rel_bytes = (g * kRelBoxW * 4 + 127) & ~127;
+    qbuf = 0;
+    stages = qbuf + 2 * kQBufBytes;
+    rel = stages + nstages * stage_bytes;
+    slices = rel + nstages * rel_bytes;
+    bars = (slices + kConsumerWarps * g * dv * 4 + 15) & ~15;
+    valid = bars + (2 * nstages + 4) * 8;
     seqlen = valid + nstages * 4;
     nt = seqlen + B * 4;
     pref = nt + B * 4;
     m = (pref + (B + 1) * 4 + 15) & ~15;
-    l = m + kConsumers * 16 * 4;
-    M = l + kConsumers * 16 * 4;
+    l = m + kConsumerWarps * 16 * 4;
+    M = l + kConsumerWarps * 16 * 4;
     L = M + 16 * 4;
-    obuf = L + 16 * 4;
-    flag = obuf + 16 * dv * 4;
-    total = flag + 16;
+    misc = L + 16 * 4;
+    total = misc + 16;
   }
+};
+
+// How the CTA ranges are cut.
+struct Plan {
+  long long T;  // tiles of all segments
+  int G;        // CTAs with work: min(gridDim.x, T)
+  int whole;    // 1: cuts snap to segment boundaries
 };
 
 // The piece of a CTA's range that falls in one (sequence, KV head) segment.
@@ -63,10 +93,7 @@ struct Piece {
   long long seg_start, seg_end;
 };
 
-__device__ __forceinline__ Piece locate_piece(long long f, long long a1,
-                                              const int* s_pref,
-                                              const int* s_nt, int B,
-                                              int Hkv) {
+__device__ __forceinline__ int seq_of(long long f, const int* s_pref, int B, int Hkv) {
   int lo = 0, hi = B - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -75,36 +102,58 @@ __device__ __forceinline__ Piece locate_piece(long long f, long long a1,
     else
       hi = mid - 1;
   }
+  return lo;
+}
+
+__device__ __forceinline__ Piece locate_piece(long long f, long long a1, const int* s_pref,
+                                              const int* s_nt, int B, int Hkv) {
   Piece pc;
-  pc.b = lo;
-  const int nt = s_nt[lo];
-  const long long off = f - static_cast<long long>(Hkv) * s_pref[lo];
+  pc.b = seq_of(f, s_pref, B, Hkv);
+  const int nt = s_nt[pc.b];
+  const long long off = f - static_cast<long long>(Hkv) * s_pref[pc.b];
   pc.kvh = static_cast<int>(off / nt);
   pc.i0 = static_cast<int>(off % nt);
-  pc.seg_start = static_cast<long long>(Hkv) * s_pref[lo] +
+  pc.seg_start = static_cast<long long>(Hkv) * s_pref[pc.b] +
                  static_cast<long long>(pc.kvh) * nt;
   pc.seg_end = pc.seg_start + nt;
   pc.n = static_cast<int>(min(a1, pc.seg_end) - f);
   return pc;
 }
 
-// CTA owning flat tile f when T tiles are cut into G ranges
-// [floor(c*T/G), floor((c+1)*T/G)).
-__device__ __forceinline__ int cta_of(long long f, long long T, int G) {
-  return static_cast<int>(((f + 1) * G - 1) / T);
+// Exact cut c of T tiles into G ranges: floor(c*T/G).
+__device__ __forceinline__ long long exact_cut(int c, const Plan& pl) {
+  return static_cast<long long>(c) * pl.T / pl.G;
 }
 
-__device__ __forceinline__ long long range_start(int c, long long T, int G) {
-  return static_cast<long long>(c) * T / G;
+// CTA owning flat tile f under exact cuts.
+__device__ __forceinline__ int cta_of(long long f, const Plan& pl) {
+  return static_cast<int>(((f + 1) * pl.G - 1) / pl.T);
 }
 
-// Per-CTA prologue: each sequence's tile count and their exclusive prefix.
-// Returns the total tile count of all (sequence, KV head) segments.
-__device__ long long decode_prologue(const DecodeParams& p, uint8_t* smem,
-                                     const DecodeSmem& L, bool zero_bad) {
+// Start of CTA c's range: the exact cut, snapped to the nearer segment
+// boundary in whole-segment mode.
+__device__ __forceinline__ long long range_cut(int c, const Plan& pl, const int* s_pref,
+                                               const int* s_nt, int B, int Hkv) {
+  long long f = exact_cut(c, pl);
+  if (pl.whole && f > 0 && f < pl.T) {
+    const int b = seq_of(f, s_pref, B, Hkv);
+    const int nt = s_nt[b];
+    const long long base = static_cast<long long>(Hkv) * s_pref[b];
+    const long long s0 = base + (f - base) / nt * nt;
+    const long long s1 = s0 + nt;
+    f = (f - s0 <= s1 - f) ? s0 : s1;
+  }
+  return f;
+}
+
+// Per-CTA prologue: each sequence's tile count, their exclusive prefix and
+// the cut plan.
+__device__ Plan decode_prologue(const DecodeParams& p, uint8_t* smem, const DecodeSmem& L,
+                                bool zero_bad) {
   int* s_len = reinterpret_cast<int*>(smem + L.seqlen);
   int* s_nt = reinterpret_cast<int*>(smem + L.nt);
   int* s_pref = reinterpret_cast<int*>(smem + L.pref);
+  int* s_misc = reinterpret_cast<int*>(smem + L.misc);
   const int tid = threadIdx.x;
   for (int b = tid; b < p.B; b += blockDim.x) {
     const int len = p.seq_lens[b];
@@ -118,96 +167,131 @@ __device__ long long decode_prologue(const DecodeParams& p, uint8_t* smem,
     const int lane = tid;
     const int chunk = (p.B + 31) / 32;
     const int beg = lane * chunk, end = min(p.B, beg + chunk);
-    int sum = 0;
-    for (int i = beg; i < end; ++i) sum += s_nt[i];
+    int sum = 0, mx = 0;
+    for (int i = beg; i < end; ++i) {
+      sum += s_nt[i];
+      mx = max(mx, s_nt[i]);
+    }
     int incl = sum;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int v = __shfl_up_sync(0xffffffffu, incl, o);
       if (lane >= o) incl += v;
+      mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
     }
     int run = incl - sum;
     for (int i = beg; i < end; ++i) {
       s_pref[i] = run;
       run += s_nt[i];
     }
-    if (lane == 31) s_pref[p.B] = incl;
+    if (lane == 31) {
+      s_pref[p.B] = incl;
+      s_misc[0] = mx;
+    }
   }
   __syncthreads();
   if (zero_bad && blockIdx.x == 0 && p.out != nullptr) {
-    // Sequences with an invalid length get zero output.
-    const int per = p.Hq * p.dv;
+    const int per = p.Hq * p.dv;  // sequences with an invalid length get zeros
     for (int b = 0; b < p.B; ++b) {
       if (s_nt[b] != 0) continue;
       __nv_bfloat16* o = p.out + static_cast<size_t>(b) * per;
       for (int i = tid; i < per; i += blockDim.x) o[i] = __float2bfloat16(0.f);
     }
   }
-  return static_cast<long long>(p.Hkv) * s_pref[p.B];
+  Plan pl;
+  pl.T = static_cast<long long>(p.Hkv) * s_pref[p.B];
+  pl.G = static_cast<int>(min(static_cast<long long>(gridDim.x), pl.T));
+  pl.whole = pl.G > 0 && static_cast<long long>(s_misc[0]) * pl.G <=
+                             pl.T + static_cast<long long>(kWholeSlackTiles) * pl.G;
+  return pl;
 }
 
 template <int DV>
 __global__ void __launch_bounds__(kDecodeThreads, 1)
-    decode_kernel(const __grid_constant__ CUtensorMap tm_k,
+    decode_kernel(const __grid_constant__ CUtensorMap tm_q,
+                  const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v,
-                  const __grid_constant__ CUtensorMap tm_rel,
-                  const DecodeParams p) {
+                  const __grid_constant__ CUtensorMap tm_rel, const DecodeParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const DecodeSmem L(p.nstages, p.stage_bytes, p.B, DV);
+  const int g = p.g;
+  const int ns = p.nstages;
+  const DecodeSmem L(ns, p.B, g, DV);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
-  uint64_t* empty = full + p.nstages;
+  uint64_t* empty = full + ns;
+  uint64_t* qfull = empty + ns;
+  uint64_t* qempty = qfull + 2;
   int* s_valid = reinterpret_cast<int*>(smem + L.valid);
   const int* s_len = reinterpret_cast<const int*>(smem + L.seqlen);
   const int* s_nt = reinterpret_cast<const int*>(smem + L.nt);
   const int* s_pref = reinterpret_cast<const int*>(smem + L.pref);
+  int* s_misc = reinterpret_cast<int*>(smem + L.misc);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   if (tid == 0) {
-    for (int s = 0; s < p.nstages; ++s) {
+    for (int s = 0; s < ns; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kConsumers);
+      mbar_init(&empty[s], kConsumerWarps / 2);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&qfull[s], 1);
+      mbar_init(&qempty[s], kConsumerWarps);
     }
     fence_mbar_init();
+    tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
     tma_prefetch_desc(&tm_rel);
   }
-  {
-    float* obuf = reinterpret_cast<float*>(smem + L.obuf);
-    for (int i = tid; i < 16 * DV; i += blockDim.x) obuf[i] = 0.f;
-  }
-  const long long T = decode_prologue(p, smem, L, true);
-  const int G = static_cast<int>(min(static_cast<long long>(gridDim.x), T));
-  if (static_cast<int>(blockIdx.x) >= G) return;
+  // query rows g..15 of both buffers stay zero
+  for (int i = tid; i < 2 * kQBufBytes / 16; i += blockDim.x)
+    reinterpret_cast<uint4*>(smem + L.qbuf)[i] = make_uint4(0, 0, 0, 0);
+  fence_proxy_async_smem();
+  const Plan pl = decode_prologue(p, smem, L, true);
+  if (static_cast<int>(blockIdx.x) >= pl.G) return;
   const int c = blockIdx.x;
-  const long long a0 = range_start(c, T, G), a1 = range_start(c + 1, T, G);
-  const int g = p.g;
+  const long long a0 = range_cut(c, pl, s_pref, s_nt, p.B, p.Hkv);
+  const long long a1 = range_cut(c + 1, pl, s_pref, s_nt, p.B, p.Hkv);
   const int stage_tx = 16384 + kTileKeys * DV * 2;
   const int rel_tx = g * kRelBoxW * 4;
+  const int q_tx = 2 * g * 64 * 2;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    int stage = 0;
-    uint32_t phase = 0;
+    int n = 0;     // CTA tile counter
+    int k = 0;     // CTA piece counter
     bool abort = false;
-    for (long long f = a0; f < a1 && !abort;) {
+    for (long long f = a0; f < a1 && !abort; ++k) {
       const Piece pc = locate_piece(f, a1, s_pref, s_nt, p.B, p.Hkv);
       const DecodeSeq sq = decode_seq(s_len[pc.b], p.window, p.max_blocks);
       const int* trow = p.block_table + static_cast<size_t>(pc.b) * p.max_blocks;
+      int bad = 0;
+      if (lane == 0) {
+        const int qb = k & 1;
+        if (!mbar_wait(&qempty[qb], ((k >> 1) & 1) ^ 1)) {
+          report(p.status, RELATTN_DEV_WAIT_TIMEOUT);
+          bad = 1;
+        } else {
+          uint8_t* qs = smem + L.qbuf + qb * kQBufBytes;
+          mbar_arrive_expect_tx(&qfull[qb], q_tx);
+          tma_load_2d(qs, &tm_q, &qfull[qb], 0, pc.b * p.Hq + pc.kvh * g);
+          tma_load_2d(qs + 2048, &tm_q, &qfull[qb], 64, pc.b * p.Hq + pc.kvh * g);
+        }
+      }
+      abort = __shfl_sync(0xffffffffu, bad, 0) != 0;
       for (int c0 = 0; c0 < pc.n && !abort; c0 += 32) {
         const int cn = min(32, pc.n - c0);
         const int tile0 = sq.tile_first + pc.i0 + c0;
         const int blk0 = tile0 >> 1;
         const int nb = ((tile0 + cn - 1) >> 1) - blk0 + 1;
         const int myid = lane < nb ? __ldg(trow + blk0 + lane) : 0;
-        for (int j = 0; j < cn; ++j) {
+        for (int j = 0; j < cn; ++j, ++n) {
           const int tile = tile0 + j;
           const int id = __shfl_sync(0xffffffffu, myid, (tile >> 1) - blk0);
-          int bad = 0;
+          const int stage = n % ns;
           if (lane == 0) {
-            if (!mbar_wait(&empty[stage], phase ^ 1)) {
+            if (!mbar_wait(&empty[stage], ((n / ns) & 1) ^ 1)) {
               report(p.status, RELATTN_DEV_WAIT_TIMEOUT);
               bad = 1;
             } else {
@@ -217,17 +301,15 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
                 const int key0 = tile * kTileKeys;
                 const int dmin = sq.p - key0 - (kTileKeys - 1);
                 const bool need_rel = dmin < p.rel_extent;
-                mbar_arrive_expect_tx(&full[stage],
-                                      stage_tx + (need_rel ? rel_tx : 0));
-                uint8_t* st = smem + static_cast<size_t>(stage) * p.stage_bytes;
+                mbar_arrive_expect_tx(&full[stage], stage_tx + (need_rel ? rel_tx : 0));
+                uint8_t* st = smem + L.stages + stage * L.stage_bytes;
                 const int row = id * kBlockSize + (tile & 1) * kTileKeys;
                 tma_load_3d(st, &tm_k, &full[stage], 0, pc.kvh, row);
                 tma_load_3d(st + 8192, &tm_k, &full[stage], 64, pc.kvh, row);
                 tma_load_3d(st + 16384, &tm_v, &full[stage], 0, pc.kvh, row);
-                if (DV == 128)
-                  tma_load_3d(st + 24576, &tm_v, &full[stage], 64, pc.kvh, row);
+                if (DV == 128) tma_load_3d(st + 24576, &tm_v, &full[stage], 64, pc.kvh, row);
                 if (need_rel)
-                  tma_load_2d(st + p.rel_off, &tm_rel, &full[stage], dmin & ~3,
+                  tma_load_2d(smem + L.rel + stage * L.rel_bytes, &tm_rel, &full[stage], dmin & ~3,
                               pc.b * p.Hq + pc.kvh * g);
               } else {
                 report(p.status, RELATTN_DEV_BAD_BLOCK_ID);
@@ -237,10 +319,6 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
           }
           abort = __shfl_sync(0xffffffffu, bad, 0) != 0;
           if (abort) break;
-          if (++stage == p.nstages) {
-            stage = 0;
-            phase ^= 1;
-          }
         }
       }
       f += pc.n;
@@ -249,55 +327,53 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   }
 
   // -------------------------------------------------------------- consumers
-  const int cw = warp - 1;           // keys 16*cw .. 16*cw+15 of each tile
-  const int ctid = tid - 32;         // 0..127
+  const int cwarp = warp - 1;        // 0..7
+  const int cw = cwarp & 3;          // keys 16*cw .. 16*cw+15 of a tile
+  // Group grp takes the tiles n with n % 2 == grp.  The stage count is even,
+  // so every stage belongs to one group and a group never waits on a stage
+  // more than one phase ahead of the phase it last consumed there (the
+  // parity waits below would alias otherwise).
+  const int grp = cwarp >> 2;
+  const int ctid = tid - 32;         // 0..255
   const int r0 = lane >> 2, cq = lane & 3;
   float* s_m = reinterpret_cast<float*>(smem + L.m);
   float* s_l = reinterpret_cast<float*>(smem + L.l);
   float* s_M = reinterpret_cast<float*>(smem + L.M);
   float* s_L = reinterpret_cast<float*>(smem + L.L);
-  float* obuf = reinterpret_cast<float*>(smem + L.obuf);
-  int* s_flag = reinterpret_cast<int*>(smem + L.flag);
-  int stage = 0;
-  uint32_t phase = 0;
+  float* slices = reinterpret_cast<float*>(smem + L.slices);
+  int n_base = 0;
+  int k = 0;
   bool abort = false;
 
-  for (long long f = a0; f < a1 && !abort;) {
+  for (long long f = a0; f < a1 && !abort; ++k) {
     const Piece pc = locate_piece(f, a1, s_pref, s_nt, p.B, p.Hkv);
     const DecodeSeq sq = decode_seq(s_len[pc.b], p.window, p.max_blocks);
     const int h0 = pc.kvh * g;
-
-    // Query fragments: row r = head h0 + r (rows >= g are zero).
-    uint32_t qa[8][4];
-    {
-      const __nv_bfloat16* qb =
-          p.q + (static_cast<size_t>(pc.b) * p.Hq + h0) * kDqk;
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int row = r0 + (i & 1) * 8;
-          const int col = ks * 16 + cq * 2 + (i >> 1) * 8;
-          qa[ks][i] = row < g ? __ldg(reinterpret_cast<const uint32_t*>(
-                                    qb + row * kDqk + col))
-                              : 0u;
-        }
+    const int qb = k & 1;
+    if (!mbar_wait(&qfull[qb], (k >> 1) & 1)) {
+      report(p.status, RELATTN_DEV_WAIT_TIMEOUT);
+      abort = true;
+      break;
     }
+    const uint32_t qbase = smem_u32(smem + L.qbuf + qb * kQBufBytes);
+
     float m_[2] = {kNegInf, kNegInf}, l_[2] = {0.f, 0.f};
     float o[DV / 8][4];
 #pragma unroll
     for (int i = 0; i < DV / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
 
-    for (int t = 0; t < pc.n; ++t) {
+    for (int t = (n_base + grp) & 1 ? 1 : 0; t < pc.n; t += 2) {
+      const int n = n_base + t;
+      const int stage = n % ns;
       const int tile = sq.tile_first + pc.i0 + t;
       const int key0 = tile * kTileKeys;
-      if (!mbar_wait(&full[stage], phase)) {
+      if (!mbar_wait(&full[stage], (n / ns) & 1)) {
         report(p.status, RELATTN_DEV_WAIT_TIMEOUT);
         abort = true;
         break;
       }
       if (s_valid[stage]) {
-        const uint8_t* st = smem + static_cast<size_t>(stage) * p.stage_bytes;
+        const uint8_t* st = smem + L.stages + stage * L.stage_bytes;
         const uint32_t kbase = smem_u32(st);
         float s[2][4];
 #pragma unroll
@@ -305,21 +381,25 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         {
           const int mi = lane >> 3;
           const int key = 16 * cw + (mi >> 1) * 8 + (lane & 7);
+          const int qrow = (mi & 1) * 8 + (lane & 7);
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks) {
+            uint32_t a[4];
+            const int qchunk = ks * 2 + (mi >> 1);
+            ldsm_x4(qbase + (qchunk >> 3) * 2048 + sw128(qrow, qchunk & 7), a[0], a[1], a[2],
+                    a[3]);
             const int chunk = ks * 2 + (mi & 1);
             uint32_t b0, b1, b2, b3;
-            ldsm_x4(kbase + (chunk >> 3) * 8192 + sw128(key, chunk & 7), b0, b1,
-                    b2, b3);
-            mma_16816(s[0], qa[ks], b0, b1);
-            mma_16816(s[1], qa[ks], b2, b3);
+            ldsm_x4(kbase + (chunk >> 3) * 8192 + sw128(key, chunk & 7), b0, b1, b2, b3);
+            mma_16816(s[0], a, b0, b1);
+            mma_16816(s[1], a, b2, b3);
           }
         }
         // logits in log2 units: (q.k/sqrt(d) + rel) * log2(e)
         const int dmin = sq.p - key0 - (kTileKeys - 1);
         const bool need_rel = dmin < p.rel_extent;
         const int d0 = dmin & ~3;
-        const float* relt = reinterpret_cast<const float*>(st + p.rel_off);
+        const float* relt = reinterpret_cast<const float*>(smem + L.rel + stage * L.rel_bytes);
         const bool edge = key0 < sq.lo || key0 + kTileKeys - 1 > sq.p;
         float x[2][4];
 #pragma unroll
@@ -374,8 +454,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
           for (int nd = 0; nd < DV / 8; nd += 2) {
             const int chunk = nd + (mi >> 1);
             uint32_t b0, b1, b2, b3;
-            ldsm_x4_t(vbase + (chunk >> 3) * 8192 + sw128(key, chunk & 7), b0, b1,
-                      b2, b3);
+            ldsm_x4_t(vbase + (chunk >> 3) * 8192 + sw128(key, chunk & 7), b0, b1, b2, b3);
             mma_16816(o[nd], pa, b0, b1);
             mma_16816(o[nd + 1], pa, b2, b3);
           }
@@ -383,113 +462,100 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[stage]);
-      if (++stage == p.nstages) {
-        stage = 0;
-        phase ^= 1;
-      }
     }
     if (abort) break;
+    n_base += pc.n;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&qempty[qb]);  // query rows no longer needed
 
-    // ---- merge the four consumer warps of this piece
+    // ---- merge the eight consumer warps of this piece
 #pragma unroll
     for (int rr = 0; rr < 2; ++rr) {
       l_[rr] += __shfl_xor_sync(0xffffffffu, l_[rr], 1);
       l_[rr] += __shfl_xor_sync(0xffffffffu, l_[rr], 2);
       if (cq == 0) {
-        s_m[cw * 16 + r0 + 8 * rr] = m_[rr];
-        s_l[cw * 16 + r0 + 8 * rr] = l_[rr];
+        s_m[cwarp * 16 + r0 + 8 * rr] = m_[rr];
+        s_l[cwarp * 16 + r0 + 8 * rr] = l_[rr];
       }
     }
-    named_barrier(1, 128);
-    float fct[2];
+    named_barrier(1, kConsumerThreads);
 #pragma unroll
     for (int rr = 0; rr < 2; ++rr) {
       const int row = r0 + 8 * rr;
+      if (row >= g) continue;
       float M = s_m[row];
 #pragma unroll
-      for (int w = 1; w < kConsumers; ++w) M = fmaxf(M, s_m[w * 16 + row]);
-      fct[rr] = M == kNegInf ? 0.f : ex2(m_[rr] - M);
-    }
-    // Sum the warps' rescaled outputs in a fixed order (deterministic).
-#pragma unroll 1
-    for (int w = 0; w < kConsumers; ++w) {
-      if (cw == w) {
+      for (int w = 1; w < kConsumerWarps; ++w) M = fmaxf(M, s_m[w * 16 + row]);
+      const float fct = M == kNegInf ? 0.f : ex2(m_[rr] - M);
+      float* sl = slices + (cwarp * g + row) * DV + cq * 2;
 #pragma unroll
-        for (int rr = 0; rr < 2; ++rr) {
-          const int row = r0 + 8 * rr;
-          if (row >= g) continue;
-#pragma unroll
-          for (int nd = 0; nd < DV / 8; ++nd) {
-            float* ob = &obuf[row * DV + nd * 8 + cq * 2];
-            ob[0] += o[nd][2 * rr] * fct[rr];
-            ob[1] += o[nd][2 * rr + 1] * fct[rr];
-          }
-        }
-      }
-      named_barrier(1, 128);
+      for (int nd = 0; nd < DV / 8; ++nd)
+        *reinterpret_cast<float2*>(sl + nd * 8) =
+            make_float2(o[nd][2 * rr] * fct, o[nd][2 * rr + 1] * fct);
     }
     if (ctid < g) {
       float M = s_m[ctid];
-      for (int w = 1; w < kConsumers; ++w) M = fmaxf(M, s_m[w * 16 + ctid]);
+      for (int w = 1; w < kConsumerWarps; ++w) M = fmaxf(M, s_m[w * 16 + ctid]);
       float Ls = 0.f;
       if (M != kNegInf)
-        for (int w = 0; w < kConsumers; ++w)
+        for (int w = 0; w < kConsumerWarps; ++w)
           Ls += s_l[w * 16 + ctid] * ex2(s_m[w * 16 + ctid] - M);
       s_M[ctid] = M;
       s_L[ctid] = Ls;
     }
-    named_barrier(1, 128);
+    named_barrier(1, kConsumerThreads);
 
     const bool whole = pc.i0 == 0 && pc.n == s_nt[pc.b];
     const int slot = 2 * c + (a0 < pc.seg_start ? 1 : 0);
     __nv_bfloat16* orow = p.out + (static_cast<size_t>(pc.b) * p.Hq + h0) * DV;
-    for (int idx = ctid; idx < g * DV / 2; idx += 128) {
+    for (int idx = ctid; idx < g * DV / 2; idx += kConsumerThreads) {
       const int row = idx / (DV / 2), col = 2 * (idx % (DV / 2));
-      const float v0 = obuf[row * DV + col], v1 = obuf[row * DV + col + 1];
-      obuf[row * DV + col] = 0.f;
-      obuf[row * DV + col + 1] = 0.f;
+      float v0 = 0.f, v1 = 0.f;
+#pragma unroll
+      for (int w = 0; w < kConsumerWarps; ++w) {
+        const float2 v = *reinterpret_cast<const float2*>(slices + (w * g + row) * DV + col);
+        v0 += v.x;
+        v1 += v.y;
+      }
       const float Ls = s_L[row];
       const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
       if (whole) {
         *reinterpret_cast<__nv_bfloat162*>(orow + row * DV + col) =
             __floats2bfloat162_rn(v0 * inv, v1 * inv);
       } else {
-        float* po = p.part_o + (static_cast<size_t>(slot) * g + row) * DV + col;
-        po[0] = v0 * inv;
-        po[1] = v1 * inv;
-        if (col == 0)
-          p.part_lse[slot * g + row] = Ls > 0.f ? s_M[row] + lg2(Ls) : kNegInf;
+        *reinterpret_cast<float2*>(p.part_o + (static_cast<size_t>(slot) * g + row) * DV + col) =
+            make_float2(v0 * inv, v1 * inv);
+        if (col == 0) p.part_lse[slot * g + row] = Ls > 0.f ? s_M[row] + lg2(Ls) : kNegInf;
       }
     }
     if (!whole) {
-      __threadfence();
-      named_barrier(1, 128);
+      const int c1 = cta_of(pc.seg_start, pl);
+      const int c2 = cta_of(pc.seg_end - 1, pl);
+      named_barrier(1, kConsumerThreads);
       if (ctid == 0) {
-        const int c1 = cta_of(pc.seg_start, T, G);
-        const int c2 = cta_of(pc.seg_end - 1, T, G);
-        const int old = atomicAdd(&p.counters[pc.b * p.Hkv + pc.kvh], 1);
-        *s_flag = (old == c2 - c1) ? 1 : 0;
+        const int old = atom_add_acq_rel(&p.counters[pc.b * p.Hkv + pc.kvh], 1);
+        s_misc[1] = (old == c2 - c1) ? 1 : 0;
       }
-      named_barrier(1, 128);
-      if (*s_flag) {
-        __threadfence();
-        const int c1 = cta_of(pc.seg_start, T, G);
-        const int c2 = cta_of(pc.seg_end - 1, T, G);
-        for (int idx = ctid; idx < g * DV; idx += 128) {
+      named_barrier(1, kConsumerThreads);
+      if (s_misc[1]) {
+        // last piece of this segment to finish: merge all pieces in order
+        const int slot1 = 2 * c1 + (exact_cut(c1, pl) < pc.seg_start ? 1 : 0);
+        for (int idx = ctid; idx < g * DV; idx += kConsumerThreads) {
           const int row = idx / DV, col = idx % DV;
-          float M = kNegInf;
+          float M = kNegInf, num = 0.f, den = 0.f;
+#pragma unroll 4
           for (int cc = c1; cc <= c2; ++cc) {
-            const int sl = 2 * cc + (range_start(cc, T, G) < pc.seg_start ? 1 : 0);
-            M = fmaxf(M, __ldcg(p.part_lse + sl * g + row));
+            const int sl = cc == c1 ? slot1 : 2 * cc;
+            const float lse = __ldcg(p.part_lse + sl * g + row);
+            const float ov = __ldcg(p.part_o + (static_cast<size_t>(sl) * g + row) * DV + col);
+            if (lse == kNegInf) continue;
+            const float M2 = fmaxf(M, lse);
+            const float sc = ex2(M - M2);  // 0 while M is -inf
+            const float w = ex2(lse - M2);
+            num = num * sc + w * ov;
+            den = den * sc + w;
+            M = M2;
           }
-          float num = 0.f, den = 0.f;
-          if (M != kNegInf)
-            for (int cc = c1; cc <= c2; ++cc) {
-              const int sl = 2 * cc + (range_start(cc, T, G) < pc.seg_start ? 1 : 0);
-              const float w = ex2(__ldcg(p.part_lse + sl * g + row) - M);
-              num += w * __ldcg(p.part_o + (static_cast<size_t>(sl) * g + row) * DV + col);
-              den += w;
-            }
           orow[row * DV + col] = __float2bfloat16(den > 0.f ? num / den : 0.f);
         }
         if (ctid == 0) p.counters[pc.b * p.Hkv + pc.kvh] = 0;
@@ -500,20 +566,19 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
 }
 
 // Replays the producer's walk and split without touching K/V.
-__global__ void __launch_bounds__(128)
-    decode_walk_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(128) decode_walk_kernel(const DecodeParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const DecodeSmem L(p.nstages, p.stage_bytes, p.B, 64);
-  const long long T = decode_prologue(p, smem, L, false);
-  const int G = static_cast<int>(min(static_cast<long long>(gridDim.x), T));
-  if (static_cast<int>(blockIdx.x) >= G || threadIdx.x != 0) return;
+  const DecodeSmem L(0, p.B, 1, 64);
+  const Plan pl = decode_prologue(p, smem, L, false);
+  if (static_cast<int>(blockIdx.x) >= pl.G || threadIdx.x != 0) return;
   const int* s_len = reinterpret_cast<const int*>(smem + L.seqlen);
   const int* s_nt = reinterpret_cast<const int*>(smem + L.nt);
   const int* s_pref = reinterpret_cast<const int*>(smem + L.pref);
   const int c = blockIdx.x;
-  const long long a0 = range_start(c, T, G), a1 = range_start(c + 1, T, G);
+  const long long a0 = range_cut(c, pl, s_pref, s_nt, p.B, p.Hkv);
+  const long long a1 = range_cut(c + 1, pl, s_pref, s_nt, p.B, p.Hkv);
   for (long long f = a0; f < a1;) {
     const Piece pc = locate_piece(f, a1, s_pref, s_nt, p.B, p.Hkv);
     const DecodeSeq sq = decode_seq(s_len[pc.b], p.window, p.max_blocks);
@@ -538,34 +603,34 @@ __global__ void __launch_bounds__(128)
 
 }  // namespace
 
-int decode_smem_bytes(int nstages, int stage_bytes, int B, int dv) {
-  return DecodeSmem(nstages, stage_bytes, B, dv).total + 1024;
+int decode_smem_bytes(int nstages, int B, int g, int dv) {
+  return DecodeSmem(nstages, B, g, dv).total + 1024;
 }
 
 cudaError_t launch_decode(const DecodeLaunch& L, cudaStream_t stream) {
-  const int smem = decode_smem_bytes(L.p.nstages, L.p.stage_bytes, L.p.B, L.p.dv);
+  const DecodeParams& p = L.p;
+  const int smem = decode_smem_bytes(p.nstages, p.B, p.g, p.dv);
   cudaError_t e;
-  if (L.p.dv == 128) {
-    e = cudaFuncSetAttribute(decode_kernel<128>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (p.dv == 128) {
+    e = cudaFuncSetAttribute(decode_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem);
     if (e != cudaSuccess) return e;
-    decode_kernel<128><<<L.grid, kDecodeThreads, smem, stream>>>(L.tm_k, L.tm_v,
-                                                                 L.tm_rel, L.p);
+    decode_kernel<128><<<L.grid, kDecodeThreads, smem, stream>>>(L.tm_q, L.tm_k, L.tm_v,
+                                                                 L.tm_rel, p);
   } else {
-    e = cudaFuncSetAttribute(decode_kernel<64>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    e = cudaFuncSetAttribute(decode_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem);
     if (e != cudaSuccess) return e;
-    decode_kernel<64><<<L.grid, kDecodeThreads, smem, stream>>>(L.tm_k, L.tm_v,
-                                                                L.tm_rel, L.p);
+    decode_kernel<64><<<L.grid, kDecodeThreads, smem, stream>>>(L.tm_q, L.tm_k, L.tm_v,
+                                                                L.tm_rel, p);
   }
   return cudaGetLastError();
 }
 
-cudaError_t launch_decode_walk(const DecodeParams& p, int grid,
-                               cudaStream_t stream) {
-  const int smem = DecodeSmem(p.nstages, p.stage_bytes, p.B, 64).total + 1024;
-  cudaError_t e = cudaFuncSetAttribute(
-      decode_walk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+cudaError_t launch_decode_walk(const DecodeParams& p, int grid, cudaStream_t stream) {
+  const int smem = decode_smem_bytes(0, p.B, 1, 64);
+  cudaError_t e = cudaFuncSetAttribute(decode_walk_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   decode_walk_kernel<<<grid, 128, smem, stream>>>(p);
   return cudaGetLastError();

@@ -26,12 +26,12 @@ struct DecodeParams {
   int32_t* dbg_count;
   int dbg_max;
   int B, Hq, Hkv, g, dv, max_blocks, num_blocks, window, rel_extent;
-  int nstages, stage_bytes, rel_off;
+  int nstages;  // even: see the consumer groups of decode_kernel
   float scale_log2;  // log2(e) / sqrt(d_qk)
 };
 
 struct DecodeLaunch {
-  CUtensorMap tm_k, tm_v, tm_rel;
+  CUtensorMap tm_q, tm_k, tm_v, tm_rel;
   DecodeParams p;
   int grid;
 };
@@ -60,7 +60,7 @@ struct PrefillLaunch {
   PrefillParams p;
 };
 
-int decode_smem_bytes(int nstages, int stage_bytes, int B, int dv);
+int decode_smem_bytes(int nstages, int B, int g, int dv);
 cudaError_t launch_decode(const DecodeLaunch& L, cudaStream_t stream);
 cudaError_t launch_decode_walk(const DecodeParams& p, int grid, cudaStream_t stream);
 
