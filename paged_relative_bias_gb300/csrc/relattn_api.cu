@@ -318,7 +318,23 @@ static int prepare_prefill(const void* q, const void* k, const void* v, const fl
   p.max_q_len = dims->max_q_len;
   p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(128.0));
   if (walk) return RELATTN_OK;
+  DeviceInfo di;
+  if (!device_info(&di)) return RELATTN_ERR_CUDA;
+  if (prefill_smem_bytes(p.B, p.dv) > di.smem_optin) return RELATTN_ERR_UNSUPPORTED;
+  const long long qtiles = static_cast<long long>(p.B) * ((p.max_q_len + 127) / 128) * p.Hq;
+  const long long want = dims->num_ctas > 0 ? dims->num_ctas : di.sms;
+  L->grid = static_cast<int>(qtiles < want ? (qtiles > 0 ? qtiles : 1) : want);
   if (!cache_maps(cache, &L->tm_k, &L->tm_v)) return RELATTN_ERR_CUDA;
+  // rel [T][Hq][E] fp32: boxes of 32 tokens x 100 distances of one head
+  const cuuint64_t rd[3] = {static_cast<cuuint64_t>(rel_extent),
+                            static_cast<cuuint64_t>(dims->num_q_heads),
+                            static_cast<cuuint64_t>(dims->num_tokens)};
+  const cuuint64_t rs[2] = {static_cast<cuuint64_t>(rel_extent) * 4,
+                            static_cast<cuuint64_t>(rel_extent) * 4 * dims->num_q_heads};
+  const cuuint32_t rb[3] = {100, 1, 32};
+  if (!make_map(&L->tm_rel, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(rel), rd, rs,
+                rb, CU_TENSOR_MAP_SWIZZLE_NONE))
+    return RELATTN_ERR_CUDA;
   return RELATTN_OK;
 }
 
@@ -334,7 +350,7 @@ int relattn_prefill(const void* q, const void* k, const void* v, const float* re
   if (dims->max_q_len == 0 || dims->num_tokens == 0) return RELATTN_OK;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = launch_cache_write(L.p, s);
-  if (e == cudaSuccess) e = launch_prefill(L, s);
+  if (e == cudaSuccess) e = launch_prefill(L, L.grid, s);
   return to_status(e);
 }
 

@@ -56,8 +56,9 @@ struct PrefillParams {
 };
 
 struct PrefillLaunch {
-  CUtensorMap tm_k, tm_v;
+  CUtensorMap tm_k, tm_v, tm_rel;
   PrefillParams p;
+  int grid;
 };
 
 int decode_smem_bytes(int nstages, int B, int g, int dv);
@@ -65,7 +66,8 @@ cudaError_t launch_decode(const DecodeLaunch& L, cudaStream_t stream);
 cudaError_t launch_decode_walk(const DecodeParams& p, int grid, cudaStream_t stream);
 
 cudaError_t launch_cache_write(const PrefillParams& p, cudaStream_t stream);
-cudaError_t launch_prefill(const PrefillLaunch& L, cudaStream_t stream);
+int prefill_smem_bytes(int B, int dv);
+cudaError_t launch_prefill(const PrefillLaunch& L, int grid, cudaStream_t stream);
 cudaError_t launch_prefill_walk(const PrefillParams& p, cudaStream_t stream);
 
 }  // namespace relattn

@@ -1,46 +1,82 @@
-// Chunked prefill with a cached prefix for relative-bias GQA attention.
+// Chunked prefill with a cached prefix for relative-bias GQA attention
+// (sm_103a, tcgen05 / TMEM).
 //
 // Two kernels on the caller's stream:
-//  * cache_write: scatters each new token's key and value into the paged
+//  * cache_write scatters each new token's key and value into the paged
 //    cache at position ctx_lens[b] + t ("Inkling-Small on Gaudi 2", section
 //    "Attention with a relative bias": later chunks and prefix-cache hits
 //    prepend the cached context);
-//  * prefill: per (64-row query tile, query head), walks the key tiles of the
-//    window [max(0, P_first - W + 1), P_last] through the block table, loads
-//    K/V tiles with TMA, computes S = QK^T with mma.sync, adds the sheared
-//    relative term rel[row, h, P_row - j] in registers (no [Lq, KV] mask is
-//    ever formed), applies the causal and window masks and an online
-//    softmax, and accumulates O = PV.
+//  * prefill_kernel: persistent CTAs take (128-row query tile, query head)
+//    work items.  Per item the window-aware walk yields the 64-key tiles of
+//    [max(0, P_first - W + 1), P_last]; for each tile
+//      S = Q K^T        tcgen05.mma, Q in TMEM, K from TMA (128B swizzle),
+//                       S into one of two TMEM buffers
+//      bias, masks      one softmax thread per query row adds
+//                       rel[row, h, P_row - j] read from a shared-memory box
+//                       (the sheared bias: each row reads its own contiguous
+//                       distance range; no [Lq, KV] mask is formed), then the
+//                       causal and window masks
+//      online softmax   the running max only moves when it grows by more
+//                       than 2^8, so O is rescaled rarely
+//      O += P V         P written back to TMEM as bf16 and used as the A
+//                       operand; V from TMA (MN-major, 128B swizzle)
+//    ("vLLM TML Inkling Support", section "Low-Latency Collectives and
+//    Kernels": the FA4 relative-attention kernel with a sheared bias; "Inkling
+//    2 Small on vLLM", section "vLLM integration and optimisation": prefill
+//    keeps the sheared-bias path).
+//
+// Warp roles: 0 = K/V TMA producer, 1 = MMA issuer and TMEM owner, 2-5 =
+// softmax (TMEM lane quarters 2, 3, 0, 1), 6 = rel TMA producer.
 #include "relattn_common.cuh"
 #include "relattn_internal.h"
+#include "relattn_tcgen05.cuh"
 
 namespace relattn {
 
 namespace {
 
-constexpr int kPrefillThreads = 128;  // 4 warps x 16 query rows
-constexpr int kQTile = 64;
-constexpr int kPrefillStages = 3;
+constexpr int kQRows = 128;
+constexpr int kCwTile = 64;                 // cache_write tokens per CTA
+constexpr int kPfWarps = 7;
+constexpr int kPfThreads = 32 * kPfWarps;
+constexpr int kKStages = 2, kVStages = 2, kRelStages = 3;
+constexpr int kKStageBytes = kTileKeys * kDqk * 2;  // 16 KB
+constexpr int kRelBoxRows = 32, kRelBoxCols = 100;
+constexpr int kRelBoxBytes = kRelBoxRows * kRelBoxCols * 4;  // 12800
+constexpr int kRelStageBytes = 4 * kRelBoxBytes;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmQ = 0, kTmS = 64, kTmO = 192;  // S buffer s at kTmS + 64 s
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kNegInf = -__builtin_huge_valf();
+constexpr float kRescaleLog2 = 8.f;  // move the running max only past 2^8
+constexpr uint32_t kIdescS = umma_idesc_bf16(128, kTileKeys, 0);
+
+enum Bar { kKFull = 0, kKEmpty = 2, kVFull = 4, kVEmpty = 6, kRFull = 8, kREmpty = 11,
+           kSFull = 14, kPFull = 16, kOFull = 18, kQFull = 19, kDrain = 20, kNumBars = 21 };
 
 __device__ __forceinline__ bool seq_ok(int ctx, int n, int max_blocks) {
   return ctx >= 0 && n >= 0 &&
          static_cast<long long>(ctx) + n <= static_cast<long long>(max_blocks) * kBlockSize;
 }
 
+// Rows [cu0, cu1) are a valid chunk of the packed [T] token rows.
+__device__ __forceinline__ bool rows_ok(int cu0, int cu1, int T) {
+  return cu0 >= 0 && cu1 >= cu0 && cu1 <= T;
+}
+
 __global__ void __launch_bounds__(256) cache_write_kernel(const PrefillParams p) {
   const int b = blockIdx.y;
   const int r0 = p.cu_seqlens[b];
-  const int n = p.cu_seqlens[b + 1] - r0;
+  const int r1 = p.cu_seqlens[b + 1];
+  const int n = r1 - r0;
   const int ctx = p.ctx_lens[b];
-  const int t0 = blockIdx.x * kQTile;
-  if (!seq_ok(ctx, n, p.max_blocks)) {
+  const int t0 = blockIdx.x * kCwTile;
+  if (!rows_ok(r0, r1, p.T) || !seq_ok(ctx, n, p.max_blocks)) {
     if (blockIdx.x == 0 && threadIdx.x == 0) report(p.status, RELATTN_DEV_BAD_LENGTH);
     return;
   }
   if (t0 >= n) return;
-  const int nt = min(kQTile, n - t0);
+  const int nt = min(kCwTile, n - t0);
   const int kch = kDqk / 8, vch = p.dv / 8;
   const int per_tok = p.Hkv * (kch + vch);
   const int* trow = p.block_table + static_cast<size_t>(b) * p.max_blocks;
@@ -58,233 +94,424 @@ __global__ void __launch_bounds__(256) cache_write_kernel(const PrefillParams p)
     const size_t slot = static_cast<size_t>(phys) * kBlockSize + pos % kBlockSize;
     const size_t row = static_cast<size_t>(r0 + t0 + tt);
     if (ch < kch) {
-      const uint4 val = __ldg(reinterpret_cast<const uint4*>(
-          p.k + (row * p.Hkv + hh) * kDqk) + ch);
+      const uint4 val = __ldg(reinterpret_cast<const uint4*>(p.k + (row * p.Hkv + hh) * kDqk) + ch);
       reinterpret_cast<uint4*>(p.k_cache + (slot * p.Hkv + hh) * kDqk)[ch] = val;
     } else {
       ch -= kch;
-      const uint4 val = __ldg(reinterpret_cast<const uint4*>(
-          p.v + (row * p.Hkv + hh) * p.dv) + ch);
+      const uint4 val = __ldg(reinterpret_cast<const uint4*>(p.v + (row * p.Hkv + hh) * p.dv) + ch);
       reinterpret_cast<uint4*>(p.v_cache + (slot * p.Hkv + hh) * p.dv)[ch] = val;
     }
   }
 }
 
+// Shared-memory carve-up (byte offsets from a 1024-aligned base).
+struct PrefillSmem {
+  int k, v, vstage, rel, bars, misc, cu0, nrows, ctx, qpref, total;
+  __host__ __device__ PrefillSmem(int B, int dv) {
+    vstage = kTileKeys * dv * 2;
+    k = 0;
+    v = k + kKStages * kKStageBytes;
+    rel = v + kVStages * vstage;
+    bars = rel + kRelStages * kRelStageBytes;
+    misc = bars + kNumBars * 8;
+    cu0 = misc + 16;
+    nrows = cu0 + B * 4;
+    ctx = nrows + B * 4;
+    qpref = ctx + B * 4;
+    total = qpref + (B + 1) * 4;
+  }
+};
+
+struct PItem {
+  int b, h, kvh, r0, rows, P0, tf, ntiles;
+};
+
+__device__ __forceinline__ void prefill_item(int idx, const PrefillParams& p, const int* s_cu0,
+                                             const int* s_n, const int* s_ctx,
+                                             const int* s_qpref, PItem& it) {
+  const int qtg = idx / p.Hq;
+  it.h = idx - qtg * p.Hq;
+  it.kvh = it.h / p.g;
+  int lo = 0, hi = p.B - 1;
+  while (lo < hi) {  // largest b with s_qpref[b] <= qtg
+    const int mid = (lo + hi + 1) >> 1;
+    if (s_qpref[mid] <= qtg)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  it.b = lo;
+  const int qt = qtg - s_qpref[lo];
+  it.r0 = s_cu0[lo] + qt * kQRows;
+  it.rows = min(kQRows, s_n[lo] - qt * kQRows);
+  it.P0 = s_ctx[lo] + qt * kQRows;
+  it.tf = window_lo(it.P0, p.window) / kTileKeys;
+  it.ntiles = (it.P0 + it.rows - 1) / kTileKeys - it.tf + 1;
+}
+
+// Per-CTA prologue: per-sequence rows, context and query-tile prefix.
+// Returns the number of (query tile, head) work items.
+__device__ int prefill_prologue(const PrefillParams& p, uint8_t* smem, const PrefillSmem& L,
+                                bool zero_bad) {
+  int* s_cu0 = reinterpret_cast<int*>(smem + L.cu0);
+  int* s_n = reinterpret_cast<int*>(smem + L.nrows);
+  int* s_ctx = reinterpret_cast<int*>(smem + L.ctx);
+  int* s_qpref = reinterpret_cast<int*>(smem + L.qpref);
+  const int tid = threadIdx.x;
+  for (int b = tid; b < p.B; b += blockDim.x) {
+    const int c0 = p.cu_seqlens[b], c1 = p.cu_seqlens[b + 1], ctx = p.ctx_lens[b];
+    const bool ok = rows_ok(c0, c1, p.T) && seq_ok(ctx, c1 - c0, p.max_blocks);
+    s_cu0[b] = c0;
+    s_n[b] = ok ? c1 - c0 : 0;
+    s_ctx[b] = ctx;
+    // query tiles of this sequence, kept in s_qpref until the scan
+    s_qpref[b] = ok ? (c1 - c0 + kQRows - 1) / kQRows : 0;
+    if (!ok && zero_bad && blockIdx.x == 0 && rows_ok(c0, c1, p.T)) {
+      for (int r = c0; r < c1; ++r)  // a skipped sequence's rows are zero
+        for (int i = 0; i < p.Hq * p.dv; ++i)
+          p.out[static_cast<size_t>(r) * p.Hq * p.dv + i] = __float2bfloat16(0.f);
+    }
+  }
+  __syncthreads();
+  if (tid < 32) {
+    const int lane = tid;
+    const int chunk = (p.B + 31) / 32;
+    const int beg = lane * chunk, end = min(p.B, beg + chunk);
+    int sum = 0;
+    for (int i = beg; i < end; ++i) sum += s_qpref[i];
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    int run = incl - sum;
+    for (int i = beg; i < end; ++i) {
+      const int cnt = s_qpref[i];
+      s_qpref[i] = run;
+      run += cnt;
+    }
+    if (lane == 31) s_qpref[p.B] = incl;
+  }
+  __syncthreads();
+  return s_qpref[p.B] * p.Hq;
+}
+
 template <int DV>
-__global__ void __launch_bounds__(kPrefillThreads)
+__global__ void __launch_bounds__(kPfThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v,
-                   const PrefillParams p) {
+                   const __grid_constant__ CUtensorMap tm_rel, const PrefillParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  constexpr int kStageBytes = 16384 + kTileKeys * DV * 2;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kPrefillStages * kStageBytes);
-  int* s_valid = reinterpret_cast<int*>(full + kPrefillStages);
-
-  const int qt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const PrefillSmem L(p.B, DV);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + L.misc);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + L.misc + 4);
+  const int* s_cu0 = reinterpret_cast<const int*>(smem + L.cu0);
+  const int* s_n = reinterpret_cast<const int*>(smem + L.nrows);
+  const int* s_ctx = reinterpret_cast<const int*>(smem + L.ctx);
+  const int* s_qpref = reinterpret_cast<const int*>(smem + L.qpref);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int r_begin = p.cu_seqlens[b];
-  const int n = p.cu_seqlens[b + 1] - r_begin;
-  const int ctx = p.ctx_lens[b];
-  const int t0 = qt * kQTile;
-  if (t0 >= n) return;
-  const int rows = min(kQTile, n - t0);
-  const int r0 = lane >> 2, cq = lane & 3;
-  const int rA = warp * 16 + r0, rB = rA + 8;  // tile-local rows of this thread
-  __nv_bfloat16* out_base = p.out + (static_cast<size_t>(r_begin + t0) * p.Hq + h) * DV;
-  if (!seq_ok(ctx, n, p.max_blocks)) {
-    for (int i = tid; i < rows * DV; i += blockDim.x)
-      out_base[static_cast<size_t>(i / DV) * p.Hq * DV + i % DV] = __float2bfloat16(0.f);
-    return;  // reported by cache_write
-  }
-  const int kvh = h / p.g;
-  const int P0 = ctx + t0;
-  const int P1 = P0 + rows - 1;
-  const int tf = window_lo(P0, p.window) / kTileKeys;
-  const int ntiles = P1 / kTileKeys - tf + 1;
-  const int* trow = p.block_table + static_cast<size_t>(b) * p.max_blocks;
 
   if (tid == 0) {
-    for (int s = 0; s < kPrefillStages; ++s) mbar_init(&full[s], 1);
+    for (int s = 0; s < kKStages; ++s) {
+      mbar_init(&bars[kKFull + s], 1);
+      mbar_init(&bars[kKEmpty + s], 1);
+      mbar_init(&bars[kVFull + s], 1);
+      mbar_init(&bars[kVEmpty + s], 1);
+      mbar_init(&bars[kSFull + s], 1);
+      mbar_init(&bars[kPFull + s], 4);
+    }
+    for (int s = 0; s < kRelStages; ++s) {
+      mbar_init(&bars[kRFull + s], 1);
+      mbar_init(&bars[kREmpty + s], 4);
+    }
+    mbar_init(&bars[kOFull], 1);
+    mbar_init(&bars[kQFull], 4);
+    mbar_init(&bars[kDrain], 1);
     fence_mbar_init();
+    *s_abort = 0;
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+    tma_prefetch_desc(&tm_rel);
   }
-  __syncthreads();
+  // K/V stages start as zeros: a tile whose block id is invalid is never
+  // loaded, and its P is zero, so its operands must at least be finite.
+  for (int i = tid; i < (L.rel - L.k) / 16; i += blockDim.x)
+    reinterpret_cast<uint4*>(smem + L.k)[i] = make_uint4(0, 0, 0, 0);
+  fence_proxy_async_smem();
+  if (warp == 1) {
+    tmem_alloc(s_tmem, kTmemCols);
+    tc_fence_before();
+  }
+  const int total = prefill_prologue(p, smem, L, true);  // contains __syncthreads
+  tc_fence_after();
+  const uint32_t tbase = *s_tmem;
+  const float scale_log2 = p.scale_log2;
 
-  auto issue = [&](int stage, int tile) {
-    const int id = __ldg(trow + (tile >> 1));
-    const bool ok = id >= 0 && id < p.num_blocks;
-    s_valid[stage] = ok ? 1 : 0;
-    if (!ok) {
-      report(p.status, RELATTN_DEV_BAD_BLOCK_ID);
-      mbar_arrive(&full[stage]);
-      return;
-    }
-    uint8_t* st = smem + stage * kStageBytes;
-    const int row = id * kBlockSize + (tile & 1) * kTileKeys;
-    mbar_arrive_expect_tx(&full[stage], kStageBytes);
-    tma_load_3d(st, &tm_k, &full[stage], 0, kvh, row);
-    tma_load_3d(st + 8192, &tm_k, &full[stage], 64, kvh, row);
-    tma_load_3d(st + 16384, &tm_v, &full[stage], 0, kvh, row);
-    if (DV == 128) tma_load_3d(st + 24576, &tm_v, &full[stage], 64, kvh, row);
-  };
-  if (tid == 0)
-    for (int s = 0; s < kPrefillStages && s < ntiles; ++s) issue(s, tf + s);
-
-  // query fragments (rows beyond the chunk are zero)
-  uint32_t qa[8][4];
-#pragma unroll
-  for (int ks = 0; ks < 8; ++ks)
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int row = (i & 1) ? rB : rA;
-      const int col = ks * 16 + cq * 2 + (i >> 1) * 8;
-      qa[ks][i] = row < rows
-                      ? __ldg(reinterpret_cast<const uint32_t*>(
-                            p.q + (static_cast<size_t>(r_begin + t0 + row) * p.Hq + h) * kDqk + col))
-                      : 0u;
-    }
-  const int PA = P0 + rA, PB = P0 + rB;
-  const int loA = window_lo(PA, p.window), loB = window_lo(PB, p.window);
-  const float* relA = p.rel + (static_cast<size_t>(r_begin + t0 + rA) * p.Hq + h) * p.rel_extent;
-  const float* relB = p.rel + (static_cast<size_t>(r_begin + t0 + rB) * p.Hq + h) * p.rel_extent;
-  const bool okA = rA < rows, okB = rB < rows;
-
-  float m_[2] = {kNegInf, kNegInf}, l_[2] = {0.f, 0.f};
-  float o[DV / 8][4];
-#pragma unroll
-  for (int i = 0; i < DV / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-
-  bool abort = false;
-  for (int k = 0; k < ntiles; ++k) {
-    const int stage = k % kPrefillStages;
-    const uint32_t parity = (k / kPrefillStages) & 1;
-    const int key0 = (tf + k) * kTileKeys;
-    // relative term and masks for this thread's 32 elements (issued before
-    // the wait so the loads overlap it)
-    float x[8][4];
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const bool second = i >= 2;
-        const int P = second ? PB : PA;
-        const int lo = second ? loB : loA;
-        const int key = key0 + nt * 8 + cq * 2 + (i & 1);
-        const int d = P - key;
-        float bias = kNegInf;
-        if ((second ? okB : okA) && key >= lo && d >= 0)
-          bias = d < p.rel_extent ? __ldg((second ? relB : relA) + d) : 0.f;
-        x[nt][i] = bias;
-      }
-    if (!mbar_wait(&full[stage], parity)) {
-      report(p.status, RELATTN_DEV_WAIT_TIMEOUT);
-      abort = true;
-    }
-    if (!abort && s_valid[stage]) {
-      const uint32_t kbase = smem_u32(smem + stage * kStageBytes);
-      float s[8][4];
-#pragma unroll
-      for (int nt = 0; nt < 8; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
-      {
-        const int mi = lane >> 3;
-#pragma unroll
-        for (int np = 0; np < 4; ++np) {
-          const int key = np * 16 + (mi >> 1) * 8 + (lane & 7);
-#pragma unroll
-          for (int ks = 0; ks < 8; ++ks) {
-            const int chunk = ks * 2 + (mi & 1);
-            uint32_t b0, b1, b2, b3;
-            ldsm_x4(kbase + (chunk >> 3) * 8192 + sw128(key, chunk & 7), b0, b1, b2, b3);
-            mma_16816(s[2 * np], qa[ks], b0, b1);
-            mma_16816(s[2 * np + 1], qa[ks], b2, b3);
-          }
+  if (warp == 0 && lane == 0) {
+    // ---------------------------------------------------- K/V TMA producer
+    int n = 0;
+    for (int idx = blockIdx.x; idx < total && !*s_abort; idx += gridDim.x) {
+      PItem it;
+      prefill_item(idx, p, s_cu0, s_n, s_ctx, s_qpref, it);
+      const int* trow = p.block_table + static_cast<size_t>(it.b) * p.max_blocks;
+      for (int k = 0; k < it.ntiles; ++k, ++n) {
+        const int tile = it.tf + k;
+        const int id = __ldg(trow + (tile >> 1));
+        const bool ok = id >= 0 && id < p.num_blocks;
+        const int row = id * kBlockSize + (tile & 1) * kTileKeys;
+        const int s = n & 1;
+        const uint32_t par = ((n >> 1) & 1) ^ 1;
+        if (!mbar_wait(&bars[kKEmpty + s], par)) { *s_abort = 1; break; }
+        if (ok) {
+          uint8_t* kd = smem + L.k + s * kKStageBytes;
+          mbar_arrive_expect_tx(&bars[kKFull + s], kKStageBytes);
+          tma_load_3d(kd, &tm_k, &bars[kKFull + s], 0, it.kvh, row);
+          tma_load_3d(kd + 8192, &tm_k, &bars[kKFull + s], 64, it.kvh, row);
+        } else {
+          report(p.status, RELATTN_DEV_BAD_BLOCK_ID);
+          mbar_arrive(&bars[kKFull + s]);
+        }
+        if (!mbar_wait(&bars[kVEmpty + s], par)) { *s_abort = 1; break; }
+        if (ok) {
+          uint8_t* vd = smem + L.v + s * L.vstage;
+          mbar_arrive_expect_tx(&bars[kVFull + s], L.vstage);
+          tma_load_3d(vd, &tm_v, &bars[kVFull + s], 0, it.kvh, row);
+          if (DV == 128) tma_load_3d(vd + 8192, &tm_v, &bars[kVFull + s], 64, it.kvh, row);
+        } else {
+          mbar_arrive(&bars[kVFull + s]);
         }
       }
+    }
+  } else if (warp == 6 && lane == 0) {
+    // ---------------------------------------------------- rel TMA producer
+    int n = 0;
+    for (int idx = blockIdx.x; idx < total && !*s_abort; idx += gridDim.x) {
+      PItem it;
+      prefill_item(idx, p, s_cu0, s_n, s_ctx, s_qpref, it);
+      for (int k = 0; k < it.ntiles; ++k, ++n) {
+        const int j0 = (it.tf + k) * kTileKeys;
+        const int rs = n % kRelStages;
+        if (!mbar_wait(&bars[kREmpty + rs], ((n / kRelStages) & 1) ^ 1)) { *s_abort = 1; break; }
+        if (it.P0 - j0 - (kTileKeys - 1) < p.rel_extent) {
+          uint8_t* rd = smem + L.rel + rs * kRelStageBytes;
+          mbar_arrive_expect_tx(&bars[kRFull + rs], kRelStageBytes);
+          for (int q = 0; q < 4; ++q) {
+            const int x = (it.P0 + 32 * q - j0 - (kTileKeys - 1)) & ~3;
+            tma_load_3d(rd + q * kRelBoxBytes, &tm_rel, &bars[kRFull + rs], x, it.h,
+                        it.r0 + 32 * q);
+          }
+        } else {
+          mbar_arrive(&bars[kRFull + rs]);  // every distance is past rel_extent
+        }
+      }
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ---------------------------------------------------------- MMA issuer
+    const uint32_t idesc_pv = umma_idesc_bf16(128, DV, 1);
+    int n = 0, items = 0;
+    auto issue_pv = [&](int m, bool acc) -> bool {
+      const int sp = m & 1;
+      const uint32_t par = (m >> 1) & 1;
+      if (!mbar_wait(&bars[kPFull + sp], par) || !mbar_wait(&bars[kVFull + sp], par)) return false;
+      tc_fence_after();
+      const uint32_t vb = smem_u32(smem + L.v + sp * L.vstage);
 #pragma unroll
-      for (int nt = 0; nt < 8; ++nt)
+      for (int kk = 0; kk < kTileKeys / 16; ++kk)
+        umma_tmem_a(tbase + kTmO, tbase + kTmS + 64 * sp + 8 * kk,
+                    umma_desc_sw128(vb + kk * 2048, kTileKeys * 128, 1024), idesc_pv,
+                    (acc || kk > 0) ? 1 : 0);
+      umma_commit(&bars[kOFull]);
+      umma_commit(&bars[kVEmpty + sp]);
+      return true;
+    };
+    for (int idx = blockIdx.x; idx < total && !*s_abort; idx += gridDim.x, ++items) {
+      PItem it;
+      prefill_item(idx, p, s_cu0, s_n, s_ctx, s_qpref, it);
+      if (!mbar_wait(&bars[kQFull], items & 1)) { *s_abort = 1; break; }
+      tc_fence_after();
+      bool ok = true;
+      for (int k = 0; k < it.ntiles && ok; ++k, ++n) {
+        const int s = n & 1;
+        if (!mbar_wait(&bars[kKFull + s], (n >> 1) & 1)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t kb = smem_u32(smem + L.k + s * kKStageBytes);
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-          x[nt][i] = x[nt][i] == kNegInf ? kNegInf
-                                         : fmaf(s[nt][i], p.scale_log2, x[nt][i] * kLog2e);
+        for (int ks = 0; ks < kDqk / 16; ++ks)
+          umma_tmem_a(tbase + kTmS + 64 * s, tbase + kTmQ + 8 * ks,
+                      umma_desc_sw128(kb + (ks >> 2) * 8192 + (ks & 3) * 32, 0, 1024), kIdescS,
+                      ks > 0 ? 1 : 0);
+        umma_commit(&bars[kSFull + s]);
+        umma_commit(&bars[kKEmpty + s]);
+        if (k > 0) ok = issue_pv(n - 1, k > 1);
+      }
+      if (ok) ok = issue_pv(n - 1, it.ntiles > 1);
+      if (!ok) { *s_abort = 1; break; }
+    }
+    // all MMAs retired before TMEM is released
+    umma_commit(&bars[kDrain]);
+    if (!mbar_wait(&bars[kDrain], 0)) report(p.status, RELATTN_DEV_WAIT_TIMEOUT);
+  } else if (warp >= 2 && warp <= 5) {
+    // ------------------------------------------------------------ softmax
+    const int q4 = warp & 3;  // TMEM lane quarter this warp may access
+    const int r = 32 * q4 + lane;
+    const uint32_t tl = tbase + (static_cast<uint32_t>(32 * q4) << 16);
+    int n = 0, pv = 0;
+    for (int idx = blockIdx.x; idx < total && !*s_abort; idx += gridDim.x) {
+      PItem it;
+      prefill_item(idx, p, s_cu0, s_n, s_ctx, s_qpref, it);
+      const bool row_ok = r < it.rows;
+      const int token = it.r0 + r;
+      const int P = it.P0 + r;
+      const int lo = window_lo(P, p.window);
+      const int* trow = p.block_table + static_cast<size_t>(it.b) * p.max_blocks;
+      // query row -> TMEM (the A operand of S = Q K^T)
+      {
+        uint32_t qr[64];
+        const uint4* src = reinterpret_cast<const uint4*>(
+            p.q + (static_cast<size_t>(token) * p.Hq + it.h) * kDqk);
 #pragma unroll
-      for (int rr = 0; rr < 2; ++rr) {
+        for (int i = 0; i < 16; ++i) {
+          const uint4 v = row_ok ? __ldg(src + i) : make_uint4(0, 0, 0, 0);
+          qr[4 * i] = v.x;
+          qr[4 * i + 1] = v.y;
+          qr[4 * i + 2] = v.z;
+          qr[4 * i + 3] = v.w;
+        }
+        tmem_st32(tl + kTmQ, qr);
+        tmem_st32(tl + kTmQ + 32, qr + 32);
+        tmem_wait_st();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[kQFull]);
+
+      float m_used = kNegInf, l = 0.f;
+      bool ok = true;
+      for (int k = 0; k < it.ntiles; ++k, ++n) {
+        const int s = n & 1;
+        const int j0 = (it.tf + k) * kTileKeys;
+        const int id = __ldg(trow + ((it.tf + k) >> 1));
+        const bool tile_ok = id >= 0 && id < p.num_blocks;
+        if (!mbar_wait(&bars[kSFull + s], (n >> 1) & 1)) { ok = false; break; }
+        tc_fence_after();
+        uint32_t sr[64];
+        tmem_ld32(tl + kTmS + 64 * s, sr);
+        tmem_ld32(tl + kTmS + 64 * s + 32, sr + 32);
+        tmem_wait_ld();
+        const int rs = n % kRelStages;
+        if (!mbar_wait(&bars[kRFull + rs], (n / kRelStages) & 1)) { ok = false; break; }
+        const bool need_rel = it.P0 - j0 - (kTileKeys - 1) < p.rel_extent;
+        const float* rrow = reinterpret_cast<const float*>(
+                                smem + L.rel + rs * kRelStageBytes + q4 * kRelBoxBytes) +
+                            lane * kRelBoxCols;
+        // box column of key j0 + c is (P - j0 - x_q) - c, x_q its first distance
+        const int xq = (it.P0 + 32 * q4 - j0 - (kTileKeys - 1)) & ~3;
+        const int cbase = P - j0 - xq;
+        const bool full = tile_ok && row_ok && j0 >= lo && j0 + kTileKeys - 1 <= P;
+        const bool any = tile_ok && row_ok && j0 + kTileKeys - 1 >= lo && j0 <= P;
+        float x[64];
         float mx = kNegInf;
 #pragma unroll
-        for (int nt = 0; nt < 8; ++nt) mx = fmaxf(mx, fmaxf(x[nt][2 * rr], x[nt][2 * rr + 1]));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-        const float m_new = fmaxf(m_[rr], mx);
-        const float m_use = m_new == kNegInf ? 0.f : m_new;
-        const float alpha = ex2(m_[rr] - m_use);
-        m_[rr] = m_new;
+        for (int c = 0; c < 64; ++c) {
+          const float bias = need_rel ? rrow[cbase - c] : 0.f;
+          float v = fmaf(__uint_as_float(sr[c]), scale_log2, bias * kLog2e);
+          if (!full) {
+            const int j = j0 + c;
+            if (!(any && j >= lo && j <= P)) v = kNegInf;
+          }
+          x[c] = v;
+          mx = fmaxf(mx, v);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[kREmpty + rs]);
+        if (k > 0) {  // the previous tile's O += P V has landed
+          if (!mbar_wait(&bars[kOFull], pv & 1)) { ok = false; break; }
+          ++pv;
+          tc_fence_after();
+        }
+        const bool grow = mx > m_used + kRescaleLog2;
+        const float m_new = grow ? mx : m_used;
+        const float alpha = (grow && m_used != kNegInf) ? ex2(m_used - m_new) : 1.f;
+        if (k > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll 1
+          for (int c0 = 0; c0 < DV; c0 += 32) {
+            uint32_t o[32];
+            tmem_ld32(tl + kTmO + c0, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            tmem_st32(tl + kTmO + c0, o);
+          }
+          tmem_wait_st();
+        }
+        l *= alpha;
+        m_used = m_new;
+        const float m_use = m_used == kNegInf ? 0.f : m_used;
+        uint32_t pk[32];
         float sum = 0.f;
 #pragma unroll
-        for (int nt = 0; nt < 8; ++nt)
+        for (int i = 0; i < 32; ++i) {
+          const float p0 = ex2(x[2 * i] - m_use), p1 = ex2(x[2 * i + 1] - m_use);
+          sum += p0 + p1;
+          pk[i] = pack_bf16(p0, p1);
+        }
+        l += sum;
+        tmem_st32(tl + kTmS + 64 * s, pk);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[kPFull + s]);
+      }
+      if (!ok || !mbar_wait(&bars[kOFull], pv & 1)) {
+        report(p.status, RELATTN_DEV_WAIT_TIMEOUT);
+        *s_abort = 1;
+        break;
+      }
+      ++pv;
+      tc_fence_after();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      __nv_bfloat16* orow = p.out + (static_cast<size_t>(token) * p.Hq + it.h) * DV;
+#pragma unroll 1
+      for (int c0 = 0; c0 < DV; c0 += 32) {
+        uint32_t o[32];
+        tmem_ld32(tl + kTmO + c0, o);
+        tmem_wait_ld();
+        if (row_ok) {
+          uint32_t w[16];
 #pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const float pv = ex2(x[nt][2 * rr + e] - m_use);
-            x[nt][2 * rr + e] = pv;
-            sum += pv;
-          }
-        l_[rr] = l_[rr] * alpha + sum;
+          for (int i = 0; i < 16; ++i)
+            w[i] = pack_bf16(__uint_as_float(o[2 * i]) * inv, __uint_as_float(o[2 * i + 1]) * inv);
+          uint4* dst = reinterpret_cast<uint4*>(orow + c0);
 #pragma unroll
-        for (int nd = 0; nd < DV / 8; ++nd) {
-          o[nd][2 * rr] *= alpha;
-          o[nd][2 * rr + 1] *= alpha;
+          for (int i = 0; i < 4; ++i)
+            dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
         }
       }
-      const uint32_t vbase = kbase + 16384;
-      const int mi = lane >> 3;
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        uint32_t pa[4];
-        pa[0] = pack_bf16(x[2 * kk][0], x[2 * kk][1]);
-        pa[1] = pack_bf16(x[2 * kk][2], x[2 * kk][3]);
-        pa[2] = pack_bf16(x[2 * kk + 1][0], x[2 * kk + 1][1]);
-        pa[3] = pack_bf16(x[2 * kk + 1][2], x[2 * kk + 1][3]);
-        const int key = kk * 16 + (mi & 1) * 8 + (lane & 7);
-#pragma unroll
-        for (int nd = 0; nd < DV / 8; nd += 2) {
-          const int chunk = nd + (mi >> 1);
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4_t(vbase + (chunk >> 3) * 8192 + sw128(key, chunk & 7), b0, b1, b2, b3);
-          mma_16816(o[nd], pa, b0, b1);
-          mma_16816(o[nd + 1], pa, b2, b3);
-        }
-      }
+      tc_fence_before();
     }
-    __syncthreads();
-    if (abort) break;
-    if (tid == 0 && k + kPrefillStages < ntiles) issue(stage, tf + k + kPrefillStages);
   }
-
-#pragma unroll
-  for (int rr = 0; rr < 2; ++rr) {
-    l_[rr] += __shfl_xor_sync(0xffffffffu, l_[rr], 1);
-    l_[rr] += __shfl_xor_sync(0xffffffffu, l_[rr], 2);
-  }
-#pragma unroll
-  for (int rr = 0; rr < 2; ++rr) {
-    const int row = rr ? rB : rA;
-    if (row >= rows) continue;
-    const float inv = l_[rr] > 0.f ? 1.f / l_[rr] : 0.f;
-    __nv_bfloat16* orow = out_base + static_cast<size_t>(row) * p.Hq * DV;
-#pragma unroll
-    for (int nd = 0; nd < DV / 8; ++nd)
-      *reinterpret_cast<__nv_bfloat162*>(orow + nd * 8 + cq * 2) =
-          __floats2bfloat162_rn(o[nd][2 * rr] * inv, o[nd][2 * rr + 1] * inv);
-  }
+  if (*s_abort && tid == 0) report(p.status, RELATTN_DEV_WAIT_TIMEOUT);
+  __syncwarp();  // lanes idle while lane 0 produced/issued rejoin here
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tbase, kTmemCols);
 }
 
+// Replays the prefill kernel's block walk (128-row query tiles, 64-key tiles).
 __global__ void prefill_walk_kernel(const PrefillParams p) {
   if (threadIdx.x != 0) return;
   const int qt = blockIdx.x, b = blockIdx.y;
-  const int n = p.cu_seqlens[b + 1] - p.cu_seqlens[b];
+  const int c0 = p.cu_seqlens[b], c1 = p.cu_seqlens[b + 1];
+  const int n = c1 - c0;
   const int ctx = p.ctx_lens[b];
-  const int t0 = qt * kQTile;
-  if (t0 >= n || !seq_ok(ctx, n, p.max_blocks)) return;
-  const int rows = min(kQTile, n - t0);
+  const int t0 = qt * kQRows;
+  if (!rows_ok(c0, c1, p.T) || !seq_ok(ctx, n, p.max_blocks) || t0 >= n) return;
+  const int rows = min(kQRows, n - t0);
   const int P0 = ctx + t0, P1 = P0 + rows - 1;
   const int tf = window_lo(P0, p.window) / kTileKeys;
   const int ntiles = P1 / kTileKeys - tf + 1;
@@ -306,34 +533,34 @@ __global__ void prefill_walk_kernel(const PrefillParams p) {
 
 }  // namespace
 
+int prefill_smem_bytes(int B, int dv) { return PrefillSmem(B, dv).total + 1024; }
+
 cudaError_t launch_cache_write(const PrefillParams& p, cudaStream_t stream) {
-  const dim3 grid((p.max_q_len + kQTile - 1) / kQTile, p.B);
+  const dim3 grid((p.max_q_len + kCwTile - 1) / kCwTile, p.B);
   cache_write_kernel<<<grid, 256, 0, stream>>>(p);
   return cudaGetLastError();
 }
 
-cudaError_t launch_prefill(const PrefillLaunch& L, cudaStream_t stream) {
+cudaError_t launch_prefill(const PrefillLaunch& L, int grid, cudaStream_t stream) {
   const PrefillParams& p = L.p;
-  const dim3 grid((p.max_q_len + kQTile - 1) / kQTile, p.Hq, p.B);
-  const int smem = kPrefillStages * (16384 + kTileKeys * p.dv * 2) + 1024 +
-                   kPrefillStages * 16 + 64;
+  const int smem = prefill_smem_bytes(p.B, p.dv);
   cudaError_t e;
   if (p.dv == 128) {
-    e = cudaFuncSetAttribute(prefill_kernel<128>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    e = cudaFuncSetAttribute(prefill_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem);
     if (e != cudaSuccess) return e;
-    prefill_kernel<128><<<grid, kPrefillThreads, smem, stream>>>(L.tm_k, L.tm_v, p);
+    prefill_kernel<128><<<grid, kPfThreads, smem, stream>>>(L.tm_k, L.tm_v, L.tm_rel, p);
   } else {
-    e = cudaFuncSetAttribute(prefill_kernel<64>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    e = cudaFuncSetAttribute(prefill_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem);
     if (e != cudaSuccess) return e;
-    prefill_kernel<64><<<grid, kPrefillThreads, smem, stream>>>(L.tm_k, L.tm_v, p);
+    prefill_kernel<64><<<grid, kPfThreads, smem, stream>>>(L.tm_k, L.tm_v, L.tm_rel, p);
   }
   return cudaGetLastError();
 }
 
 cudaError_t launch_prefill_walk(const PrefillParams& p, cudaStream_t stream) {
-  const dim3 grid((p.max_q_len + kQTile - 1) / kQTile, p.B);
+  const dim3 grid((p.max_q_len + kQRows - 1) / kQRows, p.B);
   prefill_walk_kernel<<<grid, 32, 0, stream>>>(p);
   return cudaGetLastError();
 }

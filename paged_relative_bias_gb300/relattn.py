@@ -269,7 +269,9 @@ def debug_walk_prefill(cu_seqlens, ctx_lens, block_table, window: int, k_cache, 
     """Replay of the prefill kernel's block walk: int32 [n, 6] records."""
     dev = block_table.device
     cache = cache_desc(k_cache, v_cache)
-    dims = Dims(ctx_lens.shape[0], num_q_heads, block_table.shape[1], 0, int(max_q_len), 0)
+    num_tokens = int(cu_seqlens[-1].item())  # test hook: a host read is fine here
+    dims = Dims(ctx_lens.shape[0], num_q_heads, block_table.shape[1], num_tokens,
+                int(max_q_len), 0)
     ws = new_workspace(workspace_size(dims, cache), dev)
     rec = torch.zeros((max_records, 6), dtype=torch.int32, device=dev)
     cnt = torch.zeros(1, dtype=torch.int32, device=dev)

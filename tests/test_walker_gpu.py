@@ -1,5 +1,8 @@
 """The device block walk is bit-exact against the oracle's block selection.
 
+Decode walks 64-key tiles per (sequence, KV head); prefill walks the 64-key
+tiles of each 128-row query tile.
+
 The decode and prefill kernels' walk (which tiles, which physical blocks,
 which CTA) is replayed by the library's debug entry points and compared with
 the oracle's independent integer functions.
@@ -95,8 +98,8 @@ def test_prefill_walk_bit_exact(window):
     for b, t0, tile, lblk, phys, _ in rec.tolist():
         got[(b, t0)].append((tile, lblk, phys))
     for b, (n, ctx) in enumerate(zip(wl.new_tokens, wl.ctx_lens)):
-        for t0 in range(0, n, 64):
-            t1 = min(n, t0 + 64) - 1
+        for t0 in range(0, n, 128):
+            t1 = min(n, t0 + 128) - 1
             blocks = dict(O.prefill_blocks(ctx, t0, t1, window, table[b]))
             lo, _ = O.visible_keys(ctx + t0, window)
             want = [(t, t // 2, blocks[t // 2]) for t in range(lo // 64, (ctx + t1) // 64 + 1)]
