@@ -302,8 +302,8 @@ def run_decode_e2e(R, case, wl, alg, ws, device, steps, warmup, flush, dist, sam
     return times, h2d, d2h
 
 
-def run_prefill(R, wl, device, steps, warmup, flush, dist, sampler):
-    case = I.make_prefill(wl, device)
+def run_prefill(R, wl, device, steps, warmup, flush, dist, sampler, case=None):
+    case = case if case is not None else I.make_prefill(wl, device)
     dims = R.prefill_dims(case["q"], case["block_table"], case["ctx_lens"], case["max_q_len"])
     ws = R.new_workspace(R.workspace_size(dims, R.cache_desc(case["k_cache"],
                                                              case["v_cache"])), device)
@@ -319,7 +319,6 @@ def run_prefill(R, wl, device, steps, warmup, flush, dist, sampler):
     times = timed_steps(step, steps, warmup, flush, dist, sampler)
     if R.read_status(ws) != 0:
         raise RuntimeError("prefill reported a device status")
-    del case
     return times
 
 
@@ -360,6 +359,38 @@ def cores_used():
     return int(os.environ.get("OMP_NUM_THREADS", "1"))
 
 
+def prefill_workload(args):
+    wl = I.WORKLOADS["chunked_prefill"]
+    if args.prefill_new_tokens:
+        wl = I.variant(wl, new_tokens=(args.prefill_new_tokens,) * len(wl.new_tokens))
+    return wl
+
+
+def ours_prefill(args, R, dist, device, peaks, flush, sampler):
+    """Chunked prefill as the timed step (TFLOP/s of visible pairs)."""
+    wl = prefill_workload(args)
+    flops, pbytes = prefill_work(wl)
+    times = run_prefill(R, wl, device, args.steps, args.warmup, flush, dist, sampler)
+    t_ms = sum(times) / len(times)
+    t_max = dist.max(sum(times))
+    value = flops * dist.world * args.steps / (t_max / 1e3) / 1e12
+    clocks = sampler.stop()
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": dist.world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t_ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) q/k/v bf16, rel fp32)",
+        "config": {"workload": describe(wl), "l2": "flushed before every step (2x L2 write)",
+                   "parallelism": f"replicas x{dist.world} (the path does not shard)"},
+        "roofline": roofline("hbm", pbytes / (t_ms / 1e3) / 1e9, peaks["hbm"], "GB/s", None),
+        "tensor_frac_of_bf16_peak": round(flops / (t_ms / 1e3) / 1e12 / peaks["bf16"], 4),
+        "peak_source": peaks["source"], "gpu_launches": 2 * args.steps, "clocks": clocks,
+        "note": "step = cache write + attention kernels"}
+    if dist.rank == 0:
+        print(json.dumps(line), flush=True)
+    dist.close()
+
+
 def ours(args):
     from paged_relative_bias_gb300 import build as B
     from paged_relative_bias_gb300 import relattn as R
@@ -376,6 +407,8 @@ def ours(args):
         flush_buf.zero_()
 
     sampler = ClockSampler(device.index)
+    if args.workload == "chunked_prefill":
+        return ours_prefill(args, R, dist, device, peaks, flush, sampler)
     wl = I.WORKLOADS[args.workload]
     case, alg, times, ws, _ = run_decode(R, wl, device, args.steps, args.warmup, flush, dist,
                                          sampler)
@@ -403,7 +436,7 @@ def ours(args):
                 "frac_of_nominal_8000": round(gbs / 8000.0, 4)})
             del c2
             torch.cuda.empty_cache()
-        wp = I.WORKLOADS["chunked_prefill"]
+        wp = prefill_workload(args)
         flops, pbytes = prefill_work(wp)
         tp = run_prefill(R, wp, device, max(3, args.secondary_steps // 4), 2, flush, dist,
                          sampler)
@@ -516,7 +549,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="local_decode",
                     choices=["local_decode", "global_decode_b1", "global_decode_b8",
-                             "diffhead_decode"])
+                             "diffhead_decode", "chunked_prefill"])
+    ap.add_argument("--prefill-new-tokens", type=int, default=0,
+                    help="new tokens per sequence of the chunked prefill (default 8192)")
     ap.add_argument("--secondary-steps", type=int, default=50)
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -48,7 +48,7 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmQ = 0, kTmS = 64, kTmO = 192;  // S buffer s at kTmS + 64 s
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kNegInf = -__builtin_huge_valf();
-constexpr float kRescaleLog2 = 8.f;  // move the running max only past 2^8
+constexpr float kRescaleNat = 5.5451774f;  // move the running max only past e^(8 ln 2)
 constexpr uint32_t kIdescS = umma_idesc_bf16(128, kTileKeys, 0);
 
 enum Bar { kKFull = 0, kKEmpty = 2, kVFull = 4, kVEmpty = 6, kRFull = 8, kREmpty = 11,
@@ -389,13 +389,24 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[kQFull]);
 
+      // Scores in natural-log units: x = q.k / sqrt(d) + rel; exp2 takes
+      // log2(e) in its FFMA.
+      const float scale = scale_log2 * 0.69314718055994531f;
+      const int dmax = p.window > 0 ? p.window - 1 : 0x7fffffff;  // visible d in [0, dmax]
       float m_used = kNegInf, l = 0.f;
       bool ok = true;
+      int next_id = __ldg(trow + (it.tf >> 1));
       for (int k = 0; k < it.ntiles; ++k, ++n) {
         const int s = n & 1;
         const int j0 = (it.tf + k) * kTileKeys;
-        const int id = __ldg(trow + ((it.tf + k) >> 1));
-        const bool tile_ok = id >= 0 && id < p.num_blocks;
+        const int id = next_id;
+        if (k + 1 < it.ntiles) next_id = __ldg(trow + ((it.tf + k + 1) >> 1));
+        // visible columns of this row: c in [clo, clo + span)
+        const int dc = P - j0;  // distance of column 0
+        const int clo = max(0, dc - dmax);
+        int span = min(kTileKeys - 1, dc) - clo + 1;
+        if (span < 0 || !row_ok || id < 0 || id >= p.num_blocks) span = 0;
+        const bool warp_full = __all_sync(0xffffffffu, clo == 0 && span == kTileKeys);
         if (!mbar_wait(&bars[kSFull + s], (n >> 1) & 1)) { ok = false; break; }
         tc_fence_after();
         uint32_t sr[64];
@@ -404,38 +415,38 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         tmem_wait_ld();
         const int rs = n % kRelStages;
         if (!mbar_wait(&bars[kRFull + rs], (n / kRelStages) & 1)) { ok = false; break; }
-        const bool need_rel = it.P0 - j0 - (kTileKeys - 1) < p.rel_extent;
-        const float* rrow = reinterpret_cast<const float*>(
-                                smem + L.rel + rs * kRelStageBytes + q4 * kRelBoxBytes) +
-                            lane * kRelBoxCols;
-        // box column of key j0 + c is (P - j0 - x_q) - c, x_q its first distance
-        const int xq = (it.P0 + 32 * q4 - j0 - (kTileKeys - 1)) & ~3;
-        const int cbase = P - j0 - xq;
-        const bool full = tile_ok && row_ok && j0 >= lo && j0 + kTileKeys - 1 <= P;
-        const bool any = tile_ok && row_ok && j0 + kTileKeys - 1 >= lo && j0 <= P;
         float x[64];
-        float mx = kNegInf;
+        if (it.P0 - j0 - (kTileKeys - 1) < p.rel_extent) {
+          // box column of key j0 + c is (P - j0 - x_q) - c, x_q its first distance
+          const int xq = (it.P0 + 32 * q4 - j0 - (kTileKeys - 1)) & ~3;
+          const float* rb = reinterpret_cast<const float*>(
+                                smem + L.rel + rs * kRelStageBytes + q4 * kRelBoxBytes) +
+                            lane * kRelBoxCols + (dc - xq);
 #pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          const float bias = need_rel ? rrow[cbase - c] : 0.f;
-          float v = fmaf(__uint_as_float(sr[c]), scale_log2, bias * kLog2e);
-          if (!full) {
-            const int j = j0 + c;
-            if (!(any && j >= lo && j <= P)) v = kNegInf;
-          }
-          x[c] = v;
-          mx = fmaxf(mx, v);
+          for (int c = 0; c < 64; ++c) x[c] = fmaf(__uint_as_float(sr[c]), scale, rb[-c]);
+        } else {  // every distance is past rel_extent: no bias
+#pragma unroll
+          for (int c = 0; c < 64; ++c) x[c] = __uint_as_float(sr[c]) * scale;
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[kREmpty + rs]);
+        if (!warp_full) {
+#pragma unroll
+          for (int c = 0; c < 64; ++c)
+            x[c] = static_cast<unsigned>(c - clo) < static_cast<unsigned>(span) ? x[c] : kNegInf;
+        }
+        float mq[4] = {x[0], x[1], x[2], x[3]};
+#pragma unroll
+        for (int c = 4; c < 64; ++c) mq[c & 3] = fmaxf(mq[c & 3], x[c]);
+        const float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
         if (k > 0) {  // the previous tile's O += P V has landed
           if (!mbar_wait(&bars[kOFull], pv & 1)) { ok = false; break; }
           ++pv;
           tc_fence_after();
         }
-        const bool grow = mx > m_used + kRescaleLog2;
+        const bool grow = mx > m_used + kRescaleNat;
         const float m_new = grow ? mx : m_used;
-        const float alpha = (grow && m_used != kNegInf) ? ex2(m_used - m_new) : 1.f;
+        const float alpha = (grow && m_used != kNegInf) ? ex2((m_used - m_new) * kLog2e) : 1.f;
         if (k > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
           for (int c0 = 0; c0 < DV; c0 += 32) {
@@ -450,16 +461,17 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         }
         l *= alpha;
         m_used = m_new;
-        const float m_use = m_used == kNegInf ? 0.f : m_used;
+        const float mb = m_used == kNegInf ? 0.f : -m_used * kLog2e;
         uint32_t pk[32];
-        float sum = 0.f;
+        float sq[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          const float p0 = ex2(x[2 * i] - m_use), p1 = ex2(x[2 * i + 1] - m_use);
-          sum += p0 + p1;
+          const float p0 = ex2(fmaf(x[2 * i], kLog2e, mb));
+          const float p1 = ex2(fmaf(x[2 * i + 1], kLog2e, mb));
+          sq[i & 3] += p0 + p1;
           pk[i] = pack_bf16(p0, p1);
         }
-        l += sum;
+        l += (sq[0] + sq[1]) + (sq[2] + sq[3]);
         tmem_st32(tl + kTmS + 64 * s, pk);
         tmem_wait_st();
         tc_fence_before();
