@@ -141,6 +141,42 @@ int relattn_decode(const void* q, const float* rel,
                    const relattn_dims* dims, void* out,
                    void* workspace, size_t workspace_bytes, void* stream);
 
+/* Size of the library-owned scratch array used by relattn_decode_noalloc. */
+#define RELATTN_NOALLOC_SCRATCH_BYTES (4u << 20)
+
+/*
+ * Paged decode without a workspace, for callers that cannot allocate device
+ * memory.  No counterpart on the pages; this is a convenience of the library.
+ *
+ * Some hosts own every device buffer themselves -- a serving engine that
+ * hands a plugin only its inputs and outputs, or a runtime with a fixed
+ * memory budget in which a foreign cudaMalloc (and the synchronisation it
+ * implies) is not allowed -- and cannot provide the workspace relattn_decode
+ * asks for.  This call takes the same arguments as relattn_decode without the
+ * workspace and computes the same result with the same kernel; its split
+ * state lives in one array of RELATTN_NOALLOC_SCRATCH_BYTES that the library
+ * declares in device memory (held by every GPU that loads the library until
+ * the process exits).  It allocates nothing and calls no allocating routine.
+ *
+ *  - Limit: if the split state for these sizes (relattn_workspace_size)
+ *    exceeds RELATTN_NOALLOC_SCRATCH_BYTES, the call returns
+ *    RELATTN_ERR_WORKSPACE and enqueues nothing.
+ *  - The first call on a device looks up the array's device address (once,
+ *    with that device current); make that first call before any stream
+ *    capture on that device.
+ *  - Every call clears the status word and counters of the array on `stream`
+ *    before its kernel, so no zero-filling is needed by the caller; device
+ *    status bits are not reported back by this call.
+ *  - All calls share the one array: calls whose work overlaps on the GPU
+ *    (different streams without ordering between them) race and corrupt each
+ *    other's results.  Order them on one stream.
+ */
+int relattn_decode_noalloc(const void* q, const float* rel,
+                           const relattn_kv_cache* kv_cache,
+                           const int32_t* block_table, const int32_t* seq_lens,
+                           int32_t window, int32_t rel_extent,
+                           const relattn_dims* dims, void* out, void* stream);
+
 /*
  * Chunked prefill with a cached prefix.
  *

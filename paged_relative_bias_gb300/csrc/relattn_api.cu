@@ -273,6 +273,57 @@ int relattn_debug_walk_decode(const int32_t* block_table, const int32_t* seq_len
   return to_status(launch_decode_walk(L.p, L.grid, static_cast<cudaStream_t>(stream)));
 }
 
+// ---- decode with library-owned scratch ----------------------------------
+// For callers that may not allocate device memory (their host owns every
+// buffer, or cannot pay for an allocation on the decode path): the split
+// state that relattn_decode keeps in the caller's workspace lives here, in
+// one array that every GPU loading this library holds until the process exits.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[RELATTN_NOALLOC_SCRATCH_BYTES];
+static void* g_noalloc_addr[kMaxDevices];  // device address of the array, per device
+
+// The device address of the scratch array on the current device.  In host
+// code the array's name is only a host-side stand-in, so the address is asked
+// from the runtime once per device (with that device current) and cached.
+static int noalloc_scratch(void** addr) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return RELATTN_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_noalloc_addr[dev]) {
+    void* a = nullptr;
+    if (cudaGetSymbolAddress(&a, g_noalloc_scratch) != cudaSuccess || !a) return RELATTN_ERR_CUDA;
+    g_noalloc_addr[dev] = a;
+  }
+  *addr = g_noalloc_addr[dev];
+  return RELATTN_OK;
+}
+
+int relattn_decode_noalloc(const void* q, const float* rel, const relattn_kv_cache* kv_cache,
+                           const int32_t* block_table, const int32_t* seq_lens, int32_t window,
+                           int32_t rel_extent, const relattn_dims* dims, void* out,
+                           void* stream) {
+  int rc = check_cache(kv_cache);
+  if (rc != RELATTN_OK) return rc;
+  rc = check_dims(dims, kv_cache);
+  if (rc != RELATTN_OK) return rc;
+  DeviceInfo di;
+  if (!device_info(&di)) return RELATTN_ERR_CUDA;
+  const WsLayout w = ws_layout(dims, kv_cache, decode_grid(dims, di));
+  if (w.total > RELATTN_NOALLOC_SCRATCH_BYTES) return RELATTN_ERR_WORKSPACE;
+  void* scratch = nullptr;
+  rc = noalloc_scratch(&scratch);
+  if (rc != RELATTN_OK) return rc;
+  DecodeLaunch L;
+  rc = prepare_decode(q, rel, kv_cache, block_table, seq_lens, window, rel_extent, dims, out,
+                      scratch, RELATTN_NOALLOC_SCRATCH_BYTES, false, &L, &di);
+  if (rc != RELATTN_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // The array keeps the previous call's contents: the status word and the
+  // split counters must start at zero (the partial results need not).
+  cudaError_t e = cudaMemsetAsync(scratch, 0, w.lse, s);
+  if (e == cudaSuccess) e = launch_decode(L, s);
+  return to_status(e);
+}
+
 static int prepare_prefill(const void* q, const void* k, const void* v, const float* rel,
                            const int32_t* cu_seqlens, const relattn_kv_cache* cache,
                            const int32_t* block_table, const int32_t* ctx_lens,

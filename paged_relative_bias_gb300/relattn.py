@@ -36,6 +36,7 @@ EXPORTS = (
     "relattn_debug_walk_decode",
     "relattn_debug_walk_prefill",
     "relattn_abi_version",
+    "relattn_decode_noalloc",
 )
 
 
@@ -98,6 +99,9 @@ def lib() -> ctypes.CDLL:
                                              c_void_p, c_int32, c_void_p, c_void_p,
                                              c_size_t, c_void_p]
     L.relattn_debug_walk_prefill.restype = c_int
+    L.relattn_decode_noalloc.argtypes = [c_void_p, c_void_p, P, c_void_p, c_void_p, c_int32,
+                                         c_int32, S, c_void_p, c_void_p]
+    L.relattn_decode_noalloc.restype = c_int
     L.relattn_abi_version.argtypes = []
     L.relattn_abi_version.restype = c_int
     _LIB = L
@@ -199,6 +203,32 @@ def relattn_decode(q, rel, k_cache, v_cache, block_table, seq_lens, window: int,
         seq_lens.data_ptr(), int(window), int(rel_extent), ctypes.byref(dims),
         out.data_ptr(), workspace.data_ptr(), workspace.numel(), _stream(dev)),
         "relattn_decode")
+    return out
+
+
+def relattn_decode_noalloc(q, rel, k_cache, v_cache, block_table, seq_lens, window: int,
+                           rel_extent: int, out, num_ctas: int = 0):
+    """Decode whose split state lives in the library's own device array.
+
+    For callers that cannot allocate device memory: nothing is allocated here
+    either, so ``out`` must be given.  Calls share that array; order them on
+    one stream.
+    """
+    dev = q.device
+    B, Hq, _ = q.shape
+    _need(q, "q", torch.bfloat16, 3, dev)
+    _need(rel, "rel", torch.float32, 3, dev)
+    _need(k_cache, "k_cache", torch.bfloat16, 4, dev)
+    _need(v_cache, "v_cache", torch.bfloat16, 4, dev)
+    _need(block_table, "block_table", torch.int32, 2, dev)
+    _need(seq_lens, "seq_lens", torch.int32, 1, dev)
+    _need(out, "out", torch.bfloat16, 3, dev)
+    cache = cache_desc(k_cache, v_cache)
+    dims = decode_dims(q, block_table, num_ctas)
+    _check(lib().relattn_decode_noalloc(
+        q.data_ptr(), rel.data_ptr(), ctypes.byref(cache), block_table.data_ptr(),
+        seq_lens.data_ptr(), int(window), int(rel_extent), ctypes.byref(dims),
+        out.data_ptr(), _stream(dev)), "relattn_decode_noalloc")
     return out
 
 

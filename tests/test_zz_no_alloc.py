@@ -1,0 +1,67 @@
+"""Decode through the library-owned scratch array, compared with the
+workspace entry point.
+
+Collected last on purpose: it must also pass after every other test has run
+in the same process (the scratch array then holds an earlier call's state).
+"""
+
+import pytest
+import torch
+
+from paged_relative_bias_gb300 import inputs as I
+from paged_relative_bias_gb300 import relattn as R
+from tests.parity import assert_parity, to_f64
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from paged_relative_bias_gb300 import build
+    build.build()
+    R.lib()
+
+
+def with_workspace(case, num_ctas):
+    dims = R.decode_dims(case["q"], case["block_table"], num_ctas)
+    ws = R.new_workspace(R.workspace_size(dims, R.cache_desc(case["k_cache"],
+                                                             case["v_cache"])), DEV)
+    out = R.relattn_decode(case["q"], case["rel"], case["k_cache"], case["v_cache"],
+                           case["block_table"], case["seq_lens"], case["window"],
+                           case["rel_extent"], workspace=ws, num_ctas=num_ctas)
+    torch.cuda.synchronize()
+    assert R.read_status(ws) == 0
+    return out
+
+
+def without_workspace(case, out, num_ctas):
+    return R.relattn_decode_noalloc(case["q"], case["rel"], case["k_cache"], case["v_cache"],
+                                    case["block_table"], case["seq_lens"], case["window"],
+                                    case["rel_extent"], out, num_ctas=num_ctas)
+
+
+@pytest.mark.parametrize("num_ctas", [0, 37])
+def test_noalloc_decode_matches_workspace_decode_twice(num_ctas):
+    wl = I.variant(I.WORKLOADS["global_decode_b8"], batch=4, lengths=("uniform", 1, 6000))
+    case = I.make_decode(wl, DEV, seed_data=13)
+    want = to_f64(with_workspace(case, num_ctas))
+    outs = [torch.empty_like(case["q"][..., :case["v_cache"].shape[-1]]) for _ in range(2)]
+    for o in outs:                       # two calls in a row, same stream
+        without_workspace(case, o, num_ctas)
+    torch.cuda.synchronize()
+    for i, o in enumerate(outs):
+        assert_parity(to_f64(o), want, what=f"noalloc call {i}")
+
+
+def test_noalloc_rejects_sizes_beyond_its_array():
+    """Split state larger than the array is refused before anything is enqueued."""
+    wl = I.DecodeWorkload("big_split", 2, 32, 2, 128, 128, 0, 64, ("list", [300, 500]))
+    case = I.make_decode(wl, DEV, seed_data=1)
+    out = torch.zeros(2, 32, 128, dtype=torch.bfloat16, device=DEV)
+    with pytest.raises(R.RelattnError) as err:
+        without_workspace(case, out, num_ctas=5000)
+    assert err.value.code == R.ERR_WORKSPACE
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(out).item() == 0
