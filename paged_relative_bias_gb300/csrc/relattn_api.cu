@@ -371,11 +371,20 @@ static int prepare_prefill(const void* q, const void* k, const void* v, const fl
   if (walk) return RELATTN_OK;
   DeviceInfo di;
   if (!device_info(&di)) return RELATTN_ERR_CUDA;
-  if (prefill_smem_bytes(p.B, p.dv) > di.smem_optin) return RELATTN_ERR_UNSUPPORTED;
+  p.ring_stages = prefill_ring_stages(p.B, p.dv, di.smem_optin);
+  if (p.ring_stages == 0) return RELATTN_ERR_UNSUPPORTED;
   const long long qtiles = static_cast<long long>(p.B) * ((p.max_q_len + 127) / 128) * p.Hq;
   const long long want = dims->num_ctas > 0 ? dims->num_ctas : di.sms;
   L->grid = static_cast<int>(qtiles < want ? (qtiles > 0 ? qtiles : 1) : want);
   if (!cache_maps(cache, &L->tm_k, &L->tm_v)) return RELATTN_ERR_CUDA;
+  // q [T][Hq][128] bf16: one head's 128-token tile as two 64-column boxes
+  const cuuint64_t qd[3] = {128, static_cast<cuuint64_t>(dims->num_q_heads),
+                            static_cast<cuuint64_t>(dims->num_tokens)};
+  const cuuint64_t qs[2] = {256, static_cast<cuuint64_t>(dims->num_q_heads) * 256};
+  const cuuint32_t qb[3] = {64, 1, 128};
+  if (!make_map(&L->tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), qd, qs, qb,
+                CU_TENSOR_MAP_SWIZZLE_128B))
+    return RELATTN_ERR_CUDA;
   // rel [T][Hq][E] fp32: boxes of 32 tokens x 100 distances of one head
   const cuuint64_t rd[3] = {static_cast<cuuint64_t>(rel_extent),
                             static_cast<cuuint64_t>(dims->num_q_heads),

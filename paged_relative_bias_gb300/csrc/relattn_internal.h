@@ -52,11 +52,12 @@ struct PrefillParams {
   int32_t* dbg_count;
   int dbg_max;
   int B, T, Hq, Hkv, g, dv, max_blocks, num_blocks, window, rel_extent, max_q_len;
+  int ring_stages;  // depth of the query/rel/scratch ring (2 or 3, as shared memory allows)
   float scale_log2;
 };
 
 struct PrefillLaunch {
-  CUtensorMap tm_k, tm_v, tm_rel;
+  CUtensorMap tm_q, tm_k, tm_v, tm_rel;
   PrefillParams p;
   int grid;
 };
@@ -66,7 +67,8 @@ cudaError_t launch_decode(const DecodeLaunch& L, cudaStream_t stream);
 cudaError_t launch_decode_walk(const DecodeParams& p, int grid, cudaStream_t stream);
 
 cudaError_t launch_cache_write(const PrefillParams& p, cudaStream_t stream);
-int prefill_smem_bytes(int B, int dv);
+int prefill_smem_bytes(int B, int dv, int ring_stages);
+int prefill_ring_stages(int B, int dv, int smem_optin);  // 0 if nothing fits
 cudaError_t launch_prefill(const PrefillLaunch& L, int grid, cudaStream_t stream);
 cudaError_t launch_prefill_walk(const PrefillParams& p, cudaStream_t stream);
 

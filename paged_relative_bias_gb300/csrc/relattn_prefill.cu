@@ -39,11 +39,20 @@ constexpr int kQRows = 128;
 constexpr int kCwTile = 64;                 // cache_write tokens per CTA
 constexpr int kPfWarps = 7;
 constexpr int kPfThreads = 32 * kPfWarps;
-constexpr int kKStages = 2, kVStages = 2, kRelStages = 3;
+constexpr int kKStages = 2, kVStages = 2, kMaxRingStages = 3;
 constexpr int kKStageBytes = kTileKeys * kDqk * 2;  // 16 KB
+constexpr int kQTileBytes = kQRows * kDqk * 2;      // 32 KB
+// rel boxes: 32 query rows x 100 distances, one per softmax warp.  Row r of a
+// box needs the 64 distances P_r - j0 - 63 .. P_r - j0; across 32 rows that is
+// 95, plus up to 3 for rounding the box start down to 16 bytes.  Lane l reads
+// word 101 l + const - c: 101 is odd, so the 32 lanes hit 32 banks.
 constexpr int kRelBoxRows = 32, kRelBoxCols = 100;
 constexpr int kRelBoxBytes = kRelBoxRows * kRelBoxCols * 4;  // 12800
-constexpr int kRelStageBytes = 4 * kRelBoxBytes;
+constexpr int kRelBoxes = kQRows / kRelBoxRows;              // 4 per tile
+// One ring of shared-memory slots carries, per work item, the query tile,
+// then the rel boxes of each key tile, then a scratch slot for storing O.
+constexpr int kRingSlotBytes = kRelBoxes * kRelBoxBytes;     // 51200 (50 KB)
+static_assert(kRingSlotBytes % 1024 == 0 && kRingSlotBytes >= kQTileBytes, "ring slot");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmQ = 0, kTmS = 64, kTmO = 192;  // S buffer s at kTmS + 64 s
 constexpr float kLog2e = 1.4426950408889634f;
@@ -51,6 +60,8 @@ constexpr float kNegInf = -__builtin_huge_valf();
 constexpr float kRescaleNat = 5.5451774f;  // move the running max only past e^(8 ln 2)
 constexpr uint32_t kIdescS = umma_idesc_bf16(128, kTileKeys, 0);
 
+// kRFull / kREmpty: ring slots (producer <-> softmax); kQFull: query tile in
+// TMEM (softmax -> MMA).
 enum Bar { kKFull = 0, kKEmpty = 2, kVFull = 4, kVEmpty = 6, kRFull = 8, kREmpty = 11,
            kSFull = 14, kPFull = 16, kOFull = 18, kQFull = 19, kDrain = 20, kNumBars = 21 };
 
@@ -106,13 +117,13 @@ __global__ void __launch_bounds__(256) cache_write_kernel(const PrefillParams p)
 
 // Shared-memory carve-up (byte offsets from a 1024-aligned base).
 struct PrefillSmem {
-  int k, v, vstage, rel, bars, misc, cu0, nrows, ctx, qpref, total;
-  __host__ __device__ PrefillSmem(int B, int dv) {
+  int k, v, vstage, ring, bars, misc, cu0, nrows, ctx, qpref, total;
+  __host__ __device__ PrefillSmem(int B, int dv, int ring_stages) {
     vstage = kTileKeys * dv * 2;
     k = 0;
     v = k + kKStages * kKStageBytes;
-    rel = v + kVStages * vstage;
-    bars = rel + kRelStages * kRelStageBytes;
+    ring = v + kVStages * vstage;  // 1024-aligned: query tiles land 128B-swizzled
+    bars = ring + ring_stages * kRingSlotBytes;
     misc = bars + kNumBars * 8;
     cu0 = misc + 16;
     nrows = cu0 + B * 4;
@@ -199,13 +210,15 @@ __device__ int prefill_prologue(const PrefillParams& p, uint8_t* smem, const Pre
 
 template <int DV>
 __global__ void __launch_bounds__(kPfThreads, 1)
-    prefill_kernel(const __grid_constant__ CUtensorMap tm_k,
+    prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
+                   const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v,
                    const __grid_constant__ CUtensorMap tm_rel, const PrefillParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const PrefillSmem L(p.B, DV);
+  const int nrs = p.ring_stages;
+  const PrefillSmem L(p.B, DV, nrs);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + L.misc);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + L.misc + 4);
@@ -224,7 +237,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       mbar_init(&bars[kSFull + s], 1);
       mbar_init(&bars[kPFull + s], 4);
     }
-    for (int s = 0; s < kRelStages; ++s) {
+    for (int s = 0; s < nrs; ++s) {
       mbar_init(&bars[kRFull + s], 1);
       mbar_init(&bars[kREmpty + s], 4);
     }
@@ -233,13 +246,14 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     mbar_init(&bars[kDrain], 1);
     fence_mbar_init();
     *s_abort = 0;
+    tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
     tma_prefetch_desc(&tm_rel);
   }
   // K/V stages start as zeros: a tile whose block id is invalid is never
   // loaded, and its P is zero, so its operands must at least be finite.
-  for (int i = tid; i < (L.rel - L.k) / 16; i += blockDim.x)
+  for (int i = tid; i < (L.ring - L.k) / 16; i += blockDim.x)
     reinterpret_cast<uint4*>(smem + L.k)[i] = make_uint4(0, 0, 0, 0);
   fence_proxy_async_smem();
   if (warp == 1) {
@@ -287,28 +301,47 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       }
     }
   } else if (warp == 6 && lane == 0) {
-    // ---------------------------------------------------- rel TMA producer
-    int n = 0;
-    for (int idx = blockIdx.x; idx < total && !*s_abort; idx += gridDim.x) {
+    // --------------------------------------------------- ring producer:
+    // per item the query tile, the rel boxes of each key tile, and an empty
+    // slot the softmax warps use to store O
+    int e = 0;
+    bool fail = false;
+    auto acquire = [&](int entry) -> uint8_t* {
+      const int slot = entry % nrs;
+      if (!mbar_wait(&bars[kREmpty + slot], ((entry / nrs) & 1) ^ 1)) return nullptr;
+      return smem + L.ring + slot * kRingSlotBytes;
+    };
+    for (int idx = blockIdx.x; idx < total && !*s_abort && !fail; idx += gridDim.x) {
       PItem it;
       prefill_item(idx, p, s_cu0, s_n, s_ctx, s_qpref, it);
-      for (int k = 0; k < it.ntiles; ++k, ++n) {
+      uint8_t* qd = acquire(e);
+      if (!qd) { fail = true; break; }
+      uint64_t* qbar = &bars[kRFull + e % nrs];
+      mbar_arrive_expect_tx(qbar, kQTileBytes);  // rows past T read as zeros
+      tma_load_3d(qd, &tm_q, qbar, 0, it.h, it.r0);
+      tma_load_3d(qd + kQTileBytes / 2, &tm_q, qbar, 64, it.h, it.r0);
+      ++e;
+      for (int k = 0; k < it.ntiles; ++k, ++e) {
         const int j0 = (it.tf + k) * kTileKeys;
-        const int rs = n % kRelStages;
-        if (!mbar_wait(&bars[kREmpty + rs], ((n / kRelStages) & 1) ^ 1)) { *s_abort = 1; break; }
+        uint8_t* rd = acquire(e);
+        if (!rd) { fail = true; break; }
+        uint64_t* rbar = &bars[kRFull + e % nrs];
         if (it.P0 - j0 - (kTileKeys - 1) < p.rel_extent) {
-          uint8_t* rd = smem + L.rel + rs * kRelStageBytes;
-          mbar_arrive_expect_tx(&bars[kRFull + rs], kRelStageBytes);
-          for (int q = 0; q < 4; ++q) {
-            const int x = (it.P0 + 32 * q - j0 - (kTileKeys - 1)) & ~3;
-            tma_load_3d(rd + q * kRelBoxBytes, &tm_rel, &bars[kRFull + rs], x, it.h,
-                        it.r0 + 32 * q);
+          mbar_arrive_expect_tx(rbar, kRingSlotBytes);
+          for (int bx = 0; bx < kRelBoxes; ++bx) {
+            const int x = (it.P0 + kRelBoxRows * bx - j0 - (kTileKeys - 1)) & ~3;
+            tma_load_3d(rd + bx * kRelBoxBytes, &tm_rel, rbar, x, it.h, it.r0 + kRelBoxRows * bx);
           }
         } else {
-          mbar_arrive(&bars[kRFull + rs]);  // every distance is past rel_extent
+          mbar_arrive(rbar);  // every distance is past rel_extent
         }
       }
+      if (fail) break;
+      if (!acquire(e)) { fail = true; break; }
+      mbar_arrive(&bars[kRFull + e % nrs]);  // the O scratch slot
+      ++e;
     }
+    if (fail) *s_abort = 1;
   } else if (warp == 1 && lane == 0) {
     // ---------------------------------------------------------- MMA issuer
     const uint32_t idesc_pv = umma_idesc_bf16(128, DV, 1);
@@ -359,35 +392,50 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const int q4 = warp & 3;  // TMEM lane quarter this warp may access
     const int r = 32 * q4 + lane;
     const uint32_t tl = tbase + (static_cast<uint32_t>(32 * q4) << 16);
-    int n = 0, pv = 0;
-    for (int idx = blockIdx.x; idx < total && !*s_abort; idx += gridDim.x) {
-      PItem it;
-      prefill_item(idx, p, s_cu0, s_n, s_ctx, s_qpref, it);
-      const bool row_ok = r < it.rows;
-      const int token = it.r0 + r;
-      const int P = it.P0 + r;
-      const int lo = window_lo(P, p.window);
-      const int* trow = p.block_table + static_cast<size_t>(it.b) * p.max_blocks;
-      // query row -> TMEM (the A operand of S = Q K^T)
-      {
-        uint32_t qr[64];
-        const uint4* src = reinterpret_cast<const uint4*>(
-            p.q + (static_cast<size_t>(token) * p.Hq + it.h) * kDqk);
+    int n = 0, e = 0, items = 0;  // key tiles and ring entries consumed
+    bool fail = false;
+    auto slot_wait = [&](int entry) -> uint8_t* {
+      const int slot = entry % nrs;
+      if (!mbar_wait(&bars[kRFull + slot], (entry / nrs) & 1)) return nullptr;
+      return smem + L.ring + slot * kRingSlotBytes;
+    };
+    // This thread's query row, from a ring slot (128-byte swizzled rows) into
+    // TMEM, the A operand of S = Q K^T; then the MMA warp may start.
+    auto load_q = [&](const uint8_t* qs, int entry) {
+      uint32_t qr[64];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const uint4 v = row_ok ? __ldg(src + i) : make_uint4(0, 0, 0, 0);
-          qr[4 * i] = v.x;
-          qr[4 * i + 1] = v.y;
-          qr[4 * i + 2] = v.z;
-          qr[4 * i + 3] = v.w;
+      for (int c = 0; c < 2; ++c)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const uint4 v =
+              *reinterpret_cast<const uint4*>(qs + c * (kQTileBytes / 2) + sw128(r, j));
+          qr[(c * 8 + j) * 4] = v.x;
+          qr[(c * 8 + j) * 4 + 1] = v.y;
+          qr[(c * 8 + j) * 4 + 2] = v.z;
+          qr[(c * 8 + j) * 4 + 3] = v.w;
         }
-        tmem_st32(tl + kTmQ, qr);
-        tmem_st32(tl + kTmQ + 32, qr + 32);
-        tmem_wait_st();
-      }
+      tmem_st32(tl + kTmQ, qr);
+      tmem_st32(tl + kTmQ + 32, qr + 32);
+      tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[kQFull]);
+      if (lane == 0) {
+        mbar_arrive(&bars[kQFull]);
+        mbar_arrive(&bars[kREmpty + entry % nrs]);
+      }
+    };
+    for (int idx = blockIdx.x; idx < total && !*s_abort; idx += gridDim.x, ++items) {
+      PItem it;
+      prefill_item(idx, p, s_cu0, s_n, s_ctx, s_qpref, it);
+      if (items == 0) {  // later items' queries are loaded during the previous epilogue
+        const uint8_t* qs = slot_wait(e);
+        if (!qs) { fail = true; break; }
+        load_q(qs, e);
+        ++e;
+      }
+      const bool row_ok = r < it.rows;
+      const int P = it.P0 + r;
+      const int* trow = p.block_table + static_cast<size_t>(it.b) * p.max_blocks;
 
       // Scores in natural-log units: x = q.k / sqrt(d) + rel; exp2 takes
       // log2(e) in its FFMA.
@@ -396,7 +444,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       float m_used = kNegInf, l = 0.f;
       bool ok = true;
       int next_id = __ldg(trow + (it.tf >> 1));
-      for (int k = 0; k < it.ntiles; ++k, ++n) {
+      for (int k = 0; k < it.ntiles; ++k, ++n, ++e) {
         const int s = n & 1;
         const int j0 = (it.tf + k) * kTileKeys;
         const int id = next_id;
@@ -413,14 +461,13 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         tmem_ld32(tl + kTmS + 64 * s, sr);
         tmem_ld32(tl + kTmS + 64 * s + 32, sr + 32);
         tmem_wait_ld();
-        const int rs = n % kRelStages;
-        if (!mbar_wait(&bars[kRFull + rs], (n / kRelStages) & 1)) { ok = false; break; }
+        const uint8_t* slot = slot_wait(e);
+        if (!slot) { ok = false; break; }
         float x[64];
         if (it.P0 - j0 - (kTileKeys - 1) < p.rel_extent) {
-          // box column of key j0 + c is (P - j0 - x_q) - c, x_q its first distance
-          const int xq = (it.P0 + 32 * q4 - j0 - (kTileKeys - 1)) & ~3;
-          const float* rb = reinterpret_cast<const float*>(
-                                smem + L.rel + rs * kRelStageBytes + q4 * kRelBoxBytes) +
+          // box column of key j0 + c is (P - j0 - xq) - c, xq the box's first distance
+          const int xq = (it.P0 + kRelBoxRows * q4 - j0 - (kTileKeys - 1)) & ~3;
+          const float* rb = reinterpret_cast<const float*>(slot + q4 * kRelBoxBytes) +
                             lane * kRelBoxCols + (dc - xq);
 #pragma unroll
           for (int c = 0; c < 64; ++c) x[c] = fmaf(__uint_as_float(sr[c]), scale, rb[-c]);
@@ -429,7 +476,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           for (int c = 0; c < 64; ++c) x[c] = __uint_as_float(sr[c]) * scale;
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bars[kREmpty + rs]);
+        if (lane == 0) mbar_arrive(&bars[kREmpty + e % nrs]);
         if (!warp_full) {
 #pragma unroll
           for (int c = 0; c < 64; ++c)
@@ -439,15 +486,15 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 #pragma unroll
         for (int c = 4; c < 64; ++c) mq[c & 3] = fmaxf(mq[c & 3], x[c]);
         const float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
-        if (k > 0) {  // the previous tile's O += P V has landed
-          if (!mbar_wait(&bars[kOFull], pv & 1)) { ok = false; break; }
-          ++pv;
-          tc_fence_after();
-        }
         const bool grow = mx > m_used + kRescaleNat;
         const float m_new = grow ? mx : m_used;
         const float alpha = (grow && m_used != kNegInf) ? ex2((m_used - m_new) * kLog2e) : 1.f;
         if (k > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+          // O must hold every earlier tile before it is rescaled.  PV of this
+          // tile cannot start before P is written below, so O's barrier is at
+          // most one phase past the one waited for.
+          if (!mbar_wait(&bars[kOFull], (n - 1) & 1)) { ok = false; break; }
+          tc_fence_after();
 #pragma unroll 1
           for (int c0 = 0; c0 < DV; c0 += 32) {
             uint32_t o[32];
@@ -478,32 +525,64 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[kPFull + s]);
       }
-      if (!ok || !mbar_wait(&bars[kOFull], pv & 1)) {
-        report(p.status, RELATTN_DEV_WAIT_TIMEOUT);
-        *s_abort = 1;
-        break;
-      }
-      ++pv;
+      // the item's last PV (phase n - 1) completes O, and every S = Q K^T of
+      // the item with it
+      if (!ok || !mbar_wait(&bars[kOFull], (n - 1) & 1)) { fail = true; break; }
       tc_fence_after();
+      // The next item's query goes into TMEM first, so its first S = Q K^T
+      // runs while this item's O is stored.  Its ring entry follows the
+      // O scratch entry.
+      const bool has_next = idx + static_cast<int>(gridDim.x) < total;
+      if (has_next) {
+        const uint8_t* qs = slot_wait(e + 1);
+        if (!qs) { fail = true; break; }
+        load_q(qs, e + 1);
+      }
+      // O / l -> bf16, through this warp's part of the scratch slot so that
+      // the global stores are whole rows (16 lanes per 256-byte row).
+      uint8_t* scr = slot_wait(e);
+      if (!scr) { fail = true; break; }
+      scr += q4 * (32 * DV * 2);
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      __nv_bfloat16* orow = p.out + (static_cast<size_t>(token) * p.Hq + it.h) * DV;
 #pragma unroll 1
       for (int c0 = 0; c0 < DV; c0 += 32) {
         uint32_t o[32];
         tmem_ld32(tl + kTmO + c0, o);
         tmem_wait_ld();
-        if (row_ok) {
-          uint32_t w[16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            w[i] = pack_bf16(__uint_as_float(o[2 * i]) * inv, __uint_as_float(o[2 * i + 1]) * inv);
-          uint4* dst = reinterpret_cast<uint4*>(orow + c0);
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+        for (int i = 0; i < 4; ++i) {
+          uint4 w;
+          w.x = pack_bf16(__uint_as_float(o[8 * i]) * inv, __uint_as_float(o[8 * i + 1]) * inv);
+          w.y = pack_bf16(__uint_as_float(o[8 * i + 2]) * inv, __uint_as_float(o[8 * i + 3]) * inv);
+          w.z = pack_bf16(__uint_as_float(o[8 * i + 4]) * inv, __uint_as_float(o[8 * i + 5]) * inv);
+          w.w = pack_bf16(__uint_as_float(o[8 * i + 6]) * inv, __uint_as_float(o[8 * i + 7]) * inv);
+          const int j = c0 / 8 + i;  // 16-byte chunk of the row
+          *reinterpret_cast<uint4*>(scr + lane * (DV * 2) + ((j ^ (lane & 7)) << 4)) = w;
         }
       }
-      tc_fence_before();
+      tc_fence_before();  // O is read before the next item's first PV overwrites it
+      __syncwarp();
+      constexpr int kCpr = DV / 8;     // 16-byte chunks per row
+      constexpr int kRpi = 32 / kCpr;  // rows per store instruction
+#pragma unroll
+      for (int i = 0; i < kCpr; ++i) {
+        const int row = i * kRpi + lane / kCpr;
+        const int ch = lane % kCpr;
+        const uint4 v =
+            *reinterpret_cast<const uint4*>(scr + row * (DV * 2) + ((ch ^ (row & 7)) << 4));
+        const int rr = 32 * q4 + row;
+        if (rr < it.rows)
+          *reinterpret_cast<uint4*>(
+              p.out + (static_cast<size_t>(it.r0 + rr) * p.Hq + it.h) * DV + ch * 8) = v;
+      }
+      fence_proxy_async_smem();  // these writes come before the slot's next TMA fill
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[kREmpty + e % nrs]);
+      e += has_next ? 2 : 1;
+    }
+    if (fail) {
+      report(p.status, RELATTN_DEV_WAIT_TIMEOUT);
+      *s_abort = 1;
     }
   }
   if (*s_abort && tid == 0) report(p.status, RELATTN_DEV_WAIT_TIMEOUT);
@@ -545,7 +624,15 @@ __global__ void prefill_walk_kernel(const PrefillParams p) {
 
 }  // namespace
 
-int prefill_smem_bytes(int B, int dv) { return PrefillSmem(B, dv).total + 1024; }
+int prefill_smem_bytes(int B, int dv, int ring_stages) {
+  return PrefillSmem(B, dv, ring_stages).total + 1024;
+}
+
+int prefill_ring_stages(int B, int dv, int smem_optin) {
+  for (int nr = kMaxRingStages; nr >= 2; --nr)
+    if (prefill_smem_bytes(B, dv, nr) <= smem_optin) return nr;
+  return 0;
+}
 
 cudaError_t launch_cache_write(const PrefillParams& p, cudaStream_t stream) {
   const dim3 grid((p.max_q_len + kCwTile - 1) / kCwTile, p.B);
@@ -555,18 +642,18 @@ cudaError_t launch_cache_write(const PrefillParams& p, cudaStream_t stream) {
 
 cudaError_t launch_prefill(const PrefillLaunch& L, int grid, cudaStream_t stream) {
   const PrefillParams& p = L.p;
-  const int smem = prefill_smem_bytes(p.B, p.dv);
+  const int smem = prefill_smem_bytes(p.B, p.dv, p.ring_stages);
   cudaError_t e;
   if (p.dv == 128) {
     e = cudaFuncSetAttribute(prefill_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              smem);
     if (e != cudaSuccess) return e;
-    prefill_kernel<128><<<grid, kPfThreads, smem, stream>>>(L.tm_k, L.tm_v, L.tm_rel, p);
+    prefill_kernel<128><<<grid, kPfThreads, smem, stream>>>(L.tm_q, L.tm_k, L.tm_v, L.tm_rel, p);
   } else {
     e = cudaFuncSetAttribute(prefill_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              smem);
     if (e != cudaSuccess) return e;
-    prefill_kernel<64><<<grid, kPfThreads, smem, stream>>>(L.tm_k, L.tm_v, L.tm_rel, p);
+    prefill_kernel<64><<<grid, kPfThreads, smem, stream>>>(L.tm_q, L.tm_k, L.tm_v, L.tm_rel, p);
   }
   return cudaGetLastError();
 }
