@@ -15,6 +15,7 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 constexpr int kMaxStages = 6;
+constexpr int kMaxDecodeGrid = 46340;  // grid^2 < 2^31
 constexpr size_t kStatusBytes = 256;
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -89,6 +90,27 @@ bool cache_maps(const relattn_kv_cache* c, CUtensorMap* tk, CUtensorMap* tv) {
   return make_map(tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, c->k, kd, ks, box,
                   CU_TENSOR_MAP_SWIZZLE_128B) &&
          make_map(tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, c->v, vd, vs, box,
+                  CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// Decode's K/V maps: one TMA copy brings a whole 64-key tile of one KV head.
+// The 4-D view (64 columns, cache row, 64-column half, head) puts the halves
+// outermost in the box, so shared memory receives [half][64 rows][128 B], the
+// same 128-byte-swizzled halves as two 3-D copies would.
+bool decode_cache_maps(const relattn_kv_cache* c, CUtensorMap* tk, CUtensorMap* tv) {
+  const cuuint64_t rows = static_cast<cuuint64_t>(c->num_blocks) * c->block_size;
+  const cuuint64_t hkv = static_cast<cuuint64_t>(c->num_kv_heads);
+  const cuuint64_t kd[4] = {64, rows, static_cast<cuuint64_t>(c->d_qk / 64), hkv};
+  const cuuint64_t ks[3] = {hkv * c->d_qk * 2, 128, static_cast<cuuint64_t>(c->d_qk) * 2};
+  const cuuint32_t kb[4] = {64, static_cast<cuuint32_t>(kTileKeys),
+                            static_cast<cuuint32_t>(c->d_qk / 64), 1};
+  const cuuint64_t vd[4] = {64, rows, static_cast<cuuint64_t>(c->d_v / 64), hkv};
+  const cuuint64_t vs[3] = {hkv * c->d_v * 2, 128, static_cast<cuuint64_t>(c->d_v) * 2};
+  const cuuint32_t vb[4] = {64, static_cast<cuuint32_t>(kTileKeys),
+                            static_cast<cuuint32_t>(c->d_v / 64), 1};
+  return make_map(tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, c->k, kd, ks, kb,
+                  CU_TENSOR_MAP_SWIZZLE_128B) &&
+         make_map(tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, c->v, vd, vs, vb,
                   CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
@@ -191,6 +213,11 @@ static int prepare_decode(const void* q, const float* rel, const relattn_kv_cach
   if (!aligned16(workspace)) return RELATTN_ERR_INVALID_ARG;
   if (!device_info(di)) return RELATTN_ERR_CUDA;
   const int grid = decode_grid(dims, *di);
+  // the kernel's work split is 32-bit: all tiles < 2^31, grid^2 < 2^31
+  if (static_cast<long long>(dims->batch) * cache->num_kv_heads * 2 * dims->max_blocks_per_seq >=
+          (1LL << 31) ||
+      grid > kMaxDecodeGrid)
+    return RELATTN_ERR_UNSUPPORTED;
   const WsLayout w = ws_layout(dims, cache, grid);
   if (ws_bytes < w.total) return RELATTN_ERR_WORKSPACE;
   const int g = dims->num_q_heads / cache->num_kv_heads;
@@ -226,7 +253,7 @@ static int prepare_decode(const void* q, const float* rel, const relattn_kv_cach
   while (p.nstages >= 2 && decode_smem_bytes(p.nstages, p.B, p.g, p.dv) > di->smem_optin)
     p.nstages -= 2;
   if (p.nstages < 2) return RELATTN_ERR_UNSUPPORTED;  // batch too large for shared memory
-  if (!cache_maps(cache, &L->tm_k, &L->tm_v)) return RELATTN_ERR_CUDA;
+  if (!decode_cache_maps(cache, &L->tm_k, &L->tm_v)) return RELATTN_ERR_CUDA;
   const cuuint64_t rd[2] = {static_cast<cuuint64_t>(rel_extent),
                             static_cast<cuuint64_t>(dims->batch) * dims->num_q_heads};
   const cuuint64_t rs[1] = {static_cast<cuuint64_t>(rel_extent) * 4};

@@ -76,28 +76,31 @@ struct DecodeSmem {
     M = l + kConsumerWarps * 16 * 4;
     L = M + 16 * 4;
     misc = L + 16 * 4;
-    total = misc + 16;
+    total = misc + 64;
   }
 };
 
-// How the CTA ranges are cut.
+// How the CTA ranges are cut.  All tile indices fit in 32 bits (the host
+// checks batch * kv heads * tiles per sequence < 2^31), so the cut arithmetic
+// is 32-bit: no 64-bit division on the kernel's start-up path.
 struct Plan {
-  long long T;  // tiles of all segments
-  int G;        // CTAs with work: min(gridDim.x, T)
-  int whole;    // 1: cuts snap to segment boundaries
+  int T;      // tiles of all segments
+  int G;      // CTAs with work: min(gridDim.x, T)
+  int whole;  // 1: cuts snap to segment boundaries
+  int tq, tr; // T / G and T % G
 };
 
 // The piece of a CTA's range that falls in one (sequence, KV head) segment.
 struct Piece {
   int b, kvh, i0, n;
-  long long seg_start, seg_end;
+  int seg_start, seg_end;
 };
 
-__device__ __forceinline__ int seq_of(long long f, const int* s_pref, int B, int Hkv) {
+__device__ __forceinline__ int seq_of(int f, const int* s_pref, int B, int Hkv) {
   int lo = 0, hi = B - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (static_cast<long long>(Hkv) * s_pref[mid] <= f)
+    if (Hkv * s_pref[mid] <= f)
       lo = mid;
     else
       hi = mid - 1;
@@ -105,58 +108,178 @@ __device__ __forceinline__ int seq_of(long long f, const int* s_pref, int B, int
   return lo;
 }
 
-__device__ __forceinline__ Piece locate_piece(long long f, long long a1, const int* s_pref,
-                                              const int* s_nt, int B, int Hkv) {
+__device__ __forceinline__ Piece locate_piece(int f, int a1, const int* s_pref, const int* s_nt,
+                                              int B, int Hkv) {
   Piece pc;
   pc.b = seq_of(f, s_pref, B, Hkv);
   const int nt = s_nt[pc.b];
-  const long long off = f - static_cast<long long>(Hkv) * s_pref[pc.b];
-  pc.kvh = static_cast<int>(off / nt);
-  pc.i0 = static_cast<int>(off % nt);
-  pc.seg_start = static_cast<long long>(Hkv) * s_pref[pc.b] +
-                 static_cast<long long>(pc.kvh) * nt;
+  const int off = f - Hkv * s_pref[pc.b];
+  pc.kvh = off / nt;
+  pc.i0 = off - pc.kvh * nt;
+  pc.seg_start = Hkv * s_pref[pc.b] + pc.kvh * nt;
   pc.seg_end = pc.seg_start + nt;
-  pc.n = static_cast<int>(min(a1, pc.seg_end) - f);
+  pc.n = min(a1, pc.seg_end) - f;
   return pc;
 }
 
-// Exact cut c of T tiles into G ranges: floor(c*T/G).
-__device__ __forceinline__ long long exact_cut(int c, const Plan& pl) {
-  return static_cast<long long>(c) * pl.T / pl.G;
+// Exact cut c of T tiles into G ranges: floor(c*T/G) = c*(T/G) + floor(c*(T%G)/G),
+// where c*(T%G) < G*G fits in 32 bits (the host bounds the grid).
+__device__ __forceinline__ int exact_cut(int c, const Plan& pl) {
+  return c * pl.tq + (c * pl.tr) / pl.G;
 }
 
-// CTA owning flat tile f under exact cuts.
-__device__ __forceinline__ int cta_of(long long f, const Plan& pl) {
-  return static_cast<int>(((f + 1) * pl.G - 1) / pl.T);
+// CTA owning flat tile f under exact cuts (split-combine only).
+__device__ __forceinline__ int cta_of(int f, const Plan& pl) {
+  return static_cast<int>((static_cast<long long>(f + 1) * pl.G - 1) / pl.T);
 }
 
 // Start of CTA c's range: the exact cut, snapped to the nearer segment
 // boundary in whole-segment mode.
-__device__ __forceinline__ long long range_cut(int c, const Plan& pl, const int* s_pref,
-                                               const int* s_nt, int B, int Hkv) {
-  long long f = exact_cut(c, pl);
+__device__ __forceinline__ int range_cut(int c, const Plan& pl, const int* s_pref,
+                                         const int* s_nt, int B, int Hkv) {
+  int f = exact_cut(c, pl);
   if (pl.whole && f > 0 && f < pl.T) {
     const int b = seq_of(f, s_pref, B, Hkv);
     const int nt = s_nt[b];
-    const long long base = static_cast<long long>(Hkv) * s_pref[b];
-    const long long s0 = base + (f - base) / nt * nt;
-    const long long s1 = s0 + nt;
+    const int base = Hkv * s_pref[b];
+    const int s0 = base + (f - base) / nt * nt;
+    const int s1 = s0 + nt;
     f = (f - s0 <= s1 - f) ? s0 : s1;
   }
   return f;
 }
 
+// Issued first thing in the kernel, so that the prologue's only dependent
+// global round trip overlaps the set-up: this thread's seq_lens entry, and an
+// L2 prefetch of the block-table row of the segment the CTA most likely owns
+// (segment c of sequence c / Hkv when every segment fits one CTA).
+__device__ __forceinline__ int decode_early_loads(const DecodeParams& p) {
+  const int tid = threadIdx.x;
+  const int len = tid < p.B ? __ldg(p.seq_lens + tid) : 0;
+  if (tid >= 32 && tid < 64) {
+    const int b = blockIdx.x / p.Hkv, line = tid - 32;
+    if (b < p.B && line * 32 < p.max_blocks)
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(p.block_table +
+                                                    static_cast<size_t>(b) * p.max_blocks +
+                                                    line * 32));
+  }
+  return len;
+}
+
+// A CTA's range of flat tiles [a0, a1) and the plan it was cut from.
+struct CtaRange {
+  Plan pl;
+  int a0, a1;
+};
+
+// Fast prologue for B <= 32, run by warp 0 alone (lane b holds sequence b):
+// tile counts, their prefix and the cuts come from shuffles and ballots in
+// registers, with no block-wide barrier on the way to the first copy.  The
+// results are published in shared memory for the other warps.  Same cut
+// arithmetic as range_cut.  len0: seq_lens[lane], already loaded.
+__device__ CtaRange decode_plan_warp(const DecodeParams& p, uint8_t* smem, const DecodeSmem& L,
+                                     int len0) {
+  int* s_len = reinterpret_cast<int*>(smem + L.seqlen);
+  int* s_nt = reinterpret_cast<int*>(smem + L.nt);
+  int* s_pref = reinterpret_cast<int*>(smem + L.pref);
+  int* s_misc = reinterpret_cast<int*>(smem + L.misc);
+  const int lane = threadIdx.x & 31;
+  const bool has = lane < p.B;
+  const int nt = has ? decode_seq(len0, p.window, p.max_blocks).ntiles : 0;
+  if (has && nt == 0 && blockIdx.x == 0) report(p.status, RELATTN_DEV_BAD_LENGTH);
+  int incl = nt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  const int excl = incl - nt;
+  const int total = __shfl_sync(0xffffffffu, incl, 31);
+  const int mx = __reduce_max_sync(0xffffffffu, nt);
+  if (has) {
+    s_len[lane] = len0;
+    s_nt[lane] = nt;
+    s_pref[lane] = excl;
+  }
+  if (lane == 0) {
+    s_pref[p.B] = total;
+    s_misc[0] = mx;
+  }
+  CtaRange cr;
+  Plan& pl = cr.pl;
+  pl.T = p.Hkv * total;
+  pl.G = min(static_cast<int>(gridDim.x), pl.T);
+  pl.whole = pl.G > 0 && static_cast<long long>(mx) * pl.G <=
+                             pl.T + static_cast<long long>(kWholeSlackTiles) * pl.G;
+  pl.tq = pl.G > 0 ? pl.T / pl.G : 0;
+  pl.tr = pl.G > 0 ? pl.T - pl.tq * pl.G : 0;
+  auto cut = [&](int c) -> int {  // range_cut, warp-wide
+    int f = c * pl.tq + (c * pl.tr) / pl.G;
+    if (pl.whole && f > 0 && f < pl.T) {
+      // the last sequence whose prefix is <= f
+      const unsigned m = __ballot_sync(0xffffffffu, has && p.Hkv * excl <= f);
+      const int b = 31 - __clz(m);
+      const int ntb = __shfl_sync(0xffffffffu, nt, b);
+      const int base = p.Hkv * __shfl_sync(0xffffffffu, excl, b);
+      const int s0 = base + (f - base) / ntb * ntb;
+      const int s1 = s0 + ntb;
+      f = (f - s0 <= s1 - f) ? s0 : s1;
+    }
+    return f;
+  };
+  const int c = blockIdx.x;
+  cr.a0 = c < pl.G ? cut(c) : 0;
+  cr.a1 = c < pl.G ? cut(c + 1) : 0;
+  if (lane == 0) {
+    s_misc[2] = pl.T;
+    s_misc[3] = pl.G;
+    s_misc[4] = pl.whole;
+    s_misc[5] = pl.tq;
+    s_misc[6] = pl.tr;
+    s_misc[7] = cr.a0;
+    s_misc[8] = cr.a1;
+  }
+  __syncwarp();
+  return cr;
+}
+
+// The other warps' side of decode_plan_warp, once its results are published.
+__device__ __forceinline__ CtaRange decode_plan_read(const uint8_t* smem, const DecodeSmem& L) {
+  const int* s_misc = reinterpret_cast<const int*>(smem + L.misc);
+  CtaRange cr;
+  cr.pl.T = s_misc[2];
+  cr.pl.G = s_misc[3];
+  cr.pl.whole = s_misc[4];
+  cr.pl.tq = s_misc[5];
+  cr.pl.tr = s_misc[6];
+  cr.a0 = s_misc[7];
+  cr.a1 = s_misc[8];
+  return cr;
+}
+
+// Sequences with an invalid length get zeros (CTA 0, the given threads).
+__device__ __forceinline__ void decode_zero_bad(const DecodeParams& p, const int* s_nt, int t,
+                                                int nthreads) {
+  if (blockIdx.x != 0 || p.out == nullptr) return;
+  const int per = p.Hq * p.dv;
+  for (int b = 0; b < p.B; ++b) {
+    if (s_nt[b] != 0) continue;
+    __nv_bfloat16* o = p.out + static_cast<size_t>(b) * per;
+    for (int i = t; i < per; i += nthreads) o[i] = __float2bfloat16(0.f);
+  }
+}
+
 // Per-CTA prologue: each sequence's tile count, their exclusive prefix and
-// the cut plan.
+// the cut plan.  len0: seq_lens[threadIdx.x], already loaded.
 __device__ Plan decode_prologue(const DecodeParams& p, uint8_t* smem, const DecodeSmem& L,
-                                bool zero_bad) {
+                                bool zero_bad, int len0) {
   int* s_len = reinterpret_cast<int*>(smem + L.seqlen);
   int* s_nt = reinterpret_cast<int*>(smem + L.nt);
   int* s_pref = reinterpret_cast<int*>(smem + L.pref);
   int* s_misc = reinterpret_cast<int*>(smem + L.misc);
   const int tid = threadIdx.x;
   for (int b = tid; b < p.B; b += blockDim.x) {
-    const int len = p.seq_lens[b];
+    const int len = b == tid ? len0 : p.seq_lens[b];
     const DecodeSeq s = decode_seq(len, p.window, p.max_blocks);
     s_len[b] = len;
     s_nt[b] = s.ntiles;
@@ -190,19 +313,14 @@ __device__ Plan decode_prologue(const DecodeParams& p, uint8_t* smem, const Deco
     }
   }
   __syncthreads();
-  if (zero_bad && blockIdx.x == 0 && p.out != nullptr) {
-    const int per = p.Hq * p.dv;  // sequences with an invalid length get zeros
-    for (int b = 0; b < p.B; ++b) {
-      if (s_nt[b] != 0) continue;
-      __nv_bfloat16* o = p.out + static_cast<size_t>(b) * per;
-      for (int i = tid; i < per; i += blockDim.x) o[i] = __float2bfloat16(0.f);
-    }
-  }
+  if (zero_bad) decode_zero_bad(p, s_nt, tid, blockDim.x);
   Plan pl;
-  pl.T = static_cast<long long>(p.Hkv) * s_pref[p.B];
-  pl.G = static_cast<int>(min(static_cast<long long>(gridDim.x), pl.T));
+  pl.T = p.Hkv * s_pref[p.B];
+  pl.G = min(static_cast<int>(gridDim.x), pl.T);
   pl.whole = pl.G > 0 && static_cast<long long>(s_misc[0]) * pl.G <=
                              pl.T + static_cast<long long>(kWholeSlackTiles) * pl.G;
+  pl.tq = pl.G > 0 ? pl.T / pl.G : 0;
+  pl.tr = pl.G > 0 ? pl.T - pl.tq * pl.G : 0;
   return pl;
 }
 
@@ -228,6 +346,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   const int* s_pref = reinterpret_cast<const int*>(smem + L.pref);
   int* s_misc = reinterpret_cast<int*>(smem + L.misc);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int len0 = decode_early_loads(p);
 
   if (tid == 0) {
     for (int s = 0; s < ns; ++s) {
@@ -244,15 +363,36 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     tma_prefetch_desc(&tm_v);
     tma_prefetch_desc(&tm_rel);
   }
-  // query rows g..15 of both buffers stay zero
-  for (int i = tid; i < 2 * kQBufBytes / 16; i += blockDim.x)
-    reinterpret_cast<uint4*>(smem + L.qbuf)[i] = make_uint4(0, 0, 0, 0);
+  // Query rows g..15 of both buffers stay zero.  With the warp-0 prologue
+  // (B <= 32) the producer starts its copies before the other warps reach a
+  // barrier, so warp 0 clears the buffers itself.
+  {
+    const int zt = p.B <= 32 ? 32 : kDecodeThreads;
+    if (tid < zt)
+      for (int i = tid; i < 2 * kQBufBytes / 16; i += zt)
+        reinterpret_cast<uint4*>(smem + L.qbuf)[i] = make_uint4(0, 0, 0, 0);
+  }
   fence_proxy_async_smem();
-  const Plan pl = decode_prologue(p, smem, L, true);
+  CtaRange cr;
+  if (p.B <= 32) {
+    // warp 0 plans alone and lets the consumers go with a non-blocking arrive
+    if (warp == 0) {
+      cr = decode_plan_warp(p, smem, L, len0);
+      named_barrier_arrive(2, kDecodeThreads);
+    } else {
+      named_barrier(2, kDecodeThreads);
+      cr = decode_plan_read(smem, L);
+      decode_zero_bad(p, s_nt, tid - 32, kConsumerThreads);
+    }
+  } else {
+    cr.pl = decode_prologue(p, smem, L, true, len0);
+    cr.a0 = range_cut(blockIdx.x, cr.pl, s_pref, s_nt, p.B, p.Hkv);
+    cr.a1 = range_cut(blockIdx.x + 1, cr.pl, s_pref, s_nt, p.B, p.Hkv);
+  }
+  const Plan pl = cr.pl;
   if (static_cast<int>(blockIdx.x) >= pl.G) return;
   const int c = blockIdx.x;
-  const long long a0 = range_cut(c, pl, s_pref, s_nt, p.B, p.Hkv);
-  const long long a1 = range_cut(c + 1, pl, s_pref, s_nt, p.B, p.Hkv);
+  const int a0 = cr.a0, a1 = cr.a1;
   const int stage_tx = 16384 + kTileKeys * DV * 2;
   const int rel_tx = g * kRelBoxW * 4;
   const int q_tx = 2 * g * 64 * 2;
@@ -262,7 +402,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     int n = 0;     // CTA tile counter
     int k = 0;     // CTA piece counter
     bool abort = false;
-    for (long long f = a0; f < a1 && !abort; ++k) {
+    for (int f = a0; f < a1 && !abort; ++k) {
       const Piece pc = locate_piece(f, a1, s_pref, s_nt, p.B, p.Hkv);
       const DecodeSeq sq = decode_seq(s_len[pc.b], p.window, p.max_blocks);
       const int* trow = p.block_table + static_cast<size_t>(pc.b) * p.max_blocks;
@@ -280,18 +420,25 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         }
       }
       abort = __shfl_sync(0xffffffffu, bad, 0) != 0;
+      bad = 0;
       for (int c0 = 0; c0 < pc.n && !abort; c0 += 32) {
         const int cn = min(32, pc.n - c0);
         const int tile0 = sq.tile_first + pc.i0 + c0;
         const int blk0 = tile0 >> 1;
         const int nb = ((tile0 + cn - 1) >> 1) - blk0 + 1;
         const int myid = lane < nb ? __ldg(trow + blk0 + lane) : 0;
-        for (int j = 0; j < cn; ++j, ++n) {
+        // Batches of at most ns tiles, one per lane: their stages are all
+        // different, so each lane waits on its own stage one phase ahead at
+        // most, and the copies of a batch go out in one pass of the warp.
+        for (int jb = 0; jb < cn && !abort; jb += ns) {
+          const int bn = min(ns, cn - jb);
+          const int j = jb + (lane < bn ? lane : 0);
           const int tile = tile0 + j;
           const int id = __shfl_sync(0xffffffffu, myid, (tile >> 1) - blk0);
-          const int stage = n % ns;
-          if (lane == 0) {
-            if (!mbar_wait(&empty[stage], ((n / ns) & 1) ^ 1)) {
+          if (lane < bn) {
+            const int nn = n + lane;
+            const int stage = nn % ns;
+            if (!mbar_wait(&empty[stage], ((nn / ns) & 1) ^ 1)) {
               report(p.status, RELATTN_DEV_WAIT_TIMEOUT);
               bad = 1;
             } else {
@@ -304,10 +451,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
                 mbar_arrive_expect_tx(&full[stage], stage_tx + (need_rel ? rel_tx : 0));
                 uint8_t* st = smem + L.stages + stage * L.stage_bytes;
                 const int row = id * kBlockSize + (tile & 1) * kTileKeys;
-                tma_load_3d(st, &tm_k, &full[stage], 0, pc.kvh, row);
-                tma_load_3d(st + 8192, &tm_k, &full[stage], 64, pc.kvh, row);
-                tma_load_3d(st + 16384, &tm_v, &full[stage], 0, pc.kvh, row);
-                if (DV == 128) tma_load_3d(st + 24576, &tm_v, &full[stage], 64, pc.kvh, row);
+                tma_load_4d(st, &tm_k, &full[stage], 0, row, 0, pc.kvh);
+                tma_load_4d(st + 16384, &tm_v, &full[stage], 0, row, 0, pc.kvh);
                 if (need_rel)
                   tma_load_2d(smem + L.rel + stage * L.rel_bytes, &tm_rel, &full[stage], dmin & ~3,
                               pc.b * p.Hq + pc.kvh * g);
@@ -317,8 +462,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
               }
             }
           }
-          abort = __shfl_sync(0xffffffffu, bad, 0) != 0;
-          if (abort) break;
+          n += bn;
+          abort = __any_sync(0xffffffffu, bad != 0);
         }
       }
       f += pc.n;
@@ -345,7 +490,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   int k = 0;
   bool abort = false;
 
-  for (long long f = a0; f < a1 && !abort; ++k) {
+  for (int f = a0; f < a1 && !abort; ++k) {
     const Piece pc = locate_piece(f, a1, s_pref, s_nt, p.B, p.Hkv);
     const DecodeSeq sq = decode_seq(s_len[pc.b], p.window, p.max_blocks);
     const int h0 = pc.kvh * g;
@@ -356,6 +501,21 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       break;
     }
     const uint32_t qbase = smem_u32(smem + L.qbuf + qb * kQBufBytes);
+    // this warp's A fragments of the query rows for all eight k-steps: the
+    // query is the same for every tile of the piece
+    uint32_t qa[8][4];
+    {
+      const int mi = lane >> 3;
+      const int qrow = (mi & 1) * 8 + (lane & 7);
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        const int qchunk = ks * 2 + (mi >> 1);
+        ldsm_x4(qbase + (qchunk >> 3) * 2048 + sw128(qrow, qchunk & 7), qa[ks][0], qa[ks][1],
+                qa[ks][2], qa[ks][3]);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&qempty[qb]);  // query rows no longer needed
 
     float m_[2] = {kNegInf, kNegInf}, l_[2] = {0.f, 0.f};
     float o[DV / 8][4];
@@ -381,18 +541,13 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         {
           const int mi = lane >> 3;
           const int key = 16 * cw + (mi >> 1) * 8 + (lane & 7);
-          const int qrow = (mi & 1) * 8 + (lane & 7);
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks) {
-            uint32_t a[4];
-            const int qchunk = ks * 2 + (mi >> 1);
-            ldsm_x4(qbase + (qchunk >> 3) * 2048 + sw128(qrow, qchunk & 7), a[0], a[1], a[2],
-                    a[3]);
             const int chunk = ks * 2 + (mi & 1);
             uint32_t b0, b1, b2, b3;
             ldsm_x4(kbase + (chunk >> 3) * 8192 + sw128(key, chunk & 7), b0, b1, b2, b3);
-            mma_16816(s[0], a, b0, b1);
-            mma_16816(s[1], a, b2, b3);
+            mma_16816(s[0], qa[ks], b0, b1);
+            mma_16816(s[1], qa[ks], b2, b3);
           }
         }
         // logits in log2 units: (q.k/sqrt(d) + rel) * log2(e)
@@ -465,8 +620,6 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     }
     if (abort) break;
     n_base += pc.n;
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&qempty[qb]);  // query rows no longer needed
 
     // ---- merge the eight consumer warps of this piece
 #pragma unroll
@@ -571,15 +724,24 @@ __global__ void __launch_bounds__(128) decode_walk_kernel(const DecodeParams p) 
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const DecodeSmem L(0, p.B, 1, 64);
-  const Plan pl = decode_prologue(p, smem, L, false);
-  if (static_cast<int>(blockIdx.x) >= pl.G || threadIdx.x != 0) return;
   const int* s_len = reinterpret_cast<const int*>(smem + L.seqlen);
   const int* s_nt = reinterpret_cast<const int*>(smem + L.nt);
   const int* s_pref = reinterpret_cast<const int*>(smem + L.pref);
+  const int len0 = decode_early_loads(p);
+  CtaRange cr;
+  if (p.B <= 32) {  // the decode kernel's fast prologue, run the same way
+    if (threadIdx.x >= 32) return;
+    cr = decode_plan_warp(p, smem, L, len0);
+  } else {
+    cr.pl = decode_prologue(p, smem, L, false, len0);
+    cr.a0 = range_cut(blockIdx.x, cr.pl, s_pref, s_nt, p.B, p.Hkv);
+    cr.a1 = range_cut(blockIdx.x + 1, cr.pl, s_pref, s_nt, p.B, p.Hkv);
+  }
+  const Plan pl = cr.pl;
+  if (static_cast<int>(blockIdx.x) >= pl.G || threadIdx.x != 0) return;
   const int c = blockIdx.x;
-  const long long a0 = range_cut(c, pl, s_pref, s_nt, p.B, p.Hkv);
-  const long long a1 = range_cut(c + 1, pl, s_pref, s_nt, p.B, p.Hkv);
-  for (long long f = a0; f < a1;) {
+  const int a0 = cr.a0, a1 = cr.a1;
+  for (int f = a0; f < a1;) {
     const Piece pc = locate_piece(f, a1, s_pref, s_nt, p.B, p.Hkv);
     const DecodeSeq sq = decode_seq(s_len[pc.b], p.window, p.max_blocks);
     const int* trow = p.block_table + static_cast<size_t>(pc.b) * p.max_blocks;
