@@ -35,6 +35,7 @@ constexpr int kDecodeThreads = 32 * (1 + kConsumerWarps);
 constexpr int kConsumerThreads = 32 * kConsumerWarps;
 constexpr int kWholeSlackTiles = 4;  // tolerated imbalance to avoid a split
 constexpr int kQBufBytes = 4096;     // 16 rows x 256 B as two swizzled halves
+constexpr int kSlicePad = 8;         // floats of padding per merge-slice row (bank spread)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kNegInf = -__builtin_huge_valf();
 
@@ -66,7 +67,7 @@ struct DecodeSmem {
     stages = qbuf + 2 * kQBufBytes;
     rel = stages + nstages * stage_bytes;
     slices = rel + nstages * rel_bytes;
-    bars = (slices + kConsumerWarps * g * dv * 4 + 15) & ~15;
+    bars = (slices + kConsumerWarps * g * (dv + kSlicePad) * 4 + 15) & ~15;
     valid = bars + (2 * nstages + 4) * 8;
     seqlen = valid + nstages * 4;
     nt = seqlen + B * 4;
@@ -166,10 +167,13 @@ __device__ __forceinline__ int decode_early_loads(const DecodeParams& p) {
   return len;
 }
 
-// A CTA's range of flat tiles [a0, a1) and the plan it was cut from.
+// A CTA's range of flat tiles [a0, a1) and the plan it was cut from;
+// first: the piece starting at a0 (valid when has_first).
 struct CtaRange {
   Plan pl;
   int a0, a1;
+  Piece first;
+  bool has_first;
 };
 
 // Fast prologue for B <= 32, run by warp 0 alone (lane b holds sequence b):
@@ -230,6 +234,21 @@ __device__ CtaRange decode_plan_warp(const DecodeParams& p, uint8_t* smem, const
   const int c = blockIdx.x;
   cr.a0 = c < pl.G ? cut(c) : 0;
   cr.a1 = c < pl.G ? cut(c + 1) : 0;
+  // the first piece, as locate_piece(a0, a1) finds it
+  cr.has_first = cr.a0 < cr.a1;
+  if (cr.has_first) {
+    const unsigned m = __ballot_sync(0xffffffffu, has && p.Hkv * excl <= cr.a0);
+    Piece& pc = cr.first;
+    pc.b = 31 - __clz(m);
+    const int ntb = __shfl_sync(0xffffffffu, nt, pc.b);
+    const int base = p.Hkv * __shfl_sync(0xffffffffu, excl, pc.b);
+    const int off = cr.a0 - base;
+    pc.kvh = off / ntb;
+    pc.i0 = off - pc.kvh * ntb;
+    pc.seg_start = base + pc.kvh * ntb;
+    pc.seg_end = pc.seg_start + ntb;
+    pc.n = min(cr.a1, pc.seg_end) - cr.a0;
+  }
   if (lane == 0) {
     s_misc[2] = pl.T;
     s_misc[3] = pl.G;
@@ -388,6 +407,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     cr.pl = decode_prologue(p, smem, L, true, len0);
     cr.a0 = range_cut(blockIdx.x, cr.pl, s_pref, s_nt, p.B, p.Hkv);
     cr.a1 = range_cut(blockIdx.x + 1, cr.pl, s_pref, s_nt, p.B, p.Hkv);
+    cr.has_first = false;
   }
   const Plan pl = cr.pl;
   if (static_cast<int>(blockIdx.x) >= pl.G) return;
@@ -403,7 +423,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     int k = 0;     // CTA piece counter
     bool abort = false;
     for (int f = a0; f < a1 && !abort; ++k) {
-      const Piece pc = locate_piece(f, a1, s_pref, s_nt, p.B, p.Hkv);
+      const Piece pc = (k == 0 && cr.has_first && warp == 0)
+                           ? cr.first
+                           : locate_piece(f, a1, s_pref, s_nt, p.B, p.Hkv);
       const DecodeSeq sq = decode_seq(s_len[pc.b], p.window, p.max_blocks);
       const int* trow = p.block_table + static_cast<size_t>(pc.b) * p.max_blocks;
       int bad = 0;
@@ -430,37 +452,45 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         // Batches of at most ns tiles, one per lane: their stages are all
         // different, so each lane waits on its own stage one phase ahead at
         // most, and the copies of a batch go out in one pass of the warp.
+        // K, V and rel of tile `tile` (CTA tile nn) into its stage; 1 on a
+        // wait timeout
+        auto issue = [&](int nn, int tile, int id) -> int {
+          const int stage = nn % ns;
+          if (!mbar_wait(&empty[stage], ((nn / ns) & 1) ^ 1)) {
+            report(p.status, RELATTN_DEV_WAIT_TIMEOUT);
+            return 1;
+          }
+          const bool ok = id >= 0 && id < p.num_blocks;
+          s_valid[stage] = ok ? 1 : 0;
+          if (ok) {
+            const int key0 = tile * kTileKeys;
+            const int dmin = sq.p - key0 - (kTileKeys - 1);
+            const bool need_rel = dmin < p.rel_extent;
+            mbar_arrive_expect_tx(&full[stage], stage_tx + (need_rel ? rel_tx : 0));
+            uint8_t* st = smem + L.stages + stage * L.stage_bytes;
+            const int row = id * kBlockSize + (tile & 1) * kTileKeys;
+            tma_load_4d(st, &tm_k, &full[stage], 0, row, 0, pc.kvh);
+            tma_load_4d(st + 16384, &tm_v, &full[stage], 0, row, 0, pc.kvh);
+            if (need_rel)
+              tma_load_2d(smem + L.rel + stage * L.rel_bytes, &tm_rel, &full[stage], dmin & ~3,
+                          pc.b * p.Hq + pc.kvh * g);
+          } else {
+            report(p.status, RELATTN_DEV_BAD_BLOCK_ID);
+            mbar_arrive(&full[stage]);
+          }
+          return 0;
+        };
         for (int jb = 0; jb < cn && !abort; jb += ns) {
           const int bn = min(ns, cn - jb);
           const int j = jb + (lane < bn ? lane : 0);
           const int tile = tile0 + j;
           const int id = __shfl_sync(0xffffffffu, myid, (tile >> 1) - blk0);
-          if (lane < bn) {
-            const int nn = n + lane;
-            const int stage = nn % ns;
-            if (!mbar_wait(&empty[stage], ((nn / ns) & 1) ^ 1)) {
-              report(p.status, RELATTN_DEV_WAIT_TIMEOUT);
-              bad = 1;
-            } else {
-              const bool ok = id >= 0 && id < p.num_blocks;
-              s_valid[stage] = ok ? 1 : 0;
-              if (ok) {
-                const int key0 = tile * kTileKeys;
-                const int dmin = sq.p - key0 - (kTileKeys - 1);
-                const bool need_rel = dmin < p.rel_extent;
-                mbar_arrive_expect_tx(&full[stage], stage_tx + (need_rel ? rel_tx : 0));
-                uint8_t* st = smem + L.stages + stage * L.stage_bytes;
-                const int row = id * kBlockSize + (tile & 1) * kTileKeys;
-                tma_load_4d(st, &tm_k, &full[stage], 0, row, 0, pc.kvh);
-                tma_load_4d(st + 16384, &tm_v, &full[stage], 0, row, 0, pc.kvh);
-                if (need_rel)
-                  tma_load_2d(smem + L.rel + stage * L.rel_bytes, &tm_rel, &full[stage], dmin & ~3,
-                              pc.b * p.Hq + pc.kvh * g);
-              } else {
-                report(p.status, RELATTN_DEV_BAD_BLOCK_ID);
-                mbar_arrive(&full[stage]);
-              }
-            }
+          if (c0 == 0 && jb == 0) {
+            // the piece's first tile goes out alone, so that its data leads
+            if (lane == 0) bad |= issue(n, tile, id);
+            if (lane > 0 && lane < bn) bad |= issue(n + lane, tile, id);
+          } else if (lane < bn) {
+            bad |= issue(n + lane, tile, id);
           }
           n += bn;
           abort = __any_sync(0xffffffffu, bad != 0);
@@ -640,7 +670,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
 #pragma unroll
       for (int w = 1; w < kConsumerWarps; ++w) M = fmaxf(M, s_m[w * 16 + row]);
       const float fct = M == kNegInf ? 0.f : ex2(m_[rr] - M);
-      float* sl = slices + (cwarp * g + row) * DV + cq * 2;
+      float* sl = slices + (cwarp * g + row) * (DV + kSlicePad) + cq * 2;
 #pragma unroll
       for (int nd = 0; nd < DV / 8; ++nd)
         *reinterpret_cast<float2*>(sl + nd * 8) =
@@ -666,7 +696,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       float v0 = 0.f, v1 = 0.f;
 #pragma unroll
       for (int w = 0; w < kConsumerWarps; ++w) {
-        const float2 v = *reinterpret_cast<const float2*>(slices + (w * g + row) * DV + col);
+        const float2 v =
+            *reinterpret_cast<const float2*>(slices + (w * g + row) * (DV + kSlicePad) + col);
         v0 += v.x;
         v1 += v.y;
       }
