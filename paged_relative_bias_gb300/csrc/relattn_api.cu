@@ -225,6 +225,7 @@ static int prepare_decode(const void* q, const float* rel, const relattn_kv_cach
   DecodeParams& p = L->p;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   p.q = static_cast<const __nv_bfloat16*>(q);
+  p.rel = rel;
   p.block_table = block_table;
   p.seq_lens = seq_lens;
   p.out = static_cast<__nv_bfloat16*>(out);

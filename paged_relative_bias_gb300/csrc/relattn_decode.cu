@@ -150,19 +150,34 @@ __device__ __forceinline__ int range_cut(int c, const Plan& pl, const int* s_pre
   return f;
 }
 
+__device__ __forceinline__ void prefetch_l2(const void* ptr) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
+}
+
 // Issued first thing in the kernel, so that the prologue's only dependent
-// global round trip overlaps the set-up: this thread's seq_lens entry, and an
-// L2 prefetch of the block-table row of the segment the CTA most likely owns
-// (segment c of sequence c / Hkv when every segment fits one CTA).
+// global round trip overlaps the set-up: this thread's seq_lens entry, and L2
+// prefetches for the segment the CTA most likely owns (segment c: sequence
+// c / Hkv, KV head c % Hkv, which holds when every segment fits one CTA) --
+// its block-table row, its g query rows and the rel rows its window needs.
+// A wrong guess costs only the prefetched bytes.
 __device__ __forceinline__ int decode_early_loads(const DecodeParams& p) {
   const int tid = threadIdx.x;
   const int len = tid < p.B ? __ldg(p.seq_lens + tid) : 0;
-  if (tid >= 32 && tid < 64) {
-    const int b = blockIdx.x / p.Hkv, line = tid - 32;
-    if (b < p.B && line * 32 < p.max_blocks)
-      asm volatile("prefetch.global.L2 [%0];" ::"l"(p.block_table +
-                                                    static_cast<size_t>(b) * p.max_blocks +
-                                                    line * 32));
+  const int b = blockIdx.x / p.Hkv, kvh = blockIdx.x - (blockIdx.x / p.Hkv) * p.Hkv;
+  if (b < p.B && p.rel != nullptr) {
+    const int lane = tid & 31;
+    const size_t row0 = static_cast<size_t>(b) * p.Hq + static_cast<size_t>(kvh) * p.g;
+    if (tid >= 32 && tid < 64) {  // block-table row: 32 lines of 128 bytes at most
+      if (lane * 32 < p.max_blocks)
+        prefetch_l2(p.block_table + static_cast<size_t>(b) * p.max_blocks + lane * 32);
+    } else if (tid >= 64 && tid < 96) {  // query rows: 2 lines each
+      if (lane < 2 * p.g) prefetch_l2(p.q + (row0 + lane / 2) * 128 + (lane & 1) * 64);
+    } else if (tid >= 96 && tid < 128) {  // rel rows: distances [0, min(E, W or E))
+      const int dist = p.window > 0 ? min(p.rel_extent, p.window) : p.rel_extent;
+      const int lines = (dist + 31) / 32;  // 32 floats per line
+      for (int i = lane; i < p.g * lines && i < 4 * 32; i += 32)
+        prefetch_l2(p.rel + (row0 + i / lines) * p.rel_extent + (i % lines) * 32);
+    }
   }
   return len;
 }

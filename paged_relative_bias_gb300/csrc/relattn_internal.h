@@ -15,6 +15,7 @@ constexpr int kRelBoxW = 68;     // distances per rel box: 64 keys + alignment
 
 struct DecodeParams {
   const __nv_bfloat16* q;      // [B][Hq][128]
+  const float* rel;            // [B][Hq][E]
   const int32_t* block_table;  // [B][max_blocks]
   const int32_t* seq_lens;     // [B]
   __nv_bfloat16* out;          // [B][Hq][dv]
