@@ -208,6 +208,24 @@ __device__ int prefill_prologue(const PrefillParams& p, uint8_t* smem, const Pre
   return s_qpref[p.B] * p.Hq;
 }
 
+// x[c] = s[c] * scale + rel for the 64 columns of one query row, from 17
+// aligned 16-byte loads.  p4 points A floats before the row's lowest needed
+// distance (the one of column 63); distances rise towards column 0.
+template <int A>
+__device__ __forceinline__ void rel_fma(float (&x)[64], const uint32_t (&sr)[64],
+                                        const float4* p4, float scale) {
+#pragma unroll
+  for (int w = 0; w < 17; ++w) {
+    const float4 v = p4[w];
+    const float f[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int t = 4 * w + e - A;  // distance above the lowest
+      if (t >= 0 && t < 64) x[63 - t] = fmaf(__uint_as_float(sr[63 - t]), scale, f[e]);
+    }
+  }
+}
+
 template <int DV>
 __global__ void __launch_bounds__(kPfThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -389,8 +407,12 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     if (!mbar_wait(&bars[kDrain], 0)) report(p.status, RELATTN_DEV_WAIT_TIMEOUT);
   } else if (warp >= 2 && warp <= 5) {
     // ------------------------------------------------------------ softmax
+    // Thread (q4, lane) owns TMEM lane 32 q4 + lane and puts query row
+    // r = 4 lane + q4 there: each warp takes every fourth row, so all its
+    // lanes see the same 16-byte alignment of their rows in the rel boxes.
     const int q4 = warp & 3;  // TMEM lane quarter this warp may access
-    const int r = 32 * q4 + lane;
+    const int r = 4 * lane + q4;
+    const int rbox = r / kRelBoxRows, rrow = r % kRelBoxRows;  // row's rel box and row in it
     const uint32_t tl = tbase + (static_cast<uint32_t>(32 * q4) << 16);
     int n = 0, e = 0, items = 0;  // key tiles and ring entries consumed
     bool fail = false;
@@ -465,12 +487,18 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         if (!slot) { ok = false; break; }
         float x[64];
         if (it.P0 - j0 - (kTileKeys - 1) < p.rel_extent) {
-          // box column of key j0 + c is (P - j0 - xq) - c, xq the box's first distance
-          const int xq = (it.P0 + kRelBoxRows * q4 - j0 - (kTileKeys - 1)) & ~3;
-          const float* rb = reinterpret_cast<const float*>(slot + q4 * kRelBoxBytes) +
-                            lane * kRelBoxCols + (dc - xq);
-#pragma unroll
-          for (int c = 0; c < 64; ++c) x[c] = fmaf(__uint_as_float(sr[c]), scale, rb[-c]);
+          // A box starts at distance (P0 + 32 box - j0 - 63) rounded down to 4,
+          // so column 63's distance sits rrow + ((P0 + 1) & 3) into this row.
+          const int col = rrow + ((it.P0 + 1) & 3);
+          const float4* p4 = reinterpret_cast<const float4*>(
+              reinterpret_cast<const float*>(slot + rbox * kRelBoxBytes) + rrow * kRelBoxCols +
+              (col & ~3));
+          switch (col & 3) {  // the same for every lane of the warp
+            case 0: rel_fma<0>(x, sr, p4, scale); break;
+            case 1: rel_fma<1>(x, sr, p4, scale); break;
+            case 2: rel_fma<2>(x, sr, p4, scale); break;
+            default: rel_fma<3>(x, sr, p4, scale); break;
+          }
         } else {  // every distance is past rel_extent: no bias
 #pragma unroll
           for (int c = 0; c < 64; ++c) x[c] = __uint_as_float(sr[c]) * scale;
@@ -538,11 +566,11 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         if (!qs) { fail = true; break; }
         load_q(qs, e + 1);
       }
-      // O / l -> bf16, through this warp's part of the scratch slot so that
-      // the global stores are whole rows (16 lanes per 256-byte row).
+      // O / l -> bf16, through the scratch slot (the tile's 128 rows, 16-byte
+      // chunks swizzled by row / 4) so that the global stores are whole rows
+      // (16 lanes per 256-byte row).
       uint8_t* scr = slot_wait(e);
       if (!scr) { fail = true; break; }
-      scr += q4 * (32 * DV * 2);
       const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll 1
       for (int c0 = 0; c0 < DV; c0 += 32) {
@@ -557,20 +585,20 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           w.z = pack_bf16(__uint_as_float(o[8 * i + 4]) * inv, __uint_as_float(o[8 * i + 5]) * inv);
           w.w = pack_bf16(__uint_as_float(o[8 * i + 6]) * inv, __uint_as_float(o[8 * i + 7]) * inv);
           const int j = c0 / 8 + i;  // 16-byte chunk of the row
-          *reinterpret_cast<uint4*>(scr + lane * (DV * 2) + ((j ^ (lane & 7)) << 4)) = w;
+          *reinterpret_cast<uint4*>(scr + r * (DV * 2) + ((j ^ ((r >> 2) & 7)) << 4)) = w;
         }
       }
       tc_fence_before();  // O is read before the next item's first PV overwrites it
-      __syncwarp();
+      named_barrier(1, 128);  // the four softmax warps: every row is in the scratch
+      // whole-row stores: this warp takes rows [32 q4, 32 q4 + 32)
       constexpr int kCpr = DV / 8;     // 16-byte chunks per row
       constexpr int kRpi = 32 / kCpr;  // rows per store instruction
 #pragma unroll
       for (int i = 0; i < kCpr; ++i) {
-        const int row = i * kRpi + lane / kCpr;
+        const int rr = 32 * q4 + i * kRpi + lane / kCpr;
         const int ch = lane % kCpr;
         const uint4 v =
-            *reinterpret_cast<const uint4*>(scr + row * (DV * 2) + ((ch ^ (row & 7)) << 4));
-        const int rr = 32 * q4 + row;
+            *reinterpret_cast<const uint4*>(scr + rr * (DV * 2) + ((ch ^ ((rr >> 2) & 7)) << 4));
         if (rr < it.rows)
           *reinterpret_cast<uint4*>(
               p.out + (static_cast<size_t>(it.r0 + rr) * p.Hq + it.h) * DV + ch * 8) = v;
