@@ -38,6 +38,11 @@ there is no blocking, fusion or reordering):
 * Decode: ``seq_lens[b]`` counts the current token, whose key and value are
   already in the cache, so the query position is ``seq_lens[b] - 1``
   (reading).
+* Multi-token decode (verification of speculative drafts): the k newest
+  tokens of a sequence, positions ``seq_lens[b] - k .. seq_lens[b] - 1``,
+  each attend causally over the cache, which already holds all k keys
+  ("vLLM TML Inkling Support", section "TML Inkling Model Architecture": up
+  to 9 tokens per step; reading: ``seq_lens`` counts all k tokens).
 * Softmax scale ``1/sqrt(d_qk)`` also when ``d_v != d_qk`` ("Inkling on Two
   DGX Sparks", section "Wall 1": head_dim 128, v_head_dim 64).
 
@@ -261,6 +266,48 @@ def decode(q, rel, k_cache, v_cache, block_table, seq_lens, window: int,
             for h in hs:
                 bias = rel_bias(rel[b, h], P, keys, rel_extent)
                 out[b, h] = attend(q[b, h], K, V, bias, d_qk)
+    return out
+
+
+def decode_multi(q, rel, k_cache, v_cache, block_table, seq_lens, window: int,
+                 rel_extent: int, batch=None, tokens=None, heads=None) -> np.ndarray:
+    """Multi-token decode, the verification step of speculative decoding.
+
+    The k newest tokens of sequence b each attend over the paged cache:
+    token i sits at position ``seq_lens[b] - k + i`` and sees keys
+    ``max(0, P - W + 1) .. P``, causal and windowed.  The keys and values of
+    all k tokens are already in the cache ("vLLM TML Inkling Support",
+    section "TML Inkling Model Architecture": chained MTP heads propose up to
+    9 tokens per forward step; "Inkling 2 Small on vLLM", section "vLLM
+    integration and optimisation": one kernel serves decode and
+    verification, with the heads of a KV group packed into one tile).
+    Reading (pages silent): ``seq_lens`` counts all k tokens, as it counts
+    the one token of a decode step.
+
+    q ``[B, k, Hq, d_qk]``, rel ``[B, k, Hq, E]``.  Returns float64
+    ``[B, k, Hq, d_v]``; entries not selected by ``batch`` / ``tokens`` /
+    ``heads`` are left NaN.
+    """
+    B, kq, Hq, d_qk = q.shape
+    Hkv = k_cache.shape[2]
+    g = Hq // Hkv
+    d_v = v_cache.shape[3]
+    out = np.full((B, kq, Hq, d_v), np.nan)
+    for b in (range(B) if batch is None else batch):
+        L = int(seq_lens[b])
+        for i in (range(kq) if tokens is None else tokens):
+            P = L - kq + i
+            lo, hi = visible_keys(P, window)
+            keys = np.arange(lo, hi + 1)
+            for kvh in range(Hkv):
+                hs = [h for h in range(kvh * g, (kvh + 1) * g)
+                      if heads is None or h in heads]
+                if not hs:
+                    continue
+                K, V = gather_kv(k_cache, v_cache, block_table[b], keys, kvh)
+                for h in hs:
+                    bias = rel_bias(rel[b, i, h], P, keys, rel_extent)
+                    out[b, i, h] = attend(q[b, i, h], K, V, bias, d_qk)
     return out
 
 

@@ -447,3 +447,66 @@ def test_cache_write_scatter_brute_force():
             if (b, s) not in touched:
                 assert np.array_equal(kc2[b, s], kc[b, s])
                 assert np.array_equal(vc2[b, s], vc[b, s])
+
+
+# ---------------------------------------------------------------------------
+# multi-token decode (verification)
+# ---------------------------------------------------------------------------
+
+def random_multi_case(seed, L, k, Hq=4, Hkv=2, d=16, dv=8, E=64, pool_extra=2):
+    c = random_decode_case(seed, L, Hq=Hq, Hkv=Hkv, d=d, dv=dv, E=E, pool_extra=pool_extra)
+    r = rng(seed + 1000)
+    c["qm"] = r.standard_normal((1, k, Hq, d))
+    c["relm"] = r.standard_normal((1, k, Hq, E))
+    return c
+
+
+def test_decode_multi_one_token_equals_decode():
+    c = random_multi_case(51, 300, 1)
+    for W, E in ((0, 64), (100, 64), (1, 4)):
+        multi = O.decode_multi(c["qm"], c["relm"], c["kc"], c["vc"], c["table"],
+                               c["seq_lens"], W, E)
+        dec = O.decode(c["qm"][:, 0], c["relm"][:, 0], c["kc"], c["vc"], c["table"],
+                       c["seq_lens"], W, E)
+        assert np.array_equal(multi[:, 0], dec)
+
+
+@pytest.mark.parametrize("k,W", [(2, 0), (4, 64), (9, 100), (5, 1)])
+def test_decode_multi_token_equals_decode_at_its_own_length(k, W):
+    """Token i sees exactly what a one-token decode at length L - k + i + 1
+    sees: later tokens' keys in the cache must not leak into earlier rows."""
+    L = 260
+    c = random_multi_case(52 + k, L, k)
+    multi = O.decode_multi(c["qm"], c["relm"], c["kc"], c["vc"], c["table"],
+                           c["seq_lens"], W, 64)
+    for i in range(k):
+        dec = O.decode(c["qm"][:, i], c["relm"][:, i], c["kc"], c["vc"], c["table"],
+                       np.array([L - k + i + 1]), W, 64)
+        np.testing.assert_allclose(multi[:, i], dec, atol=1e-13, rtol=0)
+
+
+@pytest.mark.parametrize("L,k,W,E", [(9, 9, 0, 16), (200, 4, 0, 300), (200, 7, 64, 40),
+                                     (260, 3, 100, 64)])
+def test_decode_multi_equals_float64_sdpa(L, k, W, E):
+    c = random_multi_case(60 + L + k, L, k, E=E, dv=6)
+    out = O.decode_multi(c["qm"], c["relm"], c["kc"], c["vc"], c["table"],
+                         c["seq_lens"], W, E)
+    ref = sdpa_reference(c["qm"][0], c["Kc"], c["Vc"], c["relm"][0],
+                         list(range(L - k, L)), W, E)
+    np.testing.assert_allclose(out[0], ref, atol=1e-12, rtol=0)
+
+
+def test_decode_multi_equals_prefill_of_the_same_tokens():
+    """A verification step over k cached tokens equals a chunked prefill of
+    those k tokens after the L - k cached before them."""
+    L, k, Hq, Hkv, d, dv, E = 300, 6, 4, 2, 16, 8, 64
+    for W in (0, 100):
+        c = random_multi_case(72, L, k, Hq=Hq, Hkv=Hkv, d=d, dv=dv, E=E)
+        multi = O.decode_multi(c["qm"], c["relm"], c["kc"], c["vc"], c["table"],
+                               c["seq_lens"], W, E)
+        newk = c["Kc"][L - k:L]
+        newv = c["Vc"][L - k:L]
+        pre, kc2, _ = O.prefill(c["qm"][0], newk, newv, c["relm"][0], [0, k], c["kc"], c["vc"],
+                                c["table"], [L - k], W, E)
+        assert np.array_equal(kc2, c["kc"])  # the same keys written back
+        np.testing.assert_allclose(multi[0], pre, atol=1e-13, rtol=0)
