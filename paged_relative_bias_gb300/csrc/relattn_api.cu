@@ -139,13 +139,16 @@ struct WsLayout {
   size_t counters, lse, part, total;
 };
 
+// Decode workspace, sized for any query-token count up to kMaxQueryTokens:
+// counters per (chunk, KV head) -- at most kMaxQueryTokens chunks per
+// sequence -- and two partial slots per CTA of kMaxDecodeRows rows each.
 WsLayout ws_layout(const relattn_dims* d, const relattn_kv_cache* c, int grid) {
-  const int g = d->num_q_heads / c->num_kv_heads;
   WsLayout w;
   w.counters = kStatusBytes;
-  w.lse = w.counters + round_up(static_cast<size_t>(d->batch) * c->num_kv_heads * 4, 256);
-  w.part = w.lse + round_up(static_cast<size_t>(2) * grid * g * 4, 256);
-  w.total = w.part + static_cast<size_t>(2) * grid * g * c->d_v * 4;
+  w.lse = w.counters + round_up(static_cast<size_t>(d->batch) * kMaxQueryTokens *
+                                    c->num_kv_heads * 4, 256);
+  w.part = w.lse + round_up(static_cast<size_t>(2) * grid * kMaxDecodeRows * 4, 256);
+  w.total = w.part + static_cast<size_t>(2) * grid * kMaxDecodeRows * c->d_v * 4;
   return w;
 }
 
@@ -195,8 +198,9 @@ int relattn_read_status(const void* workspace, uint32_t* status, void* stream) {
   return to_status(e);
 }
 
+// kq: query tokens per sequence (1 for relattn_decode).
 static int prepare_decode(const void* q, const float* rel, const relattn_kv_cache* cache,
-                          const int32_t* block_table, const int32_t* seq_lens,
+                          const int32_t* block_table, const int32_t* seq_lens, int32_t kq,
                           int32_t window, int32_t rel_extent, const relattn_dims* dims,
                           void* out, void* workspace, size_t ws_bytes, bool walk,
                           DecodeLaunch* L, DeviceInfo* di) {
@@ -213,9 +217,13 @@ static int prepare_decode(const void* q, const float* rel, const relattn_kv_cach
   if (!aligned16(workspace)) return RELATTN_ERR_INVALID_ARG;
   if (!device_info(di)) return RELATTN_ERR_CUDA;
   const int grid = decode_grid(dims, *di);
+  if (kq < 1 || kq > kMaxQueryTokens) return RELATTN_ERR_UNSUPPORTED;
+  const int gq = dims->num_q_heads / cache->num_kv_heads;
+  const int kpc = kq < kMaxDecodeRows / gq ? kq : kMaxDecodeRows / gq;  // tokens per chunk
+  const int nck = (kq + kpc - 1) / kpc;
   // the kernel's work split is 32-bit: all tiles < 2^31, grid^2 < 2^31
-  if (static_cast<long long>(dims->batch) * cache->num_kv_heads * 2 * dims->max_blocks_per_seq >=
-          (1LL << 31) ||
+  if (static_cast<long long>(dims->batch) * nck * cache->num_kv_heads * 2 *
+              dims->max_blocks_per_seq >= (1LL << 31) ||
       grid > kMaxDecodeGrid)
     return RELATTN_ERR_UNSUPPORTED;
   const WsLayout w = ws_layout(dims, cache, grid);
@@ -242,6 +250,10 @@ static int prepare_decode(const void* q, const float* rel, const relattn_kv_cach
   p.num_blocks = cache->num_blocks;
   p.window = window;
   p.rel_extent = rel_extent;
+  p.k = kq;
+  p.kpc = kpc;
+  p.nck = nck;
+  p.Bv = dims->batch * nck;
   p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(128.0));
   L->grid = grid;
   if (walk) {
@@ -251,22 +263,26 @@ static int prepare_decode(const void* q, const float* rel, const relattn_kv_cach
   // An even number of stages: the decode kernel's two consumer groups each
   // own every other stage.
   p.nstages = kMaxStages;
-  while (p.nstages >= 2 && decode_smem_bytes(p.nstages, p.B, p.g, p.dv) > di->smem_optin)
+  while (p.nstages >= 2 &&
+         decode_smem_bytes(p.nstages, p.B, p.Bv, p.kpc, p.g, p.dv) > di->smem_optin)
     p.nstages -= 2;
   if (p.nstages < 2) return RELATTN_ERR_UNSUPPORTED;  // batch too large for shared memory
   if (!decode_cache_maps(cache, &L->tm_k, &L->tm_v)) return RELATTN_ERR_CUDA;
+  // rel [B][k][Hq][E] fp32: boxes of one token's g heads x kRelBoxW distances
   const cuuint64_t rd[2] = {static_cast<cuuint64_t>(rel_extent),
-                            static_cast<cuuint64_t>(dims->batch) * dims->num_q_heads};
+                            static_cast<cuuint64_t>(dims->batch) * kq * dims->num_q_heads};
   const cuuint64_t rs[1] = {static_cast<cuuint64_t>(rel_extent) * 4};
   const cuuint32_t rb[2] = {static_cast<cuuint32_t>(kRelBoxW), static_cast<cuuint32_t>(g)};
   if (!make_map(&L->tm_rel, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(rel), rd,
                 rs, rb, CU_TENSOR_MAP_SWIZZLE_NONE))
     return RELATTN_ERR_CUDA;
-  // query rows of one KV group: [B*Hq][128] bf16, two 64-column halves
-  const cuuint64_t qd[2] = {128, static_cast<cuuint64_t>(dims->batch) * dims->num_q_heads};
-  const cuuint64_t qs[1] = {256};
-  const cuuint32_t qbx[2] = {64, static_cast<cuuint32_t>(g)};
-  if (!make_map(&L->tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(q), qd, qs,
+  // query rows of one chunk: q [B*k][Hq][128] bf16 as (column, head, token);
+  // a box is one 64-column half of kpc tokens x g heads (rows token * g + head)
+  const cuuint64_t qd[3] = {128, static_cast<cuuint64_t>(dims->num_q_heads),
+                            static_cast<cuuint64_t>(dims->batch) * kq};
+  const cuuint64_t qs[2] = {256, static_cast<cuuint64_t>(dims->num_q_heads) * 256};
+  const cuuint32_t qbx[3] = {64, static_cast<cuuint32_t>(g), static_cast<cuuint32_t>(kpc)};
+  if (!make_map(&L->tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), qd, qs,
                 qbx, CU_TENSOR_MAP_SWIZZLE_128B))
     return RELATTN_ERR_CUDA;
   return RELATTN_OK;
@@ -278,8 +294,21 @@ int relattn_decode(const void* q, const float* rel, const relattn_kv_cache* kv_c
                    size_t workspace_bytes, void* stream) {
   DecodeLaunch L;
   DeviceInfo di;
-  const int rc = prepare_decode(q, rel, kv_cache, block_table, seq_lens, window, rel_extent,
+  const int rc = prepare_decode(q, rel, kv_cache, block_table, seq_lens, 1, window, rel_extent,
                                 dims, out, workspace, workspace_bytes, false, &L, &di);
+  if (rc != RELATTN_OK) return rc;
+  return to_status(launch_decode(L, static_cast<cudaStream_t>(stream)));
+}
+
+int relattn_decode_multi(const void* q, const float* rel, const relattn_kv_cache* kv_cache,
+                         const int32_t* block_table, const int32_t* seq_lens,
+                         int32_t num_query_tokens, int32_t window, int32_t rel_extent,
+                         const relattn_dims* dims, void* out, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+  DecodeLaunch L;
+  DeviceInfo di;
+  const int rc = prepare_decode(q, rel, kv_cache, block_table, seq_lens, num_query_tokens, window,
+                                rel_extent, dims, out, workspace, workspace_bytes, false, &L, &di);
   if (rc != RELATTN_OK) return rc;
   return to_status(launch_decode(L, static_cast<cudaStream_t>(stream)));
 }
@@ -292,7 +321,7 @@ int relattn_debug_walk_decode(const int32_t* block_table, const int32_t* seq_len
   if (!records || !count || max_records < 0) return RELATTN_ERR_INVALID_ARG;
   DecodeLaunch L;
   DeviceInfo di;
-  const int rc = prepare_decode(nullptr, nullptr, cache, block_table, seq_lens, window, 4, dims,
+  const int rc = prepare_decode(nullptr, nullptr, cache, block_table, seq_lens, 1, window, 4, dims,
                                 nullptr, workspace, workspace_bytes, true, &L, &di);
   if (rc != RELATTN_OK) return rc;
   L.p.dbg_records = records;
@@ -341,7 +370,7 @@ int relattn_decode_noalloc(const void* q, const float* rel, const relattn_kv_cac
   rc = noalloc_scratch(&scratch);
   if (rc != RELATTN_OK) return rc;
   DecodeLaunch L;
-  rc = prepare_decode(q, rel, kv_cache, block_table, seq_lens, window, rel_extent, dims, out,
+  rc = prepare_decode(q, rel, kv_cache, block_table, seq_lens, 1, window, rel_extent, dims, out,
                       scratch, RELATTN_NOALLOC_SCRATCH_BYTES, false, &L, &di);
   if (rc != RELATTN_OK) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

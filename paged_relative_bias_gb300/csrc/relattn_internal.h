@@ -27,6 +27,10 @@ struct DecodeParams {
   int32_t* dbg_count;
   int dbg_max;
   int B, Hq, Hkv, g, dv, max_blocks, num_blocks, window, rel_extent;
+  // query tokens per sequence (k; 1 for plain decode), packed kpc at a time
+  // with the g heads into the rows of one tile: nck = ceil(k / kpc) chunks
+  // per sequence, Bv = B * nck chunks ("virtual sequences") in all
+  int k, kpc, nck, Bv;
   int nstages;  // even: see the consumer groups of decode_kernel
   float scale_log2;  // log2(e) / sqrt(d_qk)
 };
@@ -63,7 +67,9 @@ struct PrefillLaunch {
   int grid;
 };
 
-int decode_smem_bytes(int nstages, int B, int g, int dv);
+int decode_smem_bytes(int nstages, int B, int Bv, int kpc, int g, int dv);
+constexpr int kMaxDecodeRows = 16;         // rows of one decode tile: g heads x tokens
+constexpr int kMaxQueryTokens = 16;        // query tokens per sequence in one decode call
 cudaError_t launch_decode(const DecodeLaunch& L, cudaStream_t stream);
 cudaError_t launch_decode_walk(const DecodeParams& p, int grid, cudaStream_t stream);
 

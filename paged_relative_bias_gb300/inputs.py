@@ -35,6 +35,7 @@ class DecodeWorkload:
     lengths: tuple       # ("uniform", lo, hi) | ("fixed", L) | ("loguniform", lo, hi)
     pool_blocks: int = 0  # 0: exactly the blocks the sequences need
     max_blocks_per_seq: int = 0  # 0: the longest sequence's block count
+    query_tokens: int = 0  # > 0: multi-token decode, q [B, k, Hq, d], rel [B, k, Hq, E]
 
 
 @dataclass(frozen=True)
@@ -79,6 +80,12 @@ WORKLOADS = {
     "diffhead_decode": DecodeWorkload(
         "diffhead_decode", 32, 64, 8, 128, 64, 0, 1024,
         ("loguniform", 1024, 131072)),
+    # Speculative verification on the local layer: 8 query tokens per
+    # sequence (7 drafted tokens and the last accepted one).
+    "verify_decode": DecodeWorkload(
+        "verify_decode", 16, 32, 8, 128, 128, 512, 512,
+        ("uniform", 4096, 32768), pool_blocks=4096, max_blocks_per_seq=256,
+        query_tokens=8),
 }
 
 
@@ -151,8 +158,9 @@ def make_decode(wl: DecodeWorkload, device="cpu", seed_data: int = 0,
     table = cut_block_tables(nblk, max_blocks, pool, lay, stride)
     g = _gen(device, seed_data)
     B, Hq, Hkv = wl.batch, wl.num_q_heads, wl.num_kv_heads
-    q = _randn((B, Hq, wl.d_qk), g, device, torch.bfloat16)
-    rel = _randn((B, Hq, wl.rel_extent), g, device, torch.float32)
+    tok = (wl.query_tokens,) if wl.query_tokens > 0 else ()
+    q = _randn((B, *tok, Hq, wl.d_qk), g, device, torch.bfloat16)
+    rel = _randn((B, *tok, Hq, wl.rel_extent), g, device, torch.float32)
     k_cache = _randn((pool, BLOCK_SIZE, Hkv, wl.d_qk), g, device, torch.bfloat16)
     v_cache = _randn((pool, BLOCK_SIZE, Hkv, wl.d_v), g, device, torch.bfloat16)
     return dict(

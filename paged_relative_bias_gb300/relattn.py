@@ -37,6 +37,7 @@ EXPORTS = (
     "relattn_debug_walk_prefill",
     "relattn_abi_version",
     "relattn_decode_noalloc",
+    "relattn_decode_multi",
 )
 
 
@@ -102,6 +103,10 @@ def lib() -> ctypes.CDLL:
     L.relattn_decode_noalloc.argtypes = [c_void_p, c_void_p, P, c_void_p, c_void_p, c_int32,
                                          c_int32, S, c_void_p, c_void_p]
     L.relattn_decode_noalloc.restype = c_int
+    L.relattn_decode_multi.argtypes = [c_void_p, c_void_p, P, c_void_p, c_void_p, c_int32,
+                                       c_int32, c_int32, S, c_void_p, c_void_p, c_size_t,
+                                       c_void_p]
+    L.relattn_decode_multi.restype = c_int
     L.relattn_abi_version.argtypes = []
     L.relattn_abi_version.restype = c_int
     _LIB = L
@@ -229,6 +234,41 @@ def relattn_decode_noalloc(q, rel, k_cache, v_cache, block_table, seq_lens, wind
         q.data_ptr(), rel.data_ptr(), ctypes.byref(cache), block_table.data_ptr(),
         seq_lens.data_ptr(), int(window), int(rel_extent), ctypes.byref(dims),
         out.data_ptr(), _stream(dev)), "relattn_decode_noalloc")
+    return out
+
+
+def relattn_decode_multi(q, rel, k_cache, v_cache, block_table, seq_lens, window: int,
+                         rel_extent: int, out=None, workspace=None, num_ctas: int = 0):
+    """Decode of k query tokens per sequence (speculative verification).
+
+    q is [B, k, Hq, d_qk], rel [B, k, Hq, rel_extent], out [B, k, Hq, d_v];
+    token i of sequence b sits at position seq_lens[b] - k + i.
+    """
+    dev = q.device
+    _need(q, "q", torch.bfloat16, 4, dev)
+    B, kq, Hq, _ = q.shape
+    _need(rel, "rel", torch.float32, 4, dev)
+    _need(k_cache, "k_cache", torch.bfloat16, 4, dev)
+    _need(v_cache, "v_cache", torch.bfloat16, 4, dev)
+    _need(block_table, "block_table", torch.int32, 2, dev)
+    _need(seq_lens, "seq_lens", torch.int32, 1, dev)
+    if tuple(rel.shape) != (B, kq, Hq, rel_extent):
+        raise ValueError("rel must be [B, k, Hq, rel_extent]")
+    if seq_lens.shape[0] != B or block_table.shape[0] != B:
+        raise ValueError("seq_lens / block_table batch mismatch")
+    cache = cache_desc(k_cache, v_cache)
+    dims = Dims(B, Hq, block_table.shape[1], 0, 0, num_ctas)
+    if out is None:
+        out = torch.empty((B, kq, Hq, v_cache.shape[3]), dtype=torch.bfloat16, device=dev)
+    else:
+        _need(out, "out", torch.bfloat16, 4, dev)
+    if workspace is None:
+        workspace = new_workspace(workspace_size(dims, cache), dev)
+    _check(lib().relattn_decode_multi(
+        q.data_ptr(), rel.data_ptr(), ctypes.byref(cache), block_table.data_ptr(),
+        seq_lens.data_ptr(), int(kq), int(window), int(rel_extent), ctypes.byref(dims),
+        out.data_ptr(), workspace.data_ptr(), workspace.numel(), _stream(dev)),
+        "relattn_decode_multi")
     return out
 
 

@@ -91,3 +91,10 @@ def oracle_prefill(case, rows=None, cache=None):
                      case["block_table"].cpu().numpy(),
                      case["ctx_lens"].cpu().numpy(), case["window"], case["rel_extent"],
                      rows=rows)
+
+
+def oracle_decode_multi(case, batch=None, tokens=None, heads=None):
+    h = host_decode_inputs(case)
+    return O.decode_multi(h["q"], h["rel"], h["k_cache"], h["v_cache"], h["block_table"],
+                          h["seq_lens"], case["window"], case["rel_extent"], batch=batch,
+                          tokens=tokens, heads=heads)
