@@ -58,17 +58,24 @@ BLOCK = 128
 # ---------------------------------------------------------------------------
 
 def decode_work(wl, seq_lens):
-    """Algorithmic bytes of one decode call and of each (sequence, KV head)."""
+    """Algorithmic bytes of one decode call and of each (sequence, KV head).
+
+    With k query tokens per sequence (positions L - k .. L - 1) the keys
+    counted are those any of them sees, once; q, the rel entries each token
+    uses and out count per token and head."""
     g = wl.num_q_heads // wl.num_kv_heads
+    k = max(1, wl.query_tokens)
     total = 0
     per_group = []
     for L in seq_lens:
-        n = min(wl.window, L) if wl.window > 0 else L
+        lo = max(0, L - k - wl.window + 1) if wl.window > 0 else 0
         P = L - 1
-        lo = P - n + 1
         blocks = P // BLOCK - lo // BLOCK + 1
-        kv = n * (wl.d_qk + wl.d_v) * 2
-        head = wl.d_qk * 2 + min(wl.rel_extent, n) * 4 + wl.d_v * 2
+        kv = (P - lo + 1) * (wl.d_qk + wl.d_v) * 2
+        head = 0
+        for Pi in range(L - k, L):
+            n = min(wl.window, Pi + 1) if wl.window > 0 else Pi + 1
+            head += wl.d_qk * 2 + min(wl.rel_extent, n) * 4 + wl.d_v * 2
         grp = kv + g * head
         per_group.append(grp)
         total += wl.num_kv_heads * grp + blocks * 4 + 4
@@ -102,7 +109,9 @@ def describe(wl):
         lens = {"fixed": lambda s: f"L={s[1]}", "uniform": lambda s: f"L~U[{s[1]},{s[2]}]",
                 "loguniform": lambda s: f"L~logU[{s[1]},{s[2]}]"}[wl.lengths[0]](wl.lengths)
         win = f"W={wl.window}" if wl.window > 0 else "global"
-        return (f"{wl.name}: decode B={wl.batch}, {wl.num_q_heads}/{wl.num_kv_heads} heads, "
+        kind = (f"{wl.query_tokens}-token decode (verification)" if wl.query_tokens > 0
+                else "decode")
+        return (f"{wl.name}: {kind} B={wl.batch}, {wl.num_q_heads}/{wl.num_kv_heads} heads, "
                 f"d_qk={wl.d_qk} d_v={wl.d_v}, {win}, rel_extent={wl.rel_extent}, {lens}, "
                 f"bf16 paged KV in 128-token blocks, random block tables")
     win = f"W={wl.window}" if wl.window > 0 else "global"
@@ -270,16 +279,23 @@ def committed_traffic(kernel_tag):
 # our arm
 # ---------------------------------------------------------------------------
 
-def decode_sets(wl, device, l2):
+def decode_sets(wl, device, l2, shared_pool=False):
     """Per-layer input sets, enough that one pass over them reads more than
     twice the L2 (a single set when one step already does).  Every set has its
     own KV pool, queries and rel; all share the first set's sequence lengths
-    and block table tensors, like the layers of one decode step."""
+    and block table tensors, like the layers of one decode step.
+
+    shared_pool: the sets share the first set's KV pool instead, each with
+    its own renumbered block table (the same bytes per call from a footprint
+    of one pool: the small case for profiler captures)."""
     first = I.make_decode(wl, device)
     alg0, _ = decode_work(wl, first["seq_lens"].cpu().tolist())
     n = 1 if alg0 >= 2 * l2 else min(16, -(-2 * l2 // alg0))
     sets = [first]
     for s in range(1, n):
+        if shared_pool:
+            sets.append(I.relayout_decode(first, seed=100 + s))
+            continue
         c = I.make_decode(wl, device, seed_data=s)  # same layout seed: same lengths and tables
         assert torch.equal(c["block_table"], first["block_table"])
         c["block_table"], c["seq_lens"] = first["block_table"], first["seq_lens"]
@@ -288,22 +304,24 @@ def decode_sets(wl, device, l2):
     return sets, algs
 
 
-def run_decode(R, wl, device, steps, warmup, dist, sampler, l2):
+def run_decode(R, wl, device, steps, warmup, dist, sampler, l2, shared_pool=False):
     """Graph-replayed decode steps rotating over the input sets."""
-    sets, algs = decode_sets(wl, device, l2)
+    sets, algs = decode_sets(wl, device, l2, shared_pool)
+    tok = (wl.query_tokens,) if wl.query_tokens > 0 else ()
+    fn = R.relattn_decode_multi if wl.query_tokens > 0 else R.relattn_decode
     wss, outs = [], []
     for case in sets:
-        dims = R.decode_dims(case["q"], case["block_table"])
+        dims = R.Dims(wl.batch, wl.num_q_heads, case["block_table"].shape[1], 0, 0, 0)
         wss.append(R.new_workspace(R.workspace_size(dims, R.cache_desc(case["k_cache"],
                                                                        case["v_cache"])),
                                    device))
-        outs.append(torch.empty((wl.batch, wl.num_q_heads, wl.d_v), dtype=torch.bfloat16,
+        outs.append(torch.empty((wl.batch, *tok, wl.num_q_heads, wl.d_v), dtype=torch.bfloat16,
                                 device=device))
 
     def call(i):
         c = sets[i]
-        R.relattn_decode(c["q"], c["rel"], c["k_cache"], c["v_cache"], c["block_table"],
-                         c["seq_lens"], wl.window, wl.rel_extent, out=outs[i], workspace=wss[i])
+        fn(c["q"], c["rel"], c["k_cache"], c["v_cache"], c["block_table"], c["seq_lens"],
+           wl.window, wl.rel_extent, out=outs[i], workspace=wss[i])
 
     # graphs[r]: calls for sets 0..r-1 back to back (r = len(sets) is one
     # full pass; shorter ones time the remainder of steps)
@@ -350,16 +368,18 @@ def run_decode_e2e(R, sets, wl, wss, device, steps, warmup, dist, sampler):
     keys = ("q", "rel", "seq_lens", "block_table")
     host = [{k: c[k].cpu().pin_memory() for k in keys} for c in sets]
     dev = {k: torch.empty_like(sets[0][k]) for k in keys}
-    out_h = torch.empty((wl.batch, wl.num_q_heads, wl.d_v), dtype=torch.bfloat16).pin_memory()
+    tok = (wl.query_tokens,) if wl.query_tokens > 0 else ()
+    fn = R.relattn_decode_multi if wl.query_tokens > 0 else R.relattn_decode
+    out_h = torch.empty((wl.batch, *tok, wl.num_q_heads, wl.d_v),
+                        dtype=torch.bfloat16).pin_memory()
     out_d = torch.empty_like(out_h, device=device)
 
     def step(k):
         i = k % len(sets)
         for name in keys:
             dev[name].copy_(host[i][name], non_blocking=True)
-        R.relattn_decode(dev["q"], dev["rel"], sets[i]["k_cache"], sets[i]["v_cache"],
-                         dev["block_table"], dev["seq_lens"], wl.window, wl.rel_extent,
-                         out=out_d, workspace=wss[i])
+        fn(dev["q"], dev["rel"], sets[i]["k_cache"], sets[i]["v_cache"], dev["block_table"],
+           dev["seq_lens"], wl.window, wl.rel_extent, out=out_d, workspace=wss[i])
         out_h.copy_(out_d, non_blocking=True)
 
     times = timed_steps(step, steps, warmup, None, dist, sampler)
@@ -390,6 +410,24 @@ def run_prefill(R, wl, device, steps, warmup, dist, sampler, case=None):
     return times
 
 
+def group_blocks(O, wl, L, table_row):
+    """[(logical, physical)] blocks holding any key the sequence's query
+    tokens see: the oracle's walk for the newest token, widened back to the
+    first visible key of the oldest one when there are several."""
+    k = max(1, wl.query_tokens)
+    blocks = O.decode_blocks(L, wl.window, table_row)
+    lo, _ = O.visible_keys(L - k, wl.window)
+    first = lo // BLOCK
+    return [(lb, int(table_row[lb])) for lb in range(first, blocks[0][0])] + blocks
+
+
+def oracle_group(O, wl, q, rel, b, kc, vc, sub, L, heads):
+    """The oracle on one (sequence, KV head) group over its gathered blocks."""
+    fn = O.decode_multi if wl.query_tokens > 0 else O.decode
+    fn(q[b:b + 1], rel[b:b + 1], kc, vc, sub, np.array([L]), wl.window, wl.rel_extent,
+       heads=heads)
+
+
 def oracle_decode_sample(case, wl, budget_s):
     """Time the float64 oracle on the workload's (sequence, KV head) groups:
     whole passes over all groups, repeated until ~budget_s of CPU time (at
@@ -406,7 +444,7 @@ def oracle_decode_sample(case, wl, budget_s):
     # each sequence's blocks, gathered once (host copies; not timed)
     per_seq = []
     for b in range(wl.batch):
-        blocks = O.decode_blocks(lens[b], wl.window, table[b])
+        blocks = group_blocks(O, wl, lens[b], table[b])
         ids = torch.tensor([p for _, p in blocks], device=case["k_cache"].device)
         sub = np.full((1, table.shape[1]), -1, dtype=np.int64)
         for i, (lblk, _) in enumerate(blocks):
@@ -420,8 +458,7 @@ def oracle_decode_sample(case, wl, budget_s):
             kc, vc, sub = per_seq[b]
             heads = list(range(kvh * g, (kvh + 1) * g))
             t0 = time.perf_counter()
-            O.decode(q[b:b + 1], rel[b:b + 1], kc, vc, sub, np.array([lens[b]]), wl.window,
-                     wl.rel_extent, heads=heads)
+            oracle_group(O, wl, q, rel, b, kc, vc, sub, lens[b], heads)
             elapsed += time.perf_counter() - t0
             done += 1
             nbytes += per_group[b]
@@ -436,8 +473,10 @@ def cores_used():
 
 def prefill_workload(args):
     wl = I.WORKLOADS["chunked_prefill"]
-    if args.prefill_new_tokens:
-        wl = I.variant(wl, new_tokens=(args.prefill_new_tokens,) * len(wl.new_tokens))
+    nseq = args.prefill_seqs or len(wl.new_tokens)
+    new = args.prefill_new_tokens or wl.new_tokens[0]
+    if (nseq, new) != (len(wl.new_tokens), wl.new_tokens[0]):
+        wl = I.variant(wl, new_tokens=(new,) * nseq, ctx_lens=wl.ctx_lens[:1] * nseq)
     return wl
 
 
@@ -483,7 +522,7 @@ def ours(args):
         return ours_prefill(args, R, dist, device, peaks, sampler)
     wl = I.WORKLOADS[args.workload]
     sets, step_bytes, times, wss = run_decode(R, wl, device, args.steps, args.warmup, dist,
-                                              sampler, l2)
+                                              sampler, l2, args.pool == "shared")
     case = sets[0]
     t_ms = sum(times) / len(times)
     t_max = dist.max(sum(times))
@@ -502,7 +541,8 @@ def ours(args):
 
     secondary = []
     if not args.no_secondary:
-        for name in ("global_decode_b1", "global_decode_b8", "diffhead_decode"):
+        for name in ("global_decode_b1", "global_decode_b8", "diffhead_decode",
+                     "verify_decode"):
             w2 = I.WORKLOADS[name]
             c2, b2, t2, _ = run_decode(R, w2, device, args.secondary_steps, 3, dist, sampler, l2)
             m2 = sum(t2) / len(t2)
@@ -544,8 +584,10 @@ def ours(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) q/k/v bf16, rel fp32)",
         "config": {"workload": describe(wl), "l2": l2_note,
-                   "layers": "each input set is one layer: own KV pool, q and rel; shared "
-                             "seq_lens and block table",
+                   "layers": ("each input set is one layer: own KV pool, q and rel; shared "
+                              "seq_lens and block table" if args.pool == "per-set" else
+                              "input sets share one KV pool, each with its own q, rel and "
+                              "renumbered block table (profiling footprint)"),
                    "parallelism": f"replicas x{dist.world} (the path does not shard)"},
         "roofline": roofline("hbm", kernel_gbs, peaks["hbm"], "GB/s",
                              committed_traffic("decode_" + args.workload)),
@@ -585,7 +627,7 @@ def reference(args):
     groups = [(b, kvh) for b in range(wl.batch) for kvh in range(wl.num_kv_heads)]
     prepared = []
     for b in range(wl.batch):
-        blocks = O.decode_blocks(lens[b], wl.window, table[b])
+        blocks = group_blocks(O, wl, lens[b], table[b])
         ids = torch.tensor([p for _, p in blocks], device=case["k_cache"].device)
         sub = np.full((1, table.shape[1]), -1, dtype=np.int64)
         for i, (lblk, _) in enumerate(blocks):
@@ -596,8 +638,7 @@ def reference(args):
     def step(i):
         b, kvh = groups[i % len(groups)]
         kc, vc, sub = prepared[b]
-        O.decode(q[b:b + 1], rel[b:b + 1], kc, vc, sub, np.array([lens[b]]), wl.window,
-                 wl.rel_extent, heads=list(range(kvh * g, (kvh + 1) * g)))
+        oracle_group(O, wl, q, rel, b, kc, vc, sub, lens[b], list(range(kvh * g, (kvh + 1) * g)))
         return per_group[b]
 
     for i in range(args.warmup):
@@ -630,9 +671,14 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="local_decode",
                     choices=["local_decode", "global_decode_b1", "global_decode_b8",
-                             "diffhead_decode", "chunked_prefill"])
+                             "diffhead_decode", "verify_decode", "chunked_prefill"])
     ap.add_argument("--prefill-new-tokens", type=int, default=0,
                     help="new tokens per sequence of the chunked prefill (default 8192)")
+    ap.add_argument("--prefill-seqs", type=int, default=0,
+                    help="sequences of the chunked prefill (default 4)")
+    ap.add_argument("--pool", choices=["per-set", "shared"], default="per-set",
+                    help="decode input sets: one KV pool each (default), or one shared pool "
+                         "with renumbered block tables (small device footprint, for ncu)")
     ap.add_argument("--secondary-steps", type=int, default=50)
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -103,16 +103,30 @@ struct VSeq {
   int ntiles;      // 0 if the sequence's length is invalid
 };
 
+// The query-token packing: k tokens per sequence, kpc per chunk, nck chunks.
+// The kernel is instantiated twice: with MULTI = false (k = 1, one-token
+// decode) these are the constants 1 and the chunk arithmetic folds away.
+template <bool MULTI>
+struct Tok {
+  int k, kpc, nck;
+  __device__ __forceinline__ explicit Tok(const DecodeParams& p)
+      : k(MULTI ? p.k : 1), kpc(MULTI ? p.kpc : 1), nck(MULTI ? p.nck : 1) {}
+  // token of tile row r (rows are token * g + head)
+  __device__ __forceinline__ int token_of_row(int r, int g) const { return MULTI ? r / g : 0; }
+};
+
+template <bool MULTI>
 __device__ __forceinline__ VSeq decode_vseq(int vb, int len, const DecodeParams& p) {
+  const Tok<MULTI> t(p);
   VSeq v;
-  v.b = vb / p.nck;
-  v.i0 = (vb - v.b * p.nck) * p.kpc;
-  v.kc = min(p.kpc, p.k - v.i0);
-  if (len < p.k || len > p.max_blocks * kBlockSize) {
+  v.b = vb / t.nck;
+  v.i0 = (vb - v.b * t.nck) * t.kpc;
+  v.kc = min(t.kpc, t.k - v.i0);
+  if (len < t.k || len > p.max_blocks * kBlockSize) {
     v.pf = v.pl = v.lo = v.tile_first = v.ntiles = 0;
     return v;
   }
-  v.pf = len - p.k + v.i0;
+  v.pf = len - t.k + v.i0;
   v.pl = v.pf + v.kc - 1;
   v.lo = window_lo(v.pf, p.window);
   v.tile_first = v.lo / kTileKeys;
@@ -199,18 +213,21 @@ __device__ __forceinline__ void prefetch_l2(const void* ptr) {
 // c / Hkv, KV head c % Hkv, which holds when every segment fits one CTA) --
 // its block-table row, its query rows and the rel rows its window needs.
 // A wrong guess costs only the prefetched bytes.
+template <bool MULTI>
 __device__ __forceinline__ int decode_early_loads(const DecodeParams& p) {
+  const Tok<MULTI> t(p);
   const int tid = threadIdx.x;
   const int len = tid < p.B ? __ldg(p.seq_lens + tid) : 0;
   const int vb = blockIdx.x / p.Hkv, kvh = blockIdx.x - (blockIdx.x / p.Hkv) * p.Hkv;
   if (vb < p.Bv && p.rel != nullptr) {
     const int lane = tid & 31;
-    const int b = vb / p.nck, i0 = (vb - b * p.nck) * p.kpc;
-    const int rows = min(p.kpc, p.k - i0) * p.g;  // (token, head) rows of the chunk
+    const int b = vb / t.nck, i0 = (vb - b * t.nck) * t.kpc;
+    const int rows = min(t.kpc, t.k - i0) * p.g;  // (token, head) rows of the chunk
     // query / rel row of chunk row r: token i0 + r / g, head kvh g + r % g
     auto qrow = [&](int r) {
-      return (static_cast<size_t>(b) * p.k + i0 + r / p.g) * p.Hq +
-             static_cast<size_t>(kvh) * p.g + r % p.g;
+      const int ti = t.token_of_row(r, p.g);
+      return (static_cast<size_t>(b) * t.k + i0 + ti) * p.Hq +
+             static_cast<size_t>(kvh) * p.g + (r - ti * p.g);
     };
     if (tid >= 32 && tid < 64) {  // block-table row: 32 lines of 128 bytes at most
       if (lane * 32 < p.max_blocks)
@@ -241,16 +258,19 @@ struct CtaRange {
 // registers, with no block-wide barrier on the way to the first copy.  The
 // results are published in shared memory for the other warps.  Same cut
 // arithmetic as range_cut.  len0: seq_lens[lane], already loaded.
+template <bool MULTI>
 __device__ CtaRange decode_plan_warp(const DecodeParams& p, uint8_t* smem, const DecodeSmem& L,
                                      int len0) {
+  const Tok<MULTI> t(p);
   int* s_len = reinterpret_cast<int*>(smem + L.seqlen);
   int* s_nt = reinterpret_cast<int*>(smem + L.nt);
   int* s_pref = reinterpret_cast<int*>(smem + L.pref);
   int* s_misc = reinterpret_cast<int*>(smem + L.misc);
   const int lane = threadIdx.x & 31;
   const bool has = lane < p.Bv;
-  const int len = __shfl_sync(0xffffffffu, len0, min(lane / p.nck, 31));  // my chunk's sequence
-  const int nt = has ? decode_vseq(lane, len, p).ntiles : 0;
+  const int len = MULTI ? __shfl_sync(0xffffffffu, len0, min(lane / t.nck, 31))  // my chunk's
+                       : len0;                                                 // sequence
+  const int nt = has ? decode_vseq<MULTI>(lane, len, p).ntiles : 0;
   if (has && nt == 0 && blockIdx.x == 0) report(p.status, RELATTN_DEV_BAD_LENGTH);
   int incl = nt;
 #pragma unroll
@@ -340,12 +360,14 @@ __device__ __forceinline__ CtaRange decode_plan_read(const uint8_t* smem, const 
 // Sequences with an invalid length get zeros for all their query tokens
 // (CTA 0, the given threads; a sequence's chunks share its length, so its
 // first chunk tells).
+template <bool MULTI>
 __device__ __forceinline__ void decode_zero_bad(const DecodeParams& p, const int* s_nt, int t,
                                                 int nthreads) {
   if (blockIdx.x != 0 || p.out == nullptr) return;
-  const int per = p.k * p.Hq * p.dv;
+  const Tok<MULTI> tk(p);
+  const int per = tk.k * p.Hq * p.dv;
   for (int b = 0; b < p.B; ++b) {
-    if (s_nt[b * p.nck] != 0) continue;
+    if (s_nt[b * tk.nck] != 0) continue;
     __nv_bfloat16* o = p.out + static_cast<size_t>(b) * per;
     for (int i = t; i < per; i += nthreads) o[i] = __float2bfloat16(0.f);
   }
@@ -353,6 +375,7 @@ __device__ __forceinline__ void decode_zero_bad(const DecodeParams& p, const int
 
 // Per-CTA prologue: each sequence's tile count, their exclusive prefix and
 // the cut plan.  len0: seq_lens[threadIdx.x], already loaded.
+template <bool MULTI>
 __device__ Plan decode_prologue(const DecodeParams& p, uint8_t* smem, const DecodeSmem& L,
                                 bool zero_bad, int len0) {
   int* s_len = reinterpret_cast<int*>(smem + L.seqlen);
@@ -363,7 +386,7 @@ __device__ Plan decode_prologue(const DecodeParams& p, uint8_t* smem, const Deco
   for (int b = tid; b < p.B; b += blockDim.x) s_len[b] = b == tid ? len0 : p.seq_lens[b];
   __syncthreads();
   for (int vb = tid; vb < p.Bv; vb += blockDim.x) {
-    const int nt = decode_vseq(vb, s_len[vb / p.nck], p).ntiles;
+    const int nt = decode_vseq<MULTI>(vb, s_len[vb / Tok<MULTI>(p).nck], p).ntiles;
     s_nt[vb] = nt;
     if (nt == 0 && blockIdx.x == 0) report(p.status, RELATTN_DEV_BAD_LENGTH);
   }
@@ -395,7 +418,7 @@ __device__ Plan decode_prologue(const DecodeParams& p, uint8_t* smem, const Deco
     }
   }
   __syncthreads();
-  if (zero_bad) decode_zero_bad(p, s_nt, tid, blockDim.x);
+  if (zero_bad) decode_zero_bad<MULTI>(p, s_nt, tid, blockDim.x);
   Plan pl;
   pl.T = p.Hkv * s_pref[p.Bv];
   pl.G = min(static_cast<int>(gridDim.x), pl.T);
@@ -406,7 +429,7 @@ __device__ Plan decode_prologue(const DecodeParams& p, uint8_t* smem, const Deco
   return pl;
 }
 
-template <int DV>
+template <int DV, bool MULTI>
 __global__ void __launch_bounds__(kDecodeThreads, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tm_q,
                   const __grid_constant__ CUtensorMap tm_k,
@@ -417,7 +440,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int g = p.g;
   const int ns = p.nstages;
-  const DecodeSmem L(ns, p.B, p.Bv, p.kpc, g, DV);
+  const Tok<MULTI> tok(p);
+  const DecodeSmem L(ns, p.B, p.Bv, tok.kpc, g, DV);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
   uint64_t* empty = full + ns;
   uint64_t* qfull = empty + ns;
@@ -428,7 +452,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   const int* s_pref = reinterpret_cast<const int*>(smem + L.pref);
   int* s_misc = reinterpret_cast<int*>(smem + L.misc);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int len0 = decode_early_loads(p);
+  const int len0 = decode_early_loads<MULTI>(p);
 
   if (tid == 0) {
     for (int s = 0; s < ns; ++s) {
@@ -459,15 +483,15 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   if (p.Bv <= 32) {
     // warp 0 plans alone and lets the consumers go with a non-blocking arrive
     if (warp == 0) {
-      cr = decode_plan_warp(p, smem, L, len0);
+      cr = decode_plan_warp<MULTI>(p, smem, L, len0);
       named_barrier_arrive(2, kDecodeThreads);
     } else {
       named_barrier(2, kDecodeThreads);
       cr = decode_plan_read(smem, L);
-      decode_zero_bad(p, s_nt, tid - 32, kConsumerThreads);
+      decode_zero_bad<MULTI>(p, s_nt, tid - 32, kConsumerThreads);
     }
   } else {
-    cr.pl = decode_prologue(p, smem, L, true, len0);
+    cr.pl = decode_prologue<MULTI>(p, smem, L, true, len0);
     cr.a0 = range_cut(blockIdx.x, cr.pl, s_pref, s_nt, p.Bv, p.Hkv);
     cr.a1 = range_cut(blockIdx.x + 1, cr.pl, s_pref, s_nt, p.Bv, p.Hkv);
     cr.has_first = false;
@@ -479,7 +503,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   const int stage_tx = 16384 + kTileKeys * DV * 2;
   const int rel_tx = g * kRelBoxW * 4;         // one token's rel box
   const int rel_stride = rel_token_bytes(g);  // its place in a stage's rel slice
-  const int q_tx = 2 * p.kpc * g * 64 * 2;    // kpc tokens x g heads, two halves
+  const int q_tx = 2 * tok.kpc * g * 64 * 2;  // kpc tokens x g heads, two halves
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -490,7 +514,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       const Piece pc = (k == 0 && cr.has_first && warp == 0)
                            ? cr.first
                            : locate_piece(f, a1, s_pref, s_nt, p.Bv, p.Hkv);
-      const VSeq sq = decode_vseq(pc.b, s_len[pc.b / p.nck], p);
+      const VSeq sq = decode_vseq<MULTI>(pc.b, s_len[pc.b / tok.nck], p);
       const int* trow = p.block_table + static_cast<size_t>(sq.b) * p.max_blocks;
       int bad = 0;
       if (lane == 0) {
@@ -503,8 +527,13 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
           // (rows past its kc tokens are read but never used)
           uint8_t* qs = smem + L.qbuf + qb * kQBufBytes;
           mbar_arrive_expect_tx(&qfull[qb], q_tx);
-          tma_load_3d(qs, &tm_q, &qfull[qb], 0, pc.kvh * g, sq.b * p.k + sq.i0);
-          tma_load_3d(qs + 2048, &tm_q, &qfull[qb], 64, pc.kvh * g, sq.b * p.k + sq.i0);
+          if constexpr (MULTI) {
+            tma_load_3d(qs, &tm_q, &qfull[qb], 0, pc.kvh * g, sq.b * tok.k + sq.i0);
+            tma_load_3d(qs + 2048, &tm_q, &qfull[qb], 64, pc.kvh * g, sq.b * tok.k + sq.i0);
+          } else {  // q [B * Hq][128]: the g rows of the group
+            tma_load_2d(qs, &tm_q, &qfull[qb], 0, sq.b * p.Hq + pc.kvh * g);
+            tma_load_2d(qs + 2048, &tm_q, &qfull[qb], 64, sq.b * p.Hq + pc.kvh * g);
+          }
         }
       }
       abort = __shfl_sync(0xffffffffu, bad, 0) != 0;
@@ -543,7 +572,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
             for (int i = 0; i < nrel; ++i)
               tma_load_2d(smem + L.rel + stage * L.rel_bytes + i * rel_stride, &tm_rel,
                           &full[stage], (dmin0 + i) & ~3,
-                          (sq.b * p.k + sq.i0 + i) * p.Hq + pc.kvh * g);
+                          (sq.b * tok.k + sq.i0 + i) * p.Hq + pc.kvh * g);
           } else {
             report(p.status, RELATTN_DEV_BAD_BLOCK_ID);
             mbar_arrive(&full[stage]);
@@ -592,7 +621,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
 
   for (int f = a0; f < a1 && !abort; ++k) {
     const Piece pc = locate_piece(f, a1, s_pref, s_nt, p.Bv, p.Hkv);
-    const VSeq sq = decode_vseq(pc.b, s_len[pc.b / p.nck], p);
+    const VSeq sq = decode_vseq<MULTI>(pc.b, s_len[pc.b / tok.nck], p);
     const int h0 = pc.kvh * g;
     const int nrows = sq.kc * g;  // valid rows of the tile: token * g + head
     // this thread's rows r0 and r0 + 8: validity, query position, first
@@ -602,7 +631,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
 #pragma unroll
     for (int rr = 0; rr < 2; ++rr) {
       const int row = r0 + 8 * rr;
-      const int ti = row / g;
+      const int ti = tok.token_of_row(row, g);
       rv[rr] = row < nrows;
       rP[rr] = sq.pf + ti;
       rlo[rr] = window_lo(rP[rr], p.window);
@@ -615,22 +644,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       abort = true;
       break;
     }
+    // the query rows stay in their buffer for the whole piece: each tile
+    // reads its A fragments from there, one k-step at a time, rather than
+    // holding all 32 registers of them next to the 4 x d_v/8 of O
     const uint32_t qbase = smem_u32(smem + L.qbuf + qb * kQBufBytes);
-    // this warp's A fragments of the query rows for all eight k-steps: the
-    // query is the same for every tile of the piece
-    uint32_t qa[8][4];
-    {
-      const int mi = lane >> 3;
-      const int qrow = (mi & 1) * 8 + (lane & 7);
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        const int qchunk = ks * 2 + (mi >> 1);
-        ldsm_x4(qbase + (qchunk >> 3) * 2048 + sw128(qrow, qchunk & 7), qa[ks][0], qa[ks][1],
-                qa[ks][2], qa[ks][3]);
-      }
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&qempty[qb]);  // query rows no longer needed
 
     float m_[2] = {kNegInf, kNegInf}, l_[2] = {0.f, 0.f};
     float o[DV / 8][4];
@@ -656,13 +673,18 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         {
           const int mi = lane >> 3;
           const int key = 16 * cw + (mi >> 1) * 8 + (lane & 7);
+          const int qrow = (mi & 1) * 8 + (lane & 7);
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks) {
+            const int qchunk = ks * 2 + (mi >> 1);
+            uint32_t qa[4];
+            ldsm_x4(qbase + (qchunk >> 3) * 2048 + sw128(qrow, qchunk & 7), qa[0], qa[1], qa[2],
+                    qa[3]);
             const int chunk = ks * 2 + (mi & 1);
             uint32_t b0, b1, b2, b3;
             ldsm_x4(kbase + (chunk >> 3) * 8192 + sw128(key, chunk & 7), b0, b1, b2, b3);
-            mma_16816(s[0], qa[ks], b0, b1);
-            mma_16816(s[1], qa[ks], b2, b3);
+            mma_16816(s[0], qa, b0, b1);
+            mma_16816(s[1], qa, b2, b3);
           }
         }
         // logits in log2 units: (q.k/sqrt(d) + rel) * log2(e).  A row's rel
@@ -670,23 +692,42 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         // rounded down to 16 bytes.
         const float* relt = reinterpret_cast<const float*>(smem + L.rel + stage * L.rel_bytes);
         const bool edge = key0 < lo_last || key0 + kTileKeys - 1 > sq.pf;  // any mask?
-        int d0[2];
-#pragma unroll
-        for (int rr = 0; rr < 2; ++rr) d0[rr] = (rP[rr] - key0 - (kTileKeys - 1)) & ~3;
         float x[2][4];
+        if constexpr (!MULTI) {
+          // one position for all rows: one box, present or not for the tile
+          const int dmin = sq.pf - key0 - (kTileKeys - 1);
+          const bool need_rel = dmin < p.rel_extent;
+          const int d0 = dmin & ~3;
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
+          for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int rr = i >> 1;
-            const int key = key0 + 16 * cw + nt * 8 + cq * 2 + (i & 1);
-            const int dist = rP[rr] - key;
-            float bias = 0.f;
-            if (rv[rr] && dist < p.rel_extent) bias = relt[rrel[rr] + (dist - d0[rr])];
-            float v = fmaf(s[nt][i], p.scale_log2, bias * kLog2e);
-            if (edge && (key < rlo[rr] || key > rP[rr])) v = kNegInf;
-            x[nt][i] = v;
-          }
+            for (int i = 0; i < 4; ++i) {
+              const int row = r0 + (i >> 1) * 8;
+              const int key = key0 + 16 * cw + nt * 8 + cq * 2 + (i & 1);
+              float bias = 0.f;
+              if (need_rel && row < g) bias = relt[row * kRelBoxW + (sq.pf - key - d0)];
+              float v = fmaf(s[nt][i], p.scale_log2, bias * kLog2e);
+              if (edge && (key < sq.lo || key > sq.pf)) v = kNegInf;
+              x[nt][i] = v;
+            }
+        } else {
+          int d0[2];
+#pragma unroll
+          for (int rr = 0; rr < 2; ++rr) d0[rr] = (rP[rr] - key0 - (kTileKeys - 1)) & ~3;
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int rr = i >> 1;
+              const int key = key0 + 16 * cw + nt * 8 + cq * 2 + (i & 1);
+              const int dist = rP[rr] - key;
+              float bias = 0.f;
+              if (rv[rr] && dist < p.rel_extent) bias = relt[rrel[rr] + (dist - d0[rr])];
+              float v = fmaf(s[nt][i], p.scale_log2, bias * kLog2e);
+              if (edge && (key < rlo[rr] || key > rP[rr])) v = kNegInf;
+              x[nt][i] = v;
+            }
+        }
         // online softmax, rows r0 (rr=0) and r0+8 (rr=1)
 #pragma unroll
         for (int rr = 0; rr < 2; ++rr) {
@@ -736,6 +777,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[stage]);
     }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&qempty[qb]);  // the piece's query rows are done
     if (abort) break;
     n_base += pc.n;
 
@@ -750,7 +793,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       }
     }
     named_barrier(1, kConsumerThreads);
-    const int srows = p.kpc * g;  // rows of a warp's merge slice
+    const int srows = tok.kpc * g;  // rows of a warp's merge slice
 #pragma unroll
     for (int rr = 0; rr < 2; ++rr) {
       const int row = r0 + 8 * rr;
@@ -781,9 +824,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     const int slot = 2 * c + (a0 < pc.seg_start ? 1 : 0);
     // out row of tile row r: token i0 + r / g of sequence b, head h0 + r % g
     auto orow = [&](int row) {
-      const int ti = row / g;
+      const int ti = tok.token_of_row(row, g);
       return p.out +
-             ((static_cast<size_t>(sq.b) * p.k + sq.i0 + ti) * p.Hq + h0 + (row - ti * g)) * DV;
+             ((static_cast<size_t>(sq.b) * tok.k + sq.i0 + ti) * p.Hq + h0 + (row - ti * g)) * DV;
     };
     for (int idx = ctid; idx < nrows * DV / 2; idx += kConsumerThreads) {
       const int row = idx / (DV / 2), col = 2 * (idx % (DV / 2));
@@ -855,13 +898,13 @@ __global__ void __launch_bounds__(128) decode_walk_kernel(const DecodeParams p) 
   const int* s_len = reinterpret_cast<const int*>(smem + L.seqlen);
   const int* s_nt = reinterpret_cast<const int*>(smem + L.nt);
   const int* s_pref = reinterpret_cast<const int*>(smem + L.pref);
-  const int len0 = decode_early_loads(p);
+  const int len0 = decode_early_loads<false>(p);
   CtaRange cr;
   if (p.Bv <= 32) {  // the decode kernel's fast prologue, run the same way
     if (threadIdx.x >= 32) return;
-    cr = decode_plan_warp(p, smem, L, len0);
+    cr = decode_plan_warp<false>(p, smem, L, len0);
   } else {
-    cr.pl = decode_prologue(p, smem, L, false, len0);
+    cr.pl = decode_prologue<false>(p, smem, L, false, len0);
     cr.a0 = range_cut(blockIdx.x, cr.pl, s_pref, s_nt, p.Bv, p.Hkv);
     cr.a1 = range_cut(blockIdx.x + 1, cr.pl, s_pref, s_nt, p.Bv, p.Hkv);
   }
@@ -871,7 +914,7 @@ __global__ void __launch_bounds__(128) decode_walk_kernel(const DecodeParams p) 
   const int a0 = cr.a0, a1 = cr.a1;
   for (int f = a0; f < a1;) {
     const Piece pc = locate_piece(f, a1, s_pref, s_nt, p.Bv, p.Hkv);
-    const VSeq sq = decode_vseq(pc.b, s_len[pc.b / p.nck], p);
+    const VSeq sq = decode_vseq<false>(pc.b, s_len[pc.b], p);
     const int* trow = p.block_table + static_cast<size_t>(sq.b) * p.max_blocks;
     for (int t = 0; t < pc.n; ++t) {
       const int tile = sq.tile_first + pc.i0 + t;
@@ -897,24 +940,25 @@ int decode_smem_bytes(int nstages, int B, int Bv, int kpc, int g, int dv) {
   return DecodeSmem(nstages, B, Bv, kpc, g, dv).total + 1024;
 }
 
+template <int DV, bool MULTI>
+static cudaError_t launch_decode_as(const DecodeLaunch& L, int smem, cudaStream_t stream) {
+  cudaError_t e = cudaFuncSetAttribute(decode_kernel<DV, MULTI>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  decode_kernel<DV, MULTI><<<L.grid, kDecodeThreads, smem, stream>>>(L.tm_q, L.tm_k, L.tm_v,
+                                                                     L.tm_rel, L.p);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_decode(const DecodeLaunch& L, cudaStream_t stream) {
   const DecodeParams& p = L.p;
   const int smem = decode_smem_bytes(p.nstages, p.B, p.Bv, p.kpc, p.g, p.dv);
-  cudaError_t e;
-  if (p.dv == 128) {
-    e = cudaFuncSetAttribute(decode_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             smem);
-    if (e != cudaSuccess) return e;
-    decode_kernel<128><<<L.grid, kDecodeThreads, smem, stream>>>(L.tm_q, L.tm_k, L.tm_v,
-                                                                 L.tm_rel, p);
-  } else {
-    e = cudaFuncSetAttribute(decode_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             smem);
-    if (e != cudaSuccess) return e;
-    decode_kernel<64><<<L.grid, kDecodeThreads, smem, stream>>>(L.tm_q, L.tm_k, L.tm_v,
-                                                                L.tm_rel, p);
-  }
-  return cudaGetLastError();
+  const bool multi = p.k > 1;
+  if (p.dv == 128)
+    return multi ? launch_decode_as<128, true>(L, smem, stream)
+                 : launch_decode_as<128, false>(L, smem, stream);
+  return multi ? launch_decode_as<64, true>(L, smem, stream)
+               : launch_decode_as<64, false>(L, smem, stream);
 }
 
 cudaError_t launch_decode_walk(const DecodeParams& p, int grid, cudaStream_t stream) {

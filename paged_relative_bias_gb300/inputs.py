@@ -170,6 +170,23 @@ def make_decode(wl: DecodeWorkload, device="cpu", seed_data: int = 0,
         window=wl.window, rel_extent=wl.rel_extent, workload=wl)
 
 
+def relayout_decode(case: dict, seed: int) -> dict:
+    """Another decode call over the same KV pool: fresh q and rel, and the
+    block table renumbered through a random permutation of the pool, so that
+    the call reads other blocks.  Entries of -1 stay -1."""
+    dev = case["q"].device
+    pool = case["k_cache"].shape[0]
+    perm = torch.randperm(pool, generator=_gen("cpu", seed), device="cpu").to(torch.int32)
+    t = case["block_table"].cpu()
+    table = torch.where(t >= 0, perm[t.clamp(min=0).long()], t)
+    g = _gen(dev, seed)
+    out = dict(case)
+    out.update(q=_randn(tuple(case["q"].shape), g, dev, torch.bfloat16),
+               rel=_randn(tuple(case["rel"].shape), g, dev, torch.float32),
+               block_table=table.to(dev))
+    return out
+
+
 def make_prefill(wl: PrefillWorkload, device="cpu", seed_data: int = 0,
                  seed_layout: int = 1) -> dict:
     """Inputs of one chunked-prefill call; every tensor lives on ``device``."""
