@@ -42,6 +42,7 @@ constexpr int kDecodeThreads = 32 * (1 + kConsumerWarps);
 constexpr int kConsumerThreads = 32 * kConsumerWarps;
 constexpr int kWholeSlackTiles = 4;  // tolerated imbalance to avoid a split
 constexpr int kQBufBytes = 4096;     // 16 rows x 256 B as two swizzled halves
+constexpr int kMiscAbort = 14;       // shared flag word: a consumer warp gave up waiting
 constexpr int kSlicePad = 8;         // floats of padding per merge-slice row (bank spread)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kNegInf = -__builtin_huge_valf();
@@ -138,11 +139,30 @@ __device__ __forceinline__ VSeq decode_vseq(int vb, int len, const DecodeParams&
 // checks batch * kv heads * tiles per sequence < 2^31), so the cut arithmetic
 // is 32-bit: no 64-bit division on the kernel's start-up path.
 struct Plan {
-  int T;      // tiles of all segments
-  int G;      // CTAs with work: min(gridDim.x, T)
-  int whole;  // 1: cuts snap to segment boundaries
-  int tq, tr; // T / G and T % G
+  int T;        // tiles of all segments
+  int G;        // CTAs with work: min(gridDim.x, T), or the segment count when per_cta
+  int whole;    // 1: cuts snap to segment boundaries
+  int per_cta;  // 1: whole, and no more segments than CTAs: CTA c takes segment c
+  int tq, tr;   // T / G and T % G (exact cuts)
 };
+
+// The plan from the tile total, the longest segment and the segment count.
+// When whole segments balance (the longest is within kWholeSlackTiles of a
+// CTA's share) and there are no more segments than CTAs, the best cut is one
+// segment per CTA, and CTA c's segment follows from c alone.
+__device__ __forceinline__ Plan make_plan(int T, int mx, int nseg) {
+  Plan pl;
+  const int grid = static_cast<int>(gridDim.x);
+  pl.T = T;
+  pl.G = min(grid, T);
+  pl.whole = pl.G > 0 && static_cast<long long>(mx) * pl.G <=
+                             T + static_cast<long long>(kWholeSlackTiles) * pl.G;
+  pl.tq = pl.G > 0 ? T / pl.G : 0;
+  pl.tr = pl.G > 0 ? T - pl.tq * pl.G : 0;
+  pl.per_cta = pl.whole && nseg <= grid;
+  if (pl.per_cta) pl.G = nseg;
+  return pl;
+}
 
 // The piece of a CTA's range that falls in one (sequence, KV head) segment.
 struct Piece {
@@ -191,6 +211,11 @@ __device__ __forceinline__ int cta_of(int f, const Plan& pl) {
 // boundary in whole-segment mode.
 __device__ __forceinline__ int range_cut(int c, const Plan& pl, const int* s_pref,
                                          const int* s_nt, int B, int Hkv) {
+  if (pl.per_cta) {  // the start of segment c (c < nseg), else the end
+    if (c >= pl.G) return pl.T;
+    const int b = c / Hkv;
+    return Hkv * s_pref[b] + (c - b * Hkv) * s_nt[b];
+  }
   int f = exact_cut(c, pl);
   if (pl.whole && f > 0 && f < pl.T) {
     const int b = seq_of(f, s_pref, B, Hkv);
@@ -258,20 +283,34 @@ struct CtaRange {
 // registers, with no block-wide barrier on the way to the first copy.  The
 // results are published in shared memory for the other warps.  Same cut
 // arithmetic as range_cut.  len0: seq_lens[lane], already loaded.
-template <bool MULTI>
+//
+// The plan is known from two warp reductions (tile total, longest segment)
+// before the prefix scan; when it gives CTA c segment c, early(b, kvh, len)
+// runs right then, with the segment's chunk, KV head and sequence length, so
+// that the copies it starts overlap the rest of the planning.
+template <bool MULTI, typename Early>
 __device__ CtaRange decode_plan_warp(const DecodeParams& p, uint8_t* smem, const DecodeSmem& L,
-                                     int len0) {
+                                     int len0, Early&& early) {
   const Tok<MULTI> t(p);
   int* s_len = reinterpret_cast<int*>(smem + L.seqlen);
   int* s_nt = reinterpret_cast<int*>(smem + L.nt);
   int* s_pref = reinterpret_cast<int*>(smem + L.pref);
   int* s_misc = reinterpret_cast<int*>(smem + L.misc);
   const int lane = threadIdx.x & 31;
+  const int c = blockIdx.x;
+  const int cb = c / p.Hkv;  // chunk of segment c (one segment per CTA)
   const bool has = lane < p.Bv;
   const int len = MULTI ? __shfl_sync(0xffffffffu, len0, min(lane / t.nck, 31))  // my chunk's
                        : len0;                                                 // sequence
   const int nt = has ? decode_vseq<MULTI>(lane, len, p).ntiles : 0;
   if (has && nt == 0 && blockIdx.x == 0) report(p.status, RELATTN_DEV_BAD_LENGTH);
+  const int mx = __reduce_max_sync(0xffffffffu, nt);
+  const int total = static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<unsigned>(nt)));
+  CtaRange cr;
+  cr.pl = make_plan(p.Hkv * total, mx, p.Bv * p.Hkv);
+  const Plan& pl = cr.pl;
+  const bool mine = pl.per_cta && c < pl.G;
+  if (mine) early(cb, c - cb * p.Hkv, __shfl_sync(0xffffffffu, len, cb));
   int incl = nt;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -279,8 +318,6 @@ __device__ CtaRange decode_plan_warp(const DecodeParams& p, uint8_t* smem, const
     if (lane >= o) incl += v;
   }
   const int excl = incl - nt;
-  const int total = __shfl_sync(0xffffffffu, incl, 31);
-  const int mx = __reduce_max_sync(0xffffffffu, nt);
   if (lane < p.B) s_len[lane] = len0;
   if (has) {
     s_nt[lane] = nt;
@@ -290,14 +327,6 @@ __device__ CtaRange decode_plan_warp(const DecodeParams& p, uint8_t* smem, const
     s_pref[p.Bv] = total;
     s_misc[0] = mx;
   }
-  CtaRange cr;
-  Plan& pl = cr.pl;
-  pl.T = p.Hkv * total;
-  pl.G = min(static_cast<int>(gridDim.x), pl.T);
-  pl.whole = pl.G > 0 && static_cast<long long>(mx) * pl.G <=
-                             pl.T + static_cast<long long>(kWholeSlackTiles) * pl.G;
-  pl.tq = pl.G > 0 ? pl.T / pl.G : 0;
-  pl.tr = pl.G > 0 ? pl.T - pl.tq * pl.G : 0;
   auto cut = [&](int c) -> int {  // range_cut, warp-wide
     int f = c * pl.tq + (c * pl.tr) / pl.G;
     if (pl.whole && f > 0 && f < pl.T) {
@@ -312,7 +341,22 @@ __device__ CtaRange decode_plan_warp(const DecodeParams& p, uint8_t* smem, const
     }
     return f;
   };
-  const int c = blockIdx.x;
+  if (pl.per_cta) {
+    // segment c: chunk c / Hkv, KV head c % Hkv, all its tiles
+    const int b = mine ? cb : 0;
+    const int ntb = __shfl_sync(0xffffffffu, nt, b);
+    const int base = p.Hkv * __shfl_sync(0xffffffffu, excl, b);
+    Piece& pc = cr.first;
+    pc.b = b;
+    pc.kvh = c - b * p.Hkv;
+    pc.i0 = 0;
+    pc.n = ntb;
+    pc.seg_start = base + pc.kvh * ntb;
+    pc.seg_end = pc.seg_start + ntb;
+    cr.a0 = mine ? pc.seg_start : 0;
+    cr.a1 = mine ? pc.seg_end : 0;
+    cr.has_first = cr.a0 < cr.a1;
+  } else {
   cr.a0 = c < pl.G ? cut(c) : 0;
   cr.a1 = c < pl.G ? cut(c + 1) : 0;
   // the first piece, as locate_piece(a0, a1) finds it
@@ -330,6 +374,7 @@ __device__ CtaRange decode_plan_warp(const DecodeParams& p, uint8_t* smem, const
     pc.seg_end = pc.seg_start + ntb;
     pc.n = min(cr.a1, pc.seg_end) - cr.a0;
   }
+  }
   if (lane == 0) {
     s_misc[2] = pl.T;
     s_misc[3] = pl.G;
@@ -338,6 +383,7 @@ __device__ CtaRange decode_plan_warp(const DecodeParams& p, uint8_t* smem, const
     s_misc[6] = pl.tr;
     s_misc[7] = cr.a0;
     s_misc[8] = cr.a1;
+    s_misc[9] = pl.per_cta;
   }
   __syncwarp();
   return cr;
@@ -354,6 +400,7 @@ __device__ __forceinline__ CtaRange decode_plan_read(const uint8_t* smem, const 
   cr.pl.tr = s_misc[6];
   cr.a0 = s_misc[7];
   cr.a1 = s_misc[8];
+  cr.pl.per_cta = s_misc[9];
   return cr;
 }
 
@@ -419,14 +466,7 @@ __device__ Plan decode_prologue(const DecodeParams& p, uint8_t* smem, const Deco
   }
   __syncthreads();
   if (zero_bad) decode_zero_bad<MULTI>(p, s_nt, tid, blockDim.x);
-  Plan pl;
-  pl.T = p.Hkv * s_pref[p.Bv];
-  pl.G = min(static_cast<int>(gridDim.x), pl.T);
-  pl.whole = pl.G > 0 && static_cast<long long>(s_misc[0]) * pl.G <=
-                             pl.T + static_cast<long long>(kWholeSlackTiles) * pl.G;
-  pl.tq = pl.G > 0 ? pl.T / pl.G : 0;
-  pl.tr = pl.G > 0 ? pl.T - pl.tq * pl.G : 0;
-  return pl;
+  return make_plan(p.Hkv * s_pref[p.Bv], s_misc[0], p.Bv * p.Hkv);
 }
 
 template <int DV, bool MULTI>
@@ -454,36 +494,113 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int len0 = decode_early_loads<MULTI>(p);
 
-  if (tid == 0) {
-    for (int s = 0; s < ns; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kConsumerWarps / 2);
-    }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&qfull[s], 1);
-      mbar_init(&qempty[s], kConsumerWarps);
-    }
+  // Barriers full[ns], empty[ns], qfull[2], qempty[2], one per lane of
+  // warp 0, so that their set-up costs the producer one step.
+  if (warp == 0) {
+    if (lane < 2 * ns + 4)
+      mbar_init(&full[lane], lane < ns ? 1
+                             : lane < 2 * ns ? kConsumerWarps / 2
+                             : lane < 2 * ns + 2 ? 1 : kConsumerWarps);
     fence_mbar_init();
-    tma_prefetch_desc(&tm_q);
-    tma_prefetch_desc(&tm_k);
-    tma_prefetch_desc(&tm_v);
-    tma_prefetch_desc(&tm_rel);
+    if (lane == 0) {
+      s_misc[kMiscAbort] = 0;
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      tma_prefetch_desc(&tm_rel);
+    }
+    __syncwarp();
   }
-  // Query rows g..15 of both buffers stay zero.  With the warp-0 prologue
-  // (B <= 32) the producer starts its copies before the other warps reach a
-  // barrier, so warp 0 clears the buffers itself.
-  {
-    const int zt = p.Bv <= 32 ? 32 : kDecodeThreads;
-    if (tid < zt)
-      for (int i = tid; i < 2 * kQBufBytes / 16; i += zt)
-        reinterpret_cast<uint4*>(smem + L.qbuf)[i] = make_uint4(0, 0, 0, 0);
-  }
-  fence_proxy_async_smem();
+  // Query rows past a chunk's kc * g are never written or cleared: the MMA
+  // rows, the softmax rows and the merge rows are independent, and those
+  // rows' results are dropped, whatever the bits there.
+  const int q_tx = 2 * tok.kpc * g * 64 * 2;  // kpc tokens x g heads, two halves
+  // The query rows of chunk sq, KV head kvh into buffer qb (one lane):
+  // rows token * g + head, tokens i0 .. i0 + kpc - 1 (rows past its kc
+  // tokens are read but never used).  False on a wait timeout.
+  auto issue_q = [&](int qb, int kvh, const VSeq& sq, int parity) -> bool {
+    if (!mbar_wait(&qempty[qb], parity)) {
+      report(p.status, RELATTN_DEV_WAIT_TIMEOUT);
+      return false;
+    }
+    uint8_t* qs = smem + L.qbuf + qb * kQBufBytes;
+    mbar_arrive_expect_tx(&qfull[qb], q_tx);
+    if constexpr (MULTI) {
+      tma_load_3d(qs, &tm_q, &qfull[qb], 0, kvh * g, sq.b * tok.k + sq.i0);
+      tma_load_3d(qs + 2048, &tm_q, &qfull[qb], 64, kvh * g, sq.b * tok.k + sq.i0);
+    } else {  // q [B * Hq][128]: the g rows of the group
+      tma_load_2d(qs, &tm_q, &qfull[qb], 0, sq.b * p.Hq + kvh * g);
+      tma_load_2d(qs + 2048, &tm_q, &qfull[qb], 64, sq.b * p.Hq + kvh * g);
+    }
+    return true;
+  };
+  const int stage_tx = 16384 + kTileKeys * DV * 2;
+  const int rel_tx = g * kRelBoxW * 4;         // one token's rel box
+  const int rel_stride = rel_token_bytes(g);  // its place in a stage's rel slice
+  // K, V and rel of tile `tile` of chunk sq, KV head kvh, into the stage of
+  // CTA tile nn (one lane per tile); 1 on a wait timeout.
+  auto issue_tile = [&](int nn, int tile, int id, const VSeq& sq, int kvh) -> int {
+    const int stage = nn % ns;
+    if (!mbar_wait(&empty[stage], ((nn / ns) & 1) ^ 1)) {
+      report(p.status, RELATTN_DEV_WAIT_TIMEOUT);
+      return 1;
+    }
+    const bool ok = id >= 0 && id < p.num_blocks;
+    s_valid[stage] = ok ? 1 : 0;
+    if (ok) {
+      const int key0 = tile * kTileKeys;
+      // token i's rel box: its g rows from distance dmin_i rounded down to
+      // 16 bytes, where dmin_i = (pf + i) - key0 - 63; tokens whose every
+      // distance here is past rel_extent need none
+      const int dmin0 = sq.pf - key0 - (kTileKeys - 1);
+      const int nrel = max(0, min(sq.kc, p.rel_extent - dmin0));
+      mbar_arrive_expect_tx(&full[stage], stage_tx + nrel * rel_tx);
+      uint8_t* st = smem + L.stages + stage * L.stage_bytes;
+      const int row = id * kBlockSize + (tile & 1) * kTileKeys;
+      tma_load_4d(st, &tm_k, &full[stage], 0, row, 0, kvh);
+      tma_load_4d(st + 16384, &tm_v, &full[stage], 0, row, 0, kvh);
+      for (int i = 0; i < nrel; ++i)
+        tma_load_2d(smem + L.rel + stage * L.rel_bytes + i * rel_stride, &tm_rel, &full[stage],
+                    (dmin0 + i) & ~3, (sq.b * tok.k + sq.i0 + i) * p.Hq + kvh * g);
+    } else {
+      report(p.status, RELATTN_DEV_BAD_BLOCK_ID);
+      mbar_arrive(&full[stage]);
+    }
+    return 0;
+  };
+  // With one segment per CTA the producer knows its first piece as soon as
+  // the plan is: it starts the query copy, loads the block ids and sends the
+  // first batch of tiles (tile 0 first, so that its data leads) then.
+  bool early_q = false;  // warp 0: first piece's query copy and first batch issued
+  int early_id = 0;      // warp 0, lane j: block j of the piece's first 32 tiles
+  int early_n = 0;       // tiles of that first batch
+  int early_bad = 0;     // a wait in it timed out
+  auto early = [&](int vb, int kvh, int len) {
+    const VSeq sq = decode_vseq<MULTI>(vb, len, p);
+    if (sq.ntiles == 0) return;
+    int ok = 1;
+    if (lane == 0) ok = issue_q(0, kvh, sq, 1) ? 1 : 0;
+    early_q = __shfl_sync(0xffffffffu, ok, 0) != 0;
+    if (!early_q) return;
+    const int cn = min(32, sq.ntiles);
+    const int blk0 = sq.tile_first >> 1;
+    const int nb = ((sq.tile_first + cn - 1) >> 1) - blk0 + 1;
+    const int* trow = p.block_table + static_cast<size_t>(sq.b) * p.max_blocks;
+    early_id = lane < nb ? __ldg(trow + blk0 + lane) : 0;
+    const int bn = min(ns, cn);
+    const int tile = sq.tile_first + (lane < bn ? lane : 0);
+    const int id = __shfl_sync(0xffffffffu, early_id, (tile >> 1) - blk0);
+    int bad = 0;
+    if (lane == 0) bad = issue_tile(0, tile, id, sq, kvh);
+    if (lane > 0 && lane < bn) bad = issue_tile(lane, tile, id, sq, kvh);
+    early_n = bn;
+    early_bad = __any_sync(0xffffffffu, bad != 0) ? 1 : 0;
+  };
   CtaRange cr;
   if (p.Bv <= 32) {
     // warp 0 plans alone and lets the consumers go with a non-blocking arrive
     if (warp == 0) {
-      cr = decode_plan_warp<MULTI>(p, smem, L, len0);
+      cr = decode_plan_warp<MULTI>(p, smem, L, len0, early);
       named_barrier_arrive(2, kDecodeThreads);
     } else {
       named_barrier(2, kDecodeThreads);
@@ -500,96 +617,43 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   if (static_cast<int>(blockIdx.x) >= pl.G) return;
   const int c = blockIdx.x;
   const int a0 = cr.a0, a1 = cr.a1;
-  const int stage_tx = 16384 + kTileKeys * DV * 2;
-  const int rel_tx = g * kRelBoxW * 4;         // one token's rel box
-  const int rel_stride = rel_token_bytes(g);  // its place in a stage's rel slice
-  const int q_tx = 2 * tok.kpc * g * 64 * 2;  // kpc tokens x g heads, two halves
-
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     int n = 0;     // CTA tile counter
     int k = 0;     // CTA piece counter
-    bool abort = false;
+    bool abort = early_bad != 0;
     for (int f = a0; f < a1 && !abort; ++k) {
       const Piece pc = (k == 0 && cr.has_first && warp == 0)
                            ? cr.first
                            : locate_piece(f, a1, s_pref, s_nt, p.Bv, p.Hkv);
       const VSeq sq = decode_vseq<MULTI>(pc.b, s_len[pc.b / tok.nck], p);
       const int* trow = p.block_table + static_cast<size_t>(sq.b) * p.max_blocks;
+      const bool pre = k == 0 && early_q;  // first piece: its first batch is out
       int bad = 0;
-      if (lane == 0) {
-        const int qb = k & 1;
-        if (!mbar_wait(&qempty[qb], ((k >> 1) & 1) ^ 1)) {
-          report(p.status, RELATTN_DEV_WAIT_TIMEOUT);
-          bad = 1;
-        } else {
-          // rows token * g + head: tokens i0 .. i0 + kpc - 1 of the chunk
-          // (rows past its kc tokens are read but never used)
-          uint8_t* qs = smem + L.qbuf + qb * kQBufBytes;
-          mbar_arrive_expect_tx(&qfull[qb], q_tx);
-          if constexpr (MULTI) {
-            tma_load_3d(qs, &tm_q, &qfull[qb], 0, pc.kvh * g, sq.b * tok.k + sq.i0);
-            tma_load_3d(qs + 2048, &tm_q, &qfull[qb], 64, pc.kvh * g, sq.b * tok.k + sq.i0);
-          } else {  // q [B * Hq][128]: the g rows of the group
-            tma_load_2d(qs, &tm_q, &qfull[qb], 0, sq.b * p.Hq + pc.kvh * g);
-            tma_load_2d(qs + 2048, &tm_q, &qfull[qb], 64, sq.b * p.Hq + pc.kvh * g);
-          }
-        }
-      }
+      if (lane == 0 && !pre) bad = issue_q(k & 1, pc.kvh, sq, ((k >> 1) & 1) ^ 1) ? 0 : 1;
       abort = __shfl_sync(0xffffffffu, bad, 0) != 0;
       bad = 0;
+      if (pre) n = early_n;
       for (int c0 = 0; c0 < pc.n && !abort; c0 += 32) {
         const int cn = min(32, pc.n - c0);
         const int tile0 = sq.tile_first + pc.i0 + c0;
         const int blk0 = tile0 >> 1;
         const int nb = ((tile0 + cn - 1) >> 1) - blk0 + 1;
-        const int myid = lane < nb ? __ldg(trow + blk0 + lane) : 0;
+        const int myid = pre && c0 == 0 ? early_id : lane < nb ? __ldg(trow + blk0 + lane) : 0;
         // Batches of at most ns tiles, one per lane: their stages are all
         // different, so each lane waits on its own stage one phase ahead at
         // most, and the copies of a batch go out in one pass of the warp.
-        // K, V and rel of tile `tile` (CTA tile nn) into its stage; 1 on a
-        // wait timeout
-        auto issue = [&](int nn, int tile, int id) -> int {
-          const int stage = nn % ns;
-          if (!mbar_wait(&empty[stage], ((nn / ns) & 1) ^ 1)) {
-            report(p.status, RELATTN_DEV_WAIT_TIMEOUT);
-            return 1;
-          }
-          const bool ok = id >= 0 && id < p.num_blocks;
-          s_valid[stage] = ok ? 1 : 0;
-          if (ok) {
-            const int key0 = tile * kTileKeys;
-            // token i's rel box: its g rows from distance dmin_i rounded down
-            // to 16 bytes, where dmin_i = (pf + i) - key0 - 63; tokens whose
-            // every distance here is past rel_extent need none
-            const int dmin0 = sq.pf - key0 - (kTileKeys - 1);
-            const int nrel = max(0, min(sq.kc, p.rel_extent - dmin0));
-            mbar_arrive_expect_tx(&full[stage], stage_tx + nrel * rel_tx);
-            uint8_t* st = smem + L.stages + stage * L.stage_bytes;
-            const int row = id * kBlockSize + (tile & 1) * kTileKeys;
-            tma_load_4d(st, &tm_k, &full[stage], 0, row, 0, pc.kvh);
-            tma_load_4d(st + 16384, &tm_v, &full[stage], 0, row, 0, pc.kvh);
-            for (int i = 0; i < nrel; ++i)
-              tma_load_2d(smem + L.rel + stage * L.rel_bytes + i * rel_stride, &tm_rel,
-                          &full[stage], (dmin0 + i) & ~3,
-                          (sq.b * tok.k + sq.i0 + i) * p.Hq + pc.kvh * g);
-          } else {
-            report(p.status, RELATTN_DEV_BAD_BLOCK_ID);
-            mbar_arrive(&full[stage]);
-          }
-          return 0;
-        };
-        for (int jb = 0; jb < cn && !abort; jb += ns) {
+        for (int jb = pre && c0 == 0 ? early_n : 0; jb < cn && !abort; jb += ns) {
           const int bn = min(ns, cn - jb);
           const int j = jb + (lane < bn ? lane : 0);
           const int tile = tile0 + j;
           const int id = __shfl_sync(0xffffffffu, myid, (tile >> 1) - blk0);
           if (c0 == 0 && jb == 0) {
             // the piece's first tile goes out alone, so that its data leads
-            if (lane == 0) bad |= issue(n, tile, id);
-            if (lane > 0 && lane < bn) bad |= issue(n + lane, tile, id);
+            if (lane == 0) bad |= issue_tile(n, tile, id, sq, pc.kvh);
+            if (lane > 0 && lane < bn) bad |= issue_tile(n + lane, tile, id, sq, pc.kvh);
           } else if (lane < bn) {
-            bad |= issue(n + lane, tile, id);
+            bad |= issue_tile(n + lane, tile, id, sq, pc.kvh);
           }
           n += bn;
           abort = __any_sync(0xffffffffu, bad != 0);
@@ -779,7 +843,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&qempty[qb]);  // the piece's query rows are done
-    if (abort) break;
+    // A wait that gave up in any consumer warp ends the piece loop of all
+    // eight at the same point: each still reaches the next named barrier,
+    // and after it they all see the flag.
+    if (abort && lane == 0) s_misc[kMiscAbort] = 1;
     n_base += pc.n;
 
     // ---- merge the eight consumer warps of this piece
@@ -793,6 +860,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       }
     }
     named_barrier(1, kConsumerThreads);
+    if (s_misc[kMiscAbort]) break;
     const int srows = tok.kpc * g;  // rows of a warp's merge slice
 #pragma unroll
     for (int rr = 0; rr < 2; ++rr) {
@@ -902,7 +970,7 @@ __global__ void __launch_bounds__(128) decode_walk_kernel(const DecodeParams p) 
   CtaRange cr;
   if (p.Bv <= 32) {  // the decode kernel's fast prologue, run the same way
     if (threadIdx.x >= 32) return;
-    cr = decode_plan_warp<false>(p, smem, L, len0);
+    cr = decode_plan_warp<false>(p, smem, L, len0, [](int, int, int) {});
   } else {
     cr.pl = decode_prologue<false>(p, smem, L, false, len0);
     cr.a0 = range_cut(blockIdx.x, cr.pl, s_pref, s_nt, p.Bv, p.Hkv);
