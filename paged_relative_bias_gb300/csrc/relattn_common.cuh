@@ -49,6 +49,19 @@ __device__ __forceinline__ void named_barrier_arrive(int id, int nthreads) {
   asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// Programmatic dependent launch.  launch_dependents lets the next kernel on
+// the stream (launched with programmatic stream serialisation) start once
+// every CTA of this grid has issued it; grid_dep_wait blocks until the grids
+// this one depends on have completed and their memory is visible.  Both are
+// no-ops for a kernel launched without the attribute.
+__device__ __forceinline__ void grid_dep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void grid_dep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 __device__ __forceinline__ void report(uint32_t* status, uint32_t bits) {
   if (status) atomicOr(status, bits);
 }

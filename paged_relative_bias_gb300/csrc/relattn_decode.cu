@@ -492,7 +492,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   const int* s_pref = reinterpret_cast<const int*>(smem + L.pref);
   int* s_misc = reinterpret_cast<int*>(smem + L.misc);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int len0 = decode_early_loads<MULTI>(p);
+  // The next kernel on the stream may start launching now; it waits for this
+  // one to finish before it touches global memory, as this one does below.
+  grid_dep_launch_dependents();
 
   // Barriers full[ns], empty[ns], qfull[2], qempty[2], one per lane of
   // warp 0, so that their set-up costs the producer one step.
@@ -511,6 +513,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     }
     __syncwarp();
   }
+  // Everything above touches only shared memory and the kernel parameters;
+  // every global access comes after the kernels before this one are done.
+  grid_dep_wait();
+  const int len0 = decode_early_loads<MULTI>(p);
   // Query rows past a chunk's kc * g are never written or cleared: the MMA
   // rows, the softmax rows and the merge rows are independent, and those
   // rows' results are dropped, whatever the bits there.
@@ -1013,9 +1019,20 @@ static cudaError_t launch_decode_as(const DecodeLaunch& L, int smem, cudaStream_
   cudaError_t e = cudaFuncSetAttribute(decode_kernel<DV, MULTI>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  decode_kernel<DV, MULTI><<<L.grid, kDecodeThreads, smem, stream>>>(L.tm_q, L.tm_k, L.tm_v,
-                                                                     L.tm_rel, L.p);
-  return cudaGetLastError();
+  // Programmatic stream serialisation: the kernel may begin while the
+  // previous kernel on the stream finishes (see grid_dep_wait in the kernel).
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(L.grid);
+  cfg.blockDim = dim3(kDecodeThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_kernel<DV, MULTI>, L.tm_q, L.tm_k, L.tm_v, L.tm_rel,
+                            L.p);
 }
 
 cudaError_t launch_decode(const DecodeLaunch& L, cudaStream_t stream) {
