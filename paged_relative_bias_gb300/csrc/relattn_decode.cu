@@ -762,40 +762,54 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         // rounded down to 16 bytes.
         const float* relt = reinterpret_cast<const float*>(smem + L.rel + stage * L.rel_bytes);
         const bool edge = key0 < lo_last || key0 + kTileKeys - 1 > sq.pf;  // any mask?
+        // this thread's keys are kb + e, e in {0, 1, 8, 9}; a row keeps the
+        // keys with e in [mlo, mhi] (all of them when no key of the tile is
+        // masked) -- compares with immediates and selects, no branches
+        const int kb = key0 + 16 * cw + cq * 2;
         float x[2][4];
         if constexpr (!MULTI) {
           // one position for all rows: one box, present or not for the tile
           const int dmin = sq.pf - key0 - (kTileKeys - 1);
           const bool need_rel = dmin < p.rel_extent;
           const int d0 = dmin & ~3;
+          const int mlo = edge ? sq.lo - kb : INT_MIN, mhi = edge ? sq.pf - kb : INT_MAX;
 #pragma unroll
           for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
               const int row = r0 + (i >> 1) * 8;
-              const int key = key0 + 16 * cw + nt * 8 + cq * 2 + (i & 1);
+              const int e = nt * 8 + (i & 1);
+              const int key = kb + e;
               float bias = 0.f;
               if (need_rel && row < g) bias = relt[row * kRelBoxW + (sq.pf - key - d0)];
-              float v = fmaf(s[nt][i], p.scale_log2, bias * kLog2e);
-              if (edge && (key < sq.lo || key > sq.pf)) v = kNegInf;
-              x[nt][i] = v;
+              const float v = fmaf(s[nt][i], p.scale_log2, bias * kLog2e);
+              x[nt][i] = (e < mlo || e > mhi) ? kNegInf : v;
             }
         } else {
-          int d0[2];
+          // per row: its token's box, present when the row's smallest
+          // distance in the tile is below rel_extent (the box reads 0 past
+          // it), and the box entry of key key0 -- the others at -offset
+          bool nr[2];
+          const float* rb[2];
+          int mlo[2], mhi[2];
 #pragma unroll
-          for (int rr = 0; rr < 2; ++rr) d0[rr] = (rP[rr] - key0 - (kTileKeys - 1)) & ~3;
+          for (int rr = 0; rr < 2; ++rr) {
+            const int dmin = rP[rr] - key0 - (kTileKeys - 1);
+            nr[rr] = rv[rr] && dmin < p.rel_extent;
+            rb[rr] = relt + rrel[rr] + (rP[rr] - key0 - (dmin & ~3));
+            mlo[rr] = edge ? rlo[rr] - kb : INT_MIN;
+            mhi[rr] = edge ? rP[rr] - kb : INT_MAX;
+          }
 #pragma unroll
           for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
               const int rr = i >> 1;
-              const int key = key0 + 16 * cw + nt * 8 + cq * 2 + (i & 1);
-              const int dist = rP[rr] - key;
-              float bias = 0.f;
-              if (rv[rr] && dist < p.rel_extent) bias = relt[rrel[rr] + (dist - d0[rr])];
-              float v = fmaf(s[nt][i], p.scale_log2, bias * kLog2e);
-              if (edge && (key < rlo[rr] || key > rP[rr])) v = kNegInf;
-              x[nt][i] = v;
+              const int e = nt * 8 + (i & 1);
+              const int ko = 16 * cw + cq * 2 + e;
+              const float bias = nr[rr] ? rb[rr][-ko] : 0.f;
+              const float v = fmaf(s[nt][i], p.scale_log2, bias * kLog2e);
+              x[nt][i] = (e < mlo[rr] || e > mhi[rr]) ? kNegInf : v;
             }
         }
         // online softmax, rows r0 (rr=0) and r0+8 (rr=1)
