@@ -174,6 +174,42 @@ int relattn_decode_multi(const void* q, const float* rel,
                          void* out, void* workspace, size_t workspace_bytes,
                          void* stream);
 
+/*
+ * Element types of rel and out for the *_ex entry points.  The plain entry
+ * points take fp32 rel and write bf16 out.
+ *
+ *  - bf16 rel halves the bytes of the relative-logit input, which is most of
+ *    a chunked prefill's traffic (fp32 [T][Hq][E]); rel is the product
+ *    r @ rel_logits_proj of the layer's fused QKVR projection ("Inkling-Small
+ *    on Gaudi 2", section "Attention with a relative bias"), which a bf16
+ *    model produces in bf16.  Reading: the bias is the bf16 value widened
+ *    exactly; everything else is unchanged.
+ *  - fp32 out: the attention output kept in fp32, as the vLLM port of
+ *    Inkling 2 Small does ("Inkling 2 Small on vLLM", section 准确率评估,
+ *    accuracy evaluation).
+ */
+#define RELATTN_DTYPE_F32 0
+#define RELATTN_DTYPE_BF16 1
+
+typedef struct relattn_io_types {
+  int32_t rel; /* RELATTN_DTYPE_F32 or RELATTN_DTYPE_BF16 */
+  int32_t out; /* RELATTN_DTYPE_BF16 or RELATTN_DTYPE_F32 */
+} relattn_io_types;
+
+/*
+ * relattn_decode_multi with the element types of rel and out given by
+ * `types` (k = 1 is relattn_decode).  rel is [B][k][Hq][rel_extent] of
+ * types->rel; out is [B][k][Hq][d_v] of types->out.  A bf16 rel needs
+ * rel_extent a multiple of 8 (fp32: of 4): RELATTN_ERR_UNSUPPORTED
+ * otherwise; an unknown type code is RELATTN_ERR_INVALID_ARG.  Same
+ * workspace, errors and device status as relattn_decode.
+ */
+int relattn_decode_ex(const void* q, const void* rel, const relattn_io_types* types,
+                      const relattn_kv_cache* kv_cache, const int32_t* block_table,
+                      const int32_t* seq_lens, int32_t num_query_tokens, int32_t window,
+                      int32_t rel_extent, const relattn_dims* dims, void* out,
+                      void* workspace, size_t workspace_bytes, void* stream);
+
 /* Size of the library-owned scratch array used by relattn_decode_noalloc. */
 #define RELATTN_NOALLOC_SCRATCH_BYTES (4u << 20)
 

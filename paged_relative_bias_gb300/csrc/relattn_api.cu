@@ -199,7 +199,32 @@ int relattn_read_status(const void* workspace, uint32_t* status, void* stream) {
 }
 
 // kq: query tokens per sequence (1 for relattn_decode).
-static int prepare_decode(const void* q, const float* rel, const relattn_kv_cache* cache,
+// Element types of rel and out, as the kernels see them.
+struct IoTypes {
+  int rel_es;   // bytes per rel element: 4 (fp32) or 2 (bf16)
+  int out_f32;  // 1: out is fp32, 0: bf16
+};
+constexpr IoTypes kDefaultIo = {4, 0};
+
+// From the C ABI's description; false for a combination that is not offered.
+static bool io_types(const relattn_io_types* t, IoTypes* io) {
+  if (!t) return false;
+  if (t->rel != RELATTN_DTYPE_F32 && t->rel != RELATTN_DTYPE_BF16) return false;
+  if (t->out != RELATTN_DTYPE_F32 && t->out != RELATTN_DTYPE_BF16) return false;
+  io->rel_es = t->rel == RELATTN_DTYPE_BF16 ? 2 : 4;
+  io->out_f32 = t->out == RELATTN_DTYPE_F32 ? 1 : 0;
+  return true;
+}
+
+// rel rows are TMA rows of rel_extent elements: 16-byte multiples, at least
+// one 16-byte unit.
+static bool rel_extent_ok(int32_t rel_extent, int es) {
+  const int unit = 16 / es;
+  return rel_extent >= unit && rel_extent % unit == 0;
+}
+
+static int prepare_decode(const void* q, const void* rel, IoTypes io,
+                          const relattn_kv_cache* cache,
                           const int32_t* block_table, const int32_t* seq_lens, int32_t kq,
                           int32_t window, int32_t rel_extent, const relattn_dims* dims,
                           void* out, void* workspace, size_t ws_bytes, bool walk,
@@ -212,7 +237,7 @@ static int prepare_decode(const void* q, const float* rel, const relattn_kv_cach
   if (!walk) {
     if (!q || !rel || !out) return RELATTN_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(rel) || !aligned16(out)) return RELATTN_ERR_INVALID_ARG;
-    if (rel_extent < 4 || rel_extent % 4 != 0) return RELATTN_ERR_UNSUPPORTED;
+    if (!rel_extent_ok(rel_extent, io.rel_es)) return RELATTN_ERR_UNSUPPORTED;
   }
   if (!aligned16(workspace)) return RELATTN_ERR_INVALID_ARG;
   if (!device_info(di)) return RELATTN_ERR_CUDA;
@@ -236,7 +261,9 @@ static int prepare_decode(const void* q, const float* rel, const relattn_kv_cach
   p.rel = rel;
   p.block_table = block_table;
   p.seq_lens = seq_lens;
-  p.out = static_cast<__nv_bfloat16*>(out);
+  p.out = out;
+  p.rel_es = io.rel_es;
+  p.out_f32 = io.out_f32;
   p.status = reinterpret_cast<uint32_t*>(ws);
   p.counters = reinterpret_cast<int32_t*>(ws + w.counters);
   p.part_lse = reinterpret_cast<float*>(ws + w.lse);
@@ -264,17 +291,20 @@ static int prepare_decode(const void* q, const float* rel, const relattn_kv_cach
   // own every other stage.
   p.nstages = kMaxStages;
   while (p.nstages >= 2 &&
-         decode_smem_bytes(p.nstages, p.B, p.Bv, p.kpc, p.g, p.dv) > di->smem_optin)
+         decode_smem_bytes(p.nstages, p.B, p.Bv, p.kpc, p.g, p.dv, p.rel_es) > di->smem_optin)
     p.nstages -= 2;
   if (p.nstages < 2) return RELATTN_ERR_UNSUPPORTED;  // batch too large for shared memory
   if (!decode_cache_maps(cache, &L->tm_k, &L->tm_v)) return RELATTN_ERR_CUDA;
-  // rel [B][k][Hq][E] fp32: boxes of one token's g heads x kRelBoxW distances
+  // rel [B][k][Hq][E] fp32 or bf16: boxes of one token's g heads x
+  // rel_box_w distances
   const cuuint64_t rd[2] = {static_cast<cuuint64_t>(rel_extent),
                             static_cast<cuuint64_t>(dims->batch) * kq * dims->num_q_heads};
-  const cuuint64_t rs[1] = {static_cast<cuuint64_t>(rel_extent) * 4};
-  const cuuint32_t rb[2] = {static_cast<cuuint32_t>(kRelBoxW), static_cast<cuuint32_t>(g)};
-  if (!make_map(&L->tm_rel, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(rel), rd,
-                rs, rb, CU_TENSOR_MAP_SWIZZLE_NONE))
+  const cuuint64_t rs[1] = {static_cast<cuuint64_t>(rel_extent) * io.rel_es};
+  const cuuint32_t rb[2] = {static_cast<cuuint32_t>(rel_box_w(io.rel_es)),
+                            static_cast<cuuint32_t>(g)};
+  if (!make_map(&L->tm_rel,
+                io.rel_es == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                2, const_cast<void*>(rel), rd, rs, rb, CU_TENSOR_MAP_SWIZZLE_NONE))
     return RELATTN_ERR_CUDA;
   // query rows of one chunk: q [B*k][Hq][128] bf16 as (column, head, token);
   // a box is one 64-column half of kpc tokens x g heads (rows token * g + head).
@@ -298,8 +328,8 @@ int relattn_decode(const void* q, const float* rel, const relattn_kv_cache* kv_c
                    size_t workspace_bytes, void* stream) {
   DecodeLaunch L;
   DeviceInfo di;
-  const int rc = prepare_decode(q, rel, kv_cache, block_table, seq_lens, 1, window, rel_extent,
-                                dims, out, workspace, workspace_bytes, false, &L, &di);
+  const int rc = prepare_decode(q, rel, kDefaultIo, kv_cache, block_table, seq_lens, 1, window,
+                                rel_extent, dims, out, workspace, workspace_bytes, false, &L, &di);
   if (rc != RELATTN_OK) return rc;
   return to_status(launch_decode(L, static_cast<cudaStream_t>(stream)));
 }
@@ -311,8 +341,25 @@ int relattn_decode_multi(const void* q, const float* rel, const relattn_kv_cache
                          size_t workspace_bytes, void* stream) {
   DecodeLaunch L;
   DeviceInfo di;
-  const int rc = prepare_decode(q, rel, kv_cache, block_table, seq_lens, num_query_tokens, window,
-                                rel_extent, dims, out, workspace, workspace_bytes, false, &L, &di);
+  const int rc = prepare_decode(q, rel, kDefaultIo, kv_cache, block_table, seq_lens,
+                                num_query_tokens, window, rel_extent, dims, out, workspace,
+                                workspace_bytes, false, &L, &di);
+  if (rc != RELATTN_OK) return rc;
+  return to_status(launch_decode(L, static_cast<cudaStream_t>(stream)));
+}
+
+int relattn_decode_ex(const void* q, const void* rel, const relattn_io_types* types,
+                      const relattn_kv_cache* kv_cache, const int32_t* block_table,
+                      const int32_t* seq_lens, int32_t num_query_tokens, int32_t window,
+                      int32_t rel_extent, const relattn_dims* dims, void* out, void* workspace,
+                      size_t workspace_bytes, void* stream) {
+  IoTypes io;
+  if (!io_types(types, &io)) return RELATTN_ERR_INVALID_ARG;
+  DecodeLaunch L;
+  DeviceInfo di;
+  const int rc = prepare_decode(q, rel, io, kv_cache, block_table, seq_lens, num_query_tokens,
+                                window, rel_extent, dims, out, workspace, workspace_bytes, false,
+                                &L, &di);
   if (rc != RELATTN_OK) return rc;
   return to_status(launch_decode(L, static_cast<cudaStream_t>(stream)));
 }
@@ -325,7 +372,8 @@ int relattn_debug_walk_decode(const int32_t* block_table, const int32_t* seq_len
   if (!records || !count || max_records < 0) return RELATTN_ERR_INVALID_ARG;
   DecodeLaunch L;
   DeviceInfo di;
-  const int rc = prepare_decode(nullptr, nullptr, cache, block_table, seq_lens, 1, window, 4, dims,
+  const int rc = prepare_decode(nullptr, nullptr, kDefaultIo, cache, block_table, seq_lens, 1,
+                                window, 4, dims,
                                 nullptr, workspace, workspace_bytes, true, &L, &di);
   if (rc != RELATTN_OK) return rc;
   L.p.dbg_records = records;
@@ -374,8 +422,8 @@ int relattn_decode_noalloc(const void* q, const float* rel, const relattn_kv_cac
   rc = noalloc_scratch(&scratch);
   if (rc != RELATTN_OK) return rc;
   DecodeLaunch L;
-  rc = prepare_decode(q, rel, kv_cache, block_table, seq_lens, 1, window, rel_extent, dims, out,
-                      scratch, RELATTN_NOALLOC_SCRATCH_BYTES, false, &L, &di);
+  rc = prepare_decode(q, rel, kDefaultIo, kv_cache, block_table, seq_lens, 1, window, rel_extent,
+                      dims, out, scratch, RELATTN_NOALLOC_SCRATCH_BYTES, false, &L, &di);
   if (rc != RELATTN_OK) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // The array keeps the previous call's contents: the status word and the

@@ -30,6 +30,8 @@
 //    (normalised output, base-2 log-sum-exp) per piece in the workspace; the
 //    CTA that finishes the segment last (counted with an acq_rel atomic)
 //    merges them in a fixed order.
+#include <type_traits>
+
 #include "relattn_common.cuh"
 #include "relattn_internal.h"
 
@@ -46,6 +48,9 @@ constexpr int kMiscAbort = 14;       // shared flag word: a consumer warp gave u
 constexpr int kSlicePad = 8;         // floats of padding per merge-slice row (bank spread)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kNegInf = -__builtin_huge_valf();
+
+__device__ __forceinline__ float rel_f32(float x) { return x; }
+__device__ __forceinline__ float rel_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
 
 __device__ __forceinline__ float lg2(float x) {
   float y;
@@ -64,7 +69,9 @@ __device__ __forceinline__ int atom_add_acq_rel(int* p, int v) {
 
 // Bytes of one token's rel box in a stage (g rows x kRelBoxW floats), padded
 // so that every box starts 128-byte aligned.
-__host__ __device__ constexpr int rel_token_bytes(int g) { return (g * kRelBoxW * 4 + 127) & ~127; }
+__host__ __device__ constexpr int rel_token_bytes(int g, int es) {
+  return (g * rel_box_w(es) * es + 127) & ~127;
+}
 
 // Shared-memory carve-up (byte offsets from a 1024-aligned base); identical
 // on host and device.  K/V stages are 1024-aligned for the 128-byte swizzle;
@@ -73,9 +80,9 @@ __host__ __device__ constexpr int rel_token_bytes(int g) { return (g * kRelBoxW 
 struct DecodeSmem {
   int qbuf, stages, stage_bytes, rel, rel_bytes, slices, bars, valid, seqlen, nt, pref, m, l,
       M, L, misc, total;
-  __host__ __device__ DecodeSmem(int nstages, int B, int Bv, int kpc, int g, int dv) {
+  __host__ __device__ DecodeSmem(int nstages, int B, int Bv, int kpc, int g, int dv, int rel_es) {
     stage_bytes = 16384 + kTileKeys * dv * 2;
-    rel_bytes = kpc * rel_token_bytes(g);
+    rel_bytes = kpc * rel_token_bytes(g, rel_es);
     qbuf = 0;
     stages = qbuf + 2 * kQBufBytes;
     rel = stages + nstages * stage_bytes;
@@ -261,9 +268,10 @@ __device__ __forceinline__ int decode_early_loads(const DecodeParams& p) {
       if (lane < 2 * rows) prefetch_l2(p.q + qrow(lane / 2) * 128 + (lane & 1) * 64);
     } else if (tid >= 96 && tid < 128) {  // rel rows: distances [0, min(E, W or E))
       const int dist = p.window > 0 ? min(p.rel_extent, p.window) : p.rel_extent;
-      const int lines = (dist + 31) / 32;  // 32 floats per line
+      const int lines = (dist * p.rel_es + 127) / 128;  // 128-byte lines
+      const char* rel = static_cast<const char*>(p.rel);
       for (int i = lane; i < rows * lines && i < 4 * 32; i += 32)
-        prefetch_l2(p.rel + qrow(i / lines) * p.rel_extent + (i % lines) * 32);
+        prefetch_l2(rel + (qrow(i / lines) * p.rel_extent) * p.rel_es + (i % lines) * 128);
     }
   }
   return len;
@@ -412,11 +420,11 @@ __device__ __forceinline__ void decode_zero_bad(const DecodeParams& p, const int
                                                 int nthreads) {
   if (blockIdx.x != 0 || p.out == nullptr) return;
   const Tok<MULTI> tk(p);
-  const int per = tk.k * p.Hq * p.dv;
+  const int per = tk.k * p.Hq * p.dv * (p.out_f32 ? 4 : 2) / 4;  // 32-bit words
   for (int b = 0; b < p.B; ++b) {
     if (s_nt[b * tk.nck] != 0) continue;
-    __nv_bfloat16* o = p.out + static_cast<size_t>(b) * per;
-    for (int i = t; i < per; i += nthreads) o[i] = __float2bfloat16(0.f);
+    uint32_t* o = static_cast<uint32_t*>(p.out) + static_cast<size_t>(b) * per;
+    for (int i = t; i < per; i += nthreads) o[i] = 0u;
   }
 }
 
@@ -469,7 +477,8 @@ __device__ Plan decode_prologue(const DecodeParams& p, uint8_t* smem, const Deco
   return make_plan(p.Hkv * s_pref[p.Bv], s_misc[0], p.Bv * p.Hkv);
 }
 
-template <int DV, bool MULTI>
+// R16: rel is bf16 (else fp32).
+template <int DV, bool MULTI, bool R16>
 __global__ void __launch_bounds__(kDecodeThreads, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tm_q,
                   const __grid_constant__ CUtensorMap tm_k,
@@ -481,7 +490,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   const int g = p.g;
   const int ns = p.nstages;
   const Tok<MULTI> tok(p);
-  const DecodeSmem L(ns, p.B, p.Bv, tok.kpc, g, DV);
+  using RelT = typename std::conditional<R16, __nv_bfloat16, float>::type;
+  constexpr int RES = R16 ? 2 : 4;                // bytes per rel element
+  constexpr int RW = R16 ? kRelBoxW16 : kRelBoxW;  // distances per rel box row
+  constexpr int RAL = R16 ? ~7 : ~3;               // box start: 16-byte aligned distance
+  const DecodeSmem L(ns, p.B, p.Bv, tok.kpc, g, DV, RES);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
   uint64_t* empty = full + ns;
   uint64_t* qfull = empty + ns;
@@ -541,8 +554,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     return true;
   };
   const int stage_tx = 16384 + kTileKeys * DV * 2;
-  const int rel_tx = g * kRelBoxW * 4;         // one token's rel box
-  const int rel_stride = rel_token_bytes(g);  // its place in a stage's rel slice
+  const int rel_tx = g * RW * RES;                 // one token's rel box
+  const int rel_stride = rel_token_bytes(g, RES);  // its place in a stage's rel slice
   // K, V and rel of tile `tile` of chunk sq, KV head kvh, into the stage of
   // CTA tile nn (one lane per tile); 1 on a wait timeout.
   auto issue_tile = [&](int nn, int tile, int id, const VSeq& sq, int kvh) -> int {
@@ -567,7 +580,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       tma_load_4d(st + 16384, &tm_v, &full[stage], 0, row, 0, kvh);
       for (int i = 0; i < nrel; ++i)
         tma_load_2d(smem + L.rel + stage * L.rel_bytes + i * rel_stride, &tm_rel, &full[stage],
-                    (dmin0 + i) & ~3, (sq.b * tok.k + sq.i0 + i) * p.Hq + kvh * g);
+                    (dmin0 + i) & RAL, (sq.b * tok.k + sq.i0 + i) * p.Hq + kvh * g);
     } else {
       report(p.status, RELATTN_DEV_BAD_BLOCK_ID);
       mbar_arrive(&full[stage]);
@@ -705,7 +718,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       rv[rr] = row < nrows;
       rP[rr] = sq.pf + ti;
       rlo[rr] = window_lo(rP[rr], p.window);
-      rrel[rr] = ti * (rel_stride / 4) + (row - ti * g) * kRelBoxW;
+      rrel[rr] = ti * (rel_stride / RES) + (row - ti * g) * RW;
     }
     const int lo_last = window_lo(sq.pl, p.window);
     const int qb = k & 1;
@@ -760,7 +773,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         // logits in log2 units: (q.k/sqrt(d) + rel) * log2(e).  A row's rel
         // box starts at its smallest distance in the tile, P - key0 - 63,
         // rounded down to 16 bytes.
-        const float* relt = reinterpret_cast<const float*>(smem + L.rel + stage * L.rel_bytes);
+        const RelT* relt = reinterpret_cast<const RelT*>(smem + L.rel + stage * L.rel_bytes);
         const bool edge = key0 < lo_last || key0 + kTileKeys - 1 > sq.pf;  // any mask?
         // this thread's keys are kb + e, e in {0, 1, 8, 9}; a row keeps the
         // keys with e in [mlo, mhi] (all of them when no key of the tile is
@@ -771,7 +784,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
           // one position for all rows: one box, present or not for the tile
           const int dmin = sq.pf - key0 - (kTileKeys - 1);
           const bool need_rel = dmin < p.rel_extent;
-          const int d0 = dmin & ~3;
+          const int d0 = dmin & RAL;
           const int mlo = edge ? sq.lo - kb : INT_MIN, mhi = edge ? sq.pf - kb : INT_MAX;
 #pragma unroll
           for (int nt = 0; nt < 2; ++nt)
@@ -781,7 +794,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
               const int e = nt * 8 + (i & 1);
               const int key = kb + e;
               float bias = 0.f;
-              if (need_rel && row < g) bias = relt[row * kRelBoxW + (sq.pf - key - d0)];
+              if (need_rel && row < g) bias = rel_f32(relt[row * RW + (sq.pf - key - d0)]);
               const float v = fmaf(s[nt][i], p.scale_log2, bias * kLog2e);
               x[nt][i] = (e < mlo || e > mhi) ? kNegInf : v;
             }
@@ -790,13 +803,13 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
           // distance in the tile is below rel_extent (the box reads 0 past
           // it), and the box entry of key key0 -- the others at -offset
           bool nr[2];
-          const float* rb[2];
+          const RelT* rb[2];
           int mlo[2], mhi[2];
 #pragma unroll
           for (int rr = 0; rr < 2; ++rr) {
             const int dmin = rP[rr] - key0 - (kTileKeys - 1);
             nr[rr] = rv[rr] && dmin < p.rel_extent;
-            rb[rr] = relt + rrel[rr] + (rP[rr] - key0 - (dmin & ~3));
+            rb[rr] = relt + rrel[rr] + (rP[rr] - key0 - (dmin & RAL));
             mlo[rr] = edge ? rlo[rr] - kb : INT_MIN;
             mhi[rr] = edge ? rP[rr] - kb : INT_MAX;
           }
@@ -807,7 +820,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
               const int rr = i >> 1;
               const int e = nt * 8 + (i & 1);
               const int ko = 16 * cw + cq * 2 + e;
-              const float bias = nr[rr] ? rb[rr][-ko] : 0.f;
+              const float bias = nr[rr] ? rel_f32(rb[rr][-ko]) : 0.f;
               const float v = fmaf(s[nt][i], p.scale_log2, bias * kLog2e);
               x[nt][i] = (e < mlo[rr] || e > mhi[rr]) ? kNegInf : v;
             }
@@ -911,10 +924,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     const bool whole = pc.i0 == 0 && pc.n == s_nt[pc.b];
     const int slot = 2 * c + (a0 < pc.seg_start ? 1 : 0);
     // out row of tile row r: token i0 + r / g of sequence b, head h0 + r % g
-    auto orow = [&](int row) {
+    // (out is bf16, or fp32 when p.out_f32: element index, either type)
+    auto orow = [&](int row) -> size_t {
       const int ti = tok.token_of_row(row, g);
-      return p.out +
-             ((static_cast<size_t>(sq.b) * tok.k + sq.i0 + ti) * p.Hq + h0 + (row - ti * g)) * DV;
+      return ((static_cast<size_t>(sq.b) * tok.k + sq.i0 + ti) * p.Hq + h0 + (row - ti * g)) * DV;
     };
     for (int idx = ctid; idx < nrows * DV / 2; idx += kConsumerThreads) {
       const int row = idx / (DV / 2), col = 2 * (idx % (DV / 2));
@@ -929,8 +942,12 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       const float Ls = s_L[row];
       const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
       if (whole) {
-        *reinterpret_cast<__nv_bfloat162*>(orow(row) + col) =
-            __floats2bfloat162_rn(v0 * inv, v1 * inv);
+        if (p.out_f32)
+          *reinterpret_cast<float2*>(static_cast<float*>(p.out) + orow(row) + col) =
+              make_float2(v0 * inv, v1 * inv);
+        else
+          *reinterpret_cast<__nv_bfloat162*>(static_cast<__nv_bfloat16*>(p.out) + orow(row) +
+                                             col) = __floats2bfloat162_rn(v0 * inv, v1 * inv);
       } else {
         *reinterpret_cast<float2*>(
             p.part_o + (static_cast<size_t>(slot) * kMaxDecodeRows + row) * DV + col) =
@@ -968,7 +985,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
             den = den * sc + w;
             M = M2;
           }
-          orow(row)[col] = __float2bfloat16(den > 0.f ? num / den : 0.f);
+          const float r = den > 0.f ? num / den : 0.f;
+          if (p.out_f32)
+            static_cast<float*>(p.out)[orow(row) + col] = r;
+          else
+            static_cast<__nv_bfloat16*>(p.out)[orow(row) + col] = __float2bfloat16(r);
         }
         if (ctid == 0) p.counters[pc.b * p.Hkv + pc.kvh] = 0;
       }
@@ -982,7 +1003,7 @@ __global__ void __launch_bounds__(128) decode_walk_kernel(const DecodeParams p) 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const DecodeSmem L(0, p.B, p.Bv, 1, 1, 64);
+  const DecodeSmem L(0, p.B, p.Bv, 1, 1, 64, 4);
   const int* s_len = reinterpret_cast<const int*>(smem + L.seqlen);
   const int* s_nt = reinterpret_cast<const int*>(smem + L.nt);
   const int* s_pref = reinterpret_cast<const int*>(smem + L.pref);
@@ -1024,13 +1045,13 @@ __global__ void __launch_bounds__(128) decode_walk_kernel(const DecodeParams p) 
 
 }  // namespace
 
-int decode_smem_bytes(int nstages, int B, int Bv, int kpc, int g, int dv) {
-  return DecodeSmem(nstages, B, Bv, kpc, g, dv).total + 1024;
+int decode_smem_bytes(int nstages, int B, int Bv, int kpc, int g, int dv, int rel_es) {
+  return DecodeSmem(nstages, B, Bv, kpc, g, dv, rel_es).total + 1024;
 }
 
-template <int DV, bool MULTI>
+template <int DV, bool MULTI, bool R16>
 static cudaError_t launch_decode_as(const DecodeLaunch& L, int smem, cudaStream_t stream) {
-  cudaError_t e = cudaFuncSetAttribute(decode_kernel<DV, MULTI>,
+  cudaError_t e = cudaFuncSetAttribute(decode_kernel<DV, MULTI, R16>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   // Programmatic stream serialisation: the kernel may begin while the
@@ -1045,23 +1066,29 @@ static cudaError_t launch_decode_as(const DecodeLaunch& L, int smem, cudaStream_
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_kernel<DV, MULTI>, L.tm_q, L.tm_k, L.tm_v, L.tm_rel,
-                            L.p);
+  return cudaLaunchKernelEx(&cfg, decode_kernel<DV, MULTI, R16>, L.tm_q, L.tm_k, L.tm_v,
+                            L.tm_rel, L.p);
+}
+
+template <int DV, bool MULTI>
+static cudaError_t launch_decode_rel(const DecodeLaunch& L, int smem, cudaStream_t stream) {
+  return L.p.rel_es == 2 ? launch_decode_as<DV, MULTI, true>(L, smem, stream)
+                         : launch_decode_as<DV, MULTI, false>(L, smem, stream);
 }
 
 cudaError_t launch_decode(const DecodeLaunch& L, cudaStream_t stream) {
   const DecodeParams& p = L.p;
-  const int smem = decode_smem_bytes(p.nstages, p.B, p.Bv, p.kpc, p.g, p.dv);
+  const int smem = decode_smem_bytes(p.nstages, p.B, p.Bv, p.kpc, p.g, p.dv, p.rel_es);
   const bool multi = p.k > 1;
   if (p.dv == 128)
-    return multi ? launch_decode_as<128, true>(L, smem, stream)
-                 : launch_decode_as<128, false>(L, smem, stream);
-  return multi ? launch_decode_as<64, true>(L, smem, stream)
-               : launch_decode_as<64, false>(L, smem, stream);
+    return multi ? launch_decode_rel<128, true>(L, smem, stream)
+                 : launch_decode_rel<128, false>(L, smem, stream);
+  return multi ? launch_decode_rel<64, true>(L, smem, stream)
+               : launch_decode_rel<64, false>(L, smem, stream);
 }
 
 cudaError_t launch_decode_walk(const DecodeParams& p, int grid, cudaStream_t stream) {
-  const int smem = decode_smem_bytes(0, p.B, p.Bv, 1, 1, 64);
+  const int smem = decode_smem_bytes(0, p.B, p.Bv, 1, 1, 64, 4);
   cudaError_t e = cudaFuncSetAttribute(decode_walk_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;

@@ -11,14 +11,20 @@ namespace relattn {
 constexpr int kBlockSize = 128;  // tokens per KV block
 constexpr int kTileKeys = 64;    // keys per pipeline stage
 constexpr int kDqk = 128;
-constexpr int kRelBoxW = 68;     // distances per rel box: 64 keys + alignment
+constexpr int kRelBoxW = 68;     // distances per fp32 rel box: 64 keys + 16-byte alignment
+constexpr int kRelBoxW16 = 72;   // distances per bf16 rel box: 64 keys + 16-byte alignment
+
+// Distances per decode rel box and its bytes per row, by rel element size.
+__host__ __device__ constexpr int rel_box_w(int es) { return es == 2 ? kRelBoxW16 : kRelBoxW; }
 
 struct DecodeParams {
-  const __nv_bfloat16* q;      // [B][Hq][128]
-  const float* rel;            // [B][Hq][E]
+  const __nv_bfloat16* q;      // [B][k][Hq][128]
+  const void* rel;             // [B][k][Hq][E], fp32 or bf16 (rel_es bytes)
   const int32_t* block_table;  // [B][max_blocks]
   const int32_t* seq_lens;     // [B]
-  __nv_bfloat16* out;          // [B][Hq][dv]
+  void* out;                   // [B][k][Hq][dv], bf16 or fp32 (out_f32)
+  int rel_es;                  // bytes per rel element: 4 (fp32) or 2 (bf16)
+  int out_f32;                 // 1: out is fp32
   uint32_t* status;            // workspace status word
   int32_t* counters;           // [B][Hkv] split-combine arrival counters
   float* part_lse;             // [2*grid][g] base-2 log-sum-exp of a piece
@@ -67,7 +73,7 @@ struct PrefillLaunch {
   int grid;
 };
 
-int decode_smem_bytes(int nstages, int B, int Bv, int kpc, int g, int dv);
+int decode_smem_bytes(int nstages, int B, int Bv, int kpc, int g, int dv, int rel_es);
 constexpr int kMaxDecodeRows = 16;         // rows of one decode tile: g heads x tokens
 constexpr int kMaxQueryTokens = 16;        // query tokens per sequence in one decode call
 cudaError_t launch_decode(const DecodeLaunch& L, cudaStream_t stream);

@@ -38,7 +38,12 @@ EXPORTS = (
     "relattn_abi_version",
     "relattn_decode_noalloc",
     "relattn_decode_multi",
+    "relattn_decode_ex",
 )
+
+DTYPE_F32 = 0
+DTYPE_BF16 = 1
+_DTYPE_CODE = {torch.float32: DTYPE_F32, torch.bfloat16: DTYPE_BF16}
 
 
 class KVCacheDesc(ctypes.Structure):
@@ -51,6 +56,10 @@ class Dims(ctypes.Structure):
     _fields_ = [("batch", c_int32), ("num_q_heads", c_int32),
                 ("max_blocks_per_seq", c_int32), ("num_tokens", c_int32),
                 ("max_q_len", c_int32), ("num_ctas", c_int32)]
+
+
+class IoTypes(ctypes.Structure):
+    _fields_ = [("rel", c_int32), ("out", c_int32)]
 
 
 class RelattnError(RuntimeError):
@@ -107,6 +116,10 @@ def lib() -> ctypes.CDLL:
                                        c_int32, c_int32, S, c_void_p, c_void_p, c_size_t,
                                        c_void_p]
     L.relattn_decode_multi.restype = c_int
+    L.relattn_decode_ex.argtypes = [c_void_p, c_void_p, POINTER(IoTypes), P, c_void_p,
+                                    c_void_p, c_int32, c_int32, c_int32, S, c_void_p, c_void_p,
+                                    c_size_t, c_void_p]
+    L.relattn_decode_ex.restype = c_int
     L.relattn_abi_version.argtypes = []
     L.relattn_abi_version.restype = c_int
     _LIB = L
@@ -180,9 +193,31 @@ def decode_dims(q, block_table, num_ctas=0) -> Dims:
     return Dims(q.shape[0], q.shape[1], block_table.shape[1], 0, 0, num_ctas)
 
 
+def _io_types(rel, out_dtype) -> IoTypes:
+    if rel.dtype not in _DTYPE_CODE:
+        raise TypeError(f"rel must be float32 or bfloat16, got {rel.dtype}")
+    if out_dtype not in _DTYPE_CODE:
+        raise TypeError(f"out must be bfloat16 or float32, got {out_dtype}")
+    return IoTypes(_DTYPE_CODE[rel.dtype], _DTYPE_CODE[out_dtype])
+
+
 def relattn_decode(q, rel, k_cache, v_cache, block_table, seq_lens, window: int,
-                   rel_extent: int, out=None, workspace=None, num_ctas: int = 0):
-    """Paged relative-bias decode; see ``relattn_decode`` in include/relattn.h."""
+                   rel_extent: int, out=None, workspace=None, num_ctas: int = 0,
+                   out_dtype=torch.bfloat16):
+    """Paged relative-bias decode; see ``relattn_decode`` in include/relattn.h.
+
+    rel may be float32 or bfloat16 and out bfloat16 or float32 (``out``'s own
+    dtype when it is given); other than fp32 rel and bf16 out goes through
+    ``relattn_decode_ex``.
+    """
+    if rel.dtype != torch.float32 or (out.dtype if out is not None else out_dtype) != torch.bfloat16:
+        if q.dim() != 3 or rel.dim() != 3:
+            raise ValueError("q must be [B, Hq, d_qk] and rel [B, Hq, rel_extent]")
+        o = relattn_decode_multi(q[:, None], rel[:, None], k_cache, v_cache, block_table,
+                                 seq_lens, window, rel_extent,
+                                 out=None if out is None else out[:, None],
+                                 workspace=workspace, num_ctas=num_ctas, out_dtype=out_dtype)
+        return o[:, 0]
     dev = q.device
     B, Hq, dqk = q.shape
     _need(q, "q", torch.bfloat16, 3, dev)
@@ -238,16 +273,20 @@ def relattn_decode_noalloc(q, rel, k_cache, v_cache, block_table, seq_lens, wind
 
 
 def relattn_decode_multi(q, rel, k_cache, v_cache, block_table, seq_lens, window: int,
-                         rel_extent: int, out=None, workspace=None, num_ctas: int = 0):
+                         rel_extent: int, out=None, workspace=None, num_ctas: int = 0,
+                         out_dtype=torch.bfloat16):
     """Decode of k query tokens per sequence (speculative verification).
 
     q is [B, k, Hq, d_qk], rel [B, k, Hq, rel_extent], out [B, k, Hq, d_v];
-    token i of sequence b sits at position seq_lens[b] - k + i.
+    token i of sequence b sits at position seq_lens[b] - k + i.  rel may be
+    float32 or bfloat16, out bfloat16 or float32 (``relattn_decode_ex``).
     """
     dev = q.device
     _need(q, "q", torch.bfloat16, 4, dev)
     B, kq, Hq, _ = q.shape
-    _need(rel, "rel", torch.float32, 4, dev)
+    out_dtype = out.dtype if out is not None else out_dtype
+    io = _io_types(rel, out_dtype)
+    _need(rel, "rel", rel.dtype, 4, dev)
     _need(k_cache, "k_cache", torch.bfloat16, 4, dev)
     _need(v_cache, "v_cache", torch.bfloat16, 4, dev)
     _need(block_table, "block_table", torch.int32, 2, dev)
@@ -259,16 +298,23 @@ def relattn_decode_multi(q, rel, k_cache, v_cache, block_table, seq_lens, window
     cache = cache_desc(k_cache, v_cache)
     dims = Dims(B, Hq, block_table.shape[1], 0, 0, num_ctas)
     if out is None:
-        out = torch.empty((B, kq, Hq, v_cache.shape[3]), dtype=torch.bfloat16, device=dev)
+        out = torch.empty((B, kq, Hq, v_cache.shape[3]), dtype=out_dtype, device=dev)
     else:
-        _need(out, "out", torch.bfloat16, 4, dev)
+        _need(out, "out", out_dtype, 4, dev)
     if workspace is None:
         workspace = new_workspace(workspace_size(dims, cache), dev)
-    _check(lib().relattn_decode_multi(
-        q.data_ptr(), rel.data_ptr(), ctypes.byref(cache), block_table.data_ptr(),
-        seq_lens.data_ptr(), int(kq), int(window), int(rel_extent), ctypes.byref(dims),
-        out.data_ptr(), workspace.data_ptr(), workspace.numel(), _stream(dev)),
-        "relattn_decode_multi")
+    if rel.dtype == torch.float32 and out_dtype == torch.bfloat16:
+        _check(lib().relattn_decode_multi(
+            q.data_ptr(), rel.data_ptr(), ctypes.byref(cache), block_table.data_ptr(),
+            seq_lens.data_ptr(), int(kq), int(window), int(rel_extent), ctypes.byref(dims),
+            out.data_ptr(), workspace.data_ptr(), workspace.numel(), _stream(dev)),
+            "relattn_decode_multi")
+    else:
+        _check(lib().relattn_decode_ex(
+            q.data_ptr(), rel.data_ptr(), ctypes.byref(io), ctypes.byref(cache),
+            block_table.data_ptr(), seq_lens.data_ptr(), int(kq), int(window),
+            int(rel_extent), ctypes.byref(dims), out.data_ptr(), workspace.data_ptr(),
+            workspace.numel(), _stream(dev)), "relattn_decode_ex")
     return out
 
 

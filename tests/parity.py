@@ -33,8 +33,10 @@ def to_f64(t: torch.Tensor) -> np.ndarray:
 
 def host_decode_inputs(case):
     """numpy copies of a decode case for the oracle (bf16 kept as bits)."""
+    rel = case["rel"]
     return dict(
-        q=bf16_bits(case["q"]), rel=case["rel"].cpu().numpy(),
+        q=bf16_bits(case["q"]),
+        rel=bf16_bits(rel) if rel.dtype == torch.bfloat16 else rel.cpu().numpy(),
         k_cache=bf16_bits(case["k_cache"]), v_cache=bf16_bits(case["v_cache"]),
         block_table=case["block_table"].cpu().numpy(),
         seq_lens=case["seq_lens"].cpu().numpy())
