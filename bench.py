@@ -65,6 +65,7 @@ def decode_work(wl, seq_lens):
     uses and out count per token and head."""
     g = wl.num_q_heads // wl.num_kv_heads
     k = max(1, wl.query_tokens)
+    res = 2 if wl.rel_dtype == "bf16" else 4
     total = 0
     per_group = []
     for L in seq_lens:
@@ -75,7 +76,7 @@ def decode_work(wl, seq_lens):
         head = 0
         for Pi in range(L - k, L):
             n = min(wl.window, Pi + 1) if wl.window > 0 else Pi + 1
-            head += wl.d_qk * 2 + min(wl.rel_extent, n) * 4 + wl.d_v * 2
+            head += wl.d_qk * 2 + min(wl.rel_extent, n) * res + wl.d_v * 2
         grp = kv + g * head
         per_group.append(grp)
         total += wl.num_kv_heads * grp + blocks * 4 + 4
@@ -99,7 +100,8 @@ def prefill_work(wl):
     Hq, Hkv = wl.num_q_heads, wl.num_kv_heads
     kvrow = Hkv * (wl.d_qk + wl.d_v) * 2
     flops *= Hq * 2 * (wl.d_qk + wl.d_v)
-    nbytes = (rel * Hq * 4 + T * Hq * (wl.d_qk + wl.d_v) * 2 + 2 * T * kvrow
+    res = 2 if wl.rel_dtype == "bf16" else 4
+    nbytes = (rel * Hq * res + T * Hq * (wl.d_qk + wl.d_v) * 2 + 2 * T * kvrow
               + kv_prefix * kvrow)
     return flops, nbytes
 
@@ -113,11 +115,11 @@ def describe(wl):
                 else "decode")
         return (f"{wl.name}: {kind} B={wl.batch}, {wl.num_q_heads}/{wl.num_kv_heads} heads, "
                 f"d_qk={wl.d_qk} d_v={wl.d_v}, {win}, rel_extent={wl.rel_extent}, {lens}, "
-                f"bf16 paged KV in 128-token blocks, random block tables")
+                f"{wl.rel_dtype} rel, bf16 paged KV in 128-token blocks, random block tables")
     win = f"W={wl.window}" if wl.window > 0 else "global"
     return (f"{wl.name}: chunked prefill {len(wl.new_tokens)}x{wl.new_tokens[0]} new tokens "
             f"after {wl.ctx_lens[0]} cached, {wl.num_q_heads}/{wl.num_kv_heads} heads, "
-            f"d={wl.d_qk}, {win}, rel_extent={wl.rel_extent}")
+            f"d={wl.d_qk}, {win}, rel_extent={wl.rel_extent}, {wl.rel_dtype} rel")
 
 
 # ---------------------------------------------------------------------------
@@ -439,7 +441,8 @@ def oracle_decode_sample(case, wl, budget_s):
     _, per_group = decode_work(wl, lens)
     g = wl.num_q_heads // wl.num_kv_heads
     q = bf16_bits(case["q"])
-    rel = case["rel"].cpu().numpy()
+    rel = (bf16_bits(case["rel"]) if case["rel"].dtype == torch.bfloat16
+           else case["rel"].cpu().numpy())
     table = case["block_table"].cpu().numpy()
     # each sequence's blocks, gathered once (host copies; not timed)
     per_seq = []
@@ -473,6 +476,8 @@ def cores_used():
 
 def prefill_workload(args):
     wl = I.WORKLOADS["chunked_prefill"]
+    if args.rel == "bf16":
+        wl = I.variant(wl, rel_dtype="bf16")
     nseq = args.prefill_seqs or len(wl.new_tokens)
     new = args.prefill_new_tokens or wl.new_tokens[0]
     if (nseq, new) != (len(wl.new_tokens), wl.new_tokens[0]):
@@ -521,6 +526,8 @@ def ours(args):
     if args.workload == "chunked_prefill":
         return ours_prefill(args, R, dist, device, peaks, sampler)
     wl = I.WORKLOADS[args.workload]
+    if args.rel == "bf16":
+        wl = I.variant(wl, rel_dtype="bf16")
     sets, step_bytes, times, wss = run_decode(R, wl, device, args.steps, args.warmup, dist,
                                               sampler, l2, args.pool == "shared")
     case = sets[0]
@@ -541,9 +548,10 @@ def ours(args):
 
     secondary = []
     if not args.no_secondary:
-        for name in ("global_decode_b1", "global_decode_b8", "diffhead_decode",
-                     "verify_decode"):
-            w2 = I.WORKLOADS[name]
+        for name, rdt in (("global_decode_b1", "f32"), ("global_decode_b8", "f32"),
+                          ("diffhead_decode", "f32"), ("verify_decode", "f32"),
+                          ("local_decode", "bf16")):
+            w2 = I.variant(I.WORKLOADS[name], rel_dtype=rdt)
             c2, b2, t2, _ = run_decode(R, w2, device, args.secondary_steps, 3, dist, sampler, l2)
             m2 = sum(t2) / len(t2)
             a2 = sum(b2) / len(b2)
@@ -556,20 +564,23 @@ def ours(args):
                 "frac_of_nominal_8000": round(gbs / 8000.0, 4)})
             del c2
             torch.cuda.empty_cache()
-        wp = prefill_workload(args)
-        flops, pbytes = prefill_work(wp)
-        tp = run_prefill(R, wp, device, max(3, args.secondary_steps // 4), 2, dist, sampler)
-        mp = sum(tp) / len(tp)
-        tflops = flops / (mp / 1e3) / 1e12
-        gbs = pbytes / (mp / 1e3) / 1e9
-        secondary.append({
-            "workload": describe(wp), "metric": "prefill TFLOP/s", "value": round(tflops, 2),
-            "unit": "TFLOP/s", "ms_per_step": round(mp, 4), "alg_flops": flops,
-            "alg_bytes": pbytes,
-            "roofline": roofline("hbm", gbs, peaks["hbm"], "GB/s", None),
-            "tensor_frac_of_bf16_peak": round(tflops / peaks["bf16"], 4),
-            "note": "step = cache write + attention kernels; rel (fp32) is most of the bytes"})
-        torch.cuda.empty_cache()
+        wp0 = prefill_workload(args)
+        for rdt in ("f32", "bf16"):
+            wp = I.variant(wp0, rel_dtype=rdt)
+            flops, pbytes = prefill_work(wp)
+            tp = run_prefill(R, wp, device, max(3, args.secondary_steps // 4), 2, dist, sampler)
+            mp = sum(tp) / len(tp)
+            tflops = flops / (mp / 1e3) / 1e12
+            gbs = pbytes / (mp / 1e3) / 1e9
+            secondary.append({
+                "workload": describe(wp), "metric": "prefill TFLOP/s", "value": round(tflops, 2),
+                "unit": "TFLOP/s", "ms_per_step": round(mp, 4), "alg_flops": flops,
+                "alg_bytes": pbytes,
+                "roofline": roofline("hbm", gbs, peaks["hbm"], "GB/s", None),
+                "tensor_frac_of_bf16_peak": round(tflops / peaks["bf16"], 4),
+                "note": f"step = cache write + attention kernels; rel ({rdt}) is most of the "
+                        f"bytes"})
+            torch.cuda.empty_cache()
     clocks = sampler.stop()
 
     cpu = None
@@ -616,13 +627,16 @@ def reference(args):
     from oracle import relattn_oracle as O
     from paged_relative_bias_gb300.inputs import bf16_bits
     wl = I.WORKLOADS[args.workload]
+    if args.rel == "bf16":
+        wl = I.variant(wl, rel_dtype="bf16")
     device = "cuda" if torch.cuda.is_available() else "cpu"
     case = I.make_decode(wl, device)
     lens = case["seq_lens"].cpu().tolist()
     _, per_group = decode_work(wl, lens)
     g = wl.num_q_heads // wl.num_kv_heads
     q = bf16_bits(case["q"])
-    rel = case["rel"].cpu().numpy()
+    rel = (bf16_bits(case["rel"]) if case["rel"].dtype == torch.bfloat16
+           else case["rel"].cpu().numpy())
     table = case["block_table"].cpu().numpy()
     groups = [(b, kvh) for b in range(wl.batch) for kvh in range(wl.num_kv_heads)]
     prepared = []
@@ -676,6 +690,8 @@ def main():
                     help="new tokens per sequence of the chunked prefill (default 8192)")
     ap.add_argument("--prefill-seqs", type=int, default=0,
                     help="sequences of the chunked prefill (default 4)")
+    ap.add_argument("--rel", choices=["f32", "bf16"], default="f32",
+                    help="element type of the rel input of the timed workload")
     ap.add_argument("--pool", choices=["per-set", "shared"], default="per-set",
                     help="decode input sets: one KV pool each (default), or one shared pool "
                          "with renumbered block tables (small device footprint, for ncu)")

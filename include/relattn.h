@@ -278,6 +278,20 @@ int relattn_prefill(const void* q, const void* k, const void* v,
                     void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * relattn_prefill with the element types of rel and out given by `types`:
+ * rel [T][Hq][rel_extent] of types->rel, out [T][Hq][d_v] of types->out.  A
+ * bf16 rel needs rel_extent a multiple of 8 (fp32: of 4):
+ * RELATTN_ERR_UNSUPPORTED otherwise; an unknown type code is
+ * RELATTN_ERR_INVALID_ARG.  Everything else as relattn_prefill.
+ */
+int relattn_prefill_ex(const void* q, const void* k, const void* v, const void* rel,
+                       const relattn_io_types* types, const int32_t* cu_seqlens,
+                       const relattn_kv_cache* kv_cache, const int32_t* block_table,
+                       const int32_t* ctx_lens, int32_t window, int32_t rel_extent,
+                       const relattn_dims* dims, void* out, void* workspace,
+                       size_t workspace_bytes, void* stream);
+
+/*
  * Read the device status word of a workspace into *status (synchronises
  * `stream`).  The word accumulates RELATTN_DEV_* bits until cleared with
  * relattn_workspace_init.

@@ -433,8 +433,8 @@ int relattn_decode_noalloc(const void* q, const float* rel, const relattn_kv_cac
   return to_status(e);
 }
 
-static int prepare_prefill(const void* q, const void* k, const void* v, const float* rel,
-                           const int32_t* cu_seqlens, const relattn_kv_cache* cache,
+static int prepare_prefill(const void* q, const void* k, const void* v, const void* rel,
+                           IoTypes io, const int32_t* cu_seqlens, const relattn_kv_cache* cache,
                            const int32_t* block_table, const int32_t* ctx_lens,
                            int32_t window, int32_t rel_extent, const relattn_dims* dims,
                            void* out, void* workspace, size_t ws_bytes, bool walk,
@@ -449,7 +449,7 @@ static int prepare_prefill(const void* q, const void* k, const void* v, const fl
     if (!q || !k || !v || !rel || !out) return RELATTN_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(rel) || !aligned16(out))
       return RELATTN_ERR_INVALID_ARG;
-    if (rel_extent < 4 || rel_extent % 4 != 0) return RELATTN_ERR_UNSUPPORTED;
+    if (!rel_extent_ok(rel_extent, io.rel_es)) return RELATTN_ERR_UNSUPPORTED;
   }
   if (!aligned16(workspace) || ws_bytes < kStatusBytes) return RELATTN_ERR_WORKSPACE;
   std::memset(L, 0, sizeof(*L));
@@ -463,7 +463,9 @@ static int prepare_prefill(const void* q, const void* k, const void* v, const fl
   p.block_table = block_table;
   p.k_cache = static_cast<__nv_bfloat16*>(cache->k);
   p.v_cache = static_cast<__nv_bfloat16*>(cache->v);
-  p.out = static_cast<__nv_bfloat16*>(out);
+  p.out = out;
+  p.rel_es = io.rel_es;
+  p.out_f32 = io.out_f32;
   p.status = static_cast<uint32_t*>(workspace);
   p.B = dims->batch;
   p.T = dims->num_tokens;
@@ -494,17 +496,37 @@ static int prepare_prefill(const void* q, const void* k, const void* v, const fl
   if (!make_map(&L->tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), qd, qs, qb,
                 CU_TENSOR_MAP_SWIZZLE_128B))
     return RELATTN_ERR_CUDA;
-  // rel [T][Hq][E] fp32: boxes of 32 tokens x 100 distances of one head
+  // rel [T][Hq][E] fp32 or bf16: boxes of 32 tokens x 100 (fp32) or 104
+  // (bf16) distances of one head
   const cuuint64_t rd[3] = {static_cast<cuuint64_t>(rel_extent),
                             static_cast<cuuint64_t>(dims->num_q_heads),
                             static_cast<cuuint64_t>(dims->num_tokens)};
-  const cuuint64_t rs[2] = {static_cast<cuuint64_t>(rel_extent) * 4,
-                            static_cast<cuuint64_t>(rel_extent) * 4 * dims->num_q_heads};
-  const cuuint32_t rb[3] = {100, 1, 32};
-  if (!make_map(&L->tm_rel, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(rel), rd, rs,
-                rb, CU_TENSOR_MAP_SWIZZLE_NONE))
+  const cuuint64_t rs[2] = {static_cast<cuuint64_t>(rel_extent) * io.rel_es,
+                            static_cast<cuuint64_t>(rel_extent) * io.rel_es * dims->num_q_heads};
+  const cuuint32_t rb[3] = {io.rel_es == 2 ? 104u : 100u, 1, 32};
+  if (!make_map(&L->tm_rel,
+                io.rel_es == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                3, const_cast<void*>(rel), rd, rs, rb, CU_TENSOR_MAP_SWIZZLE_NONE))
     return RELATTN_ERR_CUDA;
   return RELATTN_OK;
+}
+
+static int relattn_prefill_io(const void* q, const void* k, const void* v, const void* rel,
+                              IoTypes io, const int32_t* cu_seqlens,
+                              const relattn_kv_cache* cache, const int32_t* block_table,
+                              const int32_t* ctx_lens, int32_t window, int32_t rel_extent,
+                              const relattn_dims* dims, void* out, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+  PrefillLaunch L;
+  const int rc = prepare_prefill(q, k, v, rel, io, cu_seqlens, cache, block_table, ctx_lens,
+                                 window, rel_extent, dims, out, workspace, workspace_bytes, false,
+                                 &L);
+  if (rc != RELATTN_OK) return rc;
+  if (dims->max_q_len == 0 || dims->num_tokens == 0) return RELATTN_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_cache_write(L.p, s);
+  if (e == cudaSuccess) e = launch_prefill(L, L.grid, s);
+  return to_status(e);
 }
 
 int relattn_prefill(const void* q, const void* k, const void* v, const float* rel,
@@ -512,15 +534,20 @@ int relattn_prefill(const void* q, const void* k, const void* v, const float* re
                     const int32_t* block_table, const int32_t* ctx_lens, int32_t window,
                     int32_t rel_extent, const relattn_dims* dims, void* out, void* workspace,
                     size_t workspace_bytes, void* stream) {
-  PrefillLaunch L;
-  const int rc = prepare_prefill(q, k, v, rel, cu_seqlens, cache, block_table, ctx_lens, window,
-                                 rel_extent, dims, out, workspace, workspace_bytes, false, &L);
-  if (rc != RELATTN_OK) return rc;
-  if (dims->max_q_len == 0 || dims->num_tokens == 0) return RELATTN_OK;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = launch_cache_write(L.p, s);
-  if (e == cudaSuccess) e = launch_prefill(L, L.grid, s);
-  return to_status(e);
+  return relattn_prefill_io(q, k, v, rel, kDefaultIo, cu_seqlens, cache, block_table, ctx_lens,
+                            window, rel_extent, dims, out, workspace, workspace_bytes, stream);
+}
+
+int relattn_prefill_ex(const void* q, const void* k, const void* v, const void* rel,
+                       const relattn_io_types* types, const int32_t* cu_seqlens,
+                       const relattn_kv_cache* cache, const int32_t* block_table,
+                       const int32_t* ctx_lens, int32_t window, int32_t rel_extent,
+                       const relattn_dims* dims, void* out, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+  IoTypes io;
+  if (!io_types(types, &io)) return RELATTN_ERR_INVALID_ARG;
+  return relattn_prefill_io(q, k, v, rel, io, cu_seqlens, cache, block_table, ctx_lens, window,
+                            rel_extent, dims, out, workspace, workspace_bytes, stream);
 }
 
 int relattn_debug_walk_prefill(const int32_t* cu_seqlens, const int32_t* ctx_lens,
@@ -530,9 +557,9 @@ int relattn_debug_walk_prefill(const int32_t* cu_seqlens, const int32_t* ctx_len
                                void* workspace, size_t workspace_bytes, void* stream) {
   if (!records || !count || max_records < 0) return RELATTN_ERR_INVALID_ARG;
   PrefillLaunch L;
-  const int rc = prepare_prefill(nullptr, nullptr, nullptr, nullptr, cu_seqlens, cache,
-                                 block_table, ctx_lens, window, 4, dims, nullptr, workspace,
-                                 workspace_bytes, true, &L);
+  const int rc = prepare_prefill(nullptr, nullptr, nullptr, nullptr, kDefaultIo, cu_seqlens,
+                                 cache, block_table, ctx_lens, window, 4, dims, nullptr,
+                                 workspace, workspace_bytes, true, &L);
   if (rc != RELATTN_OK) return rc;
   if (dims->max_q_len == 0) return RELATTN_OK;
   L.p.dbg_records = records;

@@ -51,13 +51,15 @@ struct PrefillParams {
   const __nv_bfloat16* q;      // [T][Hq][128]
   const __nv_bfloat16* k;      // [T][Hkv][128]
   const __nv_bfloat16* v;      // [T][Hkv][dv]
-  const float* rel;            // [T][Hq][E]
+  const void* rel;             // [T][Hq][E], fp32 or bf16 (rel_es bytes)
   const int32_t* cu_seqlens;   // [B+1]
   const int32_t* ctx_lens;     // [B]
   const int32_t* block_table;  // [B][max_blocks]
   __nv_bfloat16* k_cache;      // [NB][128][Hkv][128]
   __nv_bfloat16* v_cache;      // [NB][128][Hkv][dv]
-  __nv_bfloat16* out;          // [T][Hq][dv]
+  void* out;                   // [T][Hq][dv], bf16 or fp32 (out_f32)
+  int rel_es;                  // bytes per rel element: 4 (fp32) or 2 (bf16)
+  int out_f32;                 // 1: out is fp32
   uint32_t* status;
   int32_t* dbg_records;
   int32_t* dbg_count;

@@ -49,6 +49,11 @@ constexpr int kQTileBytes = kQRows * kDqk * 2;      // 32 KB
 constexpr int kRelBoxRows = 32, kRelBoxCols = 100;
 constexpr int kRelBoxBytes = kRelBoxRows * kRelBoxCols * 4;  // 12800
 constexpr int kRelBoxes = kQRows / kRelBoxRows;              // 4 per tile
+// bf16 rel boxes: the box start rounds down to 8 distances (16 bytes), so
+// 95 + 7 columns are needed: 104 (208-byte rows).  Rows are read as 8-byte
+// pieces (4 distances), whose alignment is the same across a warp.
+constexpr int kRelBoxCols16 = 104;
+constexpr int kRelBoxBytes16 = kRelBoxRows * kRelBoxCols16 * 2;  // 6656 (52 x 128)
 // One ring of shared-memory slots carries, per work item, the query tile,
 // then the rel boxes of each key tile, then a scratch slot for storing O.
 constexpr int kRingSlotBytes = kRelBoxes * kRelBoxBytes;     // 51200 (50 KB)
@@ -178,9 +183,10 @@ __device__ int prefill_prologue(const PrefillParams& p, uint8_t* smem, const Pre
     // query tiles of this sequence, kept in s_qpref until the scan
     s_qpref[b] = ok ? (c1 - c0 + kQRows - 1) / kQRows : 0;
     if (!ok && zero_bad && blockIdx.x == 0 && rows_ok(c0, c1, p.T)) {
+      const int per = p.Hq * p.dv * (p.out_f32 ? 4 : 2) / 4;  // 32-bit words per row
+      uint32_t* o = static_cast<uint32_t*>(p.out);
       for (int r = c0; r < c1; ++r)  // a skipped sequence's rows are zero
-        for (int i = 0; i < p.Hq * p.dv; ++i)
-          p.out[static_cast<size_t>(r) * p.Hq * p.dv + i] = __float2bfloat16(0.f);
+        for (int i = 0; i < per; ++i) o[static_cast<size_t>(r) * per + i] = 0u;
     }
   }
   __syncthreads();
@@ -226,7 +232,26 @@ __device__ __forceinline__ void rel_fma(float (&x)[64], const uint32_t (&sr)[64]
   }
 }
 
-template <int DV>
+// The same from bf16 rel: 17 aligned 8-byte loads of four distances, each
+// widened exactly (a bf16 is the top half of a binary32).
+template <int A>
+__device__ __forceinline__ void rel_fma16(float (&x)[64], const uint32_t (&sr)[64],
+                                          const uint2* p2, float scale) {
+#pragma unroll
+  for (int w = 0; w < 17; ++w) {
+    const uint2 v = p2[w];
+    const float f[4] = {__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xffff0000u),
+                        __uint_as_float(v.y << 16), __uint_as_float(v.y & 0xffff0000u)};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int t = 4 * w + e - A;  // distance above the lowest
+      if (t >= 0 && t < 64) x[63 - t] = fmaf(__uint_as_float(sr[63 - t]), scale, f[e]);
+    }
+  }
+}
+
+// R16: rel is bf16 (else fp32).  O32: out is fp32 (else bf16).
+template <int DV, bool R16, bool O32>
 __global__ void __launch_bounds__(kPfThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
                    const __grid_constant__ CUtensorMap tm_k,
@@ -345,10 +370,11 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         if (!rd) { fail = true; break; }
         uint64_t* rbar = &bars[kRFull + e % nrs];
         if (it.P0 - j0 - (kTileKeys - 1) < p.rel_extent) {
-          mbar_arrive_expect_tx(rbar, kRingSlotBytes);
+          constexpr int kBox = R16 ? kRelBoxBytes16 : kRelBoxBytes;
+          mbar_arrive_expect_tx(rbar, kRelBoxes * kBox);
           for (int bx = 0; bx < kRelBoxes; ++bx) {
-            const int x = (it.P0 + kRelBoxRows * bx - j0 - (kTileKeys - 1)) & ~3;
-            tma_load_3d(rd + bx * kRelBoxBytes, &tm_rel, rbar, x, it.h, it.r0 + kRelBoxRows * bx);
+            const int x = (it.P0 + kRelBoxRows * bx - j0 - (kTileKeys - 1)) & (R16 ? ~7 : ~3);
+            tma_load_3d(rd + bx * kBox, &tm_rel, rbar, x, it.h, it.r0 + kRelBoxRows * bx);
           }
         } else {
           mbar_arrive(rbar);  // every distance is past rel_extent
@@ -487,17 +513,33 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         if (!slot) { ok = false; break; }
         float x[64];
         if (it.P0 - j0 - (kTileKeys - 1) < p.rel_extent) {
-          // A box starts at distance (P0 + 32 box - j0 - 63) rounded down to 4,
-          // so column 63's distance sits rrow + ((P0 + 1) & 3) into this row.
-          const int col = rrow + ((it.P0 + 1) & 3);
-          const float4* p4 = reinterpret_cast<const float4*>(
-              reinterpret_cast<const float*>(slot + rbox * kRelBoxBytes) + rrow * kRelBoxCols +
-              (col & ~3));
-          switch (col & 3) {  // the same for every lane of the warp
-            case 0: rel_fma<0>(x, sr, p4, scale); break;
-            case 1: rel_fma<1>(x, sr, p4, scale); break;
-            case 2: rel_fma<2>(x, sr, p4, scale); break;
-            default: rel_fma<3>(x, sr, p4, scale); break;
+          if constexpr (R16) {
+            // A box starts at distance (P0 + 32 box - j0 - 63) rounded down to
+            // 8, so column 63's distance sits rrow + ((P0 + 1) & 7) into this
+            // row; it is read from the 4-distance piece below it.
+            const int col = rrow + ((it.P0 + 1) & 7);
+            const uint2* p2 = reinterpret_cast<const uint2*>(
+                reinterpret_cast<const __nv_bfloat16*>(slot + rbox * kRelBoxBytes16) +
+                rrow * kRelBoxCols16 + (col & ~3));
+            switch (col & 3) {  // rrow = 4 lane + q4 (mod 32): the same for the warp
+              case 0: rel_fma16<0>(x, sr, p2, scale); break;
+              case 1: rel_fma16<1>(x, sr, p2, scale); break;
+              case 2: rel_fma16<2>(x, sr, p2, scale); break;
+              default: rel_fma16<3>(x, sr, p2, scale); break;
+            }
+          } else {
+            // A box starts at distance (P0 + 32 box - j0 - 63) rounded down to 4,
+            // so column 63's distance sits rrow + ((P0 + 1) & 3) into this row.
+            const int col = rrow + ((it.P0 + 1) & 3);
+            const float4* p4 = reinterpret_cast<const float4*>(
+                reinterpret_cast<const float*>(slot + rbox * kRelBoxBytes) + rrow * kRelBoxCols +
+                (col & ~3));
+            switch (col & 3) {  // the same for every lane of the warp
+              case 0: rel_fma<0>(x, sr, p4, scale); break;
+              case 1: rel_fma<1>(x, sr, p4, scale); break;
+              case 2: rel_fma<2>(x, sr, p4, scale); break;
+              default: rel_fma<3>(x, sr, p4, scale); break;
+            }
           }
         } else {  // every distance is past rel_extent: no bias
 #pragma unroll
@@ -566,42 +608,72 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         if (!qs) { fail = true; break; }
         load_q(qs, e + 1);
       }
-      // O / l -> bf16, through the scratch slot (the tile's 128 rows, 16-byte
+      // O / l -> out, through the scratch slot (the tile's 128 rows, 16-byte
       // chunks swizzled by row / 4) so that the global stores are whole rows
-      // (16 lanes per 256-byte row).
+      // (16 lanes per 256-byte row).  A bf16 row is DV * 2 bytes; an fp32 row
+      // is twice that and goes in two halves of DV / 2 columns, each the size
+      // of a bf16 row.
       uint8_t* scr = slot_wait(e);
       if (!scr) { fail = true; break; }
       const float inv = l > 0.f ? 1.f / l : 0.f;
-#pragma unroll 1
-      for (int c0 = 0; c0 < DV; c0 += 32) {
-        uint32_t o[32];
-        tmem_ld32(tl + kTmO + c0, o);
-        tmem_wait_ld();
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          uint4 w;
-          w.x = pack_bf16(__uint_as_float(o[8 * i]) * inv, __uint_as_float(o[8 * i + 1]) * inv);
-          w.y = pack_bf16(__uint_as_float(o[8 * i + 2]) * inv, __uint_as_float(o[8 * i + 3]) * inv);
-          w.z = pack_bf16(__uint_as_float(o[8 * i + 4]) * inv, __uint_as_float(o[8 * i + 5]) * inv);
-          w.w = pack_bf16(__uint_as_float(o[8 * i + 6]) * inv, __uint_as_float(o[8 * i + 7]) * inv);
-          const int j = c0 / 8 + i;  // 16-byte chunk of the row
-          *reinterpret_cast<uint4*>(scr + r * (DV * 2) + ((j ^ ((r >> 2) & 7)) << 4)) = w;
-        }
-      }
-      tc_fence_before();  // O is read before the next item's first PV overwrites it
-      named_barrier(1, 128);  // the four softmax warps: every row is in the scratch
-      // whole-row stores: this warp takes rows [32 q4, 32 q4 + 32)
-      constexpr int kCpr = DV / 8;     // 16-byte chunks per row
+      constexpr int kCpr = DV / 8;     // 16-byte chunks per scratch row
       constexpr int kRpi = 32 / kCpr;  // rows per store instruction
+      constexpr int passes = O32 ? 2 : 1;
 #pragma unroll
-      for (int i = 0; i < kCpr; ++i) {
-        const int rr = 32 * q4 + i * kRpi + lane / kCpr;
-        const int ch = lane % kCpr;
-        const uint4 v =
-            *reinterpret_cast<const uint4*>(scr + rr * (DV * 2) + ((ch ^ ((rr >> 2) & 7)) << 4));
-        if (rr < it.rows)
-          *reinterpret_cast<uint4*>(
-              p.out + (static_cast<size_t>(it.r0 + rr) * p.Hq + it.h) * DV + ch * 8) = v;
+      for (int half = 0; half < passes; ++half) {
+        if (half > 0) named_barrier(1, 128);  // the first half's stores have read the scratch
+        constexpr int cw = O32 ? DV / 2 : DV;  // columns of this pass
+#pragma unroll 1
+        for (int c0 = 0; c0 < cw; c0 += 32) {
+          uint32_t o[32];
+          tmem_ld32(tl + kTmO + half * cw + c0, o);
+          tmem_wait_ld();
+          if constexpr (O32) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              uint4 w;
+              w.x = __float_as_uint(__uint_as_float(o[4 * i]) * inv);
+              w.y = __float_as_uint(__uint_as_float(o[4 * i + 1]) * inv);
+              w.z = __float_as_uint(__uint_as_float(o[4 * i + 2]) * inv);
+              w.w = __float_as_uint(__uint_as_float(o[4 * i + 3]) * inv);
+              const int j = c0 / 4 + i;  // 16-byte chunk of the row
+              *reinterpret_cast<uint4*>(scr + r * (DV * 2) + ((j ^ ((r >> 2) & 7)) << 4)) = w;
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              uint4 w;
+              w.x = pack_bf16(__uint_as_float(o[8 * i]) * inv, __uint_as_float(o[8 * i + 1]) * inv);
+              w.y = pack_bf16(__uint_as_float(o[8 * i + 2]) * inv,
+                              __uint_as_float(o[8 * i + 3]) * inv);
+              w.z = pack_bf16(__uint_as_float(o[8 * i + 4]) * inv,
+                              __uint_as_float(o[8 * i + 5]) * inv);
+              w.w = pack_bf16(__uint_as_float(o[8 * i + 6]) * inv,
+                              __uint_as_float(o[8 * i + 7]) * inv);
+              const int j = c0 / 8 + i;  // 16-byte chunk of the row
+              *reinterpret_cast<uint4*>(scr + r * (DV * 2) + ((j ^ ((r >> 2) & 7)) << 4)) = w;
+            }
+          }
+        }
+        // O is read before the next item's first PV overwrites it
+        if (half == passes - 1) tc_fence_before();
+        named_barrier(1, 128);  // the four softmax warps: every row is in the scratch
+        // whole-row stores: this warp takes rows [32 q4, 32 q4 + 32)
+#pragma unroll
+        for (int i = 0; i < kCpr; ++i) {
+          const int rr = 32 * q4 + i * kRpi + lane / kCpr;
+          const int ch = lane % kCpr;
+          const uint4 v =
+              *reinterpret_cast<const uint4*>(scr + rr * (DV * 2) + ((ch ^ ((rr >> 2) & 7)) << 4));
+          if (rr < it.rows) {
+            const size_t orow = (static_cast<size_t>(it.r0 + rr) * p.Hq + it.h) * DV;
+            if constexpr (O32)
+              *reinterpret_cast<uint4*>(static_cast<float*>(p.out) + orow + half * (DV / 2) +
+                                        ch * 4) = v;
+            else
+              *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + orow + ch * 8) = v;
+          }
+        }
       }
       fence_proxy_async_smem();  // these writes come before the slot's next TMA fill
       __syncwarp();
@@ -668,22 +740,33 @@ cudaError_t launch_cache_write(const PrefillParams& p, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+template <int DV, bool R16, bool O32>
+static cudaError_t launch_prefill_as(const PrefillLaunch& L, int grid, int smem,
+                                     cudaStream_t stream) {
+  cudaError_t e = cudaFuncSetAttribute(prefill_kernel<DV, R16, O32>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  prefill_kernel<DV, R16, O32><<<grid, kPfThreads, smem, stream>>>(L.tm_q, L.tm_k, L.tm_v,
+                                                                   L.tm_rel, L.p);
+  return cudaGetLastError();
+}
+
+template <int DV, bool R16>
+static cudaError_t launch_prefill_out(const PrefillLaunch& L, int grid, int smem,
+                                      cudaStream_t stream) {
+  return L.p.out_f32 ? launch_prefill_as<DV, R16, true>(L, grid, smem, stream)
+                     : launch_prefill_as<DV, R16, false>(L, grid, smem, stream);
+}
+
 cudaError_t launch_prefill(const PrefillLaunch& L, int grid, cudaStream_t stream) {
   const PrefillParams& p = L.p;
   const int smem = prefill_smem_bytes(p.B, p.dv, p.ring_stages);
-  cudaError_t e;
-  if (p.dv == 128) {
-    e = cudaFuncSetAttribute(prefill_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             smem);
-    if (e != cudaSuccess) return e;
-    prefill_kernel<128><<<grid, kPfThreads, smem, stream>>>(L.tm_q, L.tm_k, L.tm_v, L.tm_rel, p);
-  } else {
-    e = cudaFuncSetAttribute(prefill_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             smem);
-    if (e != cudaSuccess) return e;
-    prefill_kernel<64><<<grid, kPfThreads, smem, stream>>>(L.tm_q, L.tm_k, L.tm_v, L.tm_rel, p);
-  }
-  return cudaGetLastError();
+  const bool r16 = p.rel_es == 2;
+  if (p.dv == 128)
+    return r16 ? launch_prefill_out<128, true>(L, grid, smem, stream)
+               : launch_prefill_out<128, false>(L, grid, smem, stream);
+  return r16 ? launch_prefill_out<64, true>(L, grid, smem, stream)
+             : launch_prefill_out<64, false>(L, grid, smem, stream);
 }
 
 cudaError_t launch_prefill_walk(const PrefillParams& p, cudaStream_t stream) {

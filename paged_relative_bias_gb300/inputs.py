@@ -36,6 +36,7 @@ class DecodeWorkload:
     pool_blocks: int = 0  # 0: exactly the blocks the sequences need
     max_blocks_per_seq: int = 0  # 0: the longest sequence's block count
     query_tokens: int = 0  # > 0: multi-token decode, q [B, k, Hq, d], rel [B, k, Hq, E]
+    rel_dtype: str = "f32"  # "bf16": rel drawn in fp32 and rounded to bf16
 
 
 @dataclass(frozen=True)
@@ -51,6 +52,7 @@ class PrefillWorkload:
     ctx_lens: tuple      # cached prefix per sequence
     block_table: tuple = ()  # explicit table rows; () draws a random one
     pool_blocks: int = 0
+    rel_dtype: str = "f32"  # "bf16": rel drawn in fp32 and rounded to bf16
 
     @property
     def batch(self) -> int:
@@ -87,6 +89,9 @@ WORKLOADS = {
         ("uniform", 4096, 32768), pool_blocks=4096, max_blocks_per_seq=256,
         query_tokens=8),
 }
+
+
+_REL_DTYPES = {"f32": torch.float32, "bf16": torch.bfloat16}
 
 
 def variant(wl, **changes):
@@ -161,6 +166,7 @@ def make_decode(wl: DecodeWorkload, device="cpu", seed_data: int = 0,
     tok = (wl.query_tokens,) if wl.query_tokens > 0 else ()
     q = _randn((B, *tok, Hq, wl.d_qk), g, device, torch.bfloat16)
     rel = _randn((B, *tok, Hq, wl.rel_extent), g, device, torch.float32)
+    rel = rel.to(_REL_DTYPES[wl.rel_dtype])
     k_cache = _randn((pool, BLOCK_SIZE, Hkv, wl.d_qk), g, device, torch.bfloat16)
     v_cache = _randn((pool, BLOCK_SIZE, Hkv, wl.d_v), g, device, torch.bfloat16)
     return dict(
@@ -215,6 +221,7 @@ def make_prefill(wl: PrefillWorkload, device="cpu", seed_data: int = 0,
     k = _randn((T, Hkv, wl.d_qk), g, device, torch.bfloat16)
     v = _randn((T, Hkv, wl.d_v), g, device, torch.bfloat16)
     rel = _randn((T, Hq, wl.rel_extent), g, device, torch.float32)
+    rel = rel.to(_REL_DTYPES[wl.rel_dtype])
     k_cache = _randn((pool, BLOCK_SIZE, Hkv, wl.d_qk), g, device, torch.bfloat16)
     v_cache = _randn((pool, BLOCK_SIZE, Hkv, wl.d_v), g, device, torch.bfloat16)
     return dict(

@@ -39,6 +39,7 @@ EXPORTS = (
     "relattn_decode_noalloc",
     "relattn_decode_multi",
     "relattn_decode_ex",
+    "relattn_prefill_ex",
 )
 
 DTYPE_F32 = 0
@@ -120,6 +121,10 @@ def lib() -> ctypes.CDLL:
                                     c_void_p, c_int32, c_int32, c_int32, S, c_void_p, c_void_p,
                                     c_size_t, c_void_p]
     L.relattn_decode_ex.restype = c_int
+    L.relattn_prefill_ex.argtypes = [c_void_p, c_void_p, c_void_p, c_void_p, POINTER(IoTypes),
+                                     c_void_p, P, c_void_p, c_void_p, c_int32, c_int32, S,
+                                     c_void_p, c_void_p, c_size_t, c_void_p]
+    L.relattn_prefill_ex.restype = c_int
     L.relattn_abi_version.argtypes = []
     L.relattn_abi_version.restype = c_int
     _LIB = L
@@ -325,14 +330,21 @@ def prefill_dims(q, block_table, ctx_lens, max_q_len: int, num_ctas=0) -> Dims:
 
 def relattn_prefill(q, k, v, rel, cu_seqlens, k_cache, v_cache, block_table, ctx_lens,
                     window: int, rel_extent: int, max_q_len: int, out=None,
-                    workspace=None):
-    """Chunked prefill with a cached prefix; writes k, v into the cache."""
+                    workspace=None, out_dtype=torch.bfloat16):
+    """Chunked prefill with a cached prefix; writes k, v into the cache.
+
+    rel may be float32 or bfloat16, out bfloat16 or float32 (``out``'s own
+    dtype when it is given); other than fp32 rel and bf16 out goes through
+    ``relattn_prefill_ex``.
+    """
     dev = q.device
     T, Hq, dqk = q.shape
+    out_dtype = out.dtype if out is not None else out_dtype
+    io = _io_types(rel, out_dtype)
     _need(q, "q", torch.bfloat16, 3, dev)
     _need(k, "k", torch.bfloat16, 3, dev)
     _need(v, "v", torch.bfloat16, 3, dev)
-    _need(rel, "rel", torch.float32, 3, dev)
+    _need(rel, "rel", rel.dtype, 3, dev)
     _need(k_cache, "k_cache", torch.bfloat16, 4, dev)
     _need(v_cache, "v_cache", torch.bfloat16, 4, dev)
     _need(block_table, "block_table", torch.int32, 2, dev)
@@ -348,16 +360,24 @@ def relattn_prefill(q, k, v, rel, cu_seqlens, k_cache, v_cache, block_table, ctx
     cache = cache_desc(k_cache, v_cache)
     dims = prefill_dims(q, block_table, ctx_lens, max_q_len)
     if out is None:
-        out = torch.empty((T, Hq, v_cache.shape[3]), dtype=torch.bfloat16, device=dev)
+        out = torch.empty((T, Hq, v_cache.shape[3]), dtype=out_dtype, device=dev)
     else:
-        _need(out, "out", torch.bfloat16, 3, dev)
+        _need(out, "out", out_dtype, 3, dev)
     if workspace is None:
         workspace = new_workspace(workspace_size(dims, cache), dev)
-    _check(lib().relattn_prefill(
-        q.data_ptr(), k.data_ptr(), v.data_ptr(), rel.data_ptr(), cu_seqlens.data_ptr(),
-        ctypes.byref(cache), block_table.data_ptr(), ctx_lens.data_ptr(), int(window),
-        int(rel_extent), ctypes.byref(dims), out.data_ptr(), workspace.data_ptr(),
-        workspace.numel(), _stream(dev)), "relattn_prefill")
+    if rel.dtype == torch.float32 and out_dtype == torch.bfloat16:
+        _check(lib().relattn_prefill(
+            q.data_ptr(), k.data_ptr(), v.data_ptr(), rel.data_ptr(), cu_seqlens.data_ptr(),
+            ctypes.byref(cache), block_table.data_ptr(), ctx_lens.data_ptr(), int(window),
+            int(rel_extent), ctypes.byref(dims), out.data_ptr(), workspace.data_ptr(),
+            workspace.numel(), _stream(dev)), "relattn_prefill")
+    else:
+        _check(lib().relattn_prefill_ex(
+            q.data_ptr(), k.data_ptr(), v.data_ptr(), rel.data_ptr(), ctypes.byref(io),
+            cu_seqlens.data_ptr(), ctypes.byref(cache), block_table.data_ptr(),
+            ctx_lens.data_ptr(), int(window), int(rel_extent), ctypes.byref(dims),
+            out.data_ptr(), workspace.data_ptr(), workspace.numel(), _stream(dev)),
+            "relattn_prefill_ex")
     return out
 
 

@@ -31,12 +31,15 @@ def to_f64(t: torch.Tensor) -> np.ndarray:
     return t.detach().cpu().double().numpy()
 
 
+def host_rel(rel: torch.Tensor):
+    """rel for the oracle: float32 values, or bf16 bit patterns."""
+    return bf16_bits(rel) if rel.dtype == torch.bfloat16 else rel.cpu().numpy()
+
+
 def host_decode_inputs(case):
     """numpy copies of a decode case for the oracle (bf16 kept as bits)."""
-    rel = case["rel"]
     return dict(
-        q=bf16_bits(case["q"]),
-        rel=bf16_bits(rel) if rel.dtype == torch.bfloat16 else rel.cpu().numpy(),
+        q=bf16_bits(case["q"]), rel=host_rel(case["rel"]),
         k_cache=bf16_bits(case["k_cache"]), v_cache=bf16_bits(case["v_cache"]),
         block_table=case["block_table"].cpu().numpy(),
         seq_lens=case["seq_lens"].cpu().numpy())
@@ -53,7 +56,7 @@ class RowRel:
     """rel rows of a few packed tokens, indexable as rel[row, h]."""
 
     def __init__(self, rel: torch.Tensor, rows):
-        self.rows = {int(r): rel[int(r)].cpu().numpy() for r in rows}
+        self.rows = {int(r): host_rel(rel[int(r)]) for r in rows}
 
     def __getitem__(self, idx):
         row, h = idx
@@ -83,7 +86,7 @@ def oracle_prefill(case, rows=None, cache=None):
     q, rel = case["q"], case["rel"]
     kc, vc = cache if cache is not None else snapshot_cache(case)
     if rows is None:
-        qn, reln = bf16_bits(q), rel.cpu().numpy()
+        qn, reln = bf16_bits(q), host_rel(rel)
     else:
         qn = RowQ(q, rows)
         qn._shape = tuple(q.shape)
