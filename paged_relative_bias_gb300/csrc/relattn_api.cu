@@ -308,16 +308,18 @@ static int prepare_decode(const void* q, const void* rel, IoTypes io,
     return RELATTN_ERR_CUDA;
   // query rows of one chunk: q [B*k][Hq][128] bf16 as (column, head, token);
   // a box is one 64-column half of kpc tokens x g heads (rows token * g + head).
-  // One token: the 2-D view [B*Hq][128] and a box of the group's g rows.
+  // The one-token kernel (g <= 8): the 2-D view [B*Hq][128] and a box of the
+  // group's g rows.
   const cuuint64_t qd[3] = {128, static_cast<cuuint64_t>(dims->num_q_heads),
                             static_cast<cuuint64_t>(dims->batch) * kq};
   const cuuint64_t qs[2] = {256, static_cast<cuuint64_t>(dims->num_q_heads) * 256};
   const cuuint32_t qbx[3] = {64, static_cast<cuuint32_t>(g), static_cast<cuuint32_t>(kpc)};
   const cuuint64_t qd1[2] = {128, static_cast<cuuint64_t>(dims->batch) * dims->num_q_heads};
-  if (!(kq > 1 ? make_map(&L->tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q),
-                          qd, qs, qbx, CU_TENSOR_MAP_SWIZZLE_128B)
-               : make_map(&L->tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(q),
-                          qd1, qs, qbx, CU_TENSOR_MAP_SWIZZLE_128B)))
+  const bool q3 = decode_multi_kernel(kq, g);
+  if (!(q3 ? make_map(&L->tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), qd, qs,
+                      qbx, CU_TENSOR_MAP_SWIZZLE_128B)
+           : make_map(&L->tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(q), qd1,
+                      qs, qbx, CU_TENSOR_MAP_SWIZZLE_128B)))
     return RELATTN_ERR_CUDA;
   return RELATTN_OK;
 }

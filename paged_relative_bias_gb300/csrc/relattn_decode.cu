@@ -45,7 +45,7 @@ constexpr int kConsumerThreads = 32 * kConsumerWarps;
 constexpr int kWholeSlackTiles = 4;  // tolerated imbalance to avoid a split
 constexpr int kQBufBytes = 4096;     // 16 rows x 256 B as two swizzled halves
 constexpr int kMiscAbort = 14;       // shared flag word: a consumer warp gave up waiting
-constexpr int kSlicePad = 8;         // floats of padding per merge-slice row (bank spread)
+constexpr int kSlicePad = 8;         // floats of padding per merge-slice row, at most
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kNegInf = -__builtin_huge_valf();
 
@@ -494,6 +494,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   constexpr int RES = R16 ? 2 : 4;                // bytes per rel element
   constexpr int RW = R16 ? kRelBoxW16 : kRelBoxW;  // distances per rel box row
   constexpr int RAL = R16 ? ~7 : ~3;               // box start: 16-byte aligned distance
+  constexpr int NB = MULTI ? 2 : 1;                // 8-row blocks of a tile's rows
+  constexpr int DB = DV / 16;                      // 16-column blocks of d_v
+  // merge-slice row padding: conflict-free writes of O^T columns (NB = 1:
+  // rows 2 cq apart by 2 (DV + 4) = 8 banks mod 32) or of O rows (NB = 2)
+  constexpr int SP = NB == 1 ? 4 : kSlicePad;
   const DecodeSmem L(ns, p.B, p.Bv, tok.kpc, g, DV, RES);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
   uint64_t* empty = full + ns;
@@ -733,9 +738,14 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     const uint32_t qbase = smem_u32(smem + L.qbuf + qb * kQBufBytes);
 
     float m_[2] = {kNegInf, kNegInf}, l_[2] = {0.f, 0.f};
-    float o[DV / 8][4];
+    // One-token kernel (at most 8 rows, NB = 1): O^T = V^T P^T, 16 columns
+    // of d_v by 8 rows per MMA; o[db] holds d_v columns 16 db + lane/4 (+8)
+    // of rows 2 cq (+1): half the MMAs of a 16-row P V and half of O's
+    // registers.  General kernel (16 rows): O = P V, o[nd] holds rows r0
+    // (+8), columns 8 nd + 2 cq (+1).
+    float o[DV / 8 / (2 / NB)][4];
 #pragma unroll
-    for (int i = 0; i < DV / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    for (int i = 0; i < DV / 8 / (2 / NB); ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
 
     for (int t = (n_base + grp) & 1 ? 1 : 0; t < pc.n; t += 2) {
       const int n = n_base + t;
@@ -789,7 +799,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
 #pragma unroll
           for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
+            for (int i = 0; i < 2 * NB; ++i) {  // rows r0 (and r0 + 8 with NB = 2)
               const int row = r0 + (i >> 1) * 8;
               const int e = nt * 8 + (i & 1);
               const int key = kb + e;
@@ -825,9 +835,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
               x[nt][i] = (e < mlo[rr] || e > mhi[rr]) ? kNegInf : v;
             }
         }
-        // online softmax, rows r0 (rr=0) and r0+8 (rr=1)
+        // online softmax, rows r0 (rr=0) and r0+8 (rr=1; only with NB = 2)
+        float al[2];
 #pragma unroll
-        for (int rr = 0; rr < 2; ++rr) {
+        for (int rr = 0; rr < NB; ++rr) {
           float mx = fmaxf(fmaxf(x[0][2 * rr], x[0][2 * rr + 1]),
                            fmaxf(x[1][2 * rr], x[1][2 * rr + 1]));
           mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
@@ -846,20 +857,50 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
               sum += pv;
             }
           l_[rr] = l_[rr] * alpha + sum;
+          al[rr] = alpha;
+        }
+        const uint32_t vbase = kbase + 16384;
+        const int mi = lane >> 3;
+        if constexpr (NB == 1) {
+          // O^T's columns are rows 2 cq (+1), whose alphas sit with the lanes
+          // holding those S rows (lanes 4 R .. 4 R + 3 hold row R)
+          const float a0 = __shfl_sync(0xffffffffu, al[0], 8 * cq);
+          const float a1 = __shfl_sync(0xffffffffu, al[0], 8 * cq + 4);
+#pragma unroll
+          for (int db = 0; db < DB; ++db) {
+            o[db][0] *= a0;
+            o[db][1] *= a1;
+            o[db][2] *= a0;
+            o[db][3] *= a1;
+          }
+          // P^T as the B operand: its fragment is this thread's own S values
+          // (keys 2 cq, 2 cq + 1 and 8 more, row lane / 4)
+          const uint32_t pb0 = pack_bf16(x[0][0], x[0][1]);
+          const uint32_t pb1 = pack_bf16(x[1][0], x[1][1]);
+          // V^T as the A operand: transposed 8x8 loads of V's [key][d_v]
+          // rows; matrices (keys 0-7 | 8-15) x (columns 16 db + 0-7 | 8-15)
+          const int key = 16 * cw + (mi >> 1) * 8 + (lane & 7);
+#pragma unroll
+          for (int db = 0; db < DB; ++db) {
+            const int chunk = 2 * db + (mi & 1);
+            uint32_t va[4];
+            ldsm_x4_t(vbase + (chunk >> 3) * 8192 + sw128(key, chunk & 7), va[0], va[1], va[2],
+                      va[3]);
+            mma_16816(o[db], va, pb0, pb1);
+          }
+        } else {
 #pragma unroll
           for (int nd = 0; nd < DV / 8; ++nd) {
-            o[nd][2 * rr] *= alpha;
-            o[nd][2 * rr + 1] *= alpha;
+            o[nd][0] *= al[0];
+            o[nd][1] *= al[0];
+            o[nd][2] *= al[1];
+            o[nd][3] *= al[1];
           }
-        }
-        uint32_t pa[4];
-        pa[0] = pack_bf16(x[0][0], x[0][1]);
-        pa[1] = pack_bf16(x[0][2], x[0][3]);
-        pa[2] = pack_bf16(x[1][0], x[1][1]);
-        pa[3] = pack_bf16(x[1][2], x[1][3]);
-        {
-          const uint32_t vbase = kbase + 16384;
-          const int mi = lane >> 3;
+          uint32_t pa[4];
+          pa[0] = pack_bf16(x[0][0], x[0][1]);
+          pa[1] = pack_bf16(x[0][2], x[0][3]);
+          pa[2] = pack_bf16(x[1][0], x[1][1]);
+          pa[3] = pack_bf16(x[1][2], x[1][3]);
           const int key = 16 * cw + (mi & 1) * 8 + (lane & 7);
 #pragma unroll
           for (int nd = 0; nd < DV / 8; nd += 2) {
@@ -884,7 +925,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
 
     // ---- merge the eight consumer warps of this piece
 #pragma unroll
-    for (int rr = 0; rr < 2; ++rr) {
+    for (int rr = 0; rr < NB; ++rr) {
       l_[rr] += __shfl_xor_sync(0xffffffffu, l_[rr], 1);
       l_[rr] += __shfl_xor_sync(0xffffffffu, l_[rr], 2);
       if (cq == 0) {
@@ -895,19 +936,37 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     named_barrier(1, kConsumerThreads);
     if (s_misc[kMiscAbort]) break;
     const int srows = tok.kpc * g;  // rows of a warp's merge slice
+    if constexpr (NB == 1) {
 #pragma unroll
-    for (int rr = 0; rr < 2; ++rr) {
-      const int row = r0 + 8 * rr;
-      if (!rv[rr]) continue;
-      float M = s_m[row];
+      for (int e = 0; e < 2; ++e) {
+        const int row = 2 * cq + e;  // this thread's O^T column
+        if (row >= nrows) continue;
+        float M = s_m[row];
 #pragma unroll
-      for (int w = 1; w < kConsumerWarps; ++w) M = fmaxf(M, s_m[w * 16 + row]);
-      const float fct = M == kNegInf ? 0.f : ex2(m_[rr] - M);
-      float* sl = slices + (cwarp * srows + row) * (DV + kSlicePad) + cq * 2;
+        for (int w = 1; w < kConsumerWarps; ++w) M = fmaxf(M, s_m[w * 16 + row]);
+        const float fct = M == kNegInf ? 0.f : ex2(s_m[cwarp * 16 + row] - M);
+        float* sl = slices + (cwarp * srows + row) * (DV + SP) + (lane >> 2);
 #pragma unroll
-      for (int nd = 0; nd < DV / 8; ++nd)
-        *reinterpret_cast<float2*>(sl + nd * 8) =
-            make_float2(o[nd][2 * rr] * fct, o[nd][2 * rr + 1] * fct);
+        for (int db = 0; db < DB; ++db) {
+          sl[16 * db] = o[db][e] * fct;
+          sl[16 * db + 8] = o[db][2 + e] * fct;
+        }
+      }
+    } else {
+#pragma unroll
+      for (int rr = 0; rr < 2; ++rr) {
+        const int row = r0 + 8 * rr;
+        if (!rv[rr]) continue;
+        float M = s_m[row];
+#pragma unroll
+        for (int w = 1; w < kConsumerWarps; ++w) M = fmaxf(M, s_m[w * 16 + row]);
+        const float fct = M == kNegInf ? 0.f : ex2(m_[rr] - M);
+        float* sl = slices + (cwarp * srows + row) * (DV + SP) + cq * 2;
+#pragma unroll
+        for (int nd = 0; nd < DV / 8; ++nd)
+          *reinterpret_cast<float2*>(sl + nd * 8) =
+              make_float2(o[nd][2 * rr] * fct, o[nd][2 * rr + 1] * fct);
+      }
     }
     if (ctid < nrows) {
       float M = s_m[ctid];
@@ -935,7 +994,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
 #pragma unroll
       for (int w = 0; w < kConsumerWarps; ++w) {
         const float2 v =
-            *reinterpret_cast<const float2*>(slices + (w * srows + row) * (DV + kSlicePad) + col);
+            *reinterpret_cast<const float2*>(slices + (w * srows + row) * (DV + SP) + col);
         v0 += v.x;
         v1 += v.y;
       }
@@ -1079,7 +1138,7 @@ static cudaError_t launch_decode_rel(const DecodeLaunch& L, int smem, cudaStream
 cudaError_t launch_decode(const DecodeLaunch& L, cudaStream_t stream) {
   const DecodeParams& p = L.p;
   const int smem = decode_smem_bytes(p.nstages, p.B, p.Bv, p.kpc, p.g, p.dv, p.rel_es);
-  const bool multi = p.k > 1;
+  const bool multi = decode_multi_kernel(p.k, p.g);
   if (p.dv == 128)
     return multi ? launch_decode_rel<128, true>(L, smem, stream)
                  : launch_decode_rel<128, false>(L, smem, stream);

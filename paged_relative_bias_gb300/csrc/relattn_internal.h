@@ -77,6 +77,10 @@ struct PrefillLaunch {
 
 int decode_smem_bytes(int nstages, int B, int Bv, int kpc, int g, int dv, int rel_es);
 constexpr int kMaxDecodeRows = 16;         // rows of one decode tile: g heads x tokens
+// The decode kernel has a one-token instantiation for tiles of at most 8 rows
+// and a general one (several tokens, or g > 8), which also takes its query
+// rows through a 3-D copy.
+inline bool decode_multi_kernel(int k, int g) { return k > 1 || g > 8; }
 constexpr int kMaxQueryTokens = 16;        // query tokens per sequence in one decode call
 cudaError_t launch_decode(const DecodeLaunch& L, cudaStream_t stream);
 cudaError_t launch_decode_walk(const DecodeParams& p, int grid, cudaStream_t stream);
