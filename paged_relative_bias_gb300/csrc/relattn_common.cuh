@@ -177,6 +177,21 @@ __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0,
       : "r"(addr));
 }
 
+// Two 8x8 matrices; lanes 0-15 give the row addresses.
+__device__ __forceinline__ void ldsm_x2(uint32_t addr, uint32_t& r0, uint32_t& r1) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];"
+               : "=r"(r0), "=r"(r1)
+               : "r"(addr));
+}
+
+// Transpose of an 8x8 matrix of 16-bit elements held as one register per
+// lane (lane t: row t/4, columns 2 (t%4) and 2 (t%4) + 1).
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t a) {
+  uint32_t d;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+  return d;
+}
+
 __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0,
                                           uint32_t& r1, uint32_t& r2,
                                           uint32_t& r3) {

@@ -760,58 +760,119 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       if (s_valid[stage]) {
         const uint8_t* st = smem + L.stages + stage * L.stage_bytes;
         const uint32_t kbase = smem_u32(st);
-        float s[2][4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) s[0][i] = s[1][i] = 0.f;
-        {
-          const int mi = lane >> 3;
-          const int key = 16 * cw + (mi >> 1) * 8 + (lane & 7);
-          const int qrow = (mi & 1) * 8 + (lane & 7);
-#pragma unroll
-          for (int ks = 0; ks < 8; ++ks) {
-            const int qchunk = ks * 2 + (mi >> 1);
-            uint32_t qa[4];
-            ldsm_x4(qbase + (qchunk >> 3) * 2048 + sw128(qrow, qchunk & 7), qa[0], qa[1], qa[2],
-                    qa[3]);
-            const int chunk = ks * 2 + (mi & 1);
-            uint32_t b0, b1, b2, b3;
-            ldsm_x4(kbase + (chunk >> 3) * 8192 + sw128(key, chunk & 7), b0, b1, b2, b3);
-            mma_16816(s[0], qa, b0, b1);
-            mma_16816(s[1], qa, b2, b3);
-          }
-        }
+        const uint32_t vbase = kbase + 16384;
+        const int mi = lane >> 3;
         // logits in log2 units: (q.k/sqrt(d) + rel) * log2(e).  A row's rel
         // box starts at its smallest distance in the tile, P - key0 - 63,
         // rounded down to 16 bytes.
         const RelT* relt = reinterpret_cast<const RelT*>(smem + L.rel + stage * L.rel_bytes);
         const bool edge = key0 < lo_last || key0 + kTileKeys - 1 > sq.pf;  // any mask?
-        // this thread's keys are kb + e, e in {0, 1, 8, 9}; a row keeps the
-        // keys with e in [mlo, mhi] (all of them when no key of the tile is
-        // masked) -- compares with immediates and selects, no branches
-        const int kb = key0 + 16 * cw + cq * 2;
-        float x[2][4];
-        if constexpr (!MULTI) {
-          // one position for all rows: one box, present or not for the tile
+        if constexpr (NB == 1) {
+          // ---- one token, at most 8 rows: S^T = K Q^T (16 keys x 8 rows per
+          // MMA), softmax down the columns, P^T moved into the B operand of
+          // O^T = V^T P^T.  st[0..1]: keys kb (this thread's key), rows
+          // 2 cq (+1); st[2..3]: keys kb + 8.
+          float sT[4] = {0.f, 0.f, 0.f, 0.f};
+          {
+            // A = the warp's 16 K rows: matrices (keys 0-7 | 8-15) x
+            // (dims 0-7 | 8-15); B = Q^T from rows 0-7 of the query buffer
+            const int key = 16 * cw + (mi & 1) * 8 + (lane & 7);
+            const int qrow = lane & 7, qhalf = (lane >> 3) & 1;
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+              const int chunk = ks * 2 + (mi >> 1);
+              uint32_t ka[4];
+              ldsm_x4(kbase + (chunk >> 3) * 8192 + sw128(key, chunk & 7), ka[0], ka[1], ka[2],
+                      ka[3]);
+              const int qchunk = ks * 2 + qhalf;
+              uint32_t qb0, qb1;
+              ldsm_x2(qbase + (qchunk >> 3) * 2048 + sw128(qrow, qchunk & 7), qb0, qb1);
+              mma_16816(sT, ka, qb0, qb1);
+            }
+          }
+          // one position for all rows: one rel box, present or not for the
+          // tile; this thread's keys are kb and kb + 8, kept when their offset
+          // (0 or 8) lies in [mlo, mhi]
+          const int kb = key0 + 16 * cw + (lane >> 2);
           const int dmin = sq.pf - key0 - (kTileKeys - 1);
           const bool need_rel = dmin < p.rel_extent;
           const int d0 = dmin & RAL;
           const int mlo = edge ? sq.lo - kb : INT_MIN, mhi = edge ? sq.pf - kb : INT_MAX;
+          float x[4];
 #pragma unroll
-          for (int nt = 0; nt < 2; ++nt)
+          for (int i = 0; i < 4; ++i) {
+            const int row = 2 * cq + (i & 1);
+            const int e = (i >> 1) * 8;
+            float bias = 0.f;
+            if (need_rel && row < g) bias = rel_f32(relt[row * RW + (sq.pf - kb - e - d0)]);
+            const float v = fmaf(sT[i], p.scale_log2, bias * kLog2e);
+            x[i] = (e < mlo || e > mhi) ? kNegInf : v;
+          }
+          // online softmax of rows 2 cq + j over the warp's 16 keys: the 8
+          // lanes with this cq hold them (lane bits 2-4)
 #pragma unroll
-            for (int i = 0; i < 2 * NB; ++i) {  // rows r0 (and r0 + 8 with NB = 2)
-              const int row = r0 + (i >> 1) * 8;
-              const int e = nt * 8 + (i & 1);
-              const int key = kb + e;
-              float bias = 0.f;
-              if (need_rel && row < g) bias = rel_f32(relt[row * RW + (sq.pf - key - d0)]);
-              const float v = fmaf(s[nt][i], p.scale_log2, bias * kLog2e);
-              x[nt][i] = (e < mlo || e > mhi) ? kNegInf : v;
+          for (int j = 0; j < 2; ++j) {
+            float mx = fmaxf(x[j], x[2 + j]);
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+            const float m_new = fmaxf(m_[j], mx);
+            const float m_use = m_new == kNegInf ? 0.f : m_new;
+            const float alpha = ex2(m_[j] - m_use);
+            m_[j] = m_new;
+            x[j] = ex2(x[j] - m_use);
+            x[2 + j] = ex2(x[2 + j] - m_use);
+            l_[j] = l_[j] * alpha + (x[j] + x[2 + j]);  // this thread's two keys
+#pragma unroll
+            for (int db = 0; db < DB; ++db) {
+              o[db][j] *= alpha;
+              o[db][2 + j] *= alpha;
             }
+          }
+          // P^T as the B operand of O^T = V^T P^T: the transposes of this
+          // thread's (keys, rows) pairs are its (rows, keys) fragments
+          const uint32_t pb0 = movmatrix_t(pack_bf16(x[0], x[1]));
+          const uint32_t pb1 = movmatrix_t(pack_bf16(x[2], x[3]));
+          // V^T as the A operand: transposed 8x8 loads of V's [key][d_v]
+          // rows; matrices (keys 0-7 | 8-15) x (columns 16 db + 0-7 | 8-15)
+          const int vkey = 16 * cw + (mi >> 1) * 8 + (lane & 7);
+#pragma unroll
+          for (int db = 0; db < DB; ++db) {
+            const int chunk = 2 * db + (mi & 1);
+            uint32_t va[4];
+            ldsm_x4_t(vbase + (chunk >> 3) * 8192 + sw128(vkey, chunk & 7), va[0], va[1], va[2],
+                      va[3]);
+            mma_16816(o[db], va, pb0, pb1);
+          }
         } else {
-          // per row: its token's box, present when the row's smallest
+          // ---- several tokens (or g > 8), 16 rows: S = Q K^T, O = P V
+          float s[2][4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) s[0][i] = s[1][i] = 0.f;
+          {
+            const int key = 16 * cw + (mi >> 1) * 8 + (lane & 7);
+            const int qrow = (mi & 1) * 8 + (lane & 7);
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+              const int qchunk = ks * 2 + (mi >> 1);
+              uint32_t qa[4];
+              ldsm_x4(qbase + (qchunk >> 3) * 2048 + sw128(qrow, qchunk & 7), qa[0], qa[1],
+                      qa[2], qa[3]);
+              const int chunk = ks * 2 + (mi & 1);
+              uint32_t b0, b1, b2, b3;
+              ldsm_x4(kbase + (chunk >> 3) * 8192 + sw128(key, chunk & 7), b0, b1, b2, b3);
+              mma_16816(s[0], qa, b0, b1);
+              mma_16816(s[1], qa, b2, b3);
+            }
+          }
+          // this thread's keys are kb + e, e in {0, 1, 8, 9}; a row keeps the
+          // keys with e in [mlo, mhi] (all of them when no key of the tile is
+          // masked) -- compares with immediates and selects, no branches.
+          // Per row: its token's box, present when the row's smallest
           // distance in the tile is below rel_extent (the box reads 0 past
           // it), and the box entry of key key0 -- the others at -offset
+          const int kb = key0 + 16 * cw + cq * 2;
+          float x[2][4];
           bool nr[2];
           const RelT* rb[2];
           int mlo[2], mhi[2];
@@ -834,67 +895,32 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
               const float v = fmaf(s[nt][i], p.scale_log2, bias * kLog2e);
               x[nt][i] = (e < mlo[rr] || e > mhi[rr]) ? kNegInf : v;
             }
-        }
-        // online softmax, rows r0 (rr=0) and r0+8 (rr=1; only with NB = 2)
-        float al[2];
+          // online softmax, rows r0 (rr=0) and r0+8 (rr=1)
 #pragma unroll
-        for (int rr = 0; rr < NB; ++rr) {
-          float mx = fmaxf(fmaxf(x[0][2 * rr], x[0][2 * rr + 1]),
-                           fmaxf(x[1][2 * rr], x[1][2 * rr + 1]));
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-          const float m_new = fmaxf(m_[rr], mx);
-          const float m_use = m_new == kNegInf ? 0.f : m_new;
-          const float alpha = ex2(m_[rr] - m_use);
-          m_[rr] = m_new;
-          float sum = 0.f;
+          for (int rr = 0; rr < 2; ++rr) {
+            float mx = fmaxf(fmaxf(x[0][2 * rr], x[0][2 * rr + 1]),
+                             fmaxf(x[1][2 * rr], x[1][2 * rr + 1]));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+            const float m_new = fmaxf(m_[rr], mx);
+            const float m_use = m_new == kNegInf ? 0.f : m_new;
+            const float alpha = ex2(m_[rr] - m_use);
+            m_[rr] = m_new;
+            float sum = 0.f;
 #pragma unroll
-          for (int nt = 0; nt < 2; ++nt)
+            for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const float pv = ex2(x[nt][2 * rr + e] - m_use);
-              x[nt][2 * rr + e] = pv;
-              sum += pv;
+              for (int e = 0; e < 2; ++e) {
+                const float pv = ex2(x[nt][2 * rr + e] - m_use);
+                x[nt][2 * rr + e] = pv;
+                sum += pv;
+              }
+            l_[rr] = l_[rr] * alpha + sum;
+#pragma unroll
+            for (int nd = 0; nd < DV / 8; ++nd) {
+              o[nd][2 * rr] *= alpha;
+              o[nd][2 * rr + 1] *= alpha;
             }
-          l_[rr] = l_[rr] * alpha + sum;
-          al[rr] = alpha;
-        }
-        const uint32_t vbase = kbase + 16384;
-        const int mi = lane >> 3;
-        if constexpr (NB == 1) {
-          // O^T's columns are rows 2 cq (+1), whose alphas sit with the lanes
-          // holding those S rows (lanes 4 R .. 4 R + 3 hold row R)
-          const float a0 = __shfl_sync(0xffffffffu, al[0], 8 * cq);
-          const float a1 = __shfl_sync(0xffffffffu, al[0], 8 * cq + 4);
-#pragma unroll
-          for (int db = 0; db < DB; ++db) {
-            o[db][0] *= a0;
-            o[db][1] *= a1;
-            o[db][2] *= a0;
-            o[db][3] *= a1;
-          }
-          // P^T as the B operand: its fragment is this thread's own S values
-          // (keys 2 cq, 2 cq + 1 and 8 more, row lane / 4)
-          const uint32_t pb0 = pack_bf16(x[0][0], x[0][1]);
-          const uint32_t pb1 = pack_bf16(x[1][0], x[1][1]);
-          // V^T as the A operand: transposed 8x8 loads of V's [key][d_v]
-          // rows; matrices (keys 0-7 | 8-15) x (columns 16 db + 0-7 | 8-15)
-          const int key = 16 * cw + (mi >> 1) * 8 + (lane & 7);
-#pragma unroll
-          for (int db = 0; db < DB; ++db) {
-            const int chunk = 2 * db + (mi & 1);
-            uint32_t va[4];
-            ldsm_x4_t(vbase + (chunk >> 3) * 8192 + sw128(key, chunk & 7), va[0], va[1], va[2],
-                      va[3]);
-            mma_16816(o[db], va, pb0, pb1);
-          }
-        } else {
-#pragma unroll
-          for (int nd = 0; nd < DV / 8; ++nd) {
-            o[nd][0] *= al[0];
-            o[nd][1] *= al[0];
-            o[nd][2] *= al[1];
-            o[nd][3] *= al[1];
           }
           uint32_t pa[4];
           pa[0] = pack_bf16(x[0][0], x[0][1]);
@@ -924,13 +950,28 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     n_base += pc.n;
 
     // ---- merge the eight consumer warps of this piece
+    if constexpr (NB == 1) {
+      // rows 2 cq + j: m is the same in the 8 lanes of this cq, l sums over
+      // their keys
 #pragma unroll
-    for (int rr = 0; rr < NB; ++rr) {
-      l_[rr] += __shfl_xor_sync(0xffffffffu, l_[rr], 1);
-      l_[rr] += __shfl_xor_sync(0xffffffffu, l_[rr], 2);
-      if (cq == 0) {
-        s_m[cwarp * 16 + r0 + 8 * rr] = m_[rr];
-        s_l[cwarp * 16 + r0 + 8 * rr] = l_[rr];
+      for (int j = 0; j < 2; ++j) {
+        l_[j] += __shfl_xor_sync(0xffffffffu, l_[j], 4);
+        l_[j] += __shfl_xor_sync(0xffffffffu, l_[j], 8);
+        l_[j] += __shfl_xor_sync(0xffffffffu, l_[j], 16);
+        if (lane < 4) {
+          s_m[cwarp * 16 + 2 * cq + j] = m_[j];
+          s_l[cwarp * 16 + 2 * cq + j] = l_[j];
+        }
+      }
+    } else {
+#pragma unroll
+      for (int rr = 0; rr < 2; ++rr) {
+        l_[rr] += __shfl_xor_sync(0xffffffffu, l_[rr], 1);
+        l_[rr] += __shfl_xor_sync(0xffffffffu, l_[rr], 2);
+        if (cq == 0) {
+          s_m[cwarp * 16 + r0 + 8 * rr] = m_[rr];
+          s_l[cwarp * 16 + r0 + 8 * rr] = l_[rr];
+        }
       }
     }
     named_barrier(1, kConsumerThreads);
