@@ -485,8 +485,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
                   const __grid_constant__ CUtensorMap tm_v,
                   const __grid_constant__ CUtensorMap tm_rel, const DecodeParams p) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem = smem_align1024(smem_raw);
   const int g = p.g;
   const int ns = p.nstages;
   const Tok<MULTI> tok(p);
@@ -1010,12 +1009,21 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       }
     }
     if (ctid < nrows) {
-      float M = s_m[ctid];
-      for (int w = 1; w < kConsumerWarps; ++w) M = fmaxf(M, s_m[w * 16 + ctid]);
+      // every warp's (m, l) of this row, loaded together, then combined
+      float mw[kConsumerWarps], lw[kConsumerWarps];
+#pragma unroll
+      for (int w = 0; w < kConsumerWarps; ++w) {
+        mw[w] = s_m[w * 16 + ctid];
+        lw[w] = s_l[w * 16 + ctid];
+      }
+      float M = mw[0];
+#pragma unroll
+      for (int w = 1; w < kConsumerWarps; ++w) M = fmaxf(M, mw[w]);
       float Ls = 0.f;
-      if (M != kNegInf)
-        for (int w = 0; w < kConsumerWarps; ++w)
-          Ls += s_l[w * 16 + ctid] * ex2(s_m[w * 16 + ctid] - M);
+      if (M != kNegInf) {
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) Ls += lw[w] * ex2(mw[w] - M);
+      }
       s_M[ctid] = M;
       s_L[ctid] = Ls;
     }
@@ -1101,8 +1109,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
 // Replays the producer's walk and split without touching K/V.
 __global__ void __launch_bounds__(128) decode_walk_kernel(const DecodeParams p) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem = smem_align1024(smem_raw);
   const DecodeSmem L(0, p.B, p.Bv, 1, 1, 64, 4);
   const int* s_len = reinterpret_cast<const int*>(smem + L.seqlen);
   const int* s_nt = reinterpret_cast<const int*>(smem + L.nt);

@@ -258,8 +258,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                    const __grid_constant__ CUtensorMap tm_v,
                    const __grid_constant__ CUtensorMap tm_rel, const PrefillParams p) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem = smem_align1024(smem_raw);
   const int nrs = p.ring_stages;
   const PrefillSmem L(p.B, DV, nrs);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
