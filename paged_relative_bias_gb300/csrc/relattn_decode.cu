@@ -79,7 +79,7 @@ __host__ __device__ constexpr int rel_token_bytes(int g, int es) {
 // own; per-sequence lengths take B entries, tile counts and prefixes Bv.
 struct DecodeSmem {
   int qbuf, stages, stage_bytes, rel, rel_bytes, slices, bars, valid, seqlen, nt, pref, m, l,
-      M, L, misc, total;
+      misc, total;
   __host__ __device__ DecodeSmem(int nstages, int B, int Bv, int kpc, int g, int dv, int rel_es) {
     stage_bytes = 16384 + kTileKeys * dv * 2;
     rel_bytes = kpc * rel_token_bytes(g, rel_es);
@@ -94,9 +94,7 @@ struct DecodeSmem {
     pref = nt + Bv * 4;
     m = (pref + (Bv + 1) * 4 + 15) & ~15;
     l = m + kConsumerWarps * 16 * 4;
-    M = l + kConsumerWarps * 16 * 4;
-    L = M + 16 * 4;
-    misc = L + 16 * 4;
+    misc = l + kConsumerWarps * 16 * 4;
     total = misc + 64;
   }
 };
@@ -699,8 +697,6 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   const int r0 = lane >> 2, cq = lane & 3;
   float* s_m = reinterpret_cast<float*>(smem + L.m);
   float* s_l = reinterpret_cast<float*>(smem + L.l);
-  float* s_M = reinterpret_cast<float*>(smem + L.M);
-  float* s_L = reinterpret_cast<float*>(smem + L.L);
   float* slices = reinterpret_cast<float*>(smem + L.slices);
   int n_base = 0;
   int k = 0;
@@ -973,23 +969,20 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         }
       }
     }
-    named_barrier(1, kConsumerThreads);
-    if (s_misc[kMiscAbort]) break;
+    // Each warp leaves its unscaled O rows in its slice; after one barrier
+    // the threads that write out weigh the eight slices of their row by
+    // exp2(m_w - M) themselves, so no second round of scaling is needed.
     const int srows = tok.kpc * g;  // rows of a warp's merge slice
     if constexpr (NB == 1) {
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         const int row = 2 * cq + e;  // this thread's O^T column
         if (row >= nrows) continue;
-        float M = s_m[row];
-#pragma unroll
-        for (int w = 1; w < kConsumerWarps; ++w) M = fmaxf(M, s_m[w * 16 + row]);
-        const float fct = M == kNegInf ? 0.f : ex2(s_m[cwarp * 16 + row] - M);
         float* sl = slices + (cwarp * srows + row) * (DV + SP) + (lane >> 2);
 #pragma unroll
         for (int db = 0; db < DB; ++db) {
-          sl[16 * db] = o[db][e] * fct;
-          sl[16 * db + 8] = o[db][2 + e] * fct;
+          sl[16 * db] = o[db][e];
+          sl[16 * db + 8] = o[db][2 + e];
         }
       }
     } else {
@@ -997,37 +990,14 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       for (int rr = 0; rr < 2; ++rr) {
         const int row = r0 + 8 * rr;
         if (!rv[rr]) continue;
-        float M = s_m[row];
-#pragma unroll
-        for (int w = 1; w < kConsumerWarps; ++w) M = fmaxf(M, s_m[w * 16 + row]);
-        const float fct = M == kNegInf ? 0.f : ex2(m_[rr] - M);
         float* sl = slices + (cwarp * srows + row) * (DV + SP) + cq * 2;
 #pragma unroll
         for (int nd = 0; nd < DV / 8; ++nd)
-          *reinterpret_cast<float2*>(sl + nd * 8) =
-              make_float2(o[nd][2 * rr] * fct, o[nd][2 * rr + 1] * fct);
+          *reinterpret_cast<float2*>(sl + nd * 8) = make_float2(o[nd][2 * rr], o[nd][2 * rr + 1]);
       }
-    }
-    if (ctid < nrows) {
-      // every warp's (m, l) of this row, loaded together, then combined
-      float mw[kConsumerWarps], lw[kConsumerWarps];
-#pragma unroll
-      for (int w = 0; w < kConsumerWarps; ++w) {
-        mw[w] = s_m[w * 16 + ctid];
-        lw[w] = s_l[w * 16 + ctid];
-      }
-      float M = mw[0];
-#pragma unroll
-      for (int w = 1; w < kConsumerWarps; ++w) M = fmaxf(M, mw[w]);
-      float Ls = 0.f;
-      if (M != kNegInf) {
-#pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) Ls += lw[w] * ex2(mw[w] - M);
-      }
-      s_M[ctid] = M;
-      s_L[ctid] = Ls;
     }
     named_barrier(1, kConsumerThreads);
+    if (s_misc[kMiscAbort]) break;
 
     const bool whole = pc.i0 == 0 && pc.n == s_nt[pc.b];
     const int slot = 2 * c + (a0 < pc.seg_start ? 1 : 0);
@@ -1039,15 +1009,28 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     };
     for (int idx = ctid; idx < nrows * DV / 2; idx += kConsumerThreads) {
       const int row = idx / (DV / 2), col = 2 * (idx % (DV / 2));
-      float v0 = 0.f, v1 = 0.f;
+      // the row's (m, l) of every warp, loaded together, then combined
+      float mw[kConsumerWarps], lw[kConsumerWarps];
+      float2 vw[kConsumerWarps];
 #pragma unroll
       for (int w = 0; w < kConsumerWarps; ++w) {
-        const float2 v =
-            *reinterpret_cast<const float2*>(slices + (w * srows + row) * (DV + SP) + col);
-        v0 += v.x;
-        v1 += v.y;
+        mw[w] = s_m[w * 16 + row];
+        lw[w] = s_l[w * 16 + row];
+        vw[w] = *reinterpret_cast<const float2*>(slices + (w * srows + row) * (DV + SP) + col);
       }
-      const float Ls = s_L[row];
+      float M = mw[0];
+#pragma unroll
+      for (int w = 1; w < kConsumerWarps; ++w) M = fmaxf(M, mw[w]);
+      float Ls = 0.f, v0 = 0.f, v1 = 0.f;
+      if (M != kNegInf) {
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) {
+          const float wt = ex2(mw[w] - M);
+          Ls += lw[w] * wt;
+          v0 += vw[w].x * wt;
+          v1 += vw[w].y * wt;
+        }
+      }
       const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
       if (whole) {
         if (p.out_f32)
@@ -1061,7 +1044,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
             p.part_o + (static_cast<size_t>(slot) * kMaxDecodeRows + row) * DV + col) =
             make_float2(v0 * inv, v1 * inv);
         if (col == 0)
-          p.part_lse[slot * kMaxDecodeRows + row] = Ls > 0.f ? s_M[row] + lg2(Ls) : kNegInf;
+          p.part_lse[slot * kMaxDecodeRows + row] = Ls > 0.f ? M + lg2(Ls) : kNegInf;
       }
     }
     if (!whole) {
