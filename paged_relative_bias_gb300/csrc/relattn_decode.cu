@@ -291,9 +291,10 @@ struct CtaRange {
 // arithmetic as range_cut.  len0: seq_lens[lane], already loaded.
 //
 // The plan is known from two warp reductions (tile total, longest segment)
-// before the prefix scan; when it gives CTA c segment c, early(b, kvh, len)
-// runs right then, with the segment's chunk, KV head and sequence length, so
-// that the copies it starts overlap the rest of the planning.
+// before the prefix scan; when it gives CTA c segment c, early(b, kvh, len,
+// ids) runs right then, with the segment's chunk, KV head, sequence length
+// and first block ids, so that the copies it starts overlap the rest of the
+// planning.
 template <bool MULTI, typename Early>
 __device__ CtaRange decode_plan_warp(const DecodeParams& p, uint8_t* smem, const DecodeSmem& L,
                                      int len0, Early&& early) {
@@ -310,13 +311,28 @@ __device__ CtaRange decode_plan_warp(const DecodeParams& p, uint8_t* smem, const
                        : len0;                                                 // sequence
   const int nt = has ? decode_vseq<MULTI>(lane, len, p).ntiles : 0;
   if (has && nt == 0 && blockIdx.x == 0) report(p.status, RELATTN_DEV_BAD_LENGTH);
+  // Speculatively, the block ids of segment c's first 32 tiles (lane j:
+  // block j from the first), loaded while the plan is reduced: they are the
+  // ones needed when the plan gives CTA c segment c.  Indices stay inside the
+  // chunk's block-table row.  (With more segments than CTAs the plan never
+  // gives one per CTA.)
+  const int lenc = __shfl_sync(0xffffffffu, len, cb < p.Bv ? cb : 0);
+  int ids = 0;
+  if (cb < p.Bv && p.Bv * p.Hkv <= static_cast<int>(gridDim.x)) {
+    const VSeq sc = decode_vseq<MULTI>(cb, lenc, p);
+    if (sc.ntiles > 0) {
+      const int blk0 = sc.tile_first >> 1;
+      const int nb = ((sc.tile_first + min(32, sc.ntiles) - 1) >> 1) - blk0 + 1;
+      if (lane < nb) ids = __ldg(p.block_table + static_cast<size_t>(sc.b) * p.max_blocks + blk0 + lane);
+    }
+  }
   const int mx = __reduce_max_sync(0xffffffffu, nt);
   const int total = static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<unsigned>(nt)));
   CtaRange cr;
   cr.pl = make_plan(p.Hkv * total, mx, p.Bv * p.Hkv);
   const Plan& pl = cr.pl;
   const bool mine = pl.per_cta && c < pl.G;
-  if (mine) early(cb, c - cb * p.Hkv, __shfl_sync(0xffffffffu, len, cb));
+  if (mine) early(cb, c - cb * p.Hkv, lenc, ids);
   int incl = nt;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -596,7 +612,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   int early_id = 0;      // warp 0, lane j: block j of the piece's first 32 tiles
   int early_n = 0;       // tiles of that first batch
   int early_bad = 0;     // a wait in it timed out
-  auto early = [&](int vb, int kvh, int len) {
+  auto early = [&](int vb, int kvh, int len, int ids) {
     const VSeq sq = decode_vseq<MULTI>(vb, len, p);
     if (sq.ntiles == 0) return;
     int ok = 1;
@@ -605,9 +621,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     if (!early_q) return;
     const int cn = min(32, sq.ntiles);
     const int blk0 = sq.tile_first >> 1;
-    const int nb = ((sq.tile_first + cn - 1) >> 1) - blk0 + 1;
-    const int* trow = p.block_table + static_cast<size_t>(sq.b) * p.max_blocks;
-    early_id = lane < nb ? __ldg(trow + blk0 + lane) : 0;
+    early_id = ids;
     const int bn = min(ns, cn);
     const int tile = sq.tile_first + (lane < bn ? lane : 0);
     const int id = __shfl_sync(0xffffffffu, early_id, (tile >> 1) - blk0);
@@ -1101,7 +1115,7 @@ __global__ void __launch_bounds__(128) decode_walk_kernel(const DecodeParams p) 
   CtaRange cr;
   if (p.Bv <= 32) {  // the decode kernel's fast prologue, run the same way
     if (threadIdx.x >= 32) return;
-    cr = decode_plan_warp<false>(p, smem, L, len0, [](int, int, int) {});
+    cr = decode_plan_warp<false>(p, smem, L, len0, [](int, int, int, int) {});
   } else {
     cr.pl = decode_prologue<false>(p, smem, L, false, len0);
     cr.a0 = range_cut(blockIdx.x, cr.pl, s_pref, s_nt, p.Bv, p.Hkv);
