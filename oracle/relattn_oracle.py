@@ -45,6 +45,14 @@ there is no blocking, fusion or reordering):
   to 9 tokens per step; reading: ``seq_lens`` counts all k tokens).
 * Softmax scale ``1/sqrt(d_qk)`` also when ``d_v != d_qk`` ("Inkling on Two
   DGX Sparks", section "Wall 1": head_dim 128, v_head_dim 64).
+* Gated output with a sink (optional; "Inkling 2 Small on vLLM",
+  architecture table row for the attention output, and the section on the
+  backbone's recent additions: a sigmoid gate on each head's output together
+  with a per-token attention sink).  Reading (the pages give no formula): the
+  sink is one more logit per (query token, head) that joins the softmax's
+  normaliser and carries no value; the gate is a logit per (query token,
+  head) whose sigmoid multiplies that head's output.  Both are inputs; the
+  projections that produce them are outside attention.
 
 Data conventions: bf16 tensors are passed as ``np.uint16`` arrays of bf16 bit
 patterns (converted exactly here); float arrays are used as float64.
@@ -210,9 +218,23 @@ def softmax_weights(s) -> np.ndarray:
     return w / w.sum()
 
 
-def attend(q_vec, K, V, bias, d_qk: int) -> np.ndarray:
-    """Output of one query: softmax(logits) @ V."""
-    return softmax_weights(logits(q_vec, K, bias, d_qk)) @ V
+def attend(q_vec, K, V, bias, d_qk: int, sink=None, gate=None) -> np.ndarray:
+    """Output of one query: softmax(logits) @ V.
+
+    With a sink logit s the weights are exp(l_j) / (sum_j exp(l_j) + exp(s));
+    with a gate logit g the output is multiplied by 1 / (1 + exp(-g)).
+    """
+    s = logits(q_vec, K, bias, d_qk)
+    if sink is None:
+        w = softmax_weights(s)
+    else:
+        m = max(s.max(), float(sink))
+        e = np.exp(s - m)
+        w = e / (e.sum() + math.exp(float(sink) - m))
+    out = w @ V
+    if gate is not None:
+        out = out / (1.0 + math.exp(-float(gate)))
+    return out
 
 
 def attend_partial(q_vec, K, V, bias, d_qk: int):
@@ -241,11 +263,12 @@ def merge_partials(outs, lses) -> np.ndarray:
 # --------------------------------------------------------------------------
 
 def decode(q, rel, k_cache, v_cache, block_table, seq_lens, window: int,
-           rel_extent: int, batch=None, heads=None) -> np.ndarray:
+           rel_extent: int, batch=None, heads=None, sink=None, gate=None) -> np.ndarray:
     """Paged decode: one query per sequence at position seq_lens[b] - 1.
 
-    Returns float64 [B, Hq, d_v]; rows/heads not selected by ``batch`` /
-    ``heads`` are left NaN.
+    ``sink`` / ``gate``: optional [B, Hq] logits (see ``attend``).  Returns
+    float64 [B, Hq, d_v]; rows/heads not selected by ``batch`` / ``heads``
+    are left NaN.
     """
     B, Hq, d_qk = q.shape
     Hkv = k_cache.shape[2]
@@ -265,12 +288,15 @@ def decode(q, rel, k_cache, v_cache, block_table, seq_lens, window: int,
             K, V = gather_kv(k_cache, v_cache, block_table[b], keys, kvh)
             for h in hs:
                 bias = rel_bias(rel[b, h], P, keys, rel_extent)
-                out[b, h] = attend(q[b, h], K, V, bias, d_qk)
+                out[b, h] = attend(q[b, h], K, V, bias, d_qk,
+                                   None if sink is None else sink[b, h],
+                                   None if gate is None else gate[b, h])
     return out
 
 
 def decode_multi(q, rel, k_cache, v_cache, block_table, seq_lens, window: int,
-                 rel_extent: int, batch=None, tokens=None, heads=None) -> np.ndarray:
+                 rel_extent: int, batch=None, tokens=None, heads=None, sink=None,
+                 gate=None) -> np.ndarray:
     """Multi-token decode, the verification step of speculative decoding.
 
     The k newest tokens of sequence b each attend over the paged cache:
@@ -284,9 +310,9 @@ def decode_multi(q, rel, k_cache, v_cache, block_table, seq_lens, window: int,
     Reading (pages silent): ``seq_lens`` counts all k tokens, as it counts
     the one token of a decode step.
 
-    q ``[B, k, Hq, d_qk]``, rel ``[B, k, Hq, E]``.  Returns float64
-    ``[B, k, Hq, d_v]``; entries not selected by ``batch`` / ``tokens`` /
-    ``heads`` are left NaN.
+    q ``[B, k, Hq, d_qk]``, rel ``[B, k, Hq, E]``, optional ``sink`` /
+    ``gate`` ``[B, k, Hq]``.  Returns float64 ``[B, k, Hq, d_v]``; entries not
+    selected by ``batch`` / ``tokens`` / ``heads`` are left NaN.
     """
     B, kq, Hq, d_qk = q.shape
     Hkv = k_cache.shape[2]
@@ -307,19 +333,22 @@ def decode_multi(q, rel, k_cache, v_cache, block_table, seq_lens, window: int,
                 K, V = gather_kv(k_cache, v_cache, block_table[b], keys, kvh)
                 for h in hs:
                     bias = rel_bias(rel[b, i, h], P, keys, rel_extent)
-                    out[b, i, h] = attend(q[b, i, h], K, V, bias, d_qk)
+                    out[b, i, h] = attend(q[b, i, h], K, V, bias, d_qk,
+                                          None if sink is None else sink[b, i, h],
+                                          None if gate is None else gate[b, i, h])
     return out
 
 
 def prefill(q, k, v, rel, cu_seqlens, k_cache, v_cache, block_table,
-            ctx_lens, window: int, rel_extent: int, rows=None):
+            ctx_lens, window: int, rel_extent: int, rows=None, sink=None, gate=None):
     """Chunked prefill against the paged cache.
 
     Writes the new keys/values into copies of the caches, then attends each
     new token (position ctx_lens[b] + t) over the cached prefix plus the new
     tokens, causal and windowed.  ``rows`` selects packed token rows to
-    compute (default: all).  Returns (out float64 [T, Hq, d_v] with unselected
-    rows NaN, k_cache', v_cache').
+    compute (default: all); ``sink`` / ``gate``: optional [T, Hq] logits (see
+    ``attend``).  Returns (out float64 [T, Hq, d_v] with unselected rows NaN,
+    k_cache', v_cache').
     """
     T, Hq, d_qk = q.shape
     Hkv = k_cache.shape[2]
@@ -343,7 +372,9 @@ def prefill(q, k, v, rel, cu_seqlens, k_cache, v_cache, block_table,
                 K, V = gather_kv(kc, vc, block_table[b], keys, kvh)
                 for h in range(kvh * g, (kvh + 1) * g):
                     bias = rel_bias(rel[row, h], P, keys, rel_extent)
-                    out[row, h] = attend(q[row, h], K, V, bias, d_qk)
+                    out[row, h] = attend(q[row, h], K, V, bias, d_qk,
+                                         None if sink is None else sink[row, h],
+                                         None if gate is None else gate[row, h])
     return out, kc, vc
 
 

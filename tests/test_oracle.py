@@ -510,3 +510,92 @@ def test_decode_multi_equals_prefill_of_the_same_tokens():
                                 c["table"], [L - k], W, E)
         assert np.array_equal(kc2, c["kc"])  # the same keys written back
         np.testing.assert_allclose(multi[0], pre, atol=1e-13, rtol=0)
+
+
+# ---------------------------------------------------------------------------
+# gated output with a sink
+# ---------------------------------------------------------------------------
+
+def test_sink_minus_inf_and_gate_plus_inf_are_the_plain_output():
+    c = random_decode_case(81, 300)
+    plain = O.decode(c["q"], c["rel"], c["kc"], c["vc"], c["table"], c["seq_lens"], 100, 64)
+    Hq = c["q"].shape[1]
+    sg = O.decode(c["q"], c["rel"], c["kc"], c["vc"], c["table"], c["seq_lens"], 100, 64,
+                  sink=np.full((1, Hq), -np.inf), gate=np.full((1, Hq), np.inf))
+    assert np.array_equal(sg, plain)
+
+
+@pytest.mark.parametrize("n,s,gt", [(1, 0.0, 0.0), (7, 1.5, -0.7), (300, -2.0, 3.0)])
+def test_sink_and_gate_closed_form(n, s, gt):
+    """q = 0 and rel = 0 make all n visible logits 0: each weight is
+    1 / (n + e^s), so out = (sum of the values) / (n + e^s) * sigmoid(g)."""
+    c = random_decode_case(82 + n, n)
+    q0 = np.zeros_like(c["q"])
+    rel0 = np.zeros_like(c["rel"])
+    Hq = q0.shape[1]
+    out = O.decode(q0, rel0, c["kc"], c["vc"], c["table"], c["seq_lens"], 0, 64,
+                   sink=np.full((1, Hq), s), gate=np.full((1, Hq), gt))
+    g = Hq // c["Kc"].shape[1]
+    for h in range(Hq):
+        want = c["Vc"][:, h // g].sum(0) / (n + math.exp(s)) / (1 + math.exp(-gt))
+        np.testing.assert_allclose(out[0, h], want, rtol=1e-12, atol=1e-14)
+
+
+def test_sink_is_an_extra_key_with_a_zero_value():
+    """The sink joins the normaliser like one more key whose logit is s and
+    whose value is 0: float64 SDPA over the keys plus such a key."""
+    L, W, E = 260, 100, 64
+    c = random_decode_case(85, L, E=E, dv=6)
+    Hq = c["q"].shape[1]
+    s = np.linspace(-1.0, 2.0, Hq)[None, :]
+    out = O.decode(c["q"], c["rel"], c["kc"], c["vc"], c["table"], c["seq_lens"], W, E,
+                   sink=s)
+    # extended keys: the visible ones plus a zero key (q.k = 0) at the end
+    P = L - 1
+    lo, _ = O.visible_keys(P, W)
+    keys = np.arange(lo, P + 1)
+    d = c["Kc"].shape[2]
+    g = Hq // c["Kc"].shape[1]
+    for h in range(Hq):
+        K = np.concatenate([c["Kc"][keys, h // g], np.zeros((1, d))])
+        V = np.concatenate([c["Vc"][keys, h // g], np.zeros((1, c["Vc"].shape[2]))])
+        bias = np.array([c["rel"][0, h, P - j] if P - j < E else 0.0 for j in keys] +
+                        [s[0, h]])
+        qt = torch.from_numpy(c["q"][0, h][None, None, :])
+        o = torch.nn.functional.scaled_dot_product_attention(
+            qt, torch.from_numpy(K)[None], torch.from_numpy(V)[None],
+            attn_mask=torch.from_numpy(bias)[None, None, :])
+        np.testing.assert_allclose(out[0, h], o[0, 0].numpy(), atol=1e-12, rtol=0)
+
+
+def test_gates_g_and_minus_g_sum_to_the_ungated_output():
+    """sigmoid(g) + sigmoid(-g) = 1, for every row of a prefill."""
+    wl_c = random_decode_case(86, 200)
+    T, Hq = 40, 4
+    r = rng(87)
+    q = r.standard_normal((T, Hq, 16))
+    k = r.standard_normal((T, 2, 16))
+    v = r.standard_normal((T, 2, 8))
+    rel = r.standard_normal((T, Hq, 64))
+    gate = r.standard_normal((T, Hq)) * 3
+    sink = r.standard_normal((T, Hq))
+    args = (q, k, v, rel, [0, T], wl_c["kc"], wl_c["vc"], wl_c["table"], [150], 100, 64)
+    a, _, _ = O.prefill(*args, sink=sink, gate=gate)
+    b, _, _ = O.prefill(*args, sink=sink, gate=-gate)
+    c, _, _ = O.prefill(*args, sink=sink)
+    np.testing.assert_allclose(a + b, c, atol=1e-12, rtol=0)
+
+
+def test_decode_multi_sink_gate_rows_equal_decode_at_their_lengths():
+    L, k = 260, 3
+    c = random_multi_case(88, L, k)
+    Hq = c["qm"].shape[2]
+    r = rng(89)
+    sink = r.standard_normal((1, k, Hq))
+    gate = r.standard_normal((1, k, Hq))
+    multi = O.decode_multi(c["qm"], c["relm"], c["kc"], c["vc"], c["table"], c["seq_lens"],
+                           64, 64, sink=sink, gate=gate)
+    for i in range(k):
+        dec = O.decode(c["qm"][:, i], c["relm"][:, i], c["kc"], c["vc"], c["table"],
+                       np.array([L - k + i + 1]), 64, 64, sink=sink[:, i], gate=gate[:, i])
+        np.testing.assert_allclose(multi[:, i], dec, atol=1e-13, rtol=0)
