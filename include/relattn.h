@@ -175,8 +175,9 @@ int relattn_decode_multi(const void* q, const float* rel,
                          void* stream);
 
 /*
- * Element types of rel and out for the *_ex entry points.  The plain entry
- * points take fp32 rel and write bf16 out.
+ * Options of the *_ex entry points: the element types of rel and out, and an
+ * optional gated output with a sink.  The plain entry points are the
+ * defaults: fp32 rel, bf16 out, no sink, no gate.
  *
  *  - bf16 rel halves the bytes of the relative-logit input, which is most of
  *    a chunked prefill's traffic (fp32 [T][Hq][E]); rel is the product
@@ -191,20 +192,34 @@ int relattn_decode_multi(const void* q, const float* rel,
 #define RELATTN_DTYPE_F32 0
 #define RELATTN_DTYPE_BF16 1
 
-typedef struct relattn_io_types {
-  int32_t rel; /* RELATTN_DTYPE_F32 or RELATTN_DTYPE_BF16 */
-  int32_t out; /* RELATTN_DTYPE_BF16 or RELATTN_DTYPE_F32 */
-} relattn_io_types;
+/*
+ *  - sink / gate: the gated attention output of Inkling 2 ("Inkling 2 Small
+ *    on vLLM", architecture table row for the attention output: a sigmoid
+ *    gate on each head's output with a per-token attention sink).  Reading
+ *    (no formula on the pages): sink[row][h] is one more logit in the
+ *    softmax's normaliser, with no value, so the weights become
+ *    exp(l_j) / (sum_j exp(l_j) + exp(sink)); gate[row][h] multiplies the
+ *    head's output by 1 / (1 + exp(-gate)).  Both are fp32 device arrays of
+ *    one value per query row and query head ([B][k][Hq] for decode, [T][Hq]
+ *    for prefill), or NULL for none; the library reads them and owns
+ *    neither.
+ */
+typedef struct relattn_options {
+  int32_t rel;       /* RELATTN_DTYPE_F32 or RELATTN_DTYPE_BF16 */
+  int32_t out;       /* RELATTN_DTYPE_BF16 or RELATTN_DTYPE_F32 */
+  const float* sink; /* NULL, or [rows][Hq] fp32 sink logits */
+  const float* gate; /* NULL, or [rows][Hq] fp32 gate logits */
+} relattn_options;
 
 /*
- * relattn_decode_multi with the element types of rel and out given by
- * `types` (k = 1 is relattn_decode).  rel is [B][k][Hq][rel_extent] of
- * types->rel; out is [B][k][Hq][d_v] of types->out.  A bf16 rel needs
+ * relattn_decode_multi with `options` (k = 1 is relattn_decode).  rel is
+ * [B][k][Hq][rel_extent] of options->rel; out is [B][k][Hq][d_v] of
+ * options->out; sink and gate, when given, are [B][k][Hq].  A bf16 rel needs
  * rel_extent a multiple of 8 (fp32: of 4): RELATTN_ERR_UNSUPPORTED
  * otherwise; an unknown type code is RELATTN_ERR_INVALID_ARG.  Same
  * workspace, errors and device status as relattn_decode.
  */
-int relattn_decode_ex(const void* q, const void* rel, const relattn_io_types* types,
+int relattn_decode_ex(const void* q, const void* rel, const relattn_options* options,
                       const relattn_kv_cache* kv_cache, const int32_t* block_table,
                       const int32_t* seq_lens, int32_t num_query_tokens, int32_t window,
                       int32_t rel_extent, const relattn_dims* dims, void* out,
@@ -278,14 +293,14 @@ int relattn_prefill(const void* q, const void* k, const void* v,
                     void* workspace, size_t workspace_bytes, void* stream);
 
 /*
- * relattn_prefill with the element types of rel and out given by `types`:
- * rel [T][Hq][rel_extent] of types->rel, out [T][Hq][d_v] of types->out.  A
+ * relattn_prefill with `options`: rel [T][Hq][rel_extent] of options->rel,
+ * out [T][Hq][d_v] of options->out, sink and gate (when given) [T][Hq].  A
  * bf16 rel needs rel_extent a multiple of 8 (fp32: of 4):
  * RELATTN_ERR_UNSUPPORTED otherwise; an unknown type code is
  * RELATTN_ERR_INVALID_ARG.  Everything else as relattn_prefill.
  */
 int relattn_prefill_ex(const void* q, const void* k, const void* v, const void* rel,
-                       const relattn_io_types* types, const int32_t* cu_seqlens,
+                       const relattn_options* options, const int32_t* cu_seqlens,
                        const relattn_kv_cache* kv_cache, const int32_t* block_table,
                        const int32_t* ctx_lens, int32_t window, int32_t rel_extent,
                        const relattn_dims* dims, void* out, void* workspace,

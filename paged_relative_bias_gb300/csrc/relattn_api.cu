@@ -199,20 +199,27 @@ int relattn_read_status(const void* workspace, uint32_t* status, void* stream) {
 }
 
 // kq: query tokens per sequence (1 for relattn_decode).
-// Element types of rel and out, as the kernels see them.
+// The call options as the kernels see them.
 struct IoTypes {
-  int rel_es;   // bytes per rel element: 4 (fp32) or 2 (bf16)
-  int out_f32;  // 1: out is fp32, 0: bf16
+  int rel_es;         // bytes per rel element: 4 (fp32) or 2 (bf16)
+  int out_f32;        // 1: out is fp32, 0: bf16
+  const float* sink;  // per (query row, head) sink logits, or null
+  const float* gate;  // per (query row, head) gate logits, or null
 };
-constexpr IoTypes kDefaultIo = {4, 0};
+constexpr IoTypes kDefaultIo = {4, 0, nullptr, nullptr};
 
-// From the C ABI's description; false for a combination that is not offered.
-static bool io_types(const relattn_io_types* t, IoTypes* io) {
+// From the C ABI's options; false for a value that is not offered (an
+// unknown type code, or a sink / gate pointer not 4-byte aligned).
+static bool io_types(const relattn_options* t, IoTypes* io) {
   if (!t) return false;
   if (t->rel != RELATTN_DTYPE_F32 && t->rel != RELATTN_DTYPE_BF16) return false;
   if (t->out != RELATTN_DTYPE_F32 && t->out != RELATTN_DTYPE_BF16) return false;
+  if ((reinterpret_cast<uintptr_t>(t->sink) & 3u) || (reinterpret_cast<uintptr_t>(t->gate) & 3u))
+    return false;
   io->rel_es = t->rel == RELATTN_DTYPE_BF16 ? 2 : 4;
   io->out_f32 = t->out == RELATTN_DTYPE_F32 ? 1 : 0;
+  io->sink = t->sink;
+  io->gate = t->gate;
   return true;
 }
 
@@ -262,6 +269,8 @@ static int prepare_decode(const void* q, const void* rel, IoTypes io,
   p.block_table = block_table;
   p.seq_lens = seq_lens;
   p.out = out;
+  p.sink = io.sink;
+  p.gate = io.gate;
   p.rel_es = io.rel_es;
   p.out_f32 = io.out_f32;
   p.status = reinterpret_cast<uint32_t*>(ws);
@@ -350,13 +359,13 @@ int relattn_decode_multi(const void* q, const float* rel, const relattn_kv_cache
   return to_status(launch_decode(L, static_cast<cudaStream_t>(stream)));
 }
 
-int relattn_decode_ex(const void* q, const void* rel, const relattn_io_types* types,
+int relattn_decode_ex(const void* q, const void* rel, const relattn_options* options,
                       const relattn_kv_cache* kv_cache, const int32_t* block_table,
                       const int32_t* seq_lens, int32_t num_query_tokens, int32_t window,
                       int32_t rel_extent, const relattn_dims* dims, void* out, void* workspace,
                       size_t workspace_bytes, void* stream) {
   IoTypes io;
-  if (!io_types(types, &io)) return RELATTN_ERR_INVALID_ARG;
+  if (!io_types(options, &io)) return RELATTN_ERR_INVALID_ARG;
   DecodeLaunch L;
   DeviceInfo di;
   const int rc = prepare_decode(q, rel, io, kv_cache, block_table, seq_lens, num_query_tokens,
@@ -466,6 +475,8 @@ static int prepare_prefill(const void* q, const void* k, const void* v, const vo
   p.k_cache = static_cast<__nv_bfloat16*>(cache->k);
   p.v_cache = static_cast<__nv_bfloat16*>(cache->v);
   p.out = out;
+  p.sink = io.sink;
+  p.gate = io.gate;
   p.rel_es = io.rel_es;
   p.out_f32 = io.out_f32;
   p.status = static_cast<uint32_t*>(workspace);
@@ -541,13 +552,13 @@ int relattn_prefill(const void* q, const void* k, const void* v, const float* re
 }
 
 int relattn_prefill_ex(const void* q, const void* k, const void* v, const void* rel,
-                       const relattn_io_types* types, const int32_t* cu_seqlens,
+                       const relattn_options* options, const int32_t* cu_seqlens,
                        const relattn_kv_cache* cache, const int32_t* block_table,
                        const int32_t* ctx_lens, int32_t window, int32_t rel_extent,
                        const relattn_dims* dims, void* out, void* workspace,
                        size_t workspace_bytes, void* stream) {
   IoTypes io;
-  if (!io_types(types, &io)) return RELATTN_ERR_INVALID_ARG;
+  if (!io_types(options, &io)) return RELATTN_ERR_INVALID_ARG;
   return relattn_prefill_io(q, k, v, rel, io, cu_seqlens, cache, block_table, ctx_lens, window,
                             rel_extent, dims, out, workspace, workspace_bytes, stream);
 }

@@ -49,6 +49,17 @@ constexpr int kSlicePad = 8;         // floats of padding per merge-slice row, a
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kNegInf = -__builtin_huge_valf();
 
+// 1 / normaliser of query row qi, whose softmax so far has maximum M (base 2)
+// and sum Ls: the optional sink logit joins the normaliser, and the optional
+// gate's sigmoid scales the output.
+__device__ __forceinline__ float out_scale(const DecodeParams& p, size_t qi, float M, float Ls) {
+  float den = Ls;
+  if (p.sink) den += ex2(__ldg(p.sink + qi) * kLog2e - M);  // 0 for a sink of -inf
+  float s = den > 0.f ? 1.f / den : 0.f;                     // 0 when den overflows
+  if (p.gate) s /= 1.f + ex2(-__ldg(p.gate + qi) * kLog2e);
+  return s;
+}
+
 __device__ __forceinline__ float rel_f32(float x) { return x; }
 __device__ __forceinline__ float rel_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
 
@@ -1045,15 +1056,16 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
           v1 += vw[w].y * wt;
         }
       }
-      const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
       if (whole) {
+        const float inv = out_scale(p, orow(row) / DV, M, Ls);
         if (p.out_f32)
           *reinterpret_cast<float2*>(static_cast<float*>(p.out) + orow(row) + col) =
               make_float2(v0 * inv, v1 * inv);
         else
           *reinterpret_cast<__nv_bfloat162*>(static_cast<__nv_bfloat16*>(p.out) + orow(row) +
                                              col) = __floats2bfloat162_rn(v0 * inv, v1 * inv);
-      } else {
+      } else {  // a partial: normalised over its own keys, no sink or gate yet
+        const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
         *reinterpret_cast<float2*>(
             p.part_o + (static_cast<size_t>(slot) * kMaxDecodeRows + row) * DV + col) =
             make_float2(v0 * inv, v1 * inv);
@@ -1090,7 +1102,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
             den = den * sc + w;
             M = M2;
           }
-          const float r = den > 0.f ? num / den : 0.f;
+          const float r = num * out_scale(p, orow(row) / DV, M, den);
           if (p.out_f32)
             static_cast<float*>(p.out)[orow(row) + col] = r;
           else

@@ -23,6 +23,8 @@ struct DecodeParams {
   const int32_t* block_table;  // [B][max_blocks]
   const int32_t* seq_lens;     // [B]
   void* out;                   // [B][k][Hq][dv], bf16 or fp32 (out_f32)
+  const float* sink;           // [B][k][Hq] sink logits, or null
+  const float* gate;           // [B][k][Hq] gate logits, or null
   int rel_es;                  // bytes per rel element: 4 (fp32) or 2 (bf16)
   int out_f32;                 // 1: out is fp32
   uint32_t* status;            // workspace status word
@@ -58,6 +60,8 @@ struct PrefillParams {
   __nv_bfloat16* k_cache;      // [NB][128][Hkv][128]
   __nv_bfloat16* v_cache;      // [NB][128][Hkv][dv]
   void* out;                   // [T][Hq][dv], bf16 or fp32 (out_f32)
+  const float* sink;           // [T][Hq] sink logits, or null
+  const float* gate;           // [T][Hq] gate logits, or null
   int rel_es;                  // bytes per rel element: 4 (fp32) or 2 (bf16)
   int out_f32;                 // 1: out is fp32
   uint32_t* status;

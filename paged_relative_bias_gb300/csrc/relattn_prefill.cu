@@ -614,7 +614,17 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       // of a bf16 row.
       uint8_t* scr = slot_wait(e);
       if (!scr) { fail = true; break; }
-      const float inv = l > 0.f ? 1.f / l : 0.f;
+      // 1 / normaliser; the optional sink logit joins it (l and m_used are in
+      // natural-log units) and the optional gate's sigmoid scales the row
+      float inv;
+      {
+        float den = l;
+        const size_t qi = static_cast<size_t>(it.r0 + r) * p.Hq + it.h;
+        if (p.sink != nullptr && row_ok)
+          den += ex2((__ldg(p.sink + qi) - m_used) * kLog2e);  // 0 for a sink of -inf
+        inv = den > 0.f ? 1.f / den : 0.f;
+        if (p.gate != nullptr && row_ok) inv /= 1.f + ex2(-__ldg(p.gate + qi) * kLog2e);
+      }
       constexpr int kCpr = DV / 8;     // 16-byte chunks per scratch row
       constexpr int kRpi = 32 / kCpr;  // rows per store instruction
       constexpr int passes = O32 ? 2 : 1;

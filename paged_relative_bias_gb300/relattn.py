@@ -59,8 +59,8 @@ class Dims(ctypes.Structure):
                 ("max_q_len", c_int32), ("num_ctas", c_int32)]
 
 
-class IoTypes(ctypes.Structure):
-    _fields_ = [("rel", c_int32), ("out", c_int32)]
+class Options(ctypes.Structure):
+    _fields_ = [("rel", c_int32), ("out", c_int32), ("sink", c_void_p), ("gate", c_void_p)]
 
 
 class RelattnError(RuntimeError):
@@ -117,11 +117,11 @@ def lib() -> ctypes.CDLL:
                                        c_int32, c_int32, S, c_void_p, c_void_p, c_size_t,
                                        c_void_p]
     L.relattn_decode_multi.restype = c_int
-    L.relattn_decode_ex.argtypes = [c_void_p, c_void_p, POINTER(IoTypes), P, c_void_p,
+    L.relattn_decode_ex.argtypes = [c_void_p, c_void_p, POINTER(Options), P, c_void_p,
                                     c_void_p, c_int32, c_int32, c_int32, S, c_void_p, c_void_p,
                                     c_size_t, c_void_p]
     L.relattn_decode_ex.restype = c_int
-    L.relattn_prefill_ex.argtypes = [c_void_p, c_void_p, c_void_p, c_void_p, POINTER(IoTypes),
+    L.relattn_prefill_ex.argtypes = [c_void_p, c_void_p, c_void_p, c_void_p, POINTER(Options),
                                      c_void_p, P, c_void_p, c_void_p, c_int32, c_int32, S,
                                      c_void_p, c_void_p, c_size_t, c_void_p]
     L.relattn_prefill_ex.restype = c_int
@@ -198,30 +198,44 @@ def decode_dims(q, block_table, num_ctas=0) -> Dims:
     return Dims(q.shape[0], q.shape[1], block_table.shape[1], 0, 0, num_ctas)
 
 
-def _io_types(rel, out_dtype) -> IoTypes:
+def _options(rel, out_dtype, sink=None, gate=None, rows_shape=None, device=None) -> Options:
+    """The *_ex options; sink / gate are float32 [rows..., Hq] tensors or None."""
     if rel.dtype not in _DTYPE_CODE:
         raise TypeError(f"rel must be float32 or bfloat16, got {rel.dtype}")
     if out_dtype not in _DTYPE_CODE:
         raise TypeError(f"out must be bfloat16 or float32, got {out_dtype}")
-    return IoTypes(_DTYPE_CODE[rel.dtype], _DTYPE_CODE[out_dtype])
+    for name, t in (("sink", sink), ("gate", gate)):
+        if t is not None:
+            _need(t, name, torch.float32, len(rows_shape), device)
+            if tuple(t.shape) != tuple(rows_shape):
+                raise ValueError(f"{name} must be {list(rows_shape)}, got {tuple(t.shape)}")
+    return Options(_DTYPE_CODE[rel.dtype], _DTYPE_CODE[out_dtype], _ptr(sink), _ptr(gate))
+
+
+def _plain(rel, out_dtype, sink, gate) -> bool:
+    return (rel.dtype == torch.float32 and out_dtype == torch.bfloat16 and sink is None
+            and gate is None)
 
 
 def relattn_decode(q, rel, k_cache, v_cache, block_table, seq_lens, window: int,
                    rel_extent: int, out=None, workspace=None, num_ctas: int = 0,
-                   out_dtype=torch.bfloat16):
+                   out_dtype=torch.bfloat16, sink=None, gate=None):
     """Paged relative-bias decode; see ``relattn_decode`` in include/relattn.h.
 
     rel may be float32 or bfloat16 and out bfloat16 or float32 (``out``'s own
-    dtype when it is given); other than fp32 rel and bf16 out goes through
-    ``relattn_decode_ex``.
+    dtype when it is given); sink / gate are optional float32 [B, Hq] logits
+    (the gated output with a sink).  Anything but fp32 rel, bf16 out and no
+    sink or gate goes through ``relattn_decode_ex``.
     """
-    if rel.dtype != torch.float32 or (out.dtype if out is not None else out_dtype) != torch.bfloat16:
+    if not _plain(rel, out.dtype if out is not None else out_dtype, sink, gate):
         if q.dim() != 3 or rel.dim() != 3:
             raise ValueError("q must be [B, Hq, d_qk] and rel [B, Hq, rel_extent]")
         o = relattn_decode_multi(q[:, None], rel[:, None], k_cache, v_cache, block_table,
                                  seq_lens, window, rel_extent,
                                  out=None if out is None else out[:, None],
-                                 workspace=workspace, num_ctas=num_ctas, out_dtype=out_dtype)
+                                 workspace=workspace, num_ctas=num_ctas, out_dtype=out_dtype,
+                                 sink=None if sink is None else sink[:, None],
+                                 gate=None if gate is None else gate[:, None])
         return o[:, 0]
     dev = q.device
     B, Hq, dqk = q.shape
@@ -279,18 +293,19 @@ def relattn_decode_noalloc(q, rel, k_cache, v_cache, block_table, seq_lens, wind
 
 def relattn_decode_multi(q, rel, k_cache, v_cache, block_table, seq_lens, window: int,
                          rel_extent: int, out=None, workspace=None, num_ctas: int = 0,
-                         out_dtype=torch.bfloat16):
+                         out_dtype=torch.bfloat16, sink=None, gate=None):
     """Decode of k query tokens per sequence (speculative verification).
 
     q is [B, k, Hq, d_qk], rel [B, k, Hq, rel_extent], out [B, k, Hq, d_v];
     token i of sequence b sits at position seq_lens[b] - k + i.  rel may be
-    float32 or bfloat16, out bfloat16 or float32 (``relattn_decode_ex``).
+    float32 or bfloat16, out bfloat16 or float32, and sink / gate optional
+    float32 [B, k, Hq] logits (``relattn_decode_ex``).
     """
     dev = q.device
     _need(q, "q", torch.bfloat16, 4, dev)
     B, kq, Hq, _ = q.shape
     out_dtype = out.dtype if out is not None else out_dtype
-    io = _io_types(rel, out_dtype)
+    io = _options(rel, out_dtype, sink, gate, (B, kq, Hq), dev)
     _need(rel, "rel", rel.dtype, 4, dev)
     _need(k_cache, "k_cache", torch.bfloat16, 4, dev)
     _need(v_cache, "v_cache", torch.bfloat16, 4, dev)
@@ -308,7 +323,7 @@ def relattn_decode_multi(q, rel, k_cache, v_cache, block_table, seq_lens, window
         _need(out, "out", out_dtype, 4, dev)
     if workspace is None:
         workspace = new_workspace(workspace_size(dims, cache), dev)
-    if rel.dtype == torch.float32 and out_dtype == torch.bfloat16:
+    if _plain(rel, out_dtype, sink, gate):
         _check(lib().relattn_decode_multi(
             q.data_ptr(), rel.data_ptr(), ctypes.byref(cache), block_table.data_ptr(),
             seq_lens.data_ptr(), int(kq), int(window), int(rel_extent), ctypes.byref(dims),
@@ -330,17 +345,18 @@ def prefill_dims(q, block_table, ctx_lens, max_q_len: int, num_ctas=0) -> Dims:
 
 def relattn_prefill(q, k, v, rel, cu_seqlens, k_cache, v_cache, block_table, ctx_lens,
                     window: int, rel_extent: int, max_q_len: int, out=None,
-                    workspace=None, out_dtype=torch.bfloat16):
+                    workspace=None, out_dtype=torch.bfloat16, sink=None, gate=None):
     """Chunked prefill with a cached prefix; writes k, v into the cache.
 
     rel may be float32 or bfloat16, out bfloat16 or float32 (``out``'s own
-    dtype when it is given); other than fp32 rel and bf16 out goes through
+    dtype when it is given), sink / gate optional float32 [T, Hq] logits;
+    anything but fp32 rel, bf16 out and no sink or gate goes through
     ``relattn_prefill_ex``.
     """
     dev = q.device
     T, Hq, dqk = q.shape
     out_dtype = out.dtype if out is not None else out_dtype
-    io = _io_types(rel, out_dtype)
+    io = _options(rel, out_dtype, sink, gate, (T, Hq), dev)
     _need(q, "q", torch.bfloat16, 3, dev)
     _need(k, "k", torch.bfloat16, 3, dev)
     _need(v, "v", torch.bfloat16, 3, dev)
@@ -365,7 +381,7 @@ def relattn_prefill(q, k, v, rel, cu_seqlens, k_cache, v_cache, block_table, ctx
         _need(out, "out", out_dtype, 3, dev)
     if workspace is None:
         workspace = new_workspace(workspace_size(dims, cache), dev)
-    if rel.dtype == torch.float32 and out_dtype == torch.bfloat16:
+    if _plain(rel, out_dtype, sink, gate):
         _check(lib().relattn_prefill(
             q.data_ptr(), k.data_ptr(), v.data_ptr(), rel.data_ptr(), cu_seqlens.data_ptr(),
             ctypes.byref(cache), block_table.data_ptr(), ctx_lens.data_ptr(), int(window),

@@ -45,11 +45,17 @@ def host_decode_inputs(case):
         seq_lens=case["seq_lens"].cpu().numpy())
 
 
+def host_opt(case, name):
+    """An optional per-(query row, head) input of a case, as numpy or None."""
+    t = case.get(name)
+    return None if t is None else t.cpu().double().numpy()
+
+
 def oracle_decode(case, batch=None, heads=None):
     h = host_decode_inputs(case)
     return O.decode(h["q"], h["rel"], h["k_cache"], h["v_cache"], h["block_table"],
                     h["seq_lens"], case["window"], case["rel_extent"], batch=batch,
-                    heads=heads)
+                    heads=heads, sink=host_opt(case, "sink"), gate=host_opt(case, "gate"))
 
 
 class RowRel:
@@ -95,11 +101,12 @@ def oracle_prefill(case, rows=None, cache=None):
                      case["cu_seqlens"].cpu().numpy(), kc, vc,
                      case["block_table"].cpu().numpy(),
                      case["ctx_lens"].cpu().numpy(), case["window"], case["rel_extent"],
-                     rows=rows)
+                     rows=rows, sink=host_opt(case, "sink"), gate=host_opt(case, "gate"))
 
 
 def oracle_decode_multi(case, batch=None, tokens=None, heads=None):
     h = host_decode_inputs(case)
     return O.decode_multi(h["q"], h["rel"], h["k_cache"], h["v_cache"], h["block_table"],
                           h["seq_lens"], case["window"], case["rel_extent"], batch=batch,
-                          tokens=tokens, heads=heads)
+                          tokens=tokens, heads=heads, sink=host_opt(case, "sink"),
+                          gate=host_opt(case, "gate"))
