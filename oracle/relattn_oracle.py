@@ -54,8 +54,16 @@ there is no blocking, fusion or reordering):
   head) whose sigmoid multiplies that head's output.  Both are inputs; the
   projections that produce them are outside attention.
 
+* FP8 KV cache (optional, decode): keys and values stored as e4m3 (1 sign,
+  4 exponent bits with bias 7, 3 mantissa bits, no infinities) times one
+  scale per cache ("vLLM TML Inkling Support": FP8 global attention is on
+  the roadmap; reading, as no format is given: the e4m3 format with a
+  per-tensor scale, key = k_scale * e4m3 value, value = v_scale * e4m3
+  value).
+
 Data conventions: bf16 tensors are passed as ``np.uint16`` arrays of bf16 bit
-patterns (converted exactly here); float arrays are used as float64.
+patterns and e4m3 tensors as ``np.uint8`` arrays of e4m3 bit patterns (both
+converted exactly here); float arrays are used as float64.
 Layouts: q ``[rows, Hq, d_qk]``, rel ``[rows, Hq, E]``, k cache
 ``[NB, 128, Hkv, d_qk]``, v cache ``[NB, 128, Hkv, d_v]``, block_table
 ``[B, max_blocks]`` int.
@@ -85,11 +93,29 @@ def bf16_bits_to_f64(bits) -> np.ndarray:
     return (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
 
 
+def e4m3_bits_to_f64(bits) -> np.ndarray:
+    """Exact value of e4m3 bit patterns: (-1)^s * 2^(e-7) * (1 + m/8) for
+    e > 0, (-1)^s * 2^-6 * m/8 for e = 0; the pattern e = 15, m = 7 is NaN."""
+    b = np.asarray(bits)
+    if b.dtype != np.uint8:
+        raise TypeError("e4m3 data must be passed as uint8 bit patterns")
+    b = b.astype(np.int64)
+    sign = np.where(b & 0x80, -1.0, 1.0)
+    e = (b >> 3) & 0xF
+    m = (b & 0x7).astype(np.float64)
+    mag = np.where(e == 0, m / 8.0 * 2.0 ** -6, (1.0 + m / 8.0) * np.exp2(e - 7.0))
+    mag = np.where((e == 15) & (m == 7), np.nan, mag)
+    return sign * mag
+
+
 def as_f64(x) -> np.ndarray:
-    """float64 view of an input: uint16 is read as bf16 bits, floats widen."""
+    """float64 view of an input: uint16 is read as bf16 bits, uint8 as e4m3
+    bits, floats widen."""
     a = np.asarray(x)
     if a.dtype == np.uint16:
         return bf16_bits_to_f64(a)
+    if a.dtype == np.uint8:
+        return e4m3_bits_to_f64(a)
     return a.astype(np.float64)
 
 
@@ -158,18 +184,20 @@ def prefill_blocks(ctx_len: int, t_first: int, t_last: int, window: int,
 # paged cache access
 # --------------------------------------------------------------------------
 
-def gather_kv(k_cache, v_cache, table_row, positions, kv_head: int):
+def gather_kv(k_cache, v_cache, table_row, positions, kv_head: int, k_scale=1.0,
+              v_scale=1.0):
     """Keys and values at the given positions of one sequence, float64.
 
     Position pos lives at slot pos % 128 of physical block
     table_row[pos // 128] ("Inkling-Small on Gaudi 2", section "Attention
-    with a relative bias": positions from each block's ordinal).
+    with a relative bias": positions from each block's ordinal).  An FP8
+    cache's entries are multiplied by its scale.
     """
     pos = np.asarray(positions, dtype=np.int64)
     phys = np.asarray(table_row, dtype=np.int64)[pos // BLOCK_SIZE]
     slot = pos % BLOCK_SIZE
-    K = as_f64(k_cache[phys, slot, kv_head])
-    V = as_f64(v_cache[phys, slot, kv_head])
+    K = as_f64(k_cache[phys, slot, kv_head]) * float(k_scale)
+    V = as_f64(v_cache[phys, slot, kv_head]) * float(v_scale)
     return K, V
 
 
@@ -263,10 +291,12 @@ def merge_partials(outs, lses) -> np.ndarray:
 # --------------------------------------------------------------------------
 
 def decode(q, rel, k_cache, v_cache, block_table, seq_lens, window: int,
-           rel_extent: int, batch=None, heads=None, sink=None, gate=None) -> np.ndarray:
+           rel_extent: int, batch=None, heads=None, sink=None, gate=None, k_scale=1.0,
+           v_scale=1.0) -> np.ndarray:
     """Paged decode: one query per sequence at position seq_lens[b] - 1.
 
-    ``sink`` / ``gate``: optional [B, Hq] logits (see ``attend``).  Returns
+    ``sink`` / ``gate``: optional [B, Hq] logits (see ``attend``);
+    ``k_scale`` / ``v_scale``: the scales of an FP8 cache.  Returns
     float64 [B, Hq, d_v]; rows/heads not selected by ``batch`` / ``heads``
     are left NaN.
     """
@@ -285,7 +315,7 @@ def decode(q, rel, k_cache, v_cache, block_table, seq_lens, window: int,
                   if heads is None or h in heads]
             if not hs:
                 continue
-            K, V = gather_kv(k_cache, v_cache, block_table[b], keys, kvh)
+            K, V = gather_kv(k_cache, v_cache, block_table[b], keys, kvh, k_scale, v_scale)
             for h in hs:
                 bias = rel_bias(rel[b, h], P, keys, rel_extent)
                 out[b, h] = attend(q[b, h], K, V, bias, d_qk,
@@ -296,7 +326,7 @@ def decode(q, rel, k_cache, v_cache, block_table, seq_lens, window: int,
 
 def decode_multi(q, rel, k_cache, v_cache, block_table, seq_lens, window: int,
                  rel_extent: int, batch=None, tokens=None, heads=None, sink=None,
-                 gate=None) -> np.ndarray:
+                 gate=None, k_scale=1.0, v_scale=1.0) -> np.ndarray:
     """Multi-token decode, the verification step of speculative decoding.
 
     The k newest tokens of sequence b each attend over the paged cache:
@@ -330,7 +360,8 @@ def decode_multi(q, rel, k_cache, v_cache, block_table, seq_lens, window: int,
                       if heads is None or h in heads]
                 if not hs:
                     continue
-                K, V = gather_kv(k_cache, v_cache, block_table[b], keys, kvh)
+                K, V = gather_kv(k_cache, v_cache, block_table[b], keys, kvh, k_scale,
+                                 v_scale)
                 for h in hs:
                     bias = rel_bias(rel[b, i, h], P, keys, rel_extent)
                     out[b, i, h] = attend(q[b, i, h], K, V, bias, d_qk,

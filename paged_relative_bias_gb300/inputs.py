@@ -37,6 +37,7 @@ class DecodeWorkload:
     max_blocks_per_seq: int = 0  # 0: the longest sequence's block count
     query_tokens: int = 0  # > 0: multi-token decode, q [B, k, Hq, d], rel [B, k, Hq, E]
     rel_dtype: str = "f32"  # "bf16": rel drawn in fp32 and rounded to bf16
+    kv_dtype: str = "bf16"  # "fp8": caches quantised to e4m3 with one scale each
 
 
 @dataclass(frozen=True)
@@ -169,11 +170,22 @@ def make_decode(wl: DecodeWorkload, device="cpu", seed_data: int = 0,
     rel = rel.to(_REL_DTYPES[wl.rel_dtype])
     k_cache = _randn((pool, BLOCK_SIZE, Hkv, wl.d_qk), g, device, torch.bfloat16)
     v_cache = _randn((pool, BLOCK_SIZE, Hkv, wl.d_v), g, device, torch.bfloat16)
+    scales = {}
+    if wl.kv_dtype == "fp8":
+        k_cache, scales["k_scale"] = quantize_e4m3(k_cache)
+        v_cache, scales["v_scale"] = quantize_e4m3(v_cache)
     return dict(
         q=q, rel=rel, k_cache=k_cache, v_cache=v_cache,
         block_table=table.to(device),
         seq_lens=torch.tensor(lens, dtype=torch.int32, device=device),
-        window=wl.window, rel_extent=wl.rel_extent, workload=wl)
+        window=wl.window, rel_extent=wl.rel_extent, workload=wl, **scales)
+
+
+def quantize_e4m3(x: torch.Tensor):
+    """(e4m3 tensor, scale) with one scale for the whole tensor: the largest
+    magnitude maps to 448, the largest finite e4m3 value."""
+    scale = float(x.float().abs().max()) / 448.0
+    return (x.float() / scale).to(torch.float8_e4m3fn), scale
 
 
 def relayout_decode(case: dict, seed: int) -> dict:

@@ -31,6 +31,13 @@ def to_f64(t: torch.Tensor) -> np.ndarray:
     return t.detach().cpu().double().numpy()
 
 
+def host_cache(t: torch.Tensor):
+    """A KV cache for the oracle: bf16 or e4m3 bit patterns."""
+    if t.dtype == torch.float8_e4m3fn:
+        return t.view(torch.uint8).cpu().numpy()
+    return bf16_bits(t)
+
+
 def host_rel(rel: torch.Tensor):
     """rel for the oracle: float32 values, or bf16 bit patterns."""
     return bf16_bits(rel) if rel.dtype == torch.bfloat16 else rel.cpu().numpy()
@@ -40,7 +47,7 @@ def host_decode_inputs(case):
     """numpy copies of a decode case for the oracle (bf16 kept as bits)."""
     return dict(
         q=bf16_bits(case["q"]), rel=host_rel(case["rel"]),
-        k_cache=bf16_bits(case["k_cache"]), v_cache=bf16_bits(case["v_cache"]),
+        k_cache=host_cache(case["k_cache"]), v_cache=host_cache(case["v_cache"]),
         block_table=case["block_table"].cpu().numpy(),
         seq_lens=case["seq_lens"].cpu().numpy())
 
@@ -55,7 +62,8 @@ def oracle_decode(case, batch=None, heads=None):
     h = host_decode_inputs(case)
     return O.decode(h["q"], h["rel"], h["k_cache"], h["v_cache"], h["block_table"],
                     h["seq_lens"], case["window"], case["rel_extent"], batch=batch,
-                    heads=heads, sink=host_opt(case, "sink"), gate=host_opt(case, "gate"))
+                    heads=heads, sink=host_opt(case, "sink"), gate=host_opt(case, "gate"),
+                    k_scale=case.get("k_scale", 1.0), v_scale=case.get("v_scale", 1.0))
 
 
 class RowRel:
@@ -109,4 +117,5 @@ def oracle_decode_multi(case, batch=None, tokens=None, heads=None):
     return O.decode_multi(h["q"], h["rel"], h["k_cache"], h["v_cache"], h["block_table"],
                           h["seq_lens"], case["window"], case["rel_extent"], batch=batch,
                           tokens=tokens, heads=heads, sink=host_opt(case, "sink"),
-                          gate=host_opt(case, "gate"))
+                          gate=host_opt(case, "gate"), k_scale=case.get("k_scale", 1.0),
+                          v_scale=case.get("v_scale", 1.0))

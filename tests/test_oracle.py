@@ -599,3 +599,38 @@ def test_decode_multi_sink_gate_rows_equal_decode_at_their_lengths():
         dec = O.decode(c["qm"][:, i], c["relm"][:, i], c["kc"], c["vc"], c["table"],
                        np.array([L - k + i + 1]), 64, 64, sink=sink[:, i], gate=gate[:, i])
         np.testing.assert_allclose(multi[:, i], dec, atol=1e-13, rtol=0)
+
+
+# ---------------------------------------------------------------------------
+# FP8 (e4m3) KV cache
+# ---------------------------------------------------------------------------
+
+def test_e4m3_decoder_against_torch_on_every_code():
+    """All 256 patterns against torch's float8_e4m3fn (an independent
+    implementation of the format); NaN patterns agree as NaN."""
+    codes = np.arange(256, dtype=np.uint8)
+    mine = O.e4m3_bits_to_f64(codes)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).double().numpy()
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(mine), nan)
+    assert np.array_equal(mine[~nan], ref[~nan])
+    # a few values by hand: 1.0, the largest 448, the smallest subnormal 2^-9
+    assert O.e4m3_bits_to_f64(np.array([0x38, 0x7E, 0x01, 0x80, 0xB8], dtype=np.uint8)).tolist() \
+        == [1.0, 448.0, 2.0 ** -9, -0.0, -1.0]
+
+
+def test_fp8_decode_equals_decode_of_the_dequantised_cache():
+    """Reading the e4m3 cache with scales is the decode of the float cache
+    holding scale * value, exactly."""
+    c = random_decode_case(110, 300)
+    r = rng(111)
+    kc8 = r.integers(0, 256, size=c["kc"].shape, dtype=np.uint8)
+    vc8 = r.integers(0, 256, size=c["vc"].shape, dtype=np.uint8)
+    kc8[(kc8 & 0x7F) == 0x7F] = 0x38  # no NaN patterns in a cache
+    vc8[(vc8 & 0x7F) == 0x7F] = 0x38
+    ks, vs = 0.013, 0.7
+    a = O.decode(c["q"], c["rel"], kc8, vc8, c["table"], c["seq_lens"], 100, 64,
+                 k_scale=ks, v_scale=vs)
+    b = O.decode(c["q"], c["rel"], O.e4m3_bits_to_f64(kc8) * ks, O.e4m3_bits_to_f64(vc8) * vs,
+                 c["table"], c["seq_lens"], 100, 64)
+    assert np.array_equal(a, b)
