@@ -66,13 +66,14 @@ def decode_work(wl, seq_lens):
     g = wl.num_q_heads // wl.num_kv_heads
     k = max(1, wl.query_tokens)
     res = 2 if wl.rel_dtype == "bf16" else 4
+    kes = 1 if wl.kv_dtype == "fp8" else 2
     total = 0
     per_group = []
     for L in seq_lens:
         lo = max(0, L - k - wl.window + 1) if wl.window > 0 else 0
         P = L - 1
         blocks = P // BLOCK - lo // BLOCK + 1
-        kv = (P - lo + 1) * (wl.d_qk + wl.d_v) * 2
+        kv = (P - lo + 1) * (wl.d_qk + wl.d_v) * kes
         head = 0
         for Pi in range(L - k, L):
             n = min(wl.window, Pi + 1) if wl.window > 0 else Pi + 1
@@ -115,7 +116,8 @@ def describe(wl):
                 else "decode")
         return (f"{wl.name}: {kind} B={wl.batch}, {wl.num_q_heads}/{wl.num_kv_heads} heads, "
                 f"d_qk={wl.d_qk} d_v={wl.d_v}, {win}, rel_extent={wl.rel_extent}, {lens}, "
-                f"{wl.rel_dtype} rel, bf16 paged KV in 128-token blocks, random block tables")
+                f"{wl.rel_dtype} rel, {'e4m3 (per-tensor scales)' if wl.kv_dtype == 'fp8' else 'bf16'} "
+                f"paged KV in 128-token blocks, random block tables")
     win = f"W={wl.window}" if wl.window > 0 else "global"
     return (f"{wl.name}: chunked prefill {len(wl.new_tokens)}x{wl.new_tokens[0]} new tokens "
             f"after {wl.ctx_lens[0]} cached, {wl.num_q_heads}/{wl.num_kv_heads} heads, "
@@ -323,7 +325,8 @@ def run_decode(R, wl, device, steps, warmup, dist, sampler, l2, shared_pool=Fals
     def call(i):
         c = sets[i]
         fn(c["q"], c["rel"], c["k_cache"], c["v_cache"], c["block_table"], c["seq_lens"],
-           wl.window, wl.rel_extent, out=outs[i], workspace=wss[i])
+           wl.window, wl.rel_extent, out=outs[i], workspace=wss[i], k_scale=c.get("k_scale"),
+           v_scale=c.get("v_scale"))
 
     # graphs[r]: calls for sets 0..r-1 back to back (r = len(sets) is one
     # full pass; shorter ones time the remainder of steps)
@@ -381,7 +384,8 @@ def run_decode_e2e(R, sets, wl, wss, device, steps, warmup, dist, sampler):
         for name in keys:
             dev[name].copy_(host[i][name], non_blocking=True)
         fn(dev["q"], dev["rel"], sets[i]["k_cache"], sets[i]["v_cache"], dev["block_table"],
-           dev["seq_lens"], wl.window, wl.rel_extent, out=out_d, workspace=wss[i])
+           dev["seq_lens"], wl.window, wl.rel_extent, out=out_d, workspace=wss[i],
+           k_scale=sets[i].get("k_scale"), v_scale=sets[i].get("v_scale"))
         out_h.copy_(out_d, non_blocking=True)
 
     times = timed_steps(step, steps, warmup, None, dist, sampler)
@@ -423,11 +427,20 @@ def group_blocks(O, wl, L, table_row):
     return [(lb, int(table_row[lb])) for lb in range(first, blocks[0][0])] + blocks
 
 
-def oracle_group(O, wl, q, rel, b, kc, vc, sub, L, heads):
+def cache_bits(t):
+    """Host copy of KV cache blocks for the oracle ([n, 128, Hkv, d]): bf16
+    bit patterns, or those of a head-major e4m3 cache ([n, Hkv, 128, d])."""
+    from paged_relative_bias_gb300.inputs import bf16_bits
+    if t.dtype == torch.float8_e4m3fn:
+        return t.view(torch.uint8).transpose(1, 2).contiguous().cpu().numpy()
+    return bf16_bits(t)
+
+
+def oracle_group(O, wl, q, rel, b, kc, vc, sub, L, heads, k_scale=1.0, v_scale=1.0):
     """The oracle on one (sequence, KV head) group over its gathered blocks."""
     fn = O.decode_multi if wl.query_tokens > 0 else O.decode
     fn(q[b:b + 1], rel[b:b + 1], kc, vc, sub, np.array([L]), wl.window, wl.rel_extent,
-       heads=heads)
+       heads=heads, k_scale=k_scale, v_scale=v_scale)
 
 
 def oracle_decode_sample(case, wl, budget_s):
@@ -452,8 +465,8 @@ def oracle_decode_sample(case, wl, budget_s):
         sub = np.full((1, table.shape[1]), -1, dtype=np.int64)
         for i, (lblk, _) in enumerate(blocks):
             sub[0, lblk] = i
-        per_seq.append((bf16_bits(case["k_cache"].index_select(0, ids)),
-                        bf16_bits(case["v_cache"].index_select(0, ids)), sub))
+        per_seq.append((cache_bits(case["k_cache"].index_select(0, ids)),
+                        cache_bits(case["v_cache"].index_select(0, ids)), sub))
     groups = [(b, kvh) for b in range(wl.batch) for kvh in range(wl.num_kv_heads)]
     done, nbytes, elapsed = 0, 0, 0.0
     while elapsed < budget_s or done == 0:
@@ -461,7 +474,8 @@ def oracle_decode_sample(case, wl, budget_s):
             kc, vc, sub = per_seq[b]
             heads = list(range(kvh * g, (kvh + 1) * g))
             t0 = time.perf_counter()
-            oracle_group(O, wl, q, rel, b, kc, vc, sub, lens[b], heads)
+            oracle_group(O, wl, q, rel, b, kc, vc, sub, lens[b], heads,
+                         case.get("k_scale", 1.0), case.get("v_scale", 1.0))
             elapsed += time.perf_counter() - t0
             done += 1
             nbytes += per_group[b]
@@ -528,6 +542,8 @@ def ours(args):
     wl = I.WORKLOADS[args.workload]
     if args.rel == "bf16":
         wl = I.variant(wl, rel_dtype="bf16")
+    if args.kv == "fp8":
+        wl = I.variant(wl, kv_dtype="fp8")
     sets, step_bytes, times, wss = run_decode(R, wl, device, args.steps, args.warmup, dist,
                                               sampler, l2, args.pool == "shared")
     case = sets[0]
@@ -548,10 +564,12 @@ def ours(args):
 
     secondary = []
     if not args.no_secondary:
-        for name, rdt in (("global_decode_b1", "f32"), ("global_decode_b8", "f32"),
-                          ("diffhead_decode", "f32"), ("verify_decode", "f32"),
-                          ("local_decode", "bf16")):
-            w2 = I.variant(I.WORKLOADS[name], rel_dtype=rdt)
+        for name, rdt, kvd in (("global_decode_b1", "f32", "bf16"),
+                               ("global_decode_b8", "f32", "bf16"),
+                               ("diffhead_decode", "f32", "bf16"), ("verify_decode", "f32", "bf16"),
+                               ("local_decode", "bf16", "bf16"), ("global_decode_b8", "f32", "fp8"),
+                               ("global_decode_b1", "f32", "fp8")):
+            w2 = I.variant(I.WORKLOADS[name], rel_dtype=rdt, kv_dtype=kvd)
             c2, b2, t2, _ = run_decode(R, w2, device, args.secondary_steps, 3, dist, sampler, l2)
             m2 = sum(t2) / len(t2)
             a2 = sum(b2) / len(b2)
@@ -629,6 +647,8 @@ def reference(args):
     wl = I.WORKLOADS[args.workload]
     if args.rel == "bf16":
         wl = I.variant(wl, rel_dtype="bf16")
+    if args.kv == "fp8":
+        wl = I.variant(wl, kv_dtype="fp8")
     device = "cuda" if torch.cuda.is_available() else "cpu"
     case = I.make_decode(wl, device)
     lens = case["seq_lens"].cpu().tolist()
@@ -646,13 +666,14 @@ def reference(args):
         sub = np.full((1, table.shape[1]), -1, dtype=np.int64)
         for i, (lblk, _) in enumerate(blocks):
             sub[0, lblk] = i
-        prepared.append((bf16_bits(case["k_cache"].index_select(0, ids)),
-                         bf16_bits(case["v_cache"].index_select(0, ids)), sub))
+        prepared.append((cache_bits(case["k_cache"].index_select(0, ids)),
+                         cache_bits(case["v_cache"].index_select(0, ids)), sub))
 
     def step(i):
         b, kvh = groups[i % len(groups)]
         kc, vc, sub = prepared[b]
-        oracle_group(O, wl, q, rel, b, kc, vc, sub, lens[b], list(range(kvh * g, (kvh + 1) * g)))
+        oracle_group(O, wl, q, rel, b, kc, vc, sub, lens[b], list(range(kvh * g, (kvh + 1) * g)),
+                     case.get("k_scale", 1.0), case.get("v_scale", 1.0))
         return per_group[b]
 
     for i in range(args.warmup):
@@ -692,6 +713,8 @@ def main():
                     help="sequences of the chunked prefill (default 4)")
     ap.add_argument("--rel", choices=["f32", "bf16"], default="f32",
                     help="element type of the rel input of the timed workload")
+    ap.add_argument("--kv", choices=["bf16", "fp8"], default="bf16",
+                    help="element type of the decode KV cache of the timed workload")
     ap.add_argument("--pool", choices=["per-set", "shared"], default="per-set",
                     help="decode input sets: one KV pool each (default), or one shared pool "
                          "with renumbered block tables (small device footprint, for ncu)")

@@ -191,6 +191,7 @@ int relattn_decode_multi(const void* q, const float* rel,
  */
 #define RELATTN_DTYPE_F32 0
 #define RELATTN_DTYPE_BF16 1
+#define RELATTN_DTYPE_E4M3 2
 
 /*
  *  - sink / gate: the gated attention output of Inkling 2 ("Inkling 2 Small
@@ -204,11 +205,27 @@ int relattn_decode_multi(const void* q, const float* rel,
  *    for prefill), or NULL for none; the library reads them and owns
  *    neither.
  */
+/*
+ *  - kv: the element type of the KV cache.  0 or RELATTN_DTYPE_BF16: bf16.
+ *    RELATTN_DTYPE_E4M3: FP8 e4m3 keys and values, one scale per cache, a
+ *    key being k_scale times its e4m3 value and a value v_scale times its
+ *    e4m3 value ("vLLM TML Inkling Support": FP8 global attention is a
+ *    roadmap item; the format is this library's reading).  e4m3 caches are
+ *    head-major, [num_blocks][num_kv_heads][128][d] (a token's head row is
+ *    only 128 bytes; this keeps each block's rows of one head contiguous),
+ *    and num_blocks * num_kv_heads * 128 must stay below 2^31.  Decode
+ *    only, one query token,
+ *    g = Hq/Hkv <= 8 and d_v = 128: RELATTN_ERR_UNSUPPORTED otherwise, and
+ *    for relattn_prefill_ex.  k_scale and v_scale must be finite and > 0.
+ */
 typedef struct relattn_options {
   int32_t rel;       /* RELATTN_DTYPE_F32 or RELATTN_DTYPE_BF16 */
   int32_t out;       /* RELATTN_DTYPE_BF16 or RELATTN_DTYPE_F32 */
   const float* sink; /* NULL, or [rows][Hq] fp32 sink logits */
   const float* gate; /* NULL, or [rows][Hq] fp32 gate logits */
+  int32_t kv;        /* 0 / RELATTN_DTYPE_BF16, or RELATTN_DTYPE_E4M3 */
+  float k_scale;     /* e4m3 cache: key scale */
+  float v_scale;     /* e4m3 cache: value scale */
 } relattn_options;
 
 /*

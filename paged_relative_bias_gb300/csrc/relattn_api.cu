@@ -14,7 +14,8 @@ namespace relattn {
 namespace {
 
 constexpr int kMaxDevices = 64;
-constexpr int kMaxStages = 6;
+constexpr int kMaxStages = 6;       // bf16 cache: 32 KB per stage
+constexpr int kMaxStagesE4m3 = 12;  // e4m3 cache: 16 KB per stage
 constexpr int kMaxDecodeGrid = 46340;  // grid^2 < 2^31
 constexpr size_t kStatusBytes = 256;
 
@@ -114,6 +115,25 @@ bool decode_cache_maps(const relattn_kv_cache* c, CUtensorMap* tk, CUtensorMap* 
                   CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
+// e4m3 caches are head-major, [NB][Hkv][128][d]: a token's head row is only
+// 128 bytes, and this keeps a block's 128 rows of one head contiguous.  As a
+// 2-D tensor of rows (block * Hkv + head) * 128 + slot, a 64-key tile is one
+// 8 KB box, landing as 64 rows x 128 bytes with the 128-byte swizzle.
+bool decode_cache_maps_e4m3(const relattn_kv_cache* c, CUtensorMap* tk, CUtensorMap* tv) {
+  const cuuint64_t rows =
+      static_cast<cuuint64_t>(c->num_blocks) * c->num_kv_heads * c->block_size;
+  const cuuint64_t kd[2] = {static_cast<cuuint64_t>(c->d_qk), rows};
+  const cuuint64_t ks[1] = {static_cast<cuuint64_t>(c->d_qk)};
+  const cuuint32_t kb[2] = {static_cast<cuuint32_t>(c->d_qk), static_cast<cuuint32_t>(kTileKeys)};
+  const cuuint64_t vd[2] = {static_cast<cuuint64_t>(c->d_v), rows};
+  const cuuint64_t vs[1] = {static_cast<cuuint64_t>(c->d_v)};
+  const cuuint32_t vb[2] = {static_cast<cuuint32_t>(c->d_v), static_cast<cuuint32_t>(kTileKeys)};
+  return make_map(tk, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, c->k, kd, ks, kb,
+                  CU_TENSOR_MAP_SWIZZLE_128B) &&
+         make_map(tv, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, c->v, vd, vs, vb,
+                  CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
 int check_cache(const relattn_kv_cache* c) {
   if (!c || !c->k || !c->v) return RELATTN_ERR_INVALID_ARG;
   if (!aligned16(c->k) || !aligned16(c->v)) return RELATTN_ERR_INVALID_ARG;
@@ -205,8 +225,10 @@ struct IoTypes {
   int out_f32;        // 1: out is fp32, 0: bf16
   const float* sink;  // per (query row, head) sink logits, or null
   const float* gate;  // per (query row, head) gate logits, or null
+  int kv_es;          // bytes per cache element: 2 (bf16) or 1 (e4m3)
+  float k_scale, v_scale;
 };
-constexpr IoTypes kDefaultIo = {4, 0, nullptr, nullptr};
+constexpr IoTypes kDefaultIo = {4, 0, nullptr, nullptr, 2, 1.f, 1.f};
 
 // From the C ABI's options; false for a value that is not offered (an
 // unknown type code, or a sink / gate pointer not 4-byte aligned).
@@ -220,6 +242,18 @@ static bool io_types(const relattn_options* t, IoTypes* io) {
   io->out_f32 = t->out == RELATTN_DTYPE_F32 ? 1 : 0;
   io->sink = t->sink;
   io->gate = t->gate;
+  if (t->kv == 0 || t->kv == RELATTN_DTYPE_BF16) {
+    io->kv_es = 2;
+    io->k_scale = io->v_scale = 1.f;
+  } else if (t->kv == RELATTN_DTYPE_E4M3) {
+    const auto ok = [](float x) { return x > 0.f && x < 3.0e38f; };  // finite, positive
+    if (!ok(t->k_scale) || !ok(t->v_scale)) return false;
+    io->kv_es = 1;
+    io->k_scale = t->k_scale;
+    io->v_scale = t->v_scale;
+  } else {
+    return false;
+  }
   return true;
 }
 
@@ -251,6 +285,11 @@ static int prepare_decode(const void* q, const void* rel, IoTypes io,
   const int grid = decode_grid(dims, *di);
   if (kq < 1 || kq > kMaxQueryTokens) return RELATTN_ERR_UNSUPPORTED;
   const int gq = dims->num_q_heads / cache->num_kv_heads;
+  // an e4m3 cache: the one-token kernel (g <= 8) with d_v = 128
+  if (io.kv_es == 1 && (decode_multi_kernel(kq, gq) || cache->d_v != 128 ||
+                        static_cast<long long>(cache->num_blocks) * cache->num_kv_heads * 128 >
+                            0x7fffffffLL))
+    return RELATTN_ERR_UNSUPPORTED;
   const int kpc = kq < kMaxDecodeRows / gq ? kq : kMaxDecodeRows / gq;  // tokens per chunk
   const int nck = (kq + kpc - 1) / kpc;
   // the kernel's work split is 32-bit: all tiles < 2^31, grid^2 < 2^31
@@ -273,6 +312,8 @@ static int prepare_decode(const void* q, const void* rel, IoTypes io,
   p.gate = io.gate;
   p.rel_es = io.rel_es;
   p.out_f32 = io.out_f32;
+  p.kv_es = io.kv_es;
+  p.v_scale = io.v_scale;
   p.status = reinterpret_cast<uint32_t*>(ws);
   p.counters = reinterpret_cast<int32_t*>(ws + w.counters);
   p.part_lse = reinterpret_cast<float*>(ws + w.lse);
@@ -290,7 +331,8 @@ static int prepare_decode(const void* q, const void* rel, IoTypes io,
   p.kpc = kpc;
   p.nck = nck;
   p.Bv = dims->batch * nck;
-  p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(128.0));
+  // log2(e) / sqrt(d_qk), times the key scale of an e4m3 cache
+  p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(128.0) * io.k_scale);
   L->grid = grid;
   if (walk) {
     p.nstages = 0;
@@ -298,12 +340,15 @@ static int prepare_decode(const void* q, const void* rel, IoTypes io,
   }
   // An even number of stages: the decode kernel's two consumer groups each
   // own every other stage.
-  p.nstages = kMaxStages;
+  p.nstages = io.kv_es == 1 ? kMaxStagesE4m3 : kMaxStages;
   while (p.nstages >= 2 &&
-         decode_smem_bytes(p.nstages, p.B, p.Bv, p.kpc, p.g, p.dv, p.rel_es) > di->smem_optin)
+         decode_smem_bytes(p.nstages, p.B, p.Bv, p.kpc, p.g, p.dv, p.rel_es, p.kv_es) >
+             di->smem_optin)
     p.nstages -= 2;
   if (p.nstages < 2) return RELATTN_ERR_UNSUPPORTED;  // batch too large for shared memory
-  if (!decode_cache_maps(cache, &L->tm_k, &L->tm_v)) return RELATTN_ERR_CUDA;
+  if (!(p.kv_es == 1 ? decode_cache_maps_e4m3(cache, &L->tm_k, &L->tm_v)
+                     : decode_cache_maps(cache, &L->tm_k, &L->tm_v)))
+    return RELATTN_ERR_CUDA;
   // rel [B][k][Hq][E] fp32 or bf16: boxes of one token's g heads x
   // rel_box_w distances
   const cuuint64_t rd[2] = {static_cast<cuuint64_t>(rel_extent),
@@ -559,6 +604,7 @@ int relattn_prefill_ex(const void* q, const void* k, const void* v, const void* 
                        size_t workspace_bytes, void* stream) {
   IoTypes io;
   if (!io_types(options, &io)) return RELATTN_ERR_INVALID_ARG;
+  if (io.kv_es != 2) return RELATTN_ERR_UNSUPPORTED;  // e4m3 caches: decode only
   return relattn_prefill_io(q, k, v, rel, io, cu_seqlens, cache, block_table, ctx_lens, window,
                             rel_extent, dims, out, workspace, workspace_bytes, stream);
 }

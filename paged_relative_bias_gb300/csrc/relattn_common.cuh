@@ -210,6 +210,16 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0,
 }
 
 // D = A(16x16, row) * B(16x8, col) + D
+// The same with f16 operands.
+__device__ __forceinline__ void mma_16816_f16(float* d, const uint32_t* a, uint32_t b0,
+                                              uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
 __device__ __forceinline__ void mma_16816(float* d, const uint32_t* a,
                                           uint32_t b0, uint32_t b1) {
   asm volatile(

@@ -30,6 +30,8 @@
 //    (normalised output, base-2 log-sum-exp) per piece in the workspace; the
 //    CTA that finishes the segment last (counted with an acq_rel atomic)
 //    merges them in a fixed order.
+#include <cuda_fp16.h>
+
 #include <type_traits>
 
 #include "relattn_common.cuh"
@@ -45,6 +47,10 @@ constexpr int kConsumerThreads = 32 * kConsumerWarps;
 constexpr int kWholeSlackTiles = 4;  // tolerated imbalance to avoid a split
 constexpr int kQBufBytes = 4096;     // 16 rows x 256 B as two swizzled halves
 constexpr int kMiscAbort = 14;       // shared flag word: a consumer warp gave up waiting
+// Per consumer warp with an e4m3 cache: its lanes' f16 B fragments of Q^T
+// for the eight k-steps of d_qk = 128 (8 x 32 lanes x 8 bytes).
+constexpr int kPrivQ = 8 * 32 * 8;
+
 constexpr int kSlicePad = 8;         // floats of padding per merge-slice row, at most
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kNegInf = -__builtin_huge_valf();
@@ -55,9 +61,38 @@ constexpr float kNegInf = -__builtin_huge_valf();
 __device__ __forceinline__ float out_scale(const DecodeParams& p, size_t qi, float M, float Ls) {
   float den = Ls;
   if (p.sink) den += ex2(__ldg(p.sink + qi) * kLog2e - M);  // 0 for a sink of -inf
-  float s = den > 0.f ? 1.f / den : 0.f;                     // 0 when den overflows
+  float s = den > 0.f ? p.v_scale / den : 0.f;               // 0 when den overflows
   if (p.gate) s /= 1.f + ex2(-__ldg(p.gate + qi) * kLog2e);
   return s;
+}
+
+// bf16 pair -> f16 pair (exact for the magnitudes of attention inputs)
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
+  const __half2 h = __floats2half2_rn(__uint_as_float(v << 16), __uint_as_float(v & 0xffff0000u));
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// Two e4m3 values (low byte first) -> f16 pair (low half first), exactly,
+// in one conversion instruction.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
+  uint32_t r;
+  const unsigned short in = static_cast<unsigned short>(two);
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(in));
+  return r;
+}
+
+// Four e4m3 values (one 32-bit word, low byte first) -> two f16 pairs: bytes
+// 0-1 in lo, bytes 2-3 in hi.
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t four, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(four));
 }
 
 __device__ __forceinline__ float rel_f32(float x) { return x; }
@@ -85,18 +120,22 @@ __host__ __device__ constexpr int rel_token_bytes(int g, int es) {
 }
 
 // Shared-memory carve-up (byte offsets from a 1024-aligned base); identical
-// on host and device.  K/V stages are 1024-aligned for the 128-byte swizzle;
-// the rel slices of the stages (kpc token boxes each) live in a ring of their
-// own; per-sequence lengths take B entries, tile counts and prefixes Bv.
+// on host and device.  K/V stages are 1024-aligned for the 128-byte swizzle
+// (bf16: two 64-column halves per tile; e4m3: one 128-byte row per key); an
+// e4m3 cache adds the consumer warps' f16 query fragments; the rel slices of
+// the stages (kpc token boxes each) live in a ring of their own;
+// per-sequence lengths take B entries, tile counts and prefixes Bv.
 struct DecodeSmem {
-  int qbuf, stages, stage_bytes, rel, rel_bytes, slices, bars, valid, seqlen, nt, pref, m, l,
-      misc, total;
-  __host__ __device__ DecodeSmem(int nstages, int B, int Bv, int kpc, int g, int dv, int rel_es) {
-    stage_bytes = 16384 + kTileKeys * dv * 2;
+  int qbuf, stages, stage_bytes, priv, rel, rel_bytes, slices, bars, valid, seqlen, nt, pref, m,
+      l, misc, total;
+  __host__ __device__ DecodeSmem(int nstages, int B, int Bv, int kpc, int g, int dv, int rel_es,
+                                 int kv_es) {
+    stage_bytes = kTileKeys * (kDqk + dv) * kv_es;
     rel_bytes = kpc * rel_token_bytes(g, rel_es);
     qbuf = 0;
     stages = qbuf + 2 * kQBufBytes;
-    rel = stages + nstages * stage_bytes;
+    priv = stages + nstages * stage_bytes;
+    rel = priv + (kv_es == 1 ? kConsumerWarps * kPrivQ : 0);
     slices = rel + nstages * rel_bytes;
     bars = (slices + kConsumerWarps * kpc * g * (dv + kSlicePad) * 4 + 15) & ~15;
     valid = bars + (2 * nstages + 4) * 8;
@@ -502,8 +541,10 @@ __device__ Plan decode_prologue(const DecodeParams& p, uint8_t* smem, const Deco
   return make_plan(p.Hkv * s_pref[p.Bv], s_misc[0], p.Bv * p.Hkv);
 }
 
-// R16: rel is bf16 (else fp32).
-template <int DV, bool MULTI, bool R16>
+// R16: rel is bf16 (else fp32).  KV8: the cache is e4m3 (one-token kernel
+// only); each consumer warp widens its keys' K and V rows and the query rows
+// to f16 in its own buffers, and the MMAs take f16 operands.
+template <int DV, bool MULTI, bool R16, bool KV8>
 __global__ void __launch_bounds__(kDecodeThreads, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tm_q,
                   const __grid_constant__ CUtensorMap tm_k,
@@ -523,7 +564,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   // merge-slice row padding: conflict-free writes of O^T columns (NB = 1:
   // rows 2 cq apart by 2 (DV + 4) = 8 banks mod 32) or of O rows (NB = 2)
   constexpr int SP = NB == 1 ? 4 : kSlicePad;
-  const DecodeSmem L(ns, p.B, p.Bv, tok.kpc, g, DV, RES);
+  static_assert(!(KV8 && MULTI), "e4m3 caches: one-token kernel only");
+  const DecodeSmem L(ns, p.B, p.Bv, tok.kpc, g, DV, RES, KV8 ? 1 : 2);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
   uint64_t* empty = full + ns;
   uint64_t* qfull = empty + ns;
@@ -582,7 +624,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     }
     return true;
   };
-  const int stage_tx = 16384 + kTileKeys * DV * 2;
+  const int stage_tx = kTileKeys * (kDqk + DV) * (KV8 ? 1 : 2);
   const int rel_tx = g * RW * RES;                 // one token's rel box
   const int rel_stride = rel_token_bytes(g, RES);  // its place in a stage's rel slice
   // K, V and rel of tile `tile` of chunk sq, KV head kvh, into the stage of
@@ -605,8 +647,14 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       mbar_arrive_expect_tx(&full[stage], stage_tx + nrel * rel_tx);
       uint8_t* st = smem + L.stages + stage * L.stage_bytes;
       const int row = id * kBlockSize + (tile & 1) * kTileKeys;
-      tma_load_4d(st, &tm_k, &full[stage], 0, row, 0, kvh);
-      tma_load_4d(st + 16384, &tm_v, &full[stage], 0, row, 0, kvh);
+      if constexpr (KV8) {  // head-major rows: 64 rows x 128 bytes, one box each
+        const int hrow = (id * p.Hkv + kvh) * kBlockSize + (tile & 1) * kTileKeys;
+        tma_load_2d(st, &tm_k, &full[stage], 0, hrow);
+        tma_load_2d(st + kTileKeys * kDqk, &tm_v, &full[stage], 0, hrow);
+      } else {
+        tma_load_4d(st, &tm_k, &full[stage], 0, row, 0, kvh);
+        tma_load_4d(st + 16384, &tm_v, &full[stage], 0, row, 0, kvh);
+      }
       for (int i = 0; i < nrel; ++i)
         tma_load_2d(smem + L.rel + stage * L.rel_bytes + i * rel_stride, &tm_rel, &full[stage],
                     (dmin0 + i) & RAL, (sq.b * tok.k + sq.i0 + i) * p.Hq + kvh * g);
@@ -756,6 +804,23 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     // reads its A fragments from there, one k-step at a time, rather than
     // holding all 32 registers of them next to the 4 x d_v/8 of O
     const uint32_t qbase = smem_u32(smem + L.qbuf + qb * kQBufBytes);
+    // e4m3 cache: the MMAs run in f16.  The lane's B fragments of Q^T (row
+    // r0) for the eight k-steps go to the warp's buffer once per piece, in the
+    // order of the dimensions of its K fragments (below), after which the
+    // shared query buffer is released.  k-step pair u reads dimensions
+    // 64 (cq >> 1) + 16 u + 8 (cq & 1) + 0..7: one 16-byte piece of the row.
+    uint2* const qfrag = reinterpret_cast<uint2*>(smem + L.priv + cwarp * kPrivQ);
+    if constexpr (KV8) {
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const uint4 v = *reinterpret_cast<const uint4*>(
+            smem + L.qbuf + qb * kQBufBytes + (cq >> 1) * 2048 + sw128(r0, 2 * u + (cq & 1)));
+        qfrag[(2 * u) * 32 + lane] = make_uint2(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y));
+        qfrag[(2 * u + 1) * 32 + lane] = make_uint2(bf16x2_to_f16x2(v.z), bf16x2_to_f16x2(v.w));
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&qempty[qb]);
+    }
 
     float m_[2] = {kNegInf, kNegInf}, l_[2] = {0.f, 0.f};
     // One-token kernel (at most 8 rows, NB = 1): O^T = V^T P^T, 16 columns
@@ -793,7 +858,31 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
           // O^T = V^T P^T.  st[0..1]: keys kb (this thread's key), rows
           // 2 cq (+1); st[2..3]: keys kb + 8.
           float sT[4] = {0.f, 0.f, 0.f, 0.f};
-          {
+          if constexpr (KV8) {
+            // A fragments straight from the e4m3 rows (128 bytes, 128-byte
+            // swizzle), widened exactly in registers.  The dot product does
+            // not care about the order of the dimensions, so k-step pair u of
+            // this lane covers the 8 dimensions its Q fragments hold: one
+            // 8-byte read of each of its key rows r0 and r0 + 8 gives columns
+            // (2 cq, +1 | 2 cq + 8, +9) of k-steps 2u and 2u + 1.  Lanes with
+            // cq < 2 read 16-byte pieces 0-3 of a row, the others 4-7, so
+            // each half-warp meets all 32 banks once.
+            const uint8_t* kr = st + (16 * cw + r0) * 128 + (cq & 1) * 8;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int off = ((4 * (cq >> 1) + u) ^ r0) * 16;
+              const uint2 k0 = *reinterpret_cast<const uint2*>(kr + off);
+              const uint2 k8 = *reinterpret_cast<const uint2*>(kr + 1024 + off);
+              uint32_t ka[4], kb[4];
+              e4m3x4_to_f16x2x2(k0.x, ka[0], ka[2]);
+              e4m3x4_to_f16x2x2(k8.x, ka[1], ka[3]);
+              e4m3x4_to_f16x2x2(k0.y, kb[0], kb[2]);
+              e4m3x4_to_f16x2x2(k8.y, kb[1], kb[3]);
+              const uint2 q0 = qfrag[(2 * u) * 32 + lane], q1 = qfrag[(2 * u + 1) * 32 + lane];
+              mma_16816_f16(sT, ka, q0.x, q0.y);
+              mma_16816_f16(sT, kb, q1.x, q1.y);
+            }
+          } else {
             // A = the warp's 16 K rows: matrices (keys 0-7 | 8-15) x
             // (dims 0-7 | 8-15); B = Q^T from rows 0-7 of the query buffer
             const int key = 16 * cw + (mi & 1) * 8 + (lane & 7);
@@ -851,18 +940,45 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
           }
           // P^T as the B operand of O^T = V^T P^T: the transposes of this
           // thread's (keys, rows) pairs are its (rows, keys) fragments
-          const uint32_t pb0 = movmatrix_t(pack_bf16(x[0], x[1]));
-          const uint32_t pb1 = movmatrix_t(pack_bf16(x[2], x[3]));
+          const uint32_t pb0 = movmatrix_t(KV8 ? pack_f16(x[0], x[1]) : pack_bf16(x[0], x[1]));
+          const uint32_t pb1 = movmatrix_t(KV8 ? pack_f16(x[2], x[3]) : pack_bf16(x[2], x[3]));
           // V^T as the A operand: transposed 8x8 loads of V's [key][d_v]
           // rows; matrices (keys 0-7 | 8-15) x (columns 16 db + 0-7 | 8-15)
-          const int vkey = 16 * cw + (mi >> 1) * 8 + (lane & 7);
+          if constexpr (KV8) {
+            // V^T fragments from the e4m3 rows: a 4-byte read gives 4
+            // dimensions of one key; two keys' reads interleaved (byte
+            // permutes) give f16 pairs (key 2 cq (+8), key + 1) for each of the
+            // 4 dimensions.  The output dimensions are permuted to match:
+            // O^T row r0 (+8) of block db is d_v column
+            // 32 (db >> 1) + 4 r0 + 2 (db & 1) (+1).  Each 4-byte read of the
+            // warp meets all 32 banks once.
+            const uint8_t* vr = st + kTileKeys * kDqk + (16 * cw + 2 * cq) * 128 + 4 * (r0 & 3);
 #pragma unroll
-          for (int db = 0; db < DB; ++db) {
-            const int chunk = 2 * db + (mi & 1);
-            uint32_t va[4];
-            ldsm_x4_t(vbase + (chunk >> 3) * 8192 + sw128(vkey, chunk & 7), va[0], va[1], va[2],
-                      va[3]);
-            mma_16816(o[db], va, pb0, pb1);
+            for (int j = 0; j < DB / 2; ++j) {
+              uint32_t va[2][4];
+#pragma unroll
+              for (int pk = 0; pk < 2; ++pk) {  // keys 2 cq (+1), then 2 cq + 8 (+1)
+                const int c = 2 * j + (r0 >> 2);
+                const uint32_t xa = *reinterpret_cast<const uint32_t*>(
+                    vr + pk * 1024 + ((c ^ (2 * cq)) << 4));
+                const uint32_t xb = *reinterpret_cast<const uint32_t*>(
+                    vr + pk * 1024 + 128 + ((c ^ (2 * cq + 1)) << 4));
+                e4m3x4_to_f16x2x2(__byte_perm(xa, xb, 0x5140), va[0][2 * pk], va[0][2 * pk + 1]);
+                e4m3x4_to_f16x2x2(__byte_perm(xa, xb, 0x7362), va[1][2 * pk], va[1][2 * pk + 1]);
+              }
+              mma_16816_f16(o[2 * j], va[0], pb0, pb1);
+              mma_16816_f16(o[2 * j + 1], va[1], pb0, pb1);
+            }
+          } else {
+            const int vkey = 16 * cw + (mi >> 1) * 8 + (lane & 7);
+#pragma unroll
+            for (int db = 0; db < DB; ++db) {
+              const int chunk = 2 * db + (mi & 1);
+              uint32_t va[4];
+              ldsm_x4_t(vbase + (chunk >> 3) * 8192 + sw128(vkey, chunk & 7), va[0], va[1], va[2],
+                        va[3]);
+              mma_16816(o[db], va, pb0, pb1);
+            }
           }
         } else {
           // ---- several tokens (or g > 8), 16 rows: S = Q K^T, O = P V
@@ -962,7 +1078,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       if (lane == 0) mbar_arrive(&empty[stage]);
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(&qempty[qb]);  // the piece's query rows are done
+    if (!KV8 && lane == 0) mbar_arrive(&qempty[qb]);  // the piece's query rows are done
     // A wait that gave up in any consumer warp ends the piece loop of all
     // eight at the same point: each still reaches the next named barrier,
     // and after it they all see the flag.
@@ -1003,6 +1119,14 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       for (int e = 0; e < 2; ++e) {
         const int row = 2 * cq + e;  // this thread's O^T column
         if (row >= nrows) continue;
+        if constexpr (KV8) {  // permuted d_v columns: see the e4m3 V^T fragments
+          float* sl = slices + (cwarp * srows + row) * (DV + SP) + 4 * r0;
+#pragma unroll
+          for (int j = 0; j < DB / 2; ++j)
+            *reinterpret_cast<float4*>(sl + 32 * j) =
+                make_float4(o[2 * j][e], o[2 * j][2 + e], o[2 * j + 1][e], o[2 * j + 1][2 + e]);
+          continue;
+        }
         float* sl = slices + (cwarp * srows + row) * (DV + SP) + (lane >> 2);
 #pragma unroll
         for (int db = 0; db < DB; ++db) {
@@ -1119,7 +1243,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
 __global__ void __launch_bounds__(128) decode_walk_kernel(const DecodeParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_align1024(smem_raw);
-  const DecodeSmem L(0, p.B, p.Bv, 1, 1, 64, 4);
+  const DecodeSmem L(0, p.B, p.Bv, 1, 1, 64, 4, 2);
   const int* s_len = reinterpret_cast<const int*>(smem + L.seqlen);
   const int* s_nt = reinterpret_cast<const int*>(smem + L.nt);
   const int* s_pref = reinterpret_cast<const int*>(smem + L.pref);
@@ -1161,13 +1285,13 @@ __global__ void __launch_bounds__(128) decode_walk_kernel(const DecodeParams p) 
 
 }  // namespace
 
-int decode_smem_bytes(int nstages, int B, int Bv, int kpc, int g, int dv, int rel_es) {
-  return DecodeSmem(nstages, B, Bv, kpc, g, dv, rel_es).total + 1024;
+int decode_smem_bytes(int nstages, int B, int Bv, int kpc, int g, int dv, int rel_es, int kv_es) {
+  return DecodeSmem(nstages, B, Bv, kpc, g, dv, rel_es, kv_es).total + 1024;
 }
 
-template <int DV, bool MULTI, bool R16>
+template <int DV, bool MULTI, bool R16, bool KV8>
 static cudaError_t launch_decode_as(const DecodeLaunch& L, int smem, cudaStream_t stream) {
-  cudaError_t e = cudaFuncSetAttribute(decode_kernel<DV, MULTI, R16>,
+  cudaError_t e = cudaFuncSetAttribute(decode_kernel<DV, MULTI, R16, KV8>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   // Programmatic stream serialisation: the kernel may begin while the
@@ -1182,19 +1306,26 @@ static cudaError_t launch_decode_as(const DecodeLaunch& L, int smem, cudaStream_
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_kernel<DV, MULTI, R16>, L.tm_q, L.tm_k, L.tm_v,
+  return cudaLaunchKernelEx(&cfg, decode_kernel<DV, MULTI, R16, KV8>, L.tm_q, L.tm_k, L.tm_v,
                             L.tm_rel, L.p);
 }
 
 template <int DV, bool MULTI>
 static cudaError_t launch_decode_rel(const DecodeLaunch& L, int smem, cudaStream_t stream) {
-  return L.p.rel_es == 2 ? launch_decode_as<DV, MULTI, true>(L, smem, stream)
-                         : launch_decode_as<DV, MULTI, false>(L, smem, stream);
+  if constexpr (!MULTI && DV == 128) {  // e4m3 caches: the one-token kernel, d_v = 128
+    if (L.p.kv_es == 1)
+      return L.p.rel_es == 2 ? launch_decode_as<DV, MULTI, true, true>(L, smem, stream)
+                             : launch_decode_as<DV, MULTI, false, true>(L, smem, stream);
+  }
+  if (L.p.kv_es != 2) return cudaErrorInvalidValue;  // the host refuses these first
+  return L.p.rel_es == 2 ? launch_decode_as<DV, MULTI, true, false>(L, smem, stream)
+                         : launch_decode_as<DV, MULTI, false, false>(L, smem, stream);
 }
 
 cudaError_t launch_decode(const DecodeLaunch& L, cudaStream_t stream) {
   const DecodeParams& p = L.p;
-  const int smem = decode_smem_bytes(p.nstages, p.B, p.Bv, p.kpc, p.g, p.dv, p.rel_es);
+  const int smem =
+      decode_smem_bytes(p.nstages, p.B, p.Bv, p.kpc, p.g, p.dv, p.rel_es, p.kv_es);
   const bool multi = decode_multi_kernel(p.k, p.g);
   if (p.dv == 128)
     return multi ? launch_decode_rel<128, true>(L, smem, stream)
@@ -1204,7 +1335,7 @@ cudaError_t launch_decode(const DecodeLaunch& L, cudaStream_t stream) {
 }
 
 cudaError_t launch_decode_walk(const DecodeParams& p, int grid, cudaStream_t stream) {
-  const int smem = decode_smem_bytes(0, p.B, p.Bv, 1, 1, 64, 4);
+  const int smem = decode_smem_bytes(0, p.B, p.Bv, 1, 1, 64, 4, 2);
   cudaError_t e = cudaFuncSetAttribute(decode_walk_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;

@@ -27,6 +27,9 @@ struct DecodeParams {
   const float* gate;           // [B][k][Hq] gate logits, or null
   int rel_es;                  // bytes per rel element: 4 (fp32) or 2 (bf16)
   int out_f32;                 // 1: out is fp32
+  int kv_es;                   // bytes per cache element: 2 (bf16) or 1 (e4m3)
+  float v_scale;               // e4m3 cache: its value scale (1 for bf16); the key
+                               // scale is folded into scale_log2
   uint32_t* status;            // workspace status word
   int32_t* counters;           // [B][Hkv] split-combine arrival counters
   float* part_lse;             // [2*grid][g] base-2 log-sum-exp of a piece
@@ -79,7 +82,7 @@ struct PrefillLaunch {
   int grid;
 };
 
-int decode_smem_bytes(int nstages, int B, int Bv, int kpc, int g, int dv, int rel_es);
+int decode_smem_bytes(int nstages, int B, int Bv, int kpc, int g, int dv, int rel_es, int kv_es);
 constexpr int kMaxDecodeRows = 16;         // rows of one decode tile: g heads x tokens
 // The decode kernel has a one-token instantiation for tiles of at most 8 rows
 // and a general one (several tokens, or g > 8), which also takes its query

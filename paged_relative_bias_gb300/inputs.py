@@ -37,7 +37,9 @@ class DecodeWorkload:
     max_blocks_per_seq: int = 0  # 0: the longest sequence's block count
     query_tokens: int = 0  # > 0: multi-token decode, q [B, k, Hq, d], rel [B, k, Hq, E]
     rel_dtype: str = "f32"  # "bf16": rel drawn in fp32 and rounded to bf16
-    kv_dtype: str = "bf16"  # "fp8": caches quantised to e4m3 with one scale each
+    # "fp8": caches quantised to e4m3 with one scale each, head-major blocks
+    # [pool, Hkv, 128, d] (a token's head row is only 128 bytes)
+    kv_dtype: str = "bf16"
 
 
 @dataclass(frozen=True)
@@ -171,9 +173,9 @@ def make_decode(wl: DecodeWorkload, device="cpu", seed_data: int = 0,
     k_cache = _randn((pool, BLOCK_SIZE, Hkv, wl.d_qk), g, device, torch.bfloat16)
     v_cache = _randn((pool, BLOCK_SIZE, Hkv, wl.d_v), g, device, torch.bfloat16)
     scales = {}
-    if wl.kv_dtype == "fp8":
-        k_cache, scales["k_scale"] = quantize_e4m3(k_cache)
-        v_cache, scales["v_scale"] = quantize_e4m3(v_cache)
+    if wl.kv_dtype == "fp8":  # head-major blocks: [pool, Hkv, 128, d]
+        k_cache, scales["k_scale"] = quantize_e4m3(k_cache.transpose(1, 2).contiguous())
+        v_cache, scales["v_scale"] = quantize_e4m3(v_cache.transpose(1, 2).contiguous())
     return dict(
         q=q, rel=rel, k_cache=k_cache, v_cache=v_cache,
         block_table=table.to(device),

@@ -10,7 +10,7 @@ from __future__ import annotations
 
 import ctypes
 import os
-from ctypes import POINTER, c_char_p, c_int, c_int32, c_size_t, c_uint32, c_void_p
+from ctypes import POINTER, c_char_p, c_float, c_int, c_int32, c_size_t, c_uint32, c_void_p
 
 import torch
 
@@ -44,6 +44,8 @@ EXPORTS = (
 
 DTYPE_F32 = 0
 DTYPE_BF16 = 1
+DTYPE_E4M3 = 2
+_CACHE_DTYPES = (torch.bfloat16, torch.float8_e4m3fn)
 _DTYPE_CODE = {torch.float32: DTYPE_F32, torch.bfloat16: DTYPE_BF16}
 
 
@@ -60,7 +62,8 @@ class Dims(ctypes.Structure):
 
 
 class Options(ctypes.Structure):
-    _fields_ = [("rel", c_int32), ("out", c_int32), ("sink", c_void_p), ("gate", c_void_p)]
+    _fields_ = [("rel", c_int32), ("out", c_int32), ("sink", c_void_p), ("gate", c_void_p),
+                ("kv", c_int32), ("k_scale", c_float), ("v_scale", c_float)]
 
 
 class RelattnError(RuntimeError):
@@ -162,6 +165,12 @@ def _need(t: torch.Tensor, name: str, dtype, dims: int, device) -> None:
 
 
 def cache_desc(k_cache: torch.Tensor, v_cache: torch.Tensor) -> KVCacheDesc:
+    """bf16 caches are [NB, 128, Hkv, d]; e4m3 caches are head-major,
+    [NB, Hkv, 128, d]."""
+    if k_cache.dtype == torch.float8_e4m3fn:
+        return KVCacheDesc(k_cache.data_ptr(), v_cache.data_ptr(), k_cache.shape[0],
+                           k_cache.shape[2], k_cache.shape[1], k_cache.shape[3],
+                           v_cache.shape[3])
     return KVCacheDesc(k_cache.data_ptr(), v_cache.data_ptr(), k_cache.shape[0],
                        k_cache.shape[1], k_cache.shape[2], k_cache.shape[3],
                        v_cache.shape[3])
@@ -198,8 +207,10 @@ def decode_dims(q, block_table, num_ctas=0) -> Dims:
     return Dims(q.shape[0], q.shape[1], block_table.shape[1], 0, 0, num_ctas)
 
 
-def _options(rel, out_dtype, sink=None, gate=None, rows_shape=None, device=None) -> Options:
-    """The *_ex options; sink / gate are float32 [rows..., Hq] tensors or None."""
+def _options(rel, out_dtype, sink=None, gate=None, rows_shape=None, device=None,
+             k_cache=None, k_scale=None, v_scale=None) -> Options:
+    """The *_ex options; sink / gate are float32 [rows..., Hq] tensors or None;
+    an e4m3 cache (float8_e4m3fn tensors) needs its two scales."""
     if rel.dtype not in _DTYPE_CODE:
         raise TypeError(f"rel must be float32 or bfloat16, got {rel.dtype}")
     if out_dtype not in _DTYPE_CODE:
@@ -209,25 +220,40 @@ def _options(rel, out_dtype, sink=None, gate=None, rows_shape=None, device=None)
             _need(t, name, torch.float32, len(rows_shape), device)
             if tuple(t.shape) != tuple(rows_shape):
                 raise ValueError(f"{name} must be {list(rows_shape)}, got {tuple(t.shape)}")
-    return Options(_DTYPE_CODE[rel.dtype], _DTYPE_CODE[out_dtype], _ptr(sink), _ptr(gate))
+    kv, ks, vs = DTYPE_BF16, 1.0, 1.0
+    if k_cache is not None and k_cache.dtype == torch.float8_e4m3fn:
+        if k_scale is None or v_scale is None:
+            raise ValueError("an e4m3 cache needs k_scale and v_scale")
+        kv, ks, vs = DTYPE_E4M3, float(k_scale), float(v_scale)
+    return Options(_DTYPE_CODE[rel.dtype], _DTYPE_CODE[out_dtype], _ptr(sink), _ptr(gate), kv,
+                   ks, vs)
 
 
-def _plain(rel, out_dtype, sink, gate) -> bool:
+def _need_cache(k_cache, v_cache, device) -> None:
+    if k_cache.dtype not in _CACHE_DTYPES or v_cache.dtype != k_cache.dtype:
+        raise TypeError("k_cache / v_cache must both be bfloat16 or both float8_e4m3fn")
+    _need(k_cache, "k_cache", k_cache.dtype, 4, device)
+    _need(v_cache, "v_cache", v_cache.dtype, 4, device)
+
+
+def _plain(rel, out_dtype, sink, gate, k_cache=None) -> bool:
     return (rel.dtype == torch.float32 and out_dtype == torch.bfloat16 and sink is None
-            and gate is None)
+            and gate is None and (k_cache is None or k_cache.dtype == torch.bfloat16))
 
 
 def relattn_decode(q, rel, k_cache, v_cache, block_table, seq_lens, window: int,
                    rel_extent: int, out=None, workspace=None, num_ctas: int = 0,
-                   out_dtype=torch.bfloat16, sink=None, gate=None):
+                   out_dtype=torch.bfloat16, sink=None, gate=None, k_scale=None,
+                   v_scale=None):
     """Paged relative-bias decode; see ``relattn_decode`` in include/relattn.h.
 
     rel may be float32 or bfloat16 and out bfloat16 or float32 (``out``'s own
     dtype when it is given); sink / gate are optional float32 [B, Hq] logits
-    (the gated output with a sink).  Anything but fp32 rel, bf16 out and no
-    sink or gate goes through ``relattn_decode_ex``.
+    (the gated output with a sink); float8_e4m3fn caches take k_scale and
+    v_scale.  Anything but fp32 rel, bf16 out, a bf16 cache and no sink or
+    gate goes through ``relattn_decode_ex``.
     """
-    if not _plain(rel, out.dtype if out is not None else out_dtype, sink, gate):
+    if not _plain(rel, out.dtype if out is not None else out_dtype, sink, gate, k_cache):
         if q.dim() != 3 or rel.dim() != 3:
             raise ValueError("q must be [B, Hq, d_qk] and rel [B, Hq, rel_extent]")
         o = relattn_decode_multi(q[:, None], rel[:, None], k_cache, v_cache, block_table,
@@ -235,7 +261,8 @@ def relattn_decode(q, rel, k_cache, v_cache, block_table, seq_lens, window: int,
                                  out=None if out is None else out[:, None],
                                  workspace=workspace, num_ctas=num_ctas, out_dtype=out_dtype,
                                  sink=None if sink is None else sink[:, None],
-                                 gate=None if gate is None else gate[:, None])
+                                 gate=None if gate is None else gate[:, None],
+                                 k_scale=k_scale, v_scale=v_scale)
         return o[:, 0]
     dev = q.device
     B, Hq, dqk = q.shape
@@ -293,7 +320,8 @@ def relattn_decode_noalloc(q, rel, k_cache, v_cache, block_table, seq_lens, wind
 
 def relattn_decode_multi(q, rel, k_cache, v_cache, block_table, seq_lens, window: int,
                          rel_extent: int, out=None, workspace=None, num_ctas: int = 0,
-                         out_dtype=torch.bfloat16, sink=None, gate=None):
+                         out_dtype=torch.bfloat16, sink=None, gate=None, k_scale=None,
+                         v_scale=None):
     """Decode of k query tokens per sequence (speculative verification).
 
     q is [B, k, Hq, d_qk], rel [B, k, Hq, rel_extent], out [B, k, Hq, d_v];
@@ -305,10 +333,9 @@ def relattn_decode_multi(q, rel, k_cache, v_cache, block_table, seq_lens, window
     _need(q, "q", torch.bfloat16, 4, dev)
     B, kq, Hq, _ = q.shape
     out_dtype = out.dtype if out is not None else out_dtype
-    io = _options(rel, out_dtype, sink, gate, (B, kq, Hq), dev)
+    io = _options(rel, out_dtype, sink, gate, (B, kq, Hq), dev, k_cache, k_scale, v_scale)
     _need(rel, "rel", rel.dtype, 4, dev)
-    _need(k_cache, "k_cache", torch.bfloat16, 4, dev)
-    _need(v_cache, "v_cache", torch.bfloat16, 4, dev)
+    _need_cache(k_cache, v_cache, dev)
     _need(block_table, "block_table", torch.int32, 2, dev)
     _need(seq_lens, "seq_lens", torch.int32, 1, dev)
     if tuple(rel.shape) != (B, kq, Hq, rel_extent):
@@ -323,7 +350,7 @@ def relattn_decode_multi(q, rel, k_cache, v_cache, block_table, seq_lens, window
         _need(out, "out", out_dtype, 4, dev)
     if workspace is None:
         workspace = new_workspace(workspace_size(dims, cache), dev)
-    if _plain(rel, out_dtype, sink, gate):
+    if _plain(rel, out_dtype, sink, gate, k_cache):
         _check(lib().relattn_decode_multi(
             q.data_ptr(), rel.data_ptr(), ctypes.byref(cache), block_table.data_ptr(),
             seq_lens.data_ptr(), int(kq), int(window), int(rel_extent), ctypes.byref(dims),

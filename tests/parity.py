@@ -32,9 +32,10 @@ def to_f64(t: torch.Tensor) -> np.ndarray:
 
 
 def host_cache(t: torch.Tensor):
-    """A KV cache for the oracle: bf16 or e4m3 bit patterns."""
+    """A KV cache for the oracle ([NB, 128, Hkv, d]): bf16 bit patterns, or
+    the e4m3 bit patterns of a head-major [NB, Hkv, 128, d] e4m3 cache."""
     if t.dtype == torch.float8_e4m3fn:
-        return t.view(torch.uint8).cpu().numpy()
+        return t.view(torch.uint8).transpose(1, 2).contiguous().cpu().numpy()
     return bf16_bits(t)
 
 

@@ -1,0 +1,118 @@
+"""GPU decode over an FP8 (e4m3) KV cache with per-tensor scales, vs the oracle.
+
+The caches are quantised to e4m3 with one scale each (the input generator);
+the oracle reads the e4m3 patterns exactly and applies the scales, so the
+same tolerance as the bf16 cache applies.  The kernel widens K and V to f16
+in shared memory and runs its MMAs in f16.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from paged_relative_bias_gb300 import inputs as I
+from paged_relative_bias_gb300 import relattn as R
+from tests.parity import assert_parity, oracle_decode, to_f64
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from paged_relative_bias_gb300 import build
+    build.build()
+    R.lib()
+
+
+def run(case, num_ctas=0, out_dtype=torch.bfloat16):
+    q = case["q"]
+    dims = R.Dims(q.shape[0], q.shape[-2], case["block_table"].shape[1], 0, 0, num_ctas)
+    ws = R.new_workspace(R.workspace_size(dims, R.cache_desc(case["k_cache"],
+                                                             case["v_cache"])), DEV)
+    fn = R.relattn_decode_multi if q.dim() == 4 else R.relattn_decode
+    out = fn(q, case["rel"], case["k_cache"], case["v_cache"], case["block_table"],
+             case["seq_lens"], case["window"], case["rel_extent"], workspace=ws,
+             num_ctas=num_ctas, out_dtype=out_dtype, sink=case.get("sink"),
+             gate=case.get("gate"), k_scale=case.get("k_scale"), v_scale=case.get("v_scale"))
+    torch.cuda.synchronize()
+    assert R.read_status(ws) == 0
+    return out
+
+
+def fp8(wl, **kw):
+    return I.variant(wl, kv_dtype="fp8", **kw)
+
+
+SMALL = {
+    "local_w512": fp8(I.WORKLOADS["local_decode"], batch=5, lengths=("uniform", 1, 3000),
+                      pool_blocks=0, max_blocks_per_seq=0),
+    "global_e1024": fp8(I.WORKLOADS["global_decode_b8"], batch=3, lengths=("uniform", 1, 6000)),
+    "mha_g1": fp8(I.DecodeWorkload("mha_g1", 3, 4, 4, 128, 128, 0, 64, ("uniform", 1, 900))),
+    "gqa6_w100_e64": fp8(I.DecodeWorkload("gqa6", 4, 12, 2, 128, 128, 100, 64,
+                                          ("uniform", 1, 1500))),
+    "gqa8": fp8(I.DecodeWorkload("gqa8", 3, 64, 8, 128, 128, 0, 1024,
+                                 ("loguniform", 64, 5000))),
+}
+
+
+@pytest.mark.parametrize("name", sorted(SMALL))
+def test_fp8_decode_small_configs(name):
+    case = I.make_decode(SMALL[name], DEV, seed_data=111, seed_layout=112)
+    assert case["k_cache"].dtype == torch.float8_e4m3fn
+    assert_parity(to_f64(run(case)), oracle_decode(case), what=name)
+
+
+EDGE_LENS = [1, 2, 63, 64, 65, 127, 128, 129, 255, 256, 257, 511, 512, 513, 1023, 1024, 1025]
+
+
+@pytest.mark.parametrize("window,extent", [(0, 1024), (512, 512), (128, 64), (1, 4)])
+def test_fp8_decode_edge_lengths(window, extent):
+    wl = fp8(I.DecodeWorkload("edge", len(EDGE_LENS), 32, 8, 128, 128, window, extent,
+                              ("list", EDGE_LENS)))
+    case = I.make_decode(wl, DEV, seed_data=113)
+    assert_parity(to_f64(run(case)), oracle_decode(case), what=f"W={window} E={extent}")
+
+
+@pytest.mark.parametrize("num_ctas", [1, 7, 152, 1000])
+def test_fp8_decode_any_split(num_ctas):
+    wl = fp8(I.DecodeWorkload("split", 6, 16, 4, 128, 128, 0, 256, ("uniform", 1, 4000)))
+    case = I.make_decode(wl, DEV, seed_data=114)
+    assert_parity(to_f64(run(case, num_ctas=num_ctas)), oracle_decode(case),
+                  what=f"num_ctas={num_ctas}")
+
+
+def test_fp8_with_bf16_rel_fp32_out_sink_and_gate():
+    wl = fp8(SMALL["local_w512"], rel_dtype="bf16")
+    case = I.make_decode(wl, DEV, seed_data=115)
+    B, Hq = case["q"].shape[:2]
+    g = torch.Generator(device="cpu")
+    g.manual_seed(116)
+    case["sink"] = torch.randn((B, Hq), generator=g).to(DEV)
+    case["gate"] = torch.randn((B, Hq), generator=g).to(DEV)
+    out = run(case, out_dtype=torch.float32)
+    assert_parity(to_f64(out), oracle_decode(case), what="fp8 + bf16 rel + sink/gate")
+
+
+def test_fp8_decode_full_size_global_b8_sampled():
+    case = I.make_decode(fp8(I.WORKLOADS["global_decode_b8"]), DEV, seed_data=0)
+    out = run(case)
+    bs, hs = [0, 3, 7], [0, 9, 31]
+    want = oracle_decode(case, batch=bs, heads=hs)
+    assert_parity(to_f64(out)[np.ix_(bs, hs)], want[np.ix_(bs, hs)], what="global b8 fp8")
+
+
+@pytest.mark.parametrize("what", ["multi_token", "dv64", "g16"])
+def test_fp8_unsupported_shapes_are_refused(what):
+    if what == "multi_token":
+        wl = fp8(I.DecodeWorkload("m", 2, 16, 4, 128, 128, 0, 64, ("uniform", 4, 300),
+                                  query_tokens=4))
+    elif what == "dv64":
+        wl = fp8(I.DecodeWorkload("d", 2, 16, 4, 128, 64, 0, 64, ("uniform", 1, 300)))
+    else:
+        wl = fp8(I.DecodeWorkload("g", 2, 32, 2, 128, 128, 0, 64, ("uniform", 1, 300)))
+    case = I.make_decode(wl, DEV, seed_data=117)
+    with pytest.raises(R.RelattnError) as e:
+        run(case)
+    assert e.value.code == R.ERR_UNSUPPORTED
