@@ -54,6 +54,14 @@ there is no blocking, fusion or reordering):
   head) whose sigmoid multiplies that head's output.  Both are inputs; the
   projections that produce them are outside attention.
 
+* Log-position scale (optional): global layers scale q and the rel logits
+  by a factor that grows with the log of the position beyond 128K ("Inkling-
+  Small on Gaudi 2", section "What was built").  Reading (no formula is
+  given): one positive factor per query token multiplies both terms of its
+  logits, ``s_i * (q_i . k_j / sqrt(d_qk) + rel[i, h, P_i - j])``; the factor
+  is an input (1 below 128K), computed by the model, and a sink logit is not
+  scaled.
+
 * FP8 KV cache (optional, decode): keys and values stored as e4m3 (1 sign,
   4 exponent bits with bias 7, 3 mantissa bits, no infinities) times one
   scale per cache ("vLLM TML Inkling Support": FP8 global attention is on
@@ -246,13 +254,16 @@ def softmax_weights(s) -> np.ndarray:
     return w / w.sum()
 
 
-def attend(q_vec, K, V, bias, d_qk: int, sink=None, gate=None) -> np.ndarray:
+def attend(q_vec, K, V, bias, d_qk: int, sink=None, gate=None, scale=None) -> np.ndarray:
     """Output of one query: softmax(logits) @ V.
 
-    With a sink logit s the weights are exp(l_j) / (sum_j exp(l_j) + exp(s));
-    with a gate logit g the output is multiplied by 1 / (1 + exp(-g)).
+    With a log-position factor the logits are ``scale * logits``; with a
+    sink logit s the weights are exp(l_j) / (sum_j exp(l_j) + exp(s)); with a
+    gate logit g the output is multiplied by 1 / (1 + exp(-g)).
     """
     s = logits(q_vec, K, bias, d_qk)
+    if scale is not None:
+        s = float(scale) * s
     if sink is None:
         w = softmax_weights(s)
     else:
@@ -292,10 +303,11 @@ def merge_partials(outs, lses) -> np.ndarray:
 
 def decode(q, rel, k_cache, v_cache, block_table, seq_lens, window: int,
            rel_extent: int, batch=None, heads=None, sink=None, gate=None, k_scale=1.0,
-           v_scale=1.0) -> np.ndarray:
+           v_scale=1.0, logit_scale=None) -> np.ndarray:
     """Paged decode: one query per sequence at position seq_lens[b] - 1.
 
-    ``sink`` / ``gate``: optional [B, Hq] logits (see ``attend``);
+    ``sink`` / ``gate``: optional [B, Hq] logits, ``logit_scale``: optional
+    [B] log-position factors (see ``attend``);
     ``k_scale`` / ``v_scale``: the scales of an FP8 cache.  Returns
     float64 [B, Hq, d_v]; rows/heads not selected by ``batch`` / ``heads``
     are left NaN.
@@ -320,13 +332,14 @@ def decode(q, rel, k_cache, v_cache, block_table, seq_lens, window: int,
                 bias = rel_bias(rel[b, h], P, keys, rel_extent)
                 out[b, h] = attend(q[b, h], K, V, bias, d_qk,
                                    None if sink is None else sink[b, h],
-                                   None if gate is None else gate[b, h])
+                                   None if gate is None else gate[b, h],
+                                   None if logit_scale is None else logit_scale[b])
     return out
 
 
 def decode_multi(q, rel, k_cache, v_cache, block_table, seq_lens, window: int,
                  rel_extent: int, batch=None, tokens=None, heads=None, sink=None,
-                 gate=None, k_scale=1.0, v_scale=1.0) -> np.ndarray:
+                 gate=None, k_scale=1.0, v_scale=1.0, logit_scale=None) -> np.ndarray:
     """Multi-token decode, the verification step of speculative decoding.
 
     The k newest tokens of sequence b each attend over the paged cache:
@@ -341,7 +354,7 @@ def decode_multi(q, rel, k_cache, v_cache, block_table, seq_lens, window: int,
     the one token of a decode step.
 
     q ``[B, k, Hq, d_qk]``, rel ``[B, k, Hq, E]``, optional ``sink`` /
-    ``gate`` ``[B, k, Hq]``.  Returns float64 ``[B, k, Hq, d_v]``; entries not
+    ``gate`` ``[B, k, Hq]`` and ``logit_scale`` ``[B, k]``.  Returns float64 ``[B, k, Hq, d_v]``; entries not
     selected by ``batch`` / ``tokens`` / ``heads`` are left NaN.
     """
     B, kq, Hq, d_qk = q.shape
@@ -366,19 +379,21 @@ def decode_multi(q, rel, k_cache, v_cache, block_table, seq_lens, window: int,
                     bias = rel_bias(rel[b, i, h], P, keys, rel_extent)
                     out[b, i, h] = attend(q[b, i, h], K, V, bias, d_qk,
                                           None if sink is None else sink[b, i, h],
-                                          None if gate is None else gate[b, i, h])
+                                          None if gate is None else gate[b, i, h],
+                                          None if logit_scale is None else logit_scale[b, i])
     return out
 
 
 def prefill(q, k, v, rel, cu_seqlens, k_cache, v_cache, block_table,
-            ctx_lens, window: int, rel_extent: int, rows=None, sink=None, gate=None):
+            ctx_lens, window: int, rel_extent: int, rows=None, sink=None, gate=None,
+            logit_scale=None):
     """Chunked prefill against the paged cache.
 
     Writes the new keys/values into copies of the caches, then attends each
     new token (position ctx_lens[b] + t) over the cached prefix plus the new
     tokens, causal and windowed.  ``rows`` selects packed token rows to
-    compute (default: all); ``sink`` / ``gate``: optional [T, Hq] logits (see
-    ``attend``).  Returns (out float64 [T, Hq, d_v] with unselected rows NaN,
+    compute (default: all); ``sink`` / ``gate``: optional [T, Hq] logits,
+    ``logit_scale``: optional [T] log-position factors (see ``attend``).  Returns (out float64 [T, Hq, d_v] with unselected rows NaN,
     k_cache', v_cache').
     """
     T, Hq, d_qk = q.shape
@@ -405,7 +420,8 @@ def prefill(q, k, v, rel, cu_seqlens, k_cache, v_cache, block_table,
                     bias = rel_bias(rel[row, h], P, keys, rel_extent)
                     out[row, h] = attend(q[row, h], K, V, bias, d_qk,
                                          None if sink is None else sink[row, h],
-                                         None if gate is None else gate[row, h])
+                                         None if gate is None else gate[row, h],
+                                         None if logit_scale is None else logit_scale[row])
     return out, kc, vc
 
 

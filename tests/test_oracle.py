@@ -634,3 +634,68 @@ def test_fp8_decode_equals_decode_of_the_dequantised_cache():
     b = O.decode(c["q"], c["rel"], O.e4m3_bits_to_f64(kc8) * ks, O.e4m3_bits_to_f64(vc8) * vs,
                  c["table"], c["seq_lens"], 100, 64)
     assert np.array_equal(a, b)
+
+
+# ---------------------------------------------------------------------------
+# log-position scale
+# ---------------------------------------------------------------------------
+
+def test_logit_scale_of_one_is_the_plain_output():
+    c = random_decode_case(120, 300)
+    plain = O.decode(c["q"], c["rel"], c["kc"], c["vc"], c["table"], c["seq_lens"], 100, 64)
+    one = O.decode(c["q"], c["rel"], c["kc"], c["vc"], c["table"], c["seq_lens"], 100, 64,
+                   logit_scale=np.ones(1))
+    assert np.array_equal(one, plain)
+
+
+@pytest.mark.parametrize("W,E", [(0, 300), (100, 40)])
+def test_logit_scale_is_q_and_rel_scaled_in_float64_sdpa(W, E):
+    """Scaling q and the rel logits of each query token by its factor, then
+    plain float64 SDPA, gives the prefill with per-token factors."""
+    r = rng(121)
+    ctx, n, Hq, Hkv, d, dv = 150, 90, 6, 2, 16, 8
+    total = ctx + n
+    nblk = (total + 127) // 128
+    table = r.permutation(nblk + 1)[:nblk]
+    Kc = r.standard_normal((total, Hkv, d))
+    Vc = r.standard_normal((total, Hkv, dv))
+    kc, vc = paged_from_contiguous(Kc[:ctx], Vc[:ctx], table, nblk + 1)
+    q = r.standard_normal((n, Hq, d))
+    rel = r.standard_normal((n, Hq, E))
+    s = r.uniform(0.3, 3.0, n)
+    out, _, _ = O.prefill(q, Kc[ctx:], Vc[ctx:], rel, [0, n], kc, vc, table[None, :], [ctx],
+                          W, E, logit_scale=s)
+    ref = sdpa_reference(q * s[:, None, None], Kc, Vc, rel * s[:, None, None],
+                         [ctx + t for t in range(n)], W, E)
+    np.testing.assert_allclose(out, ref, atol=1e-12, rtol=0)
+
+
+@pytest.mark.parametrize("n,sink", [(1, 0.5), (300, -1.0), (77, 2.0)])
+def test_logit_scale_to_zero_gives_the_mean_and_leaves_the_sink_alone(n, sink):
+    """A vanishing factor makes every key's logit 0 while the sink logit
+    keeps its value: each weight tends to 1 / (n + e^sink)."""
+    c = random_decode_case(122 + n, n)
+    Hq = c["q"].shape[1]
+    out = O.decode(c["q"], c["rel"], c["kc"], c["vc"], c["table"], c["seq_lens"], 0, 64,
+                   sink=np.full((1, Hq), sink), logit_scale=np.array([1e-13]))
+    g = Hq // c["Kc"].shape[1]
+    for h in range(Hq):
+        want = c["Vc"][:, h // g].sum(0) / (n + math.exp(sink))
+        np.testing.assert_allclose(out[0, h], want, rtol=0, atol=1e-9)
+
+
+def test_logit_scale_rows_agree_across_decode_multi_and_prefill():
+    """Token i of a verification step with factor s_i equals a one-token
+    decode at its length with that factor, and the last row of a prefill."""
+    L, k = 260, 4
+    c = random_multi_case(125, L, k)
+    s = np.array([[0.5, 1.0, 1.7, 2.5]])
+    multi = O.decode_multi(c["qm"], c["relm"], c["kc"], c["vc"], c["table"], c["seq_lens"],
+                           64, 64, logit_scale=s)
+    for i in range(k):
+        dec = O.decode(c["qm"][:, i], c["relm"][:, i], c["kc"], c["vc"], c["table"],
+                       np.array([L - k + i + 1]), 64, 64, logit_scale=s[:, i])
+        np.testing.assert_allclose(multi[:, i], dec, atol=1e-13, rtol=0)
+    pre, _, _ = O.prefill(c["qm"][0], c["Kc"][L - k:L], c["Vc"][L - k:L], c["relm"][0], [0, k],
+                          c["kc"], c["vc"], c["table"], [L - k], 64, 64, logit_scale=s[0])
+    np.testing.assert_allclose(multi[0], pre, atol=1e-13, rtol=0)
