@@ -218,6 +218,17 @@ int relattn_decode_multi(const void* q, const float* rel,
  *    g = Hq/Hkv <= 8 and d_v = 128: RELATTN_ERR_UNSUPPORTED otherwise, and
  *    for relattn_prefill_ex.  k_scale and v_scale must be finite and > 0.
  */
+/*
+ *  - logit_scale: the log-position scale of the global layers, which
+ *    multiplies q and the rel logits by a factor growing with the log of the
+ *    position beyond 128K ("Inkling-Small on Gaudi 2", section "What was
+ *    built").  Reading (no formula on the pages): one factor s per query
+ *    token, an fp32 device array ([B][k] for decode, [T] for prefill) or
+ *    NULL for none, and the logit of that token becomes
+ *    s * (q . k / sqrt(d_qk) + rel); a sink logit is not scaled.  The model
+ *    computes the factors (1 below 128K).  Each must be finite and > 0 (not
+ *    checked: the library does not read device data on the host).
+ */
 typedef struct relattn_options {
   int32_t rel;       /* RELATTN_DTYPE_F32 or RELATTN_DTYPE_BF16 */
   int32_t out;       /* RELATTN_DTYPE_BF16 or RELATTN_DTYPE_F32 */
@@ -226,6 +237,7 @@ typedef struct relattn_options {
   int32_t kv;        /* 0 / RELATTN_DTYPE_BF16, or RELATTN_DTYPE_E4M3 */
   float k_scale;     /* e4m3 cache: key scale */
   float v_scale;     /* e4m3 cache: value scale */
+  const float* logit_scale; /* NULL, or [rows] fp32 per-token logit factors */
 } relattn_options;
 
 /*

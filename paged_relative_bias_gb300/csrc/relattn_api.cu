@@ -227,21 +227,25 @@ struct IoTypes {
   const float* gate;  // per (query row, head) gate logits, or null
   int kv_es;          // bytes per cache element: 2 (bf16) or 1 (e4m3)
   float k_scale, v_scale;
+  const float* logit_scale;  // per query token logit factors, or null
 };
-constexpr IoTypes kDefaultIo = {4, 0, nullptr, nullptr, 2, 1.f, 1.f};
+constexpr IoTypes kDefaultIo = {4, 0, nullptr, nullptr, 2, 1.f, 1.f, nullptr};
 
 // From the C ABI's options; false for a value that is not offered (an
-// unknown type code, or a sink / gate pointer not 4-byte aligned).
+// unknown type code, or a sink / gate / logit_scale pointer not 4-byte
+// aligned).
 static bool io_types(const relattn_options* t, IoTypes* io) {
   if (!t) return false;
   if (t->rel != RELATTN_DTYPE_F32 && t->rel != RELATTN_DTYPE_BF16) return false;
   if (t->out != RELATTN_DTYPE_F32 && t->out != RELATTN_DTYPE_BF16) return false;
-  if ((reinterpret_cast<uintptr_t>(t->sink) & 3u) || (reinterpret_cast<uintptr_t>(t->gate) & 3u))
+  if ((reinterpret_cast<uintptr_t>(t->sink) & 3u) || (reinterpret_cast<uintptr_t>(t->gate) & 3u) ||
+      (reinterpret_cast<uintptr_t>(t->logit_scale) & 3u))
     return false;
   io->rel_es = t->rel == RELATTN_DTYPE_BF16 ? 2 : 4;
   io->out_f32 = t->out == RELATTN_DTYPE_F32 ? 1 : 0;
   io->sink = t->sink;
   io->gate = t->gate;
+  io->logit_scale = t->logit_scale;
   if (t->kv == 0 || t->kv == RELATTN_DTYPE_BF16) {
     io->kv_es = 2;
     io->k_scale = io->v_scale = 1.f;
@@ -310,6 +314,7 @@ static int prepare_decode(const void* q, const void* rel, IoTypes io,
   p.out = out;
   p.sink = io.sink;
   p.gate = io.gate;
+  p.logit_scale = io.logit_scale;
   p.rel_es = io.rel_es;
   p.out_f32 = io.out_f32;
   p.kv_es = io.kv_es;
@@ -522,6 +527,7 @@ static int prepare_prefill(const void* q, const void* k, const void* v, const vo
   p.out = out;
   p.sink = io.sink;
   p.gate = io.gate;
+  p.logit_scale = io.logit_scale;
   p.rel_es = io.rel_es;
   p.out_f32 = io.out_f32;
   p.status = static_cast<uint32_t*>(workspace);

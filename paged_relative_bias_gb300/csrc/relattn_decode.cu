@@ -77,15 +77,6 @@ __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
-// Two e4m3 values (low byte first) -> f16 pair (low half first), exactly,
-// in one conversion instruction.
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
-  uint32_t r;
-  const unsigned short in = static_cast<unsigned short>(two);
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(in));
-  return r;
-}
-
 // Four e4m3 values (one 32-bit word, low byte first) -> two f16 pairs: bytes
 // 0-1 in lo, bytes 2-3 in hi.
 __device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t four, uint32_t& lo, uint32_t& hi) {
@@ -542,9 +533,10 @@ __device__ Plan decode_prologue(const DecodeParams& p, uint8_t* smem, const Deco
 }
 
 // R16: rel is bf16 (else fp32).  KV8: the cache is e4m3 (one-token kernel
-// only); each consumer warp widens its keys' K and V rows and the query rows
-// to f16 in its own buffers, and the MMAs take f16 operands.
-template <int DV, bool MULTI, bool R16, bool KV8>
+// only); the consumer warps widen its bytes to f16 in registers and the MMAs
+// take f16 operands.  LS: per-token logit factors are given (general kernel
+// only: the one-token kernel reads them whenever they are given, at no cost).
+template <int DV, bool MULTI, bool R16, bool KV8, bool LS>
 __global__ void __launch_bounds__(kDecodeThreads, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tm_q,
                   const __grid_constant__ CUtensorMap tm_k,
@@ -565,6 +557,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   // rows 2 cq apart by 2 (DV + 4) = 8 banks mod 32) or of O rows (NB = 2)
   constexpr int SP = NB == 1 ? 4 : kSlicePad;
   static_assert(!(KV8 && MULTI), "e4m3 caches: one-token kernel only");
+  static_assert(!LS || MULTI, "logit factors: a template case of the general kernel only");
   const DecodeSmem L(ns, p.B, p.Bv, tok.kpc, g, DV, RES, KV8 ? 1 : 2);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
   uint64_t* empty = full + ns;
@@ -794,6 +787,21 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       rrel[rr] = ti * (rel_stride / RES) + (row - ti * g) * RW;
     }
     const int lo_last = window_lo(sq.pl, p.window);
+    // The log-position factor f of a row's token scales both terms of its
+    // logits.  One-token kernel (all rows one token): f goes into the two
+    // logit constants.  General kernel: the logits x stay unscaled and f
+    // enters the softmax, exp2(f (x - m)), with m the running max of x
+    // (f > 0), and the row's m is reported as f m.
+    float fr[2] = {1.f, 1.f};
+    if ((LS || !MULTI) && p.logit_scale != nullptr) {
+#pragma unroll
+      for (int rr = 0; rr < 2; ++rr) {
+        const int ti = NB == 1 ? 0 : tok.token_of_row(r0 + 8 * rr, g);
+        if (NB == 1 || rv[rr])
+          fr[rr] = __ldg(p.logit_scale + static_cast<size_t>(sq.b) * p.k + sq.i0 + ti);
+      }
+    }
+    const float sl2 = p.scale_log2 * fr[0], bl2 = kLog2e * fr[0];  // one-token kernel
     const int qb = k & 1;
     if (!mbar_wait(&qfull[qb], (k >> 1) & 1)) {
       report(p.status, RELATTN_DEV_WAIT_TIMEOUT);
@@ -914,7 +922,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
             const int e = (i >> 1) * 8;
             float bias = 0.f;
             if (need_rel && row < g) bias = rel_f32(relt[row * RW + (sq.pf - kb - e - d0)]);
-            const float v = fmaf(sT[i], p.scale_log2, bias * kLog2e);
+            const float v = fmaf(sT[i], sl2, bias * bl2);
             x[i] = (e < mlo || e > mhi) ? kNegInf : v;
           }
           // online softmax of rows 2 cq + j over the warp's 16 keys: the 8
@@ -1040,14 +1048,15 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
             const float m_new = fmaxf(m_[rr], mx);
             const float m_use = m_new == kNegInf ? 0.f : m_new;
-            const float alpha = ex2(m_[rr] - m_use);
+            const float alpha = ex2((m_[rr] - m_use) * fr[rr]);
+            const float nmf = -m_use * fr[rr];
             m_[rr] = m_new;
             float sum = 0.f;
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
               for (int e = 0; e < 2; ++e) {
-                const float pv = ex2(x[nt][2 * rr + e] - m_use);
+                const float pv = ex2(fmaf(x[nt][2 * rr + e], fr[rr], nmf));
                 x[nt][2 * rr + e] = pv;
                 sum += pv;
               }
@@ -1105,7 +1114,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         l_[rr] += __shfl_xor_sync(0xffffffffu, l_[rr], 1);
         l_[rr] += __shfl_xor_sync(0xffffffffu, l_[rr], 2);
         if (cq == 0) {
-          s_m[cwarp * 16 + r0 + 8 * rr] = m_[rr];
+          s_m[cwarp * 16 + r0 + 8 * rr] = m_[rr] * fr[rr];
           s_l[cwarp * 16 + r0 + 8 * rr] = l_[rr];
         }
       }
@@ -1289,9 +1298,9 @@ int decode_smem_bytes(int nstages, int B, int Bv, int kpc, int g, int dv, int re
   return DecodeSmem(nstages, B, Bv, kpc, g, dv, rel_es, kv_es).total + 1024;
 }
 
-template <int DV, bool MULTI, bool R16, bool KV8>
+template <int DV, bool MULTI, bool R16, bool KV8, bool LS = false>
 static cudaError_t launch_decode_as(const DecodeLaunch& L, int smem, cudaStream_t stream) {
-  cudaError_t e = cudaFuncSetAttribute(decode_kernel<DV, MULTI, R16, KV8>,
+  cudaError_t e = cudaFuncSetAttribute(decode_kernel<DV, MULTI, R16, KV8, LS>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   // Programmatic stream serialisation: the kernel may begin while the
@@ -1306,7 +1315,7 @@ static cudaError_t launch_decode_as(const DecodeLaunch& L, int smem, cudaStream_
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_kernel<DV, MULTI, R16, KV8>, L.tm_q, L.tm_k, L.tm_v,
+  return cudaLaunchKernelEx(&cfg, decode_kernel<DV, MULTI, R16, KV8, LS>, L.tm_q, L.tm_k, L.tm_v,
                             L.tm_rel, L.p);
 }
 
@@ -1318,6 +1327,11 @@ static cudaError_t launch_decode_rel(const DecodeLaunch& L, int smem, cudaStream
                              : launch_decode_as<DV, MULTI, false, true>(L, smem, stream);
   }
   if (L.p.kv_es != 2) return cudaErrorInvalidValue;  // the host refuses these first
+  if constexpr (MULTI) {  // a copy with the logit factors, so the plain one keeps registers
+    if (L.p.logit_scale != nullptr)
+      return L.p.rel_es == 2 ? launch_decode_as<DV, MULTI, true, false, true>(L, smem, stream)
+                             : launch_decode_as<DV, MULTI, false, false, true>(L, smem, stream);
+  }
   return L.p.rel_es == 2 ? launch_decode_as<DV, MULTI, true, false>(L, smem, stream)
                          : launch_decode_as<DV, MULTI, false, false>(L, smem, stream);
 }

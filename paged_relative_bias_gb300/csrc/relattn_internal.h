@@ -25,6 +25,7 @@ struct DecodeParams {
   void* out;                   // [B][k][Hq][dv], bf16 or fp32 (out_f32)
   const float* sink;           // [B][k][Hq] sink logits, or null
   const float* gate;           // [B][k][Hq] gate logits, or null
+  const float* logit_scale;    // [B][k] per-token logit factors, or null
   int rel_es;                  // bytes per rel element: 4 (fp32) or 2 (bf16)
   int out_f32;                 // 1: out is fp32
   int kv_es;                   // bytes per cache element: 2 (bf16) or 1 (e4m3)
@@ -65,6 +66,7 @@ struct PrefillParams {
   void* out;                   // [T][Hq][dv], bf16 or fp32 (out_f32)
   const float* sink;           // [T][Hq] sink logits, or null
   const float* gate;           // [T][Hq] gate logits, or null
+  const float* logit_scale;    // [T] per-token logit factors, or null
   int rel_es;                  // bytes per rel element: 4 (fp32) or 2 (bf16)
   int out_f32;                 // 1: out is fp32
   uint32_t* status;

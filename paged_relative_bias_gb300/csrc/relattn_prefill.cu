@@ -485,8 +485,17 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       const int* trow = p.block_table + static_cast<size_t>(it.b) * p.max_blocks;
 
       // Scores in natural-log units: x = q.k / sqrt(d) + rel; exp2 takes
-      // log2(e) in its FFMA.
+      // log2(e) in its FFMA.  A row's log-position factor f multiplies x:
+      // it is folded into that log2(e) (l2f), and the lazy rescale moves the
+      // running max of x only past kRescaleNat / f, so f x stays within
+      // kRescaleNat of it.
       const float scale = scale_log2 * 0.69314718055994531f;
+      float l2f = kLog2e, grow_by = kRescaleNat;
+      if (p.logit_scale != nullptr && row_ok) {
+        const float f = __ldg(p.logit_scale + it.r0 + r);
+        l2f = kLog2e * f;
+        grow_by = kRescaleNat / f;
+      }
       const int dmax = p.window > 0 ? p.window - 1 : 0x7fffffff;  // visible d in [0, dmax]
       float m_used = kNegInf, l = 0.f;
       bool ok = true;
@@ -555,9 +564,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 #pragma unroll
         for (int c = 4; c < 64; ++c) mq[c & 3] = fmaxf(mq[c & 3], x[c]);
         const float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
-        const bool grow = mx > m_used + kRescaleNat;
+        const bool grow = mx > m_used + grow_by;
         const float m_new = grow ? mx : m_used;
-        const float alpha = (grow && m_used != kNegInf) ? ex2((m_used - m_new) * kLog2e) : 1.f;
+        const float alpha = (grow && m_used != kNegInf) ? ex2((m_used - m_new) * l2f) : 1.f;
         if (k > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
           // O must hold every earlier tile before it is rescaled.  PV of this
           // tile cannot start before P is written below, so O's barrier is at
@@ -577,13 +586,13 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         }
         l *= alpha;
         m_used = m_new;
-        const float mb = m_used == kNegInf ? 0.f : -m_used * kLog2e;
+        const float mb = m_used == kNegInf ? 0.f : -m_used * l2f;
         uint32_t pk[32];
         float sq[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          const float p0 = ex2(fmaf(x[2 * i], kLog2e, mb));
-          const float p1 = ex2(fmaf(x[2 * i + 1], kLog2e, mb));
+          const float p0 = ex2(fmaf(x[2 * i], l2f, mb));
+          const float p1 = ex2(fmaf(x[2 * i + 1], l2f, mb));
           sq[i & 3] += p0 + p1;
           pk[i] = pack_bf16(p0, p1);
         }
@@ -614,14 +623,15 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       // of a bf16 row.
       uint8_t* scr = slot_wait(e);
       if (!scr) { fail = true; break; }
-      // 1 / normaliser; the optional sink logit joins it (l and m_used are in
-      // natural-log units) and the optional gate's sigmoid scales the row
+      // 1 / normaliser; the optional sink logit (not scaled by the factor)
+      // joins it, against l's reference f m_used, and the optional gate's
+      // sigmoid scales the row
       float inv;
       {
         float den = l;
         const size_t qi = static_cast<size_t>(it.r0 + r) * p.Hq + it.h;
         if (p.sink != nullptr && row_ok)
-          den += ex2((__ldg(p.sink + qi) - m_used) * kLog2e);  // 0 for a sink of -inf
+          den += ex2(__ldg(p.sink + qi) * kLog2e - m_used * l2f);  // 0 for a sink of -inf
         inv = den > 0.f ? 1.f / den : 0.f;
         if (p.gate != nullptr && row_ok) inv /= 1.f + ex2(-__ldg(p.gate + qi) * kLog2e);
       }

@@ -63,7 +63,8 @@ class Dims(ctypes.Structure):
 
 class Options(ctypes.Structure):
     _fields_ = [("rel", c_int32), ("out", c_int32), ("sink", c_void_p), ("gate", c_void_p),
-                ("kv", c_int32), ("k_scale", c_float), ("v_scale", c_float)]
+                ("kv", c_int32), ("k_scale", c_float), ("v_scale", c_float),
+                ("logit_scale", c_void_p)]
 
 
 class RelattnError(RuntimeError):
@@ -208,9 +209,10 @@ def decode_dims(q, block_table, num_ctas=0) -> Dims:
 
 
 def _options(rel, out_dtype, sink=None, gate=None, rows_shape=None, device=None,
-             k_cache=None, k_scale=None, v_scale=None) -> Options:
-    """The *_ex options; sink / gate are float32 [rows..., Hq] tensors or None;
-    an e4m3 cache (float8_e4m3fn tensors) needs its two scales."""
+             k_cache=None, k_scale=None, v_scale=None, logit_scale=None) -> Options:
+    """The *_ex options; sink / gate are float32 [rows..., Hq] tensors or None,
+    logit_scale a float32 [rows...] tensor or None; an e4m3 cache
+    (float8_e4m3fn tensors) needs its two scales."""
     if rel.dtype not in _DTYPE_CODE:
         raise TypeError(f"rel must be float32 or bfloat16, got {rel.dtype}")
     if out_dtype not in _DTYPE_CODE:
@@ -220,13 +222,18 @@ def _options(rel, out_dtype, sink=None, gate=None, rows_shape=None, device=None,
             _need(t, name, torch.float32, len(rows_shape), device)
             if tuple(t.shape) != tuple(rows_shape):
                 raise ValueError(f"{name} must be {list(rows_shape)}, got {tuple(t.shape)}")
+    if logit_scale is not None:
+        _need(logit_scale, "logit_scale", torch.float32, len(rows_shape) - 1, device)
+        if tuple(logit_scale.shape) != tuple(rows_shape[:-1]):
+            raise ValueError(f"logit_scale must be {list(rows_shape[:-1])}, "
+                             f"got {tuple(logit_scale.shape)}")
     kv, ks, vs = DTYPE_BF16, 1.0, 1.0
     if k_cache is not None and k_cache.dtype == torch.float8_e4m3fn:
         if k_scale is None or v_scale is None:
             raise ValueError("an e4m3 cache needs k_scale and v_scale")
         kv, ks, vs = DTYPE_E4M3, float(k_scale), float(v_scale)
     return Options(_DTYPE_CODE[rel.dtype], _DTYPE_CODE[out_dtype], _ptr(sink), _ptr(gate), kv,
-                   ks, vs)
+                   ks, vs, _ptr(logit_scale))
 
 
 def _need_cache(k_cache, v_cache, device) -> None:
@@ -236,24 +243,27 @@ def _need_cache(k_cache, v_cache, device) -> None:
     _need(v_cache, "v_cache", v_cache.dtype, 4, device)
 
 
-def _plain(rel, out_dtype, sink, gate, k_cache=None) -> bool:
+def _plain(rel, out_dtype, sink, gate, k_cache=None, logit_scale=None) -> bool:
     return (rel.dtype == torch.float32 and out_dtype == torch.bfloat16 and sink is None
-            and gate is None and (k_cache is None or k_cache.dtype == torch.bfloat16))
+            and gate is None and logit_scale is None
+            and (k_cache is None or k_cache.dtype == torch.bfloat16))
 
 
 def relattn_decode(q, rel, k_cache, v_cache, block_table, seq_lens, window: int,
                    rel_extent: int, out=None, workspace=None, num_ctas: int = 0,
                    out_dtype=torch.bfloat16, sink=None, gate=None, k_scale=None,
-                   v_scale=None):
+                   v_scale=None, logit_scale=None):
     """Paged relative-bias decode; see ``relattn_decode`` in include/relattn.h.
 
     rel may be float32 or bfloat16 and out bfloat16 or float32 (``out``'s own
     dtype when it is given); sink / gate are optional float32 [B, Hq] logits
     (the gated output with a sink); float8_e4m3fn caches take k_scale and
-    v_scale.  Anything but fp32 rel, bf16 out, a bf16 cache and no sink or
-    gate goes through ``relattn_decode_ex``.
+    v_scale; logit_scale is an optional float32 [B] of log-position factors.
+    Anything but fp32 rel, bf16 out, a bf16 cache and none of the optional
+    inputs goes through ``relattn_decode_ex``.
     """
-    if not _plain(rel, out.dtype if out is not None else out_dtype, sink, gate, k_cache):
+    if not _plain(rel, out.dtype if out is not None else out_dtype, sink, gate, k_cache,
+                  logit_scale):
         if q.dim() != 3 or rel.dim() != 3:
             raise ValueError("q must be [B, Hq, d_qk] and rel [B, Hq, rel_extent]")
         o = relattn_decode_multi(q[:, None], rel[:, None], k_cache, v_cache, block_table,
@@ -262,7 +272,9 @@ def relattn_decode(q, rel, k_cache, v_cache, block_table, seq_lens, window: int,
                                  workspace=workspace, num_ctas=num_ctas, out_dtype=out_dtype,
                                  sink=None if sink is None else sink[:, None],
                                  gate=None if gate is None else gate[:, None],
-                                 k_scale=k_scale, v_scale=v_scale)
+                                 k_scale=k_scale, v_scale=v_scale,
+                                 logit_scale=None if logit_scale is None
+                                 else logit_scale[:, None])
         return o[:, 0]
     dev = q.device
     B, Hq, dqk = q.shape
@@ -321,19 +333,21 @@ def relattn_decode_noalloc(q, rel, k_cache, v_cache, block_table, seq_lens, wind
 def relattn_decode_multi(q, rel, k_cache, v_cache, block_table, seq_lens, window: int,
                          rel_extent: int, out=None, workspace=None, num_ctas: int = 0,
                          out_dtype=torch.bfloat16, sink=None, gate=None, k_scale=None,
-                         v_scale=None):
+                         v_scale=None, logit_scale=None):
     """Decode of k query tokens per sequence (speculative verification).
 
     q is [B, k, Hq, d_qk], rel [B, k, Hq, rel_extent], out [B, k, Hq, d_v];
     token i of sequence b sits at position seq_lens[b] - k + i.  rel may be
-    float32 or bfloat16, out bfloat16 or float32, and sink / gate optional
-    float32 [B, k, Hq] logits (``relattn_decode_ex``).
+    float32 or bfloat16, out bfloat16 or float32, sink / gate optional
+    float32 [B, k, Hq] logits and logit_scale an optional float32 [B, k]
+    (``relattn_decode_ex``).
     """
     dev = q.device
     _need(q, "q", torch.bfloat16, 4, dev)
     B, kq, Hq, _ = q.shape
     out_dtype = out.dtype if out is not None else out_dtype
-    io = _options(rel, out_dtype, sink, gate, (B, kq, Hq), dev, k_cache, k_scale, v_scale)
+    io = _options(rel, out_dtype, sink, gate, (B, kq, Hq), dev, k_cache, k_scale, v_scale,
+                  logit_scale)
     _need(rel, "rel", rel.dtype, 4, dev)
     _need_cache(k_cache, v_cache, dev)
     _need(block_table, "block_table", torch.int32, 2, dev)
@@ -350,7 +364,7 @@ def relattn_decode_multi(q, rel, k_cache, v_cache, block_table, seq_lens, window
         _need(out, "out", out_dtype, 4, dev)
     if workspace is None:
         workspace = new_workspace(workspace_size(dims, cache), dev)
-    if _plain(rel, out_dtype, sink, gate, k_cache):
+    if _plain(rel, out_dtype, sink, gate, k_cache, logit_scale):
         _check(lib().relattn_decode_multi(
             q.data_ptr(), rel.data_ptr(), ctypes.byref(cache), block_table.data_ptr(),
             seq_lens.data_ptr(), int(kq), int(window), int(rel_extent), ctypes.byref(dims),
@@ -372,18 +386,20 @@ def prefill_dims(q, block_table, ctx_lens, max_q_len: int, num_ctas=0) -> Dims:
 
 def relattn_prefill(q, k, v, rel, cu_seqlens, k_cache, v_cache, block_table, ctx_lens,
                     window: int, rel_extent: int, max_q_len: int, out=None,
-                    workspace=None, out_dtype=torch.bfloat16, sink=None, gate=None):
+                    workspace=None, out_dtype=torch.bfloat16, sink=None, gate=None,
+                    logit_scale=None):
     """Chunked prefill with a cached prefix; writes k, v into the cache.
 
     rel may be float32 or bfloat16, out bfloat16 or float32 (``out``'s own
-    dtype when it is given), sink / gate optional float32 [T, Hq] logits;
-    anything but fp32 rel, bf16 out and no sink or gate goes through
+    dtype when it is given), sink / gate optional float32 [T, Hq] logits,
+    logit_scale an optional float32 [T] of log-position factors; anything but
+    fp32 rel, bf16 out and none of the optional inputs goes through
     ``relattn_prefill_ex``.
     """
     dev = q.device
     T, Hq, dqk = q.shape
     out_dtype = out.dtype if out is not None else out_dtype
-    io = _options(rel, out_dtype, sink, gate, (T, Hq), dev)
+    io = _options(rel, out_dtype, sink, gate, (T, Hq), dev, logit_scale=logit_scale)
     _need(q, "q", torch.bfloat16, 3, dev)
     _need(k, "k", torch.bfloat16, 3, dev)
     _need(v, "v", torch.bfloat16, 3, dev)
@@ -408,7 +424,7 @@ def relattn_prefill(q, k, v, rel, cu_seqlens, k_cache, v_cache, block_table, ctx
         _need(out, "out", out_dtype, 3, dev)
     if workspace is None:
         workspace = new_workspace(workspace_size(dims, cache), dev)
-    if _plain(rel, out_dtype, sink, gate):
+    if _plain(rel, out_dtype, sink, gate, logit_scale=logit_scale):
         _check(lib().relattn_prefill(
             q.data_ptr(), k.data_ptr(), v.data_ptr(), rel.data_ptr(), cu_seqlens.data_ptr(),
             ctypes.byref(cache), block_table.data_ptr(), ctx_lens.data_ptr(), int(window),

@@ -54,7 +54,7 @@ def host_decode_inputs(case):
 
 
 def host_opt(case, name):
-    """An optional per-(query row, head) input of a case, as numpy or None."""
+    """An optional per-query-row (and head) input of a case, as numpy or None."""
     t = case.get(name)
     return None if t is None else t.cpu().double().numpy()
 
@@ -64,7 +64,8 @@ def oracle_decode(case, batch=None, heads=None):
     return O.decode(h["q"], h["rel"], h["k_cache"], h["v_cache"], h["block_table"],
                     h["seq_lens"], case["window"], case["rel_extent"], batch=batch,
                     heads=heads, sink=host_opt(case, "sink"), gate=host_opt(case, "gate"),
-                    k_scale=case.get("k_scale", 1.0), v_scale=case.get("v_scale", 1.0))
+                    k_scale=case.get("k_scale", 1.0), v_scale=case.get("v_scale", 1.0),
+                    logit_scale=host_opt(case, "logit_scale"))
 
 
 class RowRel:
@@ -110,7 +111,8 @@ def oracle_prefill(case, rows=None, cache=None):
                      case["cu_seqlens"].cpu().numpy(), kc, vc,
                      case["block_table"].cpu().numpy(),
                      case["ctx_lens"].cpu().numpy(), case["window"], case["rel_extent"],
-                     rows=rows, sink=host_opt(case, "sink"), gate=host_opt(case, "gate"))
+                     rows=rows, sink=host_opt(case, "sink"), gate=host_opt(case, "gate"),
+                     logit_scale=host_opt(case, "logit_scale"))
 
 
 def oracle_decode_multi(case, batch=None, tokens=None, heads=None):
@@ -119,4 +121,5 @@ def oracle_decode_multi(case, batch=None, tokens=None, heads=None):
                           h["seq_lens"], case["window"], case["rel_extent"], batch=batch,
                           tokens=tokens, heads=heads, sink=host_opt(case, "sink"),
                           gate=host_opt(case, "gate"), k_scale=case.get("k_scale", 1.0),
-                          v_scale=case.get("v_scale", 1.0))
+                          v_scale=case.get("v_scale", 1.0),
+                          logit_scale=host_opt(case, "logit_scale"))
