@@ -98,17 +98,22 @@ bool cache_maps(const relattn_kv_cache* c, CUtensorMap* tk, CUtensorMap* tv) {
 // The 4-D view (64 columns, cache row, 64-column half, head) puts the halves
 // outermost in the box, so shared memory receives [half][64 rows][128 B], the
 // same 128-byte-swizzled halves as two 3-D copies would.
-bool decode_cache_maps(const relattn_kv_cache* c, CUtensorMap* tk, CUtensorMap* tv) {
+// box_rows = kTileKeys: a whole tile, both 64-column halves in one box.
+// box_rows = kTileKeys / 2: half a tile, one 64-column half per box (so that
+// it lands where it would in a whole tile).
+bool decode_cache_maps(const relattn_kv_cache* c, int box_rows, CUtensorMap* tk,
+                       CUtensorMap* tv) {
+  const bool whole = box_rows == kTileKeys;
   const cuuint64_t rows = static_cast<cuuint64_t>(c->num_blocks) * c->block_size;
   const cuuint64_t hkv = static_cast<cuuint64_t>(c->num_kv_heads);
   const cuuint64_t kd[4] = {64, rows, static_cast<cuuint64_t>(c->d_qk / 64), hkv};
   const cuuint64_t ks[3] = {hkv * c->d_qk * 2, 128, static_cast<cuuint64_t>(c->d_qk) * 2};
-  const cuuint32_t kb[4] = {64, static_cast<cuuint32_t>(kTileKeys),
-                            static_cast<cuuint32_t>(c->d_qk / 64), 1};
+  const cuuint32_t kb[4] = {64, static_cast<cuuint32_t>(box_rows),
+                            whole ? static_cast<cuuint32_t>(c->d_qk / 64) : 1u, 1};
   const cuuint64_t vd[4] = {64, rows, static_cast<cuuint64_t>(c->d_v / 64), hkv};
   const cuuint64_t vs[3] = {hkv * c->d_v * 2, 128, static_cast<cuuint64_t>(c->d_v) * 2};
-  const cuuint32_t vb[4] = {64, static_cast<cuuint32_t>(kTileKeys),
-                            static_cast<cuuint32_t>(c->d_v / 64), 1};
+  const cuuint32_t vb[4] = {64, static_cast<cuuint32_t>(box_rows),
+                            whole ? static_cast<cuuint32_t>(c->d_v / 64) : 1u, 1};
   return make_map(tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, c->k, kd, ks, kb,
                   CU_TENSOR_MAP_SWIZZLE_128B) &&
          make_map(tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, c->v, vd, vs, vb,
@@ -118,16 +123,18 @@ bool decode_cache_maps(const relattn_kv_cache* c, CUtensorMap* tk, CUtensorMap* 
 // e4m3 caches are head-major, [NB][Hkv][128][d]: a token's head row is only
 // 128 bytes, and this keeps a block's 128 rows of one head contiguous.  As a
 // 2-D tensor of rows (block * Hkv + head) * 128 + slot, a 64-key tile is one
-// 8 KB box, landing as 64 rows x 128 bytes with the 128-byte swizzle.
-bool decode_cache_maps_e4m3(const relattn_kv_cache* c, CUtensorMap* tk, CUtensorMap* tv) {
+// 8 KB box, landing as 64 rows x 128 bytes with the 128-byte swizzle (or
+// half of one, box_rows = 32).
+bool decode_cache_maps_e4m3(const relattn_kv_cache* c, int box_rows, CUtensorMap* tk,
+                            CUtensorMap* tv) {
   const cuuint64_t rows =
       static_cast<cuuint64_t>(c->num_blocks) * c->num_kv_heads * c->block_size;
   const cuuint64_t kd[2] = {static_cast<cuuint64_t>(c->d_qk), rows};
   const cuuint64_t ks[1] = {static_cast<cuuint64_t>(c->d_qk)};
-  const cuuint32_t kb[2] = {static_cast<cuuint32_t>(c->d_qk), static_cast<cuuint32_t>(kTileKeys)};
+  const cuuint32_t kb[2] = {static_cast<cuuint32_t>(c->d_qk), static_cast<cuuint32_t>(box_rows)};
   const cuuint64_t vd[2] = {static_cast<cuuint64_t>(c->d_v), rows};
   const cuuint64_t vs[1] = {static_cast<cuuint64_t>(c->d_v)};
-  const cuuint32_t vb[2] = {static_cast<cuuint32_t>(c->d_v), static_cast<cuuint32_t>(kTileKeys)};
+  const cuuint32_t vb[2] = {static_cast<cuuint32_t>(c->d_v), static_cast<cuuint32_t>(box_rows)};
   return make_map(tk, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, c->k, kd, ks, kb,
                   CU_TENSOR_MAP_SWIZZLE_128B) &&
          make_map(tv, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, c->v, vd, vs, vb,
@@ -351,8 +358,12 @@ static int prepare_decode(const void* q, const void* rel, IoTypes io,
              di->smem_optin)
     p.nstages -= 2;
   if (p.nstages < 2) return RELATTN_ERR_UNSUPPORTED;  // batch too large for shared memory
-  if (!(p.kv_es == 1 ? decode_cache_maps_e4m3(cache, &L->tm_k, &L->tm_v)
-                     : decode_cache_maps(cache, &L->tm_k, &L->tm_v)))
+  // whole tiles, and (one-token kernel, bf16 cache) half tiles for the edges
+  // of a sequence's key range
+  const bool halves = p.kv_es == 2 && !decode_multi_kernel(kq, gq);
+  if (!(p.kv_es == 1 ? decode_cache_maps_e4m3(cache, kTileKeys, &L->tm_k, &L->tm_v)
+                     : decode_cache_maps(cache, kTileKeys, &L->tm_k, &L->tm_v)) ||
+      (halves && !decode_cache_maps(cache, kTileKeys / 2, &L->tm_kh, &L->tm_vh)))
     return RELATTN_ERR_CUDA;
   // rel [B][k][Hq][E] fp32 or bf16: boxes of one token's g heads x
   // rel_box_w distances

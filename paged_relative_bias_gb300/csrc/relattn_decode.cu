@@ -536,12 +536,24 @@ __device__ Plan decode_prologue(const DecodeParams& p, uint8_t* smem, const Deco
 // only); the consumer warps widen its bytes to f16 in registers and the MMAs
 // take f16 operands.  LS: per-token logit factors are given (general kernel
 // only: the one-token kernel reads them whenever they are given, at no cost).
+// The K and V tensor maps of half-tile boxes, a parameter of the one-token
+// kernel over a bf16 cache only (the others keep their smaller parameter
+// block).
+template <bool H>
+struct HalfMaps {
+  CUtensorMap k, v;
+};
+template <>
+struct HalfMaps<false> {};
+
 template <int DV, bool MULTI, bool R16, bool KV8, bool LS>
 __global__ void __launch_bounds__(kDecodeThreads, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tm_q,
                   const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v,
-                  const __grid_constant__ CUtensorMap tm_rel, const DecodeParams p) {
+                  const __grid_constant__ CUtensorMap tm_rel,
+                  const __grid_constant__ HalfMaps<!MULTI && !KV8> hm,
+                  const DecodeParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_align1024(smem_raw);
   const int g = p.g;
@@ -587,6 +599,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
       tma_prefetch_desc(&tm_rel);
+      if constexpr (!MULTI && !KV8) {  // the half-tile boxes (see issue_tile)
+        tma_prefetch_desc(&hm.k);
+        tma_prefetch_desc(&hm.v);
+      }
     }
     __syncwarp();
   }
@@ -621,7 +637,13 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   const int rel_tx = g * RW * RES;                 // one token's rel box
   const int rel_stride = rel_token_bytes(g, RES);  // its place in a stage's rel slice
   // K, V and rel of tile `tile` of chunk sq, KV head kvh, into the stage of
-  // CTA tile nn (one lane per tile); 1 on a wait timeout.
+  // CTA tile nn (one lane per tile); 1 on a wait timeout.  One-token kernel
+  // over a bf16 cache: a tile at an edge of the key range [lo, p] whose first
+  // or last 32 keys all lie outside it brings only the other 32, and the
+  // consumer warps of the 32 left out skip the tile (their rows in the stage
+  // are never read).  (In the general kernel, at the register cap, and over
+  // an e4m3 cache, whose tiles all fit in flight at once, the tests cost more
+  // than the bytes saved.)
   auto issue_tile = [&](int nn, int tile, int id, const VSeq& sq, int kvh) -> int {
     const int stage = nn % ns;
     if (!mbar_wait(&empty[stage], ((nn / ns) & 1) ^ 1)) {
@@ -637,16 +659,28 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       // distance here is past rel_extent need none
       const int dmin0 = sq.pf - key0 - (kTileKeys - 1);
       const int nrel = max(0, min(sq.kc, p.rel_extent - dmin0));
-      mbar_arrive_expect_tx(&full[stage], stage_tx + nrel * rel_tx);
+      constexpr int kHalf = kTileKeys / 2;
+      constexpr bool kHalves = !MULTI && !KV8;
+      const int h0 = kHalves && key0 + kHalf - 1 < sq.lo ? kHalf : 0;  // first 32 not needed
+      const bool half = h0 > 0 || (kHalves && key0 + kHalf > sq.pl);  // or the last 32
+      mbar_arrive_expect_tx(&full[stage], (half ? stage_tx / 2 : stage_tx) + nrel * rel_tx);
       uint8_t* st = smem + L.stages + stage * L.stage_bytes;
       const int row = id * kBlockSize + (tile & 1) * kTileKeys;
+      constexpr int kVOff = KV8 ? kTileKeys * kDqk : 16384;  // V's place in a stage
       if constexpr (KV8) {  // head-major rows: 64 rows x 128 bytes, one box each
         const int hrow = (id * p.Hkv + kvh) * kBlockSize + (tile & 1) * kTileKeys;
         tma_load_2d(st, &tm_k, &full[stage], 0, hrow);
-        tma_load_2d(st + kTileKeys * kDqk, &tm_v, &full[stage], 0, hrow);
-      } else {
+        tma_load_2d(st + kVOff, &tm_v, &full[stage], 0, hrow);
+      } else if (!half) {
         tma_load_4d(st, &tm_k, &full[stage], 0, row, 0, kvh);
-        tma_load_4d(st + 16384, &tm_v, &full[stage], 0, row, 0, kvh);
+        tma_load_4d(st + kVOff, &tm_v, &full[stage], 0, row, 0, kvh);
+      } else if constexpr (kHalves) {  // one box per 64-column half (8 KB apart)
+        tma_load_4d(st + h0 * 128, &hm.k, &full[stage], 0, row + h0, 0, kvh);
+        tma_load_4d(st + 8192 + h0 * 128, &hm.k, &full[stage], 0, row + h0, 1, kvh);
+#pragma unroll
+        for (int hh = 0; hh < DV / 64; ++hh)
+          tma_load_4d(st + kVOff + hh * 8192 + h0 * 128, &hm.v, &full[stage], 0, row + h0, hh,
+                      kvh);
       }
       for (int i = 0; i < nrel; ++i)
         tma_load_2d(smem + L.rel + stage * L.rel_bytes + i * rel_stride, &tm_rel, &full[stage],
@@ -850,7 +884,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         abort = true;
         break;
       }
-      if (s_valid[stage]) {
+      // one-token kernel, bf16 cache: a warp whose 16 keys all lie outside
+      // [lo, p] has nothing to add (and its rows may not have been loaded)
+      const bool idle =
+          !MULTI && !KV8 && (key0 + 16 * cw + 15 < sq.lo || key0 + 16 * cw > sq.pl);
+      if (s_valid[stage] && !idle) {
         const uint8_t* st = smem + L.stages + stage * L.stage_bytes;
         const uint32_t kbase = smem_u32(st);
         const uint32_t vbase = kbase + 16384;
@@ -1315,8 +1353,13 @@ static cudaError_t launch_decode_as(const DecodeLaunch& L, int smem, cudaStream_
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  HalfMaps<!MULTI && !KV8> hm;
+  if constexpr (!MULTI && !KV8) {
+    hm.k = L.tm_kh;
+    hm.v = L.tm_vh;
+  }
   return cudaLaunchKernelEx(&cfg, decode_kernel<DV, MULTI, R16, KV8, LS>, L.tm_q, L.tm_k, L.tm_v,
-                            L.tm_rel, L.p);
+                            L.tm_rel, hm, L.p);
 }
 
 template <int DV, bool MULTI>

@@ -49,6 +49,7 @@ struct DecodeParams {
 
 struct DecodeLaunch {
   CUtensorMap tm_q, tm_k, tm_v, tm_rel;
+  CUtensorMap tm_kh, tm_vh;  // K and V boxes of half a tile (32 keys)
   DecodeParams p;
   int grid;
 };
