@@ -371,25 +371,48 @@ def run_decode_e2e(R, sets, wl, wss, device, steps, warmup, dist, sampler):
     inputs and the D2H of out inside the timed region, rotating over the same
     input sets (their KV pools stay resident, like a serving cache)."""
     keys = ("q", "rel", "seq_lens", "block_table")
-    host = [{k: c[k].cpu().pin_memory() for k in keys} for c in sets]
-    dev = {k: torch.empty_like(sets[0][k]) for k in keys}
+    # one pinned staging buffer per set holding the step's inputs back to
+    # back (256-byte aligned pieces), so each step is one H2D copy; the
+    # device buffer's pieces are the call's input tensors
+    offs, size = {}, 0
+    for k in keys:
+        offs[k] = size
+        size += (sets[0][k].numel() * sets[0][k].element_size() + 255) // 256 * 256
+    host = []
+    for c in sets:
+        buf = torch.empty(size, dtype=torch.uint8).pin_memory()
+        for k in keys:
+            nb = c[k].numel() * c[k].element_size()
+            buf[offs[k]:offs[k] + nb].copy_(c[k].cpu().contiguous().view(-1).view(torch.uint8))
+        host.append(buf)
+    dbuf = torch.empty(size, dtype=torch.uint8, device=device)
+    dev = {k: dbuf[offs[k]:offs[k] + sets[0][k].numel() * sets[0][k].element_size()]
+           .view(sets[0][k].dtype).view(sets[0][k].shape) for k in keys}
     tok = (wl.query_tokens,) if wl.query_tokens > 0 else ()
-    fn = R.relattn_decode_multi if wl.query_tokens > 0 else R.relattn_decode
     out_h = torch.empty((wl.batch, *tok, wl.num_q_heads, wl.d_v),
                         dtype=torch.bfloat16).pin_memory()
     out_d = torch.empty_like(out_h, device=device)
 
+    # the C-ABI call of each set, checked and marshalled once (its buffers
+    # stay in place; only their contents change from step to step)
+    runs = [R.bind_decode(dev["q"], dev["rel"], c["k_cache"], c["v_cache"], dev["block_table"],
+                          dev["seq_lens"], wl.window, wl.rel_extent, out_d, wss[i],
+                          k_scale=c.get("k_scale"), v_scale=c.get("v_scale"))
+            for i, c in enumerate(sets)]
+
     def step(k):
         i = k % len(sets)
-        for name in keys:
-            dev[name].copy_(host[i][name], non_blocking=True)
-        fn(dev["q"], dev["rel"], sets[i]["k_cache"], sets[i]["v_cache"], dev["block_table"],
-           dev["seq_lens"], wl.window, wl.rel_extent, out=out_d, workspace=wss[i],
-           k_scale=sets[i].get("k_scale"), v_scale=sets[i].get("v_scale"))
+        dbuf.copy_(host[i], non_blocking=True)
+        runs[i]()
         out_h.copy_(out_d, non_blocking=True)
 
     times = timed_steps(step, steps, warmup, None, dist, sampler)
-    h2d = sum(t.numel() * t.element_size() for t in host[0].values())
+    step(0)  # the staged pieces are the set's inputs, and the output is the device call's
+    torch.cuda.synchronize()
+    for k in keys:
+        if not torch.equal(dev[k], sets[0][k]):
+            raise RuntimeError(f"e2e staging of {k} does not match its input")
+    h2d = size  # the whole staging buffer (the four inputs and their padding)
     d2h = out_h.numel() * out_h.element_size()
     return times, h2d, d2h
 

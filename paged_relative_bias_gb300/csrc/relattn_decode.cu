@@ -1338,8 +1338,7 @@ int decode_smem_bytes(int nstages, int B, int Bv, int kpc, int g, int dv, int re
 
 template <int DV, bool MULTI, bool R16, bool KV8, bool LS = false>
 static cudaError_t launch_decode_as(const DecodeLaunch& L, int smem, cudaStream_t stream) {
-  cudaError_t e = cudaFuncSetAttribute(decode_kernel<DV, MULTI, R16, KV8, LS>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = ensure_smem<decode_kernel<DV, MULTI, R16, KV8, LS>>(smem);
   if (e != cudaSuccess) return e;
   // Programmatic stream serialisation: the kernel may begin while the
   // previous kernel on the stream finishes (see grid_dep_wait in the kernel).

@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace relattn {
 
 constexpr int kBlockSize = 128;  // tokens per KV block
@@ -46,6 +48,27 @@ struct DecodeParams {
   int nstages;  // even: see the consumer groups of decode_kernel
   float scale_log2;  // log2(e) / sqrt(d_qk)
 };
+
+// Raise kernel K's dynamic shared-memory limit to `smem` bytes on the current
+// device, calling the runtime only the first time (or for a larger size):
+// one attribute call per launch is host time every call would pay.
+template <auto K>
+cudaError_t ensure_smem(int smem) {
+  constexpr int kDevices = 64;
+  static std::atomic<int> set[kDevices];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < kDevices && set[dev].load(std::memory_order_relaxed) >= smem)
+    return cudaSuccess;
+  e = cudaFuncSetAttribute(K, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e == cudaSuccess && dev >= 0 && dev < kDevices) {
+    int cur = set[dev].load(std::memory_order_relaxed);
+    while (cur < smem && !set[dev].compare_exchange_weak(cur, smem)) {
+    }
+  }
+  return e;
+}
 
 struct DecodeLaunch {
   CUtensorMap tm_q, tm_k, tm_v, tm_rel;

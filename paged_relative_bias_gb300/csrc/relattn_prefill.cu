@@ -762,8 +762,7 @@ cudaError_t launch_cache_write(const PrefillParams& p, cudaStream_t stream) {
 template <int DV, bool R16, bool O32>
 static cudaError_t launch_prefill_as(const PrefillLaunch& L, int grid, int smem,
                                      cudaStream_t stream) {
-  cudaError_t e = cudaFuncSetAttribute(prefill_kernel<DV, R16, O32>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = ensure_smem<prefill_kernel<DV, R16, O32>>(smem);
   if (e != cudaSuccess) return e;
   prefill_kernel<DV, R16, O32><<<grid, kPfThreads, smem, stream>>>(L.tm_q, L.tm_k, L.tm_v,
                                                                    L.tm_rel, L.p);

@@ -276,6 +276,15 @@ def relattn_decode(q, rel, k_cache, v_cache, block_table, seq_lens, window: int,
                                  logit_scale=None if logit_scale is None
                                  else logit_scale[:, None])
         return o[:, 0]
+    fn, args, out = _decode_call(q, rel, k_cache, v_cache, block_table, seq_lens, window,
+                                 rel_extent, out, workspace, num_ctas)
+    _check(fn(*args, _stream(q.device)), fn.__name__)
+    return out
+
+
+def _decode_call(q, rel, k_cache, v_cache, block_table, seq_lens, window, rel_extent, out,
+                 workspace, num_ctas):
+    """(C function, its arguments but the stream, out) of a plain decode."""
     dev = q.device
     B, Hq, dqk = q.shape
     _need(q, "q", torch.bfloat16, 3, dev)
@@ -296,12 +305,10 @@ def relattn_decode(q, rel, k_cache, v_cache, block_table, seq_lens, window: int,
         _need(out, "out", torch.bfloat16, 3, dev)
     if workspace is None:
         workspace = new_workspace(workspace_size(dims, cache), dev)
-    _check(lib().relattn_decode(
+    return lib().relattn_decode, (
         q.data_ptr(), rel.data_ptr(), ctypes.byref(cache), block_table.data_ptr(),
         seq_lens.data_ptr(), int(window), int(rel_extent), ctypes.byref(dims),
-        out.data_ptr(), workspace.data_ptr(), workspace.numel(), _stream(dev)),
-        "relattn_decode")
-    return out
+        out.data_ptr(), workspace.data_ptr(), workspace.numel()), out
 
 
 def relattn_decode_noalloc(q, rel, k_cache, v_cache, block_table, seq_lens, window: int,
@@ -342,6 +349,18 @@ def relattn_decode_multi(q, rel, k_cache, v_cache, block_table, seq_lens, window
     float32 [B, k, Hq] logits and logit_scale an optional float32 [B, k]
     (``relattn_decode_ex``).
     """
+    fn, args, out = _decode_multi_call(q, rel, k_cache, v_cache, block_table, seq_lens, window,
+                                       rel_extent, out, workspace, num_ctas, out_dtype, sink,
+                                       gate, k_scale, v_scale, logit_scale)
+    _check(fn(*args, _stream(q.device)), fn.__name__)
+    return out
+
+
+def _decode_multi_call(q, rel, k_cache, v_cache, block_table, seq_lens, window, rel_extent,
+                       out, workspace, num_ctas, out_dtype, sink, gate, k_scale, v_scale,
+                       logit_scale):
+    """(C function, its arguments but the stream, out) of a multi-token or
+    typed decode."""
     dev = q.device
     _need(q, "q", torch.bfloat16, 4, dev)
     B, kq, Hq, _ = q.shape
@@ -365,18 +384,49 @@ def relattn_decode_multi(q, rel, k_cache, v_cache, block_table, seq_lens, window
     if workspace is None:
         workspace = new_workspace(workspace_size(dims, cache), dev)
     if _plain(rel, out_dtype, sink, gate, k_cache, logit_scale):
-        _check(lib().relattn_decode_multi(
+        return lib().relattn_decode_multi, (
             q.data_ptr(), rel.data_ptr(), ctypes.byref(cache), block_table.data_ptr(),
             seq_lens.data_ptr(), int(kq), int(window), int(rel_extent), ctypes.byref(dims),
-            out.data_ptr(), workspace.data_ptr(), workspace.numel(), _stream(dev)),
-            "relattn_decode_multi")
+            out.data_ptr(), workspace.data_ptr(), workspace.numel()), out
+    return lib().relattn_decode_ex, (
+        q.data_ptr(), rel.data_ptr(), ctypes.byref(io), ctypes.byref(cache),
+        block_table.data_ptr(), seq_lens.data_ptr(), int(kq), int(window),
+        int(rel_extent), ctypes.byref(dims), out.data_ptr(), workspace.data_ptr(),
+        workspace.numel()), out
+
+
+def bind_decode(q, rel, k_cache, v_cache, block_table, seq_lens, window: int,
+                rel_extent: int, out, workspace, num_ctas: int = 0, sink=None, gate=None,
+                k_scale=None, v_scale=None, logit_scale=None):
+    """Check and marshal one decode call for buffers that stay in place (a
+    serving loop that refills q, rel, seq_lens and block_table between
+    steps); returns run(), which enqueues that same C-ABI call on the
+    device's current stream and raises on a non-zero return code.  q is
+    [B, Hq, d_qk] (``relattn_decode``) or [B, k, Hq, d_qk]
+    (``relattn_decode_multi``); every tensor must outlive run.
+    """
+    if q.dim() == 3 and _plain(rel, out.dtype, sink, gate, k_cache, logit_scale):
+        fn, args, out = _decode_call(q, rel, k_cache, v_cache, block_table, seq_lens, window,
+                                     rel_extent, out, workspace, num_ctas)
     else:
-        _check(lib().relattn_decode_ex(
-            q.data_ptr(), rel.data_ptr(), ctypes.byref(io), ctypes.byref(cache),
-            block_table.data_ptr(), seq_lens.data_ptr(), int(kq), int(window),
-            int(rel_extent), ctypes.byref(dims), out.data_ptr(), workspace.data_ptr(),
-            workspace.numel(), _stream(dev)), "relattn_decode_ex")
-    return out
+        if q.dim() == 3:
+            q, rel, out = q[:, None], rel[:, None], out[:, None]
+            sink = None if sink is None else sink[:, None]
+            gate = None if gate is None else gate[:, None]
+            logit_scale = None if logit_scale is None else logit_scale[:, None]
+        fn, args, out = _decode_multi_call(q, rel, k_cache, v_cache, block_table, seq_lens,
+                                           window, rel_extent, out, workspace, num_ctas,
+                                           out.dtype, sink, gate, k_scale, v_scale,
+                                           logit_scale)
+    dev = q.device
+    keep = (q, rel, k_cache, v_cache, block_table, seq_lens, out, workspace, sink, gate,
+            logit_scale)
+
+    def run():
+        _check(fn(*args, _stream(dev)), fn.__name__)
+        return keep
+
+    return run
 
 
 def prefill_dims(q, block_table, ctx_lens, max_q_len: int, num_ctas=0) -> Dims:

@@ -97,3 +97,45 @@ def test_product_path_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(R, "library_path", lambda: str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="no CPU fallback"):
         R.lib()
+
+
+def test_bound_decode_marshals_like_the_wrapper(monkeypatch):
+    """bind_decode checks its inputs once and then makes the same C call,
+    with the same arguments, as relattn_decode (a fake library records them)."""
+    import torch
+    calls = []
+
+    class Fake:
+        def __getattr__(self, name):
+            def f(*args):
+                calls.append((name, args[:-1]))
+                return 0
+            f.__name__ = name
+            return f
+
+    monkeypatch.setattr(R, "_LIB", Fake())
+    monkeypatch.setattr(R, "lib", lambda: R._LIB)
+    monkeypatch.setattr(R, "_stream", lambda dev: 0)
+    B, Hq, Hkv = 2, 8, 2
+    q = torch.zeros((B, Hq, 128), dtype=torch.bfloat16)
+    rel = torch.zeros((B, Hq, 64), dtype=torch.float32)
+    kc = torch.zeros((4, 128, Hkv, 128), dtype=torch.bfloat16)
+    vc = torch.zeros((4, 128, Hkv, 128), dtype=torch.bfloat16)
+    bt = torch.zeros((B, 2), dtype=torch.int32)
+    sl = torch.ones((B,), dtype=torch.int32)
+    out = torch.empty((B, Hq, 128), dtype=torch.bfloat16)
+    ws = torch.empty(4096, dtype=torch.uint8)
+    R.relattn_decode(q, rel, kc, vc, bt, sl, 0, 64, out=out, workspace=ws)
+    run = R.bind_decode(q, rel, kc, vc, bt, sl, 0, 64, out, ws)
+    assert len(calls) == 1  # binding makes no call
+    run()
+    run()
+    assert [c[0] for c in calls] == ["relattn_decode"] * 3
+
+    def plain(args):  # pointers and ints; structures by their fields
+        return [tuple(getattr(a._obj, f[0]) for f in a._obj._fields_) if hasattr(a, "_obj")
+                else a for a in args]
+
+    assert plain(calls[1][1]) == plain(calls[0][1]) == plain(calls[2][1])
+    with pytest.raises(ValueError):
+        R.bind_decode(q, rel[:, :, :32], kc, vc, bt, sl, 0, 64, out, ws)
