@@ -214,9 +214,12 @@ int relattn_decode_multi(const void* q, const float* rel,
  *    head-major, [num_blocks][num_kv_heads][128][d] (a token's head row is
  *    only 128 bytes; this keeps each block's rows of one head contiguous),
  *    and num_blocks * num_kv_heads * 128 must stay below 2^31.  Decode
- *    only, one query token,
- *    g = Hq/Hkv <= 8 and d_v = 128: RELATTN_ERR_UNSUPPORTED otherwise, and
- *    for relattn_prefill_ex.  k_scale and v_scale must be finite and > 0.
+ *    only (one or several query tokens, any g), d_v = 128:
+ *    RELATTN_ERR_UNSUPPORTED otherwise, and for relattn_prefill_ex.  The
+ *    kernels compute with f16 operands: every e4m3 value is exact in f16,
+ *    and q is rounded from bf16 to f16 (exact within f16's range, 2^-14 ..
+ *    65504, and its 11-bit precision).  k_scale and v_scale must be finite
+ *    and > 0.
  */
 /*
  *  - logit_scale: the log-position scale of the global layers, which

@@ -296,8 +296,8 @@ static int prepare_decode(const void* q, const void* rel, IoTypes io,
   const int grid = decode_grid(dims, *di);
   if (kq < 1 || kq > kMaxQueryTokens) return RELATTN_ERR_UNSUPPORTED;
   const int gq = dims->num_q_heads / cache->num_kv_heads;
-  // an e4m3 cache: the one-token kernel (g <= 8) with d_v = 128
-  if (io.kv_es == 1 && (decode_multi_kernel(kq, gq) || cache->d_v != 128 ||
+  // an e4m3 cache: d_v = 128, and 32-bit head-major row coordinates
+  if (io.kv_es == 1 && (cache->d_v != 128 ||
                         static_cast<long long>(cache->num_blocks) * cache->num_kv_heads * 128 >
                             0x7fffffffLL))
     return RELATTN_ERR_UNSUPPORTED;

@@ -47,9 +47,12 @@ constexpr int kConsumerThreads = 32 * kConsumerWarps;
 constexpr int kWholeSlackTiles = 4;  // tolerated imbalance to avoid a split
 constexpr int kQBufBytes = 4096;     // 16 rows x 256 B as two swizzled halves
 constexpr int kMiscAbort = 14;       // shared flag word: a consumer warp gave up waiting
-// Per consumer warp with an e4m3 cache: its lanes' f16 B fragments of Q^T
-// for the eight k-steps of d_qk = 128 (8 x 32 lanes x 8 bytes).
+// e4m3 cache, f16 query fragments.  One-token kernel: per consumer warp,
+// its lanes' B fragments of Q^T for the eight k-steps of d_qk = 128 (8 x 32
+// lanes x 8 bytes).  General kernel: one copy for all warps, the lanes' A
+// fragments of Q (8 k-steps x 32 lanes x 16 bytes).
 constexpr int kPrivQ = 8 * 32 * 8;
+constexpr int kPrivQA = 8 * 32 * 16;
 
 constexpr int kSlicePad = 8;         // floats of padding per merge-slice row, at most
 constexpr float kLog2e = 1.4426950408889634f;
@@ -126,7 +129,9 @@ struct DecodeSmem {
     qbuf = 0;
     stages = qbuf + 2 * kQBufBytes;
     priv = stages + nstages * stage_bytes;
-    rel = priv + (kv_es == 1 ? kConsumerWarps * kPrivQ : 0);
+    // the general kernel runs when a tile packs several tokens or g > 8
+    const bool multi = kpc > 1 || g > 8;
+    rel = priv + (kv_es == 1 ? (multi ? kPrivQA : kConsumerWarps * kPrivQ) : 0);
     slices = rel + nstages * rel_bytes;
     bars = (slices + kConsumerWarps * kpc * g * (dv + kSlicePad) * 4 + 15) & ~15;
     valid = bars + (2 * nstages + 4) * 8;
@@ -568,7 +573,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   // merge-slice row padding: conflict-free writes of O^T columns (NB = 1:
   // rows 2 cq apart by 2 (DV + 4) = 8 banks mod 32) or of O rows (NB = 2)
   constexpr int SP = NB == 1 ? 4 : kSlicePad;
-  static_assert(!(KV8 && MULTI), "e4m3 caches: one-token kernel only");
+  static_assert(!KV8 || DV == 128, "e4m3 caches: d_v = 128");
   static_assert(!LS || MULTI, "logit factors: a template case of the general kernel only");
   const DecodeSmem L(ns, p.B, p.Bv, tok.kpc, g, DV, RES, KV8 ? 1 : 2);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
@@ -837,8 +842,34 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     }
     const float sl2 = p.scale_log2 * fr[0], bl2 = kLog2e * fr[0];  // one-token kernel
     const int qb = k & 1;
-    if (!mbar_wait(&qfull[qb], (k >> 1) & 1)) {
-      report(p.status, RELATTN_DEV_WAIT_TIMEOUT);
+    bool qok = mbar_wait(&qfull[qb], (k >> 1) & 1);
+    if (!qok) report(p.status, RELATTN_DEV_WAIT_TIMEOUT);
+    if constexpr (KV8 && MULTI) {
+      // e4m3 cache, general kernel: the MMAs run in f16.  The eight warps
+      // write the lanes' A fragments of Q (rows r0 and r0 + 8) for the eight
+      // k-steps once per piece, in the order of the dimensions of the K
+      // fragments (below), and release the query buffer; thread (s, l) writes
+      // k-step s of lane l.  Every warp reaches the barrier, also after a
+      // failed wait, and then all leave together.
+      if (qok) {
+        const int fl = ctid & 31, fs = ctid >> 5;
+        const int fr = fl >> 2, ft = fl & 3;
+        const int d0 = 64 * (ft >> 1) + 16 * (fs >> 1) + 8 * (ft & 1) + 4 * (fs & 1);
+        const uint8_t* qsrc = smem + L.qbuf + qb * kQBufBytes;
+        auto pair = [&](int row, int d) {  // bf16 of dimensions d, d + 1 -> f16
+          return bf16x2_to_f16x2(*reinterpret_cast<const uint32_t*>(
+              qsrc + (d >> 6) * 2048 + sw128(row, (d & 63) >> 3) + (d & 7) * 2));
+        };
+        reinterpret_cast<uint4*>(smem + L.priv)[fs * 32 + fl] =
+            make_uint4(pair(fr, d0), pair(fr + 8, d0), pair(fr, d0 + 2), pair(fr + 8, d0 + 2));
+      } else if (lane == 0) {
+        s_misc[kMiscAbort] = 1;
+      }
+      named_barrier(1, kConsumerThreads);
+      if (s_misc[kMiscAbort]) qok = false;
+      else if (lane == 0) mbar_arrive(&qempty[qb]);
+    }
+    if (!qok) {
       abort = true;
       break;
     }
@@ -852,7 +883,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     // shared query buffer is released.  k-step pair u reads dimensions
     // 64 (cq >> 1) + 16 u + 8 (cq & 1) + 0..7: one 16-byte piece of the row.
     uint2* const qfrag = reinterpret_cast<uint2*>(smem + L.priv + cwarp * kPrivQ);
-    if constexpr (KV8) {
+    if constexpr (KV8 && !MULTI) {
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const uint4 v = *reinterpret_cast<const uint4*>(
@@ -1031,7 +1062,30 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
           float s[2][4];
 #pragma unroll
           for (int i = 0; i < 4; ++i) s[0][i] = s[1][i] = 0.f;
-          {
+          if constexpr (KV8) {
+            // B fragments of K^T straight from the e4m3 rows, as in the
+            // one-token kernel: k-step pair u of this lane covers dimensions
+            // 64 (cq >> 1) + 16 u + 8 (cq & 1) + 0..7 of key r0 of each
+            // 8-key half; the A fragments of Q were written in that order
+            const uint4* qf = reinterpret_cast<const uint4*>(smem + L.priv);
+            const uint8_t* kr = st + (16 * cw + r0) * 128 + (cq & 1) * 8;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int off = ((4 * (cq >> 1) + u) ^ r0) * 16;
+              const uint2 k0 = *reinterpret_cast<const uint2*>(kr + off);
+              const uint2 k8 = *reinterpret_cast<const uint2*>(kr + 1024 + off);
+#pragma unroll
+              for (int v = 0; v < 2; ++v) {  // k-steps 2u, 2u + 1: bytes 0-3, then 4-7
+                const uint4 qa = qf[(2 * u + v) * 32 + lane];
+                const uint32_t a[4] = {qa.x, qa.y, qa.z, qa.w};
+                uint32_t b[2][2];
+                e4m3x4_to_f16x2x2(v ? k0.y : k0.x, b[0][0], b[0][1]);
+                e4m3x4_to_f16x2x2(v ? k8.y : k8.x, b[1][0], b[1][1]);
+                mma_16816_f16(s[0], a, b[0][0], b[0][1]);
+                mma_16816_f16(s[1], a, b[1][0], b[1][1]);
+              }
+            }
+          } else {
             const int key = 16 * cw + (mi >> 1) * 8 + (lane & 7);
             const int qrow = (mi & 1) * 8 + (lane & 7);
 #pragma unroll
@@ -1106,18 +1160,48 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
             }
           }
           uint32_t pa[4];
-          pa[0] = pack_bf16(x[0][0], x[0][1]);
-          pa[1] = pack_bf16(x[0][2], x[0][3]);
-          pa[2] = pack_bf16(x[1][0], x[1][1]);
-          pa[3] = pack_bf16(x[1][2], x[1][3]);
-          const int key = 16 * cw + (mi & 1) * 8 + (lane & 7);
+          if constexpr (KV8) {
+            pa[0] = pack_f16(x[0][0], x[0][1]);
+            pa[1] = pack_f16(x[0][2], x[0][3]);
+            pa[2] = pack_f16(x[1][0], x[1][1]);
+            pa[3] = pack_f16(x[1][2], x[1][3]);
+            // B fragments of V from the e4m3 rows: two keys' 4-byte reads
+            // interleaved give f16 pairs (key 2 cq (+8), key + 1) for 4
+            // dimensions, one per n-tile: n-tile nd's column r0 is d_v column
+            // 32 (nd >> 2) + 4 r0 + (nd & 3) (undone when the slices are
+            // written); as in the one-token kernel every read meets all 32
+            // banks once
+            const uint8_t* vr = st + kTileKeys * kDqk + (16 * cw + 2 * cq) * 128 + 4 * (r0 & 3);
 #pragma unroll
-          for (int nd = 0; nd < DV / 8; nd += 2) {
-            const int chunk = nd + (mi >> 1);
-            uint32_t b0, b1, b2, b3;
-            ldsm_x4_t(vbase + (chunk >> 3) * 8192 + sw128(key, chunk & 7), b0, b1, b2, b3);
-            mma_16816(o[nd], pa, b0, b1);
-            mma_16816(o[nd + 1], pa, b2, b3);
+            for (int j = 0; j < DV / 32; ++j) {
+              uint32_t vb[4][2];
+              const int c = 2 * j + (r0 >> 2);
+#pragma unroll
+              for (int pk = 0; pk < 2; ++pk) {  // keys 2 cq (+1), then 2 cq + 8 (+1)
+                const uint32_t xa = *reinterpret_cast<const uint32_t*>(
+                    vr + pk * 1024 + ((c ^ (2 * cq)) << 4));
+                const uint32_t xb = *reinterpret_cast<const uint32_t*>(
+                    vr + pk * 1024 + 128 + ((c ^ (2 * cq + 1)) << 4));
+                e4m3x4_to_f16x2x2(__byte_perm(xa, xb, 0x5140), vb[0][pk], vb[1][pk]);
+                e4m3x4_to_f16x2x2(__byte_perm(xa, xb, 0x7362), vb[2][pk], vb[3][pk]);
+              }
+#pragma unroll
+              for (int e = 0; e < 4; ++e) mma_16816_f16(o[4 * j + e], pa, vb[e][0], vb[e][1]);
+            }
+          } else {
+            pa[0] = pack_bf16(x[0][0], x[0][1]);
+            pa[1] = pack_bf16(x[0][2], x[0][3]);
+            pa[2] = pack_bf16(x[1][0], x[1][1]);
+            pa[3] = pack_bf16(x[1][2], x[1][3]);
+            const int key = 16 * cw + (mi & 1) * 8 + (lane & 7);
+#pragma unroll
+            for (int nd = 0; nd < DV / 8; nd += 2) {
+              const int chunk = nd + (mi >> 1);
+              uint32_t b0, b1, b2, b3;
+              ldsm_x4_t(vbase + (chunk >> 3) * 8192 + sw128(key, chunk & 7), b0, b1, b2, b3);
+              mma_16816(o[nd], pa, b0, b1);
+              mma_16816(o[nd + 1], pa, b2, b3);
+            }
           }
         }
       }
@@ -1186,6 +1270,17 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       for (int rr = 0; rr < 2; ++rr) {
         const int row = r0 + 8 * rr;
         if (!rv[rr]) continue;
+        if constexpr (KV8) {  // permuted d_v columns: see the e4m3 V fragments
+          float* sl = slices + (cwarp * srows + row) * (DV + SP) + 8 * cq;
+#pragma unroll
+          for (int j = 0; j < DV / 32; ++j)
+#pragma unroll
+            for (int e = 0; e < 2; ++e)
+              *reinterpret_cast<float4*>(sl + 32 * j + 4 * e) =
+                  make_float4(o[4 * j][2 * rr + e], o[4 * j + 1][2 * rr + e],
+                              o[4 * j + 2][2 * rr + e], o[4 * j + 3][2 * rr + e]);
+          continue;
+        }
         float* sl = slices + (cwarp * srows + row) * (DV + SP) + cq * 2;
 #pragma unroll
         for (int nd = 0; nd < DV / 8; ++nd)
@@ -1363,14 +1458,19 @@ static cudaError_t launch_decode_as(const DecodeLaunch& L, int smem, cudaStream_
 
 template <int DV, bool MULTI>
 static cudaError_t launch_decode_rel(const DecodeLaunch& L, int smem, cudaStream_t stream) {
-  if constexpr (!MULTI && DV == 128) {  // e4m3 caches: the one-token kernel, d_v = 128
+  // The general kernel has a copy with the logit factors, so that the plain
+  // one keeps its registers.
+  // (Over an e4m3 cache the general kernel has one copy, which reads the
+  // factors whenever they are given: a plain copy measured no fewer spills.)
+  const bool ls = MULTI && L.p.logit_scale != nullptr;
+  if constexpr (DV == 128) {  // e4m3 caches: d_v = 128
     if (L.p.kv_es == 1)
-      return L.p.rel_es == 2 ? launch_decode_as<DV, MULTI, true, true>(L, smem, stream)
-                             : launch_decode_as<DV, MULTI, false, true>(L, smem, stream);
+      return L.p.rel_es == 2 ? launch_decode_as<DV, MULTI, true, true, MULTI>(L, smem, stream)
+                             : launch_decode_as<DV, MULTI, false, true, MULTI>(L, smem, stream);
   }
   if (L.p.kv_es != 2) return cudaErrorInvalidValue;  // the host refuses these first
-  if constexpr (MULTI) {  // a copy with the logit factors, so the plain one keeps registers
-    if (L.p.logit_scale != nullptr)
+  if constexpr (MULTI) {
+    if (ls)
       return L.p.rel_es == 2 ? launch_decode_as<DV, MULTI, true, false, true>(L, smem, stream)
                              : launch_decode_as<DV, MULTI, false, false, true>(L, smem, stream);
   }

@@ -2,8 +2,9 @@
 
 The caches are quantised to e4m3 with one scale each (the input generator);
 the oracle reads the e4m3 patterns exactly and applies the scales, so the
-same tolerance as the bf16 cache applies.  The kernel widens K and V to f16
-in shared memory and runs its MMAs in f16.
+same tolerance as the bf16 cache applies.  The kernels widen K and V to f16
+in registers and run their MMAs in f16: the one-token kernel and the general
+one (several query tokens, or g > 8).
 """
 
 import numpy as np
@@ -12,7 +13,7 @@ import torch
 
 from paged_relative_bias_gb300 import inputs as I
 from paged_relative_bias_gb300 import relattn as R
-from tests.parity import assert_parity, oracle_decode, to_f64
+from tests.parity import assert_parity, oracle_decode, oracle_decode_multi, to_f64
 
 pytestmark = pytest.mark.gpu
 
@@ -35,7 +36,8 @@ def run(case, num_ctas=0, out_dtype=torch.bfloat16):
     out = fn(q, case["rel"], case["k_cache"], case["v_cache"], case["block_table"],
              case["seq_lens"], case["window"], case["rel_extent"], workspace=ws,
              num_ctas=num_ctas, out_dtype=out_dtype, sink=case.get("sink"),
-             gate=case.get("gate"), k_scale=case.get("k_scale"), v_scale=case.get("v_scale"))
+             gate=case.get("gate"), k_scale=case.get("k_scale"), v_scale=case.get("v_scale"),
+             logit_scale=case.get("logit_scale"))
     torch.cuda.synchronize()
     assert R.read_status(ws) == 0
     return out
@@ -103,16 +105,80 @@ def test_fp8_decode_full_size_global_b8_sampled():
     assert_parity(to_f64(out)[np.ix_(bs, hs)], want[np.ix_(bs, hs)], what="global b8 fp8")
 
 
-@pytest.mark.parametrize("what", ["multi_token", "dv64", "g16"])
-def test_fp8_unsupported_shapes_are_refused(what):
-    if what == "multi_token":
-        wl = fp8(I.DecodeWorkload("m", 2, 16, 4, 128, 128, 0, 64, ("uniform", 4, 300),
-                                  query_tokens=4))
-    elif what == "dv64":
-        wl = fp8(I.DecodeWorkload("d", 2, 16, 4, 128, 64, 0, 64, ("uniform", 1, 300)))
-    else:
-        wl = fp8(I.DecodeWorkload("g", 2, 32, 2, 128, 128, 0, 64, ("uniform", 1, 300)))
+def test_fp8_decode_dv64_is_refused():
+    wl = fp8(I.DecodeWorkload("d", 2, 16, 4, 128, 64, 0, 64, ("uniform", 1, 300)))
     case = I.make_decode(wl, DEV, seed_data=117)
     with pytest.raises(R.RelattnError) as e:
         run(case)
     assert e.value.code == R.ERR_UNSUPPORTED
+
+
+# ---- the general kernel over an e4m3 cache: several query tokens, or g > 8
+
+@pytest.mark.parametrize("k", [2, 3, 4, 8, 9, 16])
+def test_fp8_multi_token_decode(k):
+    """Verification over a global layer's e4m3 cache (g = 4: up to 4 tokens
+    per chunk, ragged last chunks beyond)."""
+    wl = fp8(I.DecodeWorkload("mt", 4, 32, 8, 128, 128, 0, 1024, ("uniform", 16, 5000),
+                              query_tokens=k))
+    case = I.make_decode(wl, DEV, seed_data=150 + k)
+    assert_parity(to_f64(run(case)), oracle_decode_multi(case), what=f"fp8 k={k}")
+
+
+@pytest.mark.parametrize("g,k", [(1, 5), (3, 4), (6, 2), (8, 2), (16, 1), (16, 3)])
+def test_fp8_general_kernel_packings(g, k):
+    Hkv = 2
+    wl = fp8(I.DecodeWorkload("pk", 3, g * Hkv, Hkv, 128, 128, 300, 256, ("uniform", 16, 2500),
+                              query_tokens=k))
+    case = I.make_decode(wl, DEV, seed_data=160 + g)
+    assert_parity(to_f64(run(case)), oracle_decode_multi(case), what=f"fp8 g={g} k={k}")
+
+
+@pytest.mark.parametrize("window,extent", [(0, 1024), (512, 512), (129, 64), (1, 4)])
+def test_fp8_multi_token_edge_lengths(window, extent):
+    lens = [8, 9, 63, 64, 65, 71, 72, 127, 128, 129, 135, 136, 255, 256, 257, 1031]
+    wl = fp8(I.DecodeWorkload("edge", len(lens), 32, 8, 128, 128, window, extent,
+                              ("list", lens), query_tokens=8))
+    case = I.make_decode(wl, DEV, seed_data=170)
+    assert_parity(to_f64(run(case)), oracle_decode_multi(case), what=f"W={window} E={extent}")
+
+
+@pytest.mark.parametrize("num_ctas", [1, 7, 152, 1000])
+def test_fp8_multi_token_any_split(num_ctas):
+    wl = fp8(I.DecodeWorkload("split", 5, 16, 4, 128, 128, 0, 256, ("uniform", 8, 4000),
+                              query_tokens=4))
+    case = I.make_decode(wl, DEV, seed_data=171)
+    assert_parity(to_f64(run(case, num_ctas=num_ctas)), oracle_decode_multi(case),
+                  what=f"num_ctas={num_ctas}")
+
+
+def test_fp8_multi_token_with_every_option():
+    """bf16 rel, fp32 out, sink, gate and log-position factors together."""
+    wl = fp8(I.DecodeWorkload("opt", 4, 32, 8, 128, 128, 0, 1024, ("uniform", 16, 3000),
+                              query_tokens=4, rel_dtype="bf16"))
+    case = I.make_decode(wl, DEV, seed_data=172)
+    g = torch.Generator(device="cpu")
+    g.manual_seed(173)
+    case["sink"] = torch.randn((4, 4, 32), generator=g).to(DEV)
+    case["gate"] = torch.randn((4, 4, 32), generator=g).to(DEV)
+    case["logit_scale"] = (0.5 + 2 * torch.rand((4, 4), generator=g)).to(DEV)
+    out = run(case, out_dtype=torch.float32)
+    assert_parity(to_f64(out), oracle_decode_multi(case), what="fp8 multi, every option")
+
+
+def test_fp8_multi_token_full_size_global_b8_sampled():
+    """Four tokens per sequence over the full B=8, 32K global workload."""
+    case = I.make_decode(fp8(I.variant(I.WORKLOADS["global_decode_b8"], query_tokens=4)), DEV,
+                         seed_data=174)
+    out = run(case)
+    bs, ts, hs = [0, 5], [0, 3], [1, 30]
+    want = oracle_decode_multi(case, batch=bs, tokens=ts, heads=hs)
+    got = to_f64(out)
+    assert_parity(got[np.ix_(bs, ts, hs)], want[np.ix_(bs, ts, hs)], what="global b8 k=4 fp8")
+
+
+def test_fp8_one_token_through_the_general_kernel_matches_the_oracle():
+    """k = 1 with g = 16 takes the general kernel (16 rows)."""
+    wl = fp8(I.DecodeWorkload("g16", 3, 32, 2, 128, 128, 0, 512, ("uniform", 1, 4000)))
+    case = I.make_decode(wl, DEV, seed_data=175)
+    assert_parity(to_f64(run(case)), oracle_decode(case), what="fp8 g=16 k=1")
