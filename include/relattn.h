@@ -217,9 +217,9 @@ int relattn_decode_multi(const void* q, const float* rel,
  *    only (one or several query tokens, any g), d_v = 128:
  *    RELATTN_ERR_UNSUPPORTED otherwise, and for relattn_prefill_ex.  The
  *    kernels compute with f16 operands: every e4m3 value is exact in f16,
- *    and q is rounded from bf16 to f16 (exact within f16's range, 2^-14 ..
- *    65504, and its 11-bit precision).  k_scale and v_scale must be finite
- *    and > 0.
+ *    and so is every bf16 q element of magnitude 2^-14 .. 65504 (f16's
+ *    normal range); smaller ones are rounded, larger ones overflow.  k_scale
+ *    and v_scale must be finite and > 0.
  */
 /*
  *  - logit_scale: the log-position scale of the global layers, which
