@@ -75,8 +75,10 @@ extern "C" {
 
 /* The paged KV cache (device memory, caller-owned). */
 typedef struct relattn_kv_cache {
-  void*   k;            /* bf16 [num_blocks][block_size][num_kv_heads][d_qk] */
-  void*   v;            /* bf16 [num_blocks][block_size][num_kv_heads][d_v]  */
+  void*   k;            /* bf16 [num_blocks][block_size][num_kv_heads][d_qk],
+                           or e4m3 [num_blocks][num_kv_heads][block_size][d_qk]
+                           (relattn_options.kv)                              */
+  void*   v;            /* the same with d_v                                 */
   int32_t num_blocks;   /* physical blocks in the pool                       */
   int32_t block_size;   /* tokens per block: must be 128                     */
   int32_t num_kv_heads; /* Hkv                                               */

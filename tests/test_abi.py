@@ -139,3 +139,22 @@ def test_bound_decode_marshals_like_the_wrapper(monkeypatch):
     assert plain(calls[1][1]) == plain(calls[0][1]) == plain(calls[2][1])
     with pytest.raises(ValueError):
         R.bind_decode(q, rel[:, :, :32], kc, vc, bt, sl, 0, 64, out, ws)
+
+
+def test_ctypes_structures_match_the_header():
+    """The binding's ctypes mirrors of the header's structures have the same
+    fields, in the same order, with the same C types."""
+    text = open(os.path.join(ROOT, "include", "relattn.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    ctype = {"int32_t": ctypes.c_int32, "float": ctypes.c_float}
+    mirrors = {"relattn_kv_cache": R.KVCacheDesc, "relattn_dims": R.Dims,
+               "relattn_options": R.Options}
+    for name, cls in mirrors.items():
+        body = re.search(r"typedef struct %s \{(.*?)\} %s;" % (name, name), text, re.S).group(1)
+        fields = []
+        for decl in filter(None, (d.strip() for d in body.split(";"))):
+            m = re.match(r"(?:const\s+)?(\w+)\s*(\*?)\s*(\w+)$", " ".join(decl.split()))
+            assert m, decl
+            base, star, field = m.groups()
+            fields.append((field, ctypes.c_void_p if star else ctype[base]))
+        assert [(f, t) for f, t in cls._fields_] == fields, name
