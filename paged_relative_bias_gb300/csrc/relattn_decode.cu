@@ -537,10 +537,6 @@ __device__ Plan decode_prologue(const DecodeParams& p, uint8_t* smem, const Deco
   return make_plan(p.Hkv * s_pref[p.Bv], s_misc[0], p.Bv * p.Hkv);
 }
 
-// R16: rel is bf16 (else fp32).  KV8: the cache is e4m3 (one-token kernel
-// only); the consumer warps widen its bytes to f16 in registers and the MMAs
-// take f16 operands.  LS: per-token logit factors are given (general kernel
-// only: the one-token kernel reads them whenever they are given, at no cost).
 // The K and V tensor maps of half-tile boxes, a parameter of the one-token
 // kernel over a bf16 cache only (the others keep their smaller parameter
 // block).
@@ -551,6 +547,11 @@ struct HalfMaps {
 template <>
 struct HalfMaps<false> {};
 
+// MULTI: the general kernel (several query tokens per tile, or g > 8), else
+// the one-token kernel.  R16: rel is bf16 (else fp32).  KV8: the cache is
+// e4m3; the consumer warps widen its bytes to f16 in registers and the MMAs
+// take f16 operands.  LS: per-token logit factors are given (general kernel
+// only: the one-token kernel reads them whenever they are given, at no cost).
 template <int DV, bool MULTI, bool R16, bool KV8, bool LS>
 __global__ void __launch_bounds__(kDecodeThreads, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tm_q,
