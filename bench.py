@@ -196,15 +196,25 @@ class ClockSampler:
 
 
 class Dist:
-    def __init__(self):
+    """The replicas of a torchrun launch (one rank per GPU, env:// rendezvous):
+    a barrier and the max over ranks of the timed seconds.  No data-path
+    collective: the path does not shard.  backend "gloo" runs the same logic
+    on host tensors (tests)."""
+
+    def __init__(self, backend: str = "nccl"):
         self.world = int(os.environ.get("WORLD_SIZE", "1"))
         self.rank = int(os.environ.get("RANK", "0"))
         self.local = int(os.environ.get("LOCAL_RANK", "0"))
         self.pg = None
+        self.dev = "cpu"
         if self.world > 1:
             import torch.distributed as dist
-            torch.cuda.set_device(self.local)
-            dist.init_process_group("nccl", device_id=torch.device("cuda", self.local))
+            if backend == "nccl":
+                torch.cuda.set_device(self.local)
+                self.dev = f"cuda:{self.local}"
+                dist.init_process_group("nccl", device_id=torch.device("cuda", self.local))
+            else:
+                dist.init_process_group(backend)
             self.pg = dist
 
     def barrier(self):
@@ -214,7 +224,7 @@ class Dist:
     def max(self, x: float) -> float:
         if not self.pg:
             return x
-        t = torch.tensor([x], dtype=torch.float64, device=f"cuda:{self.local}")
+        t = torch.tensor([x], dtype=torch.float64, device=self.dev)
         self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
         return float(t.item())
 
