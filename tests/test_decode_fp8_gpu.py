@@ -182,3 +182,28 @@ def test_fp8_one_token_through_the_general_kernel_matches_the_oracle():
     wl = fp8(I.DecodeWorkload("g16", 3, 32, 2, 128, 128, 0, 512, ("uniform", 1, 4000)))
     case = I.make_decode(wl, DEV, seed_data=175)
     assert_parity(to_f64(run(case)), oracle_decode(case), what="fp8 g=16 k=1")
+
+
+def test_prefill_refuses_an_e4m3_cache():
+    """Only decode reads e4m3 caches: relattn_prefill_ex returns UNSUPPORTED
+    for kv = E4M3 (called through the C ABI), and the binding refuses a
+    float8 cache before the call."""
+    import ctypes
+    p = I.make_prefill(I.WORKLOADS["tiny_prefill"], DEV)
+    dims = R.prefill_dims(p["q"], p["block_table"], p["ctx_lens"], p["max_q_len"])
+    cache = R.cache_desc(p["k_cache"], p["v_cache"])
+    ws = R.new_workspace(R.workspace_size(dims, cache), DEV)
+    out = torch.empty((p["num_tokens"], 4, 128), dtype=torch.bfloat16, device=DEV)
+    opt = R.Options(R.DTYPE_F32, R.DTYPE_BF16, None, None, R.DTYPE_E4M3, 1.0, 1.0, None)
+    rc = R.lib().relattn_prefill_ex(
+        p["q"].data_ptr(), p["k"].data_ptr(), p["v"].data_ptr(), p["rel"].data_ptr(),
+        ctypes.byref(opt), p["cu_seqlens"].data_ptr(), ctypes.byref(cache),
+        p["block_table"].data_ptr(), p["ctx_lens"].data_ptr(), p["window"], p["rel_extent"],
+        ctypes.byref(dims), out.data_ptr(), ws.data_ptr(), ws.numel(),
+        torch.cuda.current_stream().cuda_stream)
+    assert rc == R.ERR_UNSUPPORTED
+    k8, v8 = (t.to(torch.float8_e4m3fn) for t in (p["k_cache"], p["v_cache"]))
+    with pytest.raises(TypeError):
+        R.relattn_prefill(p["q"], p["k"], p["v"], p["rel"], p["cu_seqlens"], k8, v8,
+                          p["block_table"], p["ctx_lens"], p["window"], p["rel_extent"],
+                          p["max_q_len"])
