@@ -116,6 +116,38 @@ def e4m3_bits_to_f64(bits) -> np.ndarray:
     return sign * mag
 
 
+# every finite non-negative e4m3 value, in code order 0x00 .. 0x7E
+_E4M3_POS = None
+
+
+def e4m3_encode(x) -> np.ndarray:
+    """The e4m3 code of each value: the nearest finite e4m3 value, ties to
+    the even code (even mantissa), the sign kept (also for zero); magnitudes
+    above the largest finite value, 448, give 448 (saturation to finite is
+    this library's reading: the pages give no quantiser), NaN gives 0x7F."""
+    global _E4M3_POS
+    if _E4M3_POS is None:
+        _E4M3_POS = e4m3_bits_to_f64(np.arange(0x7F, dtype=np.uint8))
+    x = np.asarray(x, dtype=np.float64)
+    mag = np.abs(x)
+    lo = np.clip(np.searchsorted(_E4M3_POS, mag, side="right") - 1, 0, 0x7E)  # value <= mag
+    hi = np.minimum(lo + 1, 0x7E)
+    d_lo = mag - _E4M3_POS[lo]
+    d_hi = _E4M3_POS[hi] - mag
+    code = np.where(d_lo < d_hi, lo, np.where(d_hi < d_lo, hi, np.where(lo % 2 == 0, lo, hi)))
+    code = np.where(mag >= 448.0, 0x7E, code)
+    code = code | np.where(np.signbit(x), 0x80, 0)
+    code = np.where(np.isnan(x), 0x7F, code)
+    return code.astype(np.uint8)
+
+
+def e4m3_quantize(bf16_bits, scale: float) -> np.ndarray:
+    """Codes of bf16 values divided by a per-tensor scale: the division in
+    float32 (as the cache-writing kernel does it), then e4m3_encode."""
+    x = bf16_bits_to_f64(bf16_bits).astype(np.float32)
+    return e4m3_encode(x / np.float32(scale))
+
+
 def as_f64(x) -> np.ndarray:
     """float64 view of an input: uint16 is read as bf16 bits, uint8 as e4m3
     bits, floats widen."""
@@ -227,6 +259,15 @@ def kv_cache_write(k_cache, v_cache, k, v, cu_seqlens, ctx_lens, block_table):
             kc[phys, pos % BLOCK_SIZE] = k[r0 + t]
             vc[phys, pos % BLOCK_SIZE] = v[r0 + t]
     return kc, vc
+
+
+def kv_cache_write_e4m3(k_cache, v_cache, k, v, cu_seqlens, ctx_lens, block_table,
+                        k_scale: float, v_scale: float):
+    """kv_cache_write into e4m3 caches (uint8 codes, layout [NB, 128, Hkv, d]):
+    the same slots, each bf16 key quantised with k_scale and each value with
+    v_scale (e4m3_quantize).  Bit-exact."""
+    return kv_cache_write(k_cache, v_cache, e4m3_quantize(k, k_scale),
+                          e4m3_quantize(v, v_scale), cu_seqlens, ctx_lens, block_table)
 
 
 # --------------------------------------------------------------------------

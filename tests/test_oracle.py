@@ -699,3 +699,60 @@ def test_logit_scale_rows_agree_across_decode_multi_and_prefill():
     pre, _, _ = O.prefill(c["qm"][0], c["Kc"][L - k:L], c["Vc"][L - k:L], c["relm"][0], [0, k],
                           c["kc"], c["vc"], c["table"], [L - k], 64, 64, logit_scale=s[0])
     np.testing.assert_allclose(multi[0], pre, atol=1e-13, rtol=0)
+
+
+# ---------------------------------------------------------------------------
+# e4m3 quantisation (the cache write into an e4m3 cache)
+# ---------------------------------------------------------------------------
+
+def test_e4m3_encode_round_trips_every_finite_code():
+    codes = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], dtype=np.uint8)
+    assert np.array_equal(O.e4m3_encode(O.e4m3_bits_to_f64(codes)), codes)
+
+
+def test_e4m3_encode_matches_torch_in_range():
+    """torch's float32 -> float8_e4m3fn conversion (round to nearest even, an
+    independent implementation) on random values inside +-448 and on values
+    near every code."""
+    r = rng(130)
+    vals = O.e4m3_bits_to_f64(np.arange(0x7F, dtype=np.uint8))
+    near = np.concatenate([vals * f for f in (0.999, 1.0, 1.001)] +
+                          [(vals[:-1] + vals[1:]) / 2])
+    x = np.concatenate([r.standard_normal(20000) * 30, r.uniform(-448, 448, 20000),
+                        r.standard_normal(5000) * 1e-3, near, -near]).astype(np.float32)
+    x = x[np.abs(x) <= 448]
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(O.e4m3_encode(x.astype(np.float64)), ref)
+
+
+def test_e4m3_encode_ties_go_to_the_even_code_and_large_values_saturate():
+    vals = O.e4m3_bits_to_f64(np.arange(0x7F, dtype=np.uint8))
+    mids = (vals[:-1] + vals[1:]) / 2          # between code i and i + 1
+    want = np.arange(0x7E) + (np.arange(0x7E) % 2)  # the even one of the two
+    assert np.array_equal(O.e4m3_encode(mids), want.astype(np.uint8))
+    big = np.array([448.0, 463.9, 464.0, 500.0, 1e6, np.inf, -1e30, -np.inf])
+    assert O.e4m3_encode(big).tolist() == [0x7E] * 6 + [0xFE] * 2
+
+
+def test_e4m3_cache_write_is_within_half_a_step_of_the_scaled_values():
+    """Quantising and reading back stays within half an e4m3 step of x / scale
+    (relative 2^-4 for normal values, 2^-10 absolute below 2^-6), for values
+    up to 448 scale, and every other slot is untouched."""
+    r = rng(131)
+    T, Hkv, d = 50, 2, 16
+    k = O.f64_to_bf16_bits(r.standard_normal((T, Hkv, d)) * 3)
+    v = O.f64_to_bf16_bits(r.standard_normal((T, Hkv, d)))
+    ks, vs = float(np.abs(O.bf16_bits_to_f64(k)).max() / 448), 0.01
+    kc = np.zeros((3, 128, Hkv, d), dtype=np.uint8)
+    vc = np.zeros((3, 128, Hkv, d), dtype=np.uint8)
+    table = np.array([[2, 0]])
+    kc2, vc2 = O.kv_cache_write_e4m3(kc, vc, k, v, [0, T], [100], table, ks, vs)
+    pos = 100 + np.arange(T)
+    for cache, src, sc in ((kc2, k, ks), (vc2, v, vs)):
+        got = O.e4m3_bits_to_f64(cache[table[0][pos // 128], pos % 128])
+        x = np.clip(O.bf16_bits_to_f64(src) / sc, -448, 448)
+        bound = np.maximum(np.abs(x) * 2.0 ** -4, 2.0 ** -10)
+        assert np.all(np.abs(got - x) <= bound + 1e-12)
+    mask = np.ones(kc2.shape[:2], dtype=bool)
+    mask[table[0][pos // 128], pos % 128] = False
+    assert not kc2[mask].any() and not vc2[mask].any()
