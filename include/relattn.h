@@ -341,6 +341,42 @@ int relattn_prefill_ex(const void* q, const void* k, const void* v, const void* 
                        size_t workspace_bytes, void* stream);
 
 /*
+ * Write new tokens' keys and values into the paged cache without attending:
+ * the first step of relattn_prefill on its own, for callers that append
+ * tokens themselves (a decode step's newest token, whose key and value
+ * relattn_decode expects in the cache already) or that fill an e4m3 cache.
+ * No counterpart on the pages beyond that step ("Inkling-Small on Gaudi 2",
+ * section "Attention with a relative bias": the prefill writes the new keys
+ * and values into the paged cache).
+ *
+ * Token t of sequence b (packed row cu_seqlens[b] + t, t < cu_seqlens[b+1] -
+ * cu_seqlens[b]) goes to slot (ctx_lens[b] + t) % 128 of physical block
+ * block_table[b][(ctx_lens[b] + t) / 128].  k [T][Hkv][d_qk] and v
+ * [T][Hkv][d_v] are bf16 (16-byte aligned), T = dims->num_tokens; dims gives
+ * batch, max_blocks_per_seq, num_tokens and max_q_len (the longest chunk);
+ * num_q_heads is not read.  options may be NULL (a bf16 cache); otherwise
+ * options->kv picks the cache's type and only kv, k_scale and v_scale are
+ * read:
+ *  - bf16: the values are copied (bit-exact);
+ *  - e4m3 (head-major cache, d_v = 128): each key is stored as the e4m3 code
+ *    of (key / k_scale), each value of (value / v_scale), the division in
+ *    fp32 and the code the nearest e4m3 value with ties to the even code,
+ *    magnitudes beyond 448 stored as +-448 (this library's reading: the
+ *    pages name FP8 caches but no quantiser).
+ * The workspace holds the status word (at least 256 bytes); a block id
+ * outside the pool or an invalid length sets RELATTN_DEV_BAD_BLOCK_ID /
+ * RELATTN_DEV_BAD_LENGTH and skips the token / sequence.  Asynchronous on
+ * `stream`; nothing is allocated.  Returns RELATTN_OK, RELATTN_ERR_INVALID_ARG,
+ * RELATTN_ERR_UNSUPPORTED (e4m3 with d_v != 128, more than 65535 sequences),
+ * RELATTN_ERR_WORKSPACE or RELATTN_ERR_CUDA.
+ */
+int relattn_cache_write(const void* k, const void* v, const relattn_options* options,
+                        const int32_t* cu_seqlens, const relattn_kv_cache* kv_cache,
+                        const int32_t* block_table, const int32_t* ctx_lens,
+                        const relattn_dims* dims, void* workspace, size_t workspace_bytes,
+                        void* stream);
+
+/*
  * Read the device status word of a workspace into *status (synchronises
  * `stream`).  The word accumulates RELATTN_DEV_* bits until cleared with
  * relattn_workspace_init.

@@ -626,6 +626,53 @@ int relattn_prefill_ex(const void* q, const void* k, const void* v, const void* 
                             rel_extent, dims, out, workspace, workspace_bytes, stream);
 }
 
+int relattn_cache_write(const void* k, const void* v, const relattn_options* options,
+                        const int32_t* cu_seqlens, const relattn_kv_cache* cache,
+                        const int32_t* block_table, const int32_t* ctx_lens,
+                        const relattn_dims* dims, void* workspace, size_t workspace_bytes,
+                        void* stream) {
+  IoTypes io = kDefaultIo;
+  if (options != nullptr && !io_types(options, &io)) return RELATTN_ERR_INVALID_ARG;
+  int rc = check_cache(cache);
+  if (rc != RELATTN_OK) return rc;
+  if (!dims || !k || !v || !cu_seqlens || !block_table || !ctx_lens || !workspace)
+    return RELATTN_ERR_INVALID_ARG;
+  if (dims->batch < 0 || dims->max_blocks_per_seq < 1 || dims->num_tokens < 0 ||
+      dims->max_q_len < 0)
+    return RELATTN_ERR_INVALID_ARG;
+  if (!aligned16(k) || !aligned16(v)) return RELATTN_ERR_INVALID_ARG;
+  if (!aligned16(workspace) || workspace_bytes < kStatusBytes) return RELATTN_ERR_WORKSPACE;
+  if (dims->batch > kCacheWriteMaxGridY ||
+      static_cast<long long>(dims->max_blocks_per_seq) * 128 > 0x7fffffffLL)
+    return RELATTN_ERR_UNSUPPORTED;
+  if (io.kv_es == 1 && (cache->d_v != 128 ||
+                        static_cast<long long>(cache->num_blocks) * cache->num_kv_heads * 128 >
+                            0x7fffffffLL))
+    return RELATTN_ERR_UNSUPPORTED;
+  PrefillParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.k = static_cast<const __nv_bfloat16*>(k);
+  p.v = static_cast<const __nv_bfloat16*>(v);
+  p.cu_seqlens = cu_seqlens;
+  p.ctx_lens = ctx_lens;
+  p.block_table = block_table;
+  p.k_cache = static_cast<__nv_bfloat16*>(cache->k);
+  p.v_cache = static_cast<__nv_bfloat16*>(cache->v);
+  p.status = static_cast<uint32_t*>(workspace);
+  p.B = dims->batch;
+  p.T = dims->num_tokens;
+  p.Hkv = cache->num_kv_heads;
+  p.dv = cache->d_v;
+  p.max_blocks = dims->max_blocks_per_seq;
+  p.num_blocks = cache->num_blocks;
+  p.max_q_len = dims->max_q_len;
+  p.kv_es = io.kv_es;
+  p.k_scale = io.k_scale;
+  p.v_scale = io.v_scale;
+  if (p.B == 0 || p.T == 0 || p.max_q_len == 0) return RELATTN_OK;
+  return to_status(launch_cache_write(p, static_cast<cudaStream_t>(stream)));
+}
+
 int relattn_debug_walk_prefill(const int32_t* cu_seqlens, const int32_t* ctx_lens,
                                const int32_t* block_table, int32_t window,
                                const relattn_kv_cache* cache, const relattn_dims* dims,

@@ -85,7 +85,7 @@ struct PrefillParams {
   const int32_t* cu_seqlens;   // [B+1]
   const int32_t* ctx_lens;     // [B]
   const int32_t* block_table;  // [B][max_blocks]
-  __nv_bfloat16* k_cache;      // [NB][128][Hkv][128]
+  __nv_bfloat16* k_cache;      // [NB][128][Hkv][128] (e4m3 caches: uint8 [NB][Hkv][128][128])
   __nv_bfloat16* v_cache;      // [NB][128][Hkv][dv]
   void* out;                   // [T][Hq][dv], bf16 or fp32 (out_f32)
   const float* sink;           // [T][Hq] sink logits, or null
@@ -100,6 +100,9 @@ struct PrefillParams {
   int B, T, Hq, Hkv, g, dv, max_blocks, num_blocks, window, rel_extent, max_q_len;
   int ring_stages;  // depth of the query/rel/scratch ring (2 or 3, as shared memory allows)
   float scale_log2;
+  // cache write into an e4m3 cache (kv_es = 1): code = e4m3(x / scale)
+  int kv_es;
+  float k_scale, v_scale;
 };
 
 struct PrefillLaunch {
@@ -119,6 +122,7 @@ cudaError_t launch_decode(const DecodeLaunch& L, cudaStream_t stream);
 cudaError_t launch_decode_walk(const DecodeParams& p, int grid, cudaStream_t stream);
 
 cudaError_t launch_cache_write(const PrefillParams& p, cudaStream_t stream);
+constexpr int kCacheWriteMaxGridY = 65535;  // sequences of one cache-write launch
 int prefill_smem_bytes(int B, int dv, int ring_stages);
 int prefill_ring_stages(int B, int dv, int smem_optin);  // 0 if nothing fits
 cudaError_t launch_prefill(const PrefillLaunch& L, int grid, cudaStream_t stream);

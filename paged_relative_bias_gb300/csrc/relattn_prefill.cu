@@ -80,6 +80,30 @@ __device__ __forceinline__ bool rows_ok(int cu0, int cu1, int T) {
   return cu0 >= 0 && cu1 >= cu0 && cu1 <= T;
 }
 
+// Four floats -> four e4m3 codes (low byte first): x / scale rounded to
+// nearest even, saturated to +-448 (cvt's satfinite).
+__device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d, float scale) {
+  unsigned short lo, hi;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;"
+      : "=h"(lo)
+      : "f"(__fdiv_rn(b, scale)), "f"(__fdiv_rn(a, scale)));
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;"
+      : "=h"(hi)
+      : "f"(__fdiv_rn(d, scale)), "f"(__fdiv_rn(c, scale)));
+  return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+}
+
+// Eight bf16 (one uint4) -> eight e4m3 codes (one uint2).
+__device__ __forceinline__ uint2 e4m3x8(uint4 x, float scale) {
+  auto f = [](uint32_t w, int hi) { return __uint_as_float(hi ? (w & 0xffff0000u) : (w << 16)); };
+  return make_uint2(e4m3x4(f(x.x, 0), f(x.x, 1), f(x.y, 0), f(x.y, 1), scale),
+                    e4m3x4(f(x.z, 0), f(x.z, 1), f(x.w, 0), f(x.w, 1), scale));
+}
+
+// KV8: the cache is e4m3, head-major [NB][Hkv][128][128], and each value is
+// quantised with its tensor's scale; one thread-iteration writes 16 codes
+// (16 bytes) from 16 bf16 values.  Otherwise a 16-byte copy.
+template <bool KV8>
 __global__ void __launch_bounds__(256) cache_write_kernel(const PrefillParams p) {
   const int b = blockIdx.y;
   const int r0 = p.cu_seqlens[b];
@@ -93,7 +117,7 @@ __global__ void __launch_bounds__(256) cache_write_kernel(const PrefillParams p)
   }
   if (t0 >= n) return;
   const int nt = min(kCwTile, n - t0);
-  const int kch = kDqk / 8, vch = p.dv / 8;
+  const int kch = kDqk / (KV8 ? 16 : 8), vch = p.dv / (KV8 ? 16 : 8);  // 16-byte pieces
   const int per_tok = p.Hkv * (kch + vch);
   const int* trow = p.block_table + static_cast<size_t>(b) * p.max_blocks;
   for (int i = threadIdx.x; i < nt * per_tok; i += blockDim.x) {
@@ -109,6 +133,20 @@ __global__ void __launch_bounds__(256) cache_write_kernel(const PrefillParams p)
     }
     const size_t slot = static_cast<size_t>(phys) * kBlockSize + pos % kBlockSize;
     const size_t row = static_cast<size_t>(r0 + t0 + tt);
+    if constexpr (KV8) {
+      // row (phys * Hkv + hh) * 128 + pos % 128 of the head-major cache
+      const size_t hrow = (static_cast<size_t>(phys) * p.Hkv + hh) * kBlockSize + pos % kBlockSize;
+      const bool isk = ch < kch;
+      if (!isk) ch -= kch;
+      const uint4* src = reinterpret_cast<const uint4*>(
+          isk ? p.k + (row * p.Hkv + hh) * kDqk : p.v + (row * p.Hkv + hh) * p.dv);
+      const float sc = isk ? p.k_scale : p.v_scale;
+      const uint2 lo = e4m3x8(__ldg(src + 2 * ch), sc), hi = e4m3x8(__ldg(src + 2 * ch + 1), sc);
+      uint8_t* dst = reinterpret_cast<uint8_t*>(isk ? p.k_cache : p.v_cache) +
+                     hrow * (isk ? kDqk : p.dv);
+      reinterpret_cast<uint4*>(dst)[ch] = make_uint4(lo.x, lo.y, hi.x, hi.y);
+      continue;
+    }
     if (ch < kch) {
       const uint4 val = __ldg(reinterpret_cast<const uint4*>(p.k + (row * p.Hkv + hh) * kDqk) + ch);
       reinterpret_cast<uint4*>(p.k_cache + (slot * p.Hkv + hh) * kDqk)[ch] = val;
@@ -755,7 +793,10 @@ int prefill_ring_stages(int B, int dv, int smem_optin) {
 
 cudaError_t launch_cache_write(const PrefillParams& p, cudaStream_t stream) {
   const dim3 grid((p.max_q_len + kCwTile - 1) / kCwTile, p.B);
-  cache_write_kernel<<<grid, 256, 0, stream>>>(p);
+  if (p.kv_es == 1)
+    cache_write_kernel<true><<<grid, 256, 0, stream>>>(p);
+  else
+    cache_write_kernel<false><<<grid, 256, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

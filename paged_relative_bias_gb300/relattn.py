@@ -40,6 +40,7 @@ EXPORTS = (
     "relattn_decode_multi",
     "relattn_decode_ex",
     "relattn_prefill_ex",
+    "relattn_cache_write",
 )
 
 DTYPE_F32 = 0
@@ -129,6 +130,9 @@ def lib() -> ctypes.CDLL:
                                      c_void_p, P, c_void_p, c_void_p, c_int32, c_int32, S,
                                      c_void_p, c_void_p, c_size_t, c_void_p]
     L.relattn_prefill_ex.restype = c_int
+    L.relattn_cache_write.argtypes = [c_void_p, c_void_p, POINTER(Options), c_void_p, P,
+                                      c_void_p, c_void_p, S, c_void_p, c_size_t, c_void_p]
+    L.relattn_cache_write.restype = c_int
     L.relattn_abi_version.argtypes = []
     L.relattn_abi_version.restype = c_int
     _LIB = L
@@ -432,6 +436,37 @@ def bind_decode(q, rel, k_cache, v_cache, block_table, seq_lens, window: int,
 def prefill_dims(q, block_table, ctx_lens, max_q_len: int, num_ctas=0) -> Dims:
     return Dims(ctx_lens.shape[0], q.shape[1], block_table.shape[1], q.shape[0],
                 int(max_q_len), num_ctas)
+
+
+def relattn_cache_write(k, v, cu_seqlens, k_cache, v_cache, block_table, ctx_lens,
+                        max_q_len: int, k_scale=None, v_scale=None, workspace=None):
+    """Write new tokens' keys and values into the paged cache without
+    attending (see ``relattn_cache_write`` in include/relattn.h): copied into a
+    bf16 cache, or quantised into a head-major float8_e4m3fn cache with its
+    k_scale / v_scale.  k is [T, Hkv, d_qk], v [T, Hkv, d_v], both bf16."""
+    dev = k.device
+    _need(k, "k", torch.bfloat16, 3, dev)
+    _need(v, "v", torch.bfloat16, 3, dev)
+    _need_cache(k_cache, v_cache, dev)
+    _need(block_table, "block_table", torch.int32, 2, dev)
+    _need(cu_seqlens, "cu_seqlens", torch.int32, 1, dev)
+    _need(ctx_lens, "ctx_lens", torch.int32, 1, dev)
+    T, B = k.shape[0], ctx_lens.shape[0]
+    if v.shape[0] != T:
+        raise ValueError("k / v must have one row per new token")
+    if cu_seqlens.shape[0] != B + 1 or block_table.shape[0] != B:
+        raise ValueError("cu_seqlens / block_table batch mismatch")
+    io = _options(torch.empty(0, dtype=torch.float32), torch.bfloat16, k_cache=k_cache,
+                  k_scale=k_scale, v_scale=v_scale)
+    cache = cache_desc(k_cache, v_cache)
+    dims = Dims(B, k.shape[1], block_table.shape[1], T, int(max_q_len), 0)
+    if workspace is None:
+        workspace = new_workspace(256, dev)
+    _check(lib().relattn_cache_write(
+        k.data_ptr(), v.data_ptr(), ctypes.byref(io), cu_seqlens.data_ptr(), ctypes.byref(cache),
+        block_table.data_ptr(), ctx_lens.data_ptr(), ctypes.byref(dims), workspace.data_ptr(),
+        workspace.numel(), _stream(dev)), "relattn_cache_write")
+    return workspace
 
 
 def relattn_prefill(q, k, v, rel, cu_seqlens, k_cache, v_cache, block_table, ctx_lens,
