@@ -427,22 +427,29 @@ def decode_multi(q, rel, k_cache, v_cache, block_table, seq_lens, window: int,
 
 def prefill(q, k, v, rel, cu_seqlens, k_cache, v_cache, block_table,
             ctx_lens, window: int, rel_extent: int, rows=None, sink=None, gate=None,
-            logit_scale=None):
+            logit_scale=None, k_scale=1.0, v_scale=1.0):
     """Chunked prefill against the paged cache.
 
     Writes the new keys/values into copies of the caches, then attends each
     new token (position ctx_lens[b] + t) over the cached prefix plus the new
     tokens, causal and windowed.  ``rows`` selects packed token rows to
     compute (default: all); ``sink`` / ``gate``: optional [T, Hq] logits,
-    ``logit_scale``: optional [T] log-position factors (see ``attend``).  Returns (out float64 [T, Hq, d_v] with unselected rows NaN,
-    k_cache', v_cache').
+    ``logit_scale``: optional [T] log-position factors (see ``attend``).
+    e4m3 caches (uint8 codes) take the new tokens quantised with ``k_scale`` /
+    ``v_scale`` (``kv_cache_write_e4m3``) and are read back with them.
+    Returns (out float64 [T, Hq, d_v] with unselected rows NaN, k_cache',
+    v_cache').
     """
     T, Hq, d_qk = q.shape
     Hkv = k_cache.shape[2]
     g = Hq // Hkv
     d_v = v_cache.shape[3]
-    kc, vc = kv_cache_write(k_cache, v_cache, k, v, cu_seqlens, ctx_lens,
-                            block_table)
+    if np.asarray(k_cache).dtype == np.uint8:  # e4m3 caches: quantise the new tokens
+        kc, vc = kv_cache_write_e4m3(k_cache, v_cache, k, v, cu_seqlens, ctx_lens,
+                                     block_table, k_scale, v_scale)
+    else:
+        kc, vc = kv_cache_write(k_cache, v_cache, k, v, cu_seqlens, ctx_lens,
+                                block_table)
     out = np.full((T, Hq, d_v), np.nan)
     B = len(ctx_lens)
     want = None if rows is None else set(int(r) for r in rows)
@@ -456,7 +463,7 @@ def prefill(q, k, v, rel, cu_seqlens, k_cache, v_cache, block_table,
             lo, hi = visible_keys(P, window)
             keys = np.arange(lo, hi + 1)
             for kvh in range(Hkv):
-                K, V = gather_kv(kc, vc, block_table[b], keys, kvh)
+                K, V = gather_kv(kc, vc, block_table[b], keys, kvh, k_scale, v_scale)
                 for h in range(kvh * g, (kvh + 1) * g):
                     bias = rel_bias(rel[row, h], P, keys, rel_extent)
                     out[row, h] = attend(q[row, h], K, V, bias, d_qk,

@@ -756,3 +756,33 @@ def test_e4m3_cache_write_is_within_half_a_step_of_the_scaled_values():
     mask = np.ones(kc2.shape[:2], dtype=bool)
     mask[table[0][pos // 128], pos % 128] = False
     assert not kc2[mask].any() and not vc2[mask].any()
+
+
+def test_e4m3_prefill_is_the_float_prefill_of_the_dequantised_tokens():
+    """Prefill over an e4m3 cache = prefill over float caches holding the
+    dequantised old entries, with the new tokens replaced by their quantised
+    values read back (the write happens first, then the attention)."""
+    r = rng(132)
+    ctx, n, Hq, Hkv, d, W, E = 150, 90, 6, 2, 16, 100, 64
+    nblk = (ctx + n + 127) // 128
+    table = r.permutation(nblk + 1)[:nblk][None, :]
+    kc8 = r.integers(0, 256, size=(nblk + 1, 128, Hkv, d), dtype=np.uint8)
+    vc8 = r.integers(0, 256, size=(nblk + 1, 128, Hkv, d), dtype=np.uint8)
+    kc8[(kc8 & 0x7F) == 0x7F] = 0x38
+    vc8[(vc8 & 0x7F) == 0x7F] = 0x38
+    q = r.standard_normal((n, Hq, d))
+    k = O.f64_to_bf16_bits(r.standard_normal((n, Hkv, d)))
+    v = O.f64_to_bf16_bits(r.standard_normal((n, Hkv, d)))
+    rel = r.standard_normal((n, Hq, E))
+    ks, vs = 0.02, 0.005
+    out8, kc2, vc2 = O.prefill(q, k, v, rel, [0, n], kc8, vc8, table, [ctx], W, E,
+                               k_scale=ks, v_scale=vs)
+    kq = O.e4m3_bits_to_f64(O.e4m3_quantize(k, ks)) * ks
+    vq = O.e4m3_bits_to_f64(O.e4m3_quantize(v, vs)) * vs
+    outf, _, _ = O.prefill(q, kq, vq, rel, [0, n], O.e4m3_bits_to_f64(kc8) * ks,
+                           O.e4m3_bits_to_f64(vc8) * vs, table, [ctx], W, E)
+    np.testing.assert_allclose(out8, outf, atol=1e-13, rtol=0)
+    # and a decode over the written cache is the prefill's last row
+    dec = O.decode(q[-1:], rel[-1:], kc2, vc2, table, np.array([ctx + n]), W, E,
+                   k_scale=ks, v_scale=vs)
+    np.testing.assert_allclose(dec[0], out8[-1], atol=1e-13, rtol=0)
