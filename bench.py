@@ -99,11 +99,12 @@ def prefill_work(wl):
         kv_prefix += max(0, ctx - lo)
     T = sum(wl.new_tokens)
     Hq, Hkv = wl.num_q_heads, wl.num_kv_heads
-    kvrow = Hkv * (wl.d_qk + wl.d_v) * 2
+    kvrow = Hkv * (wl.d_qk + wl.d_v) * 2  # a new token's bf16 key and value rows
+    kvc = kvrow // 2 if wl.kv_dtype == "fp8" else kvrow  # ... as cached
     flops *= Hq * 2 * (wl.d_qk + wl.d_v)
     res = 2 if wl.rel_dtype == "bf16" else 4
-    nbytes = (rel * Hq * res + T * Hq * (wl.d_qk + wl.d_v) * 2 + 2 * T * kvrow
-              + kv_prefix * kvrow)
+    nbytes = (rel * Hq * res + T * Hq * (wl.d_qk + wl.d_v) * 2 + T * kvrow + T * kvc
+              + kv_prefix * kvc)
     return flops, nbytes
 
 
@@ -121,7 +122,8 @@ def describe(wl):
     win = f"W={wl.window}" if wl.window > 0 else "global"
     return (f"{wl.name}: chunked prefill {len(wl.new_tokens)}x{wl.new_tokens[0]} new tokens "
             f"after {wl.ctx_lens[0]} cached, {wl.num_q_heads}/{wl.num_kv_heads} heads, "
-            f"d={wl.d_qk}, {win}, rel_extent={wl.rel_extent}, {wl.rel_dtype} rel")
+            f"d={wl.d_qk}, {win}, rel_extent={wl.rel_extent}, {wl.rel_dtype} rel"
+            + (", e4m3 cache (per-tensor scales)" if wl.kv_dtype == "fp8" else ""))
 
 
 # ---------------------------------------------------------------------------
@@ -439,7 +441,8 @@ def run_prefill(R, wl, device, steps, warmup, dist, sampler, case=None):
         R.relattn_prefill(case["q"], case["k"], case["v"], case["rel"], case["cu_seqlens"],
                           case["k_cache"], case["v_cache"], case["block_table"],
                           case["ctx_lens"], wl.window, wl.rel_extent, case["max_q_len"],
-                          out=out, workspace=ws)
+                          out=out, workspace=ws, k_scale=case.get("k_scale"),
+                          v_scale=case.get("v_scale"))
 
     # a step reads several GB (rel alone is T * Hq * E * 4 bytes), far more
     # than the L2: no flush is needed between steps
@@ -567,6 +570,8 @@ def prefill_workload(args):
     wl = I.WORKLOADS["chunked_prefill"]
     if args.rel == "bf16":
         wl = I.variant(wl, rel_dtype="bf16")
+    if args.kv == "fp8":
+        wl = I.variant(wl, kv_dtype="fp8")
     nseq = args.prefill_seqs or len(wl.new_tokens)
     new = args.prefill_new_tokens or wl.new_tokens[0]
     if (nseq, new) != (len(wl.new_tokens), wl.new_tokens[0]):
@@ -658,8 +663,8 @@ def ours(args):
             del c2
             torch.cuda.empty_cache()
         wp0 = prefill_workload(args)
-        for rdt in ("f32", "bf16"):
-            wp = I.variant(wp0, rel_dtype=rdt)
+        for rdt, kvd in (("f32", "bf16"), ("bf16", "bf16"), ("f32", "fp8")):
+            wp = I.variant(wp0, rel_dtype=rdt, kv_dtype=kvd)
             flops, pbytes = prefill_work(wp)
             tp = run_prefill(R, wp, device, max(3, args.secondary_steps // 4), 2, dist, sampler)
             mp = sum(tp) / len(tp)
@@ -672,7 +677,8 @@ def ours(args):
                 "roofline": roofline("hbm", gbs, peaks["hbm"], "GB/s", None),
                 "tensor_frac_of_bf16_peak": round(tflops / peaks["bf16"], 4),
                 "note": f"step = cache write + attention kernels; rel ({rdt}) is most of the "
-                        f"bytes"})
+                        f"bytes" + ("; the cache is e4m3, widened to f16 in shared memory, "
+                                    "f16 MMAs" if kvd == "fp8" else "")})
             torch.cuda.empty_cache()
     clocks = sampler.stop()
 

@@ -553,16 +553,23 @@ static int prepare_prefill(const void* q, const void* k, const void* v, const vo
   p.window = window;
   p.rel_extent = rel_extent;
   p.max_q_len = dims->max_q_len;
-  p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(128.0));
+  // log2(e) / sqrt(d_qk), times the key scale of an e4m3 cache
+  p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(128.0) * io.k_scale);
+  p.kv_es = io.kv_es;
+  p.k_scale = io.k_scale;
+  p.v_scale = io.v_scale;
   if (walk) return RELATTN_OK;
   DeviceInfo di;
   if (!device_info(&di)) return RELATTN_ERR_CUDA;
-  p.ring_stages = prefill_ring_stages(p.B, p.dv, di.smem_optin);
+  p.ring_stages = prefill_ring_stages(p.B, p.dv, p.kv_es, di.smem_optin);
   if (p.ring_stages == 0) return RELATTN_ERR_UNSUPPORTED;
   const long long qtiles = static_cast<long long>(p.B) * ((p.max_q_len + 127) / 128) * p.Hq;
   const long long want = dims->num_ctas > 0 ? dims->num_ctas : di.sms;
   L->grid = static_cast<int>(qtiles < want ? (qtiles > 0 ? qtiles : 1) : want);
-  if (!cache_maps(cache, &L->tm_k, &L->tm_v)) return RELATTN_ERR_CUDA;
+  // e4m3 caches: 2-D boxes of 64 head-major rows, landing in staging slots
+  if (!(io.kv_es == 1 ? decode_cache_maps_e4m3(cache, kTileKeys, &L->tm_k, &L->tm_v)
+                      : cache_maps(cache, &L->tm_k, &L->tm_v)))
+    return RELATTN_ERR_CUDA;
   // q [T][Hq][128] bf16: one head's 128-token tile as two 64-column boxes
   const cuuint64_t qd[3] = {128, static_cast<cuuint64_t>(dims->num_q_heads),
                             static_cast<cuuint64_t>(dims->num_tokens)};
@@ -621,7 +628,10 @@ int relattn_prefill_ex(const void* q, const void* k, const void* v, const void* 
                        size_t workspace_bytes, void* stream) {
   IoTypes io;
   if (!io_types(options, &io)) return RELATTN_ERR_INVALID_ARG;
-  if (io.kv_es != 2) return RELATTN_ERR_UNSUPPORTED;  // e4m3 caches: decode only
+  if (io.kv_es == 1 && (!cache || cache->d_v != 128 ||
+                        static_cast<long long>(cache->num_blocks) * cache->num_kv_heads * 128 >
+                            0x7fffffffLL))
+    return RELATTN_ERR_UNSUPPORTED;  // e4m3 caches: d_v = 128, 32-bit row coordinates
   return relattn_prefill_io(q, k, v, rel, io, cu_seqlens, cache, block_table, ctx_lens, window,
                             rel_extent, dims, out, workspace, workspace_bytes, stream);
 }

@@ -69,26 +69,6 @@ __device__ __forceinline__ float out_scale(const DecodeParams& p, size_t qi, flo
   return s;
 }
 
-// bf16 pair -> f16 pair (exact for the magnitudes of attention inputs)
-__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
-  const __half2 h = __floats2half2_rn(__uint_as_float(v << 16), __uint_as_float(v & 0xffff0000u));
-  return *reinterpret_cast<const uint32_t*>(&h);
-}
-
-__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
-  const __half2 h = __floats2half2_rn(lo, hi);
-  return *reinterpret_cast<const uint32_t*>(&h);
-}
-
-// Four e4m3 values (one 32-bit word, low byte first) -> two f16 pairs: bytes
-// 0-1 in lo, bytes 2-3 in hi.
-__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t four, uint32_t& lo, uint32_t& hi) {
-  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
-      "cvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
-      : "=r"(lo), "=r"(hi)
-      : "r"(four));
-}
-
 __device__ __forceinline__ float rel_f32(float x) { return x; }
 __device__ __forceinline__ float rel_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
 

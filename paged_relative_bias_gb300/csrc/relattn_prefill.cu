@@ -37,8 +37,7 @@ namespace {
 
 constexpr int kQRows = 128;
 constexpr int kCwTile = 64;                 // cache_write tokens per CTA
-constexpr int kPfWarps = 7;
-constexpr int kPfThreads = 32 * kPfWarps;
+constexpr int kPfWarps = 7;  // (an e4m3 cache adds an eighth: the V widener)
 constexpr int kKStages = 2, kVStages = 2, kMaxRingStages = 3;
 constexpr int kKStageBytes = kTileKeys * kDqk * 2;  // 16 KB
 constexpr int kQTileBytes = kQRows * kDqk * 2;      // 32 KB
@@ -67,8 +66,12 @@ constexpr uint32_t kIdescS = umma_idesc_bf16(128, kTileKeys, 0);
 
 // kRFull / kREmpty: ring slots (producer <-> softmax); kQFull: query tile in
 // TMEM (softmax -> MMA).
+// kStgK / kStgV: an e4m3 cache's K / V tile in its staging slot (TMA -> the
+// warp that widens it into the K / V stage).
 enum Bar { kKFull = 0, kKEmpty = 2, kVFull = 4, kVEmpty = 6, kRFull = 8, kREmpty = 11,
-           kSFull = 14, kPFull = 16, kOFull = 18, kQFull = 19, kDrain = 20, kNumBars = 21 };
+           kSFull = 14, kPFull = 16, kOFull = 18, kQFull = 19, kDrain = 20, kStgK = 21,
+           kStgV = 23, kNumBars = 25 };
+constexpr int kStgBytes = kTileKeys * (kDqk + 128);  // one e4m3 tile: K then V, 16 KB
 
 __device__ __forceinline__ bool seq_ok(int ctx, int n, int max_blocks) {
   return ctx >= 0 && n >= 0 &&
@@ -158,15 +161,17 @@ __global__ void __launch_bounds__(256) cache_write_kernel(const PrefillParams p)
   }
 }
 
-// Shared-memory carve-up (byte offsets from a 1024-aligned base).
+// Shared-memory carve-up (byte offsets from a 1024-aligned base).  An e4m3
+// cache adds two staging slots for its tiles.
 struct PrefillSmem {
-  int k, v, vstage, ring, bars, misc, cu0, nrows, ctx, qpref, total;
-  __host__ __device__ PrefillSmem(int B, int dv, int ring_stages) {
+  int k, v, vstage, ring, stg, bars, misc, cu0, nrows, ctx, qpref, total;
+  __host__ __device__ PrefillSmem(int B, int dv, int ring_stages, int kv_es) {
     vstage = kTileKeys * dv * 2;
     k = 0;
     v = k + kKStages * kKStageBytes;
     ring = v + kVStages * vstage;  // 1024-aligned: query tiles land 128B-swizzled
-    bars = ring + ring_stages * kRingSlotBytes;
+    stg = ring + ring_stages * kRingSlotBytes;
+    bars = stg + (kv_es == 1 ? 2 * kStgBytes : 0);
     misc = bars + kNumBars * 8;
     cu0 = misc + 16;
     nrows = cu0 + B * 4;
@@ -288,17 +293,49 @@ __device__ __forceinline__ void rel_fma16(float (&x)[64], const uint32_t (&sr)[6
   }
 }
 
-// R16: rel is bf16 (else fp32).  O32: out is fp32 (else bf16).
-template <int DV, bool R16, bool O32>
-__global__ void __launch_bounds__(kPfThreads, 1)
+// One e4m3 tile (64 rows x 128 bytes, 128-byte swizzle) -> its values as
+// f16 in the layout the bf16 copies have (two 64-column halves 8 KB apart,
+// rows of 128 bytes, 128-byte swizzle).  Lane l takes 16-byte piece j = l & 7
+// of rows l / 8 + 4 t, t = 0..15: all 16 loads first, then the conversions
+// and stores (the compiler cannot move a load past a store to shared memory).
+__device__ __forceinline__ void widen_tile(const uint8_t* src, uint8_t* dst, int lane) {
+  const int j = lane & 7, r0 = lane >> 3;
+  const int c = 2 * (j & 3);
+  uint4 x[16];
+#pragma unroll
+  for (int t = 0; t < 16; ++t) {
+    const int r = r0 + 4 * t;
+    x[t] = *reinterpret_cast<const uint4*>(src + r * 128 + ((j ^ (r & 7)) << 4));
+  }
+#pragma unroll
+  for (int t = 0; t < 16; ++t) {
+    const int r = r0 + 4 * t;
+    uint32_t h[8];
+    e4m3x4_to_f16x2x2(x[t].x, h[0], h[1]);
+    e4m3x4_to_f16x2x2(x[t].y, h[2], h[3]);
+    e4m3x4_to_f16x2x2(x[t].z, h[4], h[5]);
+    e4m3x4_to_f16x2x2(x[t].w, h[6], h[7]);
+    uint8_t* row = dst + (j >> 2) * 8192 + r * 128;
+    *reinterpret_cast<uint4*>(row + ((c ^ (r & 7)) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
+    *reinterpret_cast<uint4*>(row + (((c + 1) ^ (r & 7)) << 4)) =
+        make_uint4(h[4], h[5], h[6], h[7]);
+  }
+}
+
+// R16: rel is bf16 (else fp32).  O32: out is fp32 (else bf16).  KV8: the
+// cache is e4m3 (d_v = 128): warp 0 widens each K tile to f16 and an eighth
+// warp each V tile, and every MMA runs in f16 (Q and P are f16 too).
+template <int DV, bool R16, bool O32, bool KV8>
+__global__ void __launch_bounds__(32 * (kPfWarps + (KV8 ? 1 : 0)), 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
                    const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v,
                    const __grid_constant__ CUtensorMap tm_rel, const PrefillParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_align1024(smem_raw);
+  static_assert(!KV8 || DV == 128, "e4m3 caches: d_v = 128");
   const int nrs = p.ring_stages;
-  const PrefillSmem L(p.B, DV, nrs);
+  const PrefillSmem L(p.B, DV, nrs, KV8 ? 1 : 2);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + L.misc);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + L.misc + 4);
@@ -324,6 +361,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     mbar_init(&bars[kOFull], 1);
     mbar_init(&bars[kQFull], 4);
     mbar_init(&bars[kDrain], 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars[kStgK + s], 1);
+      mbar_init(&bars[kStgV + s], 1);
+    }
     fence_mbar_init();
     *s_abort = 0;
     tma_prefetch_desc(&tm_q);
@@ -345,7 +386,63 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   const uint32_t tbase = *s_tmem;
   const float scale_log2 = p.scale_log2;
 
-  if (warp == 0 && lane == 0) {
+  if (KV8 && (warp == 0 || warp == kPfWarps)) {
+    // ------------------------- K (warp 0) or V (warp 7) of an e4m3 cache:
+    // lane 0 brings tile n into staging slot n & 1 (one 2-D box of 64
+    // head-major rows), then the warp widens tile n - 1 into its K or V stage
+    // (n - 1) & 1 as f16; the slot tile n lands in was last read when tile
+    // n - 2 was widened, before this copy was issued.
+    if constexpr (KV8) {
+      const bool isv = warp != 0;
+      const CUtensorMap* tm = isv ? &tm_v : &tm_k;
+      uint64_t* stg_bar = &bars[isv ? kStgV : kStgK];
+      uint64_t* full = &bars[isv ? kVFull : kKFull];
+      uint64_t* empty = &bars[isv ? kVEmpty : kKEmpty];
+      uint8_t* stage0 = smem + (isv ? L.v : L.k);
+      const int stage_bytes = isv ? L.vstage : kKStageBytes;
+      uint8_t* stg0 = smem + L.stg + (isv ? kTileKeys * kDqk : 0);
+      int n = 0;
+      bool okp = false;  // tile n - 1 had a valid block id
+      auto widen = [&](int m, bool ok) -> bool {
+        const int s = m & 1;
+        if (!mbar_wait(&empty[s], ((m >> 1) & 1) ^ 1)) return false;
+        if (ok) {
+          if (!mbar_wait(&stg_bar[s], (m >> 1) & 1)) return false;
+          widen_tile(stg0 + s * kStgBytes, stage0 + s * stage_bytes, lane);
+          // the MMAs read the stage through the async proxy, and the next
+          // copy into this staging slot comes after these reads
+          fence_proxy_async_smem();
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&full[s]);
+        return true;
+      };
+      bool fail = false;
+      for (int idx = blockIdx.x; idx < total && !*s_abort && !fail; idx += gridDim.x) {
+        PItem it;
+        prefill_item(idx, p, s_cu0, s_n, s_ctx, s_qpref, it);
+        const int* trow = p.block_table + static_cast<size_t>(it.b) * p.max_blocks;
+        for (int k = 0; k < it.ntiles; ++k, ++n) {
+          const int tile = it.tf + k;
+          const int id = __ldg(trow + (tile >> 1));
+          const bool ok = id >= 0 && id < p.num_blocks;
+          if (lane == 0) {
+            if (ok) {
+              const int hrow = (id * p.Hkv + it.kvh) * kBlockSize + (tile & 1) * kTileKeys;
+              mbar_arrive_expect_tx(&stg_bar[n & 1], kTileKeys * kDqk);
+              tma_load_2d(stg0 + (n & 1) * kStgBytes, tm, &stg_bar[n & 1], 0, hrow);
+            } else if (!isv) {
+              report(p.status, RELATTN_DEV_BAD_BLOCK_ID);
+            }
+          }
+          if (n > 0 && !widen(n - 1, okp)) { fail = true; break; }
+          okp = ok;
+        }
+      }
+      if (!fail && n > 0 && !widen(n - 1, okp)) fail = true;
+      if (fail && lane == 0) *s_abort = 1;
+    }
+  } else if (!KV8 && warp == 0 && lane == 0) {
     // ---------------------------------------------------- K/V TMA producer
     int n = 0;
     for (int idx = blockIdx.x; idx < total && !*s_abort; idx += gridDim.x) {
@@ -425,7 +522,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     if (fail) *s_abort = 1;
   } else if (warp == 1 && lane == 0) {
     // ---------------------------------------------------------- MMA issuer
-    const uint32_t idesc_pv = umma_idesc_bf16(128, DV, 1);
+    const uint32_t idesc_pv = KV8 ? umma_idesc_f16(128, DV, 1) : umma_idesc_bf16(128, DV, 1);
+    const uint32_t idesc_s = KV8 ? umma_idesc_f16(128, kTileKeys, 0) : kIdescS;
     int n = 0, items = 0;
     auto issue_pv = [&](int m, bool acc) -> bool {
       const int sp = m & 1;
@@ -456,7 +554,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 #pragma unroll
         for (int ks = 0; ks < kDqk / 16; ++ks)
           umma_tmem_a(tbase + kTmS + 64 * s, tbase + kTmQ + 8 * ks,
-                      umma_desc_sw128(kb + (ks >> 2) * 8192 + (ks & 3) * 32, 0, 1024), kIdescS,
+                      umma_desc_sw128(kb + (ks >> 2) * 8192 + (ks & 3) * 32, 0, 1024), idesc_s,
                       ks > 0 ? 1 : 0);
         umma_commit(&bars[kSFull + s]);
         umma_commit(&bars[kKEmpty + s]);
@@ -494,10 +592,17 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         for (int j = 0; j < 8; ++j) {
           const uint4 v =
               *reinterpret_cast<const uint4*>(qs + c * (kQTileBytes / 2) + sw128(r, j));
-          qr[(c * 8 + j) * 4] = v.x;
-          qr[(c * 8 + j) * 4 + 1] = v.y;
-          qr[(c * 8 + j) * 4 + 2] = v.z;
-          qr[(c * 8 + j) * 4 + 3] = v.w;
+          if constexpr (KV8) {  // the f16 MMAs take the query in f16
+            qr[(c * 8 + j) * 4] = bf16x2_to_f16x2(v.x);
+            qr[(c * 8 + j) * 4 + 1] = bf16x2_to_f16x2(v.y);
+            qr[(c * 8 + j) * 4 + 2] = bf16x2_to_f16x2(v.z);
+            qr[(c * 8 + j) * 4 + 3] = bf16x2_to_f16x2(v.w);
+          } else {
+            qr[(c * 8 + j) * 4] = v.x;
+            qr[(c * 8 + j) * 4 + 1] = v.y;
+            qr[(c * 8 + j) * 4 + 2] = v.z;
+            qr[(c * 8 + j) * 4 + 3] = v.w;
+          }
         }
       tmem_st32(tl + kTmQ, qr);
       tmem_st32(tl + kTmQ + 32, qr + 32);
@@ -632,7 +737,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           const float p0 = ex2(fmaf(x[2 * i], l2f, mb));
           const float p1 = ex2(fmaf(x[2 * i + 1], l2f, mb));
           sq[i & 3] += p0 + p1;
-          pk[i] = pack_bf16(p0, p1);
+          pk[i] = KV8 ? pack_f16(p0, p1) : pack_bf16(p0, p1);
         }
         l += (sq[0] + sq[1]) + (sq[2] + sq[3]);
         tmem_st32(tl + kTmS + 64 * s, pk);
@@ -670,7 +775,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         const size_t qi = static_cast<size_t>(it.r0 + r) * p.Hq + it.h;
         if (p.sink != nullptr && row_ok)
           den += ex2(__ldg(p.sink + qi) * kLog2e - m_used * l2f);  // 0 for a sink of -inf
-        inv = den > 0.f ? 1.f / den : 0.f;
+        if constexpr (KV8)  // an e4m3 cache's value scale
+          inv = den > 0.f ? p.v_scale / den : 0.f;
+        else
+          inv = den > 0.f ? 1.f / den : 0.f;
         if (p.gate != nullptr && row_ok) inv /= 1.f + ex2(-__ldg(p.gate + qi) * kLog2e);
       }
       constexpr int kCpr = DV / 8;     // 16-byte chunks per scratch row
@@ -781,13 +889,13 @@ __global__ void prefill_walk_kernel(const PrefillParams p) {
 
 }  // namespace
 
-int prefill_smem_bytes(int B, int dv, int ring_stages) {
-  return PrefillSmem(B, dv, ring_stages).total + 1024;
+int prefill_smem_bytes(int B, int dv, int ring_stages, int kv_es) {
+  return PrefillSmem(B, dv, ring_stages, kv_es).total + 1024;
 }
 
-int prefill_ring_stages(int B, int dv, int smem_optin) {
+int prefill_ring_stages(int B, int dv, int kv_es, int smem_optin) {
   for (int nr = kMaxRingStages; nr >= 2; --nr)
-    if (prefill_smem_bytes(B, dv, nr) <= smem_optin) return nr;
+    if (prefill_smem_bytes(B, dv, nr, kv_es) <= smem_optin) return nr;
   return 0;
 }
 
@@ -800,32 +908,37 @@ cudaError_t launch_cache_write(const PrefillParams& p, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-template <int DV, bool R16, bool O32>
+template <int DV, bool R16, bool O32, bool KV8>
 static cudaError_t launch_prefill_as(const PrefillLaunch& L, int grid, int smem,
                                      cudaStream_t stream) {
-  cudaError_t e = ensure_smem<prefill_kernel<DV, R16, O32>>(smem);
+  cudaError_t e = ensure_smem<prefill_kernel<DV, R16, O32, KV8>>(smem);
   if (e != cudaSuccess) return e;
-  prefill_kernel<DV, R16, O32><<<grid, kPfThreads, smem, stream>>>(L.tm_q, L.tm_k, L.tm_v,
-                                                                   L.tm_rel, L.p);
+  prefill_kernel<DV, R16, O32, KV8><<<grid, 32 * (kPfWarps + (KV8 ? 1 : 0)), smem, stream>>>(
+      L.tm_q, L.tm_k, L.tm_v, L.tm_rel, L.p);
   return cudaGetLastError();
 }
 
-template <int DV, bool R16>
+template <int DV, bool R16, bool KV8>
 static cudaError_t launch_prefill_out(const PrefillLaunch& L, int grid, int smem,
                                       cudaStream_t stream) {
-  return L.p.out_f32 ? launch_prefill_as<DV, R16, true>(L, grid, smem, stream)
-                     : launch_prefill_as<DV, R16, false>(L, grid, smem, stream);
+  return L.p.out_f32 ? launch_prefill_as<DV, R16, true, KV8>(L, grid, smem, stream)
+                     : launch_prefill_as<DV, R16, false, KV8>(L, grid, smem, stream);
 }
 
 cudaError_t launch_prefill(const PrefillLaunch& L, int grid, cudaStream_t stream) {
   const PrefillParams& p = L.p;
-  const int smem = prefill_smem_bytes(p.B, p.dv, p.ring_stages);
+  const int smem = prefill_smem_bytes(p.B, p.dv, p.ring_stages, p.kv_es);
   const bool r16 = p.rel_es == 2;
-  if (p.dv == 128)
-    return r16 ? launch_prefill_out<128, true>(L, grid, smem, stream)
-               : launch_prefill_out<128, false>(L, grid, smem, stream);
-  return r16 ? launch_prefill_out<64, true>(L, grid, smem, stream)
-             : launch_prefill_out<64, false>(L, grid, smem, stream);
+  if (p.dv == 128) {
+    if (p.kv_es == 1)  // e4m3 caches: d_v = 128 only
+      return r16 ? launch_prefill_out<128, true, true>(L, grid, smem, stream)
+                 : launch_prefill_out<128, false, true>(L, grid, smem, stream);
+    return r16 ? launch_prefill_out<128, true, false>(L, grid, smem, stream)
+               : launch_prefill_out<128, false, false>(L, grid, smem, stream);
+  }
+  if (p.kv_es == 1) return cudaErrorInvalidValue;  // the host refuses these first
+  return r16 ? launch_prefill_out<64, true, false>(L, grid, smem, stream)
+             : launch_prefill_out<64, false, false>(L, grid, smem, stream);
 }
 
 cudaError_t launch_prefill_walk(const PrefillParams& p, cudaStream_t stream) {

@@ -56,6 +56,7 @@ class PrefillWorkload:
     block_table: tuple = ()  # explicit table rows; () draws a random one
     pool_blocks: int = 0
     rel_dtype: str = "f32"  # "bf16": rel drawn in fp32 and rounded to bf16
+    kv_dtype: str = "bf16"  # "fp8": the cache quantised to e4m3 (head-major), one scale each
 
     @property
     def batch(self) -> int:
@@ -238,8 +239,12 @@ def make_prefill(wl: PrefillWorkload, device="cpu", seed_data: int = 0,
     rel = rel.to(_REL_DTYPES[wl.rel_dtype])
     k_cache = _randn((pool, BLOCK_SIZE, Hkv, wl.d_qk), g, device, torch.bfloat16)
     v_cache = _randn((pool, BLOCK_SIZE, Hkv, wl.d_v), g, device, torch.bfloat16)
+    scales = {}
+    if wl.kv_dtype == "fp8":  # head-major blocks: [pool, Hkv, 128, d]
+        k_cache, scales["k_scale"] = quantize_e4m3(k_cache.transpose(1, 2).contiguous())
+        v_cache, scales["v_scale"] = quantize_e4m3(v_cache.transpose(1, 2).contiguous())
     return dict(
-        q=q, k=k, v=v, rel=rel, k_cache=k_cache, v_cache=v_cache,
+        q=q, k=k, v=v, rel=rel, k_cache=k_cache, v_cache=v_cache, **scales,
         block_table=table.to(device),
         cu_seqlens=torch.tensor(cu, dtype=torch.int32, device=device),
         ctx_lens=torch.tensor(list(wl.ctx_lens), dtype=torch.int32, device=device),

@@ -472,25 +472,26 @@ def relattn_cache_write(k, v, cu_seqlens, k_cache, v_cache, block_table, ctx_len
 def relattn_prefill(q, k, v, rel, cu_seqlens, k_cache, v_cache, block_table, ctx_lens,
                     window: int, rel_extent: int, max_q_len: int, out=None,
                     workspace=None, out_dtype=torch.bfloat16, sink=None, gate=None,
-                    logit_scale=None):
+                    logit_scale=None, k_scale=None, v_scale=None):
     """Chunked prefill with a cached prefix; writes k, v into the cache.
 
     rel may be float32 or bfloat16, out bfloat16 or float32 (``out``'s own
     dtype when it is given), sink / gate optional float32 [T, Hq] logits,
-    logit_scale an optional float32 [T] of log-position factors; anything but
-    fp32 rel, bf16 out and none of the optional inputs goes through
-    ``relattn_prefill_ex``.
+    logit_scale an optional float32 [T] of log-position factors; a
+    float8_e4m3fn cache (head-major) takes its k_scale and v_scale.  Anything
+    but fp32 rel, bf16 out, a bf16 cache and none of the optional inputs goes
+    through ``relattn_prefill_ex``.
     """
     dev = q.device
     T, Hq, dqk = q.shape
     out_dtype = out.dtype if out is not None else out_dtype
-    io = _options(rel, out_dtype, sink, gate, (T, Hq), dev, logit_scale=logit_scale)
+    io = _options(rel, out_dtype, sink, gate, (T, Hq), dev, k_cache, k_scale, v_scale,
+                  logit_scale)
     _need(q, "q", torch.bfloat16, 3, dev)
     _need(k, "k", torch.bfloat16, 3, dev)
     _need(v, "v", torch.bfloat16, 3, dev)
     _need(rel, "rel", rel.dtype, 3, dev)
-    _need(k_cache, "k_cache", torch.bfloat16, 4, dev)
-    _need(v_cache, "v_cache", torch.bfloat16, 4, dev)
+    _need_cache(k_cache, v_cache, dev)
     _need(block_table, "block_table", torch.int32, 2, dev)
     _need(cu_seqlens, "cu_seqlens", torch.int32, 1, dev)
     _need(ctx_lens, "ctx_lens", torch.int32, 1, dev)
@@ -509,7 +510,7 @@ def relattn_prefill(q, k, v, rel, cu_seqlens, k_cache, v_cache, block_table, ctx
         _need(out, "out", out_dtype, 3, dev)
     if workspace is None:
         workspace = new_workspace(workspace_size(dims, cache), dev)
-    if _plain(rel, out_dtype, sink, gate, logit_scale=logit_scale):
+    if _plain(rel, out_dtype, sink, gate, k_cache, logit_scale):
         _check(lib().relattn_prefill(
             q.data_ptr(), k.data_ptr(), v.data_ptr(), rel.data_ptr(), cu_seqlens.data_ptr(),
             ctypes.byref(cache), block_table.data_ptr(), ctx_lens.data_ptr(), int(window),

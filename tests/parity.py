@@ -89,8 +89,9 @@ class RowQ(RowRel):
 
 
 def snapshot_cache(case):
-    """Host copy of the paged cache (take it before a prefill writes into it)."""
-    return bf16_bits(case["k_cache"]), bf16_bits(case["v_cache"])
+    """Host copy of the paged cache (take it before a prefill writes into it),
+    in the oracle's [NB, 128, Hkv, d] layout."""
+    return host_cache(case["k_cache"]), host_cache(case["v_cache"])
 
 
 def oracle_prefill(case, rows=None, cache=None):
@@ -112,7 +113,8 @@ def oracle_prefill(case, rows=None, cache=None):
                      case["block_table"].cpu().numpy(),
                      case["ctx_lens"].cpu().numpy(), case["window"], case["rel_extent"],
                      rows=rows, sink=host_opt(case, "sink"), gate=host_opt(case, "gate"),
-                     logit_scale=host_opt(case, "logit_scale"))
+                     logit_scale=host_opt(case, "logit_scale"),
+                     k_scale=case.get("k_scale", 1.0), v_scale=case.get("v_scale", 1.0))
 
 
 def oracle_decode_multi(case, batch=None, tokens=None, heads=None):

@@ -184,17 +184,18 @@ def test_fp8_one_token_through_the_general_kernel_matches_the_oracle():
     assert_parity(to_f64(run(case)), oracle_decode(case), what="fp8 g=16 k=1")
 
 
-def test_prefill_refuses_an_e4m3_cache():
-    """Only decode reads e4m3 caches: relattn_prefill_ex returns UNSUPPORTED
-    for kv = E4M3 (called through the C ABI), and the binding refuses a
-    float8 cache before the call."""
+def test_prefill_refuses_an_e4m3_cache_with_dv64():
+    """e4m3 caches need d_v = 128, in prefill as in decode: relattn_prefill_ex
+    returns UNSUPPORTED otherwise (called through the C ABI)."""
     import ctypes
-    p = I.make_prefill(I.WORKLOADS["tiny_prefill"], DEV)
+    wl = I.PrefillWorkload("p64", 4, 1, 128, 64, 64, 64, (130,), (0,), kv_dtype="fp8")
+    p = I.make_prefill(wl, DEV)
     dims = R.prefill_dims(p["q"], p["block_table"], p["ctx_lens"], p["max_q_len"])
     cache = R.cache_desc(p["k_cache"], p["v_cache"])
     ws = R.new_workspace(R.workspace_size(dims, cache), DEV)
-    out = torch.empty((p["num_tokens"], 4, 128), dtype=torch.bfloat16, device=DEV)
-    opt = R.Options(R.DTYPE_F32, R.DTYPE_BF16, None, None, R.DTYPE_E4M3, 1.0, 1.0, None)
+    out = torch.empty((p["num_tokens"], 4, 64), dtype=torch.bfloat16, device=DEV)
+    opt = R.Options(R.DTYPE_F32, R.DTYPE_BF16, None, None, R.DTYPE_E4M3, p["k_scale"],
+                    p["v_scale"], None)
     rc = R.lib().relattn_prefill_ex(
         p["q"].data_ptr(), p["k"].data_ptr(), p["v"].data_ptr(), p["rel"].data_ptr(),
         ctypes.byref(opt), p["cu_seqlens"].data_ptr(), ctypes.byref(cache),
@@ -202,8 +203,3 @@ def test_prefill_refuses_an_e4m3_cache():
         ctypes.byref(dims), out.data_ptr(), ws.data_ptr(), ws.numel(),
         torch.cuda.current_stream().cuda_stream)
     assert rc == R.ERR_UNSUPPORTED
-    k8, v8 = (t.to(torch.float8_e4m3fn) for t in (p["k_cache"], p["v_cache"]))
-    with pytest.raises(TypeError):
-        R.relattn_prefill(p["q"], p["k"], p["v"], p["rel"], p["cu_seqlens"], k8, v8,
-                          p["block_table"], p["ctx_lens"], p["window"], p["rel_extent"],
-                          p["max_q_len"])
