@@ -216,12 +216,13 @@ int relattn_decode_multi(const void* q, const float* rel,
  *    head-major, [num_blocks][num_kv_heads][128][d] (a token's head row is
  *    only 128 bytes; this keeps each block's rows of one head contiguous),
  *    and num_blocks * num_kv_heads * 128 must stay below 2^31.  Decode
- *    only (one or several query tokens, any g), d_v = 128:
- *    RELATTN_ERR_UNSUPPORTED otherwise, and for relattn_prefill_ex.  The
- *    kernels compute with f16 operands: every e4m3 value is exact in f16,
- *    and so is every bf16 q element of magnitude 2^-14 .. 65504 (f16's
- *    normal range); smaller ones are rounded, larger ones overflow.  k_scale
- *    and v_scale must be finite and > 0.
+ *    (one or several query tokens, any g) and prefill; d_v = 128
+ *    (RELATTN_ERR_UNSUPPORTED otherwise).  The prefill quantises its new
+ *    keys and values into the cache as relattn_cache_write does, then
+ *    attends over the cache.  The kernels compute with f16 operands: every
+ *    e4m3 value is exact in f16, and so is every bf16 q element of magnitude
+ *    2^-14 .. 65504 (f16's normal range); smaller ones are rounded, larger
+ *    ones overflow; P is f16.  k_scale and v_scale must be finite and > 0.
  */
 /*
  *  - logit_scale: the log-position scale of the global layers, which
@@ -328,8 +329,9 @@ int relattn_prefill(const void* q, const void* k, const void* v,
 
 /*
  * relattn_prefill with `options`: rel [T][Hq][rel_extent] of options->rel,
- * out [T][Hq][d_v] of options->out, sink and gate (when given) [T][Hq].  A
- * bf16 rel needs rel_extent a multiple of 8 (fp32: of 4):
+ * out [T][Hq][d_v] of options->out, sink and gate (when given) [T][Hq],
+ * logit_scale (when given) [T], and an e4m3 cache when options->kv says so
+ * (see above).  A bf16 rel needs rel_extent a multiple of 8 (fp32: of 4):
  * RELATTN_ERR_UNSUPPORTED otherwise; an unknown type code is
  * RELATTN_ERR_INVALID_ARG.  Everything else as relattn_prefill.
  */
