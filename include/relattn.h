@@ -261,7 +261,7 @@ int relattn_decode_ex(const void* q, const void* rel, const relattn_options* opt
                       void* workspace, size_t workspace_bytes, void* stream);
 
 /* Size of the library-owned scratch array used by relattn_decode_noalloc. */
-#define RELATTN_NOALLOC_SCRATCH_BYTES (4u << 20)
+#define RELATTN_NOALLOC_SCRATCH_BYTES (8u << 20)
 
 /*
  * Paged decode without a workspace, for callers that cannot allocate device

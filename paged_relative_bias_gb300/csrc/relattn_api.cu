@@ -168,14 +168,14 @@ struct WsLayout {
 
 // Decode workspace, sized for any query-token count up to kMaxQueryTokens:
 // counters per (chunk, KV head) -- at most kMaxQueryTokens chunks per
-// sequence -- and two partial slots per CTA of kMaxDecodeRows rows each.
+// sequence -- and two partial slots per CTA of kMaxChunkRows rows each.
 WsLayout ws_layout(const relattn_dims* d, const relattn_kv_cache* c, int grid) {
   WsLayout w;
   w.counters = kStatusBytes;
   w.lse = w.counters + round_up(static_cast<size_t>(d->batch) * kMaxQueryTokens *
                                     c->num_kv_heads * 4, 256);
-  w.part = w.lse + round_up(static_cast<size_t>(2) * grid * kMaxDecodeRows * 4, 256);
-  w.total = w.part + static_cast<size_t>(2) * grid * kMaxDecodeRows * c->d_v * 4;
+  w.part = w.lse + round_up(static_cast<size_t>(2) * grid * kMaxChunkRows * 4, 256);
+  w.total = w.part + static_cast<size_t>(2) * grid * kMaxChunkRows * c->d_v * 4;
   return w;
 }
 
@@ -301,7 +301,11 @@ static int prepare_decode(const void* q, const void* rel, IoTypes io,
                         static_cast<long long>(cache->num_blocks) * cache->num_kv_heads * 128 >
                             0x7fffffffLL))
     return RELATTN_ERR_UNSUPPORTED;
-  const int kpc = kq < kMaxDecodeRows / gq ? kq : kMaxDecodeRows / gq;  // tokens per chunk
+  // tokens per chunk: a 16-row tile's worth, or 32 rows split between the
+  // consumer groups when more tokens than that share a KV head
+  const bool split = decode_multi_kernel(kq, gq) && decode_row_split(kq, gq);
+  const int crow = split ? kMaxChunkRows : kMaxDecodeRows;
+  const int kpc = kq < crow / gq ? kq : crow / gq;
   const int nck = (kq + kpc - 1) / kpc;
   // the kernel's work split is 32-bit: all tiles < 2^31, grid^2 < 2^31
   if (static_cast<long long>(dims->batch) * nck * cache->num_kv_heads * 2 *
@@ -351,12 +355,14 @@ static int prepare_decode(const void* q, const void* rel, IoTypes io,
     return RELATTN_OK;
   }
   // An even number of stages: the decode kernel's two consumer groups each
-  // own every other stage.
+  // own every other stage (any number when they split the rows and both
+  // take every stage).
+  p.rs = split ? 1 : 0;
   p.nstages = io.kv_es == 1 ? kMaxStagesE4m3 : kMaxStages;
   while (p.nstages >= 2 &&
          decode_smem_bytes(p.nstages, p.B, p.Bv, p.kpc, p.g, p.dv, p.rel_es, p.kv_es) >
              di->smem_optin)
-    p.nstages -= 2;
+    p.nstages -= split ? 1 : 2;
   if (p.nstages < 2) return RELATTN_ERR_UNSUPPORTED;  // batch too large for shared memory
   // whole tiles, and (one-token kernel, bf16 cache) half tiles for the edges
   // of a sequence's key range

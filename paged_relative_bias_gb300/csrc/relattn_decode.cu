@@ -45,7 +45,7 @@ constexpr int kConsumerWarps = 8;  // two groups of four
 constexpr int kDecodeThreads = 32 * (1 + kConsumerWarps);
 constexpr int kConsumerThreads = 32 * kConsumerWarps;
 constexpr int kWholeSlackTiles = 4;  // tolerated imbalance to avoid a split
-constexpr int kQBufBytes = 4096;     // 16 rows x 256 B as two swizzled halves
+constexpr int kQBufBytes = 4096;     // 16 rows x 256 B as two swizzled halves (32 rows: twice)
 constexpr int kMiscAbort = 14;       // shared flag word: a consumer warp gave up waiting
 // e4m3 cache, f16 query fragments.  One-token kernel: per consumer warp,
 // its lanes' B fragments of Q^T for the eight k-steps of d_qk = 128 (8 x 32
@@ -100,20 +100,25 @@ __host__ __device__ constexpr int rel_token_bytes(int g, int es) {
 // the stages (kpc token boxes each) live in a ring of their own;
 // per-sequence lengths take B entries, tile counts and prefixes Bv.
 struct DecodeSmem {
-  int qbuf, stages, stage_bytes, priv, rel, rel_bytes, slices, bars, valid, seqlen, nt, pref, m,
-      l, misc, total;
+  int qbuf, qbytes, stages, stage_bytes, priv, rel, rel_bytes, slices, bars, valid, seqlen, nt,
+      pref, m, l, misc, total;
   __host__ __device__ DecodeSmem(int nstages, int B, int Bv, int kpc, int g, int dv, int rel_es,
                                  int kv_es) {
     stage_bytes = kTileKeys * (kDqk + dv) * kv_es;
     rel_bytes = kpc * rel_token_bytes(g, rel_es);
+    // chunks of up to 32 rows are split between the two consumer groups
+    const int rows = kpc * g;
+    const int halves = rows > kMaxDecodeRows ? 2 : 1;
     qbuf = 0;
-    stages = qbuf + 2 * kQBufBytes;
+    qbytes = halves * kQBufBytes;
+    stages = qbuf + 2 * qbytes;
     priv = stages + nstages * stage_bytes;
     // the general kernel runs when a tile packs several tokens or g > 8
     const bool multi = kpc > 1 || g > 8;
-    rel = priv + (kv_es == 1 ? (multi ? kPrivQA : kConsumerWarps * kPrivQ) : 0);
+    rel = priv + (kv_es == 1 ? (multi ? halves * kPrivQA : kConsumerWarps * kPrivQ) : 0);
     slices = rel + nstages * rel_bytes;
-    bars = (slices + kConsumerWarps * kpc * g * (dv + kSlicePad) * 4 + 15) & ~15;
+    const int wrows = rows < kMaxDecodeRows ? rows : kMaxDecodeRows;  // rows of one warp
+    bars = (slices + kConsumerWarps * wrows * (dv + kSlicePad) * 4 + 15) & ~15;
     valid = bars + (2 * nstages + 4) * 8;
     seqlen = valid + nstages * 4;
     nt = seqlen + B * 4;
@@ -532,7 +537,9 @@ struct HalfMaps<false> {};
 // e4m3; the consumer warps widen its bytes to f16 in registers and the MMAs
 // take f16 operands.  LS: per-token logit factors are given (general kernel
 // only: the one-token kernel reads them whenever they are given, at no cost).
-template <int DV, bool MULTI, bool R16, bool KV8, bool LS>
+// RS (general kernel only): a chunk of up to 32 rows, both consumer groups
+// on every tile, group grp taking rows 16 grp .. 16 grp + 15.
+template <int DV, bool MULTI, bool R16, bool KV8, bool LS, bool RS>
 __global__ void __launch_bounds__(kDecodeThreads, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tm_q,
                   const __grid_constant__ CUtensorMap tm_k,
@@ -556,6 +563,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   constexpr int SP = NB == 1 ? 4 : kSlicePad;
   static_assert(!KV8 || DV == 128, "e4m3 caches: d_v = 128");
   static_assert(!LS || MULTI, "logit factors: a template case of the general kernel only");
+  static_assert(!RS || MULTI, "row split: the general kernel only");
+  constexpr int QH = RS ? 2 * 2048 : 2048;  // bytes of one 64-column half of a query buffer
+  constexpr int QB = 2 * QH;                // bytes of a query buffer (DecodeSmem::qbytes)
   const DecodeSmem L(ns, p.B, p.Bv, tok.kpc, g, DV, RES, KV8 ? 1 : 2);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
   uint64_t* empty = full + ns;
@@ -576,7 +586,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   if (warp == 0) {
     if (lane < 2 * ns + 4)
       mbar_init(&full[lane], lane < ns ? 1
-                             : lane < 2 * ns ? kConsumerWarps / 2
+                             : lane < 2 * ns ? (RS ? kConsumerWarps : kConsumerWarps / 2)
                              : lane < 2 * ns + 2 ? 1 : kConsumerWarps);
     fence_mbar_init();
     if (lane == 0) {
@@ -608,14 +618,14 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       report(p.status, RELATTN_DEV_WAIT_TIMEOUT);
       return false;
     }
-    uint8_t* qs = smem + L.qbuf + qb * kQBufBytes;
+    uint8_t* qs = smem + L.qbuf + qb * QB;
     mbar_arrive_expect_tx(&qfull[qb], q_tx);
     if constexpr (MULTI) {
       tma_load_3d(qs, &tm_q, &qfull[qb], 0, kvh * g, sq.b * tok.k + sq.i0);
-      tma_load_3d(qs + 2048, &tm_q, &qfull[qb], 64, kvh * g, sq.b * tok.k + sq.i0);
+      tma_load_3d(qs + QH, &tm_q, &qfull[qb], 64, kvh * g, sq.b * tok.k + sq.i0);
     } else {  // q [B * Hq][128]: the g rows of the group
       tma_load_2d(qs, &tm_q, &qfull[qb], 0, sq.b * p.Hq + kvh * g);
-      tma_load_2d(qs + 2048, &tm_q, &qfull[qb], 64, sq.b * p.Hq + kvh * g);
+      tma_load_2d(qs + QH, &tm_q, &qfull[qb], 64, sq.b * p.Hq + kvh * g);
     }
     return true;
   };
@@ -779,6 +789,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   // more than one phase ahead of the phase it last consumed there (the
   // parity waits below would alias otherwise).
   const int grp = cwarp >> 2;
+  const int ro = RS ? 16 * grp : 0;  // the group's first row of a chunk
   const int ctid = tid - 32;         // 0..255
   const int r0 = lane >> 2, cq = lane & 3;
   float* s_m = reinterpret_cast<float*>(smem + L.m);
@@ -799,7 +810,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     int rP[2], rlo[2], rrel[2];
 #pragma unroll
     for (int rr = 0; rr < 2; ++rr) {
-      const int row = r0 + 8 * rr;
+      const int row = ro + r0 + 8 * rr;
       const int ti = tok.token_of_row(row, g);
       rv[rr] = row < nrows;
       rP[rr] = sq.pf + ti;
@@ -816,7 +827,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     if ((LS || !MULTI) && p.logit_scale != nullptr) {
 #pragma unroll
       for (int rr = 0; rr < 2; ++rr) {
-        const int ti = NB == 1 ? 0 : tok.token_of_row(r0 + 8 * rr, g);
+        const int ti = NB == 1 ? 0 : tok.token_of_row(ro + r0 + 8 * rr, g);
         if (NB == 1 || rv[rr])
           fr[rr] = __ldg(p.logit_scale + static_cast<size_t>(sq.b) * p.k + sq.i0 + ti);
       }
@@ -836,13 +847,16 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         const int fl = ctid & 31, fs = ctid >> 5;
         const int fr = fl >> 2, ft = fl & 3;
         const int d0 = 64 * (ft >> 1) + 16 * (fs >> 1) + 8 * (ft & 1) + 4 * (fs & 1);
-        const uint8_t* qsrc = smem + L.qbuf + qb * kQBufBytes;
+        const uint8_t* qsrc = smem + L.qbuf + qb * QB;
         auto pair = [&](int row, int d) {  // bf16 of dimensions d, d + 1 -> f16
           return bf16x2_to_f16x2(*reinterpret_cast<const uint32_t*>(
-              qsrc + (d >> 6) * 2048 + sw128(row, (d & 63) >> 3) + (d & 7) * 2));
+              qsrc + (d >> 6) * QH + sw128(row, (d & 63) >> 3) + (d & 7) * 2));
         };
-        reinterpret_cast<uint4*>(smem + L.priv)[fs * 32 + fl] =
-            make_uint4(pair(fr, d0), pair(fr + 8, d0), pair(fr, d0 + 2), pair(fr + 8, d0 + 2));
+#pragma unroll
+        for (int h = 0; h < (RS ? 2 : 1); ++h)  // RS: rows 16 h .. 16 h + 15 for group h
+          reinterpret_cast<uint4*>(smem + L.priv + h * kPrivQA)[fs * 32 + fl] =
+              make_uint4(pair(16 * h + fr, d0), pair(16 * h + fr + 8, d0),
+                         pair(16 * h + fr, d0 + 2), pair(16 * h + fr + 8, d0 + 2));
       } else if (lane == 0) {
         s_misc[kMiscAbort] = 1;
       }
@@ -857,7 +871,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     // the query rows stay in their buffer for the whole piece: each tile
     // reads its A fragments from there, one k-step at a time, rather than
     // holding all 32 registers of them next to the 4 x d_v/8 of O
-    const uint32_t qbase = smem_u32(smem + L.qbuf + qb * kQBufBytes);
+    const uint32_t qbase = smem_u32(smem + L.qbuf + qb * QB);
     // e4m3 cache: the MMAs run in f16.  The lane's B fragments of Q^T (row
     // r0) for the eight k-steps go to the warp's buffer once per piece, in the
     // order of the dimensions of its K fragments (below), after which the
@@ -868,7 +882,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const uint4 v = *reinterpret_cast<const uint4*>(
-            smem + L.qbuf + qb * kQBufBytes + (cq >> 1) * 2048 + sw128(r0, 2 * u + (cq & 1)));
+            smem + L.qbuf + qb * QB + (cq >> 1) * QH + sw128(r0, 2 * u + (cq & 1)));
         qfrag[(2 * u) * 32 + lane] = make_uint2(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y));
         qfrag[(2 * u + 1) * 32 + lane] = make_uint2(bf16x2_to_f16x2(v.z), bf16x2_to_f16x2(v.w));
       }
@@ -886,7 +900,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
 #pragma unroll
     for (int i = 0; i < DV / 8 / (2 / NB); ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
 
-    for (int t = (n_base + grp) & 1 ? 1 : 0; t < pc.n; t += 2) {
+    for (int t = RS ? 0 : ((n_base + grp) & 1 ? 1 : 0); t < pc.n; t += RS ? 1 : 2) {
       const int n = n_base + t;
       const int stage = n % ns;
       const int tile = sq.tile_first + pc.i0 + t;
@@ -953,7 +967,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
                       ka[3]);
               const int qchunk = ks * 2 + qhalf;
               uint32_t qb0, qb1;
-              ldsm_x2(qbase + (qchunk >> 3) * 2048 + sw128(qrow, qchunk & 7), qb0, qb1);
+              ldsm_x2(qbase + (qchunk >> 3) * QH + sw128(qrow, qchunk & 7), qb0, qb1);
               mma_16816(sT, ka, qb0, qb1);
             }
           }
@@ -1048,7 +1062,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
             // one-token kernel: k-step pair u of this lane covers dimensions
             // 64 (cq >> 1) + 16 u + 8 (cq & 1) + 0..7 of key r0 of each
             // 8-key half; the A fragments of Q were written in that order
-            const uint4* qf = reinterpret_cast<const uint4*>(smem + L.priv);
+            const uint4* qf = reinterpret_cast<const uint4*>(smem + L.priv + (RS ? grp * kPrivQA : 0));
             const uint8_t* kr = st + (16 * cw + r0) * 128 + (cq & 1) * 8;
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
@@ -1068,12 +1082,12 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
             }
           } else {
             const int key = 16 * cw + (mi >> 1) * 8 + (lane & 7);
-            const int qrow = (mi & 1) * 8 + (lane & 7);
+            const int qrow = ro + (mi & 1) * 8 + (lane & 7);
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
               const int qchunk = ks * 2 + (mi >> 1);
               uint32_t qa[4];
-              ldsm_x4(qbase + (qchunk >> 3) * 2048 + sw128(qrow, qchunk & 7), qa[0], qa[1],
+              ldsm_x4(qbase + (qchunk >> 3) * QH + sw128(qrow, qchunk & 7), qa[0], qa[1],
                       qa[2], qa[3]);
               const int chunk = ks * 2 + (mi & 1);
               uint32_t b0, b1, b2, b3;
@@ -1225,7 +1239,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     // Each warp leaves its unscaled O rows in its slice; after one barrier
     // the threads that write out weigh the eight slices of their row by
     // exp2(m_w - M) themselves, so no second round of scaling is needed.
-    const int srows = tok.kpc * g;  // rows of a warp's merge slice
+    const int srows = RS ? kMaxDecodeRows : tok.kpc * g;  // rows of a warp's merge slice
     if constexpr (NB == 1) {
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
@@ -1281,22 +1295,27 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     };
     for (int idx = ctid; idx < nrows * DV / 2; idx += kConsumerThreads) {
       const int row = idx / (DV / 2), col = 2 * (idx % (DV / 2));
-      // the row's (m, l) of every warp, loaded together, then combined
-      float mw[kConsumerWarps], lw[kConsumerWarps];
-      float2 vw[kConsumerWarps];
+      // the row's (m, l) of every warp that holds it (RS: the four warps of
+      // its group, at its row within the group), loaded together, combined
+      constexpr int NW = RS ? kConsumerWarps / 2 : kConsumerWarps;
+      const int w0 = RS ? NW * (row / kMaxDecodeRows) : 0;
+      const int lr = RS ? row % kMaxDecodeRows : row;
+      float mw[NW], lw[NW];
+      float2 vw[NW];
 #pragma unroll
-      for (int w = 0; w < kConsumerWarps; ++w) {
-        mw[w] = s_m[w * 16 + row];
-        lw[w] = s_l[w * 16 + row];
-        vw[w] = *reinterpret_cast<const float2*>(slices + (w * srows + row) * (DV + SP) + col);
+      for (int w = 0; w < NW; ++w) {
+        mw[w] = s_m[(w0 + w) * 16 + lr];
+        lw[w] = s_l[(w0 + w) * 16 + lr];
+        vw[w] = *reinterpret_cast<const float2*>(slices + ((w0 + w) * srows + lr) * (DV + SP) +
+                                                 col);
       }
       float M = mw[0];
 #pragma unroll
-      for (int w = 1; w < kConsumerWarps; ++w) M = fmaxf(M, mw[w]);
+      for (int w = 1; w < NW; ++w) M = fmaxf(M, mw[w]);
       float Ls = 0.f, v0 = 0.f, v1 = 0.f;
       if (M != kNegInf) {
 #pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) {
+        for (int w = 0; w < NW; ++w) {
           const float wt = ex2(mw[w] - M);
           Ls += lw[w] * wt;
           v0 += vw[w].x * wt;
@@ -1314,10 +1333,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       } else {  // a partial: normalised over its own keys, no sink or gate yet
         const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
         *reinterpret_cast<float2*>(
-            p.part_o + (static_cast<size_t>(slot) * kMaxDecodeRows + row) * DV + col) =
+            p.part_o + (static_cast<size_t>(slot) * kMaxChunkRows + row) * DV + col) =
             make_float2(v0 * inv, v1 * inv);
         if (col == 0)
-          p.part_lse[slot * kMaxDecodeRows + row] = Ls > 0.f ? M + lg2(Ls) : kNegInf;
+          p.part_lse[slot * kMaxChunkRows + row] = Ls > 0.f ? M + lg2(Ls) : kNegInf;
       }
     }
     if (!whole) {
@@ -1338,9 +1357,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
 #pragma unroll 4
           for (int cc = c1; cc <= c2; ++cc) {
             const int sl = cc == c1 ? slot1 : 2 * cc;
-            const float lse = __ldcg(p.part_lse + sl * kMaxDecodeRows + row);
+            const float lse = __ldcg(p.part_lse + sl * kMaxChunkRows + row);
             const float ov =
-                __ldcg(p.part_o + (static_cast<size_t>(sl) * kMaxDecodeRows + row) * DV + col);
+                __ldcg(p.part_o + (static_cast<size_t>(sl) * kMaxChunkRows + row) * DV + col);
             if (lse == kNegInf) continue;
             const float M2 = fmaxf(M, lse);
             const float sc = ex2(M - M2);  // 0 while M is -inf
@@ -1412,9 +1431,9 @@ int decode_smem_bytes(int nstages, int B, int Bv, int kpc, int g, int dv, int re
   return DecodeSmem(nstages, B, Bv, kpc, g, dv, rel_es, kv_es).total + 1024;
 }
 
-template <int DV, bool MULTI, bool R16, bool KV8, bool LS = false>
-static cudaError_t launch_decode_as(const DecodeLaunch& L, int smem, cudaStream_t stream) {
-  cudaError_t e = ensure_smem<decode_kernel<DV, MULTI, R16, KV8, LS>>(smem);
+template <int DV, bool MULTI, bool R16, bool KV8, bool LS, bool RS>
+static cudaError_t launch_decode_rs(const DecodeLaunch& L, int smem, cudaStream_t stream) {
+  cudaError_t e = ensure_smem<decode_kernel<DV, MULTI, R16, KV8, LS, RS>>(smem);
   if (e != cudaSuccess) return e;
   // Programmatic stream serialisation: the kernel may begin while the
   // previous kernel on the stream finishes (see grid_dep_wait in the kernel).
@@ -1433,8 +1452,17 @@ static cudaError_t launch_decode_as(const DecodeLaunch& L, int smem, cudaStream_
     hm.k = L.tm_kh;
     hm.v = L.tm_vh;
   }
-  return cudaLaunchKernelEx(&cfg, decode_kernel<DV, MULTI, R16, KV8, LS>, L.tm_q, L.tm_k, L.tm_v,
-                            L.tm_rel, hm, L.p);
+  return cudaLaunchKernelEx(&cfg, decode_kernel<DV, MULTI, R16, KV8, LS, RS>, L.tm_q, L.tm_k,
+                            L.tm_v, L.tm_rel, hm, L.p);
+}
+
+// The general kernel has a copy for chunks split between the consumer groups.
+template <int DV, bool MULTI, bool R16, bool KV8, bool LS = false>
+static cudaError_t launch_decode_as(const DecodeLaunch& L, int smem, cudaStream_t stream) {
+  if constexpr (MULTI) {
+    if (L.p.rs) return launch_decode_rs<DV, MULTI, R16, KV8, LS, true>(L, smem, stream);
+  }
+  return launch_decode_rs<DV, MULTI, R16, KV8, LS, false>(L, smem, stream);
 }
 
 template <int DV, bool MULTI>

@@ -45,8 +45,9 @@ struct DecodeParams {
   // with the g heads into the rows of one tile: nck = ceil(k / kpc) chunks
   // per sequence, Bv = B * nck chunks ("virtual sequences") in all
   int k, kpc, nck, Bv;
-  int nstages;  // even: see the consumer groups of decode_kernel
+  int nstages;  // even unless rows are split: see the consumer groups of decode_kernel
   float scale_log2;  // log2(e) / sqrt(d_qk)
+  int rs;            // 1: chunks of up to 32 rows, split between the consumer groups
 };
 
 // Raise kernel K's dynamic shared-memory limit to `smem` bytes on the current
@@ -113,6 +114,10 @@ struct PrefillLaunch {
 
 int decode_smem_bytes(int nstages, int B, int Bv, int kpc, int g, int dv, int rel_es, int kv_es);
 constexpr int kMaxDecodeRows = 16;         // rows of one decode tile: g heads x tokens
+constexpr int kMaxChunkRows = 32;          // rows of one chunk (two tiles' rows when split)
+// The general kernel splits a chunk's rows between its two consumer groups
+// when more tokens than one 16-row tile holds share a KV head (g <= 8).
+inline bool decode_row_split(int k, int g) { return g <= 8 && k * g > kMaxDecodeRows; }
 // The decode kernel has a one-token instantiation for tiles of at most 8 rows
 // and a general one (several tokens, or g > 8), which also takes its query
 // rows through a 3-D copy.
