@@ -165,8 +165,10 @@ int relattn_decode(const void* q, const float* rel,
  *   depend on k.
  *
  * The g heads of a KV head and up to 16 / g of the tokens share one tile and
- * one read of their keys; larger k is cut into chunks of that many tokens,
- * each reading the keys its tokens see.
+ * one read of their keys; when more tokens than that share a KV head (and
+ * g <= 8), up to 32 / g of them share a read, their rows split between two
+ * tiles.  Larger k is cut into chunks of that many tokens, each reading the
+ * keys its tokens see.
  */
 int relattn_decode_multi(const void* q, const float* rel,
                          const relattn_kv_cache* kv_cache,
