@@ -864,10 +864,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       if (s_misc[kMiscAbort]) qok = false;
       else if (lane == 0) mbar_arrive(&qempty[qb]);
     }
-    if (!qok) {
-      abort = true;
-      break;
-    }
+    // A failed query wait does not leave the piece loop here: the warp skips
+    // the tiles and meets the other warps at the merge barrier, after which
+    // they all see the abort flag and leave together (a warp leaving early
+    // would strand the others at that barrier).
+    if (!qok) abort = true;
     // the query rows stay in their buffer for the whole piece: each tile
     // reads its A fragments from there, one k-step at a time, rather than
     // holding all 32 registers of them next to the 4 x d_v/8 of O
@@ -878,7 +879,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     // shared query buffer is released.  k-step pair u reads dimensions
     // 64 (cq >> 1) + 16 u + 8 (cq & 1) + 0..7: one 16-byte piece of the row.
     uint2* const qfrag = reinterpret_cast<uint2*>(smem + L.priv + cwarp * kPrivQ);
-    if constexpr (KV8 && !MULTI) {
+    if (KV8 && !MULTI && qok) {
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const uint4 v = *reinterpret_cast<const uint4*>(
@@ -900,7 +901,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
 #pragma unroll
     for (int i = 0; i < DV / 8 / (2 / NB); ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
 
-    for (int t = RS ? 0 : ((n_base + grp) & 1 ? 1 : 0); t < pc.n; t += RS ? 1 : 2) {
+    for (int t = RS ? 0 : ((n_base + grp) & 1 ? 1 : 0); t < pc.n && !abort; t += RS ? 1 : 2) {
       const int n = n_base + t;
       const int stage = n % ns;
       const int tile = sq.tile_first + pc.i0 + t;
