@@ -69,9 +69,13 @@ def test_multi_gqa4(k, W, E):
 
 
 @pytest.mark.parametrize("Hq,Hkv,k,dv", [(4, 4, 16, 128), (4, 4, 7, 64), (12, 2, 5, 128),
-                                         (16, 2, 3, 128), (32, 2, 2, 64), (24, 8, 9, 64)])
+                                         (16, 2, 3, 128), (32, 2, 2, 64), (24, 8, 9, 64),
+                                         (4, 2, 16, 128), (16, 2, 2, 64)])
 def test_multi_head_ratios(Hq, Hkv, k, dv):
-    """Every packing: g = 1 (16 tokens a tile), 3, 6, 8, 16 (one token a tile)."""
+    """Every packing: g = 1 (16 tokens a tile), 2, 3, 6, 8, 16 (one token a
+    tile); rows split between the consumer groups when more than 16 rows
+    share a KV head (g = 2 with 16 tokens, g = 3 with 9, g = 6 with 5, g = 8
+    with 3), one 16-row tile otherwise (g = 8 with 2)."""
     case = I.make_decode(wl("ratio", 3, Hq, Hkv, 300, 512, k, ("uniform", k, 2500), dv=dv),
                          DEV, seed_data=30 + Hq + k, seed_layout=31)
     check(case, what=f"Hq={Hq} Hkv={Hkv} k={k} dv={dv}")
@@ -102,9 +106,9 @@ def test_multi_any_split_matches(num_ctas):
 
 def test_multi_many_chunks_block_prologue():
     """More than 32 chunks: the whole block plans the split (not one warp)."""
-    case = I.make_decode(wl("many", 20, 32, 8, 512, 512, 8, ("uniform", 8, 5000)), DEV,
+    case = I.make_decode(wl("many", 40, 32, 8, 512, 512, 8, ("uniform", 8, 5000)), DEV,
                          seed_data=51)
-    check(case, what="B=20 k=8")
+    check(case, what="B=40 k=8")
 
 
 def test_multi_one_token_equals_decode_bitwise():
