@@ -74,6 +74,19 @@ __device__ __forceinline__ void named_barrier(int id, int nthreads) {
 
 // Arrive at a named barrier without waiting (the producer side of a
 // hand-off to warps that wait with named_barrier on the same id and count).
+// Named barrier that also ORs a predicate over its threads: every thread
+// gets the same answer, so they can all take the same branch after it.
+__device__ __forceinline__ bool named_barrier_or(int id, int nthreads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
+}
+
 __device__ __forceinline__ void named_barrier_arrive(int id, int nthreads) {
   asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }

@@ -617,10 +617,15 @@ __global__ void __launch_bounds__(32 * (kPfWarps + (KV8 ? 1 : 0)), 1)
     for (int idx = blockIdx.x; idx < total && !*s_abort; idx += gridDim.x, ++items) {
       PItem it;
       prefill_item(idx, p, s_cu0, s_n, s_ctx, s_qpref, it);
+      // A wait that gives up marks the item bad: the warp skips the rest of
+      // its work but still meets the other softmax warps at the barrier
+      // before the epilogue, after which all four leave together (a warp
+      // leaving alone would strand the others at a named barrier).
+      bool bad = false;
       if (items == 0) {  // later items' queries are loaded during the previous epilogue
         const uint8_t* qs = slot_wait(e);
-        if (!qs) { fail = true; break; }
-        load_q(qs, e);
+        if (!qs) bad = true;
+        else load_q(qs, e);
         ++e;
       }
       const bool row_ok = r < it.rows;
@@ -641,9 +646,9 @@ __global__ void __launch_bounds__(32 * (kPfWarps + (KV8 ? 1 : 0)), 1)
       }
       const int dmax = p.window > 0 ? p.window - 1 : 0x7fffffff;  // visible d in [0, dmax]
       float m_used = kNegInf, l = 0.f;
-      bool ok = true;
+      bool ok = !bad;
       int next_id = __ldg(trow + (it.tf >> 1));
-      for (int k = 0; k < it.ntiles; ++k, ++n, ++e) {
+      for (int k = 0; k < it.ntiles && ok; ++k, ++n, ++e) {
         const int s = n & 1;
         const int j0 = (it.tf + k) * kTileKeys;
         const int id = next_id;
@@ -748,24 +753,27 @@ __global__ void __launch_bounds__(32 * (kPfWarps + (KV8 ? 1 : 0)), 1)
       }
       // the item's last PV (phase n - 1) completes O, and every S = Q K^T of
       // the item with it
-      if (!ok || !mbar_wait(&bars[kOFull], (n - 1) & 1)) { fail = true; break; }
+      if (!ok || !mbar_wait(&bars[kOFull], (n - 1) & 1)) bad = true;
       tc_fence_after();
       // The next item's query goes into TMEM first, so its first S = Q K^T
       // runs while this item's O is stored.  Its ring entry follows the
       // O scratch entry.
       const bool has_next = idx + static_cast<int>(gridDim.x) < total;
-      if (has_next) {
+      if (has_next && !bad) {
         const uint8_t* qs = slot_wait(e + 1);
-        if (!qs) { fail = true; break; }
-        load_q(qs, e + 1);
+        if (!qs) bad = true;
+        else load_q(qs, e + 1);
       }
       // O / l -> out, through the scratch slot (the tile's 128 rows, 16-byte
       // chunks swizzled by row / 4) so that the global stores are whole rows
       // (16 lanes per 256-byte row).  A bf16 row is DV * 2 bytes; an fp32 row
       // is twice that and goes in two halves of DV / 2 columns, each the size
       // of a bf16 row.
-      uint8_t* scr = slot_wait(e);
-      if (!scr) { fail = true; break; }
+      uint8_t* scr = bad ? nullptr : slot_wait(e);
+      if (!scr) bad = true;
+      // the four softmax warps, once per item: all leave if any thread gave
+      // up a wait or another role raised the abort flag
+      if (named_barrier_or(1, 128, bad || *s_abort)) { fail = true; break; }
       // 1 / normaliser; the optional sink logit (not scaled by the factor)
       // joins it, against l's reference f m_used, and the optional gate's
       // sigmoid scales the row
