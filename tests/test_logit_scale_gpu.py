@@ -6,7 +6,6 @@ relattn_decode_ex / relattn_prefill_ex.  A factor of 1 reproduces the plain
 output bit for bit; a sink logit is not scaled.
 """
 
-import numpy as np
 import pytest
 import torch
 

@@ -4,7 +4,6 @@ import numpy as np
 import pytest
 import torch
 
-from oracle import relattn_oracle as O
 from paged_relative_bias_gb300 import inputs as I
 from paged_relative_bias_gb300 import relattn as R
 from paged_relative_bias_gb300.inputs import bf16_bits

@@ -12,7 +12,6 @@ from collections import defaultdict
 
 import numpy as np
 import pytest
-import torch
 
 from oracle import relattn_oracle as O
 from paged_relative_bias_gb300 import inputs as I
