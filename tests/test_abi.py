@@ -158,3 +158,39 @@ def test_ctypes_structures_match_the_header():
             base, star, field = m.groups()
             fields.append((field, ctypes.c_void_p if star else ctype[base]))
         assert [(f, t) for f, t in cls._fields_] == fields, name
+
+
+def test_options_and_cache_write_rejected_on_host(lib):
+    """relattn_options and relattn_cache_write arguments that are not offered
+    fail before any CUDA work (no GPU is needed to see the codes)."""
+    dims = R.Dims(1, 4, 2, 16, 16, 0)
+    cache = R.KVCacheDesc(16, 16, 2, 128, 1, 128, 128)
+    e4m3_64 = R.KVCacheDesc(16, 16, 2, 128, 1, 128, 64)
+
+    def opts(rel=R.DTYPE_F32, out=R.DTYPE_BF16, sink=None, kv=R.DTYPE_BF16, ks=1.0, vs=1.0,
+             ls=None):
+        return R.Options(rel, out, sink, None, kv, ks, vs, ls)
+
+    def decode_ex(o):
+        return lib.relattn_decode_ex(16, 16, ctypes.byref(o), ctypes.byref(cache), 16, 16, 1, 0,
+                                     64, ctypes.byref(dims), 16, 16, 1 << 20, None)
+
+    assert decode_ex(opts(rel=7)) == R.ERR_INVALID_ARG            # unknown rel type
+    assert decode_ex(opts(out=R.DTYPE_E4M3)) == R.ERR_INVALID_ARG  # e4m3 is no output type
+    assert decode_ex(opts(sink=18)) == R.ERR_INVALID_ARG           # sink not 4-byte aligned
+    assert decode_ex(opts(ls=18)) == R.ERR_INVALID_ARG             # factors not aligned
+    assert decode_ex(opts(kv=R.DTYPE_E4M3, ks=0.0)) == R.ERR_INVALID_ARG  # scale must be > 0
+    assert decode_ex(opts(kv=5)) == R.ERR_INVALID_ARG
+
+    def write(k=16, v=16, o=None, c=cache, d=dims, ws=16, ws_bytes=256):
+        return lib.relattn_cache_write(k, v, None if o is None else ctypes.byref(o), 16,
+                                       ctypes.byref(c), 16, 16, ctypes.byref(d), ws, ws_bytes,
+                                       None)
+
+    assert write(k=None) == R.ERR_INVALID_ARG
+    assert write(k=24) == R.ERR_INVALID_ARG                      # k not 16-byte aligned
+    assert write(ws_bytes=128) == R.ERR_WORKSPACE                # below the status word
+    assert write(o=opts(rel=9)) == R.ERR_INVALID_ARG
+    assert write(o=opts(kv=R.DTYPE_E4M3, ks=0.5, vs=0.5), c=e4m3_64) == R.ERR_UNSUPPORTED
+    assert write(d=R.Dims(70000, 4, 2, 16, 16, 0)) == R.ERR_UNSUPPORTED  # > 65535 sequences
+    assert write(d=R.Dims(0, 4, 2, 0, 0, 0)) == R.OK             # nothing to write: no launch
