@@ -421,6 +421,18 @@ int relattn_debug_walk_prefill(const int32_t* cu_seqlens,
                                void* workspace, size_t workspace_bytes,
                                void* stream);
 
+/*
+ * Test hook for failure detection: one thread waits on a shared-memory
+ * barrier that nothing completes.  Every wait in the library's kernels has a
+ * limit (about 2 s) after which it gives up, records
+ * RELATTN_DEV_WAIT_TIMEOUT in the workspace's status word and lets the kernel
+ * end; this call exercises that path on its own, so a test can see the
+ * status bit and that the context stays usable.  Returns after enqueueing
+ * (the kernel runs for about 2 s); RELATTN_ERR_WORKSPACE for a workspace
+ * below 256 bytes or not 16-byte aligned.
+ */
+int relattn_debug_wait_timeout(void* workspace, size_t workspace_bytes, void* stream);
+
 /* ABI version of this header (major * 100 + minor). */
 int relattn_abi_version(void);
 

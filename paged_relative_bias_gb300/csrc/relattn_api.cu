@@ -689,6 +689,13 @@ int relattn_cache_write(const void* k, const void* v, const relattn_options* opt
   return to_status(launch_cache_write(p, static_cast<cudaStream_t>(stream)));
 }
 
+int relattn_debug_wait_timeout(void* workspace, size_t workspace_bytes, void* stream) {
+  if (!workspace || !aligned16(workspace) || workspace_bytes < kStatusBytes)
+    return RELATTN_ERR_WORKSPACE;
+  return to_status(
+      launch_wait_timeout(static_cast<uint32_t*>(workspace), static_cast<cudaStream_t>(stream)));
+}
+
 int relattn_debug_walk_prefill(const int32_t* cu_seqlens, const int32_t* ctx_lens,
                                const int32_t* block_table, int32_t window,
                                const relattn_kv_cache* cache, const relattn_dims* dims,

@@ -127,6 +127,7 @@ cudaError_t launch_decode(const DecodeLaunch& L, cudaStream_t stream);
 cudaError_t launch_decode_walk(const DecodeParams& p, int grid, cudaStream_t stream);
 
 cudaError_t launch_cache_write(const PrefillParams& p, cudaStream_t stream);
+cudaError_t launch_wait_timeout(uint32_t* status, cudaStream_t stream);
 constexpr int kCacheWriteMaxGridY = 65535;  // sequences of one cache-write launch
 int prefill_smem_bytes(int B, int dv, int ring_stages, int kv_es);
 int prefill_ring_stages(int B, int dv, int kv_es, int smem_optin);  // 0 if nothing fits

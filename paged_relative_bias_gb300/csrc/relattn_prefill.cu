@@ -907,6 +907,21 @@ int prefill_ring_stages(int B, int dv, int kv_es, int smem_optin) {
   return 0;
 }
 
+// One thread waits on a barrier that nothing completes; the bounded wait
+// gives up after its limit and reports it in the status word.
+__global__ void wait_timeout_kernel(uint32_t* status) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x != 0) return;
+  mbar_init(&bar, 1);
+  fence_mbar_init();
+  if (!mbar_wait(&bar, 0)) report(status, RELATTN_DEV_WAIT_TIMEOUT);
+}
+
+cudaError_t launch_wait_timeout(uint32_t* status, cudaStream_t stream) {
+  wait_timeout_kernel<<<1, 32, 0, stream>>>(status);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_cache_write(const PrefillParams& p, cudaStream_t stream) {
   const dim3 grid((p.max_q_len + kCwTile - 1) / kCwTile, p.B);
   if (p.kv_es == 1)

@@ -41,6 +41,7 @@ EXPORTS = (
     "relattn_decode_ex",
     "relattn_prefill_ex",
     "relattn_cache_write",
+    "relattn_debug_wait_timeout",
 )
 
 DTYPE_F32 = 0
@@ -133,6 +134,8 @@ def lib() -> ctypes.CDLL:
     L.relattn_cache_write.argtypes = [c_void_p, c_void_p, POINTER(Options), c_void_p, P,
                                       c_void_p, c_void_p, S, c_void_p, c_size_t, c_void_p]
     L.relattn_cache_write.restype = c_int
+    L.relattn_debug_wait_timeout.argtypes = [c_void_p, c_size_t, c_void_p]
+    L.relattn_debug_wait_timeout.restype = c_int
     L.relattn_abi_version.argtypes = []
     L.relattn_abi_version.restype = c_int
     _LIB = L
