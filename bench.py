@@ -807,7 +807,8 @@ def main():
     ap.add_argument("--rel", choices=["f32", "bf16"], default="f32",
                     help="element type of the rel input of the timed workload")
     ap.add_argument("--kv", choices=["bf16", "fp8"], default="bf16",
-                    help="element type of the decode KV cache of the timed workload")
+                    help="element type of the KV cache of the timed workload (decode or "
+                         "prefill)")
     ap.add_argument("--pool", choices=["per-set", "shared"], default="per-set",
                     help="decode input sets: one KV pool each (default), or one shared pool "
                          "with renumbered block tables (small device footprint, for ncu)")
