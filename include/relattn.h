@@ -45,8 +45,10 @@
  *    status word and carries on.  A skipped sequence's output rows are zero.
  *  - The workspace (size from relattn_workspace_size) must be zero-filled
  *    once before first use (relattn_workspace_init).  Calls leave it ready for
- *    the next call.  Calls that share one workspace must be ordered on one
- *    stream: concurrent calls on the same workspace race.
+ *    the next call, also a call whose waits gave up (its split counters still
+ *    complete and return to zero); the status word keeps its bits until the
+ *    workspace is zero-filled again.  Calls that share one workspace must be
+ *    ordered on one stream: concurrent calls on the same workspace race.
  */
 #ifndef RELATTN_H_
 #define RELATTN_H_
@@ -283,8 +285,10 @@ int relattn_decode_ex(const void* q, const void* rel, const relattn_options* opt
  *    exceeds RELATTN_NOALLOC_SCRATCH_BYTES, the call returns
  *    RELATTN_ERR_WORKSPACE and enqueues nothing.
  *  - The first call on a device looks up the array's device address (once,
- *    with that device current); make that first call before any stream
- *    capture on that device.
+ *    with that device current) and keeps it for the life of the process;
+ *    make that first call before any stream capture on that device.  Calls
+ *    must run in the device's primary context (the runtime's), and not after
+ *    cudaDeviceReset, since either would leave the kept address stale.
  *  - Every call clears the status word and counters of the array on `stream`
  *    before its kernel, so no zero-filling is needed by the caller; device
  *    status bits are not reported back by this call.
@@ -432,6 +436,25 @@ int relattn_debug_walk_prefill(const int32_t* cu_seqlens,
  * below 256 bytes or not 16-byte aligned.
  */
 int relattn_debug_wait_timeout(void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Test hook for failure detection in the decode kernel: relattn_decode with
+ * one change -- in every CTA the consumer warps treat the query wait of
+ * their piece number `piece` (0 = the first piece of the CTA's range) as if
+ * it had run past its limit.  They record RELATTN_DEV_WAIT_TIMEOUT and give
+ * up the rest of their range, as after a real timeout: every split segment
+ * that the rest of the range touches still receives the CTA's (empty)
+ * partial and its arrival, so the workspace's split counters end at zero and
+ * the next call on the same workspace is correct.  The CTA's producer warp
+ * then finds no free stage and gives up after its own limit (about 2 s).
+ * Output rows of the abandoned pieces are undefined.  RELATTN_ERR_INVALID_ARG
+ * for piece < 0; otherwise arguments, errors and status as relattn_decode.
+ */
+int relattn_debug_decode_give_up(const void* q, const float* rel,
+                                 const relattn_kv_cache* kv_cache, const int32_t* block_table,
+                                 const int32_t* seq_lens, int32_t window, int32_t rel_extent,
+                                 const relattn_dims* dims, void* out, void* workspace,
+                                 size_t workspace_bytes, int32_t piece, void* stream);
 
 /* ABI version of this header (major * 100 + minor). */
 int relattn_abi_version(void);

@@ -442,6 +442,21 @@ int relattn_decode_ex(const void* q, const void* rel, const relattn_options* opt
   return to_status(launch_decode(L, static_cast<cudaStream_t>(stream)));
 }
 
+int relattn_debug_decode_give_up(const void* q, const float* rel,
+                                 const relattn_kv_cache* kv_cache, const int32_t* block_table,
+                                 const int32_t* seq_lens, int32_t window, int32_t rel_extent,
+                                 const relattn_dims* dims, void* out, void* workspace,
+                                 size_t workspace_bytes, int32_t piece, void* stream) {
+  if (piece < 0) return RELATTN_ERR_INVALID_ARG;
+  DecodeLaunch L;
+  DeviceInfo di;
+  const int rc = prepare_decode(q, rel, kDefaultIo, kv_cache, block_table, seq_lens, 1, window,
+                                rel_extent, dims, out, workspace, workspace_bytes, false, &L, &di);
+  if (rc != RELATTN_OK) return rc;
+  L.p.dbg_give_up = piece + 1;
+  return to_status(launch_decode(L, static_cast<cudaStream_t>(stream)));
+}
+
 int relattn_debug_walk_decode(const int32_t* block_table, const int32_t* seq_lens,
                               int32_t window, const relattn_kv_cache* cache,
                               const relattn_dims* dims, int32_t* records, int32_t max_records,

@@ -799,7 +799,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   int k = 0;
   bool abort = false;
 
-  for (int f = a0; f < a1 && !abort; ++k) {
+  int f = a0;
+  for (; f < a1 && !abort; ++k) {
     const Piece pc = locate_piece(f, a1, s_pref, s_nt, p.Bv, p.Hkv);
     const VSeq sq = decode_vseq<MULTI>(pc.b, s_len[pc.b / tok.nck], p);
     const int h0 = pc.kvh * g;
@@ -835,6 +836,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     const float sl2 = p.scale_log2 * fr[0], bl2 = kLog2e * fr[0];  // one-token kernel
     const int qb = k & 1;
     bool qok = mbar_wait(&qfull[qb], (k >> 1) & 1);
+    if (p.dbg_give_up == k + 1) qok = false;  // test hook (after the wait: no copy in flight)
     if (!qok) report(p.status, RELATTN_DEV_WAIT_TIMEOUT);
     if constexpr (KV8 && MULTI) {
       // e4m3 cache, general kernel: the MMAs run in f16.  The eight warps
@@ -1376,6 +1378,26 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
             static_cast<__nv_bfloat16*>(p.out)[orow(row) + col] = __float2bfloat16(r);
         }
         if (ctid == 0) p.counters[pc.b * p.Hkv + pc.kvh] = 0;
+      }
+    }
+    f += pc.n;
+  }
+  // After a wait gave up (the loop left at the piece starting at f), every
+  // split segment that the rest of this CTA's range touches still gets this
+  // CTA's partial -- an empty one (lse = -inf, weight 0) -- and its arrival,
+  // so each segment's counter completes and returns to zero and the
+  // workspace stays ready for the next call.  A segment whose last arrival
+  // is this one is left unmerged (the status word reports the timeout).
+  for (; f < a1;) {
+    const Piece pc = locate_piece(f, a1, s_pref, s_nt, p.Bv, p.Hkv);
+    if (!(pc.i0 == 0 && pc.n == s_nt[pc.b])) {
+      const int slot = 2 * c + (a0 < pc.seg_start ? 1 : 0);
+      if (ctid < kMaxChunkRows) p.part_lse[slot * kMaxChunkRows + ctid] = kNegInf;
+      named_barrier(1, kConsumerThreads);
+      if (ctid == 0) {
+        const int c1 = cta_of(pc.seg_start, pl), c2 = cta_of(pc.seg_end - 1, pl);
+        int* cnt = &p.counters[pc.b * p.Hkv + pc.kvh];
+        if (atom_add_acq_rel(cnt, 1) == c2 - c1) *cnt = 0;
       }
     }
     f += pc.n;

@@ -40,6 +40,8 @@ struct DecodeParams {
   int32_t* dbg_records;        // walk replay only
   int32_t* dbg_count;
   int dbg_max;
+  int dbg_give_up;             // test hook: > 0 makes the consumer warps of every CTA
+                               // treat the query wait of piece dbg_give_up - 1 as given up
   int B, Hq, Hkv, g, dv, max_blocks, num_blocks, window, rel_extent;
   // query tokens per sequence (k; 1 for plain decode), packed kpc at a time
   // with the g heads into the rows of one tile: nck = ceil(k / kpc) chunks

@@ -42,6 +42,7 @@ EXPORTS = (
     "relattn_prefill_ex",
     "relattn_cache_write",
     "relattn_debug_wait_timeout",
+    "relattn_debug_decode_give_up",
 )
 
 DTYPE_F32 = 0
@@ -136,6 +137,10 @@ def lib() -> ctypes.CDLL:
     L.relattn_cache_write.restype = c_int
     L.relattn_debug_wait_timeout.argtypes = [c_void_p, c_size_t, c_void_p]
     L.relattn_debug_wait_timeout.restype = c_int
+    L.relattn_debug_decode_give_up.argtypes = [c_void_p, c_void_p, P, c_void_p, c_void_p,
+                                               c_int32, c_int32, S, c_void_p, c_void_p,
+                                               c_size_t, c_int32, c_void_p]
+    L.relattn_debug_decode_give_up.restype = c_int
     L.relattn_abi_version.argtypes = []
     L.relattn_abi_version.restype = c_int
     _LIB = L
