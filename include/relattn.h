@@ -412,9 +412,32 @@ int relattn_debug_walk_decode(const int32_t* block_table,
                               void* stream);
 
 /*
- * Test hook: replay the prefill kernel's block walk.  Each (query tile, key
- * tile) visit appends { sequence, first_row_of_query_tile, key_tile,
- * logical_block, physical_block, 0 } (6 int32) to `records`.
+ * Test hook: relattn_debug_walk_decode for num_query_tokens tokens per
+ * sequence and the cache type of options->kv (the other option fields are
+ * not used; options may be NULL), with 8-int32 records per visited tile:
+ *   { cta, sequence, first_token_of_chunk, kv_head, key_tile,
+ *     physical_block, first_key, keys }
+ * where the tile's keys first_key .. first_key + keys - 1 are the ones the
+ * kernel brings: the whole 64-key tile, or with one query token over a bf16
+ * cache, the 32-key half that holds the visible keys at an edge of the
+ * range.  A chunk is the group of query tokens that share one pass over
+ * their keys; its tokens start at first_token_of_chunk.
+ */
+int relattn_debug_walk_decode_ex(const int32_t* block_table, const int32_t* seq_lens,
+                                 int32_t num_query_tokens, int32_t window,
+                                 const relattn_options* options, const relattn_kv_cache* cache,
+                                 const relattn_dims* dims, int32_t* records,
+                                 int32_t max_records, int32_t* count, void* workspace,
+                                 size_t workspace_bytes, void* stream);
+
+/*
+ * Test hook: replay the prefill kernel's work split and block walk (the
+ * kernel of bf16 caches, whose work items are a 128-row query tile and a pair
+ * of query heads of one KV group), with the same device code and grid as
+ * relattn_prefill.  Each (work item, key tile) visit appends
+ * { sequence, first_row_of_query_tile (within the sequence), key_tile,
+ *   logical_block, physical_block, first_head_of_item } (6 int32) to
+ * `records`.
  */
 int relattn_debug_walk_prefill(const int32_t* cu_seqlens,
                                const int32_t* ctx_lens,

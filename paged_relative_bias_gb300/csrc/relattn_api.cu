@@ -475,6 +475,28 @@ int relattn_debug_walk_decode(const int32_t* block_table, const int32_t* seq_len
   return to_status(launch_decode_walk(L.p, L.grid, static_cast<cudaStream_t>(stream)));
 }
 
+int relattn_debug_walk_decode_ex(const int32_t* block_table, const int32_t* seq_lens,
+                                 int32_t num_query_tokens, int32_t window,
+                                 const relattn_options* options, const relattn_kv_cache* cache,
+                                 const relattn_dims* dims, int32_t* records,
+                                 int32_t max_records, int32_t* count, void* workspace,
+                                 size_t workspace_bytes, void* stream) {
+  if (!records || !count || max_records < 0) return RELATTN_ERR_INVALID_ARG;
+  IoTypes io = kDefaultIo;
+  if (options && !io_types(options, &io)) return RELATTN_ERR_INVALID_ARG;
+  DecodeLaunch L;
+  DeviceInfo di;
+  const int rc = prepare_decode(nullptr, nullptr, io, cache, block_table, seq_lens,
+                                num_query_tokens, window, 4, dims, nullptr, workspace,
+                                workspace_bytes, true, &L, &di);
+  if (rc != RELATTN_OK) return rc;
+  L.p.dbg_records = records;
+  L.p.dbg_count = count;
+  L.p.dbg_max = max_records;
+  L.p.dbg_wide = 1;
+  return to_status(launch_decode_walk(L.p, L.grid, static_cast<cudaStream_t>(stream)));
+}
+
 // ---- decode with library-owned scratch ----------------------------------
 // For callers that may not allocate device memory (their host owns every
 // buffer, or cannot pay for an allocation on the decode path): the split
@@ -579,14 +601,19 @@ static int prepare_prefill(const void* q, const void* k, const void* v, const vo
   p.kv_es = io.kv_es;
   p.k_scale = io.k_scale;
   p.v_scale = io.v_scale;
-  if (walk) return RELATTN_OK;
   DeviceInfo di;
   if (!device_info(&di)) return RELATTN_ERR_CUDA;
-  p.ring_stages = prefill_ring_stages(p.B, p.dv, p.kv_es, di.smem_optin);
+  // bf16 caches: two heads of a KV group per work item when its ring fits;
+  // otherwise (e4m3 caches, or very many sequences) one head per item
+  const int pair_slots = io.kv_es == 2 ? prefill_pair_slots(p.B, p.dv, p.rel_es, di.smem_optin) : 0;
+  L->pair = pair_slots > 0 ? 1 : 0;
+  p.ring_stages = L->pair ? pair_slots : prefill_ring_stages(p.B, p.dv, p.kv_es, di.smem_optin);
   if (p.ring_stages == 0) return RELATTN_ERR_UNSUPPORTED;
-  const long long qtiles = static_cast<long long>(p.B) * ((p.max_q_len + 127) / 128) * p.Hq;
+  const long long heads = L->pair ? static_cast<long long>(p.Hkv) * ((p.g + 1) / 2) : p.Hq;
+  const long long items = static_cast<long long>(p.B) * ((p.max_q_len + 127) / 128) * heads;
   const long long want = dims->num_ctas > 0 ? dims->num_ctas : di.sms;
-  L->grid = static_cast<int>(qtiles < want ? (qtiles > 0 ? qtiles : 1) : want);
+  L->grid = static_cast<int>(items < want ? (items > 0 ? items : 1) : want);
+  if (walk) return RELATTN_OK;
   // e4m3 caches: 2-D boxes of 64 head-major rows, landing in staging slots
   if (!(io.kv_es == 1 ? decode_cache_maps_e4m3(cache, kTileKeys, &L->tm_k, &L->tm_v)
                       : cache_maps(cache, &L->tm_k, &L->tm_v)))
@@ -628,7 +655,7 @@ static int relattn_prefill_io(const void* q, const void* k, const void* v, const
   if (dims->max_q_len == 0 || dims->num_tokens == 0) return RELATTN_OK;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = launch_cache_write(L.p, s);
-  if (e == cudaSuccess) e = launch_prefill(L, L.grid, s);
+  if (e == cudaSuccess) e = L.pair ? launch_prefill_pair(L, L.grid, s) : launch_prefill(L, L.grid, s);
   return to_status(e);
 }
 
@@ -726,7 +753,7 @@ int relattn_debug_walk_prefill(const int32_t* cu_seqlens, const int32_t* ctx_len
   L.p.dbg_records = records;
   L.p.dbg_count = count;
   L.p.dbg_max = max_records;
-  return to_status(launch_prefill_walk(L.p, static_cast<cudaStream_t>(stream)));
+  return to_status(launch_prefill_walk(L.p, L.grid, static_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

@@ -171,6 +171,23 @@ __device__ __forceinline__ VSeq decode_vseq(int vb, int len, const DecodeParams&
   return v;
 }
 
+// The keys of 64-key tile `tile` that the producer brings for chunk sq:
+// [first, first + n).  With HALVES (the one-token kernel over a bf16 cache)
+// a tile at an edge of the key range [lo, pl] whose first or last 32 keys all
+// lie outside it brings only the other 32; otherwise the whole tile.
+struct TileKeys {
+  int first, n;
+};
+
+template <bool HALVES>
+__device__ __forceinline__ TileKeys tile_keys(int tile, const VSeq& sq) {
+  constexpr int kHalf = kTileKeys / 2;
+  const int key0 = tile * kTileKeys;
+  const int h0 = HALVES && key0 + kHalf - 1 < sq.lo ? kHalf : 0;  // first 32 not needed
+  const bool half = h0 > 0 || (HALVES && key0 + kHalf > sq.pl);  // or the last 32
+  return TileKeys{key0 + h0, half ? kHalf : kTileKeys};
+}
+
 // How the CTA ranges are cut.  All tile indices fit in 32 bits (the host
 // checks batch * kv heads * tiles per sequence < 2^31), so the cut arithmetic
 // is 32-bit: no 64-bit division on the kernel's start-up path.
@@ -655,10 +672,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       // distance here is past rel_extent need none
       const int dmin0 = sq.pf - key0 - (kTileKeys - 1);
       const int nrel = max(0, min(sq.kc, p.rel_extent - dmin0));
-      constexpr int kHalf = kTileKeys / 2;
       constexpr bool kHalves = !MULTI && !KV8;
-      const int h0 = kHalves && key0 + kHalf - 1 < sq.lo ? kHalf : 0;  // first 32 not needed
-      const bool half = h0 > 0 || (kHalves && key0 + kHalf > sq.pl);  // or the last 32
+      const TileKeys tk = tile_keys<kHalves>(tile, sq);
+      const int h0 = tk.first - key0;
+      const bool half = tk.n < kTileKeys;
       mbar_arrive_expect_tx(&full[stage], (half ? stage_tx / 2 : stage_tx) + nrel * rel_tx);
       uint8_t* st = smem + L.stages + stage * L.stage_bytes;
       const int row = id * kBlockSize + (tile & 1) * kTileKeys;
@@ -1404,21 +1421,28 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   }
 }
 
-// Replays the producer's walk and split without touching K/V.
+// Replays the producer's walk and split without touching K/V, with the same
+// device functions and grid as decode_kernel (MULTI: the general kernel's
+// chunks of query tokens; HALVES: the one-token bf16 kernel's half tiles).
+// Each tile appends { cta, sequence, kv_head, key_tile, logical_block,
+// physical_block }, or with p.dbg_wide { cta, sequence, first_token_of_chunk,
+// kv_head, key_tile, physical_block, first_key, keys }.
+template <bool MULTI, bool HALVES>
 __global__ void __launch_bounds__(128) decode_walk_kernel(const DecodeParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_align1024(smem_raw);
+  const Tok<MULTI> tok(p);
   const DecodeSmem L(0, p.B, p.Bv, 1, 1, 64, 4, 2);
   const int* s_len = reinterpret_cast<const int*>(smem + L.seqlen);
   const int* s_nt = reinterpret_cast<const int*>(smem + L.nt);
   const int* s_pref = reinterpret_cast<const int*>(smem + L.pref);
-  const int len0 = decode_early_loads<false>(p);
+  const int len0 = decode_early_loads<MULTI>(p);
   CtaRange cr;
   if (p.Bv <= 32) {  // the decode kernel's fast prologue, run the same way
     if (threadIdx.x >= 32) return;
-    cr = decode_plan_warp<false>(p, smem, L, len0, [](int, int, int, int) {});
+    cr = decode_plan_warp<MULTI>(p, smem, L, len0, [](int, int, int, int) {});
   } else {
-    cr.pl = decode_prologue<false>(p, smem, L, false, len0);
+    cr.pl = decode_prologue<MULTI>(p, smem, L, false, len0);
     cr.a0 = range_cut(blockIdx.x, cr.pl, s_pref, s_nt, p.Bv, p.Hkv);
     cr.a1 = range_cut(blockIdx.x + 1, cr.pl, s_pref, s_nt, p.Bv, p.Hkv);
   }
@@ -1428,20 +1452,33 @@ __global__ void __launch_bounds__(128) decode_walk_kernel(const DecodeParams p) 
   const int a0 = cr.a0, a1 = cr.a1;
   for (int f = a0; f < a1;) {
     const Piece pc = locate_piece(f, a1, s_pref, s_nt, p.Bv, p.Hkv);
-    const VSeq sq = decode_vseq<false>(pc.b, s_len[pc.b], p);
+    const VSeq sq = decode_vseq<MULTI>(pc.b, s_len[pc.b / tok.nck], p);
     const int* trow = p.block_table + static_cast<size_t>(sq.b) * p.max_blocks;
     for (int t = 0; t < pc.n; ++t) {
       const int tile = sq.tile_first + pc.i0 + t;
       const int id = trow[tile >> 1];
+      const TileKeys tk = tile_keys<HALVES>(tile, sq);
       const int r = atomicAdd(p.dbg_count, 1);
       if (r < p.dbg_max) {
-        int32_t* rec = p.dbg_records + 6 * static_cast<size_t>(r);
-        rec[0] = c;
-        rec[1] = pc.b;
-        rec[2] = pc.kvh;
-        rec[3] = tile;
-        rec[4] = tile >> 1;
-        rec[5] = id;
+        if (p.dbg_wide) {
+          int32_t* rec = p.dbg_records + 8 * static_cast<size_t>(r);
+          rec[0] = c;
+          rec[1] = sq.b;
+          rec[2] = sq.i0;
+          rec[3] = pc.kvh;
+          rec[4] = tile;
+          rec[5] = id;
+          rec[6] = tk.first;
+          rec[7] = tk.n;
+        } else {
+          int32_t* rec = p.dbg_records + 6 * static_cast<size_t>(r);
+          rec[0] = c;
+          rec[1] = sq.b;
+          rec[2] = pc.kvh;
+          rec[3] = tile;
+          rec[4] = tile >> 1;
+          rec[5] = id;
+        }
       }
     }
     f += pc.n;
@@ -1524,10 +1561,13 @@ cudaError_t launch_decode(const DecodeLaunch& L, cudaStream_t stream) {
 
 cudaError_t launch_decode_walk(const DecodeParams& p, int grid, cudaStream_t stream) {
   const int smem = decode_smem_bytes(0, p.B, p.Bv, 1, 1, 64, 4, 2);
-  cudaError_t e = cudaFuncSetAttribute(decode_walk_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  const bool multi = decode_multi_kernel(p.k, p.g);
+  const bool halves = !multi && p.kv_es == 2;
+  auto kern = multi ? decode_walk_kernel<true, false>
+                    : halves ? decode_walk_kernel<false, true> : decode_walk_kernel<false, false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  decode_walk_kernel<<<grid, 128, smem, stream>>>(p);
+  kern<<<grid, 128, smem, stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -40,6 +40,7 @@ struct DecodeParams {
   int32_t* dbg_records;        // walk replay only
   int32_t* dbg_count;
   int dbg_max;
+  int dbg_wide;                // walk replay: 8-field records (chunk and keys brought)
   int dbg_give_up;             // test hook: > 0 makes the consumer warps of every CTA
                                // treat the query wait of piece dbg_give_up - 1 as given up
   int B, Hq, Hkv, g, dv, max_blocks, num_blocks, window, rel_extent;
@@ -112,6 +113,7 @@ struct PrefillLaunch {
   CUtensorMap tm_q, tm_k, tm_v, tm_rel;
   PrefillParams p;
   int grid;
+  int pair;  // 1: the two-heads-per-item kernel (bf16 caches), 0: one head per item
 };
 
 int decode_smem_bytes(int nstages, int B, int Bv, int kpc, int g, int dv, int rel_es, int kv_es);
@@ -134,6 +136,13 @@ constexpr int kCacheWriteMaxGridY = 65535;  // sequences of one cache-write laun
 int prefill_smem_bytes(int B, int dv, int ring_stages, int kv_es);
 int prefill_ring_stages(int B, int dv, int kv_es, int smem_optin);  // 0 if nothing fits
 cudaError_t launch_prefill(const PrefillLaunch& L, int grid, cudaStream_t stream);
-cudaError_t launch_prefill_walk(const PrefillParams& p, cudaStream_t stream);
+// Replay of the bf16-cache prefill's work split and block walk on its grid.
+cudaError_t launch_prefill_walk(const PrefillParams& p, int grid, cudaStream_t stream);
+// The bf16-cache prefill with two query heads of one KV group per work item:
+// its ring slots for these sizes (0 if fewer than it needs fit), its shared
+// memory, and its launch (p.ring_stages = the slots).
+int prefill_pair_slots(int B, int dv, int rel_es, int smem_optin);
+int prefill_pair_smem_bytes(int B, int dv, int rel_es, int nslots);
+cudaError_t launch_prefill_pair(const PrefillLaunch& L, int grid, cudaStream_t stream);
 
 }  // namespace relattn

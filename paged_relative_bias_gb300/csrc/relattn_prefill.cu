@@ -29,39 +29,24 @@
 // softmax (TMEM lane quarters 2, 3, 0, 1), 6 = rel TMA producer.
 #include "relattn_common.cuh"
 #include "relattn_internal.h"
+#include "relattn_prefill.cuh"
 #include "relattn_tcgen05.cuh"
 
 namespace relattn {
 
 namespace {
 
-constexpr int kQRows = 128;
+using namespace prefill;
+
 constexpr int kCwTile = 64;                 // cache_write tokens per CTA
 constexpr int kPfWarps = 7;  // (an e4m3 cache adds an eighth: the V widener)
 constexpr int kKStages = 2, kVStages = 2, kMaxRingStages = 3;
-constexpr int kKStageBytes = kTileKeys * kDqk * 2;  // 16 KB
-constexpr int kQTileBytes = kQRows * kDqk * 2;      // 32 KB
-// rel boxes: 32 query rows x 100 distances, one per softmax warp.  Row r of a
-// box needs the 64 distances P_r - j0 - 63 .. P_r - j0; across 32 rows that is
-// 95, plus up to 3 for rounding the box start down to 16 bytes.  Lane l reads
-// word 101 l + const - c: 101 is odd, so the 32 lanes hit 32 banks.
-constexpr int kRelBoxRows = 32, kRelBoxCols = 100;
-constexpr int kRelBoxBytes = kRelBoxRows * kRelBoxCols * 4;  // 12800
-constexpr int kRelBoxes = kQRows / kRelBoxRows;              // 4 per tile
-// bf16 rel boxes: the box start rounds down to 8 distances (16 bytes), so
-// 95 + 7 columns are needed: 104 (208-byte rows).  Rows are read as 8-byte
-// pieces (4 distances), whose alignment is the same across a warp.
-constexpr int kRelBoxCols16 = 104;
-constexpr int kRelBoxBytes16 = kRelBoxRows * kRelBoxCols16 * 2;  // 6656 (52 x 128)
 // One ring of shared-memory slots carries, per work item, the query tile,
 // then the rel boxes of each key tile, then a scratch slot for storing O.
 constexpr int kRingSlotBytes = kRelBoxes * kRelBoxBytes;     // 51200 (50 KB)
 static_assert(kRingSlotBytes % 1024 == 0 && kRingSlotBytes >= kQTileBytes, "ring slot");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmQ = 0, kTmS = 64, kTmO = 192;  // S buffer s at kTmS + 64 s
-constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kNegInf = -__builtin_huge_valf();
-constexpr float kRescaleNat = 5.5451774f;  // move the running max only past e^(8 ln 2)
 constexpr uint32_t kIdescS = umma_idesc_bf16(128, kTileKeys, 0);
 
 // kRFull / kREmpty: ring slots (producer <-> softmax); kQFull: query tile in
@@ -72,16 +57,6 @@ enum Bar { kKFull = 0, kKEmpty = 2, kVFull = 4, kVEmpty = 6, kRFull = 8, kREmpty
            kSFull = 14, kPFull = 16, kOFull = 18, kQFull = 19, kDrain = 20, kStgK = 21,
            kStgV = 23, kNumBars = 25 };
 constexpr int kStgBytes = kTileKeys * (kDqk + 128);  // one e4m3 tile: K then V, 16 KB
-
-__device__ __forceinline__ bool seq_ok(int ctx, int n, int max_blocks) {
-  return ctx >= 0 && n >= 0 &&
-         static_cast<long long>(ctx) + n <= static_cast<long long>(max_blocks) * kBlockSize;
-}
-
-// Rows [cu0, cu1) are a valid chunk of the packed [T] token rows.
-__device__ __forceinline__ bool rows_ok(int cu0, int cu1, int T) {
-  return cu0 >= 0 && cu1 >= cu0 && cu1 <= T;
-}
 
 // Four floats -> four e4m3 codes (low byte first): x / scale rounded to
 // nearest even, saturated to +-448 (cvt's satfinite).
@@ -185,112 +160,25 @@ struct PItem {
   int b, h, kvh, r0, rows, P0, tf, ntiles;
 };
 
-__device__ __forceinline__ void prefill_item(int idx, const PrefillParams& p, const int* s_cu0,
-                                             const int* s_n, const int* s_ctx,
-                                             const int* s_qpref, PItem& it) {
+// Work item idx: query tile idx / Hq, head idx % Hq (the heads of one query
+// tile run on neighbouring CTAs, so its K/V tiles are shared in L2).
+__device__ __forceinline__ void prefill_item(int idx, const PrefillParams& p, const SeqArrays& a,
+                                             PItem& it) {
   const int qtg = idx / p.Hq;
   it.h = idx - qtg * p.Hq;
   it.kvh = it.h / p.g;
-  int lo = 0, hi = p.B - 1;
-  while (lo < hi) {  // largest b with s_qpref[b] <= qtg
-    const int mid = (lo + hi + 1) >> 1;
-    if (s_qpref[mid] <= qtg)
-      lo = mid;
-    else
-      hi = mid - 1;
-  }
-  it.b = lo;
-  const int qt = qtg - s_qpref[lo];
-  it.r0 = s_cu0[lo] + qt * kQRows;
-  it.rows = min(kQRows, s_n[lo] - qt * kQRows);
-  it.P0 = s_ctx[lo] + qt * kQRows;
-  it.tf = window_lo(it.P0, p.window) / kTileKeys;
-  it.ntiles = (it.P0 + it.rows - 1) / kTileKeys - it.tf + 1;
+  const QTile t = query_tile(qtg, p, a);
+  it.b = t.b;
+  it.r0 = t.r0;
+  it.rows = t.rows;
+  it.P0 = t.P0;
+  it.tf = t.tf;
+  it.ntiles = t.ntiles;
 }
 
-// Per-CTA prologue: per-sequence rows, context and query-tile prefix.
-// Returns the number of (query tile, head) work items.
-__device__ int prefill_prologue(const PrefillParams& p, uint8_t* smem, const PrefillSmem& L,
-                                bool zero_bad) {
-  int* s_cu0 = reinterpret_cast<int*>(smem + L.cu0);
-  int* s_n = reinterpret_cast<int*>(smem + L.nrows);
-  int* s_ctx = reinterpret_cast<int*>(smem + L.ctx);
-  int* s_qpref = reinterpret_cast<int*>(smem + L.qpref);
-  const int tid = threadIdx.x;
-  for (int b = tid; b < p.B; b += blockDim.x) {
-    const int c0 = p.cu_seqlens[b], c1 = p.cu_seqlens[b + 1], ctx = p.ctx_lens[b];
-    const bool ok = rows_ok(c0, c1, p.T) && seq_ok(ctx, c1 - c0, p.max_blocks);
-    s_cu0[b] = c0;
-    s_n[b] = ok ? c1 - c0 : 0;
-    s_ctx[b] = ctx;
-    // query tiles of this sequence, kept in s_qpref until the scan
-    s_qpref[b] = ok ? (c1 - c0 + kQRows - 1) / kQRows : 0;
-    if (!ok && zero_bad && blockIdx.x == 0 && rows_ok(c0, c1, p.T)) {
-      const int per = p.Hq * p.dv * (p.out_f32 ? 4 : 2) / 4;  // 32-bit words per row
-      uint32_t* o = static_cast<uint32_t*>(p.out);
-      for (int r = c0; r < c1; ++r)  // a skipped sequence's rows are zero
-        for (int i = 0; i < per; ++i) o[static_cast<size_t>(r) * per + i] = 0u;
-    }
-  }
-  __syncthreads();
-  if (tid < 32) {
-    const int lane = tid;
-    const int chunk = (p.B + 31) / 32;
-    const int beg = lane * chunk, end = min(p.B, beg + chunk);
-    int sum = 0;
-    for (int i = beg; i < end; ++i) sum += s_qpref[i];
-    int incl = sum;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int v = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += v;
-    }
-    int run = incl - sum;
-    for (int i = beg; i < end; ++i) {
-      const int cnt = s_qpref[i];
-      s_qpref[i] = run;
-      run += cnt;
-    }
-    if (lane == 31) s_qpref[p.B] = incl;
-  }
-  __syncthreads();
-  return s_qpref[p.B] * p.Hq;
-}
-
-// x[c] = s[c] * scale + rel for the 64 columns of one query row, from 17
-// aligned 16-byte loads.  p4 points A floats before the row's lowest needed
-// distance (the one of column 63); distances rise towards column 0.
-template <int A>
-__device__ __forceinline__ void rel_fma(float (&x)[64], const uint32_t (&sr)[64],
-                                        const float4* p4, float scale) {
-#pragma unroll
-  for (int w = 0; w < 17; ++w) {
-    const float4 v = p4[w];
-    const float f[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int t = 4 * w + e - A;  // distance above the lowest
-      if (t >= 0 && t < 64) x[63 - t] = fmaf(__uint_as_float(sr[63 - t]), scale, f[e]);
-    }
-  }
-}
-
-// The same from bf16 rel: 17 aligned 8-byte loads of four distances, each
-// widened exactly (a bf16 is the top half of a binary32).
-template <int A>
-__device__ __forceinline__ void rel_fma16(float (&x)[64], const uint32_t (&sr)[64],
-                                          const uint2* p2, float scale) {
-#pragma unroll
-  for (int w = 0; w < 17; ++w) {
-    const uint2 v = p2[w];
-    const float f[4] = {__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xffff0000u),
-                        __uint_as_float(v.y << 16), __uint_as_float(v.y & 0xffff0000u)};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int t = 4 * w + e - A;  // distance above the lowest
-      if (t >= 0 && t < 64) x[63 - t] = fmaf(__uint_as_float(sr[63 - t]), scale, f[e]);
-    }
-  }
+__device__ __forceinline__ SeqArrays seq_arrays(uint8_t* smem, const PrefillSmem& L) {
+  return SeqArrays{reinterpret_cast<int*>(smem + L.cu0), reinterpret_cast<int*>(smem + L.nrows),
+                   reinterpret_cast<int*>(smem + L.ctx), reinterpret_cast<int*>(smem + L.qpref)};
 }
 
 // One e4m3 tile (64 rows x 128 bytes, 128-byte swizzle) -> its values as
@@ -339,10 +227,7 @@ __global__ void __launch_bounds__(32 * (kPfWarps + (KV8 ? 1 : 0)), 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + L.misc);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + L.misc + 4);
-  const int* s_cu0 = reinterpret_cast<const int*>(smem + L.cu0);
-  const int* s_n = reinterpret_cast<const int*>(smem + L.nrows);
-  const int* s_ctx = reinterpret_cast<const int*>(smem + L.ctx);
-  const int* s_qpref = reinterpret_cast<const int*>(smem + L.qpref);
+  const SeqArrays sa = seq_arrays(smem, L);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   if (tid == 0) {
@@ -381,7 +266,7 @@ __global__ void __launch_bounds__(32 * (kPfWarps + (KV8 ? 1 : 0)), 1)
     tmem_alloc(s_tmem, kTmemCols);
     tc_fence_before();
   }
-  const int total = prefill_prologue(p, smem, L, true);  // contains __syncthreads
+  const int total = prologue(p, sa, true) * p.Hq;  // contains __syncthreads
   tc_fence_after();
   const uint32_t tbase = *s_tmem;
   const float scale_log2 = p.scale_log2;
@@ -420,7 +305,7 @@ __global__ void __launch_bounds__(32 * (kPfWarps + (KV8 ? 1 : 0)), 1)
       bool fail = false;
       for (int idx = blockIdx.x; idx < total && !*s_abort && !fail; idx += gridDim.x) {
         PItem it;
-        prefill_item(idx, p, s_cu0, s_n, s_ctx, s_qpref, it);
+        prefill_item(idx, p, sa, it);
         const int* trow = p.block_table + static_cast<size_t>(it.b) * p.max_blocks;
         for (int k = 0; k < it.ntiles; ++k, ++n) {
           const int tile = it.tf + k;
@@ -447,7 +332,7 @@ __global__ void __launch_bounds__(32 * (kPfWarps + (KV8 ? 1 : 0)), 1)
     int n = 0;
     for (int idx = blockIdx.x; idx < total && !*s_abort; idx += gridDim.x) {
       PItem it;
-      prefill_item(idx, p, s_cu0, s_n, s_ctx, s_qpref, it);
+      prefill_item(idx, p, sa, it);
       const int* trow = p.block_table + static_cast<size_t>(it.b) * p.max_blocks;
       for (int k = 0; k < it.ntiles; ++k, ++n) {
         const int tile = it.tf + k;
@@ -490,7 +375,7 @@ __global__ void __launch_bounds__(32 * (kPfWarps + (KV8 ? 1 : 0)), 1)
     };
     for (int idx = blockIdx.x; idx < total && !*s_abort && !fail; idx += gridDim.x) {
       PItem it;
-      prefill_item(idx, p, s_cu0, s_n, s_ctx, s_qpref, it);
+      prefill_item(idx, p, sa, it);
       uint8_t* qd = acquire(e);
       if (!qd) { fail = true; break; }
       uint64_t* qbar = &bars[kRFull + e % nrs];
@@ -542,7 +427,7 @@ __global__ void __launch_bounds__(32 * (kPfWarps + (KV8 ? 1 : 0)), 1)
     };
     for (int idx = blockIdx.x; idx < total && !*s_abort; idx += gridDim.x, ++items) {
       PItem it;
-      prefill_item(idx, p, s_cu0, s_n, s_ctx, s_qpref, it);
+      prefill_item(idx, p, sa, it);
       if (!mbar_wait(&bars[kQFull], items & 1)) { *s_abort = 1; break; }
       tc_fence_after();
       bool ok = true;
@@ -616,7 +501,7 @@ __global__ void __launch_bounds__(32 * (kPfWarps + (KV8 ? 1 : 0)), 1)
     };
     for (int idx = blockIdx.x; idx < total && !*s_abort; idx += gridDim.x, ++items) {
       PItem it;
-      prefill_item(idx, p, s_cu0, s_n, s_ctx, s_qpref, it);
+      prefill_item(idx, p, sa, it);
       // A wait that gives up marks the item bad: the warp skips the rest of
       // its work but still meets the other softmax warps at the barrier
       // before the epilogue, after which all four leave together (a warp
@@ -866,35 +751,6 @@ __global__ void __launch_bounds__(32 * (kPfWarps + (KV8 ? 1 : 0)), 1)
   if (warp == 1) tmem_dealloc(tbase, kTmemCols);
 }
 
-// Replays the prefill kernel's block walk (128-row query tiles, 64-key tiles).
-__global__ void prefill_walk_kernel(const PrefillParams p) {
-  if (threadIdx.x != 0) return;
-  const int qt = blockIdx.x, b = blockIdx.y;
-  const int c0 = p.cu_seqlens[b], c1 = p.cu_seqlens[b + 1];
-  const int n = c1 - c0;
-  const int ctx = p.ctx_lens[b];
-  const int t0 = qt * kQRows;
-  if (!rows_ok(c0, c1, p.T) || !seq_ok(ctx, n, p.max_blocks) || t0 >= n) return;
-  const int rows = min(kQRows, n - t0);
-  const int P0 = ctx + t0, P1 = P0 + rows - 1;
-  const int tf = window_lo(P0, p.window) / kTileKeys;
-  const int ntiles = P1 / kTileKeys - tf + 1;
-  const int* trow = p.block_table + static_cast<size_t>(b) * p.max_blocks;
-  for (int k = 0; k < ntiles; ++k) {
-    const int tile = tf + k;
-    const int r = atomicAdd(p.dbg_count, 1);
-    if (r < p.dbg_max) {
-      int32_t* rec = p.dbg_records + 6 * static_cast<size_t>(r);
-      rec[0] = b;
-      rec[1] = t0;
-      rec[2] = tile;
-      rec[3] = tile >> 1;
-      rec[4] = trow[tile >> 1];
-      rec[5] = 0;
-    }
-  }
-}
-
 }  // namespace
 
 int prefill_smem_bytes(int B, int dv, int ring_stages, int kv_es) {
@@ -964,10 +820,5 @@ cudaError_t launch_prefill(const PrefillLaunch& L, int grid, cudaStream_t stream
              : launch_prefill_out<64, false, false>(L, grid, smem, stream);
 }
 
-cudaError_t launch_prefill_walk(const PrefillParams& p, cudaStream_t stream) {
-  const dim3 grid((p.max_q_len + kQRows - 1) / kQRows, p.B);
-  prefill_walk_kernel<<<grid, 32, 0, stream>>>(p);
-  return cudaGetLastError();
-}
 
 }  // namespace relattn

@@ -1,0 +1,221 @@
+// Device pieces shared by the chunked-prefill kernels: the per-sequence
+// prologue, the query-tile lookup, the validity checks and the sheared-bias
+// loads from a rel box.
+#pragma once
+
+#include "relattn_common.cuh"
+#include "relattn_internal.h"
+
+namespace relattn {
+namespace prefill {
+
+constexpr int kQRows = 128;  // query rows of one tile (the M of every MMA)
+// rel boxes: 32 query rows x 100 distances, one per softmax warp.  Row r of a
+// box needs the 64 distances P_r - j0 - 63 .. P_r - j0; across 32 rows that is
+// 95, plus up to 3 for rounding the box start down to 16 bytes.  Lane l reads
+// word 101 l + const - c: 101 is odd, so the 32 lanes hit 32 banks.
+constexpr int kRelBoxRows = 32, kRelBoxCols = 100;
+constexpr int kRelBoxBytes = kRelBoxRows * kRelBoxCols * 4;  // 12800
+constexpr int kRelBoxes = kQRows / kRelBoxRows;              // 4 per tile
+// bf16 rel boxes: the box start rounds down to 8 distances (16 bytes), so
+// 95 + 7 columns are needed: 104 (208-byte rows).  Rows are read as 8-byte
+// pieces (4 distances), whose alignment is the same across a warp.
+constexpr int kRelBoxCols16 = 104;
+constexpr int kRelBoxBytes16 = kRelBoxRows * kRelBoxCols16 * 2;  // 6656 (52 x 128)
+constexpr int kQTileBytes = kQRows * kDqk * 2;                   // 32 KB
+constexpr int kKStageBytes = kTileKeys * kDqk * 2;               // 16 KB
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kNegInf = -__builtin_huge_valf();
+constexpr float kRescaleNat = 5.5451774f;  // move the running max only past e^(8 ln 2)
+
+__device__ __forceinline__ bool seq_ok(int ctx, int n, int max_blocks) {
+  return ctx >= 0 && n >= 0 &&
+         static_cast<long long>(ctx) + n <= static_cast<long long>(max_blocks) * kBlockSize;
+}
+
+// Rows [cu0, cu1) are a valid chunk of the packed [T] token rows.
+__device__ __forceinline__ bool rows_ok(int cu0, int cu1, int T) {
+  return cu0 >= 0 && cu1 >= cu0 && cu1 <= T;
+}
+
+// Per-sequence arrays a CTA keeps in shared memory: first packed row, row
+// count (0 for an invalid sequence), cached prefix, and the prefix sum of
+// query tiles (B + 1 entries).
+struct SeqArrays {
+  int* cu0;
+  int* n;
+  int* ctx;
+  int* qpref;
+};
+
+// Per-CTA prologue: fills the arrays and returns the number of 128-row query
+// tiles over all sequences.  zero_bad: CTA 0 writes zeros to the output rows
+// of a sequence whose lengths are invalid (its rows are skipped).
+__device__ inline int prologue(const PrefillParams& p, SeqArrays a, bool zero_bad) {
+  const int tid = threadIdx.x;
+  for (int b = tid; b < p.B; b += blockDim.x) {
+    const int c0 = p.cu_seqlens[b], c1 = p.cu_seqlens[b + 1], ctx = p.ctx_lens[b];
+    const bool ok = rows_ok(c0, c1, p.T) && seq_ok(ctx, c1 - c0, p.max_blocks);
+    a.cu0[b] = c0;
+    a.n[b] = ok ? c1 - c0 : 0;
+    a.ctx[b] = ctx;
+    // query tiles of this sequence, kept in qpref until the scan
+    a.qpref[b] = ok ? (c1 - c0 + kQRows - 1) / kQRows : 0;
+    if (!ok && zero_bad && blockIdx.x == 0 && rows_ok(c0, c1, p.T)) {
+      const int per = p.Hq * p.dv * (p.out_f32 ? 4 : 2) / 4;  // 32-bit words per row
+      uint32_t* o = static_cast<uint32_t*>(p.out);
+      for (int r = c0; r < c1; ++r)  // a skipped sequence's rows are zero
+        for (int i = 0; i < per; ++i) o[static_cast<size_t>(r) * per + i] = 0u;
+    }
+  }
+  __syncthreads();
+  if (tid < 32) {
+    const int lane = tid;
+    const int chunk = (p.B + 31) / 32;
+    const int beg = lane * chunk, end = min(p.B, beg + chunk);
+    int sum = 0;
+    for (int i = beg; i < end; ++i) sum += a.qpref[i];
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    int run = incl - sum;
+    for (int i = beg; i < end; ++i) {
+      const int cnt = a.qpref[i];
+      a.qpref[i] = run;
+      run += cnt;
+    }
+    if (lane == 31) a.qpref[p.B] = incl;
+  }
+  __syncthreads();
+  return a.qpref[p.B];
+}
+
+// Query tile qtg (0 .. tiles - 1): its sequence, first packed row, valid rows,
+// position of its first row, and its window-aware range of 64-key tiles
+// [tf, tf + ntiles): the tiles holding a key that one of its rows sees.
+struct QTile {
+  int b, r0, rows, P0, tf, ntiles;
+};
+
+__device__ __forceinline__ QTile query_tile(int qtg, const PrefillParams& p,
+                                            const SeqArrays& a) {
+  int lo = 0, hi = p.B - 1;
+  while (lo < hi) {  // largest b with qpref[b] <= qtg
+    const int mid = (lo + hi + 1) >> 1;
+    if (a.qpref[mid] <= qtg)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  QTile t;
+  t.b = lo;
+  const int qt = qtg - a.qpref[lo];
+  t.r0 = a.cu0[lo] + qt * kQRows;
+  t.rows = min(kQRows, a.n[lo] - qt * kQRows);
+  t.P0 = a.ctx[lo] + qt * kQRows;
+  t.tf = window_lo(t.P0, p.window) / kTileKeys;
+  t.ntiles = (t.P0 + t.rows - 1) / kTileKeys - t.tf + 1;
+  return t;
+}
+
+// Key tile `tile` (64 keys) of a sequence whose block-table row is trow: the
+// physical block holding it, whether that id is inside the pool, and the
+// tile's first row in the cache's [blocks * 128] token rows.
+struct KvTile {
+  int id, row;
+  bool ok;
+};
+
+__device__ __forceinline__ KvTile kv_tile(const int* trow, int tile, int num_blocks) {
+  KvTile t;
+  t.id = __ldg(trow + (tile >> 1));
+  t.ok = t.id >= 0 && t.id < num_blocks;
+  t.row = t.id * kBlockSize + (tile & 1) * kTileKeys;
+  return t;
+}
+
+// x[c] = s[c] * scale + rel for the 64 columns of one query row, from 17
+// aligned 16-byte loads.  p4 points A floats before the row's lowest needed
+// distance (the one of column 63); distances rise towards column 0.
+template <int A>
+__device__ __forceinline__ void rel_fma(float (&x)[64], const uint32_t (&sr)[64],
+                                        const float4* p4, float scale) {
+#pragma unroll
+  for (int w = 0; w < 17; ++w) {
+    const float4 v = p4[w];
+    const float f[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int t = 4 * w + e - A;  // distance above the lowest
+      if (t >= 0 && t < 64) x[63 - t] = fmaf(__uint_as_float(sr[63 - t]), scale, f[e]);
+    }
+  }
+}
+
+// The same from bf16 rel: 17 aligned 8-byte loads of four distances, each
+// widened exactly (a bf16 is the top half of a binary32).
+template <int A>
+__device__ __forceinline__ void rel_fma16(float (&x)[64], const uint32_t (&sr)[64],
+                                          const uint2* p2, float scale) {
+#pragma unroll
+  for (int w = 0; w < 17; ++w) {
+    const uint2 v = p2[w];
+    const float f[4] = {__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xffff0000u),
+                        __uint_as_float(v.y << 16), __uint_as_float(v.y & 0xffff0000u)};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int t = 4 * w + e - A;  // distance above the lowest
+      if (t >= 0 && t < 64) x[63 - t] = fmaf(__uint_as_float(sr[63 - t]), scale, f[e]);
+    }
+  }
+}
+
+// The scaled scores plus the sheared bias of one query row for one 64-key
+// tile whose rel boxes sit at `slot`: row r of the tile (box r / 32, row
+// r % 32 in it), P0 the position of the tile's first row.  Every distance of
+// the tile past rel_extent: pass has_rel = false (no bias).
+template <bool R16>
+__device__ __forceinline__ void scores_with_bias(float (&x)[64], const uint32_t (&sr)[64],
+                                                 const uint8_t* slot, int r, int P0,
+                                                 bool has_rel, float scale) {
+  const int rbox = r / kRelBoxRows, rrow = r % kRelBoxRows;
+  if (!has_rel) {
+#pragma unroll
+    for (int c = 0; c < 64; ++c) x[c] = __uint_as_float(sr[c]) * scale;
+    return;
+  }
+  if constexpr (R16) {
+    // A box starts at distance (P0 + 32 box - j0 - 63) rounded down to 8, so
+    // column 63's distance sits rrow + ((P0 + 1) & 7) into this row; it is
+    // read from the 4-distance piece below it.
+    const int col = rrow + ((P0 + 1) & 7);
+    const uint2* p2 = reinterpret_cast<const uint2*>(
+        reinterpret_cast<const __nv_bfloat16*>(slot + rbox * kRelBoxBytes16) +
+        rrow * kRelBoxCols16 + (col & ~3));
+    switch (col & 3) {  // rrow = 4 lane + q4 (mod 32): the same for the warp
+      case 0: rel_fma16<0>(x, sr, p2, scale); break;
+      case 1: rel_fma16<1>(x, sr, p2, scale); break;
+      case 2: rel_fma16<2>(x, sr, p2, scale); break;
+      default: rel_fma16<3>(x, sr, p2, scale); break;
+    }
+  } else {
+    // A box starts at distance (P0 + 32 box - j0 - 63) rounded down to 4, so
+    // column 63's distance sits rrow + ((P0 + 1) & 3) into this row.
+    const int col = rrow + ((P0 + 1) & 3);
+    const float4* p4 = reinterpret_cast<const float4*>(
+        reinterpret_cast<const float*>(slot + rbox * kRelBoxBytes) + rrow * kRelBoxCols +
+        (col & ~3));
+    switch (col & 3) {  // the same for every lane of the warp
+      case 0: rel_fma<0>(x, sr, p4, scale); break;
+      case 1: rel_fma<1>(x, sr, p4, scale); break;
+      case 2: rel_fma<2>(x, sr, p4, scale); break;
+      default: rel_fma<3>(x, sr, p4, scale); break;
+    }
+  }
+}
+
+}  // namespace prefill
+}  // namespace relattn

@@ -43,6 +43,7 @@ EXPORTS = (
     "relattn_cache_write",
     "relattn_debug_wait_timeout",
     "relattn_debug_decode_give_up",
+    "relattn_debug_walk_decode_ex",
 )
 
 DTYPE_F32 = 0
@@ -141,6 +142,10 @@ def lib() -> ctypes.CDLL:
                                                c_int32, c_int32, S, c_void_p, c_void_p,
                                                c_size_t, c_int32, c_void_p]
     L.relattn_debug_decode_give_up.restype = c_int
+    L.relattn_debug_walk_decode_ex.argtypes = [c_void_p, c_void_p, c_int32, c_int32,
+                                               POINTER(Options), P, S, c_void_p, c_int32,
+                                               c_void_p, c_void_p, c_size_t, c_void_p]
+    L.relattn_debug_walk_decode_ex.restype = c_int
     L.relattn_abi_version.argtypes = []
     L.relattn_abi_version.restype = c_int
     _LIB = L
@@ -480,7 +485,7 @@ def relattn_cache_write(k, v, cu_seqlens, k_cache, v_cache, block_table, ctx_len
 def relattn_prefill(q, k, v, rel, cu_seqlens, k_cache, v_cache, block_table, ctx_lens,
                     window: int, rel_extent: int, max_q_len: int, out=None,
                     workspace=None, out_dtype=torch.bfloat16, sink=None, gate=None,
-                    logit_scale=None, k_scale=None, v_scale=None):
+                    logit_scale=None, k_scale=None, v_scale=None, num_ctas: int = 0):
     """Chunked prefill with a cached prefix; writes k, v into the cache.
 
     rel may be float32 or bfloat16, out bfloat16 or float32 (``out``'s own
@@ -511,7 +516,7 @@ def relattn_prefill(q, k, v, rel, cu_seqlens, k_cache, v_cache, block_table, ctx
     if cu_seqlens.shape[0] != B + 1 or block_table.shape[0] != B:
         raise ValueError("cu_seqlens / block_table batch mismatch")
     cache = cache_desc(k_cache, v_cache)
-    dims = prefill_dims(q, block_table, ctx_lens, max_q_len)
+    dims = prefill_dims(q, block_table, ctx_lens, max_q_len, num_ctas)
     if out is None:
         out = torch.empty((T, Hq, v_cache.shape[3]), dtype=out_dtype, device=dev)
     else:
@@ -547,6 +552,32 @@ def debug_walk_decode(block_table, seq_lens, window: int, k_cache, v_cache, num_
         block_table.data_ptr(), seq_lens.data_ptr(), int(window), ctypes.byref(cache),
         ctypes.byref(dims), rec.data_ptr(), max_records, cnt.data_ptr(), ws.data_ptr(),
         ws.numel(), _stream(dev)), "relattn_debug_walk_decode")
+    n = int(cnt.item())
+    if n > max_records:
+        raise RuntimeError("walk produced more records than the buffer holds")
+    return rec[:n].cpu(), read_status(ws)
+
+
+def debug_walk_decode_ex(block_table, seq_lens, num_query_tokens: int, window: int, k_cache,
+                         v_cache, num_q_heads: int, num_ctas: int = 0,
+                         max_records: int = 1 << 20):
+    """Replay of the decode kernel's walk for k query tokens per sequence over
+    the cache's type: int32 [n, 8] records (cta, sequence, first token of the
+    chunk, KV head, key tile, physical block, first key brought, keys)."""
+    dev = block_table.device
+    cache = cache_desc(k_cache, v_cache)
+    dims = Dims(block_table.shape[0], num_q_heads, block_table.shape[1], 0, 0, num_ctas)
+    ws = new_workspace(workspace_size(dims, cache), dev)
+    opts = Options(DTYPE_F32, DTYPE_BF16, None, None,
+                   DTYPE_E4M3 if k_cache.dtype == torch.float8_e4m3fn else DTYPE_BF16,
+                   1.0, 1.0, None)
+    rec = torch.zeros((max_records, 8), dtype=torch.int32, device=dev)
+    cnt = torch.zeros(1, dtype=torch.int32, device=dev)
+    _check(lib().relattn_debug_walk_decode_ex(
+        block_table.data_ptr(), seq_lens.data_ptr(), int(num_query_tokens), int(window),
+        ctypes.byref(opts), ctypes.byref(cache), ctypes.byref(dims), rec.data_ptr(),
+        max_records, cnt.data_ptr(), ws.data_ptr(), ws.numel(), _stream(dev)),
+        "relattn_debug_walk_decode_ex")
     n = int(cnt.item())
     if n > max_records:
         raise RuntimeError("walk produced more records than the buffer holds")

@@ -21,21 +21,22 @@ def built():
     R.lib()
 
 
-def run_prefill(case, ws=None):
+def run_prefill(case, ws=None, num_ctas=0):
     return R.relattn_prefill(case["q"], case["k"], case["v"], case["rel"],
                              case["cu_seqlens"], case["k_cache"], case["v_cache"],
                              case["block_table"], case["ctx_lens"], case["window"],
-                             case["rel_extent"], case["max_q_len"], workspace=ws)
+                             case["rel_extent"], case["max_q_len"], workspace=ws,
+                             num_ctas=num_ctas)
 
 
-def check_case(case, rows=None, what=""):
+def check_case(case, rows=None, what="", num_ctas=0):
     cache0 = snapshot_cache(case)
     want, kc_want, vc_want = oracle_prefill(case, rows=rows, cache=cache0)
     dims = R.prefill_dims(case["q"], case["block_table"], case["ctx_lens"],
                           case["max_q_len"])
     ws = R.new_workspace(R.workspace_size(dims, R.cache_desc(case["k_cache"],
                                                              case["v_cache"])), DEV)
-    out = run_prefill(case, ws)
+    out = run_prefill(case, ws, num_ctas)
     torch.cuda.synchronize()
     assert R.read_status(ws) == 0
     # the cache write is a copy: bit-exact, everywhere
@@ -68,6 +69,27 @@ SMALL = {
 def test_prefill_small_configs(name):
     case = I.make_prefill(SMALL[name], DEV, seed_data=2, seed_layout=3)
     check_case(case, what=name)
+
+
+# Head-group sizes and grids for the two-heads-per-item kernel: odd groups
+# leave one head alone in an item (the second softmax group skips it), and a
+# small grid makes each CTA run many items back to back through its ring.
+ITEMS = {
+    "g3_three_ctas": (I.PrefillWorkload("g3", 6, 2, 128, 128, 300, 256, (260, 129), (70, 0)), 3),
+    "g5_one_cta": (I.PrefillWorkload("g5", 5, 1, 128, 128, 0, 128, (300,), (40,)), 1),
+    "g1_two_ctas": (I.PrefillWorkload("g1", 2, 2, 128, 64, 200, 128, (257, 3), (0, 90)), 2),
+    "g6_seven_ctas": (I.PrefillWorkload("g6s", 12, 2, 128, 128, 1024, 1024, (384, 100),
+                                        (700, 0)), 7),
+    "g2_bf16_many_items": (I.PrefillWorkload("g2m", 8, 4, 128, 128, 512, 512, (640, 512),
+                                             (1000, 64)), 5),
+}
+
+
+@pytest.mark.parametrize("name", sorted(ITEMS))
+def test_prefill_items_and_grids(name):
+    wl, ctas = ITEMS[name]
+    case = I.make_prefill(wl, DEV, seed_data=6, seed_layout=7)
+    check_case(case, what=name, num_ctas=ctas)
 
 
 def test_prefill_then_decode_agree():
