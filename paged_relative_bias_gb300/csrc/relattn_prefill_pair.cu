@@ -26,9 +26,10 @@
 // a scratch slot per head for storing O.  Each entry is consumed by the
 // softmax group of its head; the producer fills entries in order.
 //
-// Warp roles: 0 = K/V TMA producer, 1 = MMA issuer and TMEM owner, 2-5 =
-// softmax of head slot 0, 6-9 = softmax of head slot 1 (TMEM lane quarters 2,
-// 3, 0, 1 each), 10 = ring producer.
+// Warp roles: 0-3 = softmax of head slot 0, 4-7 = softmax of head slot 1
+// (TMEM lane quarters 0-3 each), 8 = K/V TMA producer, 9 = MMA issuer and
+// TMEM owner, 10 = ring producer, 11 idle.  The producer warpgroup (8-11)
+// hands most of its registers to the two softmax warpgroups.
 #include "relattn_common.cuh"
 #include "relattn_internal.h"
 #include "relattn_prefill.cuh"
@@ -40,8 +41,16 @@ namespace {
 
 using namespace prefill;
 
-constexpr int kWarps = 11;
+constexpr int kWarps = 12;
 constexpr int kThreads = 32 * kWarps;
+constexpr int kKvWarp = 8, kMmaWarp = 9, kRingWarp = 10;  // warpgroup 2
+// Registers per thread: the launch gives every thread kLaunchRegs (the most
+// that 384 threads may hold on one SM; the host checks that the kernel was
+// built with exactly that many), then the producer warpgroup drops to
+// kProdRegs and the two softmax warpgroups rise to kSoftRegs:
+// 2 x 128 x 208 + 128 x 88 = 384 x 168.
+constexpr int kLaunchRegs = 168, kSoftRegs = 208, kProdRegs = 88;
+static_assert(2 * 128 * kSoftRegs + 128 * kProdRegs <= kThreads * kLaunchRegs, "register split");
 constexpr int kMaxSlots = 6;  // ring slots, at most
 constexpr int kMinSlots = 3;  // fewer would deadlock the ring (see the epilogue)
 constexpr uint32_t kTmemCols = 512;
@@ -171,7 +180,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   for (int i = tid; i < (L.ring - L.k) / 16; i += blockDim.x)
     reinterpret_cast<uint4*>(smem + L.k)[i] = make_uint4(0, 0, 0, 0);
   fence_proxy_async_smem();
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     tmem_alloc(s_tmem, kTmemCols);
     tc_fence_before();
   }
@@ -179,7 +188,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tbase = *s_tmem;
 
-  if (warp == 0 && lane == 0) {
+  if (warp >= kKvWarp) {
+  // Each warpgroup changes its register count inside its own branch, so that
+  // the compiler allocates each role's code with that role's count.
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProdRegs));
+  if (warp == kKvWarp && lane == 0) {
     // ---------------------------------------------------- K/V TMA producer
     int n = 0;
     for (int idx = blockIdx.x; idx < total && !*s_abort; idx += gridDim.x) {
@@ -212,7 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-  } else if (warp == kWarps - 1 && lane == 0) {
+  } else if (warp == kRingWarp && lane == 0) {
     // --------------------------------------------------- ring producer
     int e = 0;
     bool fail = false;
@@ -257,7 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     if (fail) *s_abort = 1;
-  } else if (warp == 1 && lane == 0) {
+  } else if (warp == kMmaWarp && lane == 0) {
     // ---------------------------------------------------------- MMA issuer
     constexpr uint32_t kIdescPV = umma_idesc_bf16(128, DV, 1);
     int n = 0;               // K/V tiles
@@ -315,13 +328,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     // all MMAs retired before TMEM is released
     umma_commit(&bars[kDrain]);
     if (!mbar_wait(&bars[kDrain], 0)) report(p.status, RELATTN_DEV_WAIT_TIMEOUT);
-  } else if (warp >= 2 && warp < kWarps - 1) {
+  }
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSoftRegs));
     // ------------------------------------------------------------ softmax
     // Group wg = 0, 1 serves head slot wg.  Thread (q4, lane) owns TMEM lane
     // 32 q4 + lane and puts query row r = 4 lane + q4 there: each warp takes
     // every fourth row, so all its lanes see the same 16-byte alignment of
     // their rows in the rel boxes.
-    const int wg = (warp - 2) >> 2;
+    const int wg = warp >> 2;
     const int bar_id = 1 + wg;  // the group's named barrier (128 threads)
     const int q4 = warp & 3;    // TMEM lane quarter this warp may access
     const int r = 4 * lane + q4;
@@ -605,7 +620,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tbase, kTmemCols);
+  if (warp == kMmaWarp) tmem_dealloc(tbase, kTmemCols);
 }
 
 // Replays the work split and block walk of prefill_pair_kernel with the same
@@ -660,6 +675,15 @@ int prefill_pair_slots(int B, int dv, int rel_es, int smem_optin) {
 
 template <int DV, bool R16, bool O32>
 static cudaError_t launch_pair_as(const PrefillLaunch& L, int grid, int smem, cudaStream_t stream) {
+  // The kernel's register split assumes the launch holds kLaunchRegs per
+  // thread; with fewer, the softmax warpgroups' raise could never be met.
+  static const int regs = [] {
+    cudaFuncAttributes a{};
+    return cudaFuncGetAttributes(&a, prefill_pair_kernel<DV, R16, O32>) == cudaSuccess
+               ? a.numRegs
+               : -1;
+  }();
+  if (regs != kLaunchRegs) return cudaErrorInvalidConfiguration;
   cudaError_t e = ensure_smem<prefill_pair_kernel<DV, R16, O32>>(smem);
   if (e != cudaSuccess) return e;
   prefill_pair_kernel<DV, R16, O32><<<grid, kThreads, smem, stream>>>(L.tm_q, L.tm_k, L.tm_v,
