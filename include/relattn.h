@@ -74,6 +74,10 @@ extern "C" {
                                          capacity: the sequence was skipped */
 #define RELATTN_DEV_WAIT_TIMEOUT 0x4u /* an internal pipeline wait ran past its
                                          limit (about 2 s): the CTA gave up */
+#define RELATTN_DEV_Q_RANGE      0x8u /* a call over an e4m3 cache, which computes
+                                         in f16, met a query element outside f16's
+                                         range (|q| > 65504 after rounding) or not
+                                         finite: that row's output is inf or NaN */
 
 /* The paged KV cache (device memory, caller-owned). */
 typedef struct relattn_kv_cache {

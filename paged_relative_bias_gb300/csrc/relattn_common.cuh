@@ -54,6 +54,12 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
+// Either f16 of a pair is infinite or NaN: a query element narrowed to f16
+// that did not fit its range (or was not finite to begin with).
+__device__ __forceinline__ bool f16x2_nonfinite(uint32_t h) {
+  return (h & 0x7c00u) == 0x7c00u || (h & 0x7c000000u) == 0x7c000000u;
+}
+
 __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
   const __half2 h = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&h);

@@ -867,15 +867,19 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         const int fr = fl >> 2, ft = fl & 3;
         const int d0 = 64 * (ft >> 1) + 16 * (fs >> 1) + 8 * (ft & 1) + 4 * (fs & 1);
         const uint8_t* qsrc = smem + L.qbuf + qb * QB;
+        bool q_range = false;  // a valid row's element did not fit f16
         auto pair = [&](int row, int d) {  // bf16 of dimensions d, d + 1 -> f16
-          return bf16x2_to_f16x2(*reinterpret_cast<const uint32_t*>(
+          const uint32_t h = bf16x2_to_f16x2(*reinterpret_cast<const uint32_t*>(
               qsrc + (d >> 6) * QH + sw128(row, (d & 63) >> 3) + (d & 7) * 2));
+          if (row < nrows && f16x2_nonfinite(h)) q_range = true;
+          return h;
         };
 #pragma unroll
         for (int h = 0; h < (RS ? 2 : 1); ++h)  // RS: rows 16 h .. 16 h + 15 for group h
           reinterpret_cast<uint4*>(smem + L.priv + h * kPrivQA)[fs * 32 + fl] =
               make_uint4(pair(16 * h + fr, d0), pair(16 * h + fr + 8, d0),
                          pair(16 * h + fr, d0 + 2), pair(16 * h + fr + 8, d0 + 2));
+        if (q_range) report(p.status, RELATTN_DEV_Q_RANGE);
       } else if (lane == 0) {
         s_misc[kMiscAbort] = 1;
       }
@@ -900,12 +904,18 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     uint2* const qfrag = reinterpret_cast<uint2*>(smem + L.priv + cwarp * kPrivQ);
     if (KV8 && !MULTI && qok) {
 #pragma unroll
+      bool q_range = false;  // an element of this lane's row r0 did not fit f16
       for (int u = 0; u < 4; ++u) {
         const uint4 v = *reinterpret_cast<const uint4*>(
             smem + L.qbuf + qb * QB + (cq >> 1) * QH + sw128(r0, 2 * u + (cq & 1)));
-        qfrag[(2 * u) * 32 + lane] = make_uint2(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y));
-        qfrag[(2 * u + 1) * 32 + lane] = make_uint2(bf16x2_to_f16x2(v.z), bf16x2_to_f16x2(v.w));
+        const uint2 a = make_uint2(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y));
+        const uint2 b = make_uint2(bf16x2_to_f16x2(v.z), bf16x2_to_f16x2(v.w));
+        q_range |= f16x2_nonfinite(a.x) || f16x2_nonfinite(a.y) || f16x2_nonfinite(b.x) ||
+                   f16x2_nonfinite(b.y);
+        qfrag[(2 * u) * 32 + lane] = a;
+        qfrag[(2 * u + 1) * 32 + lane] = b;
       }
+      if (q_range && r0 < nrows) report(p.status, RELATTN_DEV_Q_RANGE);
       __syncwarp();
       if (lane == 0) mbar_arrive(&qempty[qb]);
     }

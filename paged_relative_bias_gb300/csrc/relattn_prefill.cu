@@ -468,9 +468,11 @@ __global__ void __launch_bounds__(32 * (kPfWarps + (KV8 ? 1 : 0)), 1)
       return smem + L.ring + slot * kRingSlotBytes;
     };
     // This thread's query row, from a ring slot (128-byte swizzled rows) into
-    // TMEM, the A operand of S = Q K^T; then the MMA warp may start.
-    auto load_q = [&](const uint8_t* qs, int entry) {
+    // TMEM, the A operand of S = Q K^T; then the MMA warp may start.  row_valid:
+    // the row is one of the item's (an e4m3 cache's f16 query is checked then).
+    auto load_q = [&](const uint8_t* qs, int entry, bool row_valid) {
       uint32_t qr[64];
+      bool q_range = false;
 #pragma unroll
       for (int c = 0; c < 2; ++c)
 #pragma unroll
@@ -482,6 +484,8 @@ __global__ void __launch_bounds__(32 * (kPfWarps + (KV8 ? 1 : 0)), 1)
             qr[(c * 8 + j) * 4 + 1] = bf16x2_to_f16x2(v.y);
             qr[(c * 8 + j) * 4 + 2] = bf16x2_to_f16x2(v.z);
             qr[(c * 8 + j) * 4 + 3] = bf16x2_to_f16x2(v.w);
+#pragma unroll
+            for (int w = 0; w < 4; ++w) q_range |= f16x2_nonfinite(qr[(c * 8 + j) * 4 + w]);
           } else {
             qr[(c * 8 + j) * 4] = v.x;
             qr[(c * 8 + j) * 4 + 1] = v.y;
@@ -489,6 +493,7 @@ __global__ void __launch_bounds__(32 * (kPfWarps + (KV8 ? 1 : 0)), 1)
             qr[(c * 8 + j) * 4 + 3] = v.w;
           }
         }
+      if (KV8 && q_range && row_valid) report(p.status, RELATTN_DEV_Q_RANGE);
       tmem_st32(tl + kTmQ, qr);
       tmem_st32(tl + kTmQ + 32, qr + 32);
       tmem_wait_st();
@@ -510,7 +515,7 @@ __global__ void __launch_bounds__(32 * (kPfWarps + (KV8 ? 1 : 0)), 1)
       if (items == 0) {  // later items' queries are loaded during the previous epilogue
         const uint8_t* qs = slot_wait(e);
         if (!qs) bad = true;
-        else load_q(qs, e);
+        else load_q(qs, e, r < it.rows);
         ++e;
       }
       const bool row_ok = r < it.rows;
@@ -646,8 +651,10 @@ __global__ void __launch_bounds__(32 * (kPfWarps + (KV8 ? 1 : 0)), 1)
       const bool has_next = idx + static_cast<int>(gridDim.x) < total;
       if (has_next && !bad) {
         const uint8_t* qs = slot_wait(e + 1);
+        PItem nit;
+        prefill_item(idx + gridDim.x, p, sa, nit);
         if (!qs) bad = true;
-        else load_q(qs, e + 1);
+        else load_q(qs, e + 1, r < nit.rows);
       }
       // O / l -> out, through the scratch slot (the tile's 128 rows, 16-byte
       // chunks swizzled by row / 4) so that the global stores are whole rows

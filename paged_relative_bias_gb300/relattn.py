@@ -25,6 +25,7 @@ ERR_CUDA = 4
 DEV_BAD_BLOCK_ID = 0x1
 DEV_BAD_LENGTH = 0x2
 DEV_WAIT_TIMEOUT = 0x4
+DEV_Q_RANGE = 0x8
 
 EXPORTS = (
     "relattn_workspace_size",
