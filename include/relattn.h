@@ -328,6 +328,14 @@ int relattn_decode_noalloc(const void* q, const float* rel,
  *
  * dims->num_tokens must equal cu_seqlens[B] and dims->max_q_len must bound
  * every chunk length (both host-side; nothing is read back).
+ *
+ * Work split: over a bf16 cache a work item is one 128-row query tile and two
+ * query heads of one KV group, which share each read of their keys and
+ * values ("Inkling 2 Small on vLLM", section "vLLM integration and
+ * optimisation"); when the one-head items of a call would fit one wave of
+ * CTAs (a latency-bound call) and no grid is forced, and over an e4m3 cache,
+ * an item is one query tile and one head.  The results do not depend on the
+ * split beyond rounding order.
  */
 int relattn_prefill(const void* q, const void* k, const void* v,
                     const float* rel, const int32_t* cu_seqlens,
@@ -435,10 +443,11 @@ int relattn_debug_walk_decode_ex(const int32_t* block_table, const int32_t* seq_
                                  size_t workspace_bytes, void* stream);
 
 /*
- * Test hook: replay the prefill kernel's work split and block walk (the
- * kernel of bf16 caches, whose work items are a 128-row query tile and a pair
- * of query heads of one KV group), with the same device code and grid as
- * relattn_prefill.  Each (work item, key tile) visit appends
+ * Test hook: replay the work split and block walk of the prefill kernel whose
+ * work items are a 128-row query tile and a pair of query heads of one KV
+ * group (the kernel relattn_prefill runs over a bf16 cache unless the call
+ * fits one wave of one-head items), with the same device code and the grid
+ * that kernel gets.  Each (work item, key tile) visit appends
  * { sequence, first_row_of_query_tile (within the sequence), key_tile,
  *   logical_block, physical_block, first_head_of_item } (6 int32) to
  * `records`.

@@ -604,8 +604,16 @@ static int prepare_prefill(const void* q, const void* k, const void* v, const vo
   DeviceInfo di;
   if (!device_info(&di)) return RELATTN_ERR_CUDA;
   // bf16 caches: two heads of a KV group per work item when its ring fits;
-  // otherwise (e4m3 caches, or very many sequences) one head per item
-  const int pair_slots = io.kv_es == 2 ? prefill_pair_slots(p.B, p.dv, p.rel_es, di.smem_optin) : 0;
+  // otherwise (e4m3 caches, or very many sequences) one head per item.  A call
+  // whose one-head items fit one wave of CTAs is latency-bound, and one head
+  // per item spreads it over more SMs; a forced grid (num_ctas > 0) keeps the
+  // two-heads kernel.
+  const long long one_head_items =
+      static_cast<long long>(p.B) * ((p.max_q_len + 127) / 128) * p.Hq;
+  const bool one_wave = !walk && dims->num_ctas == 0 && one_head_items <= di.sms;
+  const int pair_slots = io.kv_es == 2 && !one_wave
+                             ? prefill_pair_slots(p.B, p.dv, p.rel_es, di.smem_optin)
+                             : 0;
   L->pair = pair_slots > 0 ? 1 : 0;
   p.ring_stages = L->pair ? pair_slots : prefill_ring_stages(p.B, p.dv, p.kv_es, di.smem_optin);
   if (p.ring_stages == 0) return RELATTN_ERR_UNSUPPORTED;

@@ -110,23 +110,25 @@ PREFILL = {
 }
 
 
+@pytest.mark.parametrize("num_ctas", [0, 148])  # 148: two heads per work item (forced grid)
 @pytest.mark.parametrize("name", sorted(PREFILL))
 @pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
-def test_gated_prefill(name, out_dtype):
+def test_gated_prefill(name, out_dtype, num_ctas):
     case = I.make_prefill(PREFILL[name], DEV, seed_data=101)
     T, Hq = case["q"].shape[:2]
     case["sink"] = logits_like((T, Hq), 102)
     case["gate"] = logits_like((T, Hq), 103)
     cache0 = snapshot_cache(case)
     want, _, _ = oracle_prefill(case, cache=cache0)
-    dims = R.prefill_dims(case["q"], case["block_table"], case["ctx_lens"], case["max_q_len"])
+    dims = R.prefill_dims(case["q"], case["block_table"], case["ctx_lens"], case["max_q_len"],
+                          num_ctas)
     ws = R.new_workspace(R.workspace_size(dims, R.cache_desc(case["k_cache"],
                                                              case["v_cache"])), DEV)
     out = R.relattn_prefill(case["q"], case["k"], case["v"], case["rel"], case["cu_seqlens"],
                             case["k_cache"], case["v_cache"], case["block_table"],
                             case["ctx_lens"], case["window"], case["rel_extent"],
                             case["max_q_len"], workspace=ws, out_dtype=out_dtype,
-                            sink=case["sink"], gate=case["gate"])
+                            sink=case["sink"], gate=case["gate"], num_ctas=num_ctas)
     torch.cuda.synchronize()
     assert R.read_status(ws) == 0
     assert_parity(to_f64(out), want, what=f"{name} out={out_dtype}")

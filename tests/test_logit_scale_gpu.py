@@ -48,8 +48,9 @@ def run_decode(case, num_ctas=0, out_dtype=torch.bfloat16):
     return out
 
 
-def run_prefill(case, out_dtype=torch.bfloat16):
-    dims = R.prefill_dims(case["q"], case["block_table"], case["ctx_lens"], case["max_q_len"])
+def run_prefill(case, out_dtype=torch.bfloat16, num_ctas=0):
+    dims = R.prefill_dims(case["q"], case["block_table"], case["ctx_lens"], case["max_q_len"],
+                          num_ctas)
     ws = R.new_workspace(R.workspace_size(dims, R.cache_desc(case["k_cache"],
                                                              case["v_cache"])), DEV)
     out = R.relattn_prefill(case["q"], case["k"], case["v"], case["rel"], case["cu_seqlens"],
@@ -57,7 +58,7 @@ def run_prefill(case, out_dtype=torch.bfloat16):
                             case["ctx_lens"], case["window"], case["rel_extent"],
                             case["max_q_len"], workspace=ws, out_dtype=out_dtype,
                             sink=case.get("sink"), gate=case.get("gate"),
-                            logit_scale=case.get("logit_scale"))
+                            logit_scale=case.get("logit_scale"), num_ctas=num_ctas)
     torch.cuda.synchronize()
     assert R.read_status(ws) == 0
     return out
@@ -136,14 +137,15 @@ PREFILL = {
 }
 
 
+@pytest.mark.parametrize("num_ctas", [0, 148])  # 148: two heads per work item (forced grid)
 @pytest.mark.parametrize("name", sorted(PREFILL))
 @pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
-def test_scaled_prefill(name, out_dtype):
+def test_scaled_prefill(name, out_dtype, num_ctas):
     case = I.make_prefill(PREFILL[name], DEV, seed_data=141)
     case["logit_scale"] = factors(case["q"].shape[:1], 142, lo=0.25, hi=4.0)
     cache0 = snapshot_cache(case)
     want, _, _ = oracle_prefill(case, cache=cache0)
-    out = run_prefill(case, out_dtype)
+    out = run_prefill(case, out_dtype, num_ctas)
     assert_parity(to_f64(out), want, what=f"{name} out={out_dtype}")
 
 

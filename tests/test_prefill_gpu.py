@@ -47,10 +47,16 @@ def check_case(case, rows=None, what="", num_ctas=0):
     return assert_parity(got[sel], want[sel], what=what)
 
 
-def test_tiny_prefill_config():
+# num_ctas 0: the library's choice (small calls: one head per work item);
+# 148: a forced grid, which keeps two heads of a KV group per work item
+GRIDS = [0, 148]
+
+
+@pytest.mark.parametrize("num_ctas", GRIDS)
+def test_tiny_prefill_config(num_ctas):
     """1 x 256 tokens, 4/1 heads, window = rel_extent = 64, table [1, 0]."""
     case = I.make_prefill(I.WORKLOADS["tiny_prefill"], DEV)
-    check_case(case, what="tiny")
+    check_case(case, what="tiny", num_ctas=num_ctas)
 
 
 SMALL = {
@@ -65,10 +71,11 @@ SMALL = {
 }
 
 
+@pytest.mark.parametrize("num_ctas", GRIDS)
 @pytest.mark.parametrize("name", sorted(SMALL))
-def test_prefill_small_configs(name):
+def test_prefill_small_configs(name, num_ctas):
     case = I.make_prefill(SMALL[name], DEV, seed_data=2, seed_layout=3)
-    check_case(case, what=name)
+    check_case(case, what=name, num_ctas=num_ctas)
 
 
 # Head-group sizes and grids for the two-heads-per-item kernel: odd groups

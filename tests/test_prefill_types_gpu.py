@@ -27,24 +27,26 @@ def built():
     R.lib()
 
 
-def run(case, out_dtype):
-    dims = R.prefill_dims(case["q"], case["block_table"], case["ctx_lens"], case["max_q_len"])
+def run(case, out_dtype, num_ctas=0):
+    dims = R.prefill_dims(case["q"], case["block_table"], case["ctx_lens"], case["max_q_len"],
+                          num_ctas)
     ws = R.new_workspace(R.workspace_size(dims, R.cache_desc(case["k_cache"],
                                                              case["v_cache"])), DEV)
     out = R.relattn_prefill(case["q"], case["k"], case["v"], case["rel"], case["cu_seqlens"],
                             case["k_cache"], case["v_cache"], case["block_table"],
                             case["ctx_lens"], case["window"], case["rel_extent"],
-                            case["max_q_len"], workspace=ws, out_dtype=out_dtype)
+                            case["max_q_len"], workspace=ws, out_dtype=out_dtype,
+                            num_ctas=num_ctas)
     torch.cuda.synchronize()
     assert R.read_status(ws) == 0
     assert out.dtype == out_dtype
     return out
 
 
-def check(case, out_dtype, rows=None, what=""):
+def check(case, out_dtype, rows=None, what="", num_ctas=0):
     cache0 = snapshot_cache(case)
     want, kc_want, vc_want = oracle_prefill(case, rows=rows, cache=cache0)
-    out = run(case, out_dtype)
+    out = run(case, out_dtype, num_ctas)
     assert np.array_equal(bf16_bits(case["k_cache"]), kc_want), "k cache"
     assert np.array_equal(bf16_bits(case["v_cache"]), vc_want), "v cache"
     sel = slice(None) if rows is None else list(rows)
@@ -64,14 +66,15 @@ SMALL = {
 }
 
 
+@pytest.mark.parametrize("num_ctas", [0, 148])  # 148: two heads per work item (forced grid)
 @pytest.mark.parametrize("name", sorted(SMALL))
 @pytest.mark.parametrize("rel_dtype,out_dtype", [(torch.bfloat16, torch.bfloat16),
                                                  (torch.float32, torch.float32),
                                                  (torch.bfloat16, torch.float32)])
-def test_typed_prefill_small(name, rel_dtype, out_dtype):
+def test_typed_prefill_small(name, rel_dtype, out_dtype, num_ctas):
     case = I.make_prefill(SMALL[name], DEV, seed_data=7, seed_layout=8)
     case["rel"] = case["rel"].to(rel_dtype)
-    check(case, out_dtype, what=f"{name} rel={rel_dtype} out={out_dtype}")
+    check(case, out_dtype, what=f"{name} rel={rel_dtype} out={out_dtype}", num_ctas=num_ctas)
 
 
 @pytest.mark.parametrize("rel_dtype", [torch.float32, torch.bfloat16])
