@@ -903,8 +903,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     // 64 (cq >> 1) + 16 u + 8 (cq & 1) + 0..7: one 16-byte piece of the row.
     uint2* const qfrag = reinterpret_cast<uint2*>(smem + L.priv + cwarp * kPrivQ);
     if (KV8 && !MULTI && qok) {
-#pragma unroll
       bool q_range = false;  // an element of this lane's row r0 did not fit f16
+#pragma unroll
       for (int u = 0; u < 4; ++u) {
         const uint4 v = *reinterpret_cast<const uint4*>(
             smem + L.qbuf + qb * QB + (cq >> 1) * QH + sw128(r0, 2 * u + (cq & 1)));

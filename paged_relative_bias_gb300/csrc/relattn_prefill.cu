@@ -458,7 +458,6 @@ __global__ void __launch_bounds__(32 * (kPfWarps + (KV8 ? 1 : 0)), 1)
     // lanes see the same 16-byte alignment of their rows in the rel boxes.
     const int q4 = warp & 3;  // TMEM lane quarter this warp may access
     const int r = 4 * lane + q4;
-    const int rbox = r / kRelBoxRows, rrow = r % kRelBoxRows;  // row's rel box and row in it
     const uint32_t tl = tbase + (static_cast<uint32_t>(32 * q4) << 16);
     int n = 0, e = 0, items = 0;  // key tiles and ring entries consumed
     bool fail = false;
@@ -558,39 +557,8 @@ __global__ void __launch_bounds__(32 * (kPfWarps + (KV8 ? 1 : 0)), 1)
         const uint8_t* slot = slot_wait(e);
         if (!slot) { ok = false; break; }
         float x[64];
-        if (it.P0 - j0 - (kTileKeys - 1) < p.rel_extent) {
-          if constexpr (R16) {
-            // A box starts at distance (P0 + 32 box - j0 - 63) rounded down to
-            // 8, so column 63's distance sits rrow + ((P0 + 1) & 7) into this
-            // row; it is read from the 4-distance piece below it.
-            const int col = rrow + ((it.P0 + 1) & 7);
-            const uint2* p2 = reinterpret_cast<const uint2*>(
-                reinterpret_cast<const __nv_bfloat16*>(slot + rbox * kRelBoxBytes16) +
-                rrow * kRelBoxCols16 + (col & ~3));
-            switch (col & 3) {  // rrow = 4 lane + q4 (mod 32): the same for the warp
-              case 0: rel_fma16<0>(x, sr, p2, scale); break;
-              case 1: rel_fma16<1>(x, sr, p2, scale); break;
-              case 2: rel_fma16<2>(x, sr, p2, scale); break;
-              default: rel_fma16<3>(x, sr, p2, scale); break;
-            }
-          } else {
-            // A box starts at distance (P0 + 32 box - j0 - 63) rounded down to 4,
-            // so column 63's distance sits rrow + ((P0 + 1) & 3) into this row.
-            const int col = rrow + ((it.P0 + 1) & 3);
-            const float4* p4 = reinterpret_cast<const float4*>(
-                reinterpret_cast<const float*>(slot + rbox * kRelBoxBytes) + rrow * kRelBoxCols +
-                (col & ~3));
-            switch (col & 3) {  // the same for every lane of the warp
-              case 0: rel_fma<0>(x, sr, p4, scale); break;
-              case 1: rel_fma<1>(x, sr, p4, scale); break;
-              case 2: rel_fma<2>(x, sr, p4, scale); break;
-              default: rel_fma<3>(x, sr, p4, scale); break;
-            }
-          }
-        } else {  // every distance is past rel_extent: no bias
-#pragma unroll
-          for (int c = 0; c < 64; ++c) x[c] = __uint_as_float(sr[c]) * scale;
-        }
+        scores_with_bias<R16>(x, sr, slot, r, it.P0,
+                              it.P0 - j0 - (kTileKeys - 1) < p.rel_extent, scale);
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[kREmpty + e % nrs]);
         if (!warp_full) {
