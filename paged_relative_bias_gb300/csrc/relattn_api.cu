@@ -77,7 +77,7 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, int rank, void* base,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-bool cache_maps(const relattn_kv_cache* c, CUtensorMap* tk, CUtensorMap* tv) {
+bool cache_maps(const relattn_kv_cache* c, int box_rows, CUtensorMap* tk, CUtensorMap* tv) {
   const cuuint64_t rows = static_cast<cuuint64_t>(c->num_blocks) * c->block_size;
   const cuuint64_t kd[3] = {static_cast<cuuint64_t>(c->d_qk),
                             static_cast<cuuint64_t>(c->num_kv_heads), rows};
@@ -87,7 +87,7 @@ bool cache_maps(const relattn_kv_cache* c, CUtensorMap* tk, CUtensorMap* tv) {
                             static_cast<cuuint64_t>(c->num_kv_heads), rows};
   const cuuint64_t vs[2] = {static_cast<cuuint64_t>(c->d_v) * 2,
                             static_cast<cuuint64_t>(c->num_kv_heads) * c->d_v * 2};
-  const cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(kTileKeys)};
+  const cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(box_rows)};
   return make_map(tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, c->k, kd, ks, box,
                   CU_TENSOR_MAP_SWIZZLE_128B) &&
          make_map(tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, c->v, vd, vs, box,
@@ -611,11 +611,19 @@ static int prepare_prefill(const void* q, const void* k, const void* v, const vo
   const long long one_head_items =
       static_cast<long long>(p.B) * ((p.max_q_len + 127) / 128) * p.Hq;
   const bool one_wave = !walk && dims->num_ctas == 0 && one_head_items <= di.sms;
-  const int pair_slots = io.kv_es == 2 && !one_wave
+  // bf16 cache and bf16 rel with d_v = 128: one head per item over 128-key
+  // tiles (the tensor pipe at N = 128) when its ring fits
+  const int wide_slots = io.kv_es == 2 && io.rel_es == 2 && p.dv == 128 && !one_wave && !walk
+                             ? prefill_wide_slots(p.B, di.smem_optin)
+                             : 0;
+  L->wide = wide_slots > 0 ? 1 : 0;
+  const int pair_slots = io.kv_es == 2 && !one_wave && !L->wide
                              ? prefill_pair_slots(p.B, p.dv, p.rel_es, di.smem_optin)
                              : 0;
   L->pair = pair_slots > 0 ? 1 : 0;
-  p.ring_stages = L->pair ? pair_slots : prefill_ring_stages(p.B, p.dv, p.kv_es, di.smem_optin);
+  p.ring_stages = L->wide   ? wide_slots
+                  : L->pair ? pair_slots
+                            : prefill_ring_stages(p.B, p.dv, p.kv_es, di.smem_optin);
   if (p.ring_stages == 0) return RELATTN_ERR_UNSUPPORTED;
   const long long heads = L->pair ? static_cast<long long>(p.Hkv) * ((p.g + 1) / 2) : p.Hq;
   const long long items = static_cast<long long>(p.B) * ((p.max_q_len + 127) / 128) * heads;
@@ -624,7 +632,7 @@ static int prepare_prefill(const void* q, const void* k, const void* v, const vo
   if (walk) return RELATTN_OK;
   // e4m3 caches: 2-D boxes of 64 head-major rows, landing in staging slots
   if (!(io.kv_es == 1 ? decode_cache_maps_e4m3(cache, kTileKeys, &L->tm_k, &L->tm_v)
-                      : cache_maps(cache, &L->tm_k, &L->tm_v)))
+                      : cache_maps(cache, L->wide ? 128 : kTileKeys, &L->tm_k, &L->tm_v)))
     return RELATTN_ERR_CUDA;
   // q [T][Hq][128] bf16: one head's 128-token tile as two 64-column boxes
   const cuuint64_t qd[3] = {128, static_cast<cuuint64_t>(dims->num_q_heads),
@@ -635,13 +643,13 @@ static int prepare_prefill(const void* q, const void* k, const void* v, const vo
                 CU_TENSOR_MAP_SWIZZLE_128B))
     return RELATTN_ERR_CUDA;
   // rel [T][Hq][E] fp32 or bf16: boxes of 32 tokens x 100 (fp32) or 104
-  // (bf16) distances of one head
+  // (bf16) distances of one head; 168 bf16 distances for 128-key tiles
   const cuuint64_t rd[3] = {static_cast<cuuint64_t>(rel_extent),
                             static_cast<cuuint64_t>(dims->num_q_heads),
                             static_cast<cuuint64_t>(dims->num_tokens)};
   const cuuint64_t rs[2] = {static_cast<cuuint64_t>(rel_extent) * io.rel_es,
                             static_cast<cuuint64_t>(rel_extent) * io.rel_es * dims->num_q_heads};
-  const cuuint32_t rb[3] = {io.rel_es == 2 ? 104u : 100u, 1, 32};
+  const cuuint32_t rb[3] = {L->wide ? 168u : io.rel_es == 2 ? 104u : 100u, 1, 32};
   if (!make_map(&L->tm_rel,
                 io.rel_es == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
                 3, const_cast<void*>(rel), rd, rs, rb, CU_TENSOR_MAP_SWIZZLE_NONE))
@@ -663,7 +671,10 @@ static int relattn_prefill_io(const void* q, const void* k, const void* v, const
   if (dims->max_q_len == 0 || dims->num_tokens == 0) return RELATTN_OK;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = launch_cache_write(L.p, s);
-  if (e == cudaSuccess) e = L.pair ? launch_prefill_pair(L, L.grid, s) : launch_prefill(L, L.grid, s);
+  if (e == cudaSuccess)
+    e = L.wide   ? launch_prefill_wide(L, L.grid, s)
+        : L.pair ? launch_prefill_pair(L, L.grid, s)
+                 : launch_prefill(L, L.grid, s);
   return to_status(e);
 }
 

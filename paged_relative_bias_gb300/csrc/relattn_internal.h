@@ -114,6 +114,7 @@ struct PrefillLaunch {
   PrefillParams p;
   int grid;
   int pair;  // 1: the two-heads-per-item kernel (bf16 caches), 0: one head per item
+  int wide;  // 1: one head per item over 128-key tiles (bf16 cache and rel, d_v = 128)
 };
 
 int decode_smem_bytes(int nstages, int B, int Bv, int kpc, int g, int dv, int rel_es, int kv_es);
@@ -144,5 +145,12 @@ cudaError_t launch_prefill_walk(const PrefillParams& p, int grid, cudaStream_t s
 int prefill_pair_slots(int B, int dv, int rel_es, int smem_optin);
 int prefill_pair_smem_bytes(int B, int dv, int rel_es, int nslots);
 cudaError_t launch_prefill_pair(const PrefillLaunch& L, int grid, cudaStream_t stream);
+// The bf16-cache, bf16-rel prefill (d_v = 128) with one head per work item and
+// 128-key tiles: ring slots (0 if fewer than it needs fit), shared memory,
+// launch (p.ring_stages = the slots; K/V maps with 128-row boxes, rel boxes of
+// 32 rows x 168 distances).
+int prefill_wide_slots(int B, int smem_optin);
+int prefill_wide_smem_bytes(int B, int nslots);
+cudaError_t launch_prefill_wide(const PrefillLaunch& L, int grid, cudaStream_t stream);
 
 }  // namespace relattn

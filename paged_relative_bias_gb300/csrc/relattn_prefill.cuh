@@ -217,5 +217,127 @@ __device__ __forceinline__ void scores_with_bias(float (&x)[64], const uint32_t 
   }
 }
 
+// bf16 rel boxes for 128-key tiles: 32 query rows x 168 distances.  A box
+// row needs the 128 distances P_r - j0 - 127 .. P_r - j0; across 32 rows that
+// is 159, plus up to 7 for rounding the box start down to 16 bytes.  A
+// 336-byte row is 84 words, so 8-byte reads of a warp spread over 16 banks.
+constexpr int kRelColsW = 168;
+constexpr int kRelBoxBytesW = kRelBoxRows * kRelColsW * 2;  // 10752 (84 x 128)
+
+// The scaled scores plus the sheared bias of one query row for half `half`
+// (keys 64 half .. 64 half + 63) of a 128-key tile whose rel boxes sit at
+// `slot`: row r of the tile, P0 the position of the tile's first row.  With
+// no distance of this half below rel_extent, pass has_rel = false.
+__device__ __forceinline__ void scores_with_bias_w(float (&x)[64], const uint32_t (&sr)[64],
+                                                   const uint8_t* slot, int r, int P0, int half,
+                                                   bool has_rel, float scale) {
+  const int rbox = r / kRelBoxRows, rrow = r % kRelBoxRows;
+  if (!has_rel) {
+#pragma unroll
+    for (int c = 0; c < 64; ++c) x[c] = __uint_as_float(sr[c]) * scale;
+    return;
+  }
+  // A box starts at distance (P0 + 32 box - j0 - 127) rounded down to 8, so
+  // the distance of this half's column 63 sits rrow + ((P0 + 1) & 7) + 64 (1 -
+  // half) into the row.
+  const int col = rrow + ((P0 + 1) & 7) + 64 * (1 - half);
+  const uint2* p2 = reinterpret_cast<const uint2*>(
+      reinterpret_cast<const __nv_bfloat16*>(slot + rbox * kRelBoxBytesW) + rrow * kRelColsW +
+      (col & ~3));
+  switch (col & 3) {  // rrow = 4 lane + q4 (mod 32): the same for the warp
+    case 0: rel_fma16<0>(x, sr, p2, scale); break;
+    case 1: rel_fma16<1>(x, sr, p2, scale); break;
+    case 2: rel_fma16<2>(x, sr, p2, scale); break;
+    default: rel_fma16<3>(x, sr, p2, scale); break;
+  }
+}
+
+// ---- paired fp32 arithmetic (sm_100 family) --------------------------------
+// Two fp32 lanes in one 64-bit register pair: one instruction does two FMAs
+// or adds, which halves the issue slots of the softmax.  (Scalar FFMA
+// streams on other warps slow the tensor pipe's MMAs; the paired form at the
+// same FLOP rate does not.)  Each lane rounds exactly as the scalar op does.
+__device__ __forceinline__ uint64_t f2(float lo, float hi) {
+  uint64_t d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2u(uint32_t lo, uint32_t hi) {
+  uint64_t d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "r"(lo), "r"(hi));
+  return d;
+}
+__device__ __forceinline__ float f2lo(uint64_t v) {
+  return __uint_as_float(static_cast<uint32_t>(v));
+}
+__device__ __forceinline__ float f2hi(uint64_t v) {
+  return __uint_as_float(static_cast<uint32_t>(v >> 32));
+}
+__device__ __forceinline__ uint64_t fma_f2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t add_f2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+// max of three (one instruction)
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// The pairs of rel_fma16: x2[i] = (x[2 i], x[2 i + 1]) = s * scale + rel for
+// columns 2 i and 2 i + 1, from 17 aligned 8-byte loads of four bf16
+// distances; p2 points A distances before the lowest needed one (column
+// 63's), distances rise towards column 0.
+template <int A>
+__device__ __forceinline__ void rel_fma16_x2(uint64_t (&x2)[32], const uint32_t (&sr)[64],
+                                             const uint2* p2, uint64_t scale2) {
+  uint32_t w[34];
+#pragma unroll
+  for (int k = 0; k < 17; ++k) {
+    const uint2 v = p2[k];
+    w[2 * k] = v.x;
+    w[2 * k + 1] = v.y;
+  }
+  // distance u (from the load's start) of column c is 63 - c + A: bf16 u
+  // sits in word u / 2, in its high half when u is odd
+  auto relf = [&](int c) -> uint32_t {
+    const int u = 63 - c + A;
+    return (u & 1) ? (w[u >> 1] & 0xffff0000u) : (w[u >> 1] << 16);
+  };
+#pragma unroll
+  for (int i = 0; i < 32; ++i)
+    x2[i] = fma_f2(f2u(sr[2 * i], sr[2 * i + 1]), scale2, f2u(relf(2 * i), relf(2 * i + 1)));
+}
+
+// scores_with_bias_w in pairs (see there).
+__device__ __forceinline__ void scores_with_bias_w2(uint64_t (&x2)[32], const uint32_t (&sr)[64],
+                                                    const uint8_t* slot, int r, int P0, int half,
+                                                    bool has_rel, float scale) {
+  const uint64_t scale2 = f2(scale, scale);
+  if (!has_rel) {
+    const uint64_t zero2 = f2(0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) x2[i] = fma_f2(f2u(sr[2 * i], sr[2 * i + 1]), scale2, zero2);
+    return;
+  }
+  const int rbox = r / kRelBoxRows, rrow = r % kRelBoxRows;
+  const int col = rrow + ((P0 + 1) & 7) + 64 * (1 - half);
+  const uint2* p2 = reinterpret_cast<const uint2*>(
+      reinterpret_cast<const __nv_bfloat16*>(slot + rbox * kRelBoxBytesW) + rrow * kRelColsW +
+      (col & ~3));
+  switch (col & 3) {  // the same for the warp
+    case 0: rel_fma16_x2<0>(x2, sr, p2, scale2); break;
+    case 1: rel_fma16_x2<1>(x2, sr, p2, scale2); break;
+    case 2: rel_fma16_x2<2>(x2, sr, p2, scale2); break;
+    default: rel_fma16_x2<3>(x2, sr, p2, scale2); break;
+  }
+}
+
 }  // namespace prefill
 }  // namespace relattn
