@@ -223,6 +223,7 @@ __global__ void __launch_bounds__(32 * (kPfWarps + (KV8 ? 1 : 0)), 1)
   uint8_t* smem = smem_align1024(smem_raw);
   static_assert(!KV8 || DV == 128, "e4m3 caches: d_v = 128");
   const int nrs = p.ring_stages;
+  const RingIndex ri(p.ring_stages);  // ring entry -> slot, phase
   const PrefillSmem L(p.B, DV, nrs, KV8 ? 1 : 2);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + L.misc);
@@ -369,8 +370,8 @@ __global__ void __launch_bounds__(32 * (kPfWarps + (KV8 ? 1 : 0)), 1)
     int e = 0;
     bool fail = false;
     auto acquire = [&](int entry) -> uint8_t* {
-      const int slot = entry % nrs;
-      if (!mbar_wait(&bars[kREmpty + slot], ((entry / nrs) & 1) ^ 1)) return nullptr;
+      const int slot = ri.slot(entry);
+      if (!mbar_wait(&bars[kREmpty + slot], ri.phase(entry) ^ 1)) return nullptr;
       return smem + L.ring + slot * kRingSlotBytes;
     };
     for (int idx = blockIdx.x; idx < total && !*s_abort && !fail; idx += gridDim.x) {
@@ -378,7 +379,7 @@ __global__ void __launch_bounds__(32 * (kPfWarps + (KV8 ? 1 : 0)), 1)
       prefill_item(idx, p, sa, it);
       uint8_t* qd = acquire(e);
       if (!qd) { fail = true; break; }
-      uint64_t* qbar = &bars[kRFull + e % nrs];
+      uint64_t* qbar = &bars[kRFull + ri.slot(e)];
       mbar_arrive_expect_tx(qbar, kQTileBytes);  // rows past T read as zeros
       tma_load_3d(qd, &tm_q, qbar, 0, it.h, it.r0);
       tma_load_3d(qd + kQTileBytes / 2, &tm_q, qbar, 64, it.h, it.r0);
@@ -387,7 +388,7 @@ __global__ void __launch_bounds__(32 * (kPfWarps + (KV8 ? 1 : 0)), 1)
         const int j0 = (it.tf + k) * kTileKeys;
         uint8_t* rd = acquire(e);
         if (!rd) { fail = true; break; }
-        uint64_t* rbar = &bars[kRFull + e % nrs];
+        uint64_t* rbar = &bars[kRFull + ri.slot(e)];
         if (it.P0 - j0 - (kTileKeys - 1) < p.rel_extent) {
           constexpr int kBox = R16 ? kRelBoxBytes16 : kRelBoxBytes;
           mbar_arrive_expect_tx(rbar, kRelBoxes * kBox);
@@ -401,7 +402,7 @@ __global__ void __launch_bounds__(32 * (kPfWarps + (KV8 ? 1 : 0)), 1)
       }
       if (fail) break;
       if (!acquire(e)) { fail = true; break; }
-      mbar_arrive(&bars[kRFull + e % nrs]);  // the O scratch slot
+      mbar_arrive(&bars[kRFull + ri.slot(e)]);  // the O scratch slot
       ++e;
     }
     if (fail) *s_abort = 1;
@@ -462,8 +463,8 @@ __global__ void __launch_bounds__(32 * (kPfWarps + (KV8 ? 1 : 0)), 1)
     int n = 0, e = 0, items = 0;  // key tiles and ring entries consumed
     bool fail = false;
     auto slot_wait = [&](int entry) -> uint8_t* {
-      const int slot = entry % nrs;
-      if (!mbar_wait(&bars[kRFull + slot], (entry / nrs) & 1)) return nullptr;
+      const int slot = ri.slot(entry);
+      if (!mbar_wait(&bars[kRFull + slot], ri.phase(entry))) return nullptr;
       return smem + L.ring + slot * kRingSlotBytes;
     };
     // This thread's query row, from a ring slot (128-byte swizzled rows) into
@@ -500,7 +501,7 @@ __global__ void __launch_bounds__(32 * (kPfWarps + (KV8 ? 1 : 0)), 1)
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(&bars[kQFull]);
-        mbar_arrive(&bars[kREmpty + entry % nrs]);
+        mbar_arrive(&bars[kREmpty + ri.slot(entry)]);
       }
     };
     for (int idx = blockIdx.x; idx < total && !*s_abort; idx += gridDim.x, ++items) {
@@ -560,7 +561,7 @@ __global__ void __launch_bounds__(32 * (kPfWarps + (KV8 ? 1 : 0)), 1)
         scores_with_bias<R16>(x, sr, slot, r, it.P0,
                               it.P0 - j0 - (kTileKeys - 1) < p.rel_extent, scale);
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bars[kREmpty + e % nrs]);
+        if (lane == 0) mbar_arrive(&bars[kREmpty + ri.slot(e)]);
         if (!warp_full) {
 #pragma unroll
           for (int c = 0; c < 64; ++c)
@@ -710,7 +711,7 @@ __global__ void __launch_bounds__(32 * (kPfWarps + (KV8 ? 1 : 0)), 1)
       }
       fence_proxy_async_smem();  // these writes come before the slot's next TMA fill
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[kREmpty + e % nrs]);
+      if (lane == 0) mbar_arrive(&bars[kREmpty + ri.slot(e)]);
       e += has_next ? 2 : 1;
     }
     if (fail) {

@@ -143,6 +143,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_align1024(smem_raw);
   const int nslots = p.ring_stages;
+  const RingIndex ri(p.ring_stages);  // ring entry -> slot, phase
   const PairSmem L(p.B, DV, R16 ? 2 : 4, nslots);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + L.misc);
@@ -230,8 +231,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     int e = 0;
     bool fail = false;
     auto acquire = [&](int entry) -> uint8_t* {
-      const int slot = entry % nslots;
-      if (!mbar_wait(&bars[kREmpty + slot], ((entry / nslots) & 1) ^ 1)) return nullptr;
+      const int slot = ri.slot(entry);
+      if (!mbar_wait(&bars[kREmpty + slot], ri.phase(entry) ^ 1)) return nullptr;
       return smem + L.ring + slot * L.slot;
     };
     for (int idx = blockIdx.x; idx < total && !*s_abort && !fail; idx += gridDim.x) {
@@ -239,7 +240,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < it.nh; ++i, ++e) {  // the query tile of each head
         uint8_t* qd = acquire(e);
         if (!qd) { fail = true; break; }
-        mbar_arrive(&bars[kRFull + e % nslots]);  // the slot's phase; the data lands on kQLoad
+        mbar_arrive(&bars[kRFull + ri.slot(e)]);  // the slot's phase; the data lands on kQLoad
         uint64_t* qbar = &bars[kQLoad + i];
         mbar_arrive_expect_tx(qbar, kQTileBytes);  // rows past T read as zeros
         tma_load_3d(qd, &tm_q, qbar, 0, it.h0 + i, it.r0);
@@ -251,7 +252,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < it.nh; ++i, ++e) {
           uint8_t* rd = acquire(e);
           if (!rd) { fail = true; break; }
-          uint64_t* rbar = &bars[kRFull + e % nslots];
+          uint64_t* rbar = &bars[kRFull + ri.slot(e)];
           if (has_rel) {
             constexpr int kBox = R16 ? kRelBoxBytes16 : kRelBoxBytes;
             mbar_arrive_expect_tx(rbar, kRelBoxes * kBox);
@@ -266,7 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       for (int i = 0; i < it.nh && !fail; ++i, ++e) {  // the O scratch of each head
         if (!acquire(e)) { fail = true; break; }
-        mbar_arrive(&bars[kRFull + e % nslots]);
+        mbar_arrive(&bars[kRFull + ri.slot(e)]);
       }
     }
     if (fail) *s_abort = 1;
@@ -348,11 +349,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto q_wait = [&](int entry) -> const uint8_t* {
       if (!mbar_wait(&bars[kQLoad + wg], nq & 1)) return nullptr;
       ++nq;
-      return smem + L.ring + (entry % nslots) * L.slot;
+      return smem + L.ring + ri.slot(entry) * L.slot;
     };
     auto slot_wait = [&](int entry) -> uint8_t* {
-      const int slot = entry % nslots;
-      if (!mbar_wait(&bars[kRFull + slot], (entry / nslots) & 1)) return nullptr;
+      const int slot = ri.slot(entry);
+      if (!mbar_wait(&bars[kRFull + slot], ri.phase(entry))) return nullptr;
       return smem + L.ring + slot * L.slot;
     };
     // This thread's query row, from a ring slot (128-byte swizzled rows) into
@@ -377,7 +378,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(&bars[kQFull + wg]);
-        mbar_arrive(&bars[kREmpty + entry % nslots]);
+        mbar_arrive(&bars[kREmpty + ri.slot(entry)]);
       }
     };
     // The first item from `idx` on in which this group has a head, with the
@@ -461,7 +462,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         scores_with_bias<R16>(x, sr, slot, r, it.P0,
                               it.P0 - j0 - (kTileKeys - 1) < p.rel_extent, scale);
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bars[kREmpty + e_rel % nslots]);
+        if (lane == 0) mbar_arrive(&bars[kREmpty + ri.slot(e_rel)]);
         if (!warp_full) {
 #pragma unroll
           for (int c = 0; c < 64; ++c)
@@ -604,7 +605,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       fence_proxy_async_smem();  // these writes come before the slot's next TMA fill
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[kREmpty + e_out % nslots]);
+      if (lane == 0) mbar_arrive(&bars[kREmpty + ri.slot(e_out)]);
       idx = nidx;
       e_base = nbase;
       it = nit;
