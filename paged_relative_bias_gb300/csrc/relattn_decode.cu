@@ -568,6 +568,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   uint8_t* smem = smem_align1024(smem_raw);
   const int g = p.g;
   const int ns = p.nstages;
+  const RingIndex ri(ns);  // stage n -> slot n % ns, phase (n / ns) & 1
   const Tok<MULTI> tok(p);
   using RelT = typename std::conditional<R16, __nv_bfloat16, float>::type;
   constexpr int RES = R16 ? 2 : 4;                // bytes per rel element
@@ -658,8 +659,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   // an e4m3 cache, whose tiles all fit in flight at once, the tests cost more
   // than the bytes saved.)
   auto issue_tile = [&](int nn, int tile, int id, const VSeq& sq, int kvh) -> int {
-    const int stage = nn % ns;
-    if (!mbar_wait(&empty[stage], ((nn / ns) & 1) ^ 1)) {
+    const int stage = ri.slot(nn);
+    if (!mbar_wait(&empty[stage], ri.phase(nn) ^ 1)) {
       report(p.status, RELATTN_DEV_WAIT_TIMEOUT);
       return 1;
     }
@@ -932,10 +933,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
 
     for (int t = RS ? 0 : ((n_base + grp) & 1 ? 1 : 0); t < pc.n && !abort; t += RS ? 1 : 2) {
       const int n = n_base + t;
-      const int stage = n % ns;
+      const int stage = ri.slot(n);
       const int tile = sq.tile_first + pc.i0 + t;
       const int key0 = tile * kTileKeys;
-      if (!mbar_wait(&full[stage], (n / ns) & 1)) {
+      if (!mbar_wait(&full[stage], ri.phase(n))) {
         report(p.status, RELATTN_DEV_WAIT_TIMEOUT);
         abort = true;
         break;

@@ -93,24 +93,6 @@ __device__ inline int prologue(const PrefillParams& p, SeqArrays a, bool zero_ba
   return a.qpref[p.B];
 }
 
-// Entry e of a ring of n slots: slot e mod n and phase (e / n) & 1, by a
-// multiply-high with the rounded-up reciprocal of n (exact for 0 <= e <
-// 2^32 / n).  A division by a run-time value would put hundreds of cycles on
-// the softmax warps' path at every ring wait.
-struct RingIndex {
-  uint32_t n, inv;
-  __device__ explicit RingIndex(int slots)
-      : n(static_cast<uint32_t>(slots)),
-        inv(static_cast<uint32_t>((0x100000000ull + slots - 1) / slots)) {}
-  __device__ __forceinline__ uint32_t quot(int e) const {
-    return __umulhi(static_cast<uint32_t>(e), inv);
-  }
-  __device__ __forceinline__ int slot(int e) const {
-    return static_cast<int>(static_cast<uint32_t>(e) - quot(e) * n);
-  }
-  __device__ __forceinline__ uint32_t phase(int e) const { return quot(e) & 1u; }
-};
-
 // Query tile qtg (0 .. tiles - 1): its sequence, first packed row, valid rows,
 // position of its first row, and its window-aware range of 64-key tiles
 // [tf, tf + ntiles): the tiles holding a key that one of its rows sees.
