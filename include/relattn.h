@@ -462,6 +462,24 @@ int relattn_debug_walk_prefill(const int32_t* cu_seqlens,
                                void* stream);
 
 /*
+ * Test hook: relattn_debug_walk_prefill for the kernel that relattn_prefill_ex
+ * runs with these options (options->rel and options->kv decide; the other
+ * fields are not used; options may be NULL for the defaults): over a bf16
+ * cache with a bf16 rel and d_v = 128, the kernel whose work items are a
+ * 128-row query tile and ONE query head over 128-key tiles, whose records
+ * are { sequence, first_row_of_query_tile, key_tile, logical_block,
+ * physical_block, head } with key_tile counting 128-key tiles (it equals
+ * logical_block); otherwise the two-heads kernel's records as above.  e4m3
+ * caches: RELATTN_ERR_UNSUPPORTED.
+ */
+int relattn_debug_walk_prefill_ex(const int32_t* cu_seqlens, const int32_t* ctx_lens,
+                                  const int32_t* block_table, int32_t window,
+                                  const relattn_options* options,
+                                  const relattn_kv_cache* cache, const relattn_dims* dims,
+                                  int32_t* records, int32_t max_records, int32_t* count,
+                                  void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Test hook for failure detection: one thread waits on a shared-memory
  * barrier that nothing completes.  Every wait in the library's kernels has a
  * limit (about 2 s) after which it gives up, records

@@ -613,7 +613,7 @@ static int prepare_prefill(const void* q, const void* k, const void* v, const vo
   const bool one_wave = !walk && dims->num_ctas == 0 && one_head_items <= di.sms;
   // bf16 cache and bf16 rel with d_v = 128: one head per item over 128-key
   // tiles (the tensor pipe at N = 128) when its ring fits
-  const int wide_slots = io.kv_es == 2 && io.rel_es == 2 && p.dv == 128 && !one_wave && !walk
+  const int wide_slots = io.kv_es == 2 && io.rel_es == 2 && p.dv == 128 && !one_wave
                              ? prefill_wide_slots(p.B, di.smem_optin)
                              : 0;
   L->wide = wide_slots > 0 ? 1 : 0;
@@ -654,6 +654,19 @@ static int prepare_prefill(const void* q, const void* k, const void* v, const vo
                 io.rel_es == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
                 3, const_cast<void*>(rel), rd, rs, rb, CU_TENSOR_MAP_SWIZZLE_NONE))
     return RELATTN_ERR_CUDA;
+  if (L->wide) {
+    // out [T][Hq][128], bf16 or fp32: a full tile's 128 rows of one head as
+    // 128-byte column boxes (64 bf16 or 32 fp32), 128-byte swizzled
+    const cuuint64_t oes = io.out_f32 ? 4 : 2;
+    const cuuint64_t od[3] = {128, static_cast<cuuint64_t>(dims->num_q_heads),
+                              static_cast<cuuint64_t>(dims->num_tokens)};
+    const cuuint64_t os[2] = {128 * oes, static_cast<cuuint64_t>(dims->num_q_heads) * 128 * oes};
+    const cuuint32_t ob[3] = {static_cast<cuuint32_t>(128 / oes), 1, 128};
+    if (!make_map(&L->tm_out,
+                  io.out_f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                  3, out, od, os, ob, CU_TENSOR_MAP_SWIZZLE_128B))
+      return RELATTN_ERR_CUDA;
+  }
   return RELATTN_OK;
 }
 
@@ -773,6 +786,30 @@ int relattn_debug_walk_prefill(const int32_t* cu_seqlens, const int32_t* ctx_len
   L.p.dbg_count = count;
   L.p.dbg_max = max_records;
   return to_status(launch_prefill_walk(L.p, L.grid, static_cast<cudaStream_t>(stream)));
+}
+
+int relattn_debug_walk_prefill_ex(const int32_t* cu_seqlens, const int32_t* ctx_lens,
+                                  const int32_t* block_table, int32_t window,
+                                  const relattn_options* options, const relattn_kv_cache* cache,
+                                  const relattn_dims* dims, int32_t* records,
+                                  int32_t max_records, int32_t* count, void* workspace,
+                                  size_t workspace_bytes, void* stream) {
+  if (!records || !count || max_records < 0) return RELATTN_ERR_INVALID_ARG;
+  IoTypes io = kDefaultIo;
+  if (options != nullptr && !io_types(options, &io)) return RELATTN_ERR_INVALID_ARG;
+  if (io.kv_es != 2) return RELATTN_ERR_UNSUPPORTED;  // bf16 caches: the kernels with a walk
+  PrefillLaunch L;
+  const int rc = prepare_prefill(nullptr, nullptr, nullptr, nullptr, io, cu_seqlens, cache,
+                                 block_table, ctx_lens, window, 16, dims, nullptr, workspace,
+                                 workspace_bytes, true, &L);
+  if (rc != RELATTN_OK) return rc;
+  if (dims->max_q_len == 0) return RELATTN_OK;
+  L.p.dbg_records = records;
+  L.p.dbg_count = count;
+  L.p.dbg_max = max_records;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return to_status(L.wide ? launch_prefill_wide_walk(L.p, L.grid, s)
+                          : launch_prefill_walk(L.p, L.grid, s));
 }
 
 }  // extern "C"

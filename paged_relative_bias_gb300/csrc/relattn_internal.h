@@ -111,6 +111,7 @@ struct PrefillParams {
 
 struct PrefillLaunch {
   CUtensorMap tm_q, tm_k, tm_v, tm_rel;
+  CUtensorMap tm_out;  // out as [T][Hq][d_v] boxes of 128 B x 128 rows (the 128-key-tile kernel)
   PrefillParams p;
   int grid;
   int pair;  // 1: the two-heads-per-item kernel (bf16 caches), 0: one head per item
@@ -152,5 +153,7 @@ cudaError_t launch_prefill_pair(const PrefillLaunch& L, int grid, cudaStream_t s
 int prefill_wide_slots(int B, int smem_optin);
 int prefill_wide_smem_bytes(int B, int nslots);
 cudaError_t launch_prefill_wide(const PrefillLaunch& L, int grid, cudaStream_t stream);
+// Replay of that kernel's work split and block walk on its grid.
+cudaError_t launch_prefill_wide_walk(const PrefillParams& p, int grid, cudaStream_t stream);
 
 }  // namespace relattn

@@ -99,6 +99,27 @@ struct WideSmem {
   }
 };
 
+// out[j] = in[(j + rot) & 7] for 8 chunks of 4 words (rot 0 .. 7), by three
+// conditional rotations.  A lane that reads or writes a 128-byte-swizzled
+// row's chunks starting at chunk lane & 7 spreads the 8 lanes of each
+// quarter-warp (rows 4 apart here) over all 8 bank groups; this puts the
+// chunks back in order (or into that order).
+__device__ __forceinline__ void rotate_chunks(uint32_t (&w)[32], int rot) {
+#pragma unroll
+  for (int b = 1; b < 8; b <<= 1) {
+    const bool on = (rot & b) != 0;
+    uint32_t t[32];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) t[4 * j + e] = on ? w[4 * ((j + b) & 7) + e] : w[4 * j + e];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) w[i] = t[i];
+  }
+}
+
+constexpr int kOutBoxBytes = 128 * 128;  // one 128-byte column box of 128 rows
+
 // Work item idx: query tile idx / Hq, head idx % Hq, so that the heads of one
 // query tile run on neighbouring CTAs.  Key tiles are 128-token blocks:
 // [tf, tf + ntiles) are the blocks holding a key that a row of the tile sees.
@@ -139,7 +160,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefill_wide_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v,
-                        const __grid_constant__ CUtensorMap tm_rel, const PrefillParams p) {
+                        const __grid_constant__ CUtensorMap tm_rel,
+                        const __grid_constant__ CUtensorMap tm_out, const PrefillParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_align1024(smem_raw);
   constexpr int nslots = NS;
@@ -175,6 +197,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
     tma_prefetch_desc(&tm_rel);
+    tma_prefetch_desc(&tm_out);
   }
   // K/V stages start as zeros: a tile whose block id is invalid is never
   // loaded, and its P is zero, so its operands must at least be finite.
@@ -383,15 +406,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     // This thread's half of its query row (dims 64 g .. 64 g + 63), from the
     // ring slot (128-byte swizzled rows) into TMEM, the A operand of S = Q K^T.
     auto load_q = [&](const uint8_t* qs, int entry) {
+      // chunk (s + rot) & 7 at step s (conflict-free, see rotate_chunks)
+      const int rot = lane & 7;
       uint32_t qr[32];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const uint4 v = *reinterpret_cast<const uint4*>(qs + g * (kQTileBytes / 2) + sw128(r, j));
-        qr[4 * j] = v.x;
-        qr[4 * j + 1] = v.y;
-        qr[4 * j + 2] = v.z;
-        qr[4 * j + 3] = v.w;
+      for (int s2 = 0; s2 < 8; ++s2) {
+        const uint4 v = *reinterpret_cast<const uint4*>(qs + g * (kQTileBytes / 2) +
+                                                        sw128(r, (s2 + rot) & 7));
+        qr[4 * s2] = v.x;
+        qr[4 * s2 + 1] = v.y;
+        qr[4 * s2 + 2] = v.z;
+        qr[4 * s2 + 3] = v.w;
       }
+      rotate_chunks(qr, (8 - rot) & 7);  // back to chunk order
       tmem_st32(tl + kColQ + 32 * g, qr);
       tmem_wait_st();
       tc_fence_before();
@@ -561,71 +588,124 @@ __global__ void __launch_bounds__(kThreads, 1)
         inv = den > 0.f ? 1.f / den : 0.f;
         if (p.gate != nullptr && row_ok) inv /= 1.f + ex2(-__ldg(p.gate + qi) * kLog2e);
       }
-      // O / l -> out, through the scratch slot (the tile's 128 rows of 256
-      // bytes, 16-byte chunks swizzled by row / 4) so that the global stores
-      // are whole rows (16 lanes per row).  A bf16 row is 256 bytes; an fp32
-      // row is twice that and goes in two passes of 64 columns.  Group g
-      // fills chunks [8 g, 8 g + 8) of every row of a pass.
-      constexpr int passes = O32 ? 2 : 1;
+      if (it.rows == kQRows) {
+        // A full tile: O / l goes into the scratch slot as 128-byte column
+        // boxes of 128 rows (the tensor map's 128-byte swizzle), which one
+        // thread stores with the tensor unit.  Group g fills box g (bf16; an
+        // fp32 row is twice as long and goes in two passes, box 2 pass + g
+        // of each).  Each lane writes its 16-byte chunks starting at chunk
+        // lane & 7, so the 8 lanes of a quarter-warp, whose rows are 4
+        // apart, hit 8 different bank groups.
+        const int rot = lane & 7;
+        constexpr int passes = O32 ? 2 : 1;
 #pragma unroll
-      for (int half = 0; half < passes; ++half) {
-        if (half > 0) named_barrier(kXchgBar, 256);  // the first pass's stores have read the scratch
-        if constexpr (O32) {
-          uint32_t o[32];
-          tmem_ld32(tl + kColO + 64 * half + 32 * g, o);
-          tmem_wait_ld();
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            uint4 w;
-            w.x = __float_as_uint(__uint_as_float(o[4 * i]) * inv);
-            w.y = __float_as_uint(__uint_as_float(o[4 * i + 1]) * inv);
-            w.z = __float_as_uint(__uint_as_float(o[4 * i + 2]) * inv);
-            w.w = __float_as_uint(__uint_as_float(o[4 * i + 3]) * inv);
-            const int j = 8 * g + i;
-            *reinterpret_cast<uint4*>(scr + r * 256 + ((j ^ ((r >> 2) & 7)) << 4)) = w;
-          }
-        } else {
-#pragma unroll
-          for (int c0 = 0; c0 < 64; c0 += 32) {
-            uint32_t o[32];
-            tmem_ld32(tl + kColO + 64 * g + c0, o);
+        for (int pass = 0; pass < passes; ++pass) {
+          uint32_t w[32];
+          if constexpr (O32) {
+            tmem_ld32(tl + kColO + 64 * pass + 32 * g, w);
             tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
+            for (int i2 = 0; i2 < 32; ++i2) w[i2] = __float_as_uint(__uint_as_float(w[i2]) * inv);
+          } else {
+#pragma unroll
+            for (int c0 = 0; c0 < 64; c0 += 32) {
+              uint32_t o[32];
+              tmem_ld32(tl + kColO + 64 * g + c0, o);
+              tmem_wait_ld();
+#pragma unroll
+              for (int i2 = 0; i2 < 16; ++i2)
+                w[c0 / 2 + i2] =
+                    pack_bf16(__uint_as_float(o[2 * i2]) * inv, __uint_as_float(o[2 * i2 + 1]) * inv);
+            }
+          }
+          if (pass == passes - 1) tc_fence_before();  // O is read before the next item's P V
+          rotate_chunks(w, rot);  // chunk (s + rot) & 7 at position s
+          uint8_t* box = scr + g * kOutBoxBytes;
+#pragma unroll
+          for (int s2 = 0; s2 < 8; ++s2)
+            *reinterpret_cast<uint4*>(box + sw128(r, (s2 + rot) & 7)) =
+                make_uint4(w[4 * s2], w[4 * s2 + 1], w[4 * s2 + 2], w[4 * s2 + 3]);
+          fence_proxy_async_smem();  // the boxes are read by the tensor unit
+          named_barrier(kXchgBar, 256);
+          if (warp == 0 && lane == 0) {
+#pragma unroll
+            for (int bx = 0; bx < 2; ++bx)
+              tma_store_3d(&tm_out, scr + bx * kOutBoxBytes, (2 * pass + bx) * (O32 ? 32 : 64),
+                           it.h, it.r0);
+            tma_store_commit();
+            tma_store_wait_read();  // the scratch may be written again
+            if (pass == passes - 1) mbar_arrive_n(&bars[kREmpty + e_out % nslots], 8);
+          }
+          __syncwarp();
+          if (pass < passes - 1) named_barrier(kXchgBar, 256);
+        }
+      } else {
+        // O / l -> out, through the scratch slot (the tile's 128 rows of 256
+        // bytes, 16-byte chunks swizzled by row / 4) so that the global stores
+        // are whole rows (16 lanes per row).  A bf16 row is 256 bytes; an fp32
+        // row is twice that and goes in two passes of 64 columns.  Group g
+        // fills chunks [8 g, 8 g + 8) of every row of a pass.
+        constexpr int passes = O32 ? 2 : 1;
+#pragma unroll
+        for (int half = 0; half < passes; ++half) {
+          if (half > 0) named_barrier(kXchgBar, 256);  // the first pass's stores have read the scratch
+          if constexpr (O32) {
+            uint32_t o[32];
+            tmem_ld32(tl + kColO + 64 * half + 32 * g, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
               uint4 w;
-              w.x = pack_bf16(__uint_as_float(o[8 * i]) * inv, __uint_as_float(o[8 * i + 1]) * inv);
-              w.y = pack_bf16(__uint_as_float(o[8 * i + 2]) * inv,
-                              __uint_as_float(o[8 * i + 3]) * inv);
-              w.z = pack_bf16(__uint_as_float(o[8 * i + 4]) * inv,
-                              __uint_as_float(o[8 * i + 5]) * inv);
-              w.w = pack_bf16(__uint_as_float(o[8 * i + 6]) * inv,
-                              __uint_as_float(o[8 * i + 7]) * inv);
-              const int j = 8 * g + c0 / 8 + i;
+              w.x = __float_as_uint(__uint_as_float(o[4 * i]) * inv);
+              w.y = __float_as_uint(__uint_as_float(o[4 * i + 1]) * inv);
+              w.z = __float_as_uint(__uint_as_float(o[4 * i + 2]) * inv);
+              w.w = __float_as_uint(__uint_as_float(o[4 * i + 3]) * inv);
+              const int j = 8 * g + i;
               *reinterpret_cast<uint4*>(scr + r * 256 + ((j ^ ((r >> 2) & 7)) << 4)) = w;
+            }
+          } else {
+#pragma unroll
+            for (int c0 = 0; c0 < 64; c0 += 32) {
+              uint32_t o[32];
+              tmem_ld32(tl + kColO + 64 * g + c0, o);
+              tmem_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                uint4 w;
+                w.x = pack_bf16(__uint_as_float(o[8 * i]) * inv, __uint_as_float(o[8 * i + 1]) * inv);
+                w.y = pack_bf16(__uint_as_float(o[8 * i + 2]) * inv,
+                                __uint_as_float(o[8 * i + 3]) * inv);
+                w.z = pack_bf16(__uint_as_float(o[8 * i + 4]) * inv,
+                                __uint_as_float(o[8 * i + 5]) * inv);
+                w.w = pack_bf16(__uint_as_float(o[8 * i + 6]) * inv,
+                                __uint_as_float(o[8 * i + 7]) * inv);
+                const int j = 8 * g + c0 / 8 + i;
+                *reinterpret_cast<uint4*>(scr + r * 256 + ((j ^ ((r >> 2) & 7)) << 4)) = w;
+              }
+            }
+          }
+          // O is read before the next item's first P V overwrites it
+          if (half == passes - 1) tc_fence_before();
+          named_barrier(kXchgBar, 256);  // every row is in the scratch
+          // whole-row stores: warp w takes rows [16 w, 16 w + 16), two per pass
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int rr = 16 * warp + 2 * i + (lane >> 4);
+            const int ch = lane & 15;
+            const uint4 v =
+                *reinterpret_cast<const uint4*>(scr + rr * 256 + ((ch ^ ((rr >> 2) & 7)) << 4));
+            if (rr < it.rows) {
+              const size_t orow = (static_cast<size_t>(it.r0 + rr) * p.Hq + it.h) * kDv;
+              if constexpr (O32)
+                *reinterpret_cast<uint4*>(static_cast<float*>(p.out) + orow + 64 * half + ch * 4) = v;
+              else
+                *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + orow + ch * 8) = v;
             }
           }
         }
-        // O is read before the next item's first P V overwrites it
-        if (half == passes - 1) tc_fence_before();
-        named_barrier(kXchgBar, 256);  // every row is in the scratch
-        // whole-row stores: warp w takes rows [16 w, 16 w + 16), two per pass
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int rr = 16 * warp + 2 * i + (lane >> 4);
-          const int ch = lane & 15;
-          const uint4 v =
-              *reinterpret_cast<const uint4*>(scr + rr * 256 + ((ch ^ ((rr >> 2) & 7)) << 4));
-          if (rr < it.rows) {
-            const size_t orow = (static_cast<size_t>(it.r0 + rr) * p.Hq + it.h) * kDv;
-            if constexpr (O32)
-              *reinterpret_cast<uint4*>(static_cast<float*>(p.out) + orow + 64 * half + ch * 4) = v;
-            else
-              *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + orow + ch * 8) = v;
-          }
-        }
+        fence_proxy_async_smem();  // these writes come before the slot's next TMA fill
+        slot_free(e_out);
       }
-      fence_proxy_async_smem();  // these writes come before the slot's next TMA fill
-      slot_free(e_out);
       idx = nidx;
       e_base = e_out + 1;
       if (has_next) it = wide_item(idx, p, sa);
@@ -636,6 +716,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       *s_abort = 1;
     }
   }
+  if (tid == 0) tma_store_wait_all();  // the O stores this thread issued are done
   if (*s_abort && tid == 0) report(p.status, RELATTN_DEV_WAIT_TIMEOUT);
   __syncwarp();  // lanes idle while lane 0 produced/issued rejoin here
   tc_fence_before();
@@ -644,7 +725,44 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kMmaWarp) tmem_dealloc(tbase, kTmemCols);
 }
 
+// Replays the work split and block walk of prefill_wide_kernel with the same
+// device functions (prologue, wide_item) and the same grid: each (item, key
+// tile) appends { sequence, first row of its query tile within the sequence,
+// key tile (a 128-key tile: the logical block), logical block, physical
+// block, head }.
+__global__ void __launch_bounds__(128) prefill_wide_walk_kernel(const PrefillParams p) {
+  extern __shared__ int seq_arrays[];  // 4 B + 1 ints
+  const SeqArrays sa{seq_arrays, seq_arrays + p.B, seq_arrays + 2 * p.B, seq_arrays + 3 * p.B};
+  const int total = prologue(p, sa, false) * p.Hq;
+  if (threadIdx.x != 0) return;
+  for (int idx = blockIdx.x; idx < total; idx += gridDim.x) {
+    const WideItem it = wide_item(idx, p, sa);
+    const int* trow = p.block_table + static_cast<size_t>(it.b) * p.max_blocks;
+    for (int k = 0; k < it.ntiles; ++k) {
+      const int tile = it.tf + k;
+      const int r = atomicAdd(p.dbg_count, 1);
+      if (r < p.dbg_max) {
+        int32_t* rec = p.dbg_records + 6 * static_cast<size_t>(r);
+        rec[0] = it.b;
+        rec[1] = it.r0 - sa.cu0[it.b];
+        rec[2] = tile;
+        rec[3] = tile;
+        rec[4] = __ldg(trow + tile);
+        rec[5] = it.h;
+      }
+    }
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_prefill_wide_walk(const PrefillParams& p, int grid, cudaStream_t stream) {
+  const int smem = (4 * p.B + 1) * 4;
+  cudaError_t e = ensure_smem<prefill_wide_walk_kernel>(smem);
+  if (e != cudaSuccess) return e;
+  prefill_wide_walk_kernel<<<grid, 128, smem, stream>>>(p);
+  return cudaGetLastError();
+}
 
 int prefill_wide_smem_bytes(int B, int nslots) { return WideSmem(B, nslots).total + 1024; }
 
@@ -667,7 +785,7 @@ static cudaError_t launch_wide_as(const PrefillLaunch& L, int grid, int smem, cu
   cudaError_t e = ensure_smem<prefill_wide_kernel<O32, NS>>(smem);
   if (e != cudaSuccess) return e;
   prefill_wide_kernel<O32, NS><<<grid, kThreads, smem, stream>>>(L.tm_q, L.tm_k, L.tm_v,
-                                                                 L.tm_rel, L.p);
+                                                                 L.tm_rel, L.tm_out, L.p);
   return cudaGetLastError();
 }
 

@@ -45,6 +45,7 @@ EXPORTS = (
     "relattn_debug_wait_timeout",
     "relattn_debug_decode_give_up",
     "relattn_debug_walk_decode_ex",
+    "relattn_debug_walk_prefill_ex",
 )
 
 DTYPE_F32 = 0
@@ -119,6 +120,10 @@ def lib() -> ctypes.CDLL:
                                              c_void_p, c_int32, c_void_p, c_void_p,
                                              c_size_t, c_void_p]
     L.relattn_debug_walk_prefill.restype = c_int
+    L.relattn_debug_walk_prefill_ex.argtypes = [c_void_p, c_void_p, c_void_p, c_int32,
+                                                POINTER(Options), P, S, c_void_p, c_int32,
+                                                c_void_p, c_void_p, c_size_t, c_void_p]
+    L.relattn_debug_walk_prefill_ex.restype = c_int
     L.relattn_decode_noalloc.argtypes = [c_void_p, c_void_p, P, c_void_p, c_void_p, c_int32,
                                          c_int32, S, c_void_p, c_void_p]
     L.relattn_decode_noalloc.restype = c_int
@@ -586,8 +591,13 @@ def debug_walk_decode_ex(block_table, seq_lens, num_query_tokens: int, window: i
 
 
 def debug_walk_prefill(cu_seqlens, ctx_lens, block_table, window: int, k_cache, v_cache,
-                       num_q_heads: int, max_q_len: int, max_records: int = 1 << 20):
-    """Replay of the prefill kernel's block walk: int32 [n, 6] records."""
+                       num_q_heads: int, max_q_len: int, max_records: int = 1 << 20,
+                       rel_dtype=None):
+    """Replay of the prefill kernel's block walk: int32 [n, 6] records.
+
+    rel_dtype None: the two-heads kernel (relattn_debug_walk_prefill); else
+    the kernel relattn_prefill runs for a rel of that dtype
+    (relattn_debug_walk_prefill_ex)."""
     dev = block_table.device
     cache = cache_desc(k_cache, v_cache)
     num_tokens = int(cu_seqlens[-1].item())  # test hook: a host read is fine here
@@ -596,11 +606,19 @@ def debug_walk_prefill(cu_seqlens, ctx_lens, block_table, window: int, k_cache, 
     ws = new_workspace(workspace_size(dims, cache), dev)
     rec = torch.zeros((max_records, 6), dtype=torch.int32, device=dev)
     cnt = torch.zeros(1, dtype=torch.int32, device=dev)
-    _check(lib().relattn_debug_walk_prefill(
-        cu_seqlens.data_ptr(), ctx_lens.data_ptr(), block_table.data_ptr(), int(window),
-        ctypes.byref(cache), ctypes.byref(dims), rec.data_ptr(), max_records,
-        cnt.data_ptr(), ws.data_ptr(), ws.numel(), _stream(dev)),
-        "relattn_debug_walk_prefill")
+    if rel_dtype is None:
+        _check(lib().relattn_debug_walk_prefill(
+            cu_seqlens.data_ptr(), ctx_lens.data_ptr(), block_table.data_ptr(), int(window),
+            ctypes.byref(cache), ctypes.byref(dims), rec.data_ptr(), max_records,
+            cnt.data_ptr(), ws.data_ptr(), ws.numel(), _stream(dev)),
+            "relattn_debug_walk_prefill")
+    else:
+        opts = Options(_DTYPE_CODE[rel_dtype], DTYPE_BF16, None, None, DTYPE_BF16, 1.0, 1.0, None)
+        _check(lib().relattn_debug_walk_prefill_ex(
+            cu_seqlens.data_ptr(), ctx_lens.data_ptr(), block_table.data_ptr(), int(window),
+            ctypes.byref(opts), ctypes.byref(cache), ctypes.byref(dims), rec.data_ptr(),
+            max_records, cnt.data_ptr(), ws.data_ptr(), ws.numel(), _stream(dev)),
+            "relattn_debug_walk_prefill_ex")
     n = int(cnt.item())
     if n > max_records:
         raise RuntimeError("walk produced more records than the buffer holds")

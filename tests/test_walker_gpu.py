@@ -12,6 +12,7 @@ from collections import defaultdict
 
 import numpy as np
 import pytest
+import torch
 
 from oracle import relattn_oracle as O
 from paged_relative_bias_gb300 import inputs as I
@@ -111,6 +112,36 @@ def test_prefill_walk_bit_exact(window, heads):
             want = [(t, t // 2, blocks[t // 2]) for t in range(lo // 64, (ctx + t1) // 64 + 1)]
             for h0 in firsts:
                 assert sorted(got.pop((b, t0, h0))) == want
+    assert not got
+
+
+@pytest.mark.parametrize("heads", [(4, 1), (6, 2), (3, 1), (2, 2)])
+@pytest.mark.parametrize("window", [0, 1, 100, 1024])
+def test_prefill_walk_wide_bit_exact(window, heads):
+    """With a bf16 rel (d_v = 128, bf16 cache) the prefill's work items are one
+    128-row query tile and one head over 128-key tiles: every item visits
+    exactly the blocks holding a key that one of its rows sees, the oracle's
+    block walk, and the items cover every (query tile, head) once."""
+    hq, hkv = heads
+    wl = I.PrefillWorkload("pww", hq, hkv, 128, 128, window, 64, (1, 64, 65, 300, 200),
+                           (0, 63, 128, 1000, 5))
+    case = I.make_prefill(wl, DEV)
+    rec, status = R.debug_walk_prefill(case["cu_seqlens"], case["ctx_lens"],
+                                       case["block_table"], window, case["k_cache"],
+                                       case["v_cache"], hq, case["max_q_len"],
+                                       rel_dtype=torch.bfloat16)
+    assert status == 0
+    table = case["block_table"].cpu().numpy()
+    got = defaultdict(list)
+    for b, t0, tile, lblk, phys, h in rec.tolist():
+        got[(b, t0, h)].append((tile, lblk, phys))
+    for b, (n, ctx) in enumerate(zip(wl.new_tokens, wl.ctx_lens)):
+        for t0 in range(0, n, 128):
+            t1 = min(n, t0 + 128) - 1
+            blocks = dict(O.prefill_blocks(ctx, t0, t1, window, table[b]))
+            want = [(lb, lb, blocks[lb]) for lb in sorted(blocks)]
+            for h in range(hq):
+                assert sorted(got.pop((b, t0, h))) == want
     assert not got
 
 
