@@ -248,9 +248,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     // --------------------------------------------------- ring producer
     int e = 0;
     bool fail = false;
+    // A bf16 full tile's O scratch, once the softmax warps have written it and
+    // released its slot, leaves through the tensor unit from this thread: when
+    // the slot is next acquired, or at the end.  pend_e[slot] is that entry
+    // (-1: none), pend_h / pend_r0 its head and first row.
+    int pend_e[nslots], pend_h[nslots], pend_r0[nslots];
+#pragma unroll
+    for (int i = 0; i < nslots; ++i) pend_e[i] = pend_h[i] = pend_r0[i] = 0, pend_e[i] = -1;
+    auto store_out = [&](int slot) {
+      const uint8_t* src = smem + L.ring + slot * kSlotBytes;
+      tma_store_3d(&tm_out, src, 0, pend_h[slot], pend_r0[slot]);
+      tma_store_3d(&tm_out, src + kOutBoxBytes, 64, pend_h[slot], pend_r0[slot]);
+      tma_store_commit();
+      tma_store_wait_read();  // the slot may be filled again
+      pend_e[slot] = -1;
+    };
     auto acquire = [&](int entry) -> uint8_t* {
       const int slot = entry % nslots;
       if (!mbar_wait(&bars[kREmpty + slot], ((entry / nslots) & 1) ^ 1)) return nullptr;
+#pragma unroll
+      for (int i = 0; i < nslots; ++i)  // (registers: no run-time index)
+        if (i == slot && pend_e[i] >= 0) store_out(i);
       return smem + L.ring + slot * kSlotBytes;
     };
     for (int idx = blockIdx.x; idx < total && !*s_abort && !fail; idx += gridDim.x) {
@@ -282,9 +300,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (fail) break;
       if (!acquire(e)) { fail = true; break; }  // the O scratch
+      if (!O32 && it.rows == kQRows) {
+#pragma unroll
+        for (int i = 0; i < nslots; ++i)
+          if (i == e % nslots) {
+            pend_e[i] = e;
+            pend_h[i] = it.h;
+            pend_r0[i] = it.r0;
+          }
+      }
       mbar_arrive(&bars[kRFull + e % nslots]);
       ++e;
     }
+    // the scratch tiles not yet stored: once their slot is released
+#pragma unroll
+    for (int i = 0; i < nslots; ++i) {
+      if (pend_e[i] < 0 || fail || *s_abort) continue;
+      if (mbar_wait(&bars[kREmpty + i], (pend_e[i] / nslots) & 1))
+        store_out(i);
+      else
+        fail = true;
+    }
+    tma_store_wait_all();  // the O stores of this thread are done
     if (fail) *s_abort = 1;
   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------- MMA issuer
@@ -590,8 +627,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (it.rows == kQRows) {
         // A full tile: O / l goes into the scratch slot as 128-byte column
-        // boxes of 128 rows (the tensor map's 128-byte swizzle), which one
-        // thread stores with the tensor unit.  Group g fills box g (bf16; an
+        // boxes of 128 rows (the tensor map's 128-byte swizzle), stored with
+        // the tensor unit by the ring producer once the 8 warps released the
+        // slot (bf16), or by one softmax thread (fp32).  Group g fills box g (bf16; an
         // fp32 row is twice as long and goes in two passes, box 2 pass + g
         // of each).  Each lane writes its 16-byte chunks starting at chunk
         // lane & 7, so the 8 lanes of a quarter-warp, whose rows are 4
@@ -626,18 +664,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             *reinterpret_cast<uint4*>(box + sw128(r, (s2 + rot) & 7)) =
                 make_uint4(w[4 * s2], w[4 * s2 + 1], w[4 * s2 + 2], w[4 * s2 + 3]);
           fence_proxy_async_smem();  // the boxes are read by the tensor unit
-          named_barrier(kXchgBar, 256);
-          if (warp == 0 && lane == 0) {
+          if constexpr (!O32) {
+            // the ring producer stores the tile once all 8 warps released it
+            slot_free(e_out);
+          } else {
+            named_barrier(kXchgBar, 256);
+            if (warp == 0 && lane == 0) {
 #pragma unroll
-            for (int bx = 0; bx < 2; ++bx)
-              tma_store_3d(&tm_out, scr + bx * kOutBoxBytes, (2 * pass + bx) * (O32 ? 32 : 64),
-                           it.h, it.r0);
-            tma_store_commit();
-            tma_store_wait_read();  // the scratch may be written again
-            if (pass == passes - 1) mbar_arrive_n(&bars[kREmpty + e_out % nslots], 8);
+              for (int bx = 0; bx < 2; ++bx)
+                tma_store_3d(&tm_out, scr + bx * kOutBoxBytes, (2 * pass + bx) * 32, it.h,
+                             it.r0);
+              tma_store_commit();
+              tma_store_wait_read();  // the scratch may be written again
+              if (pass == passes - 1) mbar_arrive_n(&bars[kREmpty + e_out % nslots], 8);
+            }
+            __syncwarp();
+            if (pass < passes - 1) named_barrier(kXchgBar, 256);
           }
-          __syncwarp();
-          if (pass < passes - 1) named_barrier(kXchgBar, 256);
         }
       } else {
         // O / l -> out, through the scratch slot (the tile's 128 rows of 256

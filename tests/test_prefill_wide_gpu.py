@@ -137,3 +137,16 @@ def test_wide_matches_two_heads_kernel_on_fp32_rel_values():
     pair = run(dict(case, rel=case["rel"].float()), 148)
     d = (wide.float() - pair.float()).abs().max().item()
     assert d <= 2e-2
+
+
+def test_wide_prefill_two_ring_slots_many_sequences():
+    """With 60 sequences the per-sequence arrays leave room for two ring slots
+    instead of three: 60 sequences of ragged lengths (partial and full query
+    tiles) run that instantiation, on a forced grid and on 7 CTAs."""
+    rng = np.random.default_rng(77)
+    new = tuple(int(x) for x in rng.integers(100, 300, size=60))
+    ctx = tuple(int(x) for x in rng.integers(0, 400, size=60))
+    wl = I.PrefillWorkload("w60", 4, 2, 128, 128, 256, 256, new, ctx)
+    for ctas in (148, 7):
+        case = I.make_prefill(bf16_rel(wl), DEV, seed_data=41, seed_layout=42)
+        check(case, ctas, what=f"60 sequences ctas={ctas}")
