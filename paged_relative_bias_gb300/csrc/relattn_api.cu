@@ -643,13 +643,13 @@ static int prepare_prefill(const void* q, const void* k, const void* v, const vo
                 CU_TENSOR_MAP_SWIZZLE_128B))
     return RELATTN_ERR_CUDA;
   // rel [T][Hq][E] fp32 or bf16: boxes of 32 tokens x 100 (fp32) or 104
-  // (bf16) distances of one head; 168 bf16 distances for 128-key tiles
+  // (bf16) distances of one head; 200 bf16 distances for 128-key tiles
   const cuuint64_t rd[3] = {static_cast<cuuint64_t>(rel_extent),
                             static_cast<cuuint64_t>(dims->num_q_heads),
                             static_cast<cuuint64_t>(dims->num_tokens)};
   const cuuint64_t rs[2] = {static_cast<cuuint64_t>(rel_extent) * io.rel_es,
                             static_cast<cuuint64_t>(rel_extent) * io.rel_es * dims->num_q_heads};
-  const cuuint32_t rb[3] = {L->wide ? 168u : io.rel_es == 2 ? 104u : 100u, 1, 32};
+  const cuuint32_t rb[3] = {L->wide ? 200u : io.rel_es == 2 ? 104u : 100u, 1, 32};
   if (!make_map(&L->tm_rel,
                 io.rel_es == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
                 3, const_cast<void*>(rel), rd, rs, rb, CU_TENSOR_MAP_SWIZZLE_NONE))

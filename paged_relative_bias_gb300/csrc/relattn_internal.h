@@ -149,7 +149,7 @@ cudaError_t launch_prefill_pair(const PrefillLaunch& L, int grid, cudaStream_t s
 // The bf16-cache, bf16-rel prefill (d_v = 128) with one head per work item and
 // 128-key tiles: ring slots (0 if fewer than it needs fit), shared memory,
 // launch (p.ring_stages = the slots; K/V maps with 128-row boxes, rel boxes of
-// 32 rows x 168 distances).
+// 32 rows x 200 distances, the odd boxes starting 32 distances lower).
 int prefill_wide_slots(int B, int smem_optin);
 int prefill_wide_smem_bytes(int B, int nslots);
 cudaError_t launch_prefill_wide(const PrefillLaunch& L, int grid, cudaStream_t stream);

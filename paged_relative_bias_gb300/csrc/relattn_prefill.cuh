@@ -217,40 +217,18 @@ __device__ __forceinline__ void scores_with_bias(float (&x)[64], const uint32_t 
   }
 }
 
-// bf16 rel boxes for 128-key tiles: 32 query rows x 168 distances.  A box
-// row needs the 128 distances P_r - j0 - 127 .. P_r - j0; across 32 rows that
-// is 159, plus up to 7 for rounding the box start down to 16 bytes.  A
-// 336-byte row is 84 words, so 8-byte reads of a warp spread over 16 banks.
-constexpr int kRelColsW = 168;
-constexpr int kRelBoxBytesW = kRelBoxRows * kRelColsW * 2;  // 10752 (84 x 128)
-
-// The scaled scores plus the sheared bias of one query row for half `half`
-// (keys 64 half .. 64 half + 63) of a 128-key tile whose rel boxes sit at
-// `slot`: row r of the tile, P0 the position of the tile's first row.  With
-// no distance of this half below rel_extent, pass has_rel = false.
-__device__ __forceinline__ void scores_with_bias_w(float (&x)[64], const uint32_t (&sr)[64],
-                                                   const uint8_t* slot, int r, int P0, int half,
-                                                   bool has_rel, float scale) {
-  const int rbox = r / kRelBoxRows, rrow = r % kRelBoxRows;
-  if (!has_rel) {
-#pragma unroll
-    for (int c = 0; c < 64; ++c) x[c] = __uint_as_float(sr[c]) * scale;
-    return;
-  }
-  // A box starts at distance (P0 + 32 box - j0 - 127) rounded down to 8, so
-  // the distance of this half's column 63 sits rrow + ((P0 + 1) & 7) + 64 (1 -
-  // half) into the row.
-  const int col = rrow + ((P0 + 1) & 7) + 64 * (1 - half);
-  const uint2* p2 = reinterpret_cast<const uint2*>(
-      reinterpret_cast<const __nv_bfloat16*>(slot + rbox * kRelBoxBytesW) + rrow * kRelColsW +
-      (col & ~3));
-  switch (col & 3) {  // rrow = 4 lane + q4 (mod 32): the same for the warp
-    case 0: rel_fma16<0>(x, sr, p2, scale); break;
-    case 1: rel_fma16<1>(x, sr, p2, scale); break;
-    case 2: rel_fma16<2>(x, sr, p2, scale); break;
-    default: rel_fma16<3>(x, sr, p2, scale); break;
-  }
-}
+// bf16 rel boxes for 128-key tiles: 32 query rows x 200 distances.  A row
+// needs the 128 distances P_r - j0 - 127 .. P_r - j0; across 32 rows that is
+// 159, plus up to 7 for rounding the box start down to 16 bytes, plus 32 in
+// the odd boxes, which start 32 distances lower.  Why: a warp's lanes read
+// rows 4 apart from all four boxes (8 rows each); with 100-word rows the 8
+// rows of one box fall on 8 distinct even bank pairs, and the 32-distance
+// (16-word) shift of the odd boxes moves theirs onto the other 16 banks, so an
+// 8-byte load of the warp uses every bank exactly twice (two wavefronts, the
+// least for 256 bytes) instead of 16 banks four times.
+constexpr int kRelColsW = 200;
+constexpr int kRelBoxBytesW = kRelBoxRows * kRelColsW * 2;  // 12800 (100 x 128)
+constexpr int kRelOddShift = 32;                            // distances, odd boxes
 
 // ---- paired fp32 arithmetic (sm_100 family) --------------------------------
 // Two fp32 lanes in one 64-bit register pair: one instruction does two FMAs
@@ -315,7 +293,11 @@ __device__ __forceinline__ void rel_fma16_x2(uint64_t (&x2)[32], const uint32_t 
     x2[i] = fma_f2(f2u(sr[2 * i], sr[2 * i + 1]), scale2, f2u(relf(2 * i), relf(2 * i + 1)));
 }
 
-// scores_with_bias_w in pairs (see there).
+// x2[i] = the scaled scores plus the sheared bias of columns 2 i and 2 i + 1 of
+// one query row, for half `half` (keys 64 half .. 64 half + 63) of a 128-key
+// tile whose rel boxes sit at `slot`: row r of the tile, P0 the position of
+// the tile's first row.  With no distance of this half below rel_extent, pass
+// has_rel = false (no bias).
 __device__ __forceinline__ void scores_with_bias_w2(uint64_t (&x2)[32], const uint32_t (&sr)[64],
                                                     const uint8_t* slot, int r, int P0, int half,
                                                     bool has_rel, float scale) {
@@ -327,7 +309,10 @@ __device__ __forceinline__ void scores_with_bias_w2(uint64_t (&x2)[32], const ui
     return;
   }
   const int rbox = r / kRelBoxRows, rrow = r % kRelBoxRows;
-  const int col = rrow + ((P0 + 1) & 7) + 64 * (1 - half);
+  // A box starts at distance (P0 + 32 box - j0 - 127) rounded down to 8 (less
+  // kRelOddShift for an odd box), so the distance of this half's column 63
+  // sits rrow + ((P0 + 1) & 7) + 64 (1 - half) (+ kRelOddShift) into the row.
+  const int col = rrow + ((P0 + 1) & 7) + 64 * (1 - half) + kRelOddShift * (rbox & 1);
   const uint2* p2 = reinterpret_cast<const uint2*>(
       reinterpret_cast<const __nv_bfloat16*>(slot + rbox * kRelBoxBytesW) + rrow * kRelColsW +
       (col & ~3));

@@ -26,8 +26,11 @@
 //
 // Shared memory: a ring of three 32 KB K/V stages, used in the order the MMA
 // warp needs them (K of tile 0, K of tile 1, V of tile 0, K of tile 2, V of
-// tile 1, ...), and a ring of 42 KB slots carrying per item: the query tile,
-// the rel boxes of each key tile, then a scratch slot for storing O.  Both
+// tile 1, ...), and a ring of two 50 KB slots carrying, after the first
+// item's query tile, per item: the rel boxes of each key tile, the next
+// item's query tile, then a scratch slot for storing O (the next query comes
+// first: the epilogue loads it before it needs the scratch, and the next
+// item's first rel boxes can then be fetched during the epilogue).  Both
 // softmax groups consume every ring entry.
 //
 // Warp roles: 0-3 and 4-7 = the softmax groups (TMEM lane quarters 0-3 each),
@@ -57,12 +60,12 @@ constexpr int kKeys = 128;                        // keys of one tile: one cache
 constexpr int kDv = 128;                          // d_v of this kernel
 constexpr int kKvStages = 3;                      // K/V ring depth
 constexpr int kKvStageBytes = kKeys * kDqk * 2;   // 32 KB (K, or V with d_v = 128)
-constexpr int kRelTileBytes = kRelBoxes * kRelBoxBytesW;  // 43008 = 42 x 1024
+constexpr int kRelTileBytes = kRelBoxes * kRelBoxBytesW;  // 51200 = 50 x 1024
 constexpr int kSlotBytes = kRelTileBytes;  // also holds a query tile or an O scratch (32 KB)
-// ring slots: 3 when shared memory allows, else 2 (the ring's depth is a
-// template parameter, so that entry -> slot and phase are cheap: a division
-// by a run-time value costs hundreds of cycles on the softmax's path)
-constexpr int kMinSlots = 2, kMaxSlots = 3;
+// ring slots: two 50 KB slots beside the 96 KB of K/V stages (the ring's depth
+// is a template parameter, so that entry -> slot and phase are cheap: a
+// division by a run-time value costs hundreds of cycles on the softmax's path)
+constexpr int kMinSlots = 2, kMaxSlots = 2;
 static_assert(kSlotBytes % 1024 == 0 && kSlotBytes >= kQTileBytes, "slot size");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColQ = 0, kColO = 320;
@@ -271,17 +274,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (i == slot && pend_e[i] >= 0) store_out(i);
       return smem + L.ring + slot * kSlotBytes;
     };
+    // the query tile of item `qit` into ring entry e; rows past T read as zeros
+    auto load_query = [&](const WideItem& qit) -> bool {
+      uint8_t* qd = acquire(e);
+      if (!qd) return false;
+      uint64_t* qbar = &bars[kRFull + e % nslots];
+      mbar_arrive_expect_tx(qbar, kQTileBytes);
+      tma_load_3d(qd, &tm_q, qbar, 0, qit.h, qit.r0);
+      tma_load_3d(qd + kQTileBytes / 2, &tm_q, qbar, 64, qit.h, qit.r0);
+      ++e;
+      return true;
+    };
+    if (static_cast<int>(blockIdx.x) < total && !load_query(wide_item(blockIdx.x, p, sa)))
+      fail = true;
     for (int idx = blockIdx.x; idx < total && !*s_abort && !fail; idx += gridDim.x) {
       const WideItem it = wide_item(idx, p, sa);
-      {  // the query tile; rows past T read as zeros
-        uint8_t* qd = acquire(e);
-        if (!qd) { fail = true; break; }
-        uint64_t* qbar = &bars[kRFull + e % nslots];
-        mbar_arrive_expect_tx(qbar, kQTileBytes);
-        tma_load_3d(qd, &tm_q, qbar, 0, it.h, it.r0);
-        tma_load_3d(qd + kQTileBytes / 2, &tm_q, qbar, 64, it.h, it.r0);
-        ++e;
-      }
       for (int k = 0; k < it.ntiles; ++k, ++e) {  // the rel boxes of each key tile
         const int j0 = (it.tf + k) * kKeys;
         uint8_t* rd = acquire(e);
@@ -290,7 +297,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (it.P0 - j0 - (kKeys - 1) < p.rel_extent) {
           mbar_arrive_expect_tx(rbar, kRelTileBytes);
           for (int bx = 0; bx < kRelBoxes; ++bx) {
-            const int x = (it.P0 + kRelBoxRows * bx - j0 - (kKeys - 1)) & ~7;
+            const int x = ((it.P0 + kRelBoxRows * bx - j0 - (kKeys - 1)) & ~7) -
+                          kRelOddShift * (bx & 1);
             tma_load_3d(rd + bx * kRelBoxBytesW, &tm_rel, rbar, x, it.h,
                         it.r0 + kRelBoxRows * bx);
           }
@@ -299,6 +307,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (fail) break;
+      const int nidx = idx + static_cast<int>(gridDim.x);
+      if (nidx < total && !load_query(wide_item(nidx, p, sa))) { fail = true; break; }
       if (!acquire(e)) { fail = true; break; }  // the O scratch
       if (!O32 && it.rows == kQRows) {
 #pragma unroll
@@ -466,21 +476,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     };
     int t = 0;       // S tiles consumed (buffer t & 1)
-    int e_base = 0;  // ring entries of all earlier items
+    int e_base = 1;  // this item's first ring entry (entry 0: the first item's query)
     int idx = blockIdx.x;
     WideItem it{};
     if (idx < total) it = wide_item(idx, p, sa);
     bool q_loaded = false;  // this item's query is in TMEM already
     while (idx < total) {
       const int n = it.ntiles;
-      const int e_out = e_base + 1 + n;  // the item's O scratch
       const int nidx = idx + static_cast<int>(gridDim.x);
       const bool has_next = nidx < total;
+      const int e_qn = e_base + n;                  // the next item's query (if any)
+      const int e_out = e_qn + (has_next ? 1 : 0);  // the item's O scratch
       bool bad = false;
       if (!q_loaded) {
-        const uint8_t* qs = slot_wait(e_base);
+        const uint8_t* qs = slot_wait(0);  // only the first item's query is not preloaded
         bad = !__all_sync(0xffffffffu, qs != nullptr);
-        if (!bad) load_q(qs, e_base);
+        if (!bad) load_q(qs, 0);
       }
       const bool row_ok = r < it.rows;
       const int P = it.P0 + r;
@@ -522,11 +533,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld32(tl + col_s(b) + 64 * g, sr);
           tmem_ld32(tl + col_s(b) + 64 * g + 32, sr + 32);
           tmem_wait_ld();
-          const uint8_t* slot = slot_wait(e_base + 1 + k);
+          const uint8_t* slot = slot_wait(e_base + k);
           ok = __all_sync(0xffffffffu, slot != nullptr);
           if (ok) {
             scores_with_bias_w2(x2, sr, slot, r, it.P0, g, it.P0 - jg - 63 < p.rel_extent, scale);
-            slot_free(e_base + 1 + k);
+            slot_free(e_base + k);
             if (!warp_full) {
 #pragma unroll
               for (int i = 0; i < 32; ++i) {
@@ -600,12 +611,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
       // The next item's query goes into TMEM first, so its first S = Q K^T
-      // runs while this item's O is stored.  Its ring entry follows the O
-      // scratch, and both are filled without waiting for this epilogue.
+      // runs while this item's O is stored.  Its ring entry comes before the
+      // O scratch, and both are filled without waiting for this epilogue.
       if (has_next && !bad) {
-        const uint8_t* qs = slot_wait(e_out + 1);
+        const uint8_t* qs = slot_wait(e_qn);
         bad = !__all_sync(0xffffffffu, qs != nullptr);
-        if (!bad) load_q(qs, e_out + 1);
+        if (!bad) load_q(qs, e_qn);
       }
       uint8_t* scr = bad ? nullptr : const_cast<uint8_t*>(slot_wait(e_out));
       if (!bad) bad = !__all_sync(0xffffffffu, scr != nullptr);
@@ -835,11 +846,9 @@ static cudaError_t launch_wide_as(const PrefillLaunch& L, int grid, int smem, cu
 template <bool O32>
 static cudaError_t launch_wide_ns(const PrefillLaunch& L, int grid, int smem,
                                   cudaStream_t stream) {
-  switch (L.p.ring_stages) {
-    case 2: return launch_wide_as<O32, 2>(L, grid, smem, stream);
-    case 3: return launch_wide_as<O32, 3>(L, grid, smem, stream);
-    default: return cudaErrorInvalidValue;
-  }
+  static_assert(kMinSlots == 2 && kMaxSlots == 2, "ring depths instantiated here");
+  return L.p.ring_stages == 2 ? launch_wide_as<O32, 2>(L, grid, smem, stream)
+                              : cudaErrorInvalidValue;
 }
 
 cudaError_t launch_prefill_wide(const PrefillLaunch& L, int grid, cudaStream_t stream) {
