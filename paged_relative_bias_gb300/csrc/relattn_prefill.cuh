@@ -93,6 +93,42 @@ __device__ inline int prologue(const PrefillParams& p, SeqArrays a, bool zero_ba
   return a.qpref[p.B];
 }
 
+// out[j] = in[(j + rot) & 7] for 8 chunks of 4 words (rot 0 .. 7), by three
+// conditional rotations.  A lane that reads or writes a 128-byte-swizzled
+// row's chunks starting at chunk lane & 7 spreads the 8 lanes of each
+// quarter-warp (rows 4 apart here) over all 8 bank groups; this puts the
+// chunks back in order (or into that order).
+__device__ __forceinline__ void rotate_chunks(uint32_t (&w)[32], int rot) {
+#pragma unroll
+  for (int b = 1; b < 8; b <<= 1) {
+    const bool on = (rot & b) != 0;
+    uint32_t t[32];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) t[4 * j + e] = on ? w[4 * ((j + b) & 7) + e] : w[4 * j + e];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) w[i] = t[i];
+  }
+}
+
+// The eight 16-byte chunks of row `row` of a 128-byte-swizzled half tile at
+// `base` (rows of 128 bytes), in chunk order, read starting at chunk lane & 7
+// (conflict-free when the lanes' rows are 4 apart; see rotate_chunks).
+__device__ __forceinline__ void load_row128(const uint8_t* base, int row, int lane,
+                                            uint32_t (&w)[32]) {
+  const int rot = lane & 7;
+#pragma unroll
+  for (int s = 0; s < 8; ++s) {
+    const uint4 v = *reinterpret_cast<const uint4*>(base + sw128(row, (s + rot) & 7));
+    w[4 * s] = v.x;
+    w[4 * s + 1] = v.y;
+    w[4 * s + 2] = v.z;
+    w[4 * s + 3] = v.w;
+  }
+  rotate_chunks(w, (8 - rot) & 7);  // back to chunk order
+}
+
 // Query tile qtg (0 .. tiles - 1): its sequence, first packed row, valid rows,
 // position of its first row, and its window-aware range of 64-key tiles
 // [tf, tf + ntiles): the tiles holding a key that one of its rows sees.

@@ -359,20 +359,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // This thread's query row, from a ring slot (128-byte swizzled rows) into
     // TMEM, the A operand of S = Q K^T; then the MMA warp may start.
     auto load_q = [&](const uint8_t* qs, int entry) {
-      uint32_t qr[64];
 #pragma unroll
-      for (int c = 0; c < 2; ++c)
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const uint4 v =
-              *reinterpret_cast<const uint4*>(qs + c * (kQTileBytes / 2) + sw128(r, j));
-          qr[(c * 8 + j) * 4] = v.x;
-          qr[(c * 8 + j) * 4 + 1] = v.y;
-          qr[(c * 8 + j) * 4 + 2] = v.z;
-          qr[(c * 8 + j) * 4 + 3] = v.w;
-        }
-      tmem_st32(cq, qr);
-      tmem_st32(cq + 32, qr + 32);
+      for (int c = 0; c < 2; ++c) {
+        uint32_t qr[32];
+        load_row128(qs + c * (kQTileBytes / 2), r, lane, qr);
+        tmem_st32(cq + 32 * c, qr);
+      }
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();

@@ -102,25 +102,6 @@ struct WideSmem {
   }
 };
 
-// out[j] = in[(j + rot) & 7] for 8 chunks of 4 words (rot 0 .. 7), by three
-// conditional rotations.  A lane that reads or writes a 128-byte-swizzled
-// row's chunks starting at chunk lane & 7 spreads the 8 lanes of each
-// quarter-warp (rows 4 apart here) over all 8 bank groups; this puts the
-// chunks back in order (or into that order).
-__device__ __forceinline__ void rotate_chunks(uint32_t (&w)[32], int rot) {
-#pragma unroll
-  for (int b = 1; b < 8; b <<= 1) {
-    const bool on = (rot & b) != 0;
-    uint32_t t[32];
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) t[4 * j + e] = on ? w[4 * ((j + b) & 7) + e] : w[4 * j + e];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) w[i] = t[i];
-  }
-}
-
 constexpr int kOutBoxBytes = 128 * 128;  // one 128-byte column box of 128 rows
 
 // Work item idx: query tile idx / Hq, head idx % Hq, so that the heads of one
@@ -453,19 +434,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // This thread's half of its query row (dims 64 g .. 64 g + 63), from the
     // ring slot (128-byte swizzled rows) into TMEM, the A operand of S = Q K^T.
     auto load_q = [&](const uint8_t* qs, int entry) {
-      // chunk (s + rot) & 7 at step s (conflict-free, see rotate_chunks)
-      const int rot = lane & 7;
       uint32_t qr[32];
-#pragma unroll
-      for (int s2 = 0; s2 < 8; ++s2) {
-        const uint4 v = *reinterpret_cast<const uint4*>(qs + g * (kQTileBytes / 2) +
-                                                        sw128(r, (s2 + rot) & 7));
-        qr[4 * s2] = v.x;
-        qr[4 * s2 + 1] = v.y;
-        qr[4 * s2 + 2] = v.z;
-        qr[4 * s2 + 3] = v.w;
-      }
-      rotate_chunks(qr, (8 - rot) & 7);  // back to chunk order
+      load_row128(qs + g * (kQTileBytes / 2), r, lane, qr);
       tmem_st32(tl + kColQ + 32 * g, qr);
       tmem_wait_st();
       tc_fence_before();
