@@ -294,8 +294,9 @@ int relattn_decode_ex(const void* q, const void* rel, const relattn_options* opt
  *    must run in the device's primary context (the runtime's), and not after
  *    cudaDeviceReset, since either would leave the kept address stale.
  *  - Every call clears the status word and counters of the array on `stream`
- *    before its kernel, so no zero-filling is needed by the caller; device
- *    status bits are not reported back by this call.
+ *    before its kernel, so no zero-filling is needed by the caller; the
+ *    call's device status bits (RELATTN_DEV_*) stay in the array's status
+ *    word until the next call, and relattn_decode_noalloc_status reads them.
  *  - All calls share the one array: calls whose work overlaps on the GPU
  *    (different streams without ordering between them) race and corrupt each
  *    other's results.  Order them on one stream.
@@ -305,6 +306,16 @@ int relattn_decode_noalloc(const void* q, const float* rel,
                            const int32_t* block_table, const int32_t* seq_lens,
                            int32_t window, int32_t rel_extent,
                            const relattn_dims* dims, void* out, void* stream);
+
+/*
+ * Device status bits of the last relattn_decode_noalloc call on the current
+ * device: the status word of the library's array, copied to host memory
+ * after the work queued on `stream` (enqueue it on the stream of the calls).
+ * Like relattn_read_status it synchronises `stream`, so it cannot be
+ * captured in a graph.  Returns RELATTN_OK, RELATTN_ERR_INVALID_ARG (status
+ * NULL) or RELATTN_ERR_CUDA.
+ */
+int relattn_decode_noalloc_status(uint32_t* status, void* stream);
 
 /*
  * Chunked prefill with a cached prefix.

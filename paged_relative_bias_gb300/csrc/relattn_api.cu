@@ -521,6 +521,14 @@ static int noalloc_scratch(void** addr) {
   return RELATTN_OK;
 }
 
+int relattn_decode_noalloc_status(uint32_t* status, void* stream) {
+  if (!status) return RELATTN_ERR_INVALID_ARG;
+  void* scratch = nullptr;
+  const int rc = noalloc_scratch(&scratch);
+  if (rc != RELATTN_OK) return rc;
+  return relattn_read_status(scratch, status, stream);  // the array starts with the status word
+}
+
 int relattn_decode_noalloc(const void* q, const float* rel, const relattn_kv_cache* kv_cache,
                            const int32_t* block_table, const int32_t* seq_lens, int32_t window,
                            int32_t rel_extent, const relattn_dims* dims, void* out,

@@ -46,6 +46,7 @@ EXPORTS = (
     "relattn_debug_decode_give_up",
     "relattn_debug_walk_decode_ex",
     "relattn_debug_walk_prefill_ex",
+    "relattn_decode_noalloc_status",
 )
 
 DTYPE_F32 = 0
@@ -124,6 +125,8 @@ def lib() -> ctypes.CDLL:
                                                 POINTER(Options), P, S, c_void_p, c_int32,
                                                 c_void_p, c_void_p, c_size_t, c_void_p]
     L.relattn_debug_walk_prefill_ex.restype = c_int
+    L.relattn_decode_noalloc_status.argtypes = [c_void_p, c_void_p]
+    L.relattn_decode_noalloc_status.restype = c_int
     L.relattn_decode_noalloc.argtypes = [c_void_p, c_void_p, P, c_void_p, c_void_p, c_int32,
                                          c_int32, S, c_void_p, c_void_p]
     L.relattn_decode_noalloc.restype = c_int
@@ -358,6 +361,17 @@ def relattn_decode_noalloc(q, rel, k_cache, v_cache, block_table, seq_lens, wind
         seq_lens.data_ptr(), int(window), int(rel_extent), ctypes.byref(dims),
         out.data_ptr(), _stream(dev)), "relattn_decode_noalloc")
     return out
+
+
+def noalloc_status(device=None) -> int:
+    """Status bits of the last relattn_decode_noalloc call on the device
+    (synchronises the current stream)."""
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    st = (ctypes.c_uint32 * 1)()
+    with torch.cuda.device(dev):
+        _check(lib().relattn_decode_noalloc_status(ctypes.addressof(st), _stream(dev)),
+               "relattn_decode_noalloc_status")
+    return int(st[0])
 
 
 def relattn_decode_multi(q, rel, k_cache, v_cache, block_table, seq_lens, window: int,

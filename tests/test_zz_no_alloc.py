@@ -73,3 +73,18 @@ def test_noalloc_rejects_sizes_beyond_its_array():
     assert err.value.code == R.ERR_WORKSPACE
     torch.cuda.synchronize()
     assert torch.count_nonzero(out).item() == 0
+
+
+def test_noalloc_status_reports_a_bad_block_id_then_clears():
+    """The call's device status bits stay in the array until the next call:
+    a block id outside the pool sets RELATTN_DEV_BAD_BLOCK_ID, and the next
+    clean call starts from zero."""
+    wl = I.variant(I.WORKLOADS["global_decode_b8"], batch=2, lengths=("uniform", 200, 900))
+    case = I.make_decode(wl, DEV, seed_data=17)
+    out = torch.empty_like(case["q"][..., :case["v_cache"].shape[-1]])
+    bad = dict(case, block_table=case["block_table"].clone())
+    bad["block_table"][1, 0] = case["k_cache"].shape[0] + 5  # outside the pool
+    without_workspace(bad, out, 0)
+    assert R.noalloc_status(DEV) & R.DEV_BAD_BLOCK_ID
+    without_workspace(case, out, 0)
+    assert R.noalloc_status(DEV) == 0
