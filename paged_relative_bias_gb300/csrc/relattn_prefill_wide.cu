@@ -574,20 +574,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(&bars[kPFull + b]);
       }
       if (!ok) bad = true;
+      // The next item's query goes into TMEM first: every S = Q K^T of this
+      // item is complete (this thread saw the last S), so the next item's
+      // first S can run while this item's last P V completes and O is stored.
+      // Its ring entry comes before the O scratch, and both are filled
+      // without waiting for this epilogue.
+      if (has_next && !bad) {
+        const uint8_t* qs = slot_wait(e_qn);
+        bad = !__all_sync(0xffffffffu, qs != nullptr);
+        if (!bad) load_q(qs, e_qn);
+      }
       // the item's last P V completes O, and every earlier MMA with it
       if (!bad) {
         const int tq = t - 1;
         bad = !__all_sync(0xffffffffu, mbar_wait(&bars[kOFull + (tq & 1)], (tq >> 1) & 1));
       }
       tc_fence_after();
-      // The next item's query goes into TMEM first, so its first S = Q K^T
-      // runs while this item's O is stored.  Its ring entry comes before the
-      // O scratch, and both are filled without waiting for this epilogue.
-      if (has_next && !bad) {
-        const uint8_t* qs = slot_wait(e_qn);
-        bad = !__all_sync(0xffffffffu, qs != nullptr);
-        if (!bad) load_q(qs, e_qn);
-      }
       uint8_t* scr = bad ? nullptr : const_cast<uint8_t*>(slot_wait(e_out));
       if (!bad) bad = !__all_sync(0xffffffffu, scr != nullptr);
       s_lsum[128 * g + r] = l;
