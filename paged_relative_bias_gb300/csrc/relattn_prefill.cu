@@ -79,8 +79,13 @@ __device__ __forceinline__ uint2 e4m3x8(uint4 x, float scale) {
 }
 
 // KV8: the cache is e4m3, head-major [NB][Hkv][128][128], and each value is
-// quantised with its tensor's scale; one thread-iteration writes 16 codes
-// (16 bytes) from 16 bf16 values.  Otherwise a 16-byte copy.
+// quantised with its tensor's scale; a 16-byte piece of the cache holds 16
+// codes from 16 bf16 values.  Otherwise a bf16 cache, [NB][128][Hkv][d], where
+// a token's Hkv key (or value) rows are contiguous both in k (v) and in its
+// cache slot, so they copy as one run of 16-byte pieces.
+// One warp per token: its pieces go out lane by lane (coalesced), with no
+// division on the way (a division by a run-time value per 16 bytes made the
+// copy instruction-bound).
 template <bool KV8>
 __global__ void __launch_bounds__(256) cache_write_kernel(const PrefillParams p) {
   const int b = blockIdx.y;
@@ -95,43 +100,48 @@ __global__ void __launch_bounds__(256) cache_write_kernel(const PrefillParams p)
   }
   if (t0 >= n) return;
   const int nt = min(kCwTile, n - t0);
-  const int kch = kDqk / (KV8 ? 16 : 8), vch = p.dv / (KV8 ? 16 : 8);  // 16-byte pieces
-  const int per_tok = p.Hkv * (kch + vch);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int kWarps = 256 / 32;
+  // 16-byte pieces of one token's keys and values (all KV heads)
+  const int kpieces = p.Hkv * (KV8 ? kDqk / 16 : kDqk / 8);
+  const int vpieces = p.Hkv * (KV8 ? p.dv / 16 : p.dv / 8);
   const int* trow = p.block_table + static_cast<size_t>(b) * p.max_blocks;
-  for (int i = threadIdx.x; i < nt * per_tok; i += blockDim.x) {
-    const int tt = i / per_tok;
-    const int rem = i - tt * per_tok;
-    const int hh = rem / (kch + vch);
-    int ch = rem - hh * (kch + vch);
+  for (int tt = warp; tt < nt; tt += kWarps) {
     const int pos = ctx + t0 + tt;
     const int phys = __ldg(trow + pos / kBlockSize);
-    if (phys < 0 || phys >= p.num_blocks) {
-      report(p.status, RELATTN_DEV_BAD_BLOCK_ID);
+    if (phys < 0 || phys >= p.num_blocks) {  // the same for the whole warp
+      if (lane == 0) report(p.status, RELATTN_DEV_BAD_BLOCK_ID);
       continue;
     }
-    const size_t slot = static_cast<size_t>(phys) * kBlockSize + pos % kBlockSize;
     const size_t row = static_cast<size_t>(r0 + t0 + tt);
+    const int in_blk = pos % kBlockSize;
     if constexpr (KV8) {
-      // row (phys * Hkv + hh) * 128 + pos % 128 of the head-major cache
-      const size_t hrow = (static_cast<size_t>(phys) * p.Hkv + hh) * kBlockSize + pos % kBlockSize;
-      const bool isk = ch < kch;
-      if (!isk) ch -= kch;
-      const uint4* src = reinterpret_cast<const uint4*>(
-          isk ? p.k + (row * p.Hkv + hh) * kDqk : p.v + (row * p.Hkv + hh) * p.dv);
-      const float sc = isk ? p.k_scale : p.v_scale;
-      const uint2 lo = e4m3x8(__ldg(src + 2 * ch), sc), hi = e4m3x8(__ldg(src + 2 * ch + 1), sc);
-      uint8_t* dst = reinterpret_cast<uint8_t*>(isk ? p.k_cache : p.v_cache) +
-                     hrow * (isk ? kDqk : p.dv);
-      reinterpret_cast<uint4*>(dst)[ch] = make_uint4(lo.x, lo.y, hi.x, hi.y);
-      continue;
-    }
-    if (ch < kch) {
-      const uint4 val = __ldg(reinterpret_cast<const uint4*>(p.k + (row * p.Hkv + hh) * kDqk) + ch);
-      reinterpret_cast<uint4*>(p.k_cache + (slot * p.Hkv + hh) * kDqk)[ch] = val;
+      // piece c of a token's keys: head c / 8, codes 16 (c % 8) .. of its row
+      // (d = 128: 8 pieces per head row), at row (phys * Hkv + head) * 128 +
+      // pos % 128 of the head-major cache
+#pragma unroll 1
+      for (int c = lane; c < kpieces + vpieces; c += 32) {
+        const bool isk = c < kpieces;
+        const int cc = isk ? c : c - kpieces;
+        const int hh = cc >> 3, ch = cc & 7;
+        const uint4* src = reinterpret_cast<const uint4*>(
+            (isk ? p.k : p.v) + (row * p.Hkv + hh) * kDqk);
+        const float sc = isk ? p.k_scale : p.v_scale;
+        const uint2 lo = e4m3x8(__ldg(src + 2 * ch), sc), hi = e4m3x8(__ldg(src + 2 * ch + 1), sc);
+        const size_t hrow = (static_cast<size_t>(phys) * p.Hkv + hh) * kBlockSize + in_blk;
+        uint8_t* dst = reinterpret_cast<uint8_t*>(isk ? p.k_cache : p.v_cache) + hrow * kDqk;
+        reinterpret_cast<uint4*>(dst)[ch] = make_uint4(lo.x, lo.y, hi.x, hi.y);
+      }
     } else {
-      ch -= kch;
-      const uint4 val = __ldg(reinterpret_cast<const uint4*>(p.v + (row * p.Hkv + hh) * p.dv) + ch);
-      reinterpret_cast<uint4*>(p.v_cache + (slot * p.Hkv + hh) * p.dv)[ch] = val;
+      const size_t slot = static_cast<size_t>(phys) * kBlockSize + in_blk;
+      const uint4* ks = reinterpret_cast<const uint4*>(p.k + row * p.Hkv * kDqk);
+      uint4* kd = reinterpret_cast<uint4*>(p.k_cache + slot * p.Hkv * kDqk);
+#pragma unroll 4
+      for (int c = lane; c < kpieces; c += 32) kd[c] = __ldg(ks + c);
+      const uint4* vs = reinterpret_cast<const uint4*>(p.v + row * p.Hkv * p.dv);
+      uint4* vd = reinterpret_cast<uint4*>(p.v_cache + slot * p.Hkv * p.dv);
+#pragma unroll 4
+      for (int c = lane; c < vpieces; c += 32) vd[c] = __ldg(vs + c);
     }
   }
 }
