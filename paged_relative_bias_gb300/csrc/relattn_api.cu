@@ -338,6 +338,7 @@ static int prepare_decode(const void* q, const void* rel, IoTypes io,
   p.Hq = dims->num_q_heads;
   p.Hkv = cache->num_kv_heads;
   p.g = g;
+  p.g_mul = static_cast<uint32_t>((65536 + g - 1) / g);
   p.dv = cache->d_v;
   p.max_blocks = dims->max_blocks_per_seq;
   p.num_blocks = cache->num_blocks;

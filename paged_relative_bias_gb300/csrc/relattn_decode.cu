@@ -1320,8 +1320,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     const int slot = 2 * c + (a0 < pc.seg_start ? 1 : 0);
     // out row of tile row r: token i0 + r / g of sequence b, head h0 + r % g
     // (out is bf16, or fp32 when p.out_f32: element index, either type)
+    // the output row of tile row `row`; its token row / g by a multiply and a
+    // shift (this runs per element pair of the store)
     auto orow = [&](int row) -> size_t {
-      const int ti = tok.token_of_row(row, g);
+      const int ti = MULTI ? static_cast<int>((static_cast<uint32_t>(row) * p.g_mul) >> 16) : 0;
       return ((static_cast<size_t>(sq.b) * tok.k + sq.i0 + ti) * p.Hq + h0 + (row - ti * g)) * DV;
     };
     for (int idx = ctid; idx < nrows * DV / 2; idx += kConsumerThreads) {

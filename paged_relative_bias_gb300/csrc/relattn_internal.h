@@ -44,6 +44,9 @@ struct DecodeParams {
   int dbg_give_up;             // test hook: > 0 makes the consumer warps of every CTA
                                // treat the query wait of piece dbg_give_up - 1 as given up
   int B, Hq, Hkv, g, dv, max_blocks, num_blocks, window, rel_extent;
+  // ceil(2^16 / g): row / g = (row * g_mul) >> 16, exact for the tile rows
+  // (row < 32, g <= 16: the error row * (g_mul g - 2^16) / (g 2^16) < 1 / g)
+  uint32_t g_mul;
   // query tokens per sequence (k; 1 for plain decode), packed kpc at a time
   // with the g heads into the rows of one tile: nck = ceil(k / kpc) chunks
   // per sequence, Bv = B * nck chunks ("virtual sequences") in all
