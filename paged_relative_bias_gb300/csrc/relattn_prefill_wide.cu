@@ -238,7 +238,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // (-1: none), pend_h / pend_r0 its head and first row.
     int pend_e[nslots], pend_h[nslots], pend_r0[nslots];
 #pragma unroll
-    for (int i = 0; i < nslots; ++i) pend_e[i] = pend_h[i] = pend_r0[i] = 0, pend_e[i] = -1;
+    for (int i = 0; i < nslots; ++i) {
+      pend_e[i] = -1;
+      pend_h[i] = 0;
+      pend_r0[i] = 0;
+    }
     auto store_out = [&](int slot) {
       const uint8_t* src = smem + L.ring + slot * kSlotBytes;
       tma_store_3d(&tm_out, src, 0, pend_h[slot], pend_r0[slot]);
