@@ -163,6 +163,25 @@ __device__ __forceinline__ uint64_t add_f2(uint64_t a, uint64_t b) {
   asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
 }
+__device__ __forceinline__ uint64_t mul_f2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+// c + the bf16 in the high (HI) or low half of w, rounded once to fp32 (a
+// mixed-precision add: the bf16 operand is read as it is, with no widening
+// instruction)
+template <bool HI>
+__device__ __forceinline__ float add_bf16_f32(uint32_t w, float c) {
+  float d;
+  if constexpr (HI)
+    asm("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %1;\n add.rn.f32.bf16 %0, h, %2;\n}"
+        : "=f"(d) : "r"(w), "f"(c));
+  else
+    asm("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %1;\n add.rn.f32.bf16 %0, l, %2;\n}"
+        : "=f"(d) : "r"(w), "f"(c));
+  return d;
+}
 // max of three (one instruction)
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float d;

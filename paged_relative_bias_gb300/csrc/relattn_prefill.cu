@@ -567,20 +567,12 @@ __global__ void __launch_bounds__(32 * (kPfWarps + (KV8 ? 1 : 0)), 1)
         tmem_wait_ld();
         const uint8_t* slot = slot_wait(e);
         if (!slot) { ok = false; break; }
-        float x[64];
-        scores_with_bias<R16>(x, sr, slot, r, it.P0,
+        uint64_t x2[32];  // the scores of columns (2 i, 2 i + 1)
+        scores_with_bias<R16>(x2, sr, slot, r, it.P0,
                               it.P0 - j0 - (kTileKeys - 1) < p.rel_extent, scale);
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[kREmpty + ri.slot(e)]);
-        if (!warp_full) {
-#pragma unroll
-          for (int c = 0; c < 64; ++c)
-            x[c] = static_cast<unsigned>(c - clo) < static_cast<unsigned>(span) ? x[c] : kNegInf;
-        }
-        float mq[4] = {x[0], x[1], x[2], x[3]};
-#pragma unroll
-        for (int c = 4; c < 64; ++c) mq[c & 3] = fmaxf(mq[c & 3], x[c]);
-        const float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
+        const float mx = mask_and_max(x2, warp_full, clo, span);
         const bool grow = mx > m_used + grow_by;
         const float m_new = grow ? mx : m_used;
         const float alpha = (grow && m_used != kNegInf) ? ex2((m_used - m_new) * l2f) : 1.f;
@@ -605,15 +597,7 @@ __global__ void __launch_bounds__(32 * (kPfWarps + (KV8 ? 1 : 0)), 1)
         m_used = m_new;
         const float mb = m_used == kNegInf ? 0.f : -m_used * l2f;
         uint32_t pk[32];
-        float sq[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float p0 = ex2(fmaf(x[2 * i], l2f, mb));
-          const float p1 = ex2(fmaf(x[2 * i + 1], l2f, mb));
-          sq[i & 3] += p0 + p1;
-          pk[i] = KV8 ? pack_f16(p0, p1) : pack_bf16(p0, p1);
-        }
-        l += (sq[0] + sq[1]) + (sq[2] + sq[3]);
+        l += exp_pack<KV8>(x2, l2f, mb, pk);
         tmem_st32(tl + kTmS + 64 * s, pk);
         tmem_wait_st();
         tc_fence_before();

@@ -173,54 +173,69 @@ __device__ __forceinline__ KvTile kv_tile(const int* trow, int tile, int num_blo
   return t;
 }
 
-// x[c] = s[c] * scale + rel for the 64 columns of one query row, from 17
-// aligned 16-byte loads.  p4 points A floats before the row's lowest needed
-// distance (the one of column 63); distances rise towards column 0.
+// x2[i] = (x[2 i], x[2 i + 1]), x[c] = s[c] * scale + rel, for the 64
+// columns of one query row, from 17 aligned 16-byte loads.  p4 points A
+// floats before the row's lowest needed distance (the one of column 63);
+// distances rise towards column 0, so float q of the loads belongs to column
+// 63 - q + A.  (Two scalar FMAs per pair: the two distances of a pair sit in
+// memory in the opposite order to the pair's columns.)
 template <int A>
-__device__ __forceinline__ void rel_fma(float (&x)[64], const uint32_t (&sr)[64],
+__device__ __forceinline__ void rel_fma(uint64_t (&x2)[32], const uint32_t (&sr)[64],
                                         const float4* p4, float scale) {
+  float rf[68];
 #pragma unroll
   for (int w = 0; w < 17; ++w) {
     const float4 v = p4[w];
-    const float f[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int t = 4 * w + e - A;  // distance above the lowest
-      if (t >= 0 && t < 64) x[63 - t] = fmaf(__uint_as_float(sr[63 - t]), scale, f[e]);
-    }
+    rf[4 * w] = v.x;
+    rf[4 * w + 1] = v.y;
+    rf[4 * w + 2] = v.z;
+    rf[4 * w + 3] = v.w;
   }
+#pragma unroll
+  for (int i = 0; i < 32; ++i)
+    x2[i] = f2(fmaf(__uint_as_float(sr[2 * i]), scale, rf[63 - 2 * i + A]),
+               fmaf(__uint_as_float(sr[2 * i + 1]), scale, rf[62 - 2 * i + A]));
 }
 
-// The same from bf16 rel: 17 aligned 8-byte loads of four distances, each
-// widened exactly (a bf16 is the top half of a binary32).
+// The same from bf16 rel: 17 aligned 8-byte loads of four distances; bf16 q
+// sits in word q / 2, in its high half when q is odd.  Each pair's scores are
+// scaled by one paired multiply, and each bias joins its score in a
+// mixed-precision add (no widening instruction).
 template <int A>
-__device__ __forceinline__ void rel_fma16(float (&x)[64], const uint32_t (&sr)[64],
-                                          const uint2* p2, float scale) {
+__device__ __forceinline__ void rel_fma16(uint64_t (&x2)[32], const uint32_t (&sr)[64],
+                                          const uint2* p2, uint64_t scale2) {
+  uint32_t w[34];
 #pragma unroll
-  for (int w = 0; w < 17; ++w) {
-    const uint2 v = p2[w];
-    const float f[4] = {__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xffff0000u),
-                        __uint_as_float(v.y << 16), __uint_as_float(v.y & 0xffff0000u)};
+  for (int k = 0; k < 17; ++k) {
+    const uint2 v = p2[k];
+    w[2 * k] = v.x;
+    w[2 * k + 1] = v.y;
+  }
+  auto plus_rel = [&](int c, float t) -> float {
+    const int q = 63 - c + A;
+    return (q & 1) ? add_bf16_f32<true>(w[q >> 1], t) : add_bf16_f32<false>(w[q >> 1], t);
+  };
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int t = 4 * w + e - A;  // distance above the lowest
-      if (t >= 0 && t < 64) x[63 - t] = fmaf(__uint_as_float(sr[63 - t]), scale, f[e]);
-    }
+  for (int i = 0; i < 32; ++i) {
+    const uint64_t t2 = mul_f2(f2u(sr[2 * i], sr[2 * i + 1]), scale2);
+    x2[i] = f2(plus_rel(2 * i, f2lo(t2)), plus_rel(2 * i + 1, f2hi(t2)));
   }
 }
 
 // The scaled scores plus the sheared bias of one query row for one 64-key
-// tile whose rel boxes sit at `slot`: row r of the tile (box r / 32, row
-// r % 32 in it), P0 the position of the tile's first row.  Every distance of
-// the tile past rel_extent: pass has_rel = false (no bias).
+// tile whose rel boxes sit at `slot`, as pairs of columns (x2[i] holds
+// columns 2 i and 2 i + 1): row r of the tile (box r / 32, row r % 32 in it),
+// P0 the position of the tile's first row.  Every distance of the tile past
+// rel_extent: pass has_rel = false (no bias).
 template <bool R16>
-__device__ __forceinline__ void scores_with_bias(float (&x)[64], const uint32_t (&sr)[64],
+__device__ __forceinline__ void scores_with_bias(uint64_t (&x2)[32], const uint32_t (&sr)[64],
                                                  const uint8_t* slot, int r, int P0,
                                                  bool has_rel, float scale) {
   const int rbox = r / kRelBoxRows, rrow = r % kRelBoxRows;
+  const uint64_t scale2 = f2(scale, scale);
   if (!has_rel) {
 #pragma unroll
-    for (int c = 0; c < 64; ++c) x[c] = __uint_as_float(sr[c]) * scale;
+    for (int i = 0; i < 32; ++i) x2[i] = mul_f2(f2u(sr[2 * i], sr[2 * i + 1]), scale2);
     return;
   }
   if constexpr (R16) {
@@ -232,10 +247,10 @@ __device__ __forceinline__ void scores_with_bias(float (&x)[64], const uint32_t 
         reinterpret_cast<const __nv_bfloat16*>(slot + rbox * kRelBoxBytes16) +
         rrow * kRelBoxCols16 + (col & ~3));
     switch (col & 3) {  // rrow = 4 lane + q4 (mod 32): the same for the warp
-      case 0: rel_fma16<0>(x, sr, p2, scale); break;
-      case 1: rel_fma16<1>(x, sr, p2, scale); break;
-      case 2: rel_fma16<2>(x, sr, p2, scale); break;
-      default: rel_fma16<3>(x, sr, p2, scale); break;
+      case 0: rel_fma16<0>(x2, sr, p2, scale2); break;
+      case 1: rel_fma16<1>(x2, sr, p2, scale2); break;
+      case 2: rel_fma16<2>(x2, sr, p2, scale2); break;
+      default: rel_fma16<3>(x2, sr, p2, scale2); break;
     }
   } else {
     // A box starts at distance (P0 + 32 box - j0 - 63) rounded down to 4, so
@@ -245,12 +260,50 @@ __device__ __forceinline__ void scores_with_bias(float (&x)[64], const uint32_t 
         reinterpret_cast<const float*>(slot + rbox * kRelBoxBytes) + rrow * kRelBoxCols +
         (col & ~3));
     switch (col & 3) {  // the same for every lane of the warp
-      case 0: rel_fma<0>(x, sr, p4, scale); break;
-      case 1: rel_fma<1>(x, sr, p4, scale); break;
-      case 2: rel_fma<2>(x, sr, p4, scale); break;
-      default: rel_fma<3>(x, sr, p4, scale); break;
+      case 0: rel_fma<0>(x2, sr, p4, scale); break;
+      case 1: rel_fma<1>(x2, sr, p4, scale); break;
+      case 2: rel_fma<2>(x2, sr, p4, scale); break;
+      default: rel_fma<3>(x2, sr, p4, scale); break;
     }
   }
+}
+
+// Hidden columns of a row (outside [clo, clo + span)) to -inf, and the row's
+// maximum over its pairs of columns (three-input max).
+__device__ __forceinline__ float mask_and_max(uint64_t (&x2)[32], bool warp_full, int clo,
+                                              int span) {
+  if (!warp_full) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const float lo = static_cast<unsigned>(2 * i - clo) < static_cast<unsigned>(span)
+                           ? f2lo(x2[i]) : kNegInf;
+      const float hi = static_cast<unsigned>(2 * i + 1 - clo) < static_cast<unsigned>(span)
+                           ? f2hi(x2[i]) : kNegInf;
+      x2[i] = f2(lo, hi);
+    }
+  }
+  float mq[4] = {kNegInf, kNegInf, kNegInf, kNegInf};
+#pragma unroll
+  for (int i = 0; i < 32; ++i) mq[i & 3] = fmax3(mq[i & 3], f2lo(x2[i]), f2hi(x2[i]));
+  return fmax3(mq[0], mq[1], fmaxf(mq[2], mq[3]));
+}
+
+// P = exp2(x l2f + mb) for a row's 64 columns, packed in pairs (bf16, or f16
+// when F16) into pk, and the sum of the 64 values (before packing).
+template <bool F16>
+__device__ __forceinline__ float exp_pack(const uint64_t (&x2)[32], float l2f, float mb,
+                                          uint32_t (&pk)[32]) {
+  const uint64_t l2f2 = f2(l2f, l2f), mb2 = f2(mb, mb);
+  uint64_t sq[2] = {f2(0.f, 0.f), f2(0.f, 0.f)};
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const uint64_t a2 = fma_f2(x2[i], l2f2, mb2);
+    const float p0 = ex2(f2lo(a2)), p1 = ex2(f2hi(a2));
+    sq[i & 1] = add_f2(sq[i & 1], f2(p0, p1));
+    pk[i] = F16 ? pack_f16(p0, p1) : pack_bf16(p0, p1);
+  }
+  const uint64_t sqt = add_f2(sq[0], sq[1]);
+  return f2lo(sqt) + f2hi(sqt);
 }
 
 // bf16 rel boxes for 128-key tiles: 32 query rows x 200 distances.  A row
@@ -281,14 +334,17 @@ __device__ __forceinline__ void rel_fma16_x2(uint64_t (&x2)[32], const uint32_t 
     w[2 * k + 1] = v.y;
   }
   // distance u (from the load's start) of column c is 63 - c + A: bf16 u
-  // sits in word u / 2, in its high half when u is odd
-  auto relf = [&](int c) -> uint32_t {
+  // sits in word u / 2, in its high half when u is odd.  The scaled score
+  // and the bf16 bias meet in one mixed-precision add.
+  auto plus_rel = [&](int c, float t) -> float {
     const int u = 63 - c + A;
-    return (u & 1) ? (w[u >> 1] & 0xffff0000u) : (w[u >> 1] << 16);
+    return (u & 1) ? add_bf16_f32<true>(w[u >> 1], t) : add_bf16_f32<false>(w[u >> 1], t);
   };
 #pragma unroll
-  for (int i = 0; i < 32; ++i)
-    x2[i] = fma_f2(f2u(sr[2 * i], sr[2 * i + 1]), scale2, f2u(relf(2 * i), relf(2 * i + 1)));
+  for (int i = 0; i < 32; ++i) {
+    const uint64_t t2 = mul_f2(f2u(sr[2 * i], sr[2 * i + 1]), scale2);
+    x2[i] = f2(plus_rel(2 * i, f2lo(t2)), plus_rel(2 * i + 1, f2hi(t2)));
+  }
 }
 
 // x2[i] = the scaled scores plus the sheared bias of columns 2 i and 2 i + 1 of
