@@ -73,6 +73,9 @@ __host__ __device__ constexpr uint32_t col_s(int b) { return 64u + 128u * b; }
 constexpr uint32_t kIdescS = umma_idesc_bf16(128, kKeys, 0);
 constexpr uint32_t kIdescPV = umma_idesc_bf16(128, kDv, 1);
 constexpr int kXchgBar = 1;  // named barrier of the two softmax groups (256 threads)
+// named barriers kPairBar + q4: the two warps (one per group) that hold the
+// same 32 query rows, for the per-tile exchange of row maxima (64 threads)
+constexpr int kPairBar = 2;
 
 // Barriers.  K/V ring: full (TMA) / empty (MMA commit).  Per S buffer: S full
 // (MMA commit), P full (the 8 softmax warps), O full (MMA commit after the
@@ -421,7 +424,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // two groups with the same (q4, lane) hold the same row.
     // A wait that gives up clears `ok` for its whole warp (the TMEM loads and
     // stores are warp-collective); the next exchange of row maxima, a
-    // bar.red.or over both groups, then takes all 256 threads out together.
+    // bar.red.or over the two warps that share its rows, takes both out of the
+    // tile loop, and the item's barrier over both groups (after the loop)
+    // takes all 256 threads out together (the other warps reach it when
+    // their tiles end or their own bounded waits give up).
     const int g = warp >> 2;
     const int q4 = warp & 3;
     const int r = 4 * lane + q4;
@@ -528,11 +534,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             mx = fmax3(mq[0], mq[1], fmaxf(mq[2], mq[3]));
           }
         }
-        // the row's max over both halves (the buffer alternates with the tile:
-        // the next barrier separates these reads from its next writes)
+        // the row's max over both halves, traded with the other group's warp
+        // that holds the same rows (the buffer alternates with the tile: the
+        // pair's next barrier separates these reads from its next writes)
         float* xm = s_xmax + (t & 1) * 256;
         xm[128 * g + r] = mx;
-        if (named_barrier_or(kXchgBar, 256, !ok)) { ok = false; break; }
+        if (named_barrier_or(kPairBar + q4, 64, !ok)) { ok = false; break; }
         mx = fmaxf(xm[r], xm[128 + r]);
         const bool grow = mx > m_used + grow_by;
         const float m_new = grow ? mx : m_used;
